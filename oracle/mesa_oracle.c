@@ -1,0 +1,230 @@
+/*
+ * mesa_oracle.c -- plain fp64 CPU oracle for the Mesa layer forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library and
+ * its Python binding) may include, link or call this file.  It exists so that
+ * tests, the smoke check and the benchmark's CPU-baseline leg can check the
+ * GPU kernels against an obviously correct, slow restatement of the method.
+ * It shares no code, header, table or helper with the CUDA path.
+ *
+ * Source: "MesaNet: Modelagem de Sequencias por Treinamento de Teste Localmente
+ * Otimo" technical summary (gist.science/pt/paper/2506.05233), section
+ * "A Camada Mesa":
+ *   - the Mesa objective (the one displayed equation): Phi_t minimises
+ *       1/2 sum_{t'<=t} zeta_{tt'} ||v_t' - Phi k_t'||^2 + 1/2 Tr(Phi Lambda Phi^T),
+ *     zeta = cumulative forget factors, Lambda symmetric positive definite;
+ *   - the readout Delta_t = Phi_t q_t, computed through the query solve
+ *     q*_t = (H_t + Lambda)^{-1} q_t by conjugate gradient;
+ *   - the "Paralelizacao" bullet: the layer keeps the state variables G_t, H_t;
+ *   - the "Computacao Dinamica" bullet: the CG iteration count depends on a
+ *     stopping criterion and varies per token.
+ * Setting the objective's gradient to zero gives Phi_t (H_t + Lambda) = G_t with
+ * H_t = sum zeta_{tt'} k_t' k_t'^T and G_t = sum zeta_{tt'} v_t' k_t'^T, so the
+ * output is o_t = G_t (H_t + Lambda)^{-1} q_t; with CG the inverse is replaced
+ * by the CG iterate.
+ *
+ * Readings taken where the page is silent (each is listed in the design notes):
+ *   - zeta_{tt'} = prod_{s=t'+1..t} gamma_s, so zeta_tt = 1 and gamma_t decays
+ *     the previous state: H_t = gamma_t H_{t-1} + k_t k_t^T (same for G_t).
+ *   - Lambda is diagonal, one vector per head, shared over batch and time.
+ *   - CG starts from x0 = 0 and is the textbook method: recursive residual,
+ *     beta = rho_{k+1}/rho_k, breakdown guards that set alpha/beta to 0.
+ *   - Stopping rule (dynamic mode, tol > 0): stop before an iteration when
+ *     ||r_k||_2 <= tol * ||q_t||_2; checked before every iteration including the
+ *     first, so q_t = 0 stops after 0 iterations.  Fixed mode (tol <= 0) runs
+ *     exactly cg_iters iterations.
+ *   - The output uses the CG iterate: o_t = G_t x_k.
+ *
+ * Everything is fp64.  The recurrence is sequential in t, so the only
+ * parallelism is over independent (batch, head) units (OpenMP when built with
+ * it; the thread count is an argument so callers can record it).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* w = (H + diag(lam)) p, H dense n x n row-major. */
+static void spd_apply(int n, const double *H, const double *lam, const double *p,
+                      double *w) {
+  for (int a = 0; a < n; a++) {
+    double s = lam[a] * p[a];
+    const double *row = H + (size_t)a * n;
+    for (int b = 0; b < n; b++) s += row[b] * p[b];
+    w[a] = s;
+  }
+}
+
+static double dot(int n, const double *a, const double *b) {
+  double s = 0.0;
+  for (int i = 0; i < n; i++) s += a[i] * b[i];
+  return s;
+}
+
+/*
+ * Textbook conjugate gradient on (H + diag(lam)) x = q, started from x = 0.
+ *   maxit: iteration cap (fixed mode: exact count)
+ *   tol  : > 0 selects the dynamic stopping rule ||r|| <= tol ||q||, else fixed
+ *   work : 3n doubles of scratch
+ * Returns the number of iterations executed.
+ */
+int oracle_cg(int n, const double *H, const double *lam, const double *q,
+              int maxit, double tol, double *x, double *work) {
+  double *r = work, *p = work + n, *w = work + 2 * n;
+  for (int i = 0; i < n; i++) {
+    x[i] = 0.0;
+    r[i] = q[i];
+    p[i] = q[i];
+  }
+  double rho = dot(n, r, r);
+  const double qnorm = sqrt(rho);
+  int it = 0;
+  for (; it < maxit; it++) {
+    if (tol > 0.0 && sqrt(rho) <= tol * qnorm) break;
+    spd_apply(n, H, lam, p, w);
+    const double sigma = dot(n, p, w);
+    const double alpha = (sigma > 0.0 && rho > 0.0) ? rho / sigma : 0.0;
+    for (int i = 0; i < n; i++) {
+      x[i] += alpha * p[i];
+      r[i] -= alpha * w[i];
+    }
+    const double rho_next = dot(n, r, r);
+    const double beta = (rho > 0.0) ? rho_next / rho : 0.0;
+    for (int i = 0; i < n; i++) p[i] = r[i] + beta * p[i];
+    rho = rho_next;
+  }
+  return it;
+}
+
+/* One token of the recurrence on one unit: decay and rank-1 update of H and G,
+ * the CG solve, and the readout o = G x.  H is dk x dk, G is dv x dk. */
+static int mesa_token(int dk, int dv, double *H, double *G, const double *q,
+                      const double *k, const double *v, double gamma,
+                      const double *lam, int maxit, double tol, double *o,
+                      double *x, double *work) {
+  for (int a = 0; a < dk; a++)
+    for (int b = 0; b < dk; b++)
+      H[(size_t)a * dk + b] = gamma * H[(size_t)a * dk + b] + k[a] * k[b];
+  for (int a = 0; a < dv; a++)
+    for (int b = 0; b < dk; b++)
+      G[(size_t)a * dk + b] = gamma * G[(size_t)a * dk + b] + v[a] * k[b];
+  const int it = oracle_cg(dk, H, lam, q, maxit, tol, x, work);
+  for (int a = 0; a < dv; a++) o[a] = dot(dk, G + (size_t)a * dk, x);
+  return it;
+}
+
+static int pick_threads(int nthreads, int units) {
+  int t = nthreads > 0 ? nthreads : 1;
+  if (t > units) t = units;
+  return t < 1 ? 1 : t;
+}
+
+/*
+ * Forward pass over a batch of independent sequences.
+ *   q, k [U, T, dk], v [U, T, dv], gamma [U, T], out [U, T, dv], iters [U, T],
+ *   U = B * heads, unit u = b * heads + h; lam [heads, dk] (unit u uses row
+ *   u % heads).
+ *   replay: NULL, or [U, T] per-token iteration counts; when given, token t
+ *   runs exactly replay[u, t] iterations (fixed mode) and tol is ignored.
+ *   H0/G0: NULL (zero initial state) or [U, dk, dk] / [U, dv, dk] initial states.
+ *   H_final/G_final: NULL, or [U, dk, dk] / [U, dv, dk] states after token T-1.
+ * Returns the number of threads used.
+ */
+int oracle_forward(int U, int heads, int T, int dk, int dv, const double *q,
+                   const double *k, const double *v, const double *gamma,
+                   const double *lam, int cg_iters, double cg_tol,
+                   const int32_t *replay, const double *H0, const double *G0,
+                   double *out, int32_t *iters, double *H_final, double *G_final,
+                   int nthreads) {
+  const int nt = pick_threads(nthreads, U);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+  for (int u = 0; u < U; u++) {
+    double *H = (double *)calloc((size_t)dk * dk, sizeof(double));
+    double *G = (double *)calloc((size_t)dv * dk, sizeof(double));
+    double *x = (double *)malloc(sizeof(double) * dk);
+    double *work = (double *)malloc(sizeof(double) * 3 * dk);
+    if (H0) memcpy(H, H0 + (size_t)u * dk * dk, sizeof(double) * dk * dk);
+    if (G0) memcpy(G, G0 + (size_t)u * dv * dk, sizeof(double) * dv * dk);
+    const double *lam_u = lam + (size_t)(u % heads) * dk;
+    for (int t = 0; t < T; t++) {
+      const size_t tok = (size_t)u * T + t;
+      int maxit = cg_iters;
+      double tol = cg_tol;
+      if (replay) {
+        maxit = replay[tok];
+        tol = 0.0;
+      }
+      iters[tok] = mesa_token(dk, dv, H, G, q + tok * dk, k + tok * dk,
+                              v + tok * dv, gamma[tok], lam_u, maxit, tol,
+                              out + tok * dv, x, work);
+    }
+    if (H_final) memcpy(H_final + (size_t)u * dk * dk, H, sizeof(double) * dk * dk);
+    if (G_final) memcpy(G_final + (size_t)u * dv * dk, G, sizeof(double) * dv * dk);
+    free(H);
+    free(G);
+    free(x);
+    free(work);
+  }
+  return nt;
+}
+
+/*
+ * One recurrent decode step for N sequences x heads units, in place:
+ *   H [U, dk, dk], G [U, dv, dk] (in/out), q, k [U, dk], v [U, dv], gamma [U],
+ *   lam [heads, dk], out [U, dv], iters [U]; U = N * heads.
+ * Returns the number of threads used.
+ */
+int oracle_decode_step(int U, int heads, int dk, int dv, double *H, double *G,
+                       const double *q, const double *k, const double *v,
+                       const double *gamma, const double *lam, int cg_iters,
+                       double cg_tol, double *out, int32_t *iters, int nthreads) {
+  const int nt = pick_threads(nthreads, U);
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nt)
+  for (int u = 0; u < U; u++) {
+    double *x = (double *)malloc(sizeof(double) * dk);
+    double *work = (double *)malloc(sizeof(double) * 3 * dk);
+    iters[u] = mesa_token(dk, dv, H + (size_t)u * dk * dk, G + (size_t)u * dv * dk,
+                          q + (size_t)u * dk, k + (size_t)u * dk, v + (size_t)u * dv,
+                          gamma[u], lam + (size_t)(u % heads) * dk, cg_iters,
+                          cg_tol, out + (size_t)u * dv, x, work);
+    free(x);
+    free(work);
+  }
+  return nt;
+}
+
+/*
+ * State trace for one unit (small cases only): H_all [T, dk, dk] and
+ * G_all [T, dv, dk] hold the states after each token, from the recurrence.
+ */
+void oracle_state_trace(int T, int dk, int dv, const double *k, const double *v,
+                        const double *gamma, double *H_all, double *G_all) {
+  double *H = (double *)calloc((size_t)dk * dk, sizeof(double));
+  double *G = (double *)calloc((size_t)dv * dk, sizeof(double));
+  for (int t = 0; t < T; t++) {
+    const double g = gamma[t];
+    const double *kt = k + (size_t)t * dk, *vt = v + (size_t)t * dv;
+    for (int a = 0; a < dk; a++)
+      for (int b = 0; b < dk; b++)
+        H[(size_t)a * dk + b] = g * H[(size_t)a * dk + b] + kt[a] * kt[b];
+    for (int a = 0; a < dv; a++)
+      for (int b = 0; b < dk; b++)
+        G[(size_t)a * dk + b] = g * G[(size_t)a * dk + b] + vt[a] * kt[b];
+    memcpy(H_all + (size_t)t * dk * dk, H, sizeof(double) * dk * dk);
+    memcpy(G_all + (size_t)t * dv * dk, G, sizeof(double) * dv * dk);
+  }
+  free(H);
+  free(G);
+}
+
+/* Exposed so callers can record how many host threads the oracle may use. */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
