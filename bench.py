@@ -1,0 +1,511 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 Mesa layer forward pass (one JSON line on stdout, rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl mesa|reference]
+
+A step is one pass of the hot path over one batch of seeded synthetic input: for the forward
+workloads one mesa_forward_chunked call (log-decays, chunk states, chunk-level scan, batched
+per-token CG with the fused readout); for the decode workload one mesa_decode_step over all
+sequences and heads.  Inputs are resident in HBM before the timed region; the L2 (129 MB) is
+flushed by a 256 MiB device write between timed steps unless the step's working set is
+larger than L2.  Kernel times come from CUDA events on the launching stream; `e2e` repeats
+the measurement through the same C-ABI call with pinned host buffers, copies included.
+Under torchrun every rank runs its own replica (independent sequences, no collective) and
+`value` is the aggregate over ranks with the max-over-ranks time.
+
+`--impl reference` times the fp64 CPU oracle (the deliberately slow restatement of the
+method used by the tests) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mesa_layer_gb300 import synth  # noqa: E402
+
+METRIC = "Mesa-layer fwd tokens/s on 1 GB300 (per CG iters) + % tensor/HBM roofline"
+DEFAULT_WORKLOAD = "fwd_fp32_d64"
+SM_COUNT = 152
+FP32_LANES_PER_SM = 128
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=synth.WORKLOAD_ORDER)
+    p.add_argument("--impl", default="mesa", choices=["mesa", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------------
+# algorithmic work (what the method must compute; causal half of the chunk blocks)
+
+
+def cg_flops(w, iters: np.ndarray) -> float:
+    """Per token-head and CG iteration: the matrix-vector product with H_t + Lambda in
+    chunk form, 2 d^2 (state term) + 2 d (C + 1) (causal intra-chunk term, both products);
+    the readout costs one more such product.  iters holds each token's own count."""
+    d, C = w.dk, w.chunk
+    per = 2.0 * d * d + 2.0 * d * (C + 1)
+    return float((iters.astype(np.float64) + 1.0).sum() * per)
+
+
+def state_flops(w) -> float:
+    """Chunk-local state sums: 2 d^2 multiply-adds per token for H and for G."""
+    return float(w.B * w.H * w.T) * 4.0 * w.dk * w.dk
+
+
+def decode_bytes(w) -> float:
+    """Per unit and step: H and G read and written in fp32, plus q, k, v, gamma, out, iters."""
+    esz = 2 if w.dtype == "bf16" else 4
+    U = w.B * w.H
+    return float(U) * (2 * 4 * (w.dk * w.dk + w.dv * w.dk) + esz * (2 * w.dk + 2 * w.dv) + 4 + 4)
+
+
+# ------------------------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str | None):
+        self.device_id = device_id
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.device_id:
+            cmd += ["-i", self.device_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def device_id_for_smi(torch, dev):
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+
+
+def oracle_sample(w, budget_s: float = 20.0):
+    """Time the fp64 oracle on a bounded sample of the workload: a subset of (batch, head)
+    units (forward) or of (sequence, head) units over a few steps (decode).  Returns
+    (tokens per second, threads used, description, seconds)."""
+    import oracle
+
+    threads = oracle.max_threads()
+    if w.decode_steps:
+        units = min(w.B * w.H, 64 * max(1, threads))
+        steps = 8
+        inp = synth.decode_inputs(w, 0)
+        q = inp["q"].reshape(1, -1, w.dk)[:, :units]
+        k = inp["k"].reshape(1, -1, w.dk)[:, :units]
+        v = inp["v"].reshape(1, -1, w.dv)[:, :units]
+        g = inp["gamma"].reshape(1, -1)[:, :units]
+        lam = synth.lambdas(w)[np.arange(units) % w.H]  # unit i keeps its head's lambda
+        Hs = np.zeros((1, units, w.dk, w.dk))
+        Gs = np.zeros((1, units, w.dv, w.dk))
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            oracle.decode_step(Hs, Gs, q, k, v, g, lam, w.cg_iters, w.cg_tol, nthreads=threads)
+        dt = time.perf_counter() - t0
+        return units * steps / dt / w.H, min(threads, units), f"{units} (sequence, head) units x {steps} steps", dt
+    # forward: whole units (sequences are sequential in t); the unit count grows until one
+    # pass takes a good part of the budget, then passes repeat until the budget is used
+    full = synth.forward_inputs(w) if w.B * w.H * w.T <= (1 << 22) else None
+    U = w.B * w.H
+    n_units = min(U, max(1, threads))
+    T = w.T
+    total_th, total_t, passes = 0, 0.0, 0
+    while True:
+        if full is not None:
+            sub = {k: full[k].reshape((U,) + full[k].shape[2:])[:n_units][None] for k in ("q", "k", "v", "gamma")}
+            lam = full["lam"][np.arange(n_units) % w.H]
+        else:
+            sub = synth.forward_inputs(synth.workload(w.name, B=1, H=n_units, T=T))
+            lam = sub["lam"]
+        t0 = time.perf_counter()
+        oracle.forward(sub["q"], sub["k"], sub["v"], sub["gamma"], lam, w.cg_iters, w.cg_tol, nthreads=threads)
+        dt = time.perf_counter() - t0
+        if n_units < U and dt < 0.25 * budget_s:
+            n_units = min(U, n_units * 2)
+            continue
+        total_th += n_units * T
+        total_t += dt
+        passes += 1
+        if total_t >= budget_s or dt > budget_s / 2:
+            break
+    desc = f"{passes} pass(es) over {n_units} (batch, head) units x {T} tokens"
+    # tokens/s of the workload = token-heads/s divided by the heads per token
+    return total_th / total_t / w.H, min(threads, n_units), desc, total_t
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = synth.workload(args.workload)
+    import oracle
+    oracle.load()
+    vals = []
+    desc = ""
+    cores = 1
+    for _ in range(max(1, args.steps)):
+        v, cores, desc, _ = oracle_sample(w, budget_s=min(15.0, 120.0 / max(1, args.steps)))
+        vals.append(v)
+    value = statistics.median(vals)
+    unit = "tokens/s"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.name, "B": w.B, "heads": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+           "chunk": w.chunk, "qkv_dtype": w.dtype,
+           "cg": (f"dynamic tol {w.cg_tol:g}, max {w.cg_iters}" if w.cg_tol > 0 else f"fixed {w.cg_iters}"),
+           "parallelism": "replicas"}
+    if w.decode_steps:
+        cfg.update({"sequences": w.B, "decode_steps": w.decode_steps, "prefix": w.prefix})
+        cfg.pop("T")
+    cfg.update(extra or {})
+    return cfg
+
+
+# ------------------------------------------------------------------------------------------
+# GPU arm
+
+
+def kind_names(lib):
+    names = []
+    for i in range(16):
+        n = lib.mesa_kernel_name(i)
+        if n is None:
+            break
+        names.append(n.decode())
+    return names
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    w = synth.workload(args.workload)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, desc, _ = oracle_sample(w, budget_s=10.0)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    import torch
+    import torch.distributed as dist
+
+    from mesa_layer_gb300 import binding, build
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    build.build()
+    lib = binding.load()
+    lib.mesa_kernel_name.restype = ctypes.c_char_p
+    lib.mesa_kernel_name.argtypes = [ctypes.c_int]
+    lib.mesa_timing_begin.argtypes = [ctypes.c_int]
+    lib.mesa_timing_end.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    names = kind_names(lib)
+    dev = torch.device("cuda", local)
+    peaks = measured_peaks()
+    if w.decode_steps:
+        res = bench_decode(args, w, rank, world, dev, lib, torch, binding)
+    else:
+        res = bench_forward(args, w, rank, world, dev, lib, torch, binding)
+    res["names"] = names
+    emit(args, w, res, peaks, cpu, rank, world, torch, dist)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def timed_loop(args, torch, lib, step_fn, flush_fn, world, dist, dev):
+    """W warm-up steps, then K steps each bracketed by CUDA events (flush outside)."""
+    for i in range(args.warmup):
+        step_fn(i)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    nk = 16
+    ms_kind = (ctypes.c_double * nk)()
+    n_kind = (ctypes.c_int * nk)()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(device_id_for_smi(torch, dev.index)).start()
+    time.sleep(0.3)
+    assert lib.mesa_timing_begin(8 * args.steps + 8) == 0
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        if flush_fn is not None:
+            flush_fn()
+        starts[i].record()
+        step_fn(i)
+        ends[i].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    assert lib.mesa_timing_end(ms_kind, n_kind, nk) == 0
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return {"step_ms": step_ms, "kind_ms": list(ms_kind), "kind_n": list(n_kind), "wall_s": wall,
+            "clocks": clocks}
+
+
+def bench_forward(args, w, rank, world, dev, lib, torch, binding):
+    import torch.distributed as dist
+    inp = synth.forward_inputs(w, seed=rank)
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    d_in = {k: torch.from_numpy(inp[k]).to(dev).to(td if k in ("q", "k", "v") else torch.float32).contiguous()
+            for k in ("q", "k", "v", "gamma", "lam")}
+    out = torch.empty((w.B, w.H, w.T, w.dv), dtype=td, device=dev)
+    iters = torch.empty((w.B, w.H, w.T), dtype=torch.int32, device=dev)
+    ws = torch.empty(binding.mesa_forward_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.chunk),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    in_bytes = sum(d_in[k].numel() * d_in[k].element_size() for k in ("q", "k", "v", "gamma"))
+    needs_flush = in_bytes < 2 * (129 << 20)
+
+    def step(i):
+        binding.mesa_forward_chunked(d_in["q"], d_in["k"], d_in["v"], d_in["gamma"], d_in["lam"],
+                                     w.cg_iters, w.cg_tol, w.chunk, out=out, iters_used=iters, workspace=ws)
+
+    res = timed_loop(args, torch, lib, step, (lambda: flush.random_(0, 255)) if needs_flush else None,
+                     world, dist, dev)
+    it = iters.cpu().numpy()
+    res.update({"iters": it, "tokens_per_step": w.B * w.T, "flush": needs_flush})
+    if not args.no_e2e:
+        res["e2e"] = e2e_forward(args, w, dev, torch, binding, inp, td, ws)
+    return res
+
+
+def e2e_forward(args, w, dev, torch, binding, inp, td, ws):
+    """Same call through the C ABI with pinned host buffers: H2D of q, k, v, gamma and D2H of
+    out and iters_used inside the timed region of every step."""
+    h = {k: torch.from_numpy(inp[k]).to(td if k in ("q", "k", "v") else torch.float32).pin_memory()
+         for k in ("q", "k", "v", "gamma")}
+    lam = torch.from_numpy(inp["lam"]).to(dev)
+    d = {k: torch.empty_like(h[k], device=dev) for k in h}
+    out = torch.empty((w.B, w.H, w.T, w.dv), dtype=td, device=dev)
+    iters = torch.empty((w.B, w.H, w.T), dtype=torch.int32, device=dev)
+    h_out = torch.empty(out.shape, dtype=td).pin_memory()
+    h_it = torch.empty(iters.shape, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = h_out.numel() * h_out.element_size() + h_it.numel() * 4
+
+    def step():
+        for k in h:
+            d[k].copy_(h[k], non_blocking=True)
+        binding.mesa_forward_chunked(d["q"], d["k"], d["v"], d["gamma"], lam, w.cg_iters, w.cg_tol, w.chunk,
+                                     out=out, iters_used=iters, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+        h_it.copy_(iters, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 50))
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(n):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h}
+
+
+def bench_decode(args, w, rank, world, dev, lib, torch, binding):
+    import torch.distributed as dist
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    N, H, d = w.B, w.H, w.dk
+    lam = torch.from_numpy(synth.lambdas(w)).to(dev)
+    Hs = torch.zeros(N, H, d, d, device=dev)
+    Gs = torch.zeros(N, H, w.dv, d, device=dev)
+    out = torch.empty(N, H, w.dv, dtype=td, device=dev)
+    iters = torch.empty(N, H, dtype=torch.int32, device=dev)
+
+    def dev_inputs(s):
+        inp = synth.decode_inputs(w, s, seed=rank)
+        return {k: torch.from_numpy(inp[k]).to(dev).to(td if k != "gamma" else torch.float32) for k in inp}
+
+    for s in range(-w.prefix, 0):  # state-only prefix (untimed): cg_iters = 0
+        x = dev_inputs(s)
+        binding.mesa_decode_step(Hs, Gs, x["q"], x["k"], x["v"], x["gamma"], lam, 0, 0.0, out=out, iters_used=iters)
+    n_steps = min(w.decode_steps, max(args.steps, 1))
+    steps = [dev_inputs(s) for s in range(n_steps)]
+    torch.cuda.synchronize()
+
+    def step(i):
+        x = steps[i % n_steps]
+        binding.mesa_decode_step(Hs, Gs, x["q"], x["k"], x["v"], x["gamma"], lam, w.cg_iters, w.cg_tol,
+                                 out=out, iters_used=iters)
+
+    res = timed_loop(args, torch, lib, step, None, world, dist, dev)
+    res.update({"iters": iters.cpu().numpy(), "tokens_per_step": N, "flush": False})
+    if not args.no_e2e:
+        h = {k: steps[0][k].cpu().pin_memory() for k in steps[0]}
+        dd = {k: torch.empty_like(steps[0][k]) for k in steps[0]}
+        h_out = torch.empty(out.shape, dtype=td).pin_memory()
+        h_it = torch.empty(iters.shape, dtype=torch.int32).pin_memory()
+
+        def estep():
+            for k in h:
+                dd[k].copy_(h[k], non_blocking=True)
+            binding.mesa_decode_step(Hs, Gs, dd["q"], dd["k"], dd["v"], dd["gamma"], lam, w.cg_iters, w.cg_tol,
+                                     out=out, iters_used=iters)
+            h_out.copy_(out, non_blocking=True)
+            h_it.copy_(iters, non_blocking=True)
+
+        for _ in range(3):
+            estep()
+        torch.cuda.synchronize()
+        n = max(3, min(args.steps, 50))
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(n):
+            estep()
+        e.record()
+        torch.cuda.synchronize()
+        res["e2e"] = {"ms_per_step": s.elapsed_time(e) / n,
+                      "h2d": sum(t.numel() * t.element_size() for t in h.values()),
+                      "d2h": h_out.numel() * h_out.element_size() + h_it.numel() * 4}
+    return res
+
+
+def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
+    step_ms = float(np.sum(res["step_ms"])) / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+    if rank != 0:
+        return
+    tokens = res["tokens_per_step"] * world
+    value = tokens / (step_ms / 1e3)
+    names = res["names"]
+    kind_ms, kind_n = res["kind_ms"], res["kind_n"]
+    top = int(np.argmax(kind_ms))
+    top_name = names[top] if top < len(names) else f"kind{top}"
+    launches = max(1, kind_n[top])
+    avg_ms = kind_ms[top] / launches
+    launches_per_step = sum(kind_n) / args.steps
+    it = res["iters"]
+    if w.decode_steps:
+        bytes_ = decode_bytes(w)
+        achieved = bytes_ / (avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": top_name,
+                "peak_source": peaks["source"]}
+    else:
+        if "cg" in top_name:
+            flops = cg_flops(w, it)
+        else:
+            flops = state_flops(w)
+        achieved = flops / (avg_ms / 1e3) / 1e12
+        peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "kernel": top_name,
+                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock"}
+    kernels = {names[i] if i < len(names) else f"kind{i}": {"ms_per_step": kind_ms[i] / args.steps,
+                                                             "launches": kind_n[i]}
+               for i in range(len(kind_ms)) if kind_n[i] > 0}
+    extra = {"mean_iters": float(it.mean()), "max_iters": int(it.max()),
+             "l2": ("flushed between timed steps (256 MiB device write)" if res["flush"]
+                    else "working set larger than L2, not flushed"),
+             "kernels": kernels, "wall_s_timed_loop": res["wall_s"]}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, see mesa_layer_gb300/synth.py)",
+            "config": workload_config(w, extra), "roofline": roof, "cpu_baseline": cpu,
+            "gpu_launches": int(sum(kind_n)), "launches_per_step": launches_per_step,
+            "clocks": res["clocks"]}
+    if "e2e" in res:
+        e = res["e2e"]
+        line["e2e"] = {"value": tokens / (e["ms_per_step"] / 1e3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                       "ms_per_step": e["ms_per_step"]}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

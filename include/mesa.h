@@ -1,0 +1,133 @@
+/*
+ * mesa.h -- C ABI of the GB300 (sm_103a) Mesa layer library (libmesa_gb300.so).
+ *
+ * What the layer computes (MesaNet technical summary, gist.science/pt/paper/2506.05233,
+ * section "A Camada Mesa"): for every token t of every (batch, head) sequence the map
+ * Phi_t minimises the forget-weighted, Lambda-regularised squared error of the Mesa
+ * objective; the output is Delta_t = Phi_t q_t = G_t q*_t with q*_t = (H_t + Lambda)^-1 q_t
+ * found by conjugate gradient.  The states ("Paralelizacao" bullet) are
+ *     H_t = gamma_t H_{t-1} + k_t k_t^T      (d_k x d_k, symmetric)
+ *     G_t = gamma_t G_{t-1} + v_t k_t^T      (d_v x d_k)
+ * i.e. zeta_{tt'} = prod_{s=t'+1..t} gamma_s, and the CG iteration count is fixed or set
+ * per token by a stopping criterion ("Computacao Dinamica" bullet).
+ *
+ * CG rule (the same in every entry point): x0 = 0, r0 = p0 = q_t, rho = r.r;
+ * before each iteration, if cg_tol > 0 and ||r|| <= cg_tol * ||q_t||, stop;
+ * w = (H_t + Lambda) p, sigma = p.w, alpha = rho/sigma (0 if sigma <= 0 or rho <= 0),
+ * x += alpha p, r -= alpha w, beta = rho_new/rho (0 if rho <= 0), p = r + beta p.
+ * cg_tol <= 0 selects fixed mode: exactly cg_iters iterations for every token.
+ * The output is o_t = G_t x (the CG iterate); iters_used[t] counts the iterations run.
+ *
+ * Conventions shared by all entry points:
+ *   - All arrays are device pointers, dense row-major (C order), owned by the caller.
+ *     The library never allocates, frees or synchronises; work is enqueued on `stream`.
+ *   - dtype selects the element type of q, k, v and out: MESA_F32 (float) or MESA_BF16
+ *     (__nv_bfloat16).  gamma, lambda_diag, states and arithmetic are fp32.
+ *   - Lambda is diagonal: lambda_diag [H, dk], one vector per head shared over batch
+ *     and time.  Forget gates gamma lie in [0, 1]; a gate below 1.8e-35 (e^-80) is
+ *     treated as e^-80 (its log is clamped).
+ *   - Supported sizes: dk == dv in {16, 32, 64, 128}; T >= 0 (any value: a ragged last
+ *     chunk is handled); chunk in {16, 32, 64, 128}.  0 <= cg_iters <= 4096.
+ *   - Return value: MESA_OK when the arguments were valid and the kernels were
+ *     enqueued; otherwise an error code and nothing was enqueued (MESA_ERR_CUDA: a
+ *     launch failed; cudaGetLastError() holds the cause).  Calls that run
+ *     concurrently on different streams must not share a workspace or a state.
+ */
+#ifndef MESA_GB300_H
+#define MESA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum mesa_status {
+  MESA_OK = 0,
+  MESA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad alignment       */
+  MESA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. dk not in set)    */
+  MESA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required        */
+  MESA_ERR_CUDA = 4          /* a kernel launch failed                            */
+};
+
+enum mesa_dtype { MESA_F32 = 0, MESA_BF16 = 1 };
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int mesa_version(void);
+
+/* Static string naming a status code. */
+const char *mesa_status_string(int status);
+
+/*
+ * Bytes of device workspace mesa_forward_chunked needs for these sizes (256-byte
+ * aligned start required).  It holds the per-token log-decays [B, H, T] and the
+ * chunk-boundary states S^H_c [B, H, ceil(T/chunk), dk, dk] and
+ * S^G_c [B, H, ceil(T/chunk), dv, dk] in fp32.  Returns 0 for unsupported sizes.
+ */
+size_t mesa_forward_workspace_size(int B, int H, int T, int dk, int dv, int chunk);
+
+/*
+ * Chunked (prefill / training) forward pass of the Mesa layer ("Paralelizacao" bullet:
+ * the sequence is split into chunks; chunk-boundary states carry the past and every CG
+ * iteration for all tokens of a chunk is one gated-linear-attention style pass).
+ *   q, k      [B, H, T, dk]  dtype
+ *   v         [B, H, T, dv]  dtype
+ *   gamma     [B, H, T]      fp32 forget gates
+ *   lambda_diag [H, dk]      fp32, > 0
+ *   cg_iters  fixed iteration count (cg_tol <= 0) or the cap (cg_tol > 0)
+ *   cg_tol    relative residual tolerance of the dynamic stopping rule, or <= 0
+ *   chunk     tokens per chunk (state interval)
+ *   out       [B, H, T, dv]  dtype (written)
+ *   iters_used [B, H, T] int32 (written) or NULL
+ *   H0, G0    NULL (zero initial state) or [B, H, dk, dk] / [B, H, dv, dk] fp32 states
+ *             before token 0 (both or neither; H0 symmetric)
+ *   H_final, G_final  NULL or [B, H, dk, dk] / [B, H, dv, dk] fp32: states after token T-1
+ *             (both or neither)
+ *   workspace device scratch of at least mesa_forward_workspace_size() bytes
+ */
+int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const void *q,
+                         const void *k, const void *v, const float *gamma,
+                         const float *lambda_diag, int cg_iters, float cg_tol, int chunk,
+                         void *out, int32_t *iters_used, const float *H0, const float *G0,
+                         float *H_final, float *G_final, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * One recurrent decode step for N sequences x H heads ("Paralelizacao" bullet: O(1)
+ * inference), in place on the caller's fp32 states:
+ *   H_state [N, H, dk, dk] (symmetric; 16-byte aligned)  <- gamma H_state + k k^T
+ *   G_state [N, H, dv, dk] (16-byte aligned)             <- gamma G_state + v k^T
+ * then CG on (H_state + Lambda) x = q and out = G_state x.
+ *   q, k [N, H, dk], v [N, H, dv] dtype; gamma [N, H] fp32; lambda_diag [H, dk] fp32;
+ *   out [N, H, dv] dtype; iters_used [N, H] int32 or NULL.
+ */
+int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state,
+                     float *G_state, const void *q, const void *k, const void *v,
+                     const float *gamma, const float *lambda_diag, int cg_iters,
+                     float cg_tol, void *out, int32_t *iters_used, cudaStream_t stream);
+
+/*
+ * Per-kernel timing for benchmarks (no counterpart on the MesaNet pages; a measurement
+ * aid).  Between mesa_timing_begin and mesa_timing_end every kernel launched by the
+ * entry points above is bracketed by two CUDA events recorded on the caller's stream.
+ *   mesa_timing_begin(max_launches): creates 2 * max_launches events (host API objects,
+ *     no device memory); launches beyond max_launches are not timed.
+ *   mesa_timing_end(ms, launches, nkinds): waits for the recorded events, writes the
+ *     summed milliseconds and the launch count per kernel kind (index = kind, see
+ *     mesa_kernel_name), destroys the events and stops timing.
+ * Not thread-safe: one timing session per process.
+ */
+int mesa_timing_begin(int max_launches);
+int mesa_timing_end(double *ms_per_kind, int *launches_per_kind, int nkinds);
+
+/* Name of a kernel kind used by the timing calls, or NULL past the last kind. */
+const char *mesa_kernel_name(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MESA_GB300_H */

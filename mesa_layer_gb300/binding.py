@@ -1,0 +1,151 @@
+"""Thin ctypes binding of libmesa_gb300.so (include/mesa.h).
+
+Argument marshalling only: torch tensors supply device pointers and the current CUDA
+stream; every step of the computation runs in the library's kernels.  Output tensors and
+the workspace are allocated with torch on the caller's side when not given.  There is no
+CPU fallback: if the library is missing or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MESA_F32, MESA_BF16 = 0, 1
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size or option",
+           3: "workspace missing or too small", 4: "CUDA launch failed"}
+
+_lib = None
+_vp, _fp, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+_i, _f, _sz = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+class MesaError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load the shared library (building it first if it is missing and nvcc exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise MesaError(f"{path} is not built: call mesa_layer_gb300.build.build()")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    lib.mesa_version.restype = _i
+    lib.mesa_status_string.restype = ctypes.c_char_p
+    lib.mesa_status_string.argtypes = [_i]
+    lib.mesa_forward_workspace_size.restype = _sz
+    lib.mesa_forward_workspace_size.argtypes = [_i] * 6
+    lib.mesa_forward_chunked.restype = _i
+    lib.mesa_forward_chunked.argtypes = [_i] * 6 + [_vp] * 5 + [_i, _f, _i, _vp, _ip] + \
+        [_fp] * 4 + [_vp, _sz, _vp]
+    lib.mesa_decode_step.restype = _i
+    lib.mesa_decode_step.argtypes = [_i] * 5 + [_fp, _fp, _vp, _vp, _vp, _fp, _fp, _i, _f, _vp, _ip, _vp]
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise MesaError(f"{what}: {_STATUS.get(status, status)}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MESA_F32
+    if t.dtype == torch.bfloat16:
+        return MESA_BF16
+    raise MesaError(f"unsupported dtype {t.dtype}: use float32 or bfloat16")
+
+
+def _require(t, name, dtype=None, device=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise MesaError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise MesaError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise MesaError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def mesa_forward_workspace_size(B, H, T, dk, dv, chunk) -> int:
+    return int(load().mesa_forward_workspace_size(B, H, T, dk, dv, chunk))
+
+
+def mesa_forward_chunked(q, k, v, gamma, lambda_diag, cg_iters, cg_tol, chunk, out=None,
+                         iters_used=None, H0=None, G0=None, H_final=None, G_final=None,
+                         workspace=None, stream=None):
+    """Chunked Mesa layer forward.  q, k [B, H, T, dk], v [B, H, T, dv] (fp32 or bf16),
+    gamma [B, H, T] fp32, lambda_diag [H, dk] fp32.  Returns (out, iters_used)."""
+    lib = load()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, q.dtype)
+    _require(gamma, "gamma", torch.float32)
+    _require(lambda_diag, "lambda_diag", torch.float32)
+    for name, t in (("H0", H0), ("G0", G0), ("H_final", H_final), ("G_final", G_final)):
+        _require(t, name, torch.float32)
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    if iters_used is None:
+        iters_used = torch.empty((B, H, T), dtype=torch.int32, device=q.device)
+    _require(out, "out", q.dtype)
+    _require(iters_used, "iters_used", torch.int32)
+    need = mesa_forward_workspace_size(B, H, T, dk, dv, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _require(workspace, "workspace")
+    st = lib.mesa_forward_chunked(B, H, T, dk, dv, code, _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
+                                  _ptr(lambda_diag), int(cg_iters), float(cg_tol), int(chunk),
+                                  _ptr(out), _ptr(iters_used), _ptr(H0), _ptr(G0), _ptr(H_final),
+                                  _ptr(G_final), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "mesa_forward_chunked")
+    return out, iters_used
+
+
+def mesa_decode_step(H_state, G_state, q, k, v, gamma, lambda_diag, cg_iters, cg_tol, out=None,
+                     iters_used=None, stream=None):
+    """One decode step in place on H_state [N, H, dk, dk] and G_state [N, H, dv, dk] (fp32).
+    q, k [N, H, dk], v [N, H, dv] (fp32 or bf16), gamma [N, H].  Returns (out, iters_used)."""
+    lib = load()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, q.dtype)
+    _require(H_state, "H_state", torch.float32)
+    _require(G_state, "G_state", torch.float32)
+    _require(gamma, "gamma", torch.float32)
+    _require(lambda_diag, "lambda_diag", torch.float32)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    if iters_used is None:
+        iters_used = torch.empty((N, H), dtype=torch.int32, device=q.device)
+    st = lib.mesa_decode_step(N, H, dk, dv, code, _ptr(H_state), _ptr(G_state), _ptr(q), _ptr(k),
+                              _ptr(v), _ptr(gamma), _ptr(lambda_diag), int(cg_iters), float(cg_tol),
+                              _ptr(out), _ptr(iters_used), _stream(stream))
+    _check(st, "mesa_decode_step")
+    return out, iters_used

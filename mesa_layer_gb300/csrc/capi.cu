@@ -1,0 +1,190 @@
+// capi.cu -- the extern "C" entry points declared in include/mesa.h: argument
+// validation, workspace carve-up and kernel dispatch.  No allocation, no synchronisation.
+#include <math.h>
+#include <stdlib.h>
+
+#include "../../include/mesa.h"
+#include "launch.h"
+
+namespace {
+
+constexpr int kMaxIters = 4096;
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool chunk_ok(int c) { return c == 16 || c == 32 || c == 64 || c == 128; }
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t workspace_parts(int B, int H, int T, int dk, int dv, int chunk, size_t *off) {
+  const size_t U = (size_t)B * H;
+  const size_t NC = (size_t)(T + chunk - 1) / chunk;
+  off[0] = 0;
+  off[1] = off[0] + align256(U * T * sizeof(float));
+  off[2] = off[1] + align256(U * NC * dk * dk * sizeof(float));
+  return off[2] + align256(U * NC * dv * dk * sizeof(float));
+}
+
+// ---- optional per-kernel timing (benchmarks only) --------------------------------------
+struct TimingState {
+  bool on = false;
+  int cap = 0, used = 0;
+  cudaEvent_t *ev = nullptr;  // 2 * cap events: begin/end pairs
+  int *kind = nullptr;
+  int pending = -1;           // index of the pair whose begin was recorded
+};
+TimingState g_timing;
+
+}  // namespace
+
+namespace mesa {
+
+void timing_mark_begin(int kind, cudaStream_t st) {
+  TimingState &t = g_timing;
+  if (!t.on || t.used >= t.cap) return;
+  t.pending = t.used;
+  t.kind[t.used] = kind;
+  cudaEventRecord(t.ev[2 * t.used], st);
+}
+
+void timing_mark_end(int kind, cudaStream_t st) {
+  TimingState &t = g_timing;
+  if (!t.on || t.pending < 0 || t.kind[t.pending] != kind) return;
+  cudaEventRecord(t.ev[2 * t.pending + 1], st);
+  t.used++;
+  t.pending = -1;
+}
+
+}  // namespace mesa
+
+extern "C" {
+
+int mesa_timing_begin(int max_launches) {
+  TimingState &t = g_timing;
+  if (t.on || max_launches <= 0 || max_launches > (1 << 20)) return MESA_ERR_INVALID_ARG;
+  t.ev = (cudaEvent_t *)calloc(2 * (size_t)max_launches, sizeof(cudaEvent_t));
+  t.kind = (int *)calloc((size_t)max_launches, sizeof(int));
+  if (!t.ev || !t.kind) return MESA_ERR_INVALID_ARG;
+  for (int i = 0; i < 2 * max_launches; i++)
+    if (cudaEventCreate(&t.ev[i]) != cudaSuccess) return MESA_ERR_CUDA;
+  t.cap = max_launches;
+  t.used = 0;
+  t.pending = -1;
+  t.on = true;
+  return MESA_OK;
+}
+
+int mesa_timing_end(double *ms_per_kind, int *launches_per_kind, int nkinds) {
+  TimingState &t = g_timing;
+  if (!t.on) return MESA_ERR_INVALID_ARG;
+  int status = MESA_OK;
+  for (int k = 0; k < nkinds; k++) {
+    if (ms_per_kind) ms_per_kind[k] = 0.0;
+    if (launches_per_kind) launches_per_kind[k] = 0;
+  }
+  for (int i = 0; i < t.used; i++) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(t.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, t.ev[2 * i], t.ev[2 * i + 1]) != cudaSuccess)
+      status = MESA_ERR_CUDA;
+    const int k = t.kind[i];
+    if (k >= 0 && k < nkinds) {
+      if (ms_per_kind) ms_per_kind[k] += ms;
+      if (launches_per_kind) launches_per_kind[k]++;
+    }
+  }
+  for (int i = 0; i < 2 * t.cap; i++) cudaEventDestroy(t.ev[i]);
+  free(t.ev);
+  free(t.kind);
+  t = TimingState();
+  return status;
+}
+
+const char *mesa_kernel_name(int kind) {
+  switch (kind) {
+    case mesa::K_ELL: return "mesa_ell_kernel";
+    case mesa::K_DELTA: return "mesa_delta_kernel";
+    case mesa::K_SCAN: return "mesa_scan_kernel";
+    case mesa::K_CG_SIMT: return "mesa_cg_simt_kernel";
+    case mesa::K_DECODE: return "mesa_decode_kernel";
+  }
+  return nullptr;
+}
+
+int mesa_version(void) { return 100; }
+
+const char *mesa_status_string(int s) {
+  switch (s) {
+    case MESA_OK: return "ok";
+    case MESA_ERR_INVALID_ARG: return "invalid argument";
+    case MESA_ERR_UNSUPPORTED: return "unsupported size or option";
+    case MESA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MESA_ERR_CUDA: return "CUDA launch failed";
+  }
+  return "unknown status";
+}
+
+size_t mesa_forward_workspace_size(int B, int H, int T, int dk, int dv, int chunk) {
+  if (B < 0 || H < 0 || T < 0 || !dim_ok(dk) || dv != dk || !chunk_ok(chunk)) return 0;
+  size_t off[3];
+  return workspace_parts(B, H, T, dk, dv, chunk, off);
+}
+
+int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const void *q,
+                         const void *k, const void *v, const float *gamma,
+                         const float *lambda_diag, int cg_iters, float cg_tol, int chunk,
+                         void *out, int32_t *iters_used, const float *H0, const float *G0,
+                         float *H_final, float *G_final, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  if (B < 0 || H < 0 || T < 0 || cg_iters < 0 || cg_iters > kMaxIters || isnan(cg_tol))
+    return MESA_ERR_INVALID_ARG;
+  if (dtype != MESA_F32 && dtype != MESA_BF16) return MESA_ERR_INVALID_ARG;
+  if ((H0 == nullptr) != (G0 == nullptr) || (H_final == nullptr) != (G_final == nullptr))
+    return MESA_ERR_INVALID_ARG;
+  if (!dim_ok(dk) || dv != dk || !chunk_ok(chunk)) return MESA_ERR_UNSUPPORTED;
+  const size_t U = (size_t)B * H;
+  if (U == 0) return MESA_OK;
+  if (!lambda_diag) return MESA_ERR_INVALID_ARG;
+  if (T == 0) {  // nothing to compute; the final state is the initial state
+    if (H_final) {
+      const size_t hb = U * dk * dk * sizeof(float), gb = U * dv * dk * sizeof(float);
+      cudaError_t e1 = H0 ? cudaMemcpyAsync(H_final, H0, hb, cudaMemcpyDeviceToDevice, stream)
+                          : cudaMemsetAsync(H_final, 0, hb, stream);
+      cudaError_t e2 = G0 ? cudaMemcpyAsync(G_final, G0, gb, cudaMemcpyDeviceToDevice, stream)
+                          : cudaMemsetAsync(G_final, 0, gb, stream);
+      if (e1 != cudaSuccess || e2 != cudaSuccess) return MESA_ERR_CUDA;
+    }
+    return MESA_OK;
+  }
+  if (!q || !k || !v || !gamma || !out) return MESA_ERR_INVALID_ARG;
+  size_t off[3];
+  const size_t need = workspace_parts(B, H, T, dk, dv, chunk, off);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return MESA_ERR_WORKSPACE;
+
+  mesa::FwdArgs a{B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol, chunk,
+                  out, iters_used, H0, G0, H_final, G_final};
+  char *w = (char *)workspace;
+  mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2])};
+  if (mesa::launch_chunk_states(a, ws, stream) != 0) return MESA_ERR_CUDA;
+  if (mesa::launch_chunk_cg_simt(a, ws, stream) != 0) return MESA_ERR_CUDA;
+  return MESA_OK;
+}
+
+int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state, float *G_state,
+                     const void *q, const void *k, const void *v, const float *gamma,
+                     const float *lambda_diag, int cg_iters, float cg_tol, void *out,
+                     int32_t *iters_used, cudaStream_t stream) {
+  if (N < 0 || H < 0 || cg_iters < 0 || cg_iters > kMaxIters || isnan(cg_tol))
+    return MESA_ERR_INVALID_ARG;
+  if (dtype != MESA_F32 && dtype != MESA_BF16) return MESA_ERR_INVALID_ARG;
+  if (!dim_ok(dk) || dv != dk) return MESA_ERR_UNSUPPORTED;
+  if ((size_t)N * H == 0) return MESA_OK;
+  if (!H_state || !G_state || !q || !k || !v || !gamma || !lambda_diag || !out)
+    return MESA_ERR_INVALID_ARG;
+  if (!aligned(H_state, 16) || !aligned(G_state, 16)) return MESA_ERR_INVALID_ARG;
+  mesa::DecArgs a{N, H, dk, dv, dtype, H_state, G_state, q, k, v, gamma, lambda_diag,
+                  cg_iters, cg_tol, out, iters_used};
+  return mesa::launch_decode(a, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+// chunk_state.cu -- per-chunk log-decays and the chunk-boundary states of the Mesa layer.
+//
+// MesaNet technical summary (gist.science/pt/paper/2506.05233), "A Camada Mesa",
+// "Paralelizacao": the layer keeps the states H_t = sum zeta k k^T and G_t = sum zeta v k^T
+// and works chunk by chunk.  With l_i = sum_{s<=i} log gamma_s inside chunk c (i = 0..C-1)
+// the state after the chunk is
+//     S_c = e^{l_{C-1}} S_{c-1} + sum_j e^{l_{C-1} - l_j} x_j k_j^T       (x = k for H, v for G)
+// (unrolling H_t = gamma_t H_{t-1} + k_t k_t^T over the chunk).  Three kernels:
+//   mesa_ell_kernel    l_i per token (block scan of log gates inside each chunk);
+//   mesa_delta_kernel  the chunk-local sums  sum_j w_j x_j k_j^T  for every chunk, in parallel;
+//   mesa_scan_kernel   the chunk-level prefix scan S_c = a_c S_{c-1} + Delta_c, in place,
+//                      parallel over state entries, sequential over chunks.
+#include "common.cuh"
+#include "launch.h"
+
+namespace mesa {
+
+// grid (NC, U), block 128 (>= chunk).  ell[u, t] for every token of chunk c.
+__global__ void __launch_bounds__(128) mesa_ell_kernel(const float *__restrict__ gamma,
+                                                       float *__restrict__ ell, int T, int C) {
+  const int c = blockIdx.x, u = blockIdx.y, i = threadIdx.x;
+  const int t = c * C + i;
+  const bool valid = (i < C) && (t < T);
+  float v = valid ? log_gate(gamma[(size_t)u * T + t]) : 0.0f;
+  // inclusive scan over the block
+  const int lane = i & 31, warp = i >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  __shared__ float wsum[4];
+  if (lane == 31) wsum[warp] = v;
+  __syncthreads();
+  for (int w = 0; w < warp; w++) v += wsum[w];
+  if (valid) ell[(size_t)u * T + t] = v;
+}
+
+// grid (NC, U, 2): z = 0 builds Delta^H = sum_j w_j k_j k_j^T, z = 1 builds
+// Delta^G = sum_j w_j v_j k_j^T, w_j = e^{l_last - l_j}.  Block 256; each thread owns a
+// (D/16) x (D/16) register tile of the D x D result.
+template <int D, typename TIO>
+__global__ void __launch_bounds__(256) mesa_delta_kernel(const TIO *__restrict__ k,
+                                                         const TIO *__restrict__ v,
+                                                         const float *__restrict__ ell,
+                                                         FwdWorkspace ws, int T, int C) {
+  constexpr int TM = D / 16;
+  extern __shared__ float smem[];
+  float *Xs = smem;              // [C, D] rows x_j (k or v)
+  float *Ks = smem + 128 * D;    // [C, D] rows k_j
+  float *wv = smem + 256 * D;    // [C]
+  const int c = blockIdx.x, u = blockIdx.y, isG = blockIdx.z;
+  const int NC = gridDim.x;
+  const int t0 = c * C;
+  const int Cv = min(C, T - t0);
+  const size_t base = ((size_t)u * T + t0) * D;
+  const TIO *X = isG ? v : k;
+  for (int e = threadIdx.x; e < Cv * D; e += blockDim.x) {
+    Ks[e] = ld(k, base + e);
+    Xs[e] = ld(X, base + e);
+  }
+  const float lend = ell[(size_t)u * T + t0 + Cv - 1];
+  for (int j = threadIdx.x; j < Cv; j += blockDim.x)
+    wv[j] = expf(lend - ell[(size_t)u * T + t0 + j]);
+  __syncthreads();
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[TM][TM];
+#pragma unroll
+  for (int m = 0; m < TM; m++)
+#pragma unroll
+    for (int n = 0; n < TM; n++) acc[m][n] = 0.0f;
+  for (int j = 0; j < Cv; j++) {
+    const float wj = wv[j];
+    float xa[TM], kb[TM];
+#pragma unroll
+    for (int m = 0; m < TM; m++) xa[m] = Xs[j * D + ty + 16 * m] * wj;
+#pragma unroll
+    for (int n = 0; n < TM; n++) kb[n] = Ks[j * D + tx + 16 * n];
+#pragma unroll
+    for (int m = 0; m < TM; m++)
+#pragma unroll
+      for (int n = 0; n < TM; n++) acc[m][n] = fmaf(xa[m], kb[n], acc[m][n]);
+  }
+  float *S = (isG ? ws.SG : ws.SH) + ((size_t)u * NC + c) * D * D;
+#pragma unroll
+  for (int m = 0; m < TM; m++)
+#pragma unroll
+    for (int n = 0; n < TM; n++) S[(ty + 16 * m) * D + tx + 16 * n] = acc[m][n];
+}
+
+// grid (ceil(2 D^2 / 256), U), block 256.  Entry e < D^2 belongs to S^H, else to S^G.
+// S_c = a_c S_{c-1} + Delta_c in place, a_c = e^{l_last(c)}; S_{-1} = H0/G0 or 0.
+template <int D>
+__global__ void __launch_bounds__(256) mesa_scan_kernel(const float *__restrict__ ell,
+                                                        FwdWorkspace ws, const float *H0,
+                                                        const float *G0, float *Hf, float *Gf,
+                                                        int T, int C, int NC) {
+  const int u = blockIdx.y;
+  int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= 2 * D * D) return;
+  const bool isG = e >= D * D;
+  if (isG) e -= D * D;
+  float *S = (isG ? ws.SG : ws.SH) + (size_t)u * NC * D * D + e;
+  const float *S0 = isG ? G0 : H0;
+  float s = S0 ? S0[(size_t)u * D * D + e] : 0.0f;
+  for (int c = 0; c < NC; c++) {
+    const int last = min(T, (c + 1) * C) - 1;
+    const float a = expf(ell[(size_t)u * T + last]);
+    s = fmaf(a, s, S[(size_t)c * D * D]);
+    S[(size_t)c * D * D] = s;
+  }
+  float *F = isG ? Gf : Hf;
+  if (F) F[(size_t)u * D * D + e] = s;
+}
+
+template <int D, typename TIO>
+static int launch_states_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+  const int U = a.B * a.H;
+  const int NC = (a.T + a.chunk - 1) / a.chunk;
+  timing_mark_begin(K_ELL, st);
+  mesa_ell_kernel<<<dim3(NC, U), 128, 0, st>>>(a.gamma, ws.ell, a.T, a.chunk);
+  timing_mark_end(K_ELL, st);
+  const size_t smem = (size_t)(256 * D + 128) * sizeof(float);
+  auto kd = mesa_delta_kernel<D, TIO>;
+  if (cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return -1;
+  timing_mark_begin(K_DELTA, st);
+  kd<<<dim3(NC, U, 2), 256, smem, st>>>((const TIO *)a.k, (const TIO *)a.v, ws.ell, ws, a.T,
+                                        a.chunk);
+  timing_mark_end(K_DELTA, st);
+  timing_mark_begin(K_SCAN, st);
+  mesa_scan_kernel<D><<<dim3((2 * D * D + 255) / 256, U), 256, 0, st>>>(
+      ws.ell, ws, a.H0, a.G0, a.H_final, a.G_final, a.T, a.chunk, NC);
+  timing_mark_end(K_SCAN, st);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_chunk_states(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+  const bool bf = a.dtype == 1;
+  switch (a.dk) {
+    case 16: return bf ? launch_states_t<16, __nv_bfloat16>(a, ws, st) : launch_states_t<16, float>(a, ws, st);
+    case 32: return bf ? launch_states_t<32, __nv_bfloat16>(a, ws, st) : launch_states_t<32, float>(a, ws, st);
+    case 64: return bf ? launch_states_t<64, __nv_bfloat16>(a, ws, st) : launch_states_t<64, float>(a, ws, st);
+    case 128: return bf ? launch_states_t<128, __nv_bfloat16>(a, ws, st) : launch_states_t<128, float>(a, ws, st);
+  }
+  return -1;
+}
+
+}  // namespace mesa

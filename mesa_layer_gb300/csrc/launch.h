@@ -1,0 +1,48 @@
+// launch.h -- host-side argument bundles and kernel launchers (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace mesa {
+
+struct FwdArgs {
+  int B, H, T, dk, dv, dtype;
+  const void *q, *k, *v;
+  const float *gamma, *lambda;
+  int cg_iters;
+  float cg_tol;
+  int chunk;
+  void *out;
+  int32_t *iters;
+  const float *H0, *G0;
+  float *H_final, *G_final;
+};
+
+struct DecArgs {
+  int N, H, dk, dv, dtype;
+  float *Hs, *Gs;
+  const void *q, *k, *v;
+  const float *gamma, *lambda;
+  int cg_iters;
+  float cg_tol;
+  void *out;
+  int32_t *iters;
+};
+
+// Kernel kinds, for the optional per-kernel timing of benchmarks (mesa_timing_*).
+enum KernelKind { K_ELL = 0, K_DELTA = 1, K_SCAN = 2, K_CG_SIMT = 3, K_DECODE = 4, K_NUM_KINDS = 8 };
+
+// Record a timing event before / after a launch of `kind` on `st` (no-op unless enabled).
+void timing_mark_begin(int kind, cudaStream_t st);
+void timing_mark_end(int kind, cudaStream_t st);
+
+// Each returns 0 when every launch was enqueued, -1 otherwise.
+int launch_chunk_states(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
+int launch_chunk_cg_simt(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
+int launch_decode(const DecArgs &a, cudaStream_t st);
+
+}  // namespace mesa

@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads, exports every
+function include/mesa.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mesa_layer_gb300 import binding, build
+
+HEADER_DIR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if fn.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(mesa_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("mesa_forward_chunked", "mesa_decode_step", "mesa_forward_workspace_size"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.mesa_version() >= 100
+    assert lib.mesa_status_string(0) == b"ok"
+    assert lib.mesa_status_string(3).startswith(b"workspace")
+
+
+def test_workspace_size(lib):
+    ws = lib.mesa_forward_workspace_size
+    assert ws(1, 1, 256, 16, 16, 64) >= 4 * (256 + 2 * 4 * 16 * 16)
+    assert ws(1, 1, 100, 16, 16, 32) <= ws(1, 1, 128, 16, 16, 32)   # ragged last chunk
+    assert ws(1, 1, 256, 17, 17, 64) == 0     # unsupported d
+    assert ws(1, 1, 256, 64, 32, 64) == 0     # dk != dv
+    assert ws(1, 1, 256, 64, 64, 48) == 0     # unsupported chunk
+    # state sections scale with the number of chunks (ceil(T / chunk))
+    a, b = ws(2, 4, 2048, 64, 64, 64), ws(2, 4, 2048, 64, 64, 128)
+    assert a > b
+
+
+def _fwd(lib, **kw):
+    args = dict(B=1, H=1, T=64, dk=16, dv=16, dtype=0, q=8, k=8, v=8, gamma=8, lam=8, iters=4, tol=0.0,
+                chunk=64, out=8, it=None, H0=None, G0=None, Hf=None, Gf=None, ws=256, wsb=1 << 20)
+    args.update(kw)
+    a = args
+    return lib.mesa_forward_chunked(a["B"], a["H"], a["T"], a["dk"], a["dv"], a["dtype"], a["q"], a["k"],
+                                    a["v"], a["gamma"], a["lam"], a["iters"], a["tol"], a["chunk"], a["out"],
+                                    a["it"], a["H0"], a["G0"], a["Hf"], a["Gf"], a["ws"], a["wsb"], None)
+
+
+def test_forward_rejects_bad_arguments_without_launching(lib):
+    # every case below returns before any CUDA call, so it runs without a GPU
+    assert _fwd(lib, dk=24, dv=24) == 2
+    assert _fwd(lib, dk=64, dv=32) == 2
+    assert _fwd(lib, chunk=48) == 2
+    assert _fwd(lib, B=-1) == 1
+    assert _fwd(lib, iters=-1) == 1
+    assert _fwd(lib, iters=100000) == 1
+    assert _fwd(lib, dtype=7) == 1
+    assert _fwd(lib, tol=float("nan")) == 1
+    assert _fwd(lib, H0=8) == 1               # H0 without G0
+    assert _fwd(lib, Hf=8) == 1               # H_final without G_final
+    assert _fwd(lib, q=None) == 1
+    assert _fwd(lib, ws=None) == 3
+    assert _fwd(lib, wsb=16) == 3
+    assert _fwd(lib, ws=264) == 3             # misaligned workspace
+    assert _fwd(lib, B=0) == 0                # empty batch: nothing to do
+    assert _fwd(lib, T=0) == 0                # empty sequence: nothing to do
+
+
+def test_decode_rejects_bad_arguments_without_launching(lib):
+    f = lib.mesa_decode_step
+    base = [1, 1, 16, 16, 0, 16, 16, 8, 8, 8, 8, 8, 4, 0.0, 8, None, None]
+    def call(i, val):
+        a = list(base)
+        a[i] = val
+        return f(*a)
+    assert call(2, 20) == 2 and call(3, 32) == 2
+    assert call(0, -1) == 1 and call(12, -2) == 1 and call(4, 3) == 1
+    assert call(5, None) == 1 and call(14, None) == 1
+    assert call(5, 20) == 1                   # H_state not 16-byte aligned
+    assert call(0, 0) == 0                    # no sequences
+
+
+def test_binding_raises_without_gpu_or_library():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    q = torch.zeros(1, 1, 4, 16)
+    with pytest.raises(Exception):
+        binding.mesa_forward_chunked(q, q, q, torch.ones(1, 1, 4), torch.ones(1, 16), 2, 0.0, 16)

@@ -1,0 +1,89 @@
+"""GPU parity of the recurrent decode step (mesa_decode_step through the C ABI) against
+the fp64 oracle, including the full-size decode workload on sampled units."""
+import numpy as np
+import pytest
+
+import oracle
+from mesa_layer_gb300 import synth
+from helpers import check_against_oracle, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from mesa_layer_gb300 import binding, build
+    build.build()
+    binding.load()
+
+
+def _run(w, steps, prefix, units=None, iters=None, tol=None):
+    """Decode `prefix` state-only steps (cg_iters = 0) and then `steps` full steps on the GPU
+    and, for `units` (list of (n, h); default all), in the oracle."""
+    import torch
+
+    from mesa_layer_gb300 import binding
+    iters = w.cg_iters if iters is None else iters
+    tol = w.cg_tol if tol is None else tol
+    N, H, d = w.B, w.H, w.dk
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    lam = synth.lambdas(w)
+    lam_t = torch.from_numpy(lam).cuda()
+    Hs = torch.zeros(N, H, d, d, device="cuda")
+    Gs = torch.zeros(N, H, d, d, device="cuda")
+    units = units or [(n, h) for n in range(N) for h in range(H)]
+    nidx = np.array([u[0] for u in units])
+    hidx = np.array([u[1] for u in units])
+    U = len(units)
+    Ho = np.zeros((U, 1, d, d))
+    Go = np.zeros((U, 1, d, d))
+    lam_u = lam[hidx]  # each sampled unit keeps its head's lambda (as a 1-head oracle unit)
+    errs, agree = [], []
+    for s in range(-prefix, steps):
+        inp = synth.decode_inputs(w, s)
+        dev = {k: torch.from_numpy(inp[k]).cuda().to(td if k != "gamma" else torch.float32)
+               for k in ("q", "k", "v", "gamma")}
+        n_it = 0 if s < 0 else iters
+        o, it = binding.mesa_decode_step(Hs, Gs, dev["q"], dev["k"], dev["v"], dev["gamma"], lam_t, n_it, tol)
+        sub = lambda x: x[nidx, hidx][:, None]
+        ro = np.zeros((U, 1, d))
+        rit = np.zeros((U, 1), dtype=np.int32)
+        for i in range(U):
+            ro[i], rit[i] = oracle.decode_step(Ho[i:i + 1], Go[i:i + 1], sub(inp["q"])[i:i + 1],
+                                               sub(inp["k"])[i:i + 1], sub(inp["v"])[i:i + 1],
+                                               sub(inp["gamma"])[i:i + 1], lam_u[i][None], n_it, tol)
+        if s >= 0:
+            torch.cuda.synchronize()
+            og = o.float().cpu().numpy()[nidx, hidx]
+            ig = it.cpu().numpy()[nidx, hidx]
+            errs.append(rel_err(og, ro[:, 0]))
+            agree.append(ig == rit[:, 0])
+            check_against_oracle(og, ig, ro[:, 0], rit[:, 0], w.dtype, tol, f"step {s}")
+    Hg = Hs.cpu().numpy()[nidx, hidx]
+    Gg = Gs.cpu().numpy()[nidx, hidx]
+    assert np.abs(Hg - Ho[:, 0]).max() <= 1e-5 * np.abs(Ho).max()
+    assert np.abs(Gg - Go[:, 0]).max() <= 1e-5 * np.abs(Go).max()
+    return np.concatenate(errs), np.concatenate(agree)
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_small(d, dtype):
+    w = synth.workload("decode_bf16_d128", B=3, H=2, dk=d, dv=d, dtype=dtype, prefix=0)
+    err, agree = _run(w, steps=24, prefix=0, iters=d + 4, tol=0.0)
+    print(f"decode d={d} {dtype}: max rel err {err.max():.3e}")
+
+
+def test_decode_dynamic_with_prefix():
+    w = synth.workload("decode_bf16_d128", B=4, H=2, dtype="f32", prefix=40)
+    err, agree = _run(w, steps=16, prefix=40, tol=1e-4)
+    print(f"decode dynamic: max rel err {err.max():.3e}, counts agree {agree.mean():.4f}")
+
+
+def test_decode_full_size_sampled_units():
+    w = synth.workload("decode_bf16_d128")
+    units = [(0, 0), (17, 5), (128, 9), (255, 15)]
+    err, agree = _run(w, steps=w.decode_steps, prefix=w.prefix, units=units)
+    print(f"decode full: max rel err {err.max():.3e}, counts agree {agree.mean():.4f}")

@@ -1,0 +1,179 @@
+"""GPU parity of the chunked forward (mesa_forward_chunked through the C ABI) against the
+fp64 oracle, on the five workloads' forward configurations and on edge cases."""
+import numpy as np
+import pytest
+
+import oracle
+from mesa_layer_gb300 import synth
+from helpers import TOL, check_against_oracle, gpu_forward, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from mesa_layer_gb300 import binding, build
+    build.build()
+    binding.load()
+
+
+def _oracle(inp, w, **kw):
+    return oracle.forward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], w.cg_iters, w.cg_tol, **kw)
+
+
+def test_tiny_fp32_d16_full():
+    w = synth.workload("tiny_fp32_d16")
+    inp = synth.forward_inputs(w)
+    o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
+    ro, rit = _oracle(inp, w)
+    err = check_against_oracle(o, it, ro, rit, w.dtype, w.cg_tol, "tiny")
+    assert (it == 16).all()
+    print(f"tiny: max rel err {err.max():.3e}")
+
+
+def test_fp32_d64_dynamic_full():
+    w = synth.workload("fwd_fp32_d64")
+    inp = synth.forward_inputs(w)
+    o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
+    ro, rit = _oracle(inp, w)
+    err = check_against_oracle(o, it, ro, rit, w.dtype, w.cg_tol, "fp32_d64")
+    print(f"fp32_d64: max rel err {err.max():.3e}, counts agree {np.mean(it == rit):.4f}, "
+          f"mean iters {it.mean():.2f}")
+
+
+def _sample_units(w, inp, units):
+    """Inputs of a subset of (batch, head) units, keeping each unit's own lambda row."""
+    sub = {}
+    for key in ("q", "k", "v", "gamma"):
+        sub[key] = np.stack([inp[key][b, h] for b, h in units])[None]
+    sub["lam_rows"] = np.stack([inp["lam"][h] for _, h in units])
+    return sub
+
+
+def _oracle_units(w, inp, units, t0=0, t1=None):
+    """Oracle on selected units over tokens [t0, t1); the state at t0 comes from the
+    oracle's own state-only pass (cg_iters = 0) over tokens [0, t0)."""
+    outs, its = [], []
+    for b, h in units:
+        sl = lambda x, a, z: x[b, h][None, None, a:z]
+        lam = inp["lam"][h][None]
+        H0 = G0 = None
+        if t0 > 0:
+            _, _, H0, G0 = oracle.forward(sl(inp["q"], 0, t0), sl(inp["k"], 0, t0), sl(inp["v"], 0, t0),
+                                          inp["gamma"][b, h][None, None, :t0], lam, 0, 0.0, want_final=True)
+        o, it = oracle.forward(sl(inp["q"], t0, t1), sl(inp["k"], t0, t1), sl(inp["v"], t0, t1),
+                               inp["gamma"][b, h][None, None, t0:t1], lam, w.cg_iters, w.cg_tol, H0=H0, G0=G0)
+        outs.append(o[0, 0])
+        its.append(it[0, 0])
+    return np.stack(outs), np.stack(its)
+
+
+def test_bf16_d128_full_size_sampled_units():
+    w = synth.workload("fwd_bf16_d128")
+    inp = synth.forward_inputs(w)
+    o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
+    assert (it == w.cg_iters).all()
+    units = [(0, 0), (3, 7), (7, 15)]
+    ro, rit = _oracle_units(w, inp, units)
+    og = np.stack([o[b, h] for b, h in units])
+    ig = np.stack([it[b, h] for b, h in units])
+    err = check_against_oracle(og, ig, ro, rit, w.dtype, w.cg_tol, "bf16_d128")
+    print(f"bf16_d128: max rel err {err.max():.3e} (mean {err.mean():.2e})")
+
+
+def test_long_bf16_full_size_sampled_windows():
+    w = synth.workload("long_bf16_d128")
+    inp = synth.forward_inputs(w)
+    o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
+    assert it.min() >= 0 and it.max() <= w.cg_iters
+    for (b, h), (t0, t1) in [((0, 0), (0, 2048)), ((0, 11), (w.T - 2048, w.T))]:
+        ro, rit = _oracle_units(w, inp, [(b, h)], t0, t1)
+        err = check_against_oracle(o[b, h, t0:t1], it[b, h, t0:t1], ro[0], rit[0], w.dtype, w.cg_tol,
+                                   f"long[{h}, {t0}:{t1}]")
+        print(f"long head {h} tokens {t0}:{t1}: max rel err {err.max():.3e}, "
+              f"counts agree {np.mean(it[b, h, t0:t1] == rit[0]):.4f}")
+
+
+EDGE = [
+    # (dtype, B, H, T, d, chunk, iters, tol)
+    ("f32", 1, 1, 1, 16, 16, 4, 0.0),          # a single token
+    ("f32", 1, 2, 100, 32, 32, 12, 0.0),       # ragged last chunk
+    ("f32", 2, 1, 130, 64, 64, 20, 1e-5),      # ragged, dynamic
+    ("f32", 1, 1, 200, 128, 128, 10, 0.0),     # d = 128, ragged
+    ("bf16", 1, 2, 257, 128, 64, 15, 0.0),     # bf16, several tiles and a 1-token tail
+    ("bf16", 2, 2, 96, 64, 16, 8, 1e-3),       # small chunks, dynamic
+    ("f32", 3, 1, 64, 16, 64, 0, 0.0),         # zero iterations: o = 0
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "-".join(map(str, c)))
+def test_edge_shapes(case):
+    dtype, B, H, T, d, chunk, iters, tol = case
+    w = synth.workload("fwd_fp32_d64", dtype=dtype, B=B, H=H, T=T, dk=d, dv=d, chunk=chunk,
+                       cg_iters=iters, cg_tol=tol)
+    inp = synth.forward_inputs(w, seed=5)
+    o, it = gpu_forward(inp, dtype, iters, tol, chunk)
+    ro, rit = _oracle(inp, w)
+    check_against_oracle(o, it, ro, rit, dtype, tol, str(case))
+    if iters == 0:
+        assert np.all(o == 0)
+
+
+@pytest.mark.parametrize("regime", ["gamma_near_zero", "gamma_one", "lambda_large", "zero_queries"])
+def test_edge_values(regime):
+    w = synth.workload("fwd_fp32_d64", B=1, H=2, T=192, dk=32, dv=32, chunk=64, cg_iters=12, cg_tol=0.0)
+    inp = synth.forward_inputs(w, seed=9)
+    if regime == "gamma_near_zero":
+        inp["gamma"][:] = np.float32(1e-3)
+        inp["gamma"][0, 0, 70] = 0.0
+    elif regime == "gamma_one":
+        inp["gamma"][:] = 1.0
+        inp["lam"][:] = 1.0
+    elif regime == "lambda_large":
+        inp["lam"][:] = 50.0
+    else:
+        inp["q"][0, 1, ::3] = 0.0
+    o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
+    ro, rit = _oracle(inp, w)
+    check_against_oracle(o, it, ro, rit, w.dtype, 0.0, regime)
+    if regime == "zero_queries":
+        assert np.all(o[0, 1, ::3] == 0)
+        # dynamic mode stops zero queries before the first iteration
+        o2, it2 = gpu_forward(inp, w.dtype, 12, 1e-3, w.chunk)
+        assert np.all(it2[0, 1, ::3] == 0) and np.all(o2[0, 1, ::3] == 0)
+
+
+def test_chunk_size_invariance():
+    w = synth.workload("fwd_fp32_d64", B=1, H=2, T=256, cg_iters=16, cg_tol=0.0)
+    inp = synth.forward_inputs(w, seed=3)
+    ro, _ = _oracle(inp, w)
+    outs = [gpu_forward(inp, w.dtype, 16, 0.0, c)[0] for c in (16, 32, 64, 128)]
+    for o in outs:
+        assert rel_err(o, ro).max() <= TOL["f32"]
+        assert rel_err(o, outs[0]).max() <= TOL["f32"]
+
+
+def test_initial_and_final_states():
+    import torch
+
+    w = synth.workload("fwd_fp32_d64", B=2, H=2, T=160, cg_iters=10, cg_tol=0.0)
+    inp = synth.forward_inputs(w, seed=4)
+    ro, rit, Hf, Gf = _oracle(inp, w, want_final=True)
+    B, H, d = w.B, w.H, w.dk
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+    Hg, Gg = torch.empty(B, H, d, d, device="cuda"), torch.empty(B, H, d, d, device="cuda")
+    o, it = gpu_forward(inp, w.dtype, w.cg_iters, 0.0, 64, H_final=Hg, G_final=Gg)
+    check_against_oracle(o, it, ro, rit, w.dtype, 0.0, "full")
+    for a, b in ((Hg, Hf), (Gg, Gf)):
+        a = a.cpu().numpy().astype(np.float64)
+        assert np.abs(a - b).max() <= 1e-5 * np.abs(b).max()
+    # split the sequence: tokens [0, 70) then [70, 160) from the exported state
+    t1 = 70
+    first = {k: (v[:, :, :t1] if k != "lam" else v) for k, v in inp.items()}
+    second = {k: (v[:, :, t1:] if k != "lam" else v) for k, v in inp.items()}
+    H1, G1 = torch.empty_like(Hg), torch.empty_like(Gg)
+    o1, _ = gpu_forward(first, w.dtype, w.cg_iters, 0.0, 32, H_final=H1, G_final=G1)
+    o2, _ = gpu_forward(second, w.dtype, w.cg_iters, 0.0, 64, H0=H1, G0=G1)
+    assert rel_err(np.concatenate([o1, o2], axis=2), ro).max() <= TOL["f32"]
