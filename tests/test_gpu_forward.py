@@ -5,7 +5,7 @@ import pytest
 
 import oracle
 from mesa_layer_gb300 import synth
-from helpers import TOL, check_against_oracle, gpu_forward, rel_err
+from helpers import TOL, check_against_oracle, gpu_forward, unit_err
 
 pytestmark = pytest.mark.gpu
 
@@ -28,9 +28,9 @@ def test_tiny_fp32_d16_full():
     inp = synth.forward_inputs(w)
     o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
     ro, rit = _oracle(inp, w)
-    err = check_against_oracle(o, it, ro, rit, w.dtype, w.cg_tol, "tiny")
+    err, tok = check_against_oracle(o, it, ro, rit, w.dtype, w.cg_tol, "tiny")
     assert (it == 16).all()
-    print(f"tiny: max rel err {err.max():.3e}")
+    print(f"tiny: max rel err {err:.3e}, per-token max {tok.max():.3e}")
 
 
 def test_fp32_d64_dynamic_full():
@@ -38,9 +38,9 @@ def test_fp32_d64_dynamic_full():
     inp = synth.forward_inputs(w)
     o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
     ro, rit = _oracle(inp, w)
-    err = check_against_oracle(o, it, ro, rit, w.dtype, w.cg_tol, "fp32_d64")
-    print(f"fp32_d64: max rel err {err.max():.3e}, counts agree {np.mean(it == rit):.4f}, "
-          f"mean iters {it.mean():.2f}")
+    err, tok = check_against_oracle(o, it, ro, rit, w.dtype, w.cg_tol, "fp32_d64")
+    print(f"fp32_d64: max rel err {err:.3e}, per-token median {np.median(tok):.2e}, counts agree "
+          f"{np.mean(it == rit):.4f}, mean iters {it.mean():.2f}")
 
 
 def _sample_units(w, inp, units):
@@ -79,8 +79,8 @@ def test_bf16_d128_full_size_sampled_units():
     ro, rit = _oracle_units(w, inp, units)
     og = np.stack([o[b, h] for b, h in units])
     ig = np.stack([it[b, h] for b, h in units])
-    err = check_against_oracle(og, ig, ro, rit, w.dtype, w.cg_tol, "bf16_d128")
-    print(f"bf16_d128: max rel err {err.max():.3e} (mean {err.mean():.2e})")
+    err, tok = check_against_oracle(og, ig, ro, rit, w.dtype, w.cg_tol, "bf16_d128")
+    print(f"bf16_d128: max rel err {err:.3e}, per-token max {tok.max():.2e} median {np.median(tok):.2e}")
 
 
 def test_long_bf16_full_size_sampled_windows():
@@ -90,9 +90,9 @@ def test_long_bf16_full_size_sampled_windows():
     assert it.min() >= 0 and it.max() <= w.cg_iters
     for (b, h), (t0, t1) in [((0, 0), (0, 2048)), ((0, 11), (w.T - 2048, w.T))]:
         ro, rit = _oracle_units(w, inp, [(b, h)], t0, t1)
-        err = check_against_oracle(o[b, h, t0:t1], it[b, h, t0:t1], ro[0], rit[0], w.dtype, w.cg_tol,
-                                   f"long[{h}, {t0}:{t1}]")
-        print(f"long head {h} tokens {t0}:{t1}: max rel err {err.max():.3e}, "
+        err, tok = check_against_oracle(o[b, h, t0:t1], it[b, h, t0:t1], ro[0], rit[0], w.dtype, w.cg_tol,
+                                        f"long[{h}, {t0}:{t1}]")
+        print(f"long head {h} tokens {t0}:{t1}: max rel err {err:.3e}, "
               f"counts agree {np.mean(it[b, h, t0:t1] == rit[0]):.4f}")
 
 
@@ -123,7 +123,9 @@ def test_edge_shapes(case):
 
 @pytest.mark.parametrize("regime", ["gamma_near_zero", "gamma_one", "lambda_large", "zero_queries"])
 def test_edge_values(regime):
-    w = synth.workload("fwd_fp32_d64", B=1, H=2, T=192, dk=32, dv=32, chunk=64, cg_iters=12, cg_tol=0.0)
+    # enough iterations to converge: these regimes check decay and masking, not how an
+    # unconverged CG iterate amplifies rounding
+    w = synth.workload("fwd_fp32_d64", B=1, H=2, T=192, dk=32, dv=32, chunk=64, cg_iters=48, cg_tol=0.0)
     inp = synth.forward_inputs(w, seed=9)
     if regime == "gamma_near_zero":
         inp["gamma"][:] = np.float32(1e-3)
@@ -141,18 +143,18 @@ def test_edge_values(regime):
     if regime == "zero_queries":
         assert np.all(o[0, 1, ::3] == 0)
         # dynamic mode stops zero queries before the first iteration
-        o2, it2 = gpu_forward(inp, w.dtype, 12, 1e-3, w.chunk)
+        o2, it2 = gpu_forward(inp, w.dtype, 48, 1e-3, w.chunk)
         assert np.all(it2[0, 1, ::3] == 0) and np.all(o2[0, 1, ::3] == 0)
 
 
 def test_chunk_size_invariance():
-    w = synth.workload("fwd_fp32_d64", B=1, H=2, T=256, cg_iters=16, cg_tol=0.0)
+    w = synth.workload("fwd_fp32_d64", B=1, H=2, T=256, dk=32, dv=32, cg_iters=40, cg_tol=0.0)
     inp = synth.forward_inputs(w, seed=3)
     ro, _ = _oracle(inp, w)
-    outs = [gpu_forward(inp, w.dtype, 16, 0.0, c)[0] for c in (16, 32, 64, 128)]
+    outs = [gpu_forward(inp, w.dtype, w.cg_iters, 0.0, c)[0] for c in (16, 32, 64, 128)]
     for o in outs:
-        assert rel_err(o, ro).max() <= TOL["f32"]
-        assert rel_err(o, outs[0]).max() <= TOL["f32"]
+        assert unit_err(o, ro).max() <= TOL["f32"]
+        assert unit_err(o, outs[0]).max() <= TOL["f32"]
 
 
 def test_initial_and_final_states():
@@ -176,4 +178,4 @@ def test_initial_and_final_states():
     H1, G1 = torch.empty_like(Hg), torch.empty_like(Gg)
     o1, _ = gpu_forward(first, w.dtype, w.cg_iters, 0.0, 32, H_final=H1, G_final=G1)
     o2, _ = gpu_forward(second, w.dtype, w.cg_iters, 0.0, 64, H0=H1, G0=G1)
-    assert rel_err(np.concatenate([o1, o2], axis=2), ro).max() <= TOL["f32"]
+    assert unit_err(np.concatenate([o1, o2], axis=2), ro).max() <= TOL["f32"]
