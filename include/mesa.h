@@ -28,6 +28,10 @@
  *     treated as e^-80 (its log is clamped).
  *   - Supported sizes: dk == dv in {16, 32, 64, 128}; T >= 0 (any value: a ragged last
  *     chunk is handled); chunk in {16, 32, 64, 128}.  0 <= cg_iters <= 4096.
+ *   - Two compute paths, same results up to rounding (the chunked form is exact for any
+ *     chunk length): bf16 inputs with dk = dv = 128 and 16-byte aligned q/k/v/out/H0/G0
+ *     run on the tensor cores with 128-token chunks (the `chunk` argument then only sizes
+ *     the workspace); everything else runs the fp32 SIMT path with `chunk`-token chunks.
  *   - Return value: MESA_OK when the arguments were valid and the kernels were
  *     enqueued; otherwise an error code and nothing was enqueued (MESA_ERR_CUDA: a
  *     launch failed; cudaGetLastError() holds the cause).  Calls that run
@@ -63,7 +67,7 @@ const char *mesa_status_string(int status);
 
 /*
  * Bytes of device workspace mesa_forward_chunked needs for these sizes (256-byte
- * aligned start required).  It holds the per-token log-decays [B, H, T] and the
+ * aligned start required).  It holds a status word, the per-token log-decays [B, H, T] and the
  * chunk-boundary states S^H_c [B, H, ceil(T/chunk), dk, dk] and
  * S^G_c [B, H, ceil(T/chunk), dv, dk] in fp32.  Returns 0 for unsupported sizes.
  */
@@ -108,6 +112,24 @@ int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state,
                      float *G_state, const void *q, const void *k, const void *v,
                      const float *gamma, const float *lambda_diag, int cg_iters,
                      float cg_tol, void *out, int32_t *iters_used, cudaStream_t stream);
+
+/*
+ * Device status word of the last mesa_forward_chunked call that used `workspace`:
+ * synchronises `stream`, then copies the word to *flags (host).  0 means no kernel gave up;
+ * bit 0 set means a tensor-core kernel's bounded wait for its matrix multiplies expired and
+ * the affected chunks' outputs were not written.  The word is cleared at the start of every
+ * forward call.
+ */
+int mesa_forward_status(const void *workspace, cudaStream_t stream, unsigned *flags);
+
+/*
+ * Diagnostic of the tensor-core building blocks (no counterpart on the MesaNet pages):
+ * device A, B [128, 128] fp32 row-major; writes C1 = fp16(A) fp16(B)^T and
+ * C2 = fp16(A) fp16(B) [128, 128] fp32, computed by tcgen05.mma with the same operand
+ * layouts and descriptors the chunked CG uses.  *status (device) gets bit 0 on a timeout.
+ */
+int mesa_tc_selftest(const float *A, const float *B, float *C1, float *C2, unsigned *status,
+                     cudaStream_t stream);
 
 /*
  * Per-kernel timing for benchmarks (no counterpart on the MesaNet pages; a measurement

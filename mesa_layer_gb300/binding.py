@@ -50,6 +50,10 @@ def load(build_if_missing: bool = True):
     lib.mesa_forward_chunked.restype = _i
     lib.mesa_forward_chunked.argtypes = [_i] * 6 + [_vp] * 5 + [_i, _f, _i, _vp, _ip] + \
         [_fp] * 4 + [_vp, _sz, _vp]
+    lib.mesa_forward_status.restype = _i
+    lib.mesa_forward_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.mesa_tc_selftest.restype = _i
+    lib.mesa_tc_selftest.argtypes = [_vp] * 5 + [_vp]
     lib.mesa_decode_step.restype = _i
     lib.mesa_decode_step.argtypes = [_i] * 5 + [_fp, _fp, _vp, _vp, _vp, _fp, _fp, _i, _f, _vp, _ip, _vp]
     _lib = lib
@@ -149,3 +153,26 @@ def mesa_decode_step(H_state, G_state, q, k, v, gamma, lambda_diag, cg_iters, cg
                               _ptr(out), _ptr(iters_used), _stream(stream))
     _check(st, "mesa_decode_step")
     return out, iters_used
+
+
+def mesa_forward_status(workspace, stream=None) -> int:
+    """Synchronise the stream and return the device status word of the last forward call
+    that used ``workspace`` (0: every kernel completed)."""
+    lib = load()
+    flags = ctypes.c_uint(0)
+    _check(lib.mesa_forward_status(_ptr(workspace), _stream(stream), ctypes.byref(flags)), "mesa_forward_status")
+    return int(flags.value)
+
+
+def mesa_tc_selftest(A, B, stream=None):
+    """Tensor-core building-block check: returns (C1 = A B^T, C2 = A B, status) computed by
+    tcgen05.mma on fp16-rounded [128, 128] inputs."""
+    lib = load()
+    _require(A, "A", torch.float32)
+    _require(B, "B", torch.float32)
+    C1 = torch.empty(128, 128, device=A.device)
+    C2 = torch.empty(128, 128, device=A.device)
+    status = torch.zeros(1, dtype=torch.int32, device=A.device)
+    _check(lib.mesa_tc_selftest(_ptr(A), _ptr(B), _ptr(C1), _ptr(C2), _ptr(status), _stream(stream)),
+           "mesa_tc_selftest")
+    return C1, C2, status

@@ -16,13 +16,26 @@ bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 bool chunk_ok(int c) { return c == 16 || c == 32 || c == 64 || c == 128; }
 bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+constexpr size_t kStatusBytes = 256;
+
+// Workspace: [status word | log-decays | S^H states | S^G states].  Sized for `chunk`,
+// which is <= 128, so it also covers the tensor-core path's 128-token chunks.
 size_t workspace_parts(int B, int H, int T, int dk, int dv, int chunk, size_t *off) {
   const size_t U = (size_t)B * H;
   const size_t NC = (size_t)(T + chunk - 1) / chunk;
-  off[0] = 0;
+  off[0] = kStatusBytes;
   off[1] = off[0] + align256(U * T * sizeof(float));
   off[2] = off[1] + align256(U * NC * dk * dk * sizeof(float));
   return off[2] + align256(U * NC * dv * dk * sizeof(float));
+}
+
+// The tensor-core path covers bf16 inputs with dk = dv = 128 (16-byte aligned operands).
+bool use_tc(int dtype, int dk, int dv, const void *q, const void *k, const void *v, const void *out,
+            const float *H0, const float *G0) {
+  if (dtype != MESA_BF16 || dk != 128 || dv != 128) return false;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return false;
+  if ((H0 && !aligned(H0, 16)) || (G0 && !aligned(G0, 16))) return false;
+  return true;
 }
 
 // ---- optional per-kernel timing (benchmarks only) --------------------------------------
@@ -107,11 +120,27 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_SCAN: return "mesa_scan_kernel";
     case mesa::K_CG_SIMT: return "mesa_cg_simt_kernel";
     case mesa::K_DECODE: return "mesa_decode_kernel";
+    case mesa::K_CG_TC: return "mesa_cg_tc_kernel";
   }
   return nullptr;
 }
 
 int mesa_version(void) { return 100; }
+
+int mesa_forward_status(const void *workspace, cudaStream_t stream, unsigned *flags) {
+  if (!workspace || !flags) return MESA_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(flags, workspace, sizeof(unsigned), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return MESA_ERR_CUDA;
+  return MESA_OK;
+}
+
+int mesa_tc_selftest(const float *A, const float *B, float *C1, float *C2, unsigned *status,
+                     cudaStream_t stream) {
+  if (!A || !B || !C1 || !C2 || !status) return MESA_ERR_INVALID_ARG;
+  return mesa::launch_tc_selftest(A, B, C1, C2, status, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
+}
 
 const char *mesa_status_string(int s) {
   switch (s) {
@@ -161,13 +190,17 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
   const size_t need = workspace_parts(B, H, T, dk, dv, chunk, off);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return MESA_ERR_WORKSPACE;
 
-  mesa::FwdArgs a{B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol, chunk,
-                  out, iters_used, H0, G0, H_final, G_final};
+  const bool tc = use_tc(dtype, dk, dv, q, k, v, out, H0, G0);
+  mesa::FwdArgs a{B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol,
+                  tc ? 128 : chunk, out, iters_used, H0, G0, H_final, G_final};
   char *w = (char *)workspace;
+  unsigned *status = (unsigned *)w;
   mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2])};
+  if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
   if (mesa::launch_chunk_states(a, ws, stream) != 0) return MESA_ERR_CUDA;
-  if (mesa::launch_chunk_cg_simt(a, ws, stream) != 0) return MESA_ERR_CUDA;
-  return MESA_OK;
+  const int rc = tc ? mesa::launch_chunk_cg_tc(a, ws, status, stream)
+                    : mesa::launch_chunk_cg_simt(a, ws, stream);
+  return rc == 0 ? MESA_OK : MESA_ERR_CUDA;
 }
 
 int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state, float *G_state,

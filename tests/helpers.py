@@ -56,9 +56,14 @@ def gpu_forward(inp: dict, dtype: str, cg_iters: int, cg_tol: float, chunk: int,
 
     from mesa_layer_gb300 import binding
     t = torch_inputs(inp, dtype)
+    B, H, T, dk = t["q"].shape
+    ws = torch.empty(max(256, binding.mesa_forward_workspace_size(B, H, T, dk, t["v"].shape[-1], chunk)),
+                     dtype=torch.uint8, device="cuda")
     out, it = binding.mesa_forward_chunked(t["q"], t["k"], t["v"], t["gamma"], t["lam"], cg_iters,
-                                           cg_tol, chunk, **kw)
+                                           cg_tol, chunk, workspace=ws, **kw)
     torch.cuda.synchronize()
+    if T > 0:
+        assert binding.mesa_forward_status(ws) == 0, "a kernel reported a bounded-wait timeout"
     return out.float().cpu().numpy().astype(np.float64), it.cpu().numpy()
 
 

@@ -1,0 +1,82 @@
+"""Tensor-core building blocks (tcgen05.mma with the swizzled fp16 operand layouts the
+chunked CG uses) against a plain matrix product, and the tensor-core forward path against
+the oracle on shapes that exercise its tiling."""
+import numpy as np
+import pytest
+
+import oracle
+from mesa_layer_gb300 import synth
+from helpers import check_against_oracle, gpu_forward, unit_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from mesa_layer_gb300 import binding, build
+    build.build()
+    binding.load()
+
+
+def test_tc_selftest_matches_fp16_products():
+    import torch
+
+    from mesa_layer_gb300 import binding
+    rng = np.random.default_rng(0)
+    A = rng.standard_normal((128, 128)).astype(np.float32)
+    B = rng.standard_normal((128, 128)).astype(np.float32)
+    A[3, :] = 0.0
+    B[:, 7] *= 1e-3
+    C1, C2, st = binding.mesa_tc_selftest(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda())
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    a16 = A.astype(np.float16).astype(np.float64)
+    b16 = B.astype(np.float16).astype(np.float64)
+    np.testing.assert_allclose(C1.cpu().numpy(), a16 @ b16.T, rtol=1e-5, atol=1e-4)
+    np.testing.assert_allclose(C2.cpu().numpy(), a16 @ b16, rtol=1e-5, atol=1e-4)
+
+
+TC_CASES = [
+    # (B, H, T, iters, tol, note)
+    (1, 1, 128, 8, 0.0, "one full chunk"),
+    (1, 2, 300, 15, 0.0, "ragged last chunk"),
+    (2, 1, 520, 30, 1e-3, "dynamic"),
+    (1, 1, 96, 0, 0.0, "zero iterations"),
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=lambda c: c[-1].replace(" ", "_"))
+def test_tc_forward_against_oracle(case):
+    B, H, T, iters, tol, _ = case
+    w = synth.workload("fwd_bf16_d128", B=B, H=H, T=T, cg_iters=iters, cg_tol=tol)
+    inp = synth.forward_inputs(w, seed=11)
+    o, it = gpu_forward(inp, "bf16", iters, tol, 64)
+    ro, rit = oracle.forward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], iters, tol)
+    err, tok = check_against_oracle(o, it, ro, rit, "bf16", tol, case[-1])
+    print(f"tc {case[-1]}: max rel err {err:.3e}")
+    if iters == 0:
+        assert np.all(o == 0)
+
+
+def test_tc_initial_state_and_final_states():
+    import torch
+
+    w = synth.workload("fwd_bf16_d128", B=1, H=2, T=384, cg_iters=12, cg_tol=0.0)
+    inp = synth.forward_inputs(w, seed=12)
+    ro, rit, Hf, Gf = oracle.forward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], 12, 0.0,
+                                     want_final=True)
+    t1 = 200
+    first = {k: (v[:, :, :t1] if k != "lam" else v) for k, v in inp.items()}
+    second = {k: (v[:, :, t1:] if k != "lam" else v) for k, v in inp.items()}
+    H1 = torch.empty(1, 2, 128, 128, device="cuda")
+    G1 = torch.empty_like(H1)
+    Hg, Gg = torch.empty_like(H1), torch.empty_like(H1)
+    o1, i1 = gpu_forward(first, "bf16", 12, 0.0, 64, H_final=H1, G_final=G1)
+    o2, i2 = gpu_forward(second, "bf16", 12, 0.0, 64, H0=H1, G0=G1, H_final=Hg, G_final=Gg)
+    o = np.concatenate([o1, o2], axis=2)
+    check_against_oracle(o, np.concatenate([i1, i2], axis=2), ro, rit, "bf16", 0.0, "split")
+    for a, b in ((Hg, Hf), (Gg, Gf)):
+        a = a.cpu().numpy().astype(np.float64)
+        assert np.abs(a - b).max() <= 1e-5 * np.abs(b).max()
