@@ -124,12 +124,13 @@ int mesa_forward_status(const void *workspace, cudaStream_t stream, unsigned *fl
 
 /*
  * Diagnostic of the tensor-core building blocks (no counterpart on the MesaNet pages):
- * device A, B [128, 128] fp32 row-major; writes C1 = fp16(A) fp16(B)^T and
- * C2 = fp16(A) fp16(B) [128, 128] fp32, computed by tcgen05.mma with the same operand
- * layouts and descriptors the chunked CG uses.  *status (device) gets bit 0 on a timeout.
+ * device A, B [128, 128] fp32 row-major; writes C1 = fp16(A) fp16(B)^T,
+ * C2 = fp16(A) fp16(B) and C3 = fp16(A)^T fp16(B) [128, 128] fp32, computed by tcgen05.mma
+ * with the operand layouts and descriptors the chunked kernels use (K-major operands,
+ * MN-major B, MN-major A).  *status (device) gets bit 0 on a timeout.
  */
-int mesa_tc_selftest(const float *A, const float *B, float *C1, float *C2, unsigned *status,
-                     cudaStream_t stream);
+int mesa_tc_selftest(const float *A, const float *B, float *C1, float *C2, float *C3,
+                     unsigned *status, cudaStream_t stream);
 
 /*
  * Per-kernel timing for benchmarks (no counterpart on the MesaNet pages; a measurement

@@ -53,7 +53,7 @@ def load(build_if_missing: bool = True):
     lib.mesa_forward_status.restype = _i
     lib.mesa_forward_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint)]
     lib.mesa_tc_selftest.restype = _i
-    lib.mesa_tc_selftest.argtypes = [_vp] * 5 + [_vp]
+    lib.mesa_tc_selftest.argtypes = [_vp] * 6 + [_vp]
     lib.mesa_decode_step.restype = _i
     lib.mesa_decode_step.argtypes = [_i] * 5 + [_fp, _fp, _vp, _vp, _vp, _fp, _fp, _i, _f, _vp, _ip, _vp]
     _lib = lib
@@ -165,14 +165,15 @@ def mesa_forward_status(workspace, stream=None) -> int:
 
 
 def mesa_tc_selftest(A, B, stream=None):
-    """Tensor-core building-block check: returns (C1 = A B^T, C2 = A B, status) computed by
-    tcgen05.mma on fp16-rounded [128, 128] inputs."""
+    """Tensor-core building-block check: returns (C1 = A B^T, C2 = A B, C3 = A^T B, status)
+    computed by tcgen05.mma on fp16-rounded [128, 128] inputs."""
     lib = load()
     _require(A, "A", torch.float32)
     _require(B, "B", torch.float32)
     C1 = torch.empty(128, 128, device=A.device)
     C2 = torch.empty(128, 128, device=A.device)
+    C3 = torch.empty(128, 128, device=A.device)
     status = torch.zeros(1, dtype=torch.int32, device=A.device)
-    _check(lib.mesa_tc_selftest(_ptr(A), _ptr(B), _ptr(C1), _ptr(C2), _ptr(status), _stream(stream)),
-           "mesa_tc_selftest")
-    return C1, C2, status
+    _check(lib.mesa_tc_selftest(_ptr(A), _ptr(B), _ptr(C1), _ptr(C2), _ptr(C3), _ptr(status),
+                                _stream(stream)), "mesa_tc_selftest")
+    return C1, C2, C3, status

@@ -121,6 +121,7 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_CG_SIMT: return "mesa_cg_simt_kernel";
     case mesa::K_DECODE: return "mesa_decode_kernel";
     case mesa::K_CG_TC: return "mesa_cg_tc_kernel";
+    case mesa::K_DELTA_TC: return "mesa_delta_tc_kernel";
   }
   return nullptr;
 }
@@ -136,10 +137,10 @@ int mesa_forward_status(const void *workspace, cudaStream_t stream, unsigned *fl
   return MESA_OK;
 }
 
-int mesa_tc_selftest(const float *A, const float *B, float *C1, float *C2, unsigned *status,
-                     cudaStream_t stream) {
-  if (!A || !B || !C1 || !C2 || !status) return MESA_ERR_INVALID_ARG;
-  return mesa::launch_tc_selftest(A, B, C1, C2, status, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
+int mesa_tc_selftest(const float *A, const float *B, float *C1, float *C2, float *C3,
+                     unsigned *status, cudaStream_t stream) {
+  if (!A || !B || !C1 || !C2 || !C3 || !status) return MESA_ERR_INVALID_ARG;
+  return mesa::launch_tc_selftest(A, B, C1, C2, C3, status, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
 }
 
 const char *mesa_status_string(int s) {
@@ -197,7 +198,7 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
   unsigned *status = (unsigned *)w;
   mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2])};
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
-  if (mesa::launch_chunk_states(a, ws, stream) != 0) return MESA_ERR_CUDA;
+  if (mesa::launch_chunk_states(a, ws, tc ? status : nullptr, stream) != 0) return MESA_ERR_CUDA;
   const int rc = tc ? mesa::launch_chunk_cg_tc(a, ws, status, stream)
                     : mesa::launch_chunk_cg_simt(a, ws, stream);
   return rc == 0 ? MESA_OK : MESA_ERR_CUDA;

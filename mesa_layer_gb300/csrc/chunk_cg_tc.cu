@@ -13,20 +13,24 @@
 // or hi*K + lo*K (K and V are bf16 inputs, exact in fp16 after scaling).  Accumulation is
 // fp32.  The CG scalars and the x, r vectors stay fp32 (x, r in tensor memory).
 //
-// One CTA of 128 threads per chunk; thread i owns token row i, which is tensor-memory lane
-// i of every accumulator, so all per-token dot products are thread-local.
+// One CTA of 512 threads per chunk.  Warp w reads tensor-memory lane quadrant q = w % 4
+// (token rows 32q .. 32q+31, one row per lane) and column group g = w / 4 (32 of the 128
+// columns), so each token row is handled by 4 threads in 4 warps; their per-row partial
+// sums and maxima meet in shared memory behind a 128-thread named barrier per quadrant.
 // Tensor memory (512 columns): [0,128) U = P S, [128,256) W = P K^T then Y = Z K,
 // [256,384) x, [384,512) r.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
+#include "tc_stage.cuh"
 
 namespace mesa {
 
 namespace {
 
-constexpr int TILE = 128;                 // tokens per chunk, rows of every MMA
-constexpr int DH = 128;                   // d_k = d_v
+using tc::DH;
+using tc::TILE;
+constexpr int NTHREADS = 512;
 constexpr uint32_t MAT_BYTES = TILE * DH * 2;  // one fp16 128x128 operand (32 KB)
 // shared-memory map (offsets from a 1024-aligned base)
 constexpr uint32_t OFF_SHI = 0, OFF_SLO = MAT_BYTES, OFF_K = 2 * MAT_BYTES,
@@ -37,147 +41,95 @@ constexpr uint32_t SMEM_TC = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
 constexpr uint32_t COL_U = 0, COL_W = 128, COL_X = 256, COL_R = 384;
 
 struct Misc {
-  float ell[TILE];
-  float lam[DH];
-  float red[4];
+  float ell2[TILE];  // log2-decays l_i * log2(e)
+  float lam[DH];     // Lambda diagonal of this head
+  float red[16];
   uint64_t mbar;
   uint32_t tmem_base;
-  int flag;
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc block too large");
 
-__device__ __forceinline__ float block_max(float v, Misc *m) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();  // previous readers of red[] are done
-  if ((threadIdx.x & 31) == 0) m->red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  return fmaxf(fmaxf(m->red[0], m->red[1]), fmaxf(m->red[2], m->red[3]));
+__device__ __forceinline__ void quad_bar(int q) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(1 + q), "r"(128) : "memory");
 }
 
-__device__ __forceinline__ void st_half(uint8_t *base, uint32_t off, __half h) {
-  *reinterpret_cast<__half *>(base + off) = h;
-}
-__device__ __forceinline__ float ld_pair(const uint8_t *hi, const uint8_t *lo, uint32_t off) {
-  return __half2float(*reinterpret_cast<const __half *>(hi + off)) +
-         __half2float(*reinterpret_cast<const __half *>(lo + off));
-}
-
-// Stage a fp32 128x128 matrix (row-major, or zero when src == nullptr) as scaled hi/lo fp16
-// operands.  Returns the scale s (operand = matrix * s).
-__device__ float stage_state(const float *src, uint8_t *hi, uint8_t *lo, Misc *m) {
-  const int t = threadIdx.x;
-  float mx = 0.0f;
-  if (src) {
-    for (int e = t * 4; e < TILE * DH; e += 4 * blockDim.x) {
-      const float4 x = *reinterpret_cast<const float4 *>(src + e);
-      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
-    }
-  }
-  const float s = 1.0f / tc::pow2_ceil(block_max(mx, m));
-  for (int e = t * 4; e < TILE * DH; e += 4 * blockDim.x) {
-    float4 x = src ? *reinterpret_cast<const float4 *>(src + e) : make_float4(0, 0, 0, 0);
-    const int r = e / DH, c = e % DH;
-    const float xs[4] = {x.x * s, x.y * s, x.z * s, x.w * s};
-#pragma unroll
-    for (int k = 0; k < 4; k++) {
-      __half h, l;
-      tc::split_f16(xs[k], h, l);
-      const uint32_t off = tc::sw128_offset(r, c + k, TILE);
-      st_half(hi, off, h);
-      st_half(lo, off, l);
-    }
-  }
-  return s;
+// Combine the 4 column groups' partials of each row.  `scr` is 2 KB of shared memory that
+// holds no live operand at the call.  With BLOCK the barriers span the whole CTA (needed
+// when other quadrants may overwrite the scratch right after their own reduction).
+template <bool MAX, bool BLOCK = false>
+__device__ __forceinline__ float rowred(float v, float *scr, int q, int g, int i) {
+  scr[g * TILE + i] = v;
+  if (BLOCK) __syncthreads(); else quad_bar(q);
+  const float a = scr[i], b = scr[TILE + i], c = scr[2 * TILE + i], d = scr[3 * TILE + i];
+  if (BLOCK) __syncthreads(); else quad_bar(q);
+  return MAX ? fmaxf(fmaxf(a, b), fmaxf(c, d)) : (a + b) + (c + d);
 }
 
-// Stage bf16 rows [0, Tv) of a chunk (rows >= Tv zero) as one scaled fp16 operand.
-__device__ float stage_rows(const __nv_bfloat16 *src, int Tv, uint8_t *dst, Misc *m) {
-  const int t = threadIdx.x;
-  float mx = 0.0f;
-  for (int e = t * 8; e < Tv * DH; e += 8 * blockDim.x) {
-    const uint4 raw = *reinterpret_cast<const uint4 *>(src + e);
-    const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+// 8 consecutive values (columns c0..c0+7 of row i) of a hi/lo operand, times mul.
+__device__ __forceinline__ void ld8(const uint8_t *hi, const uint8_t *lo, int i, int c0, float mul,
+                                    float (&o)[8]) {
+  const uint32_t off = tc::sw128_offset(i, c0, TILE);
+  const uint4 h = *reinterpret_cast<const uint4 *>(hi + off);
+  const uint4 l = *reinterpret_cast<const uint4 *>(lo + off);
+  const __half *hh = reinterpret_cast<const __half *>(&h);
+  const __half *ll = reinterpret_cast<const __half *>(&l);
 #pragma unroll
-    for (int k = 0; k < 8; k++) mx = fmaxf(mx, fabsf(__bfloat162float(b[k])));
-  }
-  const float s = 1.0f / tc::pow2_ceil(block_max(mx, m));
-  for (int e = t * 8; e < TILE * DH; e += 8 * blockDim.x) {
-    const int r = e / DH, c = e % DH;
-    uint4 raw = make_uint4(0, 0, 0, 0);
-    if (r < Tv) raw = *reinterpret_cast<const uint4 *>(src + e);
-    const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-    __align__(16) __half h[8];
-#pragma unroll
-    for (int k = 0; k < 8; k++) h[k] = __float2half_rn(__bfloat162float(b[k]) * s);
-    // 8 consecutive columns of one row stay one 16-byte chunk of the swizzled layout
-    *reinterpret_cast<uint4 *>(dst + tc::sw128_offset(r, c, TILE)) = *reinterpret_cast<uint4 *>(h);
-  }
-  return s;
+  for (int k = 0; k < 8; k++) o[k] = mul * (__half2float(hh[k]) + __half2float(ll[k]));
 }
 
-// Write one row (this thread's) of a scaled hi/lo operand from 128 values held in tensor
-// memory columns [col, col+128) of this thread's lane, multiplied by `mul`.
-__device__ __forceinline__ void row_to_operand(uint32_t tl, uint32_t col, float mul, float inv_scale,
-                                               uint8_t *hi, uint8_t *lo, int row) {
+__device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, const float (&x)[8],
+                                    float inv_scale) {
+  __align__(16) __half h[8], l[8];
 #pragma unroll
-  for (int cc = 0; cc < 4; cc++) {
-    float v[32];
-    tc::tmem_ld32(tl + col + cc * 32, v);
-    tc::tmem_ld_wait();
-#pragma unroll
-    for (int g = 0; g < 4; g++) {
-      __align__(16) __half h[8], l[8];
-#pragma unroll
-      for (int k = 0; k < 8; k++) tc::split_f16(v[g * 8 + k] * mul * inv_scale, h[k], l[k]);
-      const uint32_t off = tc::sw128_offset(row, cc * 32 + g * 8, TILE);
-      *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<uint4 *>(h);
-      *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<uint4 *>(l);
-    }
-  }
+  for (int k = 0; k < 8; k++) tc::split_f16(x[k] * inv_scale, h[k], l[k]);
+  const uint32_t off = tc::sw128_offset(i, c0, TILE);
+  *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<uint4 *>(h);
+  *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<uint4 *>(l);
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(NTHREADS, 1)
     mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, unsigned *status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t *Shi = sm + OFF_SHI, *Slo = sm + OFF_SLO, *Ks = sm + OFF_K;
   uint8_t *Phi = sm + OFF_PHI, *Plo = sm + OFF_PLO, *Zhi = sm + OFF_ZHI, *Zlo = sm + OFF_ZLO;
+  // row-reduction scratch: the first 2 KB of the Z operand, used only while Z is not live
+  float *scr = reinterpret_cast<float *>(Zhi);
   Misc *m = reinterpret_cast<Misc *>(sm + OFF_MISC);
   const uint32_t aShi = tc::smem_u32(Shi), aSlo = tc::smem_u32(Slo), aK = tc::smem_u32(Ks);
   const uint32_t aPhi = tc::smem_u32(Phi), aPlo = tc::smem_u32(Plo);
   const uint32_t aZhi = tc::smem_u32(Zhi), aZlo = tc::smem_u32(Zlo);
   const uint32_t aBar = tc::smem_u32(&m->mbar);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qd = warp & 3, grp = warp >> 2;  // lane quadrant, column group
+  const int i = 32 * qd + lane;               // token row of this thread
+  const int c0 = 32 * grp;                    // first column of this thread
   const int c = blockIdx.x, u = blockIdx.y;
   const int T = a.T;
   const int t0 = c * TILE;
   const int Tv = min(TILE, T - t0);
-  const int i = tid;  // token row
   const bool valid = i < Tv;
   const size_t tokbase = (size_t)u * T + t0;
   const __nv_bfloat16 *q = (const __nv_bfloat16 *)a.q;
   const __nv_bfloat16 *k = (const __nv_bfloat16 *)a.k;
   const __nv_bfloat16 *v = (const __nv_bfloat16 *)a.v;
+  constexpr float kLog2e = 1.4426950408889634f;
 
   // ---- set-up: tensor memory, barrier, per-chunk constants ----------------------------
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 512);
-  if (tid == 0) {
-    tc::mbar_init(aBar, 1);
-    m->flag = 0;
-  }
-  m->ell[tid] = valid ? ws.ell[tokbase + i] : 0.0f;
-  m->lam[tid] = a.lambda[(size_t)(u % a.H) * DH + tid];
+  if (tid == 0) tc::mbar_init(aBar, 1);
+  if (tid < TILE) m->ell2[tid] = (tid < Tv ? ws.ell[tokbase + tid] : 0.0f) * kLog2e;
+  if (tid >= 256 && tid < 256 + DH) m->lam[tid - 256] = a.lambda[(size_t)(u % a.H) * DH + tid - 256];
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tbase = m->tmem_base;
-  const uint32_t tl = tbase + ((uint32_t)(32 * warp) << 16);  // this warp's lane quadrant
-  const float ell_i = m->ell[i];
-  const float el_i = valid ? expf(ell_i) : 0.0f;
+  const uint32_t tl = tbase + ((uint32_t)(32 * qd) << 16) + c0;  // lane quadrant, column group
+  const float ell2_i = m->ell2[i];
+  const float el_i = valid ? exp2f(ell2_i) : 0.0f;
 
   const float *SH = nullptr, *SG = nullptr;
   if (c > 0) {
@@ -187,50 +139,43 @@ __global__ void __launch_bounds__(128, 1)
     SH = a.H0 + (size_t)u * DH * DH;
     SG = a.G0 + (size_t)u * DH * DH;
   }
-  const float sS = stage_state(SH, Shi, Slo, m);
-  const float sK = stage_rows(k + tokbase * DH, Tv, Ks, m);
+  const float sS = tc::stage_state(SH, Shi, Slo, m->red);
+  const float sK = tc::stage_rows(k + tokbase * DH, Tv, Ks, m->red);
 
-  // CG start: x = 0, r = p = q_i
+  // CG start: x = 0, r = p = q_i (this thread's 32 columns)
   float rho, nq, mP;
   {
-    float qa[DH];
-    const uint4 *src = reinterpret_cast<const uint4 *>(q + (tokbase + i) * DH);
+    float qa[32];
+    const uint4 *src = reinterpret_cast<const uint4 *>(q + (tokbase + i) * DH + c0);
 #pragma unroll
-    for (int g = 0; g < 16; g++) {
-      uint4 raw = valid ? src[g] : make_uint4(0, 0, 0, 0);
+    for (int g = 0; g < 4; g++) {
+      const uint4 raw = valid ? src[g] : make_uint4(0, 0, 0, 0);
       const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) qa[g * 8 + kk] = __bfloat162float(b[kk]);
     }
     float s = 0.0f, mx = 0.0f;
 #pragma unroll
-    for (int d = 0; d < DH; d++) {
+    for (int d = 0; d < 32; d++) {
       s = fmaf(qa[d], qa[d], s);
       mx = fmaxf(mx, fabsf(qa[d]));
     }
-    rho = s;
-    nq = sqrtf(s);
+    rho = rowred<false>(s, scr, qd, grp, i);
+    mx = rowred<true>(mx, scr, qd, grp, i);
+    nq = sqrtf(rho);
     mP = tc::pow2_ceil(mx);
+    float z[32];
+#pragma unroll
+    for (int kk = 0; kk < 32; kk++) z[kk] = 0.0f;
+    tc::tmem_st32(tl + COL_X, z);
+    tc::tmem_st32(tl + COL_R, qa);
     const float inv = 1.0f / mP;
 #pragma unroll
-    for (int cc = 0; cc < 4; cc++) {
-      float z[32], r[32];
+    for (int g = 0; g < 4; g++) {
+      float x8[8];
 #pragma unroll
-      for (int kk = 0; kk < 32; kk++) {
-        z[kk] = 0.0f;
-        r[kk] = qa[cc * 32 + kk];
-      }
-      tc::tmem_st32(tl + COL_X + cc * 32, z);
-      tc::tmem_st32(tl + COL_R + cc * 32, r);
-#pragma unroll
-      for (int g = 0; g < 4; g++) {
-        __align__(16) __half h[8], l[8];
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) tc::split_f16(r[g * 8 + kk] * inv, h[kk], l[kk]);
-        const uint32_t off = tc::sw128_offset(i, cc * 32 + g * 8, TILE);
-        *reinterpret_cast<uint4 *>(Phi + off) = *reinterpret_cast<uint4 *>(h);
-        *reinterpret_cast<uint4 *>(Plo + off) = *reinterpret_cast<uint4 *>(l);
-      }
+      for (int kk = 0; kk < 8; kk++) x8[kk] = qa[g * 8 + kk];
+      st8(Phi, Plo, i, c0 + 8 * g, x8, inv);
     }
     tc::tmem_st_wait();
   }
@@ -243,7 +188,7 @@ __global__ void __launch_bounds__(128, 1)
   const bool dynamic = a.cg_tol > 0.0f;
   bool failed = false;
 
-  // Issue helpers (one thread).  U (cols 0..127) = P S, W (cols 128..255) = P K^T.
+  // U (cols 0..127) = P S, W (cols 128..255) = P K^T; one thread issues.
   auto issue_state_and_keys = [&]() {
     const uint32_t dU = tbase + COL_U, dW = tbase + COL_W;
 #pragma unroll 1
@@ -252,10 +197,10 @@ __global__ void __launch_bounds__(128, 1)
       const uint64_t sh = tc::kmajor_desc(aShi, TILE, s), sl = tc::kmajor_desc(aSlo, TILE, s);
       const uint64_t kb = tc::kmajor_desc(aK, TILE, s);
       tc::mma_f16(dU, ph, sh, id_kk, s > 0);
-      tc::mma_f16(dU, ph, sl, id_kk, true);
-      tc::mma_f16(dU, pl, sh, id_kk, true);
       tc::mma_f16(dW, ph, kb, id_kk, s > 0);
+      tc::mma_f16(dU, ph, sl, id_kk, true);
       tc::mma_f16(dW, pl, kb, id_kk, true);
+      tc::mma_f16(dU, pl, sh, id_kk, true);
     }
     tc::mma_commit(aBar);
   };
@@ -279,27 +224,30 @@ __global__ void __launch_bounds__(128, 1)
     if (bad && tid == 0) atomicOr(status, tc::kErrMmaTimeout);
     return !bad;
   };
-  // Z = (W * m / sK) o D into the Z operand (row scale zs returned); W read from tensor memory.
+  // Z = (W * mrow / sK) o D into the Z operand; returns the row scale.
   auto build_z = [&](float mrow) -> float {
     const float f = mrow / sK;
+    float w[32];
+    tc::tmem_ld32(tl + COL_W, w);
+    tc::tmem_ld_wait();
     float zmax = 0.0f;
 #pragma unroll
-    for (int cc = 0; cc < 4; cc++) {
-      float w[32];
-      tc::tmem_ld32(tl + COL_W + cc * 32, w);
-      tc::tmem_ld_wait();
-#pragma unroll
-      for (int kk = 0; kk < 32; kk++) {
-        const int j = cc * 32 + kk;
-        const float dij = (valid && j <= i) ? expf(ell_i - m->ell[j]) : 0.0f;
-        w[kk] = w[kk] * f * dij;
-        zmax = fmaxf(zmax, fabsf(w[kk]));
-      }
-      tc::tmem_st32(tl + COL_W + cc * 32, w);
+    for (int kk = 0; kk < 32; kk++) {
+      const int j = c0 + kk;
+      const float dij = (valid && j <= i) ? exp2f(ell2_i - m->ell2[j]) : 0.0f;
+      w[kk] *= f * dij;
+      zmax = fmaxf(zmax, fabsf(w[kk]));
     }
-    tc::tmem_st_wait();
-    const float zs = tc::pow2_ceil(zmax);
-    row_to_operand(tl, COL_W, 1.0f, 1.0f / zs, Zhi, Zlo, i);
+    // the scratch lies inside the Z operand written next: block-wide barriers
+    const float zs = tc::pow2_ceil(rowred<true, true>(zmax, scr, qd, grp, i));
+    const float inv = 1.0f / zs;
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+      float x8[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) x8[kk] = w[g * 8 + kk];
+      st8(Zhi, Zlo, i, c0 + 8 * g, x8, inv);
+    }
     return zs;
   };
 
@@ -312,104 +260,110 @@ __global__ void __launch_bounds__(128, 1)
     tc::fence_after_sync();
     if (!any) break;
     if (tid == 0) issue_state_and_keys();
-    if (!wait_mma()) { failed = true; break; }
+    if (!wait_mma()) {
+      failed = true;
+      break;
+    }
     const float zs = build_z(mP);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) issue_intra();
-    if (!wait_mma()) { failed = true; break; }
+    if (!wait_mma()) {
+      failed = true;
+      break;
+    }
 
-    // AP = e^l (mP/sS) U + (zs/sK) Y + lambda p  -> U columns; sigma = p.AP
+    // AP = e^l (mP/sS) U + (zs/sK) Y + lambda p   (kept in registers); sigma = p.AP
     const float fu = el_i * mP / sS, fy = zs / sK;
-    float sigma = 0.0f;
-#pragma unroll
-    for (int cc = 0; cc < 4; cc++) {
-      float uu[32], yy[32];
-      tc::tmem_ld32(tl + COL_U + cc * 32, uu);
-      tc::tmem_ld32(tl + COL_W + cc * 32, yy);
+    float ap[32];
+    float sg = 0.0f;
+    {
+      float yy[32];
+      tc::tmem_ld32(tl + COL_U, ap);
+      tc::tmem_ld32(tl + COL_W, yy);
       tc::tmem_ld_wait();
 #pragma unroll
-      for (int kk = 0; kk < 32; kk++) {
-        const int d = cc * 32 + kk;
-        const float p = mP * ld_pair(Phi, Plo, tc::sw128_offset(i, d, TILE));
-        const float ap = fmaf(fu, uu[kk], fmaf(fy, yy[kk], m->lam[d] * p));
-        uu[kk] = ap;
-        sigma = fmaf(p, ap, sigma);
-      }
-      tc::tmem_st32(tl + COL_U + cc * 32, uu);
-    }
-    tc::tmem_st_wait();
-    const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
-    // x += alpha p, r -= alpha AP, rho' = r.r  (alpha = 0 leaves a finished row unchanged;
-    // tensor-memory accesses stay unconditional: they are warp-collective)
-    float rn = 0.0f, rmax = 0.0f;
+      for (int g = 0; g < 4; g++) {
+        float p8[8];
+        ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
 #pragma unroll
-    for (int cc = 0; cc < 4; cc++) {
-      float ap[32], xx[32], rr[32];
-      tc::tmem_ld32(tl + COL_U + cc * 32, ap);
-      tc::tmem_ld32(tl + COL_X + cc * 32, xx);
-      tc::tmem_ld32(tl + COL_R + cc * 32, rr);
-      tc::tmem_ld_wait();
-#pragma unroll
-      for (int kk = 0; kk < 32; kk++) {
-        const int d = cc * 32 + kk;
-        const float p = mP * ld_pair(Phi, Plo, tc::sw128_offset(i, d, TILE));
-        xx[kk] = fmaf(alpha, p, xx[kk]);
-        rr[kk] = fmaf(-alpha, ap[kk], rr[kk]);
-        rn = fmaf(rr[kk], rr[kk], rn);
-        rmax = fmaxf(rmax, fabsf(rr[kk]));
-      }
-      tc::tmem_st32(tl + COL_X + cc * 32, xx);
-      tc::tmem_st32(tl + COL_R + cc * 32, rr);
-    }
-    tc::tmem_st_wait();
-    const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
-    // p = r + beta p, re-scaled: |p_new| <= max|r| + beta max|p| <= rmax + beta mP
-    const float mNew = tc::pow2_ceil(rmax + beta * mP);
-    const float inv = 1.0f / mNew;
-#pragma unroll
-    for (int cc = 0; cc < 4; cc++) {
-      float rr[32];
-      tc::tmem_ld32(tl + COL_R + cc * 32, rr);
-      tc::tmem_ld_wait();
-      if (act) {
-#pragma unroll
-        for (int g = 0; g < 4; g++) {
-          __align__(16) __half h[8], l[8];
-          const uint32_t off = tc::sw128_offset(i, cc * 32 + g * 8, TILE);
-#pragma unroll
-          for (int kk = 0; kk < 8; kk++) {
-            const float pold = mP * ld_pair(Phi, Plo, off + 2 * kk);
-            tc::split_f16(fmaf(beta, pold, rr[g * 8 + kk]) * inv, h[kk], l[kk]);
-          }
-          *reinterpret_cast<uint4 *>(Phi + off) = *reinterpret_cast<uint4 *>(h);
-          *reinterpret_cast<uint4 *>(Plo + off) = *reinterpret_cast<uint4 *>(l);
+        for (int kk = 0; kk < 8; kk++) {
+          const int e = g * 8 + kk;
+          ap[e] = fmaf(fu, ap[e], fmaf(fy, yy[e], m->lam[c0 + e] * p8[kk]));
+          sg = fmaf(p8[kk], ap[e], sg);
         }
       }
     }
+    const float sigma = rowred<false>(sg, scr, qd, grp, i);
+    const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
+    // r -= alpha AP, x += alpha p   (alpha = 0 leaves a finished row unchanged; the
+    // tensor-memory accesses stay unconditional: they are warp-collective)
+    float rr[32];
+    float rn = 0.0f, rmax = 0.0f;
+    tc::tmem_ld32(tl + COL_R, rr);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int kk = 0; kk < 32; kk++) {
+      rr[kk] = fmaf(-alpha, ap[kk], rr[kk]);
+      rn = fmaf(rr[kk], rr[kk], rn);
+      rmax = fmaxf(rmax, fabsf(rr[kk]));
+    }
+    tc::tmem_st32(tl + COL_R, rr);
+    {
+      float xx[32];
+      tc::tmem_ld32(tl + COL_X, xx);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 4; g++) {
+        float p8[8];
+        ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) xx[g * 8 + kk] = fmaf(alpha, p8[kk], xx[g * 8 + kk]);
+      }
+      tc::tmem_st32(tl + COL_X, xx);
+    }
+    rn = rowred<false>(rn, scr, qd, grp, i);
+    rmax = rowred<true>(rmax, scr, qd, grp, i);
+    const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
+    // p = r + beta p, re-scaled: |p_new| <= max|r| + beta max|p| <= rmax + beta mP
     if (act) {
+      const float mNew = tc::pow2_ceil(rmax + beta * mP);
+      const float inv = 1.0f / mNew;
+#pragma unroll
+      for (int g = 0; g < 4; g++) {
+        float p8[8];
+        ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) p8[kk] = fmaf(beta, p8[kk], rr[g * 8 + kk]);
+        st8(Phi, Plo, i, c0 + 8 * g, p8, inv);
+      }
       mP = mNew;
       rho = rn;
       cnt++;
     }
+    tc::tmem_st_wait();
   }
 
   // ---- readout O = e^l X S^G^T + ((X K^T) o D) V ------------------------------------------
   if (!failed) {
+    float xx[32];
+    tc::tmem_ld32(tl + COL_X, xx);
+    tc::tmem_ld_wait();
     float mx = 0.0f;
 #pragma unroll
-    for (int cc = 0; cc < 4; cc++) {
-      float xx[32];
-      tc::tmem_ld32(tl + COL_X + cc * 32, xx);
-      tc::tmem_ld_wait();
+    for (int kk = 0; kk < 32; kk++) mx = fmaxf(mx, fabsf(xx[kk]));
+    const float mX = tc::pow2_ceil(rowred<true>(mx, scr, qd, grp, i));
+    const float inv = 1.0f / mX;
 #pragma unroll
-      for (int kk = 0; kk < 32; kk++) mx = fmaxf(mx, fabsf(xx[kk]));
+    for (int g = 0; g < 4; g++) {
+      float x8[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) x8[kk] = xx[g * 8 + kk];
+      st8(Phi, Plo, i, c0 + 8 * g, x8, inv);
     }
-    const float mX = tc::pow2_ceil(mx);
-    row_to_operand(tl, COL_X, 1.0f, 1.0f / mX, Phi, Plo, i);
-    const float sG = stage_state(SG, Shi, Slo, m);
+    const float sG = tc::stage_state(SG, Shi, Slo, m->red);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -418,8 +372,7 @@ __global__ void __launch_bounds__(128, 1)
     failed = !wait_mma();
     if (!failed) {
       const float zs = build_z(mX);
-      __syncthreads();  // every thread is done reading the keys' operand through W
-      const float sV = stage_rows(v + tokbase * DH, Tv, Ks, m);
+      const float sV = tc::stage_rows(v + tokbase * DH, Tv, Ks, m->red);
       tc::fence_smem_to_async();
       tc::fence_before_sync();
       __syncthreads();
@@ -428,25 +381,22 @@ __global__ void __launch_bounds__(128, 1)
       failed = !wait_mma();
       if (!failed) {
         const float fu = el_i * mX / sG, fy = zs / sV;
-        __nv_bfloat16 *out = (__nv_bfloat16 *)a.out + (tokbase + i) * DH;
+        float uu[32], yy[32];
+        tc::tmem_ld32(tl + COL_U, uu);
+        tc::tmem_ld32(tl + COL_W, yy);
+        tc::tmem_ld_wait();
+        if (valid) {
+          __nv_bfloat16 *out = (__nv_bfloat16 *)a.out + (tokbase + i) * DH + c0;
 #pragma unroll
-        for (int cc = 0; cc < 4; cc++) {
-          float uu[32], yy[32];
-          tc::tmem_ld32(tl + COL_U + cc * 32, uu);
-          tc::tmem_ld32(tl + COL_W + cc * 32, yy);
-          tc::tmem_ld_wait();
-          if (valid) {
+          for (int g = 0; g < 4; g++) {
+            __align__(16) __nv_bfloat16 o8[8];
 #pragma unroll
-            for (int g = 0; g < 4; g++) {
-              __align__(16) __nv_bfloat16 o8[8];
-#pragma unroll
-              for (int kk = 0; kk < 8; kk++)
-                o8[kk] = __float2bfloat16_rn(fmaf(fu, uu[g * 8 + kk], fy * yy[g * 8 + kk]));
-              *reinterpret_cast<uint4 *>(out + cc * 32 + g * 8) = *reinterpret_cast<uint4 *>(o8);
-            }
+            for (int kk = 0; kk < 8; kk++)
+              o8[kk] = __float2bfloat16_rn(fmaf(fu, uu[g * 8 + kk], fy * yy[g * 8 + kk]));
+            *reinterpret_cast<uint4 *>(out + 8 * g) = *reinterpret_cast<uint4 *>(o8);
           }
+          if (grp == 0 && a.iters) a.iters[tokbase + i] = cnt;
         }
-        if (valid && a.iters) a.iters[tokbase + i] = cnt;
       }
     }
   }
@@ -464,7 +414,7 @@ int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *statu
                            (int)SMEM_TC) != cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_TC, st);
-  mesa_cg_tc_kernel<<<dim3(NC, U), 128, SMEM_TC, st>>>(a, ws, NC, status);
+  mesa_cg_tc_kernel<<<dim3(NC, U), NTHREADS, SMEM_TC, st>>>(a, ws, NC, status);
   timing_mark_end(K_CG_TC, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

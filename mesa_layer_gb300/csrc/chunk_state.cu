@@ -114,20 +114,26 @@ __global__ void __launch_bounds__(256) mesa_scan_kernel(const float *__restrict_
 }
 
 template <int D, typename TIO>
-static int launch_states_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+static int launch_states_t(const FwdArgs &a, const FwdWorkspace &ws, unsigned *tc_status,
+                           cudaStream_t st) {
   const int U = a.B * a.H;
   const int NC = (a.T + a.chunk - 1) / a.chunk;
   timing_mark_begin(K_ELL, st);
   mesa_ell_kernel<<<dim3(NC, U), 128, 0, st>>>(a.gamma, ws.ell, a.T, a.chunk);
   timing_mark_end(K_ELL, st);
-  const size_t smem = (size_t)(256 * D + 128) * sizeof(float);
-  auto kd = mesa_delta_kernel<D, TIO>;
-  if (cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return -1;
-  timing_mark_begin(K_DELTA, st);
-  kd<<<dim3(NC, U, 2), 256, smem, st>>>((const TIO *)a.k, (const TIO *)a.v, ws.ell, ws, a.T,
-                                        a.chunk);
-  timing_mark_end(K_DELTA, st);
+  if (tc_status) {
+    if (launch_delta_tc(a, ws, tc_status, st) != 0) return -1;
+  } else {
+    const size_t smem = (size_t)(256 * D + 128) * sizeof(float);
+    auto kd = mesa_delta_kernel<D, TIO>;
+    if (cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return -1;
+    timing_mark_begin(K_DELTA, st);
+    kd<<<dim3(NC, U, 2), 256, smem, st>>>((const TIO *)a.k, (const TIO *)a.v, ws.ell, ws, a.T,
+                                          a.chunk);
+    timing_mark_end(K_DELTA, st);
+  }
   timing_mark_begin(K_SCAN, st);
   mesa_scan_kernel<D><<<dim3((2 * D * D + 255) / 256, U), 256, 0, st>>>(
       ws.ell, ws, a.H0, a.G0, a.H_final, a.G_final, a.T, a.chunk, NC);
@@ -135,13 +141,14 @@ static int launch_states_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
-int launch_chunk_states(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+int launch_chunk_states(const FwdArgs &a, const FwdWorkspace &ws, unsigned *tc_status,
+                        cudaStream_t st) {
   const bool bf = a.dtype == 1;
   switch (a.dk) {
-    case 16: return bf ? launch_states_t<16, __nv_bfloat16>(a, ws, st) : launch_states_t<16, float>(a, ws, st);
-    case 32: return bf ? launch_states_t<32, __nv_bfloat16>(a, ws, st) : launch_states_t<32, float>(a, ws, st);
-    case 64: return bf ? launch_states_t<64, __nv_bfloat16>(a, ws, st) : launch_states_t<64, float>(a, ws, st);
-    case 128: return bf ? launch_states_t<128, __nv_bfloat16>(a, ws, st) : launch_states_t<128, float>(a, ws, st);
+    case 16: return bf ? launch_states_t<16, __nv_bfloat16>(a, ws, nullptr, st) : launch_states_t<16, float>(a, ws, nullptr, st);
+    case 32: return bf ? launch_states_t<32, __nv_bfloat16>(a, ws, nullptr, st) : launch_states_t<32, float>(a, ws, nullptr, st);
+    case 64: return bf ? launch_states_t<64, __nv_bfloat16>(a, ws, nullptr, st) : launch_states_t<64, float>(a, ws, nullptr, st);
+    case 128: return bf ? launch_states_t<128, __nv_bfloat16>(a, ws, tc_status, st) : launch_states_t<128, float>(a, ws, nullptr, st);
   }
   return -1;
 }

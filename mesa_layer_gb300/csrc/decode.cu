@@ -156,10 +156,165 @@ __global__ void __launch_bounds__(4 * D) mesa_decode_kernel(DecArgs a) {
   if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
 }
 
+
+// d = 128 specialisation.  Same update, CG rule and readout; differences:
+//  - 8 rows x 128 columns per warp, one float4 of each row per lane (H in 32 registers),
+//    and row sums by a shuffle reduce-scatter (9 shuffles for the 8 rows instead of 40):
+//    after it, row 8w + (lane >> 2) is held, replicated, by the 4 lanes of that group, which
+//    also hold that row's x, r, p and lambda;
+//  - G is copied to shared memory with cp.async at the start (it is needed only for the
+//    readout), so its HBM read overlaps the CG;
+//  - at most 64 registers per thread, so two units run on one SM and one unit's HBM
+//    traffic overlaps the other's CG.
+template <typename TIO>
+__global__ void __launch_bounds__(512, 2) mesa_decode128_kernel(DecArgs a) {
+  constexpr int D = 128, NW = 16;
+  const int u = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = 8 * warp + (lane >> 2);  // the row this lane's group holds after reduce
+  extern __shared__ __align__(16) float dsm[];
+  float *Gs = dsm;                         // [128][128]
+  float *kvec = Gs + D * D, *vvec = kvec + D, *pvec = vvec + D;
+  float *red = pvec + D;                   // [2][NW]
+
+  const float4 *Hg = reinterpret_cast<const float4 *>(a.Hs + (size_t)u * D * D);
+  float4 *Hw = reinterpret_cast<float4 *>(a.Hs + (size_t)u * D * D);
+  float4 *Gw = reinterpret_cast<float4 *>(a.Gs + (size_t)u * D * D);
+  // G -> shared memory, asynchronously (8 x 16 bytes per thread)
+  {
+    const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(Gs);
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      const int e = threadIdx.x + 512 * k;  // float4 index
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sbase + 16 * e),
+                   "l"(reinterpret_cast<const float4 *>(a.Gs + (size_t)u * D * D) + e)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  }
+  float4 h[8];
+#pragma unroll
+  for (int j = 0; j < 8; j++) h[j] = Hg[(8 * warp + j) * 32 + lane];
+  const TIO *q = (const TIO *)a.q, *k = (const TIO *)a.k, *v = (const TIO *)a.v;
+  if (threadIdx.x < D) {
+    kvec[threadIdx.x] = ld(k, (size_t)u * D + threadIdx.x);
+    vvec[threadIdx.x] = ld(v, (size_t)u * D + threadIdx.x);
+    pvec[threadIdx.x] = ld(q, (size_t)u * D + threadIdx.x);
+  }
+  const float g = a.gamma[u];
+  const float lam_r = a.lambda[(size_t)(u % a.H) * D + row];
+  __syncthreads();
+
+  const float4 kc = reinterpret_cast<const float4 *>(kvec)[lane];
+#pragma unroll
+  for (int j = 0; j < 8; j++) {
+    const float kr = kvec[8 * warp + j];
+    h[j].x = fmaf(g, h[j].x, kr * kc.x);
+    h[j].y = fmaf(g, h[j].y, kr * kc.y);
+    h[j].z = fmaf(g, h[j].z, kr * kc.z);
+    h[j].w = fmaf(g, h[j].w, kr * kc.w);
+    Hw[(8 * warp + j) * 32 + lane] = h[j];
+  }
+
+  // reduce-scatter of s[0..7] over the 32 lanes: returns the full sum of row lane >> 2
+  auto rowsum = [&](float (&s)[8]) -> float {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float t4[4], t2[2];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const float send = b4 ? s[j] : s[j + 4];
+      t4[j] = (b4 ? s[j + 4] : s[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; j++) {
+      const float send = b3 ? t4[j] : t4[j + 2];
+      t2[j] = (b3 ? t4[j + 2] : t4[j]) + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float t = (b2 ? t2[1] : t2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? t2[0] : t2[1], 4);
+    t += __shfl_xor_sync(0xffffffffu, t, 2);
+    t += __shfl_xor_sync(0xffffffffu, t, 1);
+    return t;
+  };
+  // sum over the warp's 8 rows of a value replicated in each 4-lane group, then over warps
+  auto block_rows_sum = [&](float val, int buf) -> float {
+    val += __shfl_xor_sync(0xffffffffu, val, 4);
+    val += __shfl_xor_sync(0xffffffffu, val, 8);
+    val += __shfl_xor_sync(0xffffffffu, val, 16);
+    if (lane == 0) red[buf * NW + warp] = val;
+    __syncthreads();
+    const float4 *r4 = reinterpret_cast<const float4 *>(red + buf * NW);
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NW / 4; k++) {
+      const float4 x = r4[k];
+      s += (x.x + x.y) + (x.z + x.w);
+    }
+    return s;
+  };
+
+  float xr = 0.0f, rr = pvec[row], pr = rr;
+  float rho = block_rows_sum(rr * rr, 0);
+  const float nq = sqrtf(rho);
+  const bool dynamic = a.cg_tol > 0.0f;
+  int it = 0;
+  for (; it < a.cg_iters; it++) {
+    if (dynamic && sqrtf(rho) <= a.cg_tol * nq) break;
+    const float4 pc = reinterpret_cast<const float4 *>(pvec)[lane];
+    float s[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++)
+      s[j] = fmaf(h[j].w, pc.w, fmaf(h[j].z, pc.z, fmaf(h[j].y, pc.y, h[j].x * pc.x)));
+    const float w = fmaf(lam_r, pr, rowsum(s));
+    const float sigma = block_rows_sum(pr * w, 1);
+    const float alpha = (sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
+    xr = fmaf(alpha, pr, xr);
+    rr = fmaf(-alpha, w, rr);
+    const float rn = block_rows_sum(rr * rr, 0);
+    const float beta = rho > 0.0f ? rn / rho : 0.0f;
+    pr = fmaf(beta, pr, rr);
+    if ((lane & 3) == 0) pvec[row] = pr;
+    rho = rn;
+    __syncthreads();
+  }
+
+  // readout: G <- gamma G + v k^T (from the shared copy), o = G x
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  __syncthreads();
+  if ((lane & 3) == 0) pvec[row] = xr;
+  __syncthreads();
+  const float4 xc = reinterpret_cast<const float4 *>(pvec)[lane];
+  float s[8];
+#pragma unroll
+  for (int j = 0; j < 8; j++) {
+    const int rj = 8 * warp + j;
+    float4 gg = reinterpret_cast<const float4 *>(Gs)[rj * 32 + lane];
+    const float vr = vvec[rj];
+    gg.x = fmaf(g, gg.x, vr * kc.x);
+    gg.y = fmaf(g, gg.y, vr * kc.y);
+    gg.z = fmaf(g, gg.z, vr * kc.z);
+    gg.w = fmaf(g, gg.w, vr * kc.w);
+    Gw[rj * 32 + lane] = gg;
+    s[j] = fmaf(gg.w, xc.w, fmaf(gg.z, xc.z, fmaf(gg.y, xc.y, gg.x * xc.x)));
+  }
+  const float o = rowsum(s);
+  if ((lane & 3) == 0) st((TIO *)a.out, (size_t)u * D + row, o);
+  if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
+}
+
+constexpr int kDecode128Smem = (128 * 128 + 3 * 128 + 2 * 16) * sizeof(float);
+
 template <int D, typename TIO>
 static int launch_dec_t(const DecArgs &a, cudaStream_t st) {
   timing_mark_begin(K_DECODE, st);
-  mesa_decode_kernel<D, TIO><<<a.N * a.H, 4 * D, 0, st>>>(a);
+  if constexpr (D == 128) {
+    auto kfn = mesa_decode128_kernel<TIO>;
+    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecode128Smem) !=
+        cudaSuccess)
+      return -1;
+    kfn<<<a.N * a.H, 512, kDecode128Smem, st>>>(a);
+  } else {
+    mesa_decode_kernel<D, TIO><<<a.N * a.H, 4 * D, 0, st>>>(a);
+  }
   timing_mark_end(K_DECODE, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

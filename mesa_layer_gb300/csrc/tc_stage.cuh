@@ -1,0 +1,144 @@
+// tc_stage.cuh -- staging of operands for the tensor-core kernels: 128 x 128 tiles in
+// the 128-byte-swizzled fp16 layout (see tc_common.cuh), scaled by powers of two and, where
+// fp32 accuracy is needed, split into hi + lo fp16 terms.  Every function is called by all
+// threads of the CTA (block-wide maxima use __syncthreads).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "tc_common.cuh"
+
+namespace mesa {
+namespace tc {
+
+constexpr int TILE = 128;  // rows of every operand tile (tokens or state rows)
+constexpr int DH = 128;    // columns (d_k = d_v)
+
+// Block-wide max; red holds one float per warp (up to 16 warps).
+__device__ __forceinline__ float block_max(float v, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();  // previous readers of red[] are done
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float m = red[0];
+  const int nw = blockDim.x >> 5;
+  for (int w = 1; w < nw; w++) m = fmaxf(m, red[w]);
+  return m;
+}
+
+__device__ __forceinline__ void st_half(uint8_t *base, uint32_t off, __half h) {
+  *reinterpret_cast<__half *>(base + off) = h;
+}
+__device__ __forceinline__ float ld_pair(const uint8_t *hi, const uint8_t *lo, uint32_t off) {
+  return __half2float(*reinterpret_cast<const __half *>(hi + off)) +
+         __half2float(*reinterpret_cast<const __half *>(lo + off));
+}
+
+// Stage a fp32 128x128 matrix (row-major, or zero when src == nullptr) as scaled hi/lo fp16
+// operands.  Returns the scale s (operand = matrix * s).
+__device__ __forceinline__ float stage_state(const float *src, uint8_t *hi, uint8_t *lo, float *red) {
+  const int t = threadIdx.x;
+  float mx = 0.0f;
+  if (src) {
+    for (int e = t * 4; e < TILE * DH; e += 4 * blockDim.x) {
+      const float4 x = *reinterpret_cast<const float4 *>(src + e);
+      mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+    }
+  }
+  const float s = 1.0f / pow2_ceil(block_max(mx, red));
+  for (int e = t * 4; e < TILE * DH; e += 4 * blockDim.x) {
+    float4 x = src ? *reinterpret_cast<const float4 *>(src + e) : make_float4(0, 0, 0, 0);
+    const int r = e / DH, c = e % DH;
+    const float xs[4] = {x.x * s, x.y * s, x.z * s, x.w * s};
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      __half h, l;
+      split_f16(xs[k], h, l);
+      const uint32_t off = sw128_offset(r, c + k, TILE);
+      st_half(hi, off, h);
+      st_half(lo, off, l);
+    }
+  }
+  return s;
+}
+
+// Stage bf16 rows [0, Tv) of a chunk (rows >= Tv zero) as one scaled fp16 operand.
+__device__ __forceinline__ float stage_rows(const __nv_bfloat16 *src, int Tv, uint8_t *dst, float *red) {
+  const int t = threadIdx.x;
+  float mx = 0.0f;
+  for (int e = t * 8; e < Tv * DH; e += 8 * blockDim.x) {
+    const uint4 raw = *reinterpret_cast<const uint4 *>(src + e);
+    const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+#pragma unroll
+    for (int k = 0; k < 8; k++) mx = fmaxf(mx, fabsf(__bfloat162float(b[k])));
+  }
+  const float s = 1.0f / pow2_ceil(block_max(mx, red));
+  for (int e = t * 8; e < TILE * DH; e += 8 * blockDim.x) {
+    const int r = e / DH, c = e % DH;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (r < Tv) raw = *reinterpret_cast<const uint4 *>(src + e);
+    const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+    __align__(16) __half h[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) h[k] = __float2half_rn(__bfloat162float(b[k]) * s);
+    // 8 consecutive columns of one row stay one 16-byte chunk of the swizzled layout
+    *reinterpret_cast<uint4 *>(dst + sw128_offset(r, c, TILE)) = *reinterpret_cast<uint4 *>(h);
+  }
+  return s;
+}
+
+// Write one row (this thread's) of a scaled hi/lo operand from 128 values held in tensor
+// memory columns [col, col+128) of this thread's lane, multiplied by `mul`.
+__device__ __forceinline__ void row_to_operand(uint32_t tl, uint32_t col, float mul, float inv_scale,
+                                               uint8_t *hi, uint8_t *lo, int row) {
+#pragma unroll
+  for (int cc = 0; cc < 4; cc++) {
+    float v[32];
+    tmem_ld32(tl + col + cc * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+      __align__(16) __half h[8], l[8];
+#pragma unroll
+      for (int k = 0; k < 8; k++) split_f16(v[g * 8 + k] * mul * inv_scale, h[k], l[k]);
+      const uint32_t off = sw128_offset(row, cc * 32 + g * 8, TILE);
+      *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<uint4 *>(h);
+      *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<uint4 *>(l);
+    }
+  }
+}
+
+
+// Stage w_j * x_j (bf16 rows x_j, j < Tv; fp32 weights w in shared memory) as hi/lo fp16
+// operands of the tile (row j, column a).  Returns the scale s (operand = w x * s).
+__device__ __forceinline__ float stage_weighted_rows(const __nv_bfloat16 *src, const float *w, int Tv,
+                                                     uint8_t *hi, uint8_t *lo, float *red) {
+  const int t = threadIdx.x;
+  float mx = 0.0f;
+  for (int e = t * 8; e < Tv * DH; e += 8 * blockDim.x) {
+    const uint4 raw = *reinterpret_cast<const uint4 *>(src + e);
+    const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+    const float wj = w[e / DH];
+#pragma unroll
+    for (int k = 0; k < 8; k++) mx = fmaxf(mx, fabsf(wj * __bfloat162float(b[k])));
+  }
+  const float s = 1.0f / pow2_ceil(block_max(mx, red));
+  for (int e = t * 8; e < TILE * DH; e += 8 * blockDim.x) {
+    const int r = e / DH, c = e % DH;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (r < Tv) raw = *reinterpret_cast<const uint4 *>(src + e);
+    const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+    const float ws = (r < Tv ? w[r] : 0.0f) * s;
+    __align__(16) __half h[8], l[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) split_f16(__bfloat162float(b[k]) * ws, h[k], l[k]);
+    const uint32_t off = sw128_offset(r, c, TILE);
+    *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<uint4 *>(h);
+    *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<uint4 *>(l);
+  }
+  return s;
+}
+
+}  // namespace tc
+}  // namespace mesa

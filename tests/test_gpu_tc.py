@@ -29,13 +29,14 @@ def test_tc_selftest_matches_fp16_products():
     B = rng.standard_normal((128, 128)).astype(np.float32)
     A[3, :] = 0.0
     B[:, 7] *= 1e-3
-    C1, C2, st = binding.mesa_tc_selftest(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda())
+    C1, C2, C3, st = binding.mesa_tc_selftest(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda())
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     a16 = A.astype(np.float16).astype(np.float64)
     b16 = B.astype(np.float16).astype(np.float64)
     np.testing.assert_allclose(C1.cpu().numpy(), a16 @ b16.T, rtol=1e-5, atol=1e-4)
     np.testing.assert_allclose(C2.cpu().numpy(), a16 @ b16, rtol=1e-5, atol=1e-4)
+    np.testing.assert_allclose(C3.cpu().numpy(), a16.T @ b16, rtol=1e-5, atol=1e-4)
 
 
 TC_CASES = [
