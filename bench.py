@@ -78,6 +78,18 @@ def cg_flops(w, iters: np.ndarray) -> float:
     return float((iters.astype(np.float64) + 1.0).sum() * per)
 
 
+def tc_executed_flops(w, iters: np.ndarray) -> float:
+    """MMA flops the tensor-core CG kernel issues: per 128-token chunk and iteration 7
+    products of 128x128x128 (3 for the split state product, 2 + 2 for the key products);
+    iterations run until the slowest token of the chunk stops, plus the readout."""
+    B, H, T = iters.shape
+    nc = (T + 127) // 128
+    pad = np.zeros((B, H, nc * 128), dtype=np.int64)
+    pad[:, :, :T] = iters
+    per_chunk = pad.reshape(B, H, nc, 128).max(axis=-1) + 1
+    return float(per_chunk.sum()) * 7 * 2.0 * 128 ** 3
+
+
 def state_flops(w) -> float:
     """Chunk-local state sums: 2 d^2 multiply-adds per token for H and for G."""
     return float(w.B * w.H * w.T) * 4.0 * w.dk * w.dk
@@ -477,15 +489,20 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
                 "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": top_name,
                 "peak_source": peaks["source"]}
     else:
-        if "cg" in top_name:
-            flops = cg_flops(w, it)
-        else:
-            flops = state_flops(w)
+        flops = cg_flops(w, it) if "cg" in top_name else state_flops(w)
         achieved = flops / (avg_ms / 1e3) / 1e12
-        peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
-        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": None, "kernel": top_name,
-                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock"}
+        if "_tc_" in top_name:
+            # fp16 tcgen05 MMAs run at the bf16 dense rate; the measured cuBLAS bf16 peak
+            peak = peaks["bf16_tflops"]
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": None, "kernel": top_name,
+                    "peak_source": f"{peaks['source']} bf16 dense (fp16 kind, same rate)",
+                    "executed_tensor_tflops": tc_executed_flops(w, it) / (avg_ms / 1e3) / 1e12}
+        else:
+            peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+            roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": None, "kernel": top_name,
+                    "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock"}
     kernels = {names[i] if i < len(names) else f"kind{i}": {"ms_per_step": kind_ms[i] / args.steps,
                                                              "launches": kind_n[i]}
                for i in range(len(kind_ms)) if kind_n[i] > 0}

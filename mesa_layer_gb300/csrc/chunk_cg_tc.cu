@@ -42,6 +42,7 @@ constexpr uint32_t COL_U = 0, COL_W = 128, COL_X = 256, COL_R = 384;
 
 struct Misc {
   float ell2[TILE];  // log2-decays l_i * log2(e)
+  float e2c[TILE];   // 2^{-l2_j} (used when the chunk's decays fit fp32 as factors)
   float lam[DH];     // Lambda diagonal of this head
   float red[16];
   uint64_t mbar;
@@ -65,23 +66,43 @@ __device__ __forceinline__ float rowred(float v, float *scr, int q, int g, int i
   return MAX ? fmaxf(fmaxf(a, b), fmaxf(c, d)) : (a + b) + (c + d);
 }
 
+// Two-value variant (a sum and a max) sharing the barriers; scratch 4 KB.
+__device__ __forceinline__ void rowred2(float &sum, float &mx, float *scr, int q, int g, int i) {
+  scr[g * TILE + i] = sum;
+  scr[4 * TILE + g * TILE + i] = mx;
+  quad_bar(q);
+  sum = (scr[i] + scr[TILE + i]) + (scr[2 * TILE + i] + scr[3 * TILE + i]);
+  mx = fmaxf(fmaxf(scr[4 * TILE + i], scr[5 * TILE + i]), fmaxf(scr[6 * TILE + i], scr[7 * TILE + i]));
+  quad_bar(q);
+}
+
 // 8 consecutive values (columns c0..c0+7 of row i) of a hi/lo operand, times mul.
 __device__ __forceinline__ void ld8(const uint8_t *hi, const uint8_t *lo, int i, int c0, float mul,
                                     float (&o)[8]) {
   const uint32_t off = tc::sw128_offset(i, c0, TILE);
   const uint4 h = *reinterpret_cast<const uint4 *>(hi + off);
   const uint4 l = *reinterpret_cast<const uint4 *>(lo + off);
-  const __half *hh = reinterpret_cast<const __half *>(&h);
-  const __half *ll = reinterpret_cast<const __half *>(&l);
+  const __half2 *hh = reinterpret_cast<const __half2 *>(&h);
+  const __half2 *ll = reinterpret_cast<const __half2 *>(&l);
 #pragma unroll
-  for (int k = 0; k < 8; k++) o[k] = mul * (__half2float(hh[k]) + __half2float(ll[k]));
+  for (int k = 0; k < 4; k++) {
+    const float2 a = __half22float2(hh[k]), b = __half22float2(ll[k]);
+    o[2 * k] = mul * (a.x + b.x);
+    o[2 * k + 1] = mul * (a.y + b.y);
+  }
 }
 
+// x * inv_scale = hi + lo (fp16 pairs, packed conversions), stored at row i, cols c0..c0+7.
 __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, const float (&x)[8],
                                     float inv_scale) {
-  __align__(16) __half h[8], l[8];
+  __align__(16) __half2 h[4], l[4];
 #pragma unroll
-  for (int k = 0; k < 8; k++) tc::split_f16(x[k] * inv_scale, h[k], l[k]);
+  for (int k = 0; k < 4; k++) {
+    const float a = x[2 * k] * inv_scale, b = x[2 * k + 1] * inv_scale;
+    h[k] = __floats2half2_rn(a, b);
+    const float2 back = __half22float2(h[k]);
+    l[k] = __floats2half2_rn(a - back.x, b - back.y);
+  }
   const uint32_t off = tc::sw128_offset(i, c0, TILE);
   *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<uint4 *>(h);
   *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<uint4 *>(l);
@@ -121,15 +142,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // ---- set-up: tensor memory, barrier, per-chunk constants ----------------------------
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 512);
   if (tid == 0) tc::mbar_init(aBar, 1);
-  if (tid < TILE) m->ell2[tid] = (tid < Tv ? ws.ell[tokbase + tid] : 0.0f) * kLog2e;
+  bool small = true;  // |l2| <= 100: D_ij = 2^{l2_i} 2^{-l2_j} without overflow
+  if (tid < TILE) {
+    const float l2 = (tid < Tv ? ws.ell[tokbase + tid] : 0.0f) * kLog2e;
+    m->ell2[tid] = l2;
+    m->e2c[tid] = tid < Tv ? exp2f(-l2) : 0.0f;
+    small = fabsf(l2) <= 100.0f;
+  }
   if (tid >= 256 && tid < 256 + DH) m->lam[tid - 256] = a.lambda[(size_t)(u % a.H) * DH + tid - 256];
   tc::fence_before_sync();
-  __syncthreads();
+  const bool factored = __syncthreads_and(small ? 1 : 0);
   tc::fence_after_sync();
   const uint32_t tbase = m->tmem_base;
   const uint32_t tl = tbase + ((uint32_t)(32 * qd) << 16) + c0;  // lane quadrant, column group
   const float ell2_i = m->ell2[i];
   const float el_i = valid ? exp2f(ell2_i) : 0.0f;
+  const float e2r_i = valid ? el_i : 0.0f;  // 2^{l2_i}; invalid rows get D = 0
 
   const float *SH = nullptr, *SG = nullptr;
   if (c > 0) {
@@ -160,8 +188,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       s = fmaf(qa[d], qa[d], s);
       mx = fmaxf(mx, fabsf(qa[d]));
     }
-    rho = rowred<false>(s, scr, qd, grp, i);
-    mx = rowred<true>(mx, scr, qd, grp, i);
+    rowred2(s, mx, scr, qd, grp, i);
+    rho = s;
     nq = sqrtf(rho);
     mP = tc::pow2_ceil(mx);
     float z[32];
@@ -188,21 +216,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const bool dynamic = a.cg_tol > 0.0f;
   bool failed = false;
 
-  // U (cols 0..127) = P S, W (cols 128..255) = P K^T; one thread issues.
-  auto issue_state_and_keys = [&]() {
+  // W (cols 128..255) = P K^T, committed to the barrier, then U (cols 0..127) = P S, which
+  // runs on the tensor pipe while the threads build Z from W.  U needs no commit of its own:
+  // the next commit (after Z K) completes only when every earlier MMA has completed.
+  // One thread issues.
+  auto issue_keys_then_state = [&]() {
     const uint32_t dU = tbase + COL_U, dW = tbase + COL_W;
+#pragma unroll 1
+    for (int s = 0; s < 8; s++) {
+      const uint64_t kb = tc::kmajor_desc(aK, TILE, s);
+      tc::mma_f16(dW, tc::kmajor_desc(aPhi, TILE, s), kb, id_kk, s > 0);
+      tc::mma_f16(dW, tc::kmajor_desc(aPlo, TILE, s), kb, id_kk, true);
+    }
+    tc::mma_commit(aBar);
 #pragma unroll 1
     for (int s = 0; s < 8; s++) {
       const uint64_t ph = tc::kmajor_desc(aPhi, TILE, s), pl = tc::kmajor_desc(aPlo, TILE, s);
       const uint64_t sh = tc::kmajor_desc(aShi, TILE, s), sl = tc::kmajor_desc(aSlo, TILE, s);
-      const uint64_t kb = tc::kmajor_desc(aK, TILE, s);
       tc::mma_f16(dU, ph, sh, id_kk, s > 0);
-      tc::mma_f16(dW, ph, kb, id_kk, s > 0);
       tc::mma_f16(dU, ph, sl, id_kk, true);
-      tc::mma_f16(dW, pl, kb, id_kk, true);
       tc::mma_f16(dU, pl, sh, id_kk, true);
     }
-    tc::mma_commit(aBar);
   };
   // Y (cols 128..255) = Z K, K read as an MN-major operand.
   auto issue_intra = [&]() {
@@ -231,12 +265,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc::tmem_ld32(tl + COL_W, w);
     tc::tmem_ld_wait();
     float zmax = 0.0f;
+    if (factored) {
+      const float fr = f * e2r_i;
 #pragma unroll
-    for (int kk = 0; kk < 32; kk++) {
-      const int j = c0 + kk;
-      const float dij = (valid && j <= i) ? exp2f(ell2_i - m->ell2[j]) : 0.0f;
-      w[kk] *= f * dij;
-      zmax = fmaxf(zmax, fabsf(w[kk]));
+      for (int g = 0; g < 8; g++) {
+        const float4 ec = reinterpret_cast<const float4 *>(m->e2c + c0)[g];
+        const float e4[4] = {ec.x, ec.y, ec.z, ec.w};
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++) {
+          const int j = c0 + 4 * g + kk;
+          w[4 * g + kk] = (j <= i) ? w[4 * g + kk] * fr * e4[kk] : 0.0f;
+          zmax = fmaxf(zmax, fabsf(w[4 * g + kk]));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 32; kk++) {
+        const int j = c0 + kk;
+        const float dij = (valid && j <= i) ? exp2f(ell2_i - m->ell2[j]) : 0.0f;
+        w[kk] *= f * dij;
+        zmax = fmaxf(zmax, fabsf(w[kk]));
+      }
     }
     // the scratch lies inside the Z operand written next: block-wide barriers
     const float zs = tc::pow2_ceil(rowred<true, true>(zmax, scr, qd, grp, i));
@@ -259,7 +308,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int any = __syncthreads_or(act ? 1 : 0);
     tc::fence_after_sync();
     if (!any) break;
-    if (tid == 0) issue_state_and_keys();
+    if (tid == 0) issue_keys_then_state();
     if (!wait_mma()) {
       failed = true;
       break;
@@ -288,10 +337,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int g = 0; g < 4; g++) {
         float p8[8];
         ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
+        const float4 l0 = reinterpret_cast<const float4 *>(m->lam + c0 + 8 * g)[0];
+        const float4 l1 = reinterpret_cast<const float4 *>(m->lam + c0 + 8 * g)[1];
+        const float l8[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
           const int e = g * 8 + kk;
-          ap[e] = fmaf(fu, ap[e], fmaf(fy, yy[e], m->lam[c0 + e] * p8[kk]));
+          ap[e] = fmaf(fu, ap[e], fmaf(fy, yy[e], l8[kk] * p8[kk]));
           sg = fmaf(p8[kk], ap[e], sg);
         }
       }
@@ -324,8 +376,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       tc::tmem_st32(tl + COL_X, xx);
     }
-    rn = rowred<false>(rn, scr, qd, grp, i);
-    rmax = rowred<true>(rmax, scr, qd, grp, i);
+    rowred2(rn, rmax, scr, qd, grp, i);
     const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
     // p = r + beta p, re-scaled: |p_new| <= max|r| + beta max|p| <= rmax + beta mP
     if (act) {
@@ -368,7 +419,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (tid == 0) issue_state_and_keys();
+    if (tid == 0) issue_keys_then_state();
     failed = !wait_mma();
     if (!failed) {
       const float zs = build_z(mX);
