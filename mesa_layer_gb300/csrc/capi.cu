@@ -122,6 +122,7 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_DECODE: return "mesa_decode_kernel";
     case mesa::K_CG_TC: return "mesa_cg_tc_kernel";
     case mesa::K_DELTA_TC: return "mesa_delta_tc_kernel";
+    case mesa::K_CG_ROWS: return "mesa_cg_rows_kernel";
   }
   return nullptr;
 }
@@ -200,7 +201,8 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
   if (mesa::launch_chunk_states(a, ws, tc ? status : nullptr, stream) != 0) return MESA_ERR_CUDA;
   const int rc = tc ? mesa::launch_chunk_cg_tc(a, ws, status, stream)
-                    : mesa::launch_chunk_cg_simt(a, ws, stream);
+                 : (dk <= 64 ? mesa::launch_chunk_cg_rows(a, ws, stream)
+                             : mesa::launch_chunk_cg_simt(a, ws, stream));
   return rc == 0 ? MESA_OK : MESA_ERR_CUDA;
 }
 

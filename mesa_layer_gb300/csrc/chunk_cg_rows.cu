@@ -1,0 +1,213 @@
+// chunk_cg_rows.cu -- batched per-token CG over one chunk, fp32, for d_k = d_v <= 64.
+//
+// Same algebra as chunk_cg_simt.cu (MesaNet technical summary, gist.science/pt/paper/
+// 2506.05233, "A Camada Mesa" and "Paralelizacao"): for token i of chunk c,
+//     (H_i + Lambda) p = e^{l_i} S^H_{c-1} p + sum_{j<=i} D_ij (k_j . p) k_j + lambda o p,
+//     o_i = e^{l_i} S^G_{c-1} x + sum_{j<=i} D_ij (k_j . x) v_j,   D_ij = e^{l_i - l_j}.
+// Different mapping: four adjacent lanes own one token row and a quarter of its columns
+// each, holding p, x, r and (H+Lambda)p for those columns in registers.  Every dot product
+// of a row is a 2-step shuffle reduction inside its lane quad, the state and key rows are
+// broadcast reads from shared memory, and the CG loop has no barrier at all: a warp (8
+// rows) iterates until its own rows have stopped, then writes their outputs.
+#include "common.cuh"
+#include "launch.h"
+
+namespace mesa {
+
+template <int D, typename TIO>
+__global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspace ws, int NC) {
+  constexpr int DC = D / 4;  // columns per lane
+  const int C = a.chunk, T = a.T;
+  const int c = blockIdx.x, u = blockIdx.y;
+  const int t0 = c * C;
+  const int Cv = min(C, T - t0);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int part = lane & 3;                 // column quarter
+  const int i = 8 * warp + (lane >> 2);      // token row in the chunk
+  const int quad0 = lane & ~3;               // first lane of this row's quad
+  const bool valid = i < Cv;
+  const size_t tokbase = (size_t)u * T + t0;
+
+  extern __shared__ __align__(16) float smem[];
+  float *SH = smem;           // [D][D]  S^H_{c-1} (symmetric)
+  float *SGt = SH + D * D;    // [D][D]  (S^G_{c-1})^T
+  float *Ks = SGt + D * D;    // [C][D]
+  float *Vs = Ks + 128 * D;   // [C][D]
+  float *e2c = Vs + 128 * D;  // [C]  2^{-l2_j}
+  float *l2s = e2c + 128;     // [C]  l2_j = l_j log2(e)
+  float *lam = l2s + 128;     // [D]
+  __shared__ int factored_s;
+
+  const TIO *q = (const TIO *)a.q, *k = (const TIO *)a.k, *v = (const TIO *)a.v;
+  {
+    const float *S = nullptr, *G = nullptr;
+    if (c > 0) {
+      S = ws.SH + ((size_t)u * NC + (c - 1)) * D * D;
+      G = ws.SG + ((size_t)u * NC + (c - 1)) * D * D;
+    } else if (a.H0) {
+      S = a.H0 + (size_t)u * D * D;
+      G = a.G0 + (size_t)u * D * D;
+    }
+    for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
+      SH[e] = S ? S[e] : 0.0f;
+      SGt[(e % D) * D + e / D] = G ? G[e] : 0.0f;
+    }
+    for (int e = threadIdx.x; e < C * D; e += blockDim.x) {
+      const bool in = e / D < Cv;
+      Ks[e] = in ? ld(k, tokbase * D + e) : 0.0f;
+      Vs[e] = in ? ld(v, tokbase * D + e) : 0.0f;
+    }
+    if (threadIdx.x == 0) factored_s = 1;
+    for (int j = threadIdx.x; j < D; j += blockDim.x) lam[j] = a.lambda[(size_t)(u % a.H) * D + j];
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < C; j += blockDim.x) {
+    const float l2 = j < Cv ? ws.ell[tokbase + j] * 1.4426950408889634f : 0.0f;
+    l2s[j] = l2;
+    e2c[j] = j < Cv ? exp2f(-l2) : 0.0f;
+    if (!(fabsf(l2) <= 100.0f)) atomicAnd(&factored_s, 0);
+  }
+  __syncthreads();
+  const bool factored = factored_s != 0;
+  const float l2_i = valid ? l2s[i] : 0.0f;
+  const float el_i = valid ? exp2f(l2_i) : 0.0f;
+  const int jend = min(Cv, 8 * warp + 8);  // keys visible to this warp's rows
+  auto dec = [&](int j) -> float {  // D_ij for this lane's row (0 above the diagonal)
+    if (!valid || j > i) return 0.0f;
+    return factored ? el_i * e2c[j] : exp2f(l2_i - l2s[j]);
+  };
+  auto quad_sum = [](float s) {
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    return s;
+  };
+
+  float p[DC], x[DC], r[DC], ap[DC];
+  float s0 = 0.0f;
+#pragma unroll
+  for (int n = 0; n < DC; n++) {
+    const float qv = valid ? ld(q, (tokbase + i) * D + part * DC + n) : 0.0f;
+    p[n] = qv;
+    r[n] = qv;
+    x[n] = 0.0f;
+    s0 = fmaf(qv, qv, s0);
+  }
+  float rho = quad_sum(s0);
+  const float nq = sqrtf(rho);
+  bool act = valid;
+  int cnt = 0;
+  const bool dynamic = a.cg_tol > 0.0f;
+
+  // y += e^{l_i} S z + sum_j D_ij (z . k_j) k_j  for this lane's columns; z as in p.
+  auto apply = [&](const float (&z)[DC], float (&y)[DC], const float *Sm, const float *Kr,
+                   const float *Vr) {
+#pragma unroll
+    for (int e = 0; e < D; e++) {
+      const float ze = el_i * __shfl_sync(0xffffffffu, z[e % DC], quad0 + e / DC);
+      const float4 *srow = reinterpret_cast<const float4 *>(Sm + e * D + part * DC);
+#pragma unroll
+      for (int n4 = 0; n4 < DC / 4; n4++) {
+        const float4 sv = srow[n4];
+        y[4 * n4] = fmaf(ze, sv.x, y[4 * n4]);
+        y[4 * n4 + 1] = fmaf(ze, sv.y, y[4 * n4 + 1]);
+        y[4 * n4 + 2] = fmaf(ze, sv.z, y[4 * n4 + 2]);
+        y[4 * n4 + 3] = fmaf(ze, sv.w, y[4 * n4 + 3]);
+      }
+    }
+    for (int j = 0; j < jend; j++) {
+      const float4 *krow = reinterpret_cast<const float4 *>(Kr + j * D + part * DC);
+      float kv[DC];
+      float dot = 0.0f;
+#pragma unroll
+      for (int n4 = 0; n4 < DC / 4; n4++) {
+        const float4 t = krow[n4];
+        kv[4 * n4] = t.x;
+        kv[4 * n4 + 1] = t.y;
+        kv[4 * n4 + 2] = t.z;
+        kv[4 * n4 + 3] = t.w;
+      }
+#pragma unroll
+      for (int n = 0; n < DC; n++) dot = fmaf(z[n], kv[n], dot);
+      const float wgt = dec(j) * quad_sum(dot);
+      if (Vr != Kr) {
+        const float4 *vrow = reinterpret_cast<const float4 *>(Vr + j * D + part * DC);
+#pragma unroll
+        for (int n4 = 0; n4 < DC / 4; n4++) {
+          const float4 t = vrow[n4];
+          kv[4 * n4] = t.x;
+          kv[4 * n4 + 1] = t.y;
+          kv[4 * n4 + 2] = t.z;
+          kv[4 * n4 + 3] = t.w;
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < DC; n++) y[n] = fmaf(wgt, kv[n], y[n]);
+    }
+  };
+
+  for (int it = 0; it < a.cg_iters; it++) {
+    if (dynamic && act && sqrtf(rho) <= a.cg_tol * nq) act = false;
+    if (!__any_sync(0xffffffffu, act)) break;
+#pragma unroll
+    for (int n = 0; n < DC; n++) ap[n] = lam[part * DC + n] * p[n];
+    apply(p, ap, SH, Ks, Ks);
+    float sg = 0.0f;
+#pragma unroll
+    for (int n = 0; n < DC; n++) sg = fmaf(p[n], ap[n], sg);
+    const float sigma = quad_sum(sg);
+    const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
+    float rs = 0.0f;
+#pragma unroll
+    for (int n = 0; n < DC; n++) {
+      x[n] = fmaf(alpha, p[n], x[n]);
+      r[n] = fmaf(-alpha, ap[n], r[n]);
+      rs = fmaf(r[n], r[n], rs);
+    }
+    const float rn = quad_sum(rs);
+    if (act) {
+      const float beta = rho > 0.0f ? rn / rho : 0.0f;
+#pragma unroll
+      for (int n = 0; n < DC; n++) p[n] = fmaf(beta, p[n], r[n]);
+      rho = rn;
+      cnt++;
+    }
+  }
+
+  // readout o = e^{l_i} S^G x + sum_j D_ij (x . k_j) v_j  (S^G stored transposed)
+  float o[DC];
+#pragma unroll
+  for (int n = 0; n < DC; n++) o[n] = 0.0f;
+  apply(x, o, SGt, Ks, Vs);
+  if (valid) {
+    TIO *out = (TIO *)a.out;
+#pragma unroll
+    for (int n = 0; n < DC; n++) st(out, (tokbase + i) * D + part * DC + n, o[n]);
+    if (part == 0 && a.iters) a.iters[tokbase + i] = cnt;
+  }
+}
+
+template <int D, typename TIO>
+static int launch_rows_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+  const int U = a.B * a.H, C = a.chunk;
+  const int NC = (a.T + C - 1) / C;
+  const size_t smem = sizeof(float) * (2 * D * D + 2 * 128 * D + 2 * 128 + D);
+  auto kfn = mesa_cg_rows_kernel<D, TIO>;
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return -1;
+  timing_mark_begin(K_CG_ROWS, st);
+  kfn<<<dim3(NC, U), 4 * ((C + 7) / 8) * 8, smem, st>>>(a, ws, NC);
+  timing_mark_end(K_CG_ROWS, st);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_chunk_cg_rows(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+  const bool bf = a.dtype == 1;
+  switch (a.dk) {
+    case 16: return bf ? launch_rows_t<16, __nv_bfloat16>(a, ws, st) : launch_rows_t<16, float>(a, ws, st);
+    case 32: return bf ? launch_rows_t<32, __nv_bfloat16>(a, ws, st) : launch_rows_t<32, float>(a, ws, st);
+    case 64: return bf ? launch_rows_t<64, __nv_bfloat16>(a, ws, st) : launch_rows_t<64, float>(a, ws, st);
+  }
+  return -1;
+}
+
+}  // namespace mesa

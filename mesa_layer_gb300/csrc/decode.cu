@@ -252,14 +252,19 @@ __global__ void __launch_bounds__(512, 2) mesa_decode128_kernel(DecArgs a) {
     return s;
   };
 
+  // p's columns live in registers (pc, this lane's float4) and p's rows with their row
+  // owners (pr), so after the second reduction of an iteration every thread updates its own
+  // copy of p from the new residual (rvec) without a further barrier.
   float xr = 0.0f, rr = pvec[row], pr = rr;
+  float4 pc = reinterpret_cast<const float4 *>(pvec)[lane];
   float rho = block_rows_sum(rr * rr, 0);
   const float nq = sqrtf(rho);
   const bool dynamic = a.cg_tol > 0.0f;
+  float *rvec = kvec;  // keys are in registers (kc, kr) from here on; reuse their slot
+  __syncthreads();     // every thread has read the keys
   int it = 0;
   for (; it < a.cg_iters; it++) {
     if (dynamic && sqrtf(rho) <= a.cg_tol * nq) break;
-    const float4 pc = reinterpret_cast<const float4 *>(pvec)[lane];
     float s[8];
 #pragma unroll
     for (int j = 0; j < 8; j++)
@@ -269,12 +274,16 @@ __global__ void __launch_bounds__(512, 2) mesa_decode128_kernel(DecArgs a) {
     const float alpha = (sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
     xr = fmaf(alpha, pr, xr);
     rr = fmaf(-alpha, w, rr);
-    const float rn = block_rows_sum(rr * rr, 0);
+    if ((lane & 3) == 0) rvec[row] = rr;
+    const float rn = block_rows_sum(rr * rr, 0);  // its barrier also publishes rvec
     const float beta = rho > 0.0f ? rn / rho : 0.0f;
     pr = fmaf(beta, pr, rr);
-    if ((lane & 3) == 0) pvec[row] = pr;
+    const float4 rc = reinterpret_cast<const float4 *>(rvec)[lane];
+    pc.x = fmaf(beta, pc.x, rc.x);
+    pc.y = fmaf(beta, pc.y, rc.y);
+    pc.z = fmaf(beta, pc.z, rc.z);
+    pc.w = fmaf(beta, pc.w, rc.w);
     rho = rn;
-    __syncthreads();
   }
 
   // readout: G <- gamma G + v k^T (from the shared copy), o = G x

@@ -35,7 +35,7 @@ struct DecArgs {
 
 // Kernel kinds, for the optional per-kernel timing of benchmarks (mesa_timing_*).
 enum KernelKind {
-  K_ELL = 0, K_DELTA = 1, K_SCAN = 2, K_CG_SIMT = 3, K_DECODE = 4, K_CG_TC = 5, K_DELTA_TC = 6, K_NUM_KINDS = 8
+  K_ELL = 0, K_DELTA = 1, K_SCAN = 2, K_CG_SIMT = 3, K_DECODE = 4, K_CG_TC = 5, K_DELTA_TC = 6, K_CG_ROWS = 7, K_NUM_KINDS = 8
 };
 
 // Record a timing event before / after a launch of `kind` on `st` (no-op unless enabled).
@@ -47,6 +47,8 @@ void timing_mark_end(int kind, cudaStream_t st);
 int launch_chunk_states(const FwdArgs &a, const FwdWorkspace &ws, unsigned *tc_status,
                         cudaStream_t st);
 int launch_chunk_cg_simt(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
+// fp32 path for dk = dv <= 64: four lanes per token row, no barrier in the CG loop.
+int launch_chunk_cg_rows(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
 // Tensor-core path: bf16 q/k/v, dk = dv = 128, 128-token chunks (states and log-decays
 // must have been built with chunk = 128).  Bounded-wait failures set bits in *status.
 int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st);
