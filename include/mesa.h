@@ -114,6 +114,31 @@ int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state,
                      float cg_tol, void *out, int32_t *iters_used, cudaStream_t stream);
 
 /*
+ * mesa_forward_chunked without a caller-provided workspace (no counterpart on the MesaNet
+ * pages).  For callers that cannot allocate device memory where they run the layer: a host
+ * that forbids cudaMalloc and owns every byte of device memory, a plugin that only receives
+ * its input and output buffers, or code recorded into a CUDA graph (cudaMalloc is not
+ * allowed during stream capture).  Inputs, outputs and results are those of
+ * mesa_forward_chunked with H0 = G0 = H_final = G_final = NULL.
+ *   - Scratch: a fixed array of MESA_NOALLOC_MAX_BYTES (16 MiB) in the library's device
+ *     image, held by every GPU that loads the library until the process exits.  A call
+ *     whose mesa_forward_workspace_size() exceeds it returns MESA_ERR_WORKSPACE and
+ *     enqueues nothing.
+ *   - The first call on a device (with that device current) looks up the array's device
+ *     address and caches it; make that first call before capturing a stream on the device.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.
+ *   - Every call shares the one array: calls that overlap on the GPU race and must be
+ *     ordered by the caller (same stream, or events).  The status word that
+ *     mesa_forward_status reads lives in the array too; it cannot be queried through this
+ *     entry point.
+ */
+#define MESA_NOALLOC_MAX_BYTES (16u << 20)
+int mesa_forward_chunked_noalloc(int B, int H, int T, int dk, int dv, int dtype, const void *q,
+                                 const void *k, const void *v, const float *gamma,
+                                 const float *lambda_diag, int cg_iters, float cg_tol, int chunk,
+                                 void *out, int32_t *iters_used, cudaStream_t stream);
+
+/*
  * Device status word of the last mesa_forward_chunked call that used `workspace`:
  * synchronises `stream`, then copies the word to *flags (host).  0 means no kernel gave up;
  * bit 0 set means a tensor-core kernel's bounded wait for its matrix multiplies expired and

@@ -50,6 +50,8 @@ def load(build_if_missing: bool = True):
     lib.mesa_forward_chunked.restype = _i
     lib.mesa_forward_chunked.argtypes = [_i] * 6 + [_vp] * 5 + [_i, _f, _i, _vp, _ip] + \
         [_fp] * 4 + [_vp, _sz, _vp]
+    lib.mesa_forward_chunked_noalloc.restype = _i
+    lib.mesa_forward_chunked_noalloc.argtypes = [_i] * 6 + [_vp] * 5 + [_i, _f, _i, _vp, _ip, _vp]
     lib.mesa_forward_status.restype = _i
     lib.mesa_forward_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint)]
     lib.mesa_tc_selftest.restype = _i
@@ -177,3 +179,29 @@ def mesa_tc_selftest(A, B, stream=None):
     _check(lib.mesa_tc_selftest(_ptr(A), _ptr(B), _ptr(C1), _ptr(C2), _ptr(C3), _ptr(status),
                                 _stream(stream)), "mesa_tc_selftest")
     return C1, C2, C3, status
+
+
+NOALLOC_MAX_BYTES = 16 << 20
+
+
+def mesa_forward_chunked_noalloc(q, k, v, gamma, lambda_diag, cg_iters, cg_tol, chunk, out=None,
+                                 iters_used=None, stream=None):
+    """mesa_forward_chunked with the library's fixed device scratch instead of a workspace
+    (no device allocation inside the call; calls must not overlap on the GPU)."""
+    lib = load()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, q.dtype)
+    _require(gamma, "gamma", torch.float32)
+    _require(lambda_diag, "lambda_diag", torch.float32)
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device)
+    if iters_used is None:
+        iters_used = torch.empty((B, H, T), dtype=torch.int32, device=q.device)
+    st = lib.mesa_forward_chunked_noalloc(B, H, T, dk, dv, code, _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
+                                          _ptr(lambda_diag), int(cg_iters), float(cg_tol), int(chunk),
+                                          _ptr(out), _ptr(iters_used), _stream(stream))
+    _check(st, "mesa_forward_chunked_noalloc")
+    return out, iters_used
