@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--impl", default="mesa", choices=["mesa", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--decode-prefix", type=int, default=None,
+                   help="decode workload: state-only prefix steps (default: the workload's)")
     return p.parse_args()
 
 
@@ -420,7 +422,8 @@ def bench_decode(args, w, rank, world, dev, lib, torch, binding):
         inp = synth.decode_inputs(w, s, seed=rank)
         return {k: torch.from_numpy(inp[k]).to(dev).to(td if k != "gamma" else torch.float32) for k in inp}
 
-    for s in range(-w.prefix, 0):  # state-only prefix (untimed): cg_iters = 0
+    prefix = w.prefix if args.decode_prefix is None else args.decode_prefix
+    for s in range(-prefix, 0):  # state-only prefix (untimed): cg_iters = 0
         x = dev_inputs(s)
         binding.mesa_decode_step(Hs, Gs, x["q"], x["k"], x["v"], x["gamma"], lam, 0, 0.0, out=out, iters_used=iters)
     n_steps = min(w.decode_steps, max(args.steps, 1))

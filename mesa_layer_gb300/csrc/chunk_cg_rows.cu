@@ -5,7 +5,9 @@
 //     (H_i + Lambda) p = e^{l_i} S^H_{c-1} p + sum_{j<=i} D_ij (k_j . p) k_j + lambda o p,
 //     o_i = e^{l_i} S^G_{c-1} x + sum_{j<=i} D_ij (k_j . x) v_j,   D_ij = e^{l_i - l_j}.
 // Different mapping: four adjacent lanes own one token row and a quarter of its columns
-// each, holding p, x, r and (H+Lambda)p for those columns in registers.  Every dot product
+// each (lane part p holds the float4 column groups p, p+4, p+8, ..., so the four lanes of a
+// row read 64 contiguous bytes of a shared row: no bank conflicts), holding p, x, r and
+// (H+Lambda)p for those columns in registers.  Every dot product
 // of a row is a 2-step shuffle reduction inside its lane quad, the state and key rows are
 // broadcast reads from shared memory, and the CG loop has no barrier at all: a warp (8
 // rows) iterates until its own rows have stopped, then writes their outputs.
@@ -76,6 +78,8 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
     if (!valid || j > i) return 0.0f;
     return factored ? el_i * e2c[j] : exp2f(l2_i - l2s[j]);
   };
+  // column of local index n (0 <= n < DC) of this lane
+  auto col = [&](int n) { return 16 * (n >> 2) + 4 * part + (n & 3); };
   auto quad_sum = [](float s) {
     s += __shfl_xor_sync(0xffffffffu, s, 1);
     s += __shfl_xor_sync(0xffffffffu, s, 2);
@@ -86,7 +90,7 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
   float s0 = 0.0f;
 #pragma unroll
   for (int n = 0; n < DC; n++) {
-    const float qv = valid ? ld(q, (tokbase + i) * D + part * DC + n) : 0.0f;
+    const float qv = valid ? ld(q, (tokbase + i) * D + col(n)) : 0.0f;
     p[n] = qv;
     r[n] = qv;
     x[n] = 0.0f;
@@ -103,11 +107,12 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
                    const float *Vr) {
 #pragma unroll
     for (int e = 0; e < D; e++) {
-      const float ze = el_i * __shfl_sync(0xffffffffu, z[e % DC], quad0 + e / DC);
-      const float4 *srow = reinterpret_cast<const float4 *>(Sm + e * D + part * DC);
+      // column e lives in lane part (e % 16) / 4, local index 4 (e / 16) + e % 4
+      const float ze = el_i * __shfl_sync(0xffffffffu, z[4 * (e >> 4) + (e & 3)], quad0 + ((e & 15) >> 2));
+      const float4 *srow = reinterpret_cast<const float4 *>(Sm + e * D);
 #pragma unroll
       for (int n4 = 0; n4 < DC / 4; n4++) {
-        const float4 sv = srow[n4];
+        const float4 sv = srow[4 * n4 + part];
         y[4 * n4] = fmaf(ze, sv.x, y[4 * n4]);
         y[4 * n4 + 1] = fmaf(ze, sv.y, y[4 * n4 + 1]);
         y[4 * n4 + 2] = fmaf(ze, sv.z, y[4 * n4 + 2]);
@@ -115,12 +120,12 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
       }
     }
     for (int j = 0; j < jend; j++) {
-      const float4 *krow = reinterpret_cast<const float4 *>(Kr + j * D + part * DC);
+      const float4 *krow = reinterpret_cast<const float4 *>(Kr + j * D);
       float kv[DC];
       float dot = 0.0f;
 #pragma unroll
       for (int n4 = 0; n4 < DC / 4; n4++) {
-        const float4 t = krow[n4];
+        const float4 t = krow[4 * n4 + part];
         kv[4 * n4] = t.x;
         kv[4 * n4 + 1] = t.y;
         kv[4 * n4 + 2] = t.z;
@@ -130,10 +135,10 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
       for (int n = 0; n < DC; n++) dot = fmaf(z[n], kv[n], dot);
       const float wgt = dec(j) * quad_sum(dot);
       if (Vr != Kr) {
-        const float4 *vrow = reinterpret_cast<const float4 *>(Vr + j * D + part * DC);
+        const float4 *vrow = reinterpret_cast<const float4 *>(Vr + j * D);
 #pragma unroll
         for (int n4 = 0; n4 < DC / 4; n4++) {
-          const float4 t = vrow[n4];
+          const float4 t = vrow[4 * n4 + part];
           kv[4 * n4] = t.x;
           kv[4 * n4 + 1] = t.y;
           kv[4 * n4 + 2] = t.z;
@@ -149,7 +154,7 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
     if (dynamic && act && sqrtf(rho) <= a.cg_tol * nq) act = false;
     if (!__any_sync(0xffffffffu, act)) break;
 #pragma unroll
-    for (int n = 0; n < DC; n++) ap[n] = lam[part * DC + n] * p[n];
+    for (int n = 0; n < DC; n++) ap[n] = lam[col(n)] * p[n];
     apply(p, ap, SH, Ks, Ks);
     float sg = 0.0f;
 #pragma unroll
@@ -181,7 +186,7 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
   if (valid) {
     TIO *out = (TIO *)a.out;
 #pragma unroll
-    for (int n = 0; n < DC; n++) st(out, (tokbase + i) * D + part * DC + n, o[n]);
+    for (int n = 0; n < DC; n++) st(out, (tokbase + i) * D + col(n), o[n]);
     if (part == 0 && a.iters) a.iters[tokbase + i] = cnt;
   }
 }

@@ -30,7 +30,6 @@ namespace {
 
 using tc::DH;
 using tc::TILE;
-constexpr int NTHREADS = 512;
 constexpr uint32_t MAT_BYTES = TILE * DH * 2;  // one fp16 128x128 operand (32 KB)
 // shared-memory map (offsets from a 1024-aligned base)
 constexpr uint32_t OFF_SHI = 0, OFF_SLO = MAT_BYTES, OFF_K = 2 * MAT_BYTES,
@@ -44,36 +43,47 @@ struct Misc {
   float ell2[TILE];  // log2-decays l_i * log2(e)
   float e2c[TILE];   // 2^{-l2_j} (used when the chunk's decays fit fp32 as factors)
   float lam[DH];     // Lambda diagonal of this head
-  float red[16];
+  float red[32];
   uint64_t mbar;
   uint32_t tmem_base;
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc block too large");
 
+// Barrier of the NG warps that share lane quadrant q (warps q, q+4, ...).
+template <int NG>
 __device__ __forceinline__ void quad_bar(int q) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(1 + q), "r"(128) : "memory");
+  asm volatile("bar.sync %0, %1;\n" ::"r"(1 + q), "r"(32 * NG) : "memory");
 }
 
-// Combine the 4 column groups' partials of each row.  `scr` is 2 KB of shared memory that
-// holds no live operand at the call.  With BLOCK the barriers span the whole CTA (needed
-// when other quadrants may overwrite the scratch right after their own reduction).
-template <bool MAX, bool BLOCK = false>
+// Combine the NG column groups' partials of each row.  `scr` is NG * 512 B of shared memory
+// that holds no live operand at the call.  With BLOCK the barriers span the whole CTA
+// (needed when other quadrants may overwrite the scratch right after their reduction).
+template <int NG, bool MAX, bool BLOCK = false>
 __device__ __forceinline__ float rowred(float v, float *scr, int q, int g, int i) {
   scr[g * TILE + i] = v;
-  if (BLOCK) __syncthreads(); else quad_bar(q);
-  const float a = scr[i], b = scr[TILE + i], c = scr[2 * TILE + i], d = scr[3 * TILE + i];
-  if (BLOCK) __syncthreads(); else quad_bar(q);
-  return MAX ? fmaxf(fmaxf(a, b), fmaxf(c, d)) : (a + b) + (c + d);
+  if (BLOCK) __syncthreads(); else quad_bar<NG>(q);
+  float r = scr[i];
+#pragma unroll
+  for (int k = 1; k < NG; k++) r = MAX ? fmaxf(r, scr[k * TILE + i]) : r + scr[k * TILE + i];
+  if (BLOCK) __syncthreads(); else quad_bar<NG>(q);
+  return r;
 }
 
-// Two-value variant (a sum and a max) sharing the barriers; scratch 4 KB.
+// Two-value variant (a sum and a max) sharing the barriers; scratch NG * 1 KB.
+template <int NG>
 __device__ __forceinline__ void rowred2(float &sum, float &mx, float *scr, int q, int g, int i) {
   scr[g * TILE + i] = sum;
-  scr[4 * TILE + g * TILE + i] = mx;
-  quad_bar(q);
-  sum = (scr[i] + scr[TILE + i]) + (scr[2 * TILE + i] + scr[3 * TILE + i]);
-  mx = fmaxf(fmaxf(scr[4 * TILE + i], scr[5 * TILE + i]), fmaxf(scr[6 * TILE + i], scr[7 * TILE + i]));
-  quad_bar(q);
+  scr[(NG + g) * TILE + i] = mx;
+  quad_bar<NG>(q);
+  float s = scr[i], m = scr[NG * TILE + i];
+#pragma unroll
+  for (int k = 1; k < NG; k++) {
+    s += scr[k * TILE + i];
+    m = fmaxf(m, scr[(NG + k) * TILE + i]);
+  }
+  sum = s;
+  mx = m;
+  quad_bar<NG>(q);
 }
 
 // 8 consecutive values (columns c0..c0+7 of row i) of a hi/lo operand, times mul.
@@ -110,8 +120,12 @@ __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, con
 
 }  // namespace
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int TPR>
+__global__ void __launch_bounds__(128 * TPR, 1)
     mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, unsigned *status) {
+  constexpr int NG = TPR;         // column groups (threads per token row)
+  constexpr int CW = DH / TPR;    // columns per thread
+  constexpr int NV = CW / 8;      // 8-column vectors per thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t *Shi = sm + OFF_SHI, *Slo = sm + OFF_SLO, *Ks = sm + OFF_K;
@@ -127,7 +141,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, grp = warp >> 2;  // lane quadrant, column group
   const int i = 32 * qd + lane;               // token row of this thread
-  const int c0 = 32 * grp;                    // first column of this thread
+  const int c0 = CW * grp;                    // first column of this thread
   const int c = blockIdx.x, u = blockIdx.y;
   const int T = a.T;
   const int t0 = c * TILE;
@@ -170,13 +184,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const float sS = tc::stage_state(SH, Shi, Slo, m->red);
   const float sK = tc::stage_rows(k + tokbase * DH, Tv, Ks, m->red);
 
-  // CG start: x = 0, r = p = q_i (this thread's 32 columns)
+  // CG start: x = 0, r = p = q_i (this thread's CW columns)
   float rho, nq, mP;
   {
-    float qa[32];
+    float qa[CW];
     const uint4 *src = reinterpret_cast<const uint4 *>(q + (tokbase + i) * DH + c0);
 #pragma unroll
-    for (int g = 0; g < 4; g++) {
+    for (int g = 0; g < NV; g++) {
       const uint4 raw = valid ? src[g] : make_uint4(0, 0, 0, 0);
       const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
 #pragma unroll
@@ -184,22 +198,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     float s = 0.0f, mx = 0.0f;
 #pragma unroll
-    for (int d = 0; d < 32; d++) {
+    for (int d = 0; d < CW; d++) {
       s = fmaf(qa[d], qa[d], s);
       mx = fmaxf(mx, fabsf(qa[d]));
     }
-    rowred2(s, mx, scr, qd, grp, i);
+    rowred2<NG>(s, mx, scr, qd, grp, i);
     rho = s;
     nq = sqrtf(rho);
     mP = tc::pow2_ceil(mx);
-    float z[32];
+    float z[CW];
 #pragma unroll
-    for (int kk = 0; kk < 32; kk++) z[kk] = 0.0f;
-    tc::tmem_st32(tl + COL_X, z);
-    tc::tmem_st32(tl + COL_R, qa);
+    for (int kk = 0; kk < CW; kk++) z[kk] = 0.0f;
+    tc::tmem_st<CW>(tl + COL_X, z);
+    tc::tmem_st<CW>(tl + COL_R, qa);
     const float inv = 1.0f / mP;
 #pragma unroll
-    for (int g = 0; g < 4; g++) {
+    for (int g = 0; g < NV; g++) {
       float x8[8];
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) x8[kk] = qa[g * 8 + kk];
@@ -261,14 +275,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // Z = (W * mrow / sK) o D into the Z operand; returns the row scale.
   auto build_z = [&](float mrow) -> float {
     const float f = mrow / sK;
-    float w[32];
-    tc::tmem_ld32(tl + COL_W, w);
+    float w[CW];
+    tc::tmem_ld<CW>(tl + COL_W, w);
     tc::tmem_ld_wait();
     float zmax = 0.0f;
     if (factored) {
       const float fr = f * e2r_i;
 #pragma unroll
-      for (int g = 0; g < 8; g++) {
+      for (int g = 0; g < CW / 4; g++) {
         const float4 ec = reinterpret_cast<const float4 *>(m->e2c + c0)[g];
         const float e4[4] = {ec.x, ec.y, ec.z, ec.w};
 #pragma unroll
@@ -280,7 +294,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     } else {
 #pragma unroll
-      for (int kk = 0; kk < 32; kk++) {
+      for (int kk = 0; kk < CW; kk++) {
         const int j = c0 + kk;
         const float dij = (valid && j <= i) ? exp2f(ell2_i - m->ell2[j]) : 0.0f;
         w[kk] *= f * dij;
@@ -288,10 +302,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     // the scratch lies inside the Z operand written next: block-wide barriers
-    const float zs = tc::pow2_ceil(rowred<true, true>(zmax, scr, qd, grp, i));
+    const float zs = tc::pow2_ceil(rowred<NG, true, true>(zmax, scr, qd, grp, i));
     const float inv = 1.0f / zs;
 #pragma unroll
-    for (int g = 0; g < 4; g++) {
+    for (int g = 0; g < NV; g++) {
       float x8[8];
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) x8[kk] = w[g * 8 + kk];
@@ -326,15 +340,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // AP = e^l (mP/sS) U + (zs/sK) Y + lambda p   (kept in registers); sigma = p.AP
     const float fu = el_i * mP / sS, fy = zs / sK;
-    float ap[32];
+    float ap[CW];
     float sg = 0.0f;
     {
-      float yy[32];
-      tc::tmem_ld32(tl + COL_U, ap);
-      tc::tmem_ld32(tl + COL_W, yy);
+      float yy[CW];
+      tc::tmem_ld<CW>(tl + COL_U, ap);
+      tc::tmem_ld<CW>(tl + COL_W, yy);
       tc::tmem_ld_wait();
 #pragma unroll
-      for (int g = 0; g < 4; g++) {
+      for (int g = 0; g < NV; g++) {
         float p8[8];
         ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
         const float4 l0 = reinterpret_cast<const float4 *>(m->lam + c0 + 8 * g)[0];
@@ -348,42 +362,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-    const float sigma = rowred<false>(sg, scr, qd, grp, i);
+    const float sigma = rowred<NG, false>(sg, scr, qd, grp, i);
     const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
     // r -= alpha AP, x += alpha p   (alpha = 0 leaves a finished row unchanged; the
     // tensor-memory accesses stay unconditional: they are warp-collective)
-    float rr[32];
+    float rr[CW];
     float rn = 0.0f, rmax = 0.0f;
-    tc::tmem_ld32(tl + COL_R, rr);
+    tc::tmem_ld<CW>(tl + COL_R, rr);
     tc::tmem_ld_wait();
 #pragma unroll
-    for (int kk = 0; kk < 32; kk++) {
+    for (int kk = 0; kk < CW; kk++) {
       rr[kk] = fmaf(-alpha, ap[kk], rr[kk]);
       rn = fmaf(rr[kk], rr[kk], rn);
       rmax = fmaxf(rmax, fabsf(rr[kk]));
     }
-    tc::tmem_st32(tl + COL_R, rr);
+    tc::tmem_st<CW>(tl + COL_R, rr);
     {
-      float xx[32];
-      tc::tmem_ld32(tl + COL_X, xx);
+      float xx[CW];
+      tc::tmem_ld<CW>(tl + COL_X, xx);
       tc::tmem_ld_wait();
 #pragma unroll
-      for (int g = 0; g < 4; g++) {
+      for (int g = 0; g < NV; g++) {
         float p8[8];
         ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) xx[g * 8 + kk] = fmaf(alpha, p8[kk], xx[g * 8 + kk]);
       }
-      tc::tmem_st32(tl + COL_X, xx);
+      tc::tmem_st<CW>(tl + COL_X, xx);
     }
-    rowred2(rn, rmax, scr, qd, grp, i);
+    rowred2<NG>(rn, rmax, scr, qd, grp, i);
     const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
     // p = r + beta p, re-scaled: |p_new| <= max|r| + beta max|p| <= rmax + beta mP
     if (act) {
       const float mNew = tc::pow2_ceil(rmax + beta * mP);
       const float inv = 1.0f / mNew;
 #pragma unroll
-      for (int g = 0; g < 4; g++) {
+      for (int g = 0; g < NV; g++) {
         float p8[8];
         ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
 #pragma unroll
@@ -399,16 +413,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   // ---- readout O = e^l X S^G^T + ((X K^T) o D) V ------------------------------------------
   if (!failed) {
-    float xx[32];
-    tc::tmem_ld32(tl + COL_X, xx);
+    float xx[CW];
+    tc::tmem_ld<CW>(tl + COL_X, xx);
     tc::tmem_ld_wait();
     float mx = 0.0f;
 #pragma unroll
-    for (int kk = 0; kk < 32; kk++) mx = fmaxf(mx, fabsf(xx[kk]));
-    const float mX = tc::pow2_ceil(rowred<true>(mx, scr, qd, grp, i));
+    for (int kk = 0; kk < CW; kk++) mx = fmaxf(mx, fabsf(xx[kk]));
+    const float mX = tc::pow2_ceil(rowred<NG, true>(mx, scr, qd, grp, i));
     const float inv = 1.0f / mX;
 #pragma unroll
-    for (int g = 0; g < 4; g++) {
+    for (int g = 0; g < NV; g++) {
       float x8[8];
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) x8[kk] = xx[g * 8 + kk];
@@ -432,14 +446,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       failed = !wait_mma();
       if (!failed) {
         const float fu = el_i * mX / sG, fy = zs / sV;
-        float uu[32], yy[32];
-        tc::tmem_ld32(tl + COL_U, uu);
-        tc::tmem_ld32(tl + COL_W, yy);
+        float uu[CW], yy[CW];
+        tc::tmem_ld<CW>(tl + COL_U, uu);
+        tc::tmem_ld<CW>(tl + COL_W, yy);
         tc::tmem_ld_wait();
         if (valid) {
           __nv_bfloat16 *out = (__nv_bfloat16 *)a.out + (tokbase + i) * DH + c0;
 #pragma unroll
-          for (int g = 0; g < 4; g++) {
+          for (int g = 0; g < NV; g++) {
             __align__(16) __nv_bfloat16 o8[8];
 #pragma unroll
             for (int kk = 0; kk < 8; kk++)
@@ -457,15 +471,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 0) tc::tmem_free(tbase, 512);
 }
 
+// Threads per token row of the CG kernel (4: 512 threads x 32 columns, 8: 1024 x 16).
+#ifndef MESA_TC_THREADS_PER_ROW
+#define MESA_TC_THREADS_PER_ROW 8
+#endif
+constexpr int kTcThreadsPerRow = MESA_TC_THREADS_PER_ROW;
+static_assert(kTcThreadsPerRow == 4 || kTcThreadsPerRow == 8, "4 or 8 threads per row");
+
 int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status,
                        cudaStream_t st) {
   const int U = a.B * a.H;
   const int NC = (a.T + TILE - 1) / TILE;
-  if (cudaFuncSetAttribute(mesa_cg_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)SMEM_TC) != cudaSuccess)
+  auto kfn = mesa_cg_tc_kernel<kTcThreadsPerRow>;
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC) !=
+      cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_TC, st);
-  mesa_cg_tc_kernel<<<dim3(NC, U), NTHREADS, SMEM_TC, st>>>(a, ws, NC, status);
+  kfn<<<dim3(NC, U), 128 * kTcThreadsPerRow, SMEM_TC, st>>>(a, ws, NC, status);
   timing_mark_end(K_CG_TC, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

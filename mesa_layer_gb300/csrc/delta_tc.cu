@@ -26,7 +26,7 @@ struct DeltaMisc {
 };
 }  // namespace
 
-__global__ void __launch_bounds__(128) mesa_delta_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC,
+__global__ void __launch_bounds__(512) mesa_delta_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC,
                                                             unsigned *status) {
   using tc::DH;
   using tc::TILE;
@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(128) mesa_delta_tc_kernel(FwdArgs a, FwdWorksp
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 256);
   if (tid == 0) tc::mbar_init(aBar, 1);
   const float lend = ws.ell[tokbase + Tv - 1];
-  m->w[tid] = tid < Tv ? expf(lend - ws.ell[tokbase + tid]) : 0.0f;
+  if (tid < TILE) m->w[tid] = tid < Tv ? expf(lend - ws.ell[tokbase + tid]) : 0.0f;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -90,22 +90,21 @@ __global__ void __launch_bounds__(128) mesa_delta_tc_kernel(FwdArgs a, FwdWorksp
     ok = wait();
   }
   if (ok) {
-    const uint32_t tl = tbase + ((uint32_t)(32 * warp) << 16);
-    float *SH = ws.SH + (((size_t)u * NC + c) * DH + tid) * DH;
-    float *SG = ws.SG + (((size_t)u * NC + c) * DH + tid) * DH;
+    // warp w: rows 32 (w % 4) .. +31 (its lane quadrant), columns 32 (w / 4) .. +31
+    const int row = 32 * (warp & 3) + (tid & 31), cg = warp >> 2;
+    const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * cg;
+    float *SH = ws.SH + (((size_t)u * NC + c) * DH + row) * DH + 32 * cg;
+    float *SG = ws.SG + (((size_t)u * NC + c) * DH + row) * DH + 32 * cg;
 #pragma unroll
     for (int half = 0; half < 2; half++) {
       const float f = 1.0f / ((half ? sAG : sAH) * sK);
       float4 *dst = reinterpret_cast<float4 *>(half ? SG : SH);
+      float x[32];
+      tc::tmem_ld32(tl + half * 128, x);
+      tc::tmem_ld_wait();
 #pragma unroll
-      for (int cc = 0; cc < 4; cc++) {
-        float x[32];
-        tc::tmem_ld32(tl + half * 128 + cc * 32, x);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int g = 0; g < 8; g++)
-          dst[cc * 8 + g] = make_float4(x[4 * g] * f, x[4 * g + 1] * f, x[4 * g + 2] * f, x[4 * g + 3] * f);
-      }
+      for (int g = 0; g < 8; g++)
+        dst[g] = make_float4(x[4 * g] * f, x[4 * g + 1] * f, x[4 * g + 2] * f, x[4 * g + 3] * f);
     }
   }
   tc::fence_before_sync();
@@ -120,7 +119,7 @@ int launch_delta_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, 
                            (int)DT_SMEM) != cudaSuccess)
     return -1;
   timing_mark_begin(K_DELTA_TC, st);
-  mesa_delta_tc_kernel<<<dim3(NC, U), 128, DT_SMEM, st>>>(a, ws, NC, status);
+  mesa_delta_tc_kernel<<<dim3(NC, U), 512, DT_SMEM, st>>>(a, ws, NC, status);
   timing_mark_end(K_DELTA_TC, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
