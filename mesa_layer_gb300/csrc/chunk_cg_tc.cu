@@ -472,8 +472,9 @@ __global__ void __launch_bounds__(128 * TPR, 1)
 }
 
 // Threads per token row of the CG kernel (4: 512 threads x 32 columns, 8: 1024 x 16).
+// Measured on the bf16 B=8 H=16 T=4096 forward: 3.37 ms with 4, 4.02 ms with 8.
 #ifndef MESA_TC_THREADS_PER_ROW
-#define MESA_TC_THREADS_PER_ROW 8
+#define MESA_TC_THREADS_PER_ROW 4
 #endif
 constexpr int kTcThreadsPerRow = MESA_TC_THREADS_PER_ROW;
 static_assert(kTcThreadsPerRow == 4 || kTcThreadsPerRow == 8, "4 or 8 threads per row");
