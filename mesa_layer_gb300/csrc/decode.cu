@@ -158,43 +158,46 @@ __global__ void __launch_bounds__(4 * D) mesa_decode_kernel(DecArgs a) {
 
 
 // d = 128 specialisation.  Same update, CG rule and readout; differences:
-//  - 8 rows x 128 columns per warp, one float4 of each row per lane (H in 32 registers),
-//    and row sums by a shuffle reduce-scatter (9 shuffles for the 8 rows instead of 40):
-//    after it, row 8w + (lane >> 2) is held, replicated, by the 4 lanes of that group, which
-//    also hold that row's x, r, p and lambda;
+//  - 8 warps (256 threads); warp w owns rows 16w .. 16w+15, lane l the columns 4l .. 4l+3
+//    of each (H in 64 registers), so the matrix-vector product is 64 FMAs per thread and
+//    the 16 row sums of a warp come from one shuffle reduce-scatter (16 shuffles): after it,
+//    row 16w + (lane >> 1) is held, replicated, by lanes 2j and 2j+1, which also hold that
+//    row's x, r, p and lambda;
+//  - p's columns live in registers and its rows with their owners, so the second block
+//    reduction of a CG step also publishes the new residual and each thread updates its
+//    own copy of p: two barriers per step;
 //  - G is copied to shared memory with cp.async at the start (it is needed only for the
 //    readout), so its HBM read overlaps the CG;
-//  - at most 64 registers per thread, so two units run on one SM and one unit's HBM
-//    traffic overlaps the other's CG.
+//  - two units per SM: one unit's HBM traffic overlaps the other's CG.
 template <typename TIO>
-__global__ void __launch_bounds__(512, 2) mesa_decode128_kernel(DecArgs a) {
-  constexpr int D = 128, NW = 16;
+__global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
+  constexpr int D = 128, NW = 8;
   const int u = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = 8 * warp + (lane >> 2);  // the row this lane's group holds after reduce
+  const int row = 16 * warp + (lane >> 1);  // the row this lane holds after the reduce
   extern __shared__ __align__(16) float dsm[];
   float *Gs = dsm;                         // [128][128]
-  float *kvec = Gs + D * D, *vvec = kvec + D, *pvec = vvec + D;
-  float *red = pvec + D;                   // [2][NW]
+  float *kvec = Gs + D * D, *vvec = kvec + D, *pvec = vvec + D, *rvec = pvec + D;
+  float *red = rvec + D;                   // [2][NW]
 
   const float4 *Hg = reinterpret_cast<const float4 *>(a.Hs + (size_t)u * D * D);
   float4 *Hw = reinterpret_cast<float4 *>(a.Hs + (size_t)u * D * D);
   float4 *Gw = reinterpret_cast<float4 *>(a.Gs + (size_t)u * D * D);
-  // G -> shared memory, asynchronously (8 x 16 bytes per thread)
+  // G -> shared memory, asynchronously (16 x 16 bytes per thread)
   {
     const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(Gs);
+    const float4 *gsrc = reinterpret_cast<const float4 *>(a.Gs + (size_t)u * D * D);
 #pragma unroll
-    for (int k = 0; k < 8; k++) {
-      const int e = threadIdx.x + 512 * k;  // float4 index
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sbase + 16 * e),
-                   "l"(reinterpret_cast<const float4 *>(a.Gs + (size_t)u * D * D) + e)
+    for (int k = 0; k < 16; k++) {
+      const int e = threadIdx.x + 256 * k;  // float4 index
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sbase + 16 * e), "l"(gsrc + e)
                    : "memory");
     }
     asm volatile("cp.async.commit_group;\n" ::: "memory");
   }
-  float4 h[8];
+  float4 h[16];
 #pragma unroll
-  for (int j = 0; j < 8; j++) h[j] = Hg[(8 * warp + j) * 32 + lane];
+  for (int j = 0; j < 16; j++) h[j] = Hg[(16 * warp + j) * 32 + lane];
   const TIO *q = (const TIO *)a.q, *k = (const TIO *)a.k, *v = (const TIO *)a.v;
   if (threadIdx.x < D) {
     kvec[threadIdx.x] = ld(k, (size_t)u * D + threadIdx.x);
@@ -207,74 +210,65 @@ __global__ void __launch_bounds__(512, 2) mesa_decode128_kernel(DecArgs a) {
 
   const float4 kc = reinterpret_cast<const float4 *>(kvec)[lane];
 #pragma unroll
-  for (int j = 0; j < 8; j++) {
-    const float kr = kvec[8 * warp + j];
+  for (int j = 0; j < 16; j++) {
+    const float kr = kvec[16 * warp + j];
     h[j].x = fmaf(g, h[j].x, kr * kc.x);
     h[j].y = fmaf(g, h[j].y, kr * kc.y);
     h[j].z = fmaf(g, h[j].z, kr * kc.z);
     h[j].w = fmaf(g, h[j].w, kr * kc.w);
-    Hw[(8 * warp + j) * 32 + lane] = h[j];
+    Hw[(16 * warp + j) * 32 + lane] = h[j];
   }
 
-  // reduce-scatter of s[0..7] over the 32 lanes: returns the full sum of row lane >> 2
-  auto rowsum = [&](float (&s)[8]) -> float {
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-    float t4[4], t2[2];
+  // reduce-scatter of s[0..15] over the 32 lanes: the full sum of row lane >> 1
+  auto rowsum = [&](float (&s)[16]) -> float {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+    float t8[8], t4[4], t2[2];
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const float send = b4 ? s[j] : s[j + 4];
-      t4[j] = (b4 ? s[j + 4] : s[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
+    for (int j = 0; j < 8; j++)
+      t8[j] = (b4 ? s[j + 8] : s[j]) + __shfl_xor_sync(0xffffffffu, b4 ? s[j] : s[j + 8], 16);
 #pragma unroll
-    for (int j = 0; j < 2; j++) {
-      const float send = b3 ? t4[j] : t4[j + 2];
-      t2[j] = (b3 ? t4[j + 2] : t4[j]) + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    float t = (b2 ? t2[1] : t2[0]) + __shfl_xor_sync(0xffffffffu, b2 ? t2[0] : t2[1], 4);
-    t += __shfl_xor_sync(0xffffffffu, t, 2);
-    t += __shfl_xor_sync(0xffffffffu, t, 1);
-    return t;
+    for (int j = 0; j < 4; j++)
+      t4[j] = (b3 ? t8[j + 4] : t8[j]) + __shfl_xor_sync(0xffffffffu, b3 ? t8[j] : t8[j + 4], 8);
+#pragma unroll
+    for (int j = 0; j < 2; j++)
+      t2[j] = (b2 ? t4[j + 2] : t4[j]) + __shfl_xor_sync(0xffffffffu, b2 ? t4[j] : t4[j + 2], 4);
+    float t = (b1 ? t2[1] : t2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? t2[0] : t2[1], 2);
+    return t + __shfl_xor_sync(0xffffffffu, t, 1);
   };
-  // sum over the warp's 8 rows of a value replicated in each 4-lane group, then over warps
+  // sum over the warp's 16 rows of a value replicated in each lane pair, then over warps
   auto block_rows_sum = [&](float val, int buf) -> float {
+    val += __shfl_xor_sync(0xffffffffu, val, 2);
     val += __shfl_xor_sync(0xffffffffu, val, 4);
     val += __shfl_xor_sync(0xffffffffu, val, 8);
     val += __shfl_xor_sync(0xffffffffu, val, 16);
     if (lane == 0) red[buf * NW + warp] = val;
     __syncthreads();
-    const float4 *r4 = reinterpret_cast<const float4 *>(red + buf * NW);
-    float s = 0.0f;
-#pragma unroll
-    for (int k = 0; k < NW / 4; k++) {
-      const float4 x = r4[k];
-      s += (x.x + x.y) + (x.z + x.w);
-    }
-    return s;
+    const float4 a0 = reinterpret_cast<const float4 *>(red + buf * NW)[0];
+    const float4 a1 = reinterpret_cast<const float4 *>(red + buf * NW)[1];
+    return ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
   };
 
   // p's columns live in registers (pc, this lane's float4) and p's rows with their row
-  // owners (pr), so after the second reduction of an iteration every thread updates its own
-  // copy of p from the new residual (rvec) without a further barrier.
+  // owners (pr); after the second reduction of a step every thread updates its own copy of
+  // p from the new residual (rvec) without a further barrier.
   float xr = 0.0f, rr = pvec[row], pr = rr;
   float4 pc = reinterpret_cast<const float4 *>(pvec)[lane];
   float rho = block_rows_sum(rr * rr, 0);
   const float nq = sqrtf(rho);
   const bool dynamic = a.cg_tol > 0.0f;
-  float *rvec = kvec;  // keys are in registers (kc, kr) from here on; reuse their slot
-  __syncthreads();     // every thread has read the keys
   int it = 0;
   for (; it < a.cg_iters; it++) {
     if (dynamic && sqrtf(rho) <= a.cg_tol * nq) break;
-    float s[8];
+    float s[16];
 #pragma unroll
-    for (int j = 0; j < 8; j++)
+    for (int j = 0; j < 16; j++)
       s[j] = fmaf(h[j].w, pc.w, fmaf(h[j].z, pc.z, fmaf(h[j].y, pc.y, h[j].x * pc.x)));
     const float w = fmaf(lam_r, pr, rowsum(s));
     const float sigma = block_rows_sum(pr * w, 1);
     const float alpha = (sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
     xr = fmaf(alpha, pr, xr);
     rr = fmaf(-alpha, w, rr);
-    if ((lane & 3) == 0) rvec[row] = rr;
+    if ((lane & 1) == 0) rvec[row] = rr;
     const float rn = block_rows_sum(rr * rr, 0);  // its barrier also publishes rvec
     const float beta = rho > 0.0f ? rn / rho : 0.0f;
     pr = fmaf(beta, pr, rr);
@@ -289,13 +283,13 @@ __global__ void __launch_bounds__(512, 2) mesa_decode128_kernel(DecArgs a) {
   // readout: G <- gamma G + v k^T (from the shared copy), o = G x
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   __syncthreads();
-  if ((lane & 3) == 0) pvec[row] = xr;
+  if ((lane & 1) == 0) pvec[row] = xr;
   __syncthreads();
   const float4 xc = reinterpret_cast<const float4 *>(pvec)[lane];
-  float s[8];
+  float s[16];
 #pragma unroll
-  for (int j = 0; j < 8; j++) {
-    const int rj = 8 * warp + j;
+  for (int j = 0; j < 16; j++) {
+    const int rj = 16 * warp + j;
     float4 gg = reinterpret_cast<const float4 *>(Gs)[rj * 32 + lane];
     const float vr = vvec[rj];
     gg.x = fmaf(g, gg.x, vr * kc.x);
@@ -306,11 +300,11 @@ __global__ void __launch_bounds__(512, 2) mesa_decode128_kernel(DecArgs a) {
     s[j] = fmaf(gg.w, xc.w, fmaf(gg.z, xc.z, fmaf(gg.y, xc.y, gg.x * xc.x)));
   }
   const float o = rowsum(s);
-  if ((lane & 3) == 0) st((TIO *)a.out, (size_t)u * D + row, o);
+  if ((lane & 1) == 0) st((TIO *)a.out, (size_t)u * D + row, o);
   if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
 }
 
-constexpr int kDecode128Smem = (128 * 128 + 3 * 128 + 2 * 16) * sizeof(float);
+constexpr int kDecode128Smem = (128 * 128 + 4 * 128 + 2 * 8) * sizeof(float);
 
 template <int D, typename TIO>
 static int launch_dec_t(const DecArgs &a, cudaStream_t st) {
@@ -320,7 +314,7 @@ static int launch_dec_t(const DecArgs &a, cudaStream_t st) {
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecode128Smem) !=
         cudaSuccess)
       return -1;
-    kfn<<<a.N * a.H, 512, kDecode128Smem, st>>>(a);
+    kfn<<<a.N * a.H, 256, kDecode128Smem, st>>>(a);
   } else {
     mesa_decode_kernel<D, TIO><<<a.N * a.H, 4 * D, 0, st>>>(a);
   }
