@@ -273,32 +273,37 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     return !bad;
   };
   // Z = (W * mrow / sK) o D into the Z operand; returns the row scale.
+  // Warps whose 32-column group lies entirely above the diagonal (every j > every row i
+  // of the quadrant) only write zeros: D_ij = 0 there.
+  const bool z_upper = c0 >= 32 * qd + 32;
   auto build_z = [&](float mrow) -> float {
     const float f = mrow / sK;
     float w[CW];
-    tc::tmem_ld<CW>(tl + COL_W, w);
-    tc::tmem_ld_wait();
     float zmax = 0.0f;
-    if (factored) {
-      const float fr = f * e2r_i;
+    if (!z_upper) {
+      tc::tmem_ld<CW>(tl + COL_W, w);
+      tc::tmem_ld_wait();
+      if (factored) {
+        const float fr = f * e2r_i;
 #pragma unroll
-      for (int g = 0; g < CW / 4; g++) {
-        const float4 ec = reinterpret_cast<const float4 *>(m->e2c + c0)[g];
-        const float e4[4] = {ec.x, ec.y, ec.z, ec.w};
+        for (int g = 0; g < CW / 4; g++) {
+          const float4 ec = reinterpret_cast<const float4 *>(m->e2c + c0)[g];
+          const float e4[4] = {ec.x, ec.y, ec.z, ec.w};
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++) {
-          const int j = c0 + 4 * g + kk;
-          w[4 * g + kk] = (j <= i) ? w[4 * g + kk] * fr * e4[kk] : 0.0f;
-          zmax = fmaxf(zmax, fabsf(w[4 * g + kk]));
+          for (int kk = 0; kk < 4; kk++) {
+            const int j = c0 + 4 * g + kk;
+            w[4 * g + kk] = (j <= i) ? w[4 * g + kk] * fr * e4[kk] : 0.0f;
+            zmax = fmaxf(zmax, fabsf(w[4 * g + kk]));
+          }
         }
-      }
-    } else {
+      } else {
 #pragma unroll
-      for (int kk = 0; kk < CW; kk++) {
-        const int j = c0 + kk;
-        const float dij = (valid && j <= i) ? exp2f(ell2_i - m->ell2[j]) : 0.0f;
-        w[kk] *= f * dij;
-        zmax = fmaxf(zmax, fabsf(w[kk]));
+        for (int kk = 0; kk < CW; kk++) {
+          const int j = c0 + kk;
+          const float dij = (valid && j <= i) ? exp2f(ell2_i - m->ell2[j]) : 0.0f;
+          w[kk] *= f * dij;
+          zmax = fmaxf(zmax, fabsf(w[kk]));
+        }
       }
     }
     // the scratch lies inside the Z operand written next: block-wide barriers
@@ -306,10 +311,16 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     const float inv = 1.0f / zs;
 #pragma unroll
     for (int g = 0; g < NV; g++) {
-      float x8[8];
+      if (z_upper) {
+        const uint32_t off = tc::sw128_offset(i, c0 + 8 * g, TILE);
+        *reinterpret_cast<uint4 *>(Zhi + off) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(Zlo + off) = make_uint4(0, 0, 0, 0);
+      } else {
+        float x8[8];
 #pragma unroll
-      for (int kk = 0; kk < 8; kk++) x8[kk] = w[g * 8 + kk];
-      st8(Zhi, Zlo, i, c0 + 8 * g, x8, inv);
+        for (int kk = 0; kk < 8; kk++) x8[kk] = w[g * 8 + kk];
+        st8(Zhi, Zlo, i, c0 + 8 * g, x8, inv);
+      }
     }
     return zs;
   };
@@ -364,8 +375,8 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     }
     const float sigma = rowred<NG, false>(sg, scr, qd, grp, i);
     const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
-    // r -= alpha AP, x += alpha p   (alpha = 0 leaves a finished row unchanged; the
-    // tensor-memory accesses stay unconditional: they are warp-collective)
+    // r -= alpha AP   (alpha = 0 leaves a finished row unchanged; the tensor-memory
+    // accesses stay unconditional: they are warp-collective)
     float rr[CW];
     float rn = 0.0f, rmax = 0.0f;
     tc::tmem_ld<CW>(tl + COL_R, rr);
@@ -377,7 +388,14 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       rmax = fmaxf(rmax, fabsf(rr[kk]));
     }
     tc::tmem_st<CW>(tl + COL_R, rr);
+    rowred2<NG>(rn, rmax, scr, qd, grp, i);
+    const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
+    // one pass over the old p: x += alpha p and p = r + beta p, re-scaled so that
+    // |p_new| <= max|r| + beta max|p| <= rmax + beta mP  (x's tensor-memory access stays
+    // unconditional; the p operand of a finished row is left as it is)
     {
+      const float mNew = tc::pow2_ceil(rmax + beta * mP);
+      const float inv = 1.0f / mNew;
       float xx[CW];
       tc::tmem_ld<CW>(tl + COL_X, xx);
       tc::tmem_ld_wait();
@@ -386,27 +404,18 @@ __global__ void __launch_bounds__(128 * TPR, 1)
         float p8[8];
         ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
 #pragma unroll
-        for (int kk = 0; kk < 8; kk++) xx[g * 8 + kk] = fmaf(alpha, p8[kk], xx[g * 8 + kk]);
+        for (int kk = 0; kk < 8; kk++) {
+          xx[g * 8 + kk] = fmaf(alpha, p8[kk], xx[g * 8 + kk]);
+          p8[kk] = fmaf(beta, p8[kk], rr[g * 8 + kk]);
+        }
+        if (act) st8(Phi, Plo, i, c0 + 8 * g, p8, inv);
       }
       tc::tmem_st<CW>(tl + COL_X, xx);
-    }
-    rowred2<NG>(rn, rmax, scr, qd, grp, i);
-    const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
-    // p = r + beta p, re-scaled: |p_new| <= max|r| + beta max|p| <= rmax + beta mP
-    if (act) {
-      const float mNew = tc::pow2_ceil(rmax + beta * mP);
-      const float inv = 1.0f / mNew;
-#pragma unroll
-      for (int g = 0; g < NV; g++) {
-        float p8[8];
-        ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) p8[kk] = fmaf(beta, p8[kk], rr[g * 8 + kk]);
-        st8(Phi, Plo, i, c0 + 8 * g, p8, inv);
+      if (act) {
+        mP = mNew;
+        rho = rn;
+        cnt++;
       }
-      mP = mNew;
-      rho = rn;
-      cnt++;
     }
     tc::tmem_st_wait();
   }
