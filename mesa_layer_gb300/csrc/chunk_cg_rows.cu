@@ -119,32 +119,50 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
         y[4 * n4 + 3] = fmaf(ze, sv.w, y[4 * n4 + 3]);
       }
     }
-    for (int j = 0; j < jend; j++) {
-      const float4 *krow = reinterpret_cast<const float4 *>(Kr + j * D);
-      float kv[DC];
-      float dot = 0.0f;
+    // keys in groups of JB: independent dot products per step hide the latency of the quad
+    // shuffles (JB = 2 at d = 64 keeps the key rows in registers without spilling)
+    constexpr int JB = D >= 64 ? 2 : 4;
+    auto load = [&](const float *base, int j, float (&kv)[DC]) {
+      const float4 *rowp = reinterpret_cast<const float4 *>(base + j * D);
 #pragma unroll
       for (int n4 = 0; n4 < DC / 4; n4++) {
-        const float4 t = krow[4 * n4 + part];
+        const float4 t = rowp[4 * n4 + part];
         kv[4 * n4] = t.x;
         kv[4 * n4 + 1] = t.y;
         kv[4 * n4 + 2] = t.z;
         kv[4 * n4 + 3] = t.w;
       }
+    };
+    int j = 0;
+    for (; j + JB <= jend; j += JB) {
+      float kv[JB][DC], dot[JB];
+#pragma unroll
+      for (int b = 0; b < JB; b++) {
+        load(Kr, j + b, kv[b]);
+        dot[b] = 0.0f;
+#pragma unroll
+        for (int n = 0; n < DC; n++) dot[b] = fmaf(z[n], kv[b][n], dot[b]);
+      }
+#pragma unroll
+      for (int b = 0; b < JB; b++) dot[b] += __shfl_xor_sync(0xffffffffu, dot[b], 1);
+#pragma unroll
+      for (int b = 0; b < JB; b++) dot[b] += __shfl_xor_sync(0xffffffffu, dot[b], 2);
+#pragma unroll
+      for (int b = 0; b < JB; b++) {
+        const float wgt = dec(j + b) * dot[b];
+        if (Vr != Kr) load(Vr, j + b, kv[b]);
+#pragma unroll
+        for (int n = 0; n < DC; n++) y[n] = fmaf(wgt, kv[b][n], y[n]);
+      }
+    }
+    for (; j < jend; j++) {
+      float kv[DC];
+      load(Kr, j, kv);
+      float dot = 0.0f;
 #pragma unroll
       for (int n = 0; n < DC; n++) dot = fmaf(z[n], kv[n], dot);
       const float wgt = dec(j) * quad_sum(dot);
-      if (Vr != Kr) {
-        const float4 *vrow = reinterpret_cast<const float4 *>(Vr + j * D);
-#pragma unroll
-        for (int n4 = 0; n4 < DC / 4; n4++) {
-          const float4 t = vrow[4 * n4 + part];
-          kv[4 * n4] = t.x;
-          kv[4 * n4 + 1] = t.y;
-          kv[4 * n4 + 2] = t.z;
-          kv[4 * n4 + 3] = t.w;
-        }
-      }
+      if (Vr != Kr) load(Vr, j, kv);
 #pragma unroll
       for (int n = 0; n < DC; n++) y[n] = fmaf(wgt, kv[n], y[n]);
     }

@@ -86,23 +86,35 @@ __device__ __forceinline__ void rowred2(float &sum, float &mx, float *scr, int q
   quad_bar<NG>(q);
 }
 
-// 8 consecutive values (columns c0..c0+7 of row i) of a hi/lo operand, times mul.
+// 8 consecutive values (columns c0..c0+7 of row i) of a scaled operand (NTERMS = 2: hi + lo),
+// times mul.
+template <int NTERMS>
 __device__ __forceinline__ void ld8(const uint8_t *hi, const uint8_t *lo, int i, int c0, float mul,
                                     float (&o)[8]) {
   const uint32_t off = tc::sw128_offset(i, c0, TILE);
   const uint4 h = *reinterpret_cast<const uint4 *>(hi + off);
-  const uint4 l = *reinterpret_cast<const uint4 *>(lo + off);
   const __half2 *hh = reinterpret_cast<const __half2 *>(&h);
-  const __half2 *ll = reinterpret_cast<const __half2 *>(&l);
+  if constexpr (NTERMS == 2) {
+    const uint4 l = *reinterpret_cast<const uint4 *>(lo + off);
+    const __half2 *ll = reinterpret_cast<const __half2 *>(&l);
 #pragma unroll
-  for (int k = 0; k < 4; k++) {
-    const float2 a = __half22float2(hh[k]), b = __half22float2(ll[k]);
-    o[2 * k] = mul * (a.x + b.x);
-    o[2 * k + 1] = mul * (a.y + b.y);
+    for (int k = 0; k < 4; k++) {
+      const float2 a = __half22float2(hh[k]), b = __half22float2(ll[k]);
+      o[2 * k] = mul * (a.x + b.x);
+      o[2 * k + 1] = mul * (a.y + b.y);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      const float2 a = __half22float2(hh[k]);
+      o[2 * k] = mul * a.x;
+      o[2 * k + 1] = mul * a.y;
+    }
   }
 }
 
-// x * inv_scale = hi + lo (fp16 pairs, packed conversions), stored at row i, cols c0..c0+7.
+// x * inv_scale = hi (+ lo) in fp16 (packed conversions), stored at row i, cols c0..c0+7.
+template <int NTERMS>
 __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, const float (&x)[8],
                                     float inv_scale) {
   __align__(16) __half2 h[4], l[4];
@@ -110,17 +122,19 @@ __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, con
   for (int k = 0; k < 4; k++) {
     const float a = x[2 * k] * inv_scale, b = x[2 * k + 1] * inv_scale;
     h[k] = __floats2half2_rn(a, b);
-    const float2 back = __half22float2(h[k]);
-    l[k] = __floats2half2_rn(a - back.x, b - back.y);
+    if constexpr (NTERMS == 2) {
+      const float2 back = __half22float2(h[k]);
+      l[k] = __floats2half2_rn(a - back.x, b - back.y);
+    }
   }
   const uint32_t off = tc::sw128_offset(i, c0, TILE);
   *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<uint4 *>(h);
-  *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<uint4 *>(l);
+  if constexpr (NTERMS == 2) *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<uint4 *>(l);
 }
 
 }  // namespace
 
-template <int TPR>
+template <int TPR, int NTERMS>
 __global__ void __launch_bounds__(128 * TPR, 1)
     mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, unsigned *status) {
   constexpr int NG = TPR;         // column groups (threads per token row)
@@ -181,7 +195,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     SH = a.H0 + (size_t)u * DH * DH;
     SG = a.G0 + (size_t)u * DH * DH;
   }
-  const float sS = tc::stage_state(SH, Shi, Slo, m->red);
+  const float sS = tc::stage_state(SH, Shi, NTERMS == 2 ? Slo : nullptr, m->red);
   const float sK = tc::stage_rows(k + tokbase * DH, Tv, Ks, m->red);
 
   // CG start: x = 0, r = p = q_i (this thread's CW columns)
@@ -217,7 +231,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       float x8[8];
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) x8[kk] = qa[g * 8 + kk];
-      st8(Phi, Plo, i, c0 + 8 * g, x8, inv);
+      st8<NTERMS>(Phi, Plo, i, c0 + 8 * g, x8, inv);
     }
     tc::tmem_st_wait();
   }
@@ -240,7 +254,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     for (int s = 0; s < 8; s++) {
       const uint64_t kb = tc::kmajor_desc(aK, TILE, s);
       tc::mma_f16(dW, tc::kmajor_desc(aPhi, TILE, s), kb, id_kk, s > 0);
-      tc::mma_f16(dW, tc::kmajor_desc(aPlo, TILE, s), kb, id_kk, true);
+      if (NTERMS == 2) tc::mma_f16(dW, tc::kmajor_desc(aPlo, TILE, s), kb, id_kk, true);
     }
     tc::mma_commit(aBar);
 #pragma unroll 1
@@ -248,8 +262,10 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       const uint64_t ph = tc::kmajor_desc(aPhi, TILE, s), pl = tc::kmajor_desc(aPlo, TILE, s);
       const uint64_t sh = tc::kmajor_desc(aShi, TILE, s), sl = tc::kmajor_desc(aSlo, TILE, s);
       tc::mma_f16(dU, ph, sh, id_kk, s > 0);
-      tc::mma_f16(dU, ph, sl, id_kk, true);
-      tc::mma_f16(dU, pl, sh, id_kk, true);
+      if (NTERMS == 2) {
+        tc::mma_f16(dU, ph, sl, id_kk, true);
+        tc::mma_f16(dU, pl, sh, id_kk, true);
+      }
     }
   };
   // Y (cols 128..255) = Z K, K read as an MN-major operand.
@@ -260,7 +276,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       const uint64_t zh = tc::kmajor_desc(aZhi, TILE, s), zl = tc::kmajor_desc(aZlo, TILE, s);
       const uint64_t kb = tc::mnmajor_desc(aK, TILE, s);
       tc::mma_f16(dY, zh, kb, id_kmn, s > 0);
-      tc::mma_f16(dY, zl, kb, id_kmn, true);
+      if (NTERMS == 2) tc::mma_f16(dY, zl, kb, id_kmn, true);
     }
     tc::mma_commit(aBar);
   };
@@ -314,12 +330,12 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       if (z_upper) {
         const uint32_t off = tc::sw128_offset(i, c0 + 8 * g, TILE);
         *reinterpret_cast<uint4 *>(Zhi + off) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(Zlo + off) = make_uint4(0, 0, 0, 0);
+        if (NTERMS == 2) *reinterpret_cast<uint4 *>(Zlo + off) = make_uint4(0, 0, 0, 0);
       } else {
         float x8[8];
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) x8[kk] = w[g * 8 + kk];
-        st8(Zhi, Zlo, i, c0 + 8 * g, x8, inv);
+        st8<NTERMS>(Zhi, Zlo, i, c0 + 8 * g, x8, inv);
       }
     }
     return zs;
@@ -361,7 +377,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
 #pragma unroll
       for (int g = 0; g < NV; g++) {
         float p8[8];
-        ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
+        ld8<NTERMS>(Phi, Plo, i, c0 + 8 * g, mP, p8);
         const float4 l0 = reinterpret_cast<const float4 *>(m->lam + c0 + 8 * g)[0];
         const float4 l1 = reinterpret_cast<const float4 *>(m->lam + c0 + 8 * g)[1];
         const float l8[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
@@ -402,13 +418,13 @@ __global__ void __launch_bounds__(128 * TPR, 1)
 #pragma unroll
       for (int g = 0; g < NV; g++) {
         float p8[8];
-        ld8(Phi, Plo, i, c0 + 8 * g, mP, p8);
+        ld8<NTERMS>(Phi, Plo, i, c0 + 8 * g, mP, p8);
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) {
           xx[g * 8 + kk] = fmaf(alpha, p8[kk], xx[g * 8 + kk]);
           p8[kk] = fmaf(beta, p8[kk], rr[g * 8 + kk]);
         }
-        if (act) st8(Phi, Plo, i, c0 + 8 * g, p8, inv);
+        if (act) st8<NTERMS>(Phi, Plo, i, c0 + 8 * g, p8, inv);
       }
       tc::tmem_st<CW>(tl + COL_X, xx);
       if (act) {
@@ -435,9 +451,9 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       float x8[8];
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) x8[kk] = xx[g * 8 + kk];
-      st8(Phi, Plo, i, c0 + 8 * g, x8, inv);
+      st8<NTERMS>(Phi, Plo, i, c0 + 8 * g, x8, inv);
     }
-    const float sG = tc::stage_state(SG, Shi, Slo, m->red);
+    const float sG = tc::stage_state(SG, Shi, NTERMS == 2 ? Slo : nullptr, m->red);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -486,13 +502,19 @@ __global__ void __launch_bounds__(128 * TPR, 1)
 #define MESA_TC_THREADS_PER_ROW 4
 #endif
 constexpr int kTcThreadsPerRow = MESA_TC_THREADS_PER_ROW;
+// fp16 terms per staged operand: 2 (hi + lo, ~22 significant bits, 7 MMAs per CG step) or
+// 1 (11 bits, 3 MMAs per CG step).
+#ifndef MESA_TC_TERMS
+#define MESA_TC_TERMS 2
+#endif
+static_assert(MESA_TC_TERMS == 1 || MESA_TC_TERMS == 2, "1 or 2 fp16 terms");
 static_assert(kTcThreadsPerRow == 4 || kTcThreadsPerRow == 8, "4 or 8 threads per row");
 
 int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status,
                        cudaStream_t st) {
   const int U = a.B * a.H;
   const int NC = (a.T + TILE - 1) / TILE;
-  auto kfn = mesa_cg_tc_kernel<kTcThreadsPerRow>;
+  auto kfn = mesa_cg_tc_kernel<kTcThreadsPerRow, MESA_TC_TERMS>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC) !=
       cudaSuccess)
     return -1;

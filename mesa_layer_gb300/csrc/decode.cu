@@ -304,159 +304,15 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
   if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
 }
 
-// d = 128, H in shared memory instead of registers (same mapping, update, CG and readout
-// as mesa_decode128_kernel).  With ~40 registers and 66 KB of shared memory per unit, three
-// units run on one SM, so more of every SM's time overlaps HBM traffic; the matrix-vector
-// product reads the unit's H from shared memory (16 x 16-byte loads per thread and step), and
-// G is read straight from HBM at the readout.
-template <typename TIO>
-__global__ void __launch_bounds__(256, 3) mesa_decode128s_kernel(DecArgs a) {
-  constexpr int D = 128, NW = 8;
-  const int u = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = 16 * warp + (lane >> 1);
-  extern __shared__ __align__(16) float dsm[];
-  float4 *Hs = reinterpret_cast<float4 *>(dsm);  // [128][32] float4
-  float *kvec = dsm + D * D, *vvec = kvec + D, *pvec = vvec + D, *rvec = pvec + D;
-  float *red = rvec + D;                           // [2][NW]
-
-  float4 *Hw = reinterpret_cast<float4 *>(a.Hs + (size_t)u * D * D);
-  const float4 *Gg = reinterpret_cast<const float4 *>(a.Gs + (size_t)u * D * D);
-  float4 *Gw = reinterpret_cast<float4 *>(a.Gs + (size_t)u * D * D);
-  {
-    const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(Hs);
-#pragma unroll
-    for (int j = 0; j < 16; j++) {
-      const int e = (16 * warp + j) * 32 + lane;  // this thread's own float4s
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sbase + 16 * e), "l"(Hw + e)
-                   : "memory");
-    }
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-  }
-  const TIO *q = (const TIO *)a.q, *k = (const TIO *)a.k, *v = (const TIO *)a.v;
-  if (threadIdx.x < D) {
-    kvec[threadIdx.x] = ld(k, (size_t)u * D + threadIdx.x);
-    vvec[threadIdx.x] = ld(v, (size_t)u * D + threadIdx.x);
-    pvec[threadIdx.x] = ld(q, (size_t)u * D + threadIdx.x);
-  }
-  const float g = a.gamma[u];
-  const float lam_r = a.lambda[(size_t)(u % a.H) * D + row];
-  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-  __syncthreads();
-
-  // H <- gamma H + k k^T on this thread's own float4s (in shared memory and in HBM)
-  const float4 kc = reinterpret_cast<const float4 *>(kvec)[lane];
-#pragma unroll
-  for (int j = 0; j < 16; j++) {
-    const int e = (16 * warp + j) * 32 + lane;
-    const float kr = kvec[16 * warp + j];
-    float4 h = Hs[e];
-    h.x = fmaf(g, h.x, kr * kc.x);
-    h.y = fmaf(g, h.y, kr * kc.y);
-    h.z = fmaf(g, h.z, kr * kc.z);
-    h.w = fmaf(g, h.w, kr * kc.w);
-    Hs[e] = h;
-    Hw[e] = h;
-  }
-
-  auto rowsum = [&](float (&s)[16]) -> float {
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
-    float t8[8], t4[4], t2[2];
-#pragma unroll
-    for (int j = 0; j < 8; j++)
-      t8[j] = (b4 ? s[j + 8] : s[j]) + __shfl_xor_sync(0xffffffffu, b4 ? s[j] : s[j + 8], 16);
-#pragma unroll
-    for (int j = 0; j < 4; j++)
-      t4[j] = (b3 ? t8[j + 4] : t8[j]) + __shfl_xor_sync(0xffffffffu, b3 ? t8[j] : t8[j + 4], 8);
-#pragma unroll
-    for (int j = 0; j < 2; j++)
-      t2[j] = (b2 ? t4[j + 2] : t4[j]) + __shfl_xor_sync(0xffffffffu, b2 ? t4[j] : t4[j + 2], 4);
-    float t = (b1 ? t2[1] : t2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? t2[0] : t2[1], 2);
-    return t + __shfl_xor_sync(0xffffffffu, t, 1);
-  };
-  auto block_rows_sum = [&](float val, int buf) -> float {
-    val += __shfl_xor_sync(0xffffffffu, val, 2);
-    val += __shfl_xor_sync(0xffffffffu, val, 4);
-    val += __shfl_xor_sync(0xffffffffu, val, 8);
-    val += __shfl_xor_sync(0xffffffffu, val, 16);
-    if (lane == 0) red[buf * NW + warp] = val;
-    __syncthreads();
-    const float4 a0 = reinterpret_cast<const float4 *>(red + buf * NW)[0];
-    const float4 a1 = reinterpret_cast<const float4 *>(red + buf * NW)[1];
-    return ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
-  };
-
-  float xr = 0.0f, rr = pvec[row], pr = rr;
-  float4 pc = reinterpret_cast<const float4 *>(pvec)[lane];
-  float rho = block_rows_sum(rr * rr, 0);
-  const float nq = sqrtf(rho);
-  const bool dynamic = a.cg_tol > 0.0f;
-  int it = 0;
-  for (; it < a.cg_iters; it++) {
-    if (dynamic && sqrtf(rho) <= a.cg_tol * nq) break;
-    float s[16];
-#pragma unroll
-    for (int j = 0; j < 16; j++) {
-      const float4 h = Hs[(16 * warp + j) * 32 + lane];
-      s[j] = fmaf(h.w, pc.w, fmaf(h.z, pc.z, fmaf(h.y, pc.y, h.x * pc.x)));
-    }
-    const float w = fmaf(lam_r, pr, rowsum(s));
-    const float sigma = block_rows_sum(pr * w, 1);
-    const float alpha = (sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
-    xr = fmaf(alpha, pr, xr);
-    rr = fmaf(-alpha, w, rr);
-    if ((lane & 1) == 0) rvec[row] = rr;
-    const float rn = block_rows_sum(rr * rr, 0);
-    const float beta = rho > 0.0f ? rn / rho : 0.0f;
-    pr = fmaf(beta, pr, rr);
-    const float4 rc = reinterpret_cast<const float4 *>(rvec)[lane];
-    pc.x = fmaf(beta, pc.x, rc.x);
-    pc.y = fmaf(beta, pc.y, rc.y);
-    pc.z = fmaf(beta, pc.z, rc.z);
-    pc.w = fmaf(beta, pc.w, rc.w);
-    rho = rn;
-  }
-
-  // readout: G <- gamma G + v k^T (read from HBM here), o = G x
-  __syncthreads();
-  if ((lane & 1) == 0) pvec[row] = xr;
-  __syncthreads();
-  const float4 xc = reinterpret_cast<const float4 *>(pvec)[lane];
-  float s[16];
-  float4 gg[16];
-#pragma unroll
-  for (int j = 0; j < 16; j++) gg[j] = Gg[(16 * warp + j) * 32 + lane];
-#pragma unroll
-  for (int j = 0; j < 16; j++) {
-    const int rj = 16 * warp + j;
-    const float vr = vvec[rj];
-    gg[j].x = fmaf(g, gg[j].x, vr * kc.x);
-    gg[j].y = fmaf(g, gg[j].y, vr * kc.y);
-    gg[j].z = fmaf(g, gg[j].z, vr * kc.z);
-    gg[j].w = fmaf(g, gg[j].w, vr * kc.w);
-    Gw[rj * 32 + lane] = gg[j];
-    s[j] = fmaf(gg[j].w, xc.w, fmaf(gg[j].z, xc.z, fmaf(gg[j].y, xc.y, gg[j].x * xc.x)));
-  }
-  const float o = rowsum(s);
-  if ((lane & 1) == 0) st((TIO *)a.out, (size_t)u * D + row, o);
-  if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
-}
-
+// (A variant with H in shared memory and three units per SM measured slower: 0.287 ms
+// against 0.256 ms per step of the 256 x 16 decode workload.)
 constexpr int kDecode128Smem = (128 * 128 + 4 * 128 + 2 * 8) * sizeof(float);
-// Which d = 128 variant runs: H in shared memory (3 units per SM) or in registers (2).
-#ifndef MESA_DECODE128_H_IN_SMEM
-#define MESA_DECODE128_H_IN_SMEM 1
-#endif
 
 template <int D, typename TIO>
 static int launch_dec_t(const DecArgs &a, cudaStream_t st) {
   timing_mark_begin(K_DECODE, st);
   if constexpr (D == 128) {
-#if MESA_DECODE128_H_IN_SMEM
-    auto kfn = mesa_decode128s_kernel<TIO>;
-#else
     auto kfn = mesa_decode128_kernel<TIO>;
-#endif
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecode128Smem) !=
         cudaSuccess)
       return -1;

@@ -36,7 +36,7 @@ __device__ __forceinline__ float ld_pair(const uint8_t *hi, const uint8_t *lo, u
 }
 
 // Stage a fp32 128x128 matrix (row-major, or zero when src == nullptr) as scaled hi/lo fp16
-// operands.  Returns the scale s (operand = matrix * s).
+// operands (hi only when lo == nullptr).  Returns the scale s (operand = matrix * s).
 __device__ __forceinline__ float stage_state(const float *src, uint8_t *hi, uint8_t *lo, float *red) {
   const int t = threadIdx.x;
   float mx = 0.0f;
@@ -57,7 +57,7 @@ __device__ __forceinline__ float stage_state(const float *src, uint8_t *hi, uint
       split_f16(xs[k], h, l);
       const uint32_t off = sw128_offset(r, c + k, TILE);
       st_half(hi, off, h);
-      st_half(lo, off, l);
+      if (lo) st_half(lo, off, l);
     }
   }
   return s;
