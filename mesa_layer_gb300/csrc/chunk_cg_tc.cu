@@ -503,7 +503,10 @@ __global__ void __launch_bounds__(128 * TPR, 1)
 #endif
 constexpr int kTcThreadsPerRow = MESA_TC_THREADS_PER_ROW;
 // fp16 terms per staged operand: 2 (hi + lo, ~22 significant bits, 7 MMAs per CG step) or
-// 1 (11 bits, 3 MMAs per CG step).
+// 1 (11 bits, 3 MMAs per CG step).  Measured on the bf16 workloads: 1 term makes this kernel
+// 23 % faster (2.56 against 3.31 ms at B=8 H=16 T=4096) but the dynamic stopping rule then
+// agrees with the fp64 iteration counts on only 92 % of tokens (tol 1e-3), against 99.9 % with
+// 2 terms; 2 is the default.
 #ifndef MESA_TC_TERMS
 #define MESA_TC_TERMS 2
 #endif
