@@ -18,15 +18,25 @@ bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 constexpr size_t kStatusBytes = 256;
 
-// Workspace: [status word | log-decays | S^H states | S^G states].  Sized for `chunk`,
-// which is <= 128, so it also covers the tensor-core path's 128-token chunks.
+// Workspace: [status word | log-decays | S^H states | S^G states | (d = 128) segment
+// log-decays Lc | segment carries].  Sized for `chunk`, which is <= 128, so it also covers
+// the tensor-core path's 128-token chunks.
 size_t workspace_parts(int B, int H, int T, int dk, int dv, int chunk, size_t *off) {
   const size_t U = (size_t)B * H;
   const size_t NC = (size_t)(T + chunk - 1) / chunk;
   off[0] = kStatusBytes;
   off[1] = off[0] + align256(U * T * sizeof(float));
   off[2] = off[1] + align256(U * NC * dk * dk * sizeof(float));
-  return off[2] + align256(U * NC * dv * dk * sizeof(float));
+  off[3] = off[2] + align256(U * NC * dv * dk * sizeof(float));
+  size_t end = off[3];
+  off[4] = end;
+  if (dk == 128 && dv == 128) {
+    const int NC128 = (T + 127) / 128;
+    const size_t nseg = (size_t)mesa::tc_segments((int)U, NC128);
+    off[4] = off[3] + align256(U * NC128 * sizeof(float));
+    end = off[4] + align256(U * nseg * 2 * dk * dk * sizeof(float));
+  }
+  return end;
 }
 
 // The tensor-core path covers bf16 inputs with dk = dv = 128 (16-byte aligned operands).
@@ -121,7 +131,7 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_CG_SIMT: return "mesa_cg_simt_kernel";
     case mesa::K_DECODE: return "mesa_decode_kernel";
     case mesa::K_CG_TC: return "mesa_cg_tc_kernel";
-    case mesa::K_DELTA_TC: return "mesa_delta_tc_kernel";
+    case mesa::K_DELTA_TC: return "mesa_states_tc_kernel";
     case mesa::K_CG_ROWS: return "mesa_cg_rows_kernel";
   }
   return nullptr;
@@ -157,7 +167,7 @@ const char *mesa_status_string(int s) {
 
 size_t mesa_forward_workspace_size(int B, int H, int T, int dk, int dv, int chunk) {
   if (B < 0 || H < 0 || T < 0 || !dim_ok(dk) || dv != dk || !chunk_ok(chunk)) return 0;
-  size_t off[3];
+  size_t off[5];
   return workspace_parts(B, H, T, dk, dv, chunk, off);
 }
 
@@ -188,7 +198,7 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
     return MESA_OK;
   }
   if (!q || !k || !v || !gamma || !out) return MESA_ERR_INVALID_ARG;
-  size_t off[3];
+  size_t off[5];
   const size_t need = workspace_parts(B, H, T, dk, dv, chunk, off);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return MESA_ERR_WORKSPACE;
 
@@ -197,7 +207,9 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
                   tc ? 128 : chunk, out, iters_used, H0, G0, H_final, G_final};
   char *w = (char *)workspace;
   unsigned *status = (unsigned *)w;
-  mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2])};
+  mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2]),
+                        (float *)(w + off[3]), (float *)(w + off[4]),
+                        tc ? mesa::tc_segments((int)U, (T + 127) / 128) : 1};
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
   if (mesa::launch_chunk_states(a, ws, tc ? status : nullptr, stream) != 0) return MESA_ERR_CUDA;
   const int rc = tc ? mesa::launch_chunk_cg_tc(a, ws, status, stream)

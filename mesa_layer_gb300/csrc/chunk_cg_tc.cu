@@ -187,15 +187,23 @@ __global__ void __launch_bounds__(128 * TPR, 1)
   const float el_i = valid ? exp2f(ell2_i) : 0.0f;
   const float e2r_i = valid ? el_i : 0.0f;  // 2^{l2_i}; invalid rows get D = 0
 
-  const float *SH = nullptr, *SG = nullptr;
+  // S_{c-1}: the segment-local state plus exp(Lc) times the carry into its segment
+  const float *SH = nullptr, *SG = nullptr, *CH = nullptr, *CG = nullptr;
+  float cf = 0.0f;
   if (c > 0) {
     SH = ws.SH + ((size_t)u * NC + (c - 1)) * DH * DH;
     SG = ws.SG + ((size_t)u * NC + (c - 1)) * DH * DH;
+    const int seg = (c - 1) / ((NC + ws.nseg - 1) / ws.nseg);
+    if (seg > 0) {
+      CH = ws.carry + ((size_t)u * ws.nseg + seg) * 2 * DH * DH;
+      CG = CH + DH * DH;
+      cf = expf(ws.Lc[(size_t)u * NC + c - 1]);
+    }
   } else if (a.H0) {
     SH = a.H0 + (size_t)u * DH * DH;
     SG = a.G0 + (size_t)u * DH * DH;
   }
-  const float sS = tc::stage_state(SH, Shi, NTERMS == 2 ? Slo : nullptr, m->red);
+  const float sS = tc::stage_state(SH, CH, cf, Shi, NTERMS == 2 ? Slo : nullptr, m->red);
   const float sK = tc::stage_rows(k + tokbase * DH, Tv, Ks, m->red);
 
   // CG start: x = 0, r = p = q_i (this thread's CW columns)
@@ -453,7 +461,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       for (int kk = 0; kk < 8; kk++) x8[kk] = xx[g * 8 + kk];
       st8<NTERMS>(Phi, Plo, i, c0 + 8 * g, x8, inv);
     }
-    const float sG = tc::stage_state(SG, Shi, NTERMS == 2 ? Slo : nullptr, m->red);
+    const float sG = tc::stage_state(SG, CG, cf, Shi, NTERMS == 2 ? Slo : nullptr, m->red);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();

@@ -121,8 +121,8 @@ static int launch_states_t(const FwdArgs &a, const FwdWorkspace &ws, unsigned *t
   timing_mark_begin(K_ELL, st);
   mesa_ell_kernel<<<dim3(NC, U), 128, 0, st>>>(a.gamma, ws.ell, a.T, a.chunk);
   timing_mark_end(K_ELL, st);
-  if (tc_status) {
-    if (launch_delta_tc(a, ws, tc_status, st) != 0) return -1;
+  if (tc_status) {  // chunk sums and the chunk-level scan on the tensor cores
+    return launch_states_tc(a, ws, tc_status, st);
   } else {
     const size_t smem = (size_t)(256 * D + 128) * sizeof(float);
     auto kd = mesa_delta_kernel<D, TIO>;

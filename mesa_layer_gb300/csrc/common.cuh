@@ -40,9 +40,27 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // Workspace carve-up of the chunked forward (all fp32, each section 256-byte aligned).
 struct FwdWorkspace {
-  float *ell;  // [U, T]        log-decay within the chunk, l_i = sum_{s<=i} log gamma_s
-  float *SH;   // [U, NC, dk, dk] states after each chunk
-  float *SG;   // [U, NC, dv, dk]
+  float *ell;    // [U, T]        log-decay within the chunk, l_i = sum_{s<=i} log gamma_s
+  float *SH;     // [U, NC, dk, dk] states after each chunk
+  float *SG;     // [U, NC, dv, dk]
+  // tensor-core path only: the chunk sequence of a unit is split into nseg segments whose
+  // states are built independently from zero (segment 0 from the initial state); SH/SG
+  // then hold segment-local states, Lc [U, NC] the log of the product of chunk decays from
+  // the segment start through each chunk, and carry [U, nseg, 2, d, d] the global state
+  // before each segment (entry 0 unused), so that
+  //     S_c = S_local_c + exp(Lc[c]) * carry[segment of c].
+  float *Lc;
+  float *carry;
+  int nseg;
 };
+
+// Segments per unit for the tensor-core state build: enough CTAs to fill the GPU when
+// there are few (batch, head) units, one segment when there are many.
+inline int tc_segments(int U, int NC) {
+  int s = U > 0 ? 256 / U : 1;
+  if (s > 16) s = 16;
+  if (s > NC) s = NC;
+  return s < 1 ? 1 : s;
+}
 
 }  // namespace mesa

@@ -1,13 +1,17 @@
-// delta_tc.cu -- chunk-local state sums on the tensor cores (bf16 inputs, d = 128).
+// delta_tc.cu -- chunk-boundary states on the tensor cores (bf16 inputs, d = 128).
 //
 // MesaNet technical summary (gist.science/pt/paper/2506.05233), "Paralelizacao": the states
-// H_t, G_t carry the past from chunk to chunk.  For a 128-token chunk with in-chunk
-// log-decays l_j and w_j = e^{l_last - l_j} the chunk adds
-//     Delta^H = sum_j w_j k_j k_j^T,      Delta^G = sum_j w_j v_j k_j^T
-// to the decayed previous state.  Here each is one 128x128x128 MMA over the chunk's tokens
-// j: A = (w x)^T read MN-major from the token-major tile (x = k or v, split hi + lo fp16),
-// B = K read MN-major (fp16, exact after a power-of-two scale).  The chunk-level prefix
-// scan that turns the sums into states runs afterwards (chunk_state.cu).
+// H_t, G_t carry the past from chunk to chunk.  For a 128-token chunk c with in-chunk
+// log-decays l_j, a_c = e^{l_last} and w_j = e^{l_last - l_j},
+//     S^H_c = a_c S^H_{c-1} + sum_j w_j k_j k_j^T,     S^G_c = a_c S^G_{c-1} + sum_j w_j v_j k_j^T.
+// mesa_states_tc_kernel walks the chunks of one segment of one (batch, head) unit in order and
+// keeps S^H, S^G as fp32 accumulators in tensor memory: per chunk it rescales them by a_c (and
+// by the change of operand scale), adds the chunk's sums with two 128x128x128 MMAs each
+// (A = (w x)^T read MN-major from the token-major tile, x = k or v, split hi + lo fp16;
+// B = K read MN-major, fp16, exact after a power-of-two scale), and writes the state.
+// Segment 0 starts from the initial state, later segments from zero; mesa_carry_tc_kernel then
+// chains the segments (carry[s] = global state before segment s) and writes the final state,
+// and the CG kernel adds exp(Lc) carry when it loads a state.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -18,7 +22,7 @@ namespace mesa {
 namespace {
 constexpr uint32_t DT_MAT = 128 * 128 * 2;
 constexpr uint32_t DT_SMEM = 3 * DT_MAT + 1024 + 1024;
-struct DeltaMisc {
+struct StateMisc {
   float w[128];
   float red[16];
   uint64_t mbar;
@@ -26,101 +30,175 @@ struct DeltaMisc {
 };
 }  // namespace
 
-__global__ void __launch_bounds__(512) mesa_delta_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC,
-                                                            unsigned *status) {
+__global__ void __launch_bounds__(512) mesa_states_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC,
+                                                             unsigned *status) {
   using tc::DH;
   using tc::TILE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t *Ks = sm, *Ahi = sm + DT_MAT, *Alo = sm + 2 * DT_MAT;
-  DeltaMisc *m = reinterpret_cast<DeltaMisc *>(sm + 3 * DT_MAT);
+  StateMisc *m = reinterpret_cast<StateMisc *>(sm + 3 * DT_MAT);
   const uint32_t aK = tc::smem_u32(Ks), aAhi = tc::smem_u32(Ahi), aAlo = tc::smem_u32(Alo);
   const uint32_t aBar = tc::smem_u32(&m->mbar);
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int c = blockIdx.x, u = blockIdx.y;
-  const int T = a.T, t0 = c * TILE;
-  const int Tv = min(TILE, T - t0);
-  const size_t tokbase = (size_t)u * T + t0;
-  const __nv_bfloat16 *k = (const __nv_bfloat16 *)a.k + tokbase * DH;
-  const __nv_bfloat16 *v = (const __nv_bfloat16 *)a.v + tokbase * DH;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seg = blockIdx.x, u = blockIdx.y;
+  const int T = a.T;
+  const int per = (NC + ws.nseg - 1) / ws.nseg;
+  const int c_begin = seg * per, c_end = min(NC, c_begin + per);
+  if (c_begin >= c_end) return;
+  // accumulator access: lane quadrant = rows, 4 groups of 32 columns per state
+  const int row = 32 * (warp & 3) + lane, cg = warp >> 2;
 
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 256);
   if (tid == 0) tc::mbar_init(aBar, 1);
-  const float lend = ws.ell[tokbase + Tv - 1];
-  if (tid < TILE) m->w[tid] = tid < Tv ? expf(lend - ws.ell[tokbase + tid]) : 0.0f;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tbase = m->tmem_base;
-  const float sK = tc::stage_rows(k, Tv, Ks, m->red);
-  const float sAH = tc::stage_weighted_rows(k, m->w, Tv, Ahi, Alo, m->red);
+  const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * cg;  // + 128 for G
   const uint32_t id = tc::idesc_f16(TILE, DH, true, true);
   uint32_t phase = 0;
-  auto issue = [&](uint32_t col) {
+  bool ok = true;
+  float sigH = 1.0f, sigG = 1.0f, Lsum = 0.0f;
+
+  auto issue = [&](uint32_t col, bool acc0) {
 #pragma unroll 1
     for (int s = 0; s < 8; s++) {
       const uint64_t kb = tc::mnmajor_desc(aK, TILE, s);
-      tc::mma_f16(tbase + col, tc::mnmajor_desc(aAhi, TILE, s), kb, id, s > 0);
+      tc::mma_f16(tbase + col, tc::mnmajor_desc(aAhi, TILE, s), kb, id, s > 0 || acc0);
       tc::mma_f16(tbase + col, tc::mnmajor_desc(aAlo, TILE, s), kb, id, true);
     }
     tc::mma_commit(aBar);
   };
   auto wait = [&]() -> bool {
-    const bool ok = tc::mbar_wait(aBar, phase);
+    const bool done = tc::mbar_wait(aBar, phase);
     phase ^= 1;
     tc::fence_after_sync();
-    const int bad = __syncthreads_or(!ok);
+    const int bad = __syncthreads_or(!done);
     if (bad && tid == 0) atomicOr(status, tc::kErrMmaTimeout);
     return !bad;
   };
-  tc::fence_smem_to_async();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  if (tid == 0) issue(0);
-  bool ok = wait();
-  float sAG = 1.0f;
-  if (ok) {
-    sAG = tc::stage_weighted_rows(v, m->w, Tv, Ahi, Alo, m->red);
+  // Accumulator columns [col, col+128): multiply this thread's 32 values by f, or (first
+  // chunk) load f * init (init == nullptr: nothing to load, the first MMA overwrites).
+  auto rescale = [&](uint32_t col, float f, bool first, const float *init) {
+    float v[32];
+    if (first) {
+      if (!init) return;
+      const float4 *src = reinterpret_cast<const float4 *>(init + ((size_t)u * DH + row) * DH + 32 * cg);
+#pragma unroll
+      for (int g = 0; g < 8; g++) {
+        const float4 x = src[g];
+        v[4 * g] = x.x * f;
+        v[4 * g + 1] = x.y * f;
+        v[4 * g + 2] = x.z * f;
+        v[4 * g + 3] = x.w * f;
+      }
+    } else {
+      tc::tmem_ld32(tl + col, v);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int kk = 0; kk < 32; kk++) v[kk] *= f;
+    }
+    tc::tmem_st32(tl + col, v);
+    tc::tmem_st_wait();
+  };
+
+  for (int c = c_begin; c < c_end && ok; c++) {
+    const bool first = c == c_begin;
+    const float *H0 = (seg == 0) ? a.H0 : nullptr;
+    const float *G0 = (seg == 0) ? a.G0 : nullptr;
+    const int t0 = c * TILE, Tv = min(TILE, T - t0);
+    const size_t tokbase = (size_t)u * T + t0;
+    const __nv_bfloat16 *k = (const __nv_bfloat16 *)a.k + tokbase * DH;
+    const __nv_bfloat16 *v = (const __nv_bfloat16 *)a.v + tokbase * DH;
+    const float lend = ws.ell[tokbase + Tv - 1];
+    const float ac = expf(lend);
+    if (tid < TILE) m->w[tid] = tid < Tv ? expf(lend - ws.ell[tokbase + tid]) : 0.0f;
+    __syncthreads();
+    const float sK = tc::stage_rows(k, Tv, Ks, m->red);
+    const float sAH = tc::stage_weighted_rows(k, m->w, Tv, Ahi, Alo, m->red);
+    const float nsigH = sAH * sK;
+    rescale(0, first ? ac * nsigH : ac * nsigH / sigH, first, H0);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (tid == 0) issue(128);
+    if (tid == 0) issue(0, !first || H0 != nullptr);
     ok = wait();
-  }
-  if (ok) {
-    // warp w: rows 32 (w % 4) .. +31 (its lane quadrant), columns 32 (w / 4) .. +31
-    const int row = 32 * (warp & 3) + (tid & 31), cg = warp >> 2;
-    const uint32_t tl = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * cg;
-    float *SH = ws.SH + (((size_t)u * NC + c) * DH + row) * DH + 32 * cg;
-    float *SG = ws.SG + (((size_t)u * NC + c) * DH + row) * DH + 32 * cg;
+    if (!ok) break;
+    const float sAG = tc::stage_weighted_rows(v, m->w, Tv, Ahi, Alo, m->red);
+    const float nsigG = sAG * sK;
+    rescale(128, first ? ac * nsigG : ac * nsigG / sigG, first, G0);
+    tc::fence_smem_to_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (tid == 0) issue(128, !first || G0 != nullptr);
+    ok = wait();
+    if (!ok) break;
+    sigH = nsigH;
+    sigG = nsigG;
+    Lsum += lend;
+    // segment-local state after chunk c
 #pragma unroll
     for (int half = 0; half < 2; half++) {
-      const float f = 1.0f / ((half ? sAG : sAH) * sK);
-      float4 *dst = reinterpret_cast<float4 *>(half ? SG : SH);
+      const float f = 1.0f / (half ? sigG : sigH);
+      float *dst = (half ? ws.SG : ws.SH) + (((size_t)u * NC + c) * DH + row) * DH + 32 * cg;
       float x[32];
       tc::tmem_ld32(tl + half * 128, x);
       tc::tmem_ld_wait();
 #pragma unroll
       for (int g = 0; g < 8; g++)
-        dst[g] = make_float4(x[4 * g] * f, x[4 * g + 1] * f, x[4 * g + 2] * f, x[4 * g + 3] * f);
+        reinterpret_cast<float4 *>(dst)[g] =
+            make_float4(x[4 * g] * f, x[4 * g + 1] * f, x[4 * g + 2] * f, x[4 * g + 3] * f);
     }
+    if (tid == 0) ws.Lc[(size_t)u * NC + c] = Lsum;
   }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_free(tbase, 256);
 }
 
-int launch_delta_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st) {
+// grid (ceil(2 D^2 / 256), U), block 256: entry e < D^2 of S^H, else of S^G.
+// carry[s] = S_global(last chunk of segment s-1) = S_local + exp(Lc) carry[s-1] (carry[0] = 0,
+// segment 0 having started from the initial state); the final state likewise.
+__global__ void __launch_bounds__(256) mesa_carry_tc_kernel(FwdWorkspace ws, int NC, float *Hf,
+                                                            float *Gf) {
+  constexpr int D = 128;
+  const int u = blockIdx.y;
+  int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= 2 * D * D) return;
+  const bool isG = e >= D * D;
+  if (isG) e -= D * D;
+  const int per = (NC + ws.nseg - 1) / ws.nseg;
+  const float *S = (isG ? ws.SG : ws.SH) + (size_t)u * NC * D * D + e;
+  float *car = ws.carry + ((size_t)u * ws.nseg * 2 + (isG ? 1 : 0)) * D * D + e;
+  float carry = 0.0f;
+  int s = 0;
+  for (; s + 1 < ws.nseg && (s + 1) * per < NC; s++) {
+    const int last = (s + 1) * per - 1;
+    carry = S[(size_t)last * D * D] + expf(ws.Lc[(size_t)u * NC + last]) * carry;
+    car[(size_t)(s + 1) * 2 * D * D] = carry;
+  }
+  float *F = isG ? Gf : Hf;
+  if (F) F[(size_t)u * D * D + e] = S[(size_t)(NC - 1) * D * D] + expf(ws.Lc[(size_t)u * NC + NC - 1]) * carry;
+}
+
+int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st) {
   const int U = a.B * a.H;
   const int NC = (a.T + 127) / 128;
-  if (cudaFuncSetAttribute(mesa_delta_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(mesa_states_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)DT_SMEM) != cudaSuccess)
     return -1;
   timing_mark_begin(K_DELTA_TC, st);
-  mesa_delta_tc_kernel<<<dim3(NC, U), 512, DT_SMEM, st>>>(a, ws, NC, status);
+  mesa_states_tc_kernel<<<dim3(ws.nseg, U), 512, DT_SMEM, st>>>(a, ws, NC, status);
   timing_mark_end(K_DELTA_TC, st);
+  if (ws.nseg > 1 || a.H_final) {
+    timing_mark_begin(K_SCAN, st);
+    mesa_carry_tc_kernel<<<dim3((2 * 128 * 128 + 255) / 256, U), 256, 0, st>>>(ws, NC, a.H_final,
+                                                                                a.G_final);
+    timing_mark_end(K_SCAN, st);
+  }
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

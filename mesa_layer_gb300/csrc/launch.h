@@ -54,8 +54,9 @@ int launch_chunk_cg_rows(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t 
 int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st);
 int launch_tc_selftest(const float *A, const float *B, float *C1, float *C2, float *C3,
                        unsigned *status, cudaStream_t st);
-// Chunk-local state sums on the tensor cores (bf16 inputs, d = 128, 128-token chunks).
-int launch_delta_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st);
+// Chunk-boundary states on the tensor cores (bf16 inputs, d = 128, 128-token chunks):
+// segment-local states, segment carries and the final state (see FwdWorkspace).
+int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st);
 int launch_decode(const DecArgs &a, cudaStream_t st);
 
 }  // namespace mesa

@@ -35,20 +35,33 @@ __device__ __forceinline__ float ld_pair(const uint8_t *hi, const uint8_t *lo, u
          __half2float(*reinterpret_cast<const __half *>(lo + off));
 }
 
-// Stage a fp32 128x128 matrix (row-major, or zero when src == nullptr) as scaled hi/lo fp16
-// operands (hi only when lo == nullptr).  Returns the scale s (operand = matrix * s).
-__device__ __forceinline__ float stage_state(const float *src, uint8_t *hi, uint8_t *lo, float *red) {
+// Stage a fp32 128x128 matrix src + f * add (row-major; src == nullptr: zero, add ==
+// nullptr: nothing added) as scaled hi/lo fp16 operands (hi only when lo == nullptr).
+// Returns the scale s (operand = matrix * s).
+__device__ __forceinline__ float stage_state(const float *src, const float *add, float f, uint8_t *hi,
+                                             uint8_t *lo, float *red) {
   const int t = threadIdx.x;
+  auto value = [&](int e) -> float4 {
+    float4 x = src ? *reinterpret_cast<const float4 *>(src + e) : make_float4(0, 0, 0, 0);
+    if (add) {
+      const float4 y = *reinterpret_cast<const float4 *>(add + e);
+      x.x = fmaf(f, y.x, x.x);
+      x.y = fmaf(f, y.y, x.y);
+      x.z = fmaf(f, y.z, x.z);
+      x.w = fmaf(f, y.w, x.w);
+    }
+    return x;
+  };
   float mx = 0.0f;
-  if (src) {
+  if (src || add) {
     for (int e = t * 4; e < TILE * DH; e += 4 * blockDim.x) {
-      const float4 x = *reinterpret_cast<const float4 *>(src + e);
+      const float4 x = value(e);
       mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
     }
   }
   const float s = 1.0f / pow2_ceil(block_max(mx, red));
   for (int e = t * 4; e < TILE * DH; e += 4 * blockDim.x) {
-    float4 x = src ? *reinterpret_cast<const float4 *>(src + e) : make_float4(0, 0, 0, 0);
+    const float4 x = (src || add) ? value(e) : make_float4(0, 0, 0, 0);
     const int r = e / DH, c = e % DH;
     const float xs[4] = {x.x * s, x.y * s, x.z * s, x.w * s};
 #pragma unroll
