@@ -54,10 +54,11 @@ struct FwdWorkspace {
   int nseg;
 };
 
-// Segments per unit for the tensor-core state build: enough CTAs to fill the GPU when
-// there are few (batch, head) units, one segment when there are many.
+// Segments per unit for the tensor-core state build (one CTA per SM each): enough CTAs to
+// fill the 152 SMs once when there are few (batch, head) units, one segment when there are
+// many.
 inline int tc_segments(int U, int NC) {
-  int s = U > 0 ? 256 / U : 1;
+  int s = U > 0 ? 148 / U : 1;
   if (s > 16) s = 16;
   if (s > NC) s = NC;
   return s < 1 ? 1 : s;

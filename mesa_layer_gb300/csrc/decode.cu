@@ -158,11 +158,12 @@ __global__ void __launch_bounds__(4 * D) mesa_decode_kernel(DecArgs a) {
 
 
 // d = 128 specialisation.  Same update, CG rule and readout; differences:
-//  - 8 warps (256 threads); warp w owns rows 16w .. 16w+15, lane l the columns 4l .. 4l+3
-//    of each (H in 64 registers), so the matrix-vector product is 64 FMAs per thread and
-//    the 16 row sums of a warp come from one shuffle reduce-scatter (16 shuffles): after it,
-//    row 16w + (lane >> 1) is held, replicated, by lanes 2j and 2j+1, which also hold that
-//    row's x, r, p and lambda;
+//  - 8 warps (256 threads); warp w owns rows 16w .. 16w+15.  Lane l = 8b + cb holds rows
+//    16w + 4b .. +3 and the float4 column groups cb, cb+8, cb+16, cb+24 of each (H in 64
+//    registers; the 8 lanes of a band read 128 contiguous bytes of a row), so a row sum is a
+//    16-term in-lane sum plus a 3-step reduce-scatter over the band's 8 lanes; after it,
+//    row 16w + 4b + ((l >> 1) & 3) is held, replicated, by lanes l and l^1, which also hold
+//    that row's x, r, p and lambda;
 //  - p's columns live in registers and its rows with their owners, so the second block
 //    reduction of a CG step also publishes the new residual and each thread updates its
 //    own copy of p: two barriers per step;
@@ -174,11 +175,13 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
   constexpr int D = 128, NW = 8;
   const int u = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = 16 * warp + (lane >> 1);  // the row this lane holds after the reduce
+  const int band = lane >> 3, cb = lane & 7;
+  const int row0 = 16 * warp + 4 * band;            // first of this lane's 4 rows
+  const int row = row0 + ((lane >> 1) & 3);         // the row this lane holds after the reduce
   extern __shared__ __align__(16) float dsm[];
-  float *Gs = dsm;                         // [128][128]
+  float *Gs = dsm;                                  // [128][128]
   float *kvec = Gs + D * D, *vvec = kvec + D, *pvec = vvec + D, *rvec = pvec + D;
-  float *red = rvec + D;                   // [2][NW]
+  float *red = rvec + D;                            // [2][NW]
 
   const float4 *Hg = reinterpret_cast<const float4 *>(a.Hs + (size_t)u * D * D);
   float4 *Hw = reinterpret_cast<float4 *>(a.Hs + (size_t)u * D * D);
@@ -195,9 +198,12 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
     }
     asm volatile("cp.async.commit_group;\n" ::: "memory");
   }
-  float4 h[16];
+  // h[i][j] = H[row0 + i][4 (cb + 8 j) .. +3]
+  float4 h[4][4];
 #pragma unroll
-  for (int j = 0; j < 16; j++) h[j] = Hg[(16 * warp + j) * 32 + lane];
+  for (int i = 0; i < 4; i++)
+#pragma unroll
+    for (int j = 0; j < 4; j++) h[i][j] = Hg[(row0 + i) * 32 + cb + 8 * j];
   const TIO *q = (const TIO *)a.q, *k = (const TIO *)a.k, *v = (const TIO *)a.v;
   if (threadIdx.x < D) {
     kvec[threadIdx.x] = ld(k, (size_t)u * D + threadIdx.x);
@@ -208,30 +214,31 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
   const float lam_r = a.lambda[(size_t)(u % a.H) * D + row];
   __syncthreads();
 
-  const float4 kc = reinterpret_cast<const float4 *>(kvec)[lane];
+  const float4 *k4 = reinterpret_cast<const float4 *>(kvec);
+  float4 kc[4];
 #pragma unroll
-  for (int j = 0; j < 16; j++) {
-    const float kr = kvec[16 * warp + j];
-    h[j].x = fmaf(g, h[j].x, kr * kc.x);
-    h[j].y = fmaf(g, h[j].y, kr * kc.y);
-    h[j].z = fmaf(g, h[j].z, kr * kc.z);
-    h[j].w = fmaf(g, h[j].w, kr * kc.w);
-    Hw[(16 * warp + j) * 32 + lane] = h[j];
+  for (int j = 0; j < 4; j++) kc[j] = k4[cb + 8 * j];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const float kr = kvec[row0 + i];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      h[i][j].x = fmaf(g, h[i][j].x, kr * kc[j].x);
+      h[i][j].y = fmaf(g, h[i][j].y, kr * kc[j].y);
+      h[i][j].z = fmaf(g, h[i][j].z, kr * kc[j].z);
+      h[i][j].w = fmaf(g, h[i][j].w, kr * kc[j].w);
+      Hw[(row0 + i) * 32 + cb + 8 * j] = h[i][j];
+    }
   }
 
-  // reduce-scatter of s[0..15] over the 32 lanes: the full sum of row lane >> 1
-  auto rowsum = [&](float (&s)[16]) -> float {
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
-    float t8[8], t4[4], t2[2];
+  // reduce-scatter of s[0..3] (rows row0 .. row0+3) over the band's 8 lanes: the full sum
+  // of row row0 + ((lane >> 1) & 3)
+  auto rowsum = [&](float (&s)[4]) -> float {
+    const bool b2 = lane & 4, b1 = lane & 2;
+    float t2[2];
 #pragma unroll
-    for (int j = 0; j < 8; j++)
-      t8[j] = (b4 ? s[j + 8] : s[j]) + __shfl_xor_sync(0xffffffffu, b4 ? s[j] : s[j + 8], 16);
-#pragma unroll
-    for (int j = 0; j < 4; j++)
-      t4[j] = (b3 ? t8[j + 4] : t8[j]) + __shfl_xor_sync(0xffffffffu, b3 ? t8[j] : t8[j + 4], 8);
-#pragma unroll
-    for (int j = 0; j < 2; j++)
-      t2[j] = (b2 ? t4[j + 2] : t4[j]) + __shfl_xor_sync(0xffffffffu, b2 ? t4[j] : t4[j + 2], 4);
+    for (int q2 = 0; q2 < 2; q2++)
+      t2[q2] = (b2 ? s[q2 + 2] : s[q2]) + __shfl_xor_sync(0xffffffffu, b2 ? s[q2] : s[q2 + 2], 4);
     float t = (b1 ? t2[1] : t2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? t2[0] : t2[1], 2);
     return t + __shfl_xor_sync(0xffffffffu, t, 1);
   };
@@ -247,22 +254,34 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
     const float4 a1 = reinterpret_cast<const float4 *>(red + buf * NW)[1];
     return ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
   };
+  auto matvec_rows = [&](const float4 (&pc)[4], float (&s)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      float t = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+        t = fmaf(h[i][j].w, pc[j].w, fmaf(h[i][j].z, pc[j].z, fmaf(h[i][j].y, pc[j].y, fmaf(h[i][j].x, pc[j].x, t))));
+      s[i] = t;
+    }
+  };
 
-  // p's columns live in registers (pc, this lane's float4) and p's rows with their row
-  // owners (pr); after the second reduction of a step every thread updates its own copy of
-  // p from the new residual (rvec) without a further barrier.
+  // p's columns live in registers (pc) and p's rows with their owners (pr); after the
+  // second reduction of a step every thread updates its own copy of p from the new
+  // residual (rvec) without a further barrier.
   float xr = 0.0f, rr = pvec[row], pr = rr;
-  float4 pc = reinterpret_cast<const float4 *>(pvec)[lane];
+  float4 pc[4];
+  const float4 *p4 = reinterpret_cast<const float4 *>(pvec);
+#pragma unroll
+  for (int j = 0; j < 4; j++) pc[j] = p4[cb + 8 * j];
   float rho = block_rows_sum(rr * rr, 0);
   const float nq = sqrtf(rho);
   const bool dynamic = a.cg_tol > 0.0f;
+  const float4 *r4 = reinterpret_cast<const float4 *>(rvec);
   int it = 0;
   for (; it < a.cg_iters; it++) {
     if (dynamic && sqrtf(rho) <= a.cg_tol * nq) break;
-    float s[16];
-#pragma unroll
-    for (int j = 0; j < 16; j++)
-      s[j] = fmaf(h[j].w, pc.w, fmaf(h[j].z, pc.z, fmaf(h[j].y, pc.y, h[j].x * pc.x)));
+    float s[4];
+    matvec_rows(pc, s);
     const float w = fmaf(lam_r, pr, rowsum(s));
     const float sigma = block_rows_sum(pr * w, 1);
     const float alpha = (sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
@@ -272,11 +291,14 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
     const float rn = block_rows_sum(rr * rr, 0);  // its barrier also publishes rvec
     const float beta = rho > 0.0f ? rn / rho : 0.0f;
     pr = fmaf(beta, pr, rr);
-    const float4 rc = reinterpret_cast<const float4 *>(rvec)[lane];
-    pc.x = fmaf(beta, pc.x, rc.x);
-    pc.y = fmaf(beta, pc.y, rc.y);
-    pc.z = fmaf(beta, pc.z, rc.z);
-    pc.w = fmaf(beta, pc.w, rc.w);
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const float4 rc = r4[cb + 8 * j];
+      pc[j].x = fmaf(beta, pc[j].x, rc.x);
+      pc[j].y = fmaf(beta, pc[j].y, rc.y);
+      pc[j].z = fmaf(beta, pc[j].z, rc.z);
+      pc[j].w = fmaf(beta, pc[j].w, rc.w);
+    }
     rho = rn;
   }
 
@@ -285,19 +307,27 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
   __syncthreads();
   if ((lane & 1) == 0) pvec[row] = xr;
   __syncthreads();
-  const float4 xc = reinterpret_cast<const float4 *>(pvec)[lane];
-  float s[16];
+  float4 xc[4];
 #pragma unroll
-  for (int j = 0; j < 16; j++) {
-    const int rj = 16 * warp + j;
-    float4 gg = reinterpret_cast<const float4 *>(Gs)[rj * 32 + lane];
-    const float vr = vvec[rj];
-    gg.x = fmaf(g, gg.x, vr * kc.x);
-    gg.y = fmaf(g, gg.y, vr * kc.y);
-    gg.z = fmaf(g, gg.z, vr * kc.z);
-    gg.w = fmaf(g, gg.w, vr * kc.w);
-    Gw[rj * 32 + lane] = gg;
-    s[j] = fmaf(gg.w, xc.w, fmaf(gg.z, xc.z, fmaf(gg.y, xc.y, gg.x * xc.x)));
+  for (int j = 0; j < 4; j++) xc[j] = p4[cb + 8 * j];
+  const float4 *G4 = reinterpret_cast<const float4 *>(Gs);
+  float s[4];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const float vr = vvec[row0 + i];
+    float t = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const int e = (row0 + i) * 32 + cb + 8 * j;
+      float4 gg = G4[e];
+      gg.x = fmaf(g, gg.x, vr * kc[j].x);
+      gg.y = fmaf(g, gg.y, vr * kc[j].y);
+      gg.z = fmaf(g, gg.z, vr * kc[j].z);
+      gg.w = fmaf(g, gg.w, vr * kc[j].w);
+      Gw[e] = gg;
+      t = fmaf(gg.w, xc[j].w, fmaf(gg.z, xc[j].z, fmaf(gg.y, xc[j].y, fmaf(gg.x, xc[j].x, t))));
+    }
+    s[i] = t;
   }
   const float o = rowsum(s);
   if ((lane & 1) == 0) st((TIO *)a.out, (size_t)u * D + row, o);

@@ -24,13 +24,13 @@ constexpr uint32_t DT_MAT = 128 * 128 * 2;
 constexpr uint32_t DT_SMEM = 3 * DT_MAT + 1024 + 1024;
 struct StateMisc {
   float w[128];
-  float red[16];
+  float red[48];
   uint64_t mbar;
   uint32_t tmem_base;
 };
 }  // namespace
 
-__global__ void __launch_bounds__(512) mesa_states_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC,
+__global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC,
                                                              unsigned *status) {
   using tc::DH;
   using tc::TILE;
@@ -103,22 +103,35 @@ __global__ void __launch_bounds__(512) mesa_states_tc_kernel(FwdArgs a, FwdWorks
     tc::tmem_st_wait();
   };
 
+  // keys and values of the next chunk are loaded into registers while the current chunk's
+  // MMAs run
+  tc::Rows8 kr, vr;
+  {
+    const size_t tb = (size_t)u * T + (size_t)c_begin * TILE;
+    const int Tv = min(TILE, T - c_begin * TILE);
+    tc::load_rows((const __nv_bfloat16 *)a.k + tb * DH, Tv, kr);
+    tc::load_rows((const __nv_bfloat16 *)a.v + tb * DH, Tv, vr);
+  }
   for (int c = c_begin; c < c_end && ok; c++) {
     const bool first = c == c_begin;
     const float *H0 = (seg == 0) ? a.H0 : nullptr;
     const float *G0 = (seg == 0) ? a.G0 : nullptr;
     const int t0 = c * TILE, Tv = min(TILE, T - t0);
     const size_t tokbase = (size_t)u * T + t0;
-    const __nv_bfloat16 *k = (const __nv_bfloat16 *)a.k + tokbase * DH;
-    const __nv_bfloat16 *v = (const __nv_bfloat16 *)a.v + tokbase * DH;
     const float lend = ws.ell[tokbase + Tv - 1];
     const float ac = expf(lend);
     if (tid < TILE) m->w[tid] = tid < Tv ? expf(lend - ws.ell[tokbase + tid]) : 0.0f;
     __syncthreads();
-    const float sK = tc::stage_rows(k, Tv, Ks, m->red);
-    const float sAH = tc::stage_weighted_rows(k, m->w, Tv, Ahi, Alo, m->red);
-    const float nsigH = sAH * sK;
+    float mk = tc::rows_absmax(kr, nullptr), mak = tc::rows_absmax(kr, m->w),
+          mav = tc::rows_absmax(vr, m->w);
+    tc::block_max3(mk, mak, mav, m->red);
+    const float sK = 1.0f / tc::pow2_ceil(mk), sAH = 1.0f / tc::pow2_ceil(mak),
+                sAG = 1.0f / tc::pow2_ceil(mav);
+    tc::store_rows(kr, nullptr, sK, Ks, nullptr);
+    tc::store_rows(kr, m->w, sAH, Ahi, Alo);
+    const float nsigH = sAH * sK, nsigG = sAG * sK;
     rescale(0, first ? ac * nsigH : ac * nsigH / sigH, first, H0);
+    rescale(128, first ? ac * nsigG : ac * nsigG / sigG, first, G0);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -126,14 +139,18 @@ __global__ void __launch_bounds__(512) mesa_states_tc_kernel(FwdArgs a, FwdWorks
     if (tid == 0) issue(0, !first || H0 != nullptr);
     ok = wait();
     if (!ok) break;
-    const float sAG = tc::stage_weighted_rows(v, m->w, Tv, Ahi, Alo, m->red);
-    const float nsigG = sAG * sK;
-    rescale(128, first ? ac * nsigG : ac * nsigG / sigG, first, G0);
+    tc::store_rows(vr, m->w, sAG, Ahi, Alo);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) issue(128, !first || G0 != nullptr);
+    if (c + 1 < c_end) {  // next chunk's rows, in flight during the MMAs and the write-out
+      const size_t tb = tokbase + TILE;
+      const int Tn = min(TILE, T - t0 - TILE);
+      tc::load_rows((const __nv_bfloat16 *)a.k + tb * DH, Tn, kr);
+      tc::load_rows((const __nv_bfloat16 *)a.v + tb * DH, Tn, vr);
+    }
     ok = wait();
     if (!ok) break;
     sigH = nsigH;

@@ -153,5 +153,85 @@ __device__ __forceinline__ float stage_weighted_rows(const __nv_bfloat16 *src, c
   return s;
 }
 
+// ---- register-held rows (512 threads: each thread holds 4 groups of 8 bf16 values) ------
+// Group n of thread t covers element e = 8 t + 4096 n of the 128 x 128 tile (row e / 128,
+// columns e % 128 .. +7).
+struct Rows8 {
+  uint4 v[4];
+};
+
+// Issue the loads of rows [0, Tv) of a bf16 tile (zeros below).  Needs blockDim.x == 512.
+__device__ __forceinline__ void load_rows(const __nv_bfloat16 *src, int Tv, Rows8 &x) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int n = 0; n < 4; n++) {
+    const int e = 8 * t + 4096 * n;
+    x.v[n] = (e / DH < Tv) ? *reinterpret_cast<const uint4 *>(src + e) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// max over this thread's values of |w_row * x|  (w == nullptr: |x|)
+__device__ __forceinline__ float rows_absmax(const Rows8 &x, const float *w) {
+  const int t = threadIdx.x;
+  float mx = 0.0f;
+#pragma unroll
+  for (int n = 0; n < 4; n++) {
+    const float wr = w ? w[(8 * t + 4096 * n) / DH] : 1.0f;
+    const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&x.v[n]);
+#pragma unroll
+    for (int k = 0; k < 8; k++) mx = fmaxf(mx, fabsf(wr * __bfloat162float(b[k])));
+  }
+  return mx;
+}
+
+// Store s * w_row * x as one fp16 operand (lo == nullptr) or as hi + lo.
+__device__ __forceinline__ void store_rows(const Rows8 &x, const float *w, float s, uint8_t *hi,
+                                           uint8_t *lo) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int n = 0; n < 4; n++) {
+    const int e = 8 * t + 4096 * n;
+    const float ws = (w ? w[e / DH] : 1.0f) * s;
+    const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&x.v[n]);
+    __align__(16) __half h[8], l[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      const float val = __bfloat162float(b[k]) * ws;
+      h[k] = __float2half_rn(val);
+      l[k] = __float2half_rn(val - __half2float(h[k]));
+    }
+    const uint32_t off = sw128_offset(e / DH, e % DH, TILE);
+    *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<uint4 *>(h);
+    if (lo) *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<uint4 *>(l);
+  }
+}
+
+// Block-wide maxima of three values at once (red holds 3 floats per warp, 16 warps max).
+__device__ __forceinline__ void block_max3(float &a, float &b, float &c, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+    c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
+  }
+  __syncthreads();
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    red[3 * w] = a;
+    red[3 * w + 1] = b;
+    red[3 * w + 2] = c;
+  }
+  __syncthreads();
+  const int nw = blockDim.x >> 5;
+  a = red[0];
+  b = red[1];
+  c = red[2];
+  for (int k = 1; k < nw; k++) {
+    a = fmaxf(a, red[3 * k]);
+    b = fmaxf(b, red[3 * k + 1]);
+    c = fmaxf(c, red[3 * k + 2]);
+  }
+}
+
 }  // namespace tc
 }  // namespace mesa

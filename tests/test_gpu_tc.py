@@ -81,3 +81,27 @@ def test_tc_initial_state_and_final_states():
     for a, b in ((Hg, Hf), (Gg, Gf)):
         a = a.cpu().numpy().astype(np.float64)
         assert np.abs(a - b).max() <= 1e-5 * np.abs(b).max()
+
+
+def test_tc_many_segments_with_initial_state():
+    """A single long sequence (40 chunks): the state build splits it into segments that start
+    from zero and are chained by carries; outputs and final states must not notice."""
+    import torch
+
+    w = synth.workload("fwd_bf16_d128", B=1, H=1, T=40 * 128 - 17, cg_iters=10, cg_tol=0.0)
+    inp = synth.forward_inputs(w, seed=13)
+    rng = np.random.default_rng(13)
+    M = rng.standard_normal((1, 1, 128, 128)).astype(np.float32) * 0.1
+    H0 = (M @ np.swapaxes(M, -1, -2)).astype(np.float32)       # symmetric PSD start state
+    G0 = (rng.standard_normal((1, 1, 128, 128)) * 0.1).astype(np.float32)
+    ro, rit, Hf, Gf = oracle.forward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], 10, 0.0,
+                                     H0=H0, G0=G0, want_final=True)
+    Hg = torch.empty(1, 1, 128, 128, device="cuda")
+    Gg = torch.empty_like(Hg)
+    o, it = gpu_forward(inp, "bf16", 10, 0.0, 128, H0=torch.from_numpy(H0).cuda(),
+                        G0=torch.from_numpy(G0).cuda(), H_final=Hg, G_final=Gg)
+    err, _ = check_against_oracle(o, it, ro, rit, "bf16", 0.0, "segments")
+    for a, b in ((Hg, Hf), (Gg, Gf)):
+        a = a.cpu().numpy().astype(np.float64)
+        assert np.abs(a - b).max() <= 1e-5 * np.abs(b).max()
+    print(f"tc segments: max rel err {err:.3e}")
