@@ -467,16 +467,23 @@ def bench_decode(args, w, rank, world, dev, lib, torch, binding):
     return res
 
 
-def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
-    step_ms = float(np.sum(res["step_ms"])) / args.steps
+def aggregate(step_ms: float, tokens_per_rank: int, world: int, torch, dist, device="cuda"):
+    """Whole-job figures of a replicated run: the slowest rank's time per step and the
+    tokens of all ranks.  Each rank runs its own replica (independent sequences), so the
+    only collective is this max."""
     if world > 1:
-        t = torch.tensor([step_ms], device="cuda")
+        t = torch.tensor([step_ms], device=device, dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         step_ms = float(t.item())
+    tokens = tokens_per_rank * world
+    return step_ms, tokens, tokens / (step_ms / 1e3)
+
+
+def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
+    step_ms, tokens, value = aggregate(float(np.sum(res["step_ms"])) / args.steps, res["tokens_per_step"],
+                                       world, torch, dist)
     if rank != 0:
         return
-    tokens = res["tokens_per_step"] * world
-    value = tokens / (step_ms / 1e3)
     names = res["names"]
     kind_ms, kind_n = res["kind_ms"], res["kind_n"]
     top = int(np.argmax(kind_ms))
