@@ -55,31 +55,31 @@ __device__ __forceinline__ void quad_bar(int q) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(1 + q), "r"(32 * NG) : "memory");
 }
 
-// Combine the NG column groups' partials of each row.  `scr` is NG * 512 B of shared memory
-// that holds no live operand at the call.  With BLOCK the barriers span the whole CTA
-// (needed when other quadrants may overwrite the scratch right after their reduction).
-template <int NG, bool MAX, bool BLOCK = false>
-__device__ __forceinline__ float rowred(float v, float *scr, int q, int g, int i) {
-  scr[g * TILE + i] = v;
-  if (BLOCK) __syncthreads(); else quad_bar<NG>(q);
-  float r = scr[i];
+// Combine the NG column groups' partials of each row of lane quadrant q.  `scr` is the
+// quadrant's own scratch (NG * 128 B per value), which only the quadrant's threads touch,
+// so a barrier of those threads suffices; `l` is the row within the quadrant (the lane).
+template <int NG, bool MAX>
+__device__ __forceinline__ float rowred(float v, float *scr, int q, int g, int l) {
+  scr[g * 32 + l] = v;
+  quad_bar<NG>(q);
+  float r = scr[l];
 #pragma unroll
-  for (int k = 1; k < NG; k++) r = MAX ? fmaxf(r, scr[k * TILE + i]) : r + scr[k * TILE + i];
-  if (BLOCK) __syncthreads(); else quad_bar<NG>(q);
+  for (int k = 1; k < NG; k++) r = MAX ? fmaxf(r, scr[k * 32 + l]) : r + scr[k * 32 + l];
+  quad_bar<NG>(q);
   return r;
 }
 
-// Two-value variant (a sum and a max) sharing the barriers; scratch NG * 1 KB.
+// Two-value variant (a sum and a max) sharing the barriers.
 template <int NG>
-__device__ __forceinline__ void rowred2(float &sum, float &mx, float *scr, int q, int g, int i) {
-  scr[g * TILE + i] = sum;
-  scr[(NG + g) * TILE + i] = mx;
+__device__ __forceinline__ void rowred2(float &sum, float &mx, float *scr, int q, int g, int l) {
+  scr[g * 32 + l] = sum;
+  scr[(NG + g) * 32 + l] = mx;
   quad_bar<NG>(q);
-  float s = scr[i], m = scr[NG * TILE + i];
+  float s = scr[l], m = scr[NG * 32 + l];
 #pragma unroll
   for (int k = 1; k < NG; k++) {
-    s += scr[k * TILE + i];
-    m = fmaxf(m, scr[(NG + k) * TILE + i]);
+    s += scr[k * 32 + l];
+    m = fmaxf(m, scr[(NG + k) * 32 + l]);
   }
   sum = s;
   mx = m;
@@ -144,8 +144,10 @@ __global__ void __launch_bounds__(128 * TPR, 1)
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t *Shi = sm + OFF_SHI, *Slo = sm + OFF_SLO, *Ks = sm + OFF_K;
   uint8_t *Phi = sm + OFF_PHI, *Plo = sm + OFF_PLO, *Zhi = sm + OFF_ZHI, *Zlo = sm + OFF_ZLO;
-  // row-reduction scratch: the first 2 KB of the Z operand, used only while Z is not live
-  float *scr = reinterpret_cast<float *>(Zhi);
+  // row-reduction scratch of this thread's lane quadrant: the start of the quadrant's own
+  // rows of the Z operand (rows 32q .. 32q+31 are bytes [4096 q, 4096 (q+1)) of each
+  // 64-column block), written only by the quadrant's threads and never while Z is live
+  float *scr = reinterpret_cast<float *>(Zhi + 4096 * ((threadIdx.x >> 5) & 3));
   Misc *m = reinterpret_cast<Misc *>(sm + OFF_MISC);
   const uint32_t aShi = tc::smem_u32(Shi), aSlo = tc::smem_u32(Slo), aK = tc::smem_u32(Ks);
   const uint32_t aPhi = tc::smem_u32(Phi), aPlo = tc::smem_u32(Plo);
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       s = fmaf(qa[d], qa[d], s);
       mx = fmaxf(mx, fabsf(qa[d]));
     }
-    rowred2<NG>(s, mx, scr, qd, grp, i);
+    rowred2<NG>(s, mx, scr, qd, grp, lane);
     rho = s;
     nq = sqrtf(rho);
     mP = tc::pow2_ceil(mx);
@@ -330,8 +332,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
         }
       }
     }
-    // the scratch lies inside the Z operand written next: block-wide barriers
-    const float zs = tc::pow2_ceil(rowred<NG, true, true>(zmax, scr, qd, grp, i));
+    const float zs = tc::pow2_ceil(rowred<NG, true>(zmax, scr, qd, grp, lane));
     const float inv = 1.0f / zs;
 #pragma unroll
     for (int g = 0; g < NV; g++) {
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
         }
       }
     }
-    const float sigma = rowred<NG, false>(sg, scr, qd, grp, i);
+    const float sigma = rowred<NG, false>(sg, scr, qd, grp, lane);
     const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
     // r -= alpha AP   (alpha = 0 leaves a finished row unchanged; the tensor-memory
     // accesses stay unconditional: they are warp-collective)
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       rmax = fmaxf(rmax, fabsf(rr[kk]));
     }
     tc::tmem_st<CW>(tl + COL_R, rr);
-    rowred2<NG>(rn, rmax, scr, qd, grp, i);
+    rowred2<NG>(rn, rmax, scr, qd, grp, lane);
     const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
     // one pass over the old p: x += alpha p and p = r + beta p, re-scaled so that
     // |p_new| <= max|r| + beta max|p| <= rmax + beta mP  (x's tensor-memory access stays
@@ -452,7 +453,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     float mx = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < CW; kk++) mx = fmaxf(mx, fabsf(xx[kk]));
-    const float mX = tc::pow2_ceil(rowred<NG, true>(mx, scr, qd, grp, i));
+    const float mX = tc::pow2_ceil(rowred<NG, true>(mx, scr, qd, grp, lane));
     const float inv = 1.0f / mX;
 #pragma unroll
     for (int g = 0; g < NV; g++) {

@@ -256,12 +256,12 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
   };
   auto matvec_rows = [&](const float4 (&pc)[4], float (&s)[4]) {
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-      float t = 0.0f;
+    for (int i = 0; i < 4; i++) {  // four independent partial sums per row: short chains
+      float t[4];
 #pragma unroll
       for (int j = 0; j < 4; j++)
-        t = fmaf(h[i][j].w, pc[j].w, fmaf(h[i][j].z, pc[j].z, fmaf(h[i][j].y, pc[j].y, fmaf(h[i][j].x, pc[j].x, t))));
-      s[i] = t;
+        t[j] = fmaf(h[i][j].w, pc[j].w, fmaf(h[i][j].z, pc[j].z, fmaf(h[i][j].y, pc[j].y, h[i][j].x * pc[j].x)));
+      s[i] = (t[0] + t[1]) + (t[2] + t[3]);
     }
   };
 
@@ -334,214 +334,20 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
   if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
 }
 
-// d = 128, persistent and pipelined: one CTA per SM walks the units u = blockIdx.x,
-// + gridDim.x, ...  While it runs the CG of one unit, the next unit's H and G stream from HBM
-// into shared memory (cp.async; H into one buffer, G into the other half of a two-buffer
-// ring), so every SM keeps HBM busy during its compute.  Per unit the work is that of
-// mesa_decode128_kernel (same mapping: lane 8b + cb of warp w holds rows 16w + 4b .. +3 and
-// float4 column groups cb, cb+8, cb+16, cb+24; H in registers for the CG).
-template <typename TIO>
-__global__ void __launch_bounds__(256, 1) mesa_decode128p_kernel(DecArgs a) {
-  constexpr int D = 128, NW = 8;
-  const int U = a.N * a.H;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int band = lane >> 3, cb = lane & 7;
-  const int row0 = 16 * warp + 4 * band;
-  const int row = row0 + ((lane >> 1) & 3);
-  extern __shared__ __align__(16) float dsm[];
-  float4 *Hn = reinterpret_cast<float4 *>(dsm);                  // [4096] next unit's H
-  float4 *Gb = reinterpret_cast<float4 *>(dsm + D * D);          // [2][4096] G ring
-  float *kvec = dsm + 3 * D * D, *vvec = kvec + D, *pvec = vvec + D, *rvec = pvec + D;
-  float *red = rvec + D;                                        // [2][NW]
-  const uint32_t sH = (uint32_t)__cvta_generic_to_shared(Hn);
-  const uint32_t sG = (uint32_t)__cvta_generic_to_shared(Gb);
-  const TIO *q = (const TIO *)a.q, *k = (const TIO *)a.k, *v = (const TIO *)a.v;
-
-  auto prefetch = [&](int u, int buf) {  // H[u] -> Hn, G[u] -> Gb[buf]; one commit group
-    const float4 *hs = reinterpret_cast<const float4 *>(a.Hs + (size_t)u * D * D);
-    const float4 *gs = reinterpret_cast<const float4 *>(a.Gs + (size_t)u * D * D);
-#pragma unroll
-    for (int kk = 0; kk < 16; kk++) {
-      const int e = threadIdx.x + 256 * kk;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sH + 16 * e), "l"(hs + e) : "memory");
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sG + 16 * (buf * 4096 + e)),
-                   "l"(gs + e)
-                   : "memory");
-    }
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-  };
-
-  auto rowsum = [&](float (&s)[4]) -> float {
-    const bool b2 = lane & 4, b1 = lane & 2;
-    float t2[2];
-#pragma unroll
-    for (int q2 = 0; q2 < 2; q2++)
-      t2[q2] = (b2 ? s[q2 + 2] : s[q2]) + __shfl_xor_sync(0xffffffffu, b2 ? s[q2] : s[q2 + 2], 4);
-    float t = (b1 ? t2[1] : t2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? t2[0] : t2[1], 2);
-    return t + __shfl_xor_sync(0xffffffffu, t, 1);
-  };
-  auto block_rows_sum = [&](float val, int buf) -> float {
-    val += __shfl_xor_sync(0xffffffffu, val, 2);
-    val += __shfl_xor_sync(0xffffffffu, val, 4);
-    val += __shfl_xor_sync(0xffffffffu, val, 8);
-    val += __shfl_xor_sync(0xffffffffu, val, 16);
-    if (lane == 0) red[buf * NW + warp] = val;
-    __syncthreads();
-    const float4 a0 = reinterpret_cast<const float4 *>(red + buf * NW)[0];
-    const float4 a1 = reinterpret_cast<const float4 *>(red + buf * NW)[1];
-    return ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
-  };
-
-  int n = 0;
-  if (blockIdx.x < U) prefetch(blockIdx.x, 0);
-  for (int u = blockIdx.x; u < U; u += gridDim.x, n ^= 1) {
-    // this unit's small inputs, then its H and G (prefetched) become visible
-    if (threadIdx.x < D) {
-      kvec[threadIdx.x] = ld(k, (size_t)u * D + threadIdx.x);
-      vvec[threadIdx.x] = ld(v, (size_t)u * D + threadIdx.x);
-      pvec[threadIdx.x] = ld(q, (size_t)u * D + threadIdx.x);
-    }
-    const float g = a.gamma[u];
-    const float lam_r = a.lambda[(size_t)(u % a.H) * D + row];
-    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-    __syncthreads();
-    float4 h[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; i++)
-#pragma unroll
-      for (int j = 0; j < 4; j++) h[i][j] = Hn[(row0 + i) * 32 + cb + 8 * j];
-    __syncthreads();  // Hn is free: stream the next unit in behind this unit's compute
-    if (u + gridDim.x < U) prefetch(u + gridDim.x, n ^ 1);
-
-    const float4 *k4 = reinterpret_cast<const float4 *>(kvec);
-    float4 kc[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) kc[j] = k4[cb + 8 * j];
-    float4 *Hw = reinterpret_cast<float4 *>(a.Hs + (size_t)u * D * D);
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const float kr = kvec[row0 + i];
-#pragma unroll
-      for (int j = 0; j < 4; j++) {
-        h[i][j].x = fmaf(g, h[i][j].x, kr * kc[j].x);
-        h[i][j].y = fmaf(g, h[i][j].y, kr * kc[j].y);
-        h[i][j].z = fmaf(g, h[i][j].z, kr * kc[j].z);
-        h[i][j].w = fmaf(g, h[i][j].w, kr * kc[j].w);
-        Hw[(row0 + i) * 32 + cb + 8 * j] = h[i][j];
-      }
-    }
-
-    float xr = 0.0f, rr = pvec[row], pr = rr;
-    float4 pc[4];
-    const float4 *p4 = reinterpret_cast<const float4 *>(pvec);
-#pragma unroll
-    for (int j = 0; j < 4; j++) pc[j] = p4[cb + 8 * j];
-    float rho = block_rows_sum(rr * rr, 0);
-    const float nq = sqrtf(rho);
-    const bool dynamic = a.cg_tol > 0.0f;
-    const float4 *r4 = reinterpret_cast<const float4 *>(rvec);
-    int it = 0;
-    for (; it < a.cg_iters; it++) {
-      if (dynamic && sqrtf(rho) <= a.cg_tol * nq) break;
-      float s[4];
-#pragma unroll
-      for (int i = 0; i < 4; i++) {
-        float t = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; j++)
-          t = fmaf(h[i][j].w, pc[j].w, fmaf(h[i][j].z, pc[j].z, fmaf(h[i][j].y, pc[j].y, fmaf(h[i][j].x, pc[j].x, t))));
-        s[i] = t;
-      }
-      const float w = fmaf(lam_r, pr, rowsum(s));
-      const float sigma = block_rows_sum(pr * w, 1);
-      const float alpha = (sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
-      xr = fmaf(alpha, pr, xr);
-      rr = fmaf(-alpha, w, rr);
-      if ((lane & 1) == 0) rvec[row] = rr;
-      const float rn = block_rows_sum(rr * rr, 0);
-      const float beta = rho > 0.0f ? rn / rho : 0.0f;
-      pr = fmaf(beta, pr, rr);
-#pragma unroll
-      for (int j = 0; j < 4; j++) {
-        const float4 rc = r4[cb + 8 * j];
-        pc[j].x = fmaf(beta, pc[j].x, rc.x);
-        pc[j].y = fmaf(beta, pc[j].y, rc.y);
-        pc[j].z = fmaf(beta, pc[j].z, rc.z);
-        pc[j].w = fmaf(beta, pc[j].w, rc.w);
-      }
-      rho = rn;
-    }
-
-    // readout from this unit's G buffer
-    __syncthreads();
-    if ((lane & 1) == 0) pvec[row] = xr;
-    __syncthreads();
-    float4 xc[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) xc[j] = p4[cb + 8 * j];
-    const float4 *G4 = Gb + n * 4096;
-    float4 *Gw = reinterpret_cast<float4 *>(a.Gs + (size_t)u * D * D);
-    float s[4];
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      const float vr = vvec[row0 + i];
-      float t = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 4; j++) {
-        const int e = (row0 + i) * 32 + cb + 8 * j;
-        float4 gg = G4[e];
-        gg.x = fmaf(g, gg.x, vr * kc[j].x);
-        gg.y = fmaf(g, gg.y, vr * kc[j].y);
-        gg.z = fmaf(g, gg.z, vr * kc[j].z);
-        gg.w = fmaf(g, gg.w, vr * kc[j].w);
-        Gw[e] = gg;
-        t = fmaf(gg.w, xc[j].w, fmaf(gg.z, xc[j].z, fmaf(gg.y, xc[j].y, fmaf(gg.x, xc[j].x, t))));
-      }
-      s[i] = t;
-    }
-    const float o = rowsum(s);
-    if ((lane & 1) == 0) st((TIO *)a.out, (size_t)u * D + row, o);
-    if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
-    __syncthreads();  // kvec, vvec, pvec and this G buffer are reused by the next unit
-  }
-  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-}
-
-constexpr int kDecode128pSmem = (3 * 128 * 128 + 4 * 128 + 2 * 8) * sizeof(float);
-
-// (A variant with H in shared memory and three units per SM measured slower: 0.287 ms
-// against 0.256 ms per step of the 256 x 16 decode workload.)
+// (Measured alternatives, 256 x 16 decode workload: H in shared memory with three units per
+// SM, 0.287 ms per step; a persistent kernel that streams the next unit's H and G in while
+// one unit per SM runs its CG, 0.328 ms; this kernel, two units per SM, 0.256 ms.)
 constexpr int kDecode128Smem = (128 * 128 + 4 * 128 + 2 * 8) * sizeof(float);
-// d = 128 decode variant: persistent pipelined (1) or one CTA per unit (0).
-#ifndef MESA_DECODE128_PERSISTENT
-#define MESA_DECODE128_PERSISTENT 1
-#endif
 
 template <int D, typename TIO>
 static int launch_dec_t(const DecArgs &a, cudaStream_t st) {
   timing_mark_begin(K_DECODE, st);
   if constexpr (D == 128) {
-#if MESA_DECODE128_PERSISTENT
-    static int sms = 0;
-    if (sms == 0) {
-      int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return -1;
-    }
-    auto kfn = mesa_decode128p_kernel<TIO>;
-    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecode128pSmem) !=
-        cudaSuccess)
-      return -1;
-    const int U = a.N * a.H;
-    kfn<<<U < sms ? U : sms, 256, kDecode128pSmem, st>>>(a);
-#else
     auto kfn = mesa_decode128_kernel<TIO>;
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecode128Smem) !=
         cudaSuccess)
       return -1;
     kfn<<<a.N * a.H, 256, kDecode128Smem, st>>>(a);
-#endif
   } else {
     mesa_decode_kernel<D, TIO><<<a.N * a.H, 4 * D, 0, st>>>(a);
   }
