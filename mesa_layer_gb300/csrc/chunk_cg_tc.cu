@@ -43,8 +43,9 @@ struct Misc {
   float ell2[TILE];  // log2-decays l_i * log2(e)
   float e2c[TILE];   // 2^{-l2_j} (used when the chunk's decays fit fp32 as factors)
   float lam[DH];     // Lambda diagonal of this head
-  float red[32];
-  uint64_t mbar;
+  float red[48];
+  uint64_t mbar;    // barrier A: W = P K^T, then Y = Z K
+  uint64_t mbar_u;  // barrier U: U = P S
   uint32_t tmem_base;
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc block too large");
@@ -53,37 +54,6 @@ static_assert(sizeof(Misc) <= MISC_BYTES, "misc block too large");
 template <int NG>
 __device__ __forceinline__ void quad_bar(int q) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(1 + q), "r"(32 * NG) : "memory");
-}
-
-// Combine the NG column groups' partials of each row of lane quadrant q.  `scr` is the
-// quadrant's own scratch (NG * 128 B per value), which only the quadrant's threads touch,
-// so a barrier of those threads suffices; `l` is the row within the quadrant (the lane).
-template <int NG, bool MAX>
-__device__ __forceinline__ float rowred(float v, float *scr, int q, int g, int l) {
-  scr[g * 32 + l] = v;
-  quad_bar<NG>(q);
-  float r = scr[l];
-#pragma unroll
-  for (int k = 1; k < NG; k++) r = MAX ? fmaxf(r, scr[k * 32 + l]) : r + scr[k * 32 + l];
-  quad_bar<NG>(q);
-  return r;
-}
-
-// Two-value variant (a sum and a max) sharing the barriers.
-template <int NG>
-__device__ __forceinline__ void rowred2(float &sum, float &mx, float *scr, int q, int g, int l) {
-  scr[g * 32 + l] = sum;
-  scr[(NG + g) * 32 + l] = mx;
-  quad_bar<NG>(q);
-  float s = scr[l], m = scr[NG * 32 + l];
-#pragma unroll
-  for (int k = 1; k < NG; k++) {
-    s += scr[k * 32 + l];
-    m = fmaxf(m, scr[(NG + k) * 32 + l]);
-  }
-  sum = s;
-  mx = m;
-  quad_bar<NG>(q);
 }
 
 // 8 consecutive values (columns c0..c0+7 of row i) of a scaled operand (NTERMS = 2: hi + lo),
@@ -134,25 +104,18 @@ __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, con
 
 }  // namespace
 
-template <int TPR, int NTERMS>
-__global__ void __launch_bounds__(128 * TPR, 1)
+template <int NTERMS>
+__global__ void __launch_bounds__(512, 1)
     mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, unsigned *status) {
-  constexpr int NG = TPR;         // column groups (threads per token row)
-  constexpr int CW = DH / TPR;    // columns per thread
+  constexpr int NG = 4;           // column groups (threads per token row)
+  constexpr int CW = DH / NG;     // columns per thread
   constexpr int NV = CW / 8;      // 8-column vectors per thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t *Shi = sm + OFF_SHI, *Slo = sm + OFF_SLO, *Ks = sm + OFF_K;
   uint8_t *Phi = sm + OFF_PHI, *Plo = sm + OFF_PLO, *Zhi = sm + OFF_ZHI, *Zlo = sm + OFF_ZLO;
-  // row-reduction scratch of this thread's lane quadrant: the start of the quadrant's own
-  // rows of the Z operand (rows 32q .. 32q+31 are bytes [4096 q, 4096 (q+1)) of each
-  // 64-column block), written only by the quadrant's threads and never while Z is live
-  float *scr = reinterpret_cast<float *>(Zhi + 4096 * ((threadIdx.x >> 5) & 3));
   Misc *m = reinterpret_cast<Misc *>(sm + OFF_MISC);
-  const uint32_t aShi = tc::smem_u32(Shi), aSlo = tc::smem_u32(Slo), aK = tc::smem_u32(Ks);
-  const uint32_t aPhi = tc::smem_u32(Phi), aPlo = tc::smem_u32(Plo);
-  const uint32_t aZhi = tc::smem_u32(Zhi), aZlo = tc::smem_u32(Zlo);
-  const uint32_t aBar = tc::smem_u32(&m->mbar);
+  const uint32_t aBarA = tc::smem_u32(&m->mbar), aBarU = tc::smem_u32(&m->mbar_u);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, grp = warp >> 2;  // lane quadrant, column group
@@ -168,10 +131,48 @@ __global__ void __launch_bounds__(128 * TPR, 1)
   const __nv_bfloat16 *k = (const __nv_bfloat16 *)a.k;
   const __nv_bfloat16 *v = (const __nv_bfloat16 *)a.v;
   constexpr float kLog2e = 1.4426950408889634f;
+  // Warps whose 32 columns of Z lie entirely above the causal diagonal (every key j > every
+  // row i of the quadrant): their block of Z is zero for every p, written once below.
+  const bool z_upper = grp > qd;
 
-  // ---- set-up: tensor memory, barrier, per-chunk constants ----------------------------
+  // Row-reduction scratch: value n of column group g for row 32 qd + l sits in float l / 8
+  // of the 16-byte chunk g of that row of Z (hi for n = 0, lo for n = 1): columns 0..31,
+  // which no warp above the diagonal owns, conflict-free across the lanes of a warp.  Only
+  // the quadrant's own threads touch its rows, and never while Z is live.
+  const uint32_t scr_row = (uint32_t)((i >> 3) * 1024 + (i & 7) * 128 + 4 * (lane >> 3));
+  auto scr = [&](int n, int g) -> float * {
+    return reinterpret_cast<float *>((n ? Zlo : Zhi) + scr_row + ((g ^ (i & 7)) << 4));
+  };
+  auto rowred = [&](float val, bool mx) -> float {
+    *scr(0, grp) = val;
+    quad_bar<NG>(qd);
+    float r = *scr(0, 0);
+#pragma unroll
+    for (int g = 1; g < NG; g++) r = mx ? fmaxf(r, *scr(0, g)) : r + *scr(0, g);
+    quad_bar<NG>(qd);
+    return r;
+  };
+  auto rowred2 = [&](float &sum, float &mx) {  // a sum and a max sharing the barriers
+    *scr(0, grp) = sum;
+    *scr(1, grp) = mx;
+    quad_bar<NG>(qd);
+    float s_ = *scr(0, 0), m_ = *scr(1, 0);
+#pragma unroll
+    for (int g = 1; g < NG; g++) {
+      s_ += *scr(0, g);
+      m_ = fmaxf(m_, *scr(1, g));
+    }
+    sum = s_;
+    mx = m_;
+    quad_bar<NG>(qd);
+  };
+
+  // ---- set-up: tensor memory, barriers, per-chunk constants --------------------------
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 512);
-  if (tid == 0) tc::mbar_init(aBar, 1);
+  if (tid == 0) {
+    tc::mbar_init(aBarA, 1);
+    tc::mbar_init(aBarU, 1);
+  }
   bool small = true;  // |l2| <= 100: D_ij = 2^{l2_i} 2^{-l2_j} without overflow
   if (tid < TILE) {
     const float l2 = (tid < Tv ? ws.ell[tokbase + tid] : 0.0f) * kLog2e;
@@ -180,14 +181,6 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     small = fabsf(l2) <= 100.0f;
   }
   if (tid >= 256 && tid < 256 + DH) m->lam[tid - 256] = a.lambda[(size_t)(u % a.H) * DH + tid - 256];
-  tc::fence_before_sync();
-  const bool factored = __syncthreads_and(small ? 1 : 0);
-  tc::fence_after_sync();
-  const uint32_t tbase = m->tmem_base;
-  const uint32_t tl = tbase + ((uint32_t)(32 * qd) << 16) + c0;  // lane quadrant, column group
-  const float ell2_i = m->ell2[i];
-  const float el_i = valid ? exp2f(ell2_i) : 0.0f;
-  const float e2r_i = valid ? el_i : 0.0f;  // 2^{l2_i}; invalid rows get D = 0
 
   // S_{c-1}: the segment-local state plus exp(Lc) times the carry into its segment
   const float *SH = nullptr, *SG = nullptr, *CH = nullptr, *CG = nullptr;
@@ -205,18 +198,52 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     SH = a.H0 + (size_t)u * DH * DH;
     SG = a.G0 + (size_t)u * DH * DH;
   }
-  const float sS = tc::stage_state(SH, CH, cf, Shi, NTERMS == 2 ? Slo : nullptr, m->red);
-  const float sK = tc::stage_rows(k + tokbase * DH, Tv, Ks, m->red);
+  // loads in flight together: this thread's query columns, the key tile, the state; the
+  // readout's state is only needed after the CG and is fetched into L2 meanwhile
+  uint4 qraw[NV];
+  {
+    const uint4 *src = reinterpret_cast<const uint4 *>(q + (tokbase + i) * DH + c0);
+#pragma unroll
+    for (int g = 0; g < NV; g++) qraw[g] = valid ? src[g] : make_uint4(0, 0, 0, 0);
+  }
+  tc::Rows8 kr;
+  tc::load_rows(k + tokbase * DH, Tv, kr);
+  tc::prefetch_l2(SG, sizeof(float) * DH * DH);
+  tc::prefetch_l2(CG, sizeof(float) * DH * DH);
+  float sS, sK;
+  {
+    tc::Mat32 S;
+    tc::load_mat(SH, CH, cf, S);
+    float mS = tc::mat_absmax(S), mK = tc::rows_absmax(kr, nullptr), unused = 0.0f;
+    tc::block_max3(mS, mK, unused, m->red);
+    sS = 1.0f / tc::pow2_ceil(mS);
+    sK = 1.0f / tc::pow2_ceil(mK);
+    tc::store_mat(S, sS, Shi, NTERMS == 2 ? Slo : nullptr);
+    tc::store_rows(kr, nullptr, sK, Ks, nullptr);
+  }
+  if (z_upper) {
+#pragma unroll
+    for (int g = 0; g < NV; g++) {
+      const uint32_t off = tc::sw128_offset(i, c0 + 8 * g, TILE);
+      *reinterpret_cast<uint4 *>(Zhi + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4 *>(Zlo + off) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  tc::fence_before_sync();
+  const bool factored = __syncthreads_and(small ? 1 : 0);
+  tc::fence_after_sync();
+  const uint32_t tbase = m->tmem_base;
+  const uint32_t tl = tbase + ((uint32_t)(32 * qd) << 16) + c0;  // lane quadrant, column group
+  const float ell2_i = m->ell2[i];
+  const float e2r_i = valid ? exp2f(ell2_i) : 0.0f;  // 2^{l2_i} = e^{l_i}; invalid rows: D = 0
 
   // CG start: x = 0, r = p = q_i (this thread's CW columns)
   float rho, nq, mP;
   {
     float qa[CW];
-    const uint4 *src = reinterpret_cast<const uint4 *>(q + (tokbase + i) * DH + c0);
 #pragma unroll
     for (int g = 0; g < NV; g++) {
-      const uint4 raw = valid ? src[g] : make_uint4(0, 0, 0, 0);
-      const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+      const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&qraw[g]);
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) qa[g * 8 + kk] = __bfloat162float(b[kk]);
     }
@@ -226,7 +253,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       s = fmaf(qa[d], qa[d], s);
       mx = fmaxf(mx, fabsf(qa[d]));
     }
-    rowred2<NG>(s, mx, scr, qd, grp, lane);
+    rowred2(s, mx);
     rho = s;
     nq = sqrtf(rho);
     mP = tc::pow2_ceil(mx);
@@ -246,71 +273,80 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     tc::tmem_st_wait();
   }
 
+  // Matrix descriptors: one K-major descriptor of the shared-memory base plus constants
+  // (in the descriptor's 16-byte units): a tile's offset, and for k-step s (K-major)
+  // (s / 4) 64-column blocks of 16 KB + (s % 4) 32 B, or (MN-major) 16 rows of 128 B.
+  // Built by the issuing thread only, so that no register holds them across the loop.
+  const uint32_t sbase = tc::smem_u32(sm);
+  auto kdesc = [&](uint32_t off, int s) -> uint64_t {
+    return tc::kmajor_desc(sbase, TILE, 0) + (uint64_t)((off >> 4) + (s >> 2) * (TILE * 128 / 16) + (s & 3) * 2);
+  };
+  auto kmn_desc = [&](int s) -> uint64_t {
+    return tc::mnmajor_desc(sbase + OFF_K, TILE, 0) + (uint64_t)(s * (2048 / 16));
+  };
   const uint32_t id_kk = tc::idesc_f16(TILE, DH, false, false);  // A, B K-major
   const uint32_t id_kmn = tc::idesc_f16(TILE, DH, false, true);  // B MN-major
-  uint32_t phase = 0;
-  bool act = valid;
-  int cnt = 0;
-  const bool dynamic = a.cg_tol > 0.0f;
-  bool failed = false;
 
-  // W (cols 128..255) = P K^T, committed to the barrier, then U (cols 0..127) = P S, which
-  // runs on the tensor pipe while the threads build Z from W.  U needs no commit of its own:
-  // the next commit (after Z K) completes only when every earlier MMA has completed.
-  // One thread issues.
-  auto issue_keys_then_state = [&]() {
-    const uint32_t dU = tbase + COL_U, dW = tbase + COL_W;
-#pragma unroll 1
+  // W (cols 128..255) = P K^T, committed to barrier A (thread 0).
+  auto issue_W = [&]() {
+#pragma unroll
     for (int s = 0; s < 8; s++) {
-      const uint64_t kb = tc::kmajor_desc(aK, TILE, s);
-      tc::mma_f16(dW, tc::kmajor_desc(aPhi, TILE, s), kb, id_kk, s > 0);
-      if (NTERMS == 2) tc::mma_f16(dW, tc::kmajor_desc(aPlo, TILE, s), kb, id_kk, true);
+      tc::mma_f16(tbase + COL_W, kdesc(OFF_PHI, s), kdesc(OFF_K, s), id_kk, s > 0);
+      if (NTERMS == 2) tc::mma_f16(tbase + COL_W, kdesc(OFF_PLO, s), kdesc(OFF_K, s), id_kk, true);
     }
-    tc::mma_commit(aBar);
-#pragma unroll 1
+    tc::mma_commit(aBarA);
+  };
+  // U (cols 0..127) = P S, committed to barrier U.  Issued by lane 0 of warp 4, which lies
+  // above the diagonal and has no Z to build: it may stall while the tensor pipe's queue is
+  // full without holding up the warps that build Z.
+  auto issue_U = [&]() {
+#pragma unroll
     for (int s = 0; s < 8; s++) {
-      const uint64_t ph = tc::kmajor_desc(aPhi, TILE, s), pl = tc::kmajor_desc(aPlo, TILE, s);
-      const uint64_t sh = tc::kmajor_desc(aShi, TILE, s), sl = tc::kmajor_desc(aSlo, TILE, s);
-      tc::mma_f16(dU, ph, sh, id_kk, s > 0);
+      tc::mma_f16(tbase + COL_U, kdesc(OFF_PHI, s), kdesc(OFF_SHI, s), id_kk, s > 0);
       if (NTERMS == 2) {
-        tc::mma_f16(dU, ph, sl, id_kk, true);
-        tc::mma_f16(dU, pl, sh, id_kk, true);
+        tc::mma_f16(tbase + COL_U, kdesc(OFF_PHI, s), kdesc(OFF_SLO, s), id_kk, true);
+        tc::mma_f16(tbase + COL_U, kdesc(OFF_PLO, s), kdesc(OFF_SHI, s), id_kk, true);
       }
     }
+    tc::mma_commit(aBarU);
   };
-  // Y (cols 128..255) = Z K, K read as an MN-major operand.
-  auto issue_intra = [&]() {
-    const uint32_t dY = tbase + COL_W;
-#pragma unroll 1
+  // Y (cols 128..255) = Z K, K read as an MN-major operand; barrier A (thread 0).
+  auto issue_Y = [&]() {
+#pragma unroll
     for (int s = 0; s < 8; s++) {
-      const uint64_t zh = tc::kmajor_desc(aZhi, TILE, s), zl = tc::kmajor_desc(aZlo, TILE, s);
-      const uint64_t kb = tc::mnmajor_desc(aK, TILE, s);
-      tc::mma_f16(dY, zh, kb, id_kmn, s > 0);
-      if (NTERMS == 2) tc::mma_f16(dY, zl, kb, id_kmn, true);
+      tc::mma_f16(tbase + COL_W, kdesc(OFF_ZHI, s), kmn_desc(s), id_kmn, s > 0);
+      if (NTERMS == 2) tc::mma_f16(tbase + COL_W, kdesc(OFF_ZLO, s), kmn_desc(s), id_kmn, true);
     }
-    tc::mma_commit(aBar);
+    tc::mma_commit(aBarA);
   };
-  auto wait_mma = [&]() -> bool {
-    const bool ok = tc::mbar_wait(aBar, phase);
-    phase ^= 1;
+  uint32_t phA = 0, phU = 0;
+  // Bounded wait for barrier A (and U); all threads agree on the outcome.
+  auto wait_mma = [&](bool with_u) -> bool {
+    bool ok = tc::mbar_wait(aBarA, phA);
+    phA ^= 1;
+    if (with_u) {
+      ok = tc::mbar_wait(aBarU, phU) && ok;
+      phU ^= 1;
+    }
     tc::fence_after_sync();
     const int bad = __syncthreads_or(!ok);
+    tc::fence_after_sync();
     if (bad && tid == 0) atomicOr(status, tc::kErrMmaTimeout);
     return !bad;
   };
-  // Z = (W * mrow / sK) o D into the Z operand; returns the row scale.
-  // Warps whose 32-column group lies entirely above the diagonal (every j > every row i
-  // of the quadrant) only write zeros: D_ij = 0 there.
-  const bool z_upper = c0 >= 32 * qd + 32;
+  // Z = (W mrow / sK) o D into the Z operand (warps above the diagonal keep their zeros);
+  // returns the row scale.  The column factor 2^{-l2_j} multiplies W here, the row factor
+  // goes into the scale.
   auto build_z = [&](float mrow) -> float {
     const float f = mrow / sK;
+    const float rowf = factored ? f * e2r_i : f;
     float w[CW];
     float zmax = 0.0f;
     if (!z_upper) {
       tc::tmem_ld<CW>(tl + COL_W, w);
       tc::tmem_ld_wait();
       if (factored) {
-        const float fr = f * e2r_i;
+        const bool diag = grp == qd;  // the only block that straddles the diagonal
 #pragma unroll
         for (int g = 0; g < CW / 4; g++) {
           const float4 ec = reinterpret_cast<const float4 *>(m->e2c + c0)[g];
@@ -318,7 +354,8 @@ __global__ void __launch_bounds__(128 * TPR, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; kk++) {
             const int j = c0 + 4 * g + kk;
-            w[4 * g + kk] = (j <= i) ? w[4 * g + kk] * fr * e4[kk] : 0.0f;
+            const float z = w[4 * g + kk] * e4[kk];
+            w[4 * g + kk] = (!diag || j <= i) ? z : 0.0f;
             zmax = fmaxf(zmax, fabsf(w[4 * g + kk]));
           }
         }
@@ -327,20 +364,16 @@ __global__ void __launch_bounds__(128 * TPR, 1)
         for (int kk = 0; kk < CW; kk++) {
           const int j = c0 + kk;
           const float dij = (valid && j <= i) ? exp2f(ell2_i - m->ell2[j]) : 0.0f;
-          w[kk] *= f * dij;
+          w[kk] *= dij;
           zmax = fmaxf(zmax, fabsf(w[kk]));
         }
       }
     }
-    const float zs = tc::pow2_ceil(rowred<NG, true>(zmax, scr, qd, grp, lane));
-    const float inv = 1.0f / zs;
+    const float zs = tc::pow2_ceil(rowred(zmax * rowf, true));
+    if (!z_upper) {
+      const float inv = rowf / zs;
 #pragma unroll
-    for (int g = 0; g < NV; g++) {
-      if (z_upper) {
-        const uint32_t off = tc::sw128_offset(i, c0 + 8 * g, TILE);
-        *reinterpret_cast<uint4 *>(Zhi + off) = make_uint4(0, 0, 0, 0);
-        if (NTERMS == 2) *reinterpret_cast<uint4 *>(Zlo + off) = make_uint4(0, 0, 0, 0);
-      } else {
+      for (int g = 0; g < NV; g++) {
         float x8[8];
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) x8[kk] = w[g * 8 + kk];
@@ -350,6 +383,11 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     return zs;
   };
 
+  bool act = valid;
+  int cnt = 0;
+  const bool dynamic = a.cg_tol > 0.0f;
+  bool failed = false;
+
   // ---- CG iterations ---------------------------------------------------------------------
   for (int it = 0; it < a.cg_iters; it++) {
     if (dynamic && act && sqrtf(rho) <= a.cg_tol * nq) act = false;
@@ -358,24 +396,25 @@ __global__ void __launch_bounds__(128 * TPR, 1)
     const int any = __syncthreads_or(act ? 1 : 0);
     tc::fence_after_sync();
     if (!any) break;
-    if (tid == 0) issue_keys_then_state();
-    if (!wait_mma()) {
+    if (tid == 0) issue_W();
+    if (!wait_mma(false)) {
       failed = true;
       break;
     }
+    if (tid == 128) issue_U();
     const float zs = build_z(mP);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (tid == 0) issue_intra();
-    if (!wait_mma()) {
+    if (tid == 0) issue_Y();
+    if (!wait_mma(true)) {
       failed = true;
       break;
     }
 
     // AP = e^l (mP/sS) U + (zs/sK) Y + lambda p   (kept in registers); sigma = p.AP
-    const float fu = el_i * mP / sS, fy = zs / sK;
+    const float fu = e2r_i * mP / sS, fy = zs / sK;
     float ap[CW];
     float sg = 0.0f;
     {
@@ -398,7 +437,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
         }
       }
     }
-    const float sigma = rowred<NG, false>(sg, scr, qd, grp, lane);
+    const float sigma = rowred(sg, false);
     const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
     // r -= alpha AP   (alpha = 0 leaves a finished row unchanged; the tensor-memory
     // accesses stay unconditional: they are warp-collective)
@@ -413,7 +452,7 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       rmax = fmaxf(rmax, fabsf(rr[kk]));
     }
     tc::tmem_st<CW>(tl + COL_R, rr);
-    rowred2<NG>(rn, rmax, scr, qd, grp, lane);
+    rowred2(rn, rmax);
     const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
     // one pass over the old p: x += alpha p and p = r + beta p, re-scaled so that
     // |p_new| <= max|r| + beta max|p| <= rmax + beta mP  (x's tensor-memory access stays
@@ -447,13 +486,15 @@ __global__ void __launch_bounds__(128 * TPR, 1)
 
   // ---- readout O = e^l X S^G^T + ((X K^T) o D) V ------------------------------------------
   if (!failed) {
+    tc::Rows8 vr;  // value tile, in flight during the staging below
+    tc::load_rows(v + tokbase * DH, Tv, vr);
     float xx[CW];
     tc::tmem_ld<CW>(tl + COL_X, xx);
     tc::tmem_ld_wait();
     float mx = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < CW; kk++) mx = fmaxf(mx, fabsf(xx[kk]));
-    const float mX = tc::pow2_ceil(rowred<NG, true>(mx, scr, qd, grp, lane));
+    const float mX = tc::pow2_ceil(rowred(mx, true));
     const float inv = 1.0f / mX;
 #pragma unroll
     for (int g = 0; g < NV; g++) {
@@ -462,24 +503,34 @@ __global__ void __launch_bounds__(128 * TPR, 1)
       for (int kk = 0; kk < 8; kk++) x8[kk] = xx[g * 8 + kk];
       st8<NTERMS>(Phi, Plo, i, c0 + 8 * g, x8, inv);
     }
-    const float sG = tc::stage_state(SG, CG, cf, Shi, NTERMS == 2 ? Slo : nullptr, m->red);
+    float sG, sV;
+    {
+      tc::Mat32 G;
+      tc::load_mat(SG, CG, cf, G);
+      float mG = tc::mat_absmax(G), mV = tc::rows_absmax(vr, nullptr), unused = 0.0f;
+      tc::block_max3(mG, mV, unused, m->red);
+      sG = 1.0f / tc::pow2_ceil(mG);
+      sV = 1.0f / tc::pow2_ceil(mV);
+      tc::store_mat(G, sG, Shi, NTERMS == 2 ? Slo : nullptr);
+    }
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (tid == 0) issue_keys_then_state();
-    failed = !wait_mma();
+    if (tid == 0) issue_W();
+    failed = !wait_mma(false);
     if (!failed) {
+      if (tid == 128) issue_U();
       const float zs = build_z(mX);
-      const float sV = tc::stage_rows(v + tokbase * DH, Tv, Ks, m->red);
+      tc::store_rows(vr, nullptr, sV, Ks, nullptr);  // X K^T is complete: K's slot is free
       tc::fence_smem_to_async();
       tc::fence_before_sync();
       __syncthreads();
       tc::fence_after_sync();
-      if (tid == 0) issue_intra();
-      failed = !wait_mma();
+      if (tid == 0) issue_Y();
+      failed = !wait_mma(true);
       if (!failed) {
-        const float fu = el_i * mX / sG, fy = zs / sV;
+        const float fu = e2r_i * mX / sG, fy = zs / sV;
         float uu[CW], yy[CW];
         tc::tmem_ld<CW>(tl + COL_U, uu);
         tc::tmem_ld<CW>(tl + COL_W, yy);
@@ -505,12 +556,6 @@ __global__ void __launch_bounds__(128 * TPR, 1)
   if (warp == 0) tc::tmem_free(tbase, 512);
 }
 
-// Threads per token row of the CG kernel (4: 512 threads x 32 columns, 8: 1024 x 16).
-// Measured on the bf16 B=8 H=16 T=4096 forward: 3.37 ms with 4, 4.02 ms with 8.
-#ifndef MESA_TC_THREADS_PER_ROW
-#define MESA_TC_THREADS_PER_ROW 4
-#endif
-constexpr int kTcThreadsPerRow = MESA_TC_THREADS_PER_ROW;
 // fp16 terms per staged operand: 2 (hi + lo, ~22 significant bits, 7 MMAs per CG step) or
 // 1 (11 bits, 3 MMAs per CG step).  Measured on the bf16 workloads: 1 term makes this kernel
 // 23 % faster (2.56 against 3.31 ms at B=8 H=16 T=4096) but the dynamic stopping rule then
@@ -520,18 +565,17 @@ constexpr int kTcThreadsPerRow = MESA_TC_THREADS_PER_ROW;
 #define MESA_TC_TERMS 2
 #endif
 static_assert(MESA_TC_TERMS == 1 || MESA_TC_TERMS == 2, "1 or 2 fp16 terms");
-static_assert(kTcThreadsPerRow == 4 || kTcThreadsPerRow == 8, "4 or 8 threads per row");
 
 int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status,
                        cudaStream_t st) {
   const int U = a.B * a.H;
   const int NC = (a.T + TILE - 1) / TILE;
-  auto kfn = mesa_cg_tc_kernel<kTcThreadsPerRow, MESA_TC_TERMS>;
+  auto kfn = mesa_cg_tc_kernel<MESA_TC_TERMS>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC) !=
       cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_TC, st);
-  kfn<<<dim3(NC, U), 128 * kTcThreadsPerRow, SMEM_TC, st>>>(a, ws, NC, status);
+  kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(a, ws, NC, status);
   timing_mark_end(K_CG_TC, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

@@ -206,6 +206,74 @@ __device__ __forceinline__ void store_rows(const Rows8 &x, const float *w, float
   }
 }
 
+// ---- register-held fp32 128 x 128 matrix (512 threads, 32 values each) ------------------
+// Group n of thread t covers element e = 8 t + 4096 n (row e / 128, columns e % 128 .. +7),
+// held as two float4.
+struct Mat32 {
+  float4 v[8];
+};
+
+// Load src + f * add (row-major fp32; src == nullptr: zero, add == nullptr: nothing added).
+// Needs blockDim.x == 512.
+__device__ __forceinline__ void load_mat(const float *src, const float *add, float f, Mat32 &x) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int n = 0; n < 4; n++) {
+    const int e = 8 * t + 4096 * n;
+    x.v[2 * n] = src ? *reinterpret_cast<const float4 *>(src + e) : make_float4(0, 0, 0, 0);
+    x.v[2 * n + 1] = src ? *reinterpret_cast<const float4 *>(src + e + 4) : make_float4(0, 0, 0, 0);
+  }
+  if (add) {
+#pragma unroll
+    for (int n = 0; n < 8; n++) {
+      const float4 y = *reinterpret_cast<const float4 *>(add + 8 * t + 4096 * (n >> 1) + 4 * (n & 1));
+      x.v[n].x = fmaf(f, y.x, x.v[n].x);
+      x.v[n].y = fmaf(f, y.y, x.v[n].y);
+      x.v[n].z = fmaf(f, y.z, x.v[n].z);
+      x.v[n].w = fmaf(f, y.w, x.v[n].w);
+    }
+  }
+}
+
+__device__ __forceinline__ float mat_absmax(const Mat32 &x) {
+  float mx = 0.0f;
+#pragma unroll
+  for (int n = 0; n < 8; n++)
+    mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.v[n].x), fabsf(x.v[n].y)), fmaxf(fabsf(x.v[n].z), fabsf(x.v[n].w))));
+  return mx;
+}
+
+// Store s * x as hi (+ lo) fp16 operands, 16 bytes per store.
+__device__ __forceinline__ void store_mat(const Mat32 &x, float s, uint8_t *hi, uint8_t *lo) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int n = 0; n < 4; n++) {
+    const int e = 8 * t + 4096 * n;
+    const float xs[8] = {x.v[2 * n].x * s,     x.v[2 * n].y * s,     x.v[2 * n].z * s,
+                         x.v[2 * n].w * s,     x.v[2 * n + 1].x * s, x.v[2 * n + 1].y * s,
+                         x.v[2 * n + 1].z * s, x.v[2 * n + 1].w * s};
+    __align__(16) __half2 h[4], l[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      h[k] = __floats2half2_rn(xs[2 * k], xs[2 * k + 1]);
+      const float2 back = __half22float2(h[k]);
+      l[k] = __floats2half2_rn(xs[2 * k] - back.x, xs[2 * k + 1] - back.y);
+    }
+    const uint32_t off = sw128_offset(e / DH, e % DH, TILE);
+    *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<uint4 *>(h);
+    if (lo) *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<uint4 *>(l);
+  }
+}
+
+// Hint the L2 to fetch `bytes` (a multiple of 128 * blockDim.x) starting at p: one 128-byte
+// line per thread and step.
+__device__ __forceinline__ void prefetch_l2(const void *p, size_t bytes) {
+  if (!p) return;
+  const char *c = reinterpret_cast<const char *>(p);
+  for (size_t o = (size_t)threadIdx.x * 128; o < bytes; o += (size_t)blockDim.x * 128)
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(c + o));
+}
+
 // Block-wide maxima of three values at once (red holds 3 floats per warp, 16 warps max).
 __device__ __forceinline__ void block_max3(float &a, float &b, float &c, float *red) {
 #pragma unroll
