@@ -237,21 +237,22 @@ __global__ void __launch_bounds__(512, 1)
   const float ell2_i = m->ell2[i];
   const float e2r_i = valid ? exp2f(ell2_i) : 0.0f;  // 2^{l2_i} = e^{l_i}; invalid rows: D = 0
 
-  // CG start: x = 0, r = p = q_i (this thread's CW columns)
+  // CG start: x = 0, r = p = q_i (this thread's CW columns).  p lives in shared memory as
+  // the scaled hi + lo MMA operand; each iteration reads it back once into registers.
   float rho, nq, mP;
   {
-    float qa[CW];
+    float p[CW];
 #pragma unroll
     for (int g = 0; g < NV; g++) {
       const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&qraw[g]);
 #pragma unroll
-      for (int kk = 0; kk < 8; kk++) qa[g * 8 + kk] = __bfloat162float(b[kk]);
+      for (int kk = 0; kk < 8; kk++) p[g * 8 + kk] = __bfloat162float(b[kk]);
     }
     float s = 0.0f, mx = 0.0f;
 #pragma unroll
     for (int d = 0; d < CW; d++) {
-      s = fmaf(qa[d], qa[d], s);
-      mx = fmaxf(mx, fabsf(qa[d]));
+      s = fmaf(p[d], p[d], s);
+      mx = fmaxf(mx, fabsf(p[d]));
     }
     rowred2(s, mx);
     rho = s;
@@ -261,13 +262,13 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
     for (int kk = 0; kk < CW; kk++) z[kk] = 0.0f;
     tc::tmem_st<CW>(tl + COL_X, z);
-    tc::tmem_st<CW>(tl + COL_R, qa);
+    tc::tmem_st<CW>(tl + COL_R, p);
     const float inv = 1.0f / mP;
 #pragma unroll
     for (int g = 0; g < NV; g++) {
       float x8[8];
 #pragma unroll
-      for (int kk = 0; kk < 8; kk++) x8[kk] = qa[g * 8 + kk];
+      for (int kk = 0; kk < 8; kk++) x8[kk] = p[g * 8 + kk];
       st8<NTERMS>(Phi, Plo, i, c0 + 8 * g, x8, inv);
     }
     tc::tmem_st_wait();
@@ -343,23 +344,29 @@ __global__ void __launch_bounds__(512, 1)
     float w[CW];
     float zmax = 0.0f;
     if (!z_upper) {
-      tc::tmem_ld<CW>(tl + COL_W, w);
-      tc::tmem_ld_wait();
       if (factored) {
         const bool diag = grp == qd;  // the only block that straddles the diagonal
 #pragma unroll
-        for (int g = 0; g < CW / 4; g++) {
-          const float4 ec = reinterpret_cast<const float4 *>(m->e2c + c0)[g];
-          const float e4[4] = {ec.x, ec.y, ec.z, ec.w};
+        for (int h = 0; h < CW / 16; h++) {
+          float wh[16];
+          tc::tmem_ld16(tl + COL_W + 16 * h, wh);
+          tc::tmem_ld_wait();
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++) {
-            const int j = c0 + 4 * g + kk;
-            const float z = w[4 * g + kk] * e4[kk];
-            w[4 * g + kk] = (!diag || j <= i) ? z : 0.0f;
-            zmax = fmaxf(zmax, fabsf(w[4 * g + kk]));
+          for (int g = 0; g < 4; g++) {
+            const float4 ec = reinterpret_cast<const float4 *>(m->e2c + c0 + 16 * h)[g];
+            const float e4[4] = {ec.x, ec.y, ec.z, ec.w};
+#pragma unroll
+            for (int kk = 0; kk < 4; kk++) {
+              const int j = c0 + 16 * h + 4 * g + kk;
+              const float z = wh[4 * g + kk] * e4[kk];
+              w[16 * h + 4 * g + kk] = (!diag || j <= i) ? z : 0.0f;
+              zmax = fmaxf(zmax, fabsf(w[16 * h + 4 * g + kk]));
+            }
           }
         }
       } else {
+        tc::tmem_ld<CW>(tl + COL_W, w);
+        tc::tmem_ld_wait();
 #pragma unroll
         for (int kk = 0; kk < CW; kk++) {
           const int j = c0 + kk;
@@ -387,6 +394,22 @@ __global__ void __launch_bounds__(512, 1)
   int cnt = 0;
   const bool dynamic = a.cg_tol > 0.0f;
   bool failed = false;
+  // x += alpha p of an iteration is applied at the start of the next (its tensor-memory
+  // traffic then overlaps the next W = P K^T) or after the last one
+  float p[CW];
+  float alpha_prev = 0.0f;
+  int iters_run = 0;  // completed iterations (the same in every thread)
+  auto x_update = [&](float al) {
+#pragma unroll
+    for (int h = 0; h < CW / 16; h++) {
+      float xx[16];
+      tc::tmem_ld16(tl + COL_X + 16 * h, xx);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int kk = 0; kk < 16; kk++) xx[kk] = fmaf(al, p[16 * h + kk], xx[kk]);
+      tc::tmem_st16(tl + COL_X + 16 * h, xx);
+    }
+  };
 
   // ---- CG iterations ---------------------------------------------------------------------
   for (int it = 0; it < a.cg_iters; it++) {
@@ -397,6 +420,9 @@ __global__ void __launch_bounds__(512, 1)
     tc::fence_after_sync();
     if (!any) break;
     if (tid == 0) issue_W();
+    __syncwarp();
+    // the previous iteration's x += alpha p runs while W = P K^T is on the tensor pipe
+    if (it > 0) x_update(alpha_prev);
     if (!wait_mma(false)) {
       failed = true;
       break;
@@ -408,86 +434,102 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) issue_Y();
+    // p back from its operand copy while Y = Z K and U = P S run
+#pragma unroll
+    for (int g = 0; g < NV; g++) {
+      float p8[8];
+      ld8<NTERMS>(Phi, Plo, i, c0 + 8 * g, mP, p8);
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) p[8 * g + kk] = p8[kk];
+    }
     if (!wait_mma(true)) {
       failed = true;
       break;
     }
 
-    // AP = e^l (mP/sS) U + (zs/sK) Y + lambda p   (kept in registers); sigma = p.AP
+    // AP = e^l (mP/sS) U + (zs/sK) Y + lambda p, written over U (whose columns are free
+    // until the next iteration's U = P S); sigma = p.AP.  The CG vectors move through
+    // tensor memory 16 columns at a time so that only p is held in registers.
     const float fu = e2r_i * mP / sS, fy = zs / sK;
-    float ap[CW];
     float sg = 0.0f;
-    {
-      float yy[CW];
-      tc::tmem_ld<CW>(tl + COL_U, ap);
-      tc::tmem_ld<CW>(tl + COL_W, yy);
+#pragma unroll
+    for (int h = 0; h < CW / 16; h++) {
+      float uu[16], yy[16];
+      tc::tmem_ld16(tl + COL_U + 16 * h, uu);
+      tc::tmem_ld16(tl + COL_W + 16 * h, yy);
       tc::tmem_ld_wait();
 #pragma unroll
-      for (int g = 0; g < NV; g++) {
-        float p8[8];
-        ld8<NTERMS>(Phi, Plo, i, c0 + 8 * g, mP, p8);
-        const float4 l0 = reinterpret_cast<const float4 *>(m->lam + c0 + 8 * g)[0];
-        const float4 l1 = reinterpret_cast<const float4 *>(m->lam + c0 + 8 * g)[1];
-        const float l8[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+      for (int g4 = 0; g4 < 4; g4++) {
+        const float4 l4 = reinterpret_cast<const float4 *>(m->lam + c0 + 16 * h)[g4];
+        const float l[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
-          const int e = g * 8 + kk;
-          ap[e] = fmaf(fu, ap[e], fmaf(fy, yy[e], l8[kk] * p8[kk]));
-          sg = fmaf(p8[kk], ap[e], sg);
+        for (int kk = 0; kk < 4; kk++) {
+          const int e = 4 * g4 + kk;
+          uu[e] = fmaf(fu, uu[e], fmaf(fy, yy[e], l[kk] * p[16 * h + e]));
+          sg = fmaf(p[16 * h + e], uu[e], sg);
         }
       }
+      tc::tmem_st16(tl + COL_U + 16 * h, uu);
     }
+    tc::tmem_st_wait();
     const float sigma = rowred(sg, false);
     const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
     // r -= alpha AP   (alpha = 0 leaves a finished row unchanged; the tensor-memory
     // accesses stay unconditional: they are warp-collective)
-    float rr[CW];
     float rn = 0.0f, rmax = 0.0f;
-    tc::tmem_ld<CW>(tl + COL_R, rr);
-    tc::tmem_ld_wait();
 #pragma unroll
-    for (int kk = 0; kk < CW; kk++) {
-      rr[kk] = fmaf(-alpha, ap[kk], rr[kk]);
-      rn = fmaf(rr[kk], rr[kk], rn);
-      rmax = fmaxf(rmax, fabsf(rr[kk]));
-    }
-    tc::tmem_st<CW>(tl + COL_R, rr);
-    rowred2(rn, rmax);
-    const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
-    // one pass over the old p: x += alpha p and p = r + beta p, re-scaled so that
-    // |p_new| <= max|r| + beta max|p| <= rmax + beta mP  (x's tensor-memory access stays
-    // unconditional; the p operand of a finished row is left as it is)
-    {
-      const float mNew = tc::pow2_ceil(rmax + beta * mP);
-      const float inv = 1.0f / mNew;
-      float xx[CW];
-      tc::tmem_ld<CW>(tl + COL_X, xx);
+    for (int h = 0; h < CW / 16; h++) {
+      float rr[16], aa[16];
+      tc::tmem_ld16(tl + COL_R + 16 * h, rr);
+      tc::tmem_ld16(tl + COL_U + 16 * h, aa);
       tc::tmem_ld_wait();
 #pragma unroll
-      for (int g = 0; g < NV; g++) {
-        float p8[8];
-        ld8<NTERMS>(Phi, Plo, i, c0 + 8 * g, mP, p8);
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) {
-          xx[g * 8 + kk] = fmaf(alpha, p8[kk], xx[g * 8 + kk]);
-          p8[kk] = fmaf(beta, p8[kk], rr[g * 8 + kk]);
-        }
-        if (act) st8<NTERMS>(Phi, Plo, i, c0 + 8 * g, p8, inv);
+      for (int kk = 0; kk < 16; kk++) {
+        rr[kk] = fmaf(-alpha, aa[kk], rr[kk]);
+        rn = fmaf(rr[kk], rr[kk], rn);
+        rmax = fmaxf(rmax, fabsf(rr[kk]));
       }
-      tc::tmem_st<CW>(tl + COL_X, xx);
-      if (act) {
-        mP = mNew;
-        rho = rn;
-        cnt++;
-      }
+      tc::tmem_st16(tl + COL_R + 16 * h, rr);
     }
     tc::tmem_st_wait();
+    rowred2(rn, rmax);
+    const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
+    // for an active row p = r + beta p, staged with the scale
+    // mNew >= max|r| + beta max|p| >= max|p_new|; the old p stays in registers for the
+    // deferred x += alpha p (a finished row keeps its p and has alpha = 0; the
+    // tensor-memory loads stay unconditional: they are warp-collective)
+    const float mNew = tc::pow2_ceil(rmax + beta * mP);
+    const float inv = 1.0f / mNew;
+#pragma unroll
+    for (int h = 0; h < CW / 16; h++) {
+      float rr[16];
+      tc::tmem_ld16(tl + COL_R + 16 * h, rr);
+      tc::tmem_ld_wait();
+      if (act) {
+#pragma unroll
+        for (int g = 0; g < 2; g++) {
+          float p8[8];
+#pragma unroll
+          for (int kk = 0; kk < 8; kk++) p8[kk] = fmaf(beta, p[16 * h + 8 * g + kk], rr[8 * g + kk]);
+          st8<NTERMS>(Phi, Plo, i, c0 + 16 * h + 8 * g, p8, inv);
+        }
+      }
+    }
+    if (act) {
+      mP = mNew;
+      rho = rn;
+      cnt++;
+    }
+    iters_run++;
+    alpha_prev = alpha;
   }
+  // the last iteration's x += alpha p
+  if (!failed && iters_run > 0) x_update(alpha_prev);
+  tc::tmem_st_wait();
 
   // ---- readout O = e^l X S^G^T + ((X K^T) o D) V ------------------------------------------
   if (!failed) {
-    tc::Rows8 vr;  // value tile, in flight during the staging below
-    tc::load_rows(v + tokbase * DH, Tv, vr);
+    tc::prefetch_l2(v + tokbase * DH, sizeof(__nv_bfloat16) * DH * Tv);  // the value tile
     float xx[CW];
     tc::tmem_ld<CW>(tl + COL_X, xx);
     tc::tmem_ld_wait();
@@ -504,9 +546,11 @@ __global__ void __launch_bounds__(512, 1)
       st8<NTERMS>(Phi, Plo, i, c0 + 8 * g, x8, inv);
     }
     float sG, sV;
+    tc::Rows8 vr;
     {
       tc::Mat32 G;
       tc::load_mat(SG, CG, cf, G);
+      tc::load_rows(v + tokbase * DH, Tv, vr);
       float mG = tc::mat_absmax(G), mV = tc::rows_absmax(vr, nullptr), unused = 0.0f;
       tc::block_max3(mG, mV, unused, m->red);
       sG = 1.0f / tc::pow2_ceil(mG);
