@@ -120,7 +120,7 @@ int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state,
  * its input and output buffers, or code recorded into a CUDA graph (cudaMalloc is not
  * allowed during stream capture).  Inputs, outputs and results are those of
  * mesa_forward_chunked with H0 = G0 = H_final = G_final = NULL.
- *   - Scratch: a fixed array of MESA_NOALLOC_MAX_BYTES (16 MiB) in the library's device
+ *   - Scratch: a fixed array of MESA_NOALLOC_MAX_BYTES (32 MiB) in the library's device
  *     image, held by every GPU that loads the library until the process exits.  A call
  *     whose mesa_forward_workspace_size() exceeds it returns MESA_ERR_WORKSPACE and
  *     enqueues nothing.
@@ -132,7 +132,7 @@ int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state,
  *     mesa_forward_status reads lives in the array too; it cannot be queried through this
  *     entry point.
  */
-#define MESA_NOALLOC_MAX_BYTES (16u << 20)
+#define MESA_NOALLOC_MAX_BYTES (32u << 20)
 int mesa_forward_chunked_noalloc(int B, int H, int T, int dk, int dv, int dtype, const void *q,
                                  const void *k, const void *v, const float *gamma,
                                  const float *lambda_diag, int cg_iters, float cg_tol, int chunk,

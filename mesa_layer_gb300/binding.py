@@ -181,7 +181,7 @@ def mesa_tc_selftest(A, B, stream=None):
     return C1, C2, C3, status
 
 
-NOALLOC_MAX_BYTES = 16 << 20
+NOALLOC_MAX_BYTES = 32 << 20
 
 
 def mesa_forward_chunked_noalloc(q, k, v, gamma, lambda_diag, cg_iters, cg_tol, chunk, out=None,

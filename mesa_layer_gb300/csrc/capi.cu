@@ -18,11 +18,23 @@ bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 constexpr size_t kStatusBytes = 256;
 
+// Chunk length the kernels work with.  Every chunk length gives the same outputs up to
+// rounding (the chunk split is an exact rewriting of the token recurrence); the CUDA-core
+// path for d <= 64 uses chunks of at most MESA_ROWS_CHUNK tokens, which shortens the
+// intra-chunk work of the last rows of a chunk (the critical path of its CG kernel).
+#ifndef MESA_ROWS_CHUNK
+#define MESA_ROWS_CHUNK 32
+#endif
+int work_chunk(int dk, int chunk) {
+  return (dk <= 64 && chunk > MESA_ROWS_CHUNK) ? MESA_ROWS_CHUNK : chunk;
+}
+
 // Workspace: [status word | log-decays | S^H states | S^G states | (d = 128) segment
-// log-decays Lc | segment carries].  Sized for `chunk`, which is <= 128, so it also covers
+// log-decays Lc | segment carries].  Sized for the working chunk (<= 128), so it also covers
 // the tensor-core path's 128-token chunks.
 size_t workspace_parts(int B, int H, int T, int dk, int dv, int chunk, size_t *off) {
   const size_t U = (size_t)B * H;
+  chunk = work_chunk(dk, chunk);
   const size_t NC = (size_t)(T + chunk - 1) / chunk;
   off[0] = kStatusBytes;
   off[1] = off[0] + align256(U * T * sizeof(float));
@@ -204,7 +216,7 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
 
   const bool tc = use_tc(dtype, dk, dv, q, k, v, out, H0, G0);
   mesa::FwdArgs a{B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol,
-                  tc ? 128 : chunk, out, iters_used, H0, G0, H_final, G_final};
+                  tc ? 128 : work_chunk(dk, chunk), out, iters_used, H0, G0, H_final, G_final};
   char *w = (char *)workspace;
   unsigned *status = (unsigned *)w;
   mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2]),

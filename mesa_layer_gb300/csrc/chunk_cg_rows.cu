@@ -30,14 +30,17 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
   const bool valid = i < Cv;
   const size_t tokbase = (size_t)u * T + t0;
 
+  // The two states are stored with a padded row stride SP = D + 4 (16-byte aligned rows):
+  // the transposed writes of S^G then spread over eight banks instead of one.
+  constexpr int SP = D + 4;
   extern __shared__ __align__(16) float smem[];
-  float *SH = smem;           // [D][D]  S^H_{c-1} (symmetric)
-  float *SGt = SH + D * D;    // [D][D]  (S^G_{c-1})^T
-  float *Ks = SGt + D * D;    // [C][D]
-  float *Vs = Ks + 128 * D;   // [C][D]
-  float *e2c = Vs + 128 * D;  // [C]  2^{-l2_j}
-  float *l2s = e2c + 128;     // [C]  l2_j = l_j log2(e)
-  float *lam = l2s + 128;     // [D]
+  float *SH = smem;           // [D][SP]  S^H_{c-1} (symmetric)
+  float *SGt = SH + D * SP;   // [D][SP]  (S^G_{c-1})^T
+  float *Ks = SGt + D * SP;   // [C][D]
+  float *Vs = Ks + C * D;     // [C][D]
+  float *e2c = Vs + C * D;    // [C]  2^{-l2_j}
+  float *l2s = e2c + C;       // [C]  l2_j = l_j log2(e)
+  float *lam = l2s + C;       // [D]
   __shared__ int factored_s;
 
   const TIO *q = (const TIO *)a.q, *k = (const TIO *)a.k, *v = (const TIO *)a.v;
@@ -50,9 +53,17 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
       S = a.H0 + (size_t)u * D * D;
       G = a.G0 + (size_t)u * D * D;
     }
-    for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
-      SH[e] = S ? S[e] : 0.0f;
-      SGt[(e % D) * D + e / D] = G ? G[e] : 0.0f;
+    // float4 loads (row r, columns c4 .. c4+3), several in flight per thread
+#pragma unroll 4
+    for (int e4 = threadIdx.x; e4 < D * D / 4; e4 += blockDim.x) {
+      const int r = (4 * e4) / D, c4 = (4 * e4) % D;
+      const float4 sv = S ? reinterpret_cast<const float4 *>(S)[e4] : make_float4(0, 0, 0, 0);
+      const float4 gv = G ? reinterpret_cast<const float4 *>(G)[e4] : make_float4(0, 0, 0, 0);
+      *reinterpret_cast<float4 *>(SH + r * SP + c4) = sv;
+      SGt[(c4 + 0) * SP + r] = gv.x;
+      SGt[(c4 + 1) * SP + r] = gv.y;
+      SGt[(c4 + 2) * SP + r] = gv.z;
+      SGt[(c4 + 3) * SP + r] = gv.w;
     }
     for (int e = threadIdx.x; e < C * D; e += blockDim.x) {
       const bool in = e / D < Cv;
@@ -109,7 +120,7 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
     for (int e = 0; e < D; e++) {
       // column e lives in lane part (e % 16) / 4, local index 4 (e / 16) + e % 4
       const float ze = el_i * __shfl_sync(0xffffffffu, z[4 * (e >> 4) + (e & 3)], quad0 + ((e & 15) >> 2));
-      const float4 *srow = reinterpret_cast<const float4 *>(Sm + e * D);
+      const float4 *srow = reinterpret_cast<const float4 *>(Sm + e * SP);
 #pragma unroll
       for (int n4 = 0; n4 < DC / 4; n4++) {
         const float4 sv = srow[4 * n4 + part];
@@ -133,15 +144,20 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
         kv[4 * n4 + 3] = t.w;
       }
     };
+    // a dot product over DC columns as four interleaved partial sums (short FMA chains)
+    auto dotp = [&](const float (&kv)[DC]) -> float {
+      float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int n = 0; n < DC; n++) t[n & 3] = fmaf(z[n], kv[n], t[n & 3]);
+      return (t[0] + t[1]) + (t[2] + t[3]);
+    };
     int j = 0;
     for (; j + JB <= jend; j += JB) {
       float kv[JB][DC], dot[JB];
 #pragma unroll
       for (int b = 0; b < JB; b++) {
         load(Kr, j + b, kv[b]);
-        dot[b] = 0.0f;
-#pragma unroll
-        for (int n = 0; n < DC; n++) dot[b] = fmaf(z[n], kv[b][n], dot[b]);
+        dot[b] = dotp(kv[b]);
       }
 #pragma unroll
       for (int b = 0; b < JB; b++) dot[b] += __shfl_xor_sync(0xffffffffu, dot[b], 1);
@@ -158,10 +174,7 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
     for (; j < jend; j++) {
       float kv[DC];
       load(Kr, j, kv);
-      float dot = 0.0f;
-#pragma unroll
-      for (int n = 0; n < DC; n++) dot = fmaf(z[n], kv[n], dot);
-      const float wgt = dec(j) * quad_sum(dot);
+      const float wgt = dec(j) * quad_sum(dotp(kv));
       if (Vr != Kr) load(Vr, j, kv);
 #pragma unroll
       for (int n = 0; n < DC; n++) y[n] = fmaf(wgt, kv[n], y[n]);
@@ -213,7 +226,7 @@ template <int D, typename TIO>
 static int launch_rows_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
   const int U = a.B * a.H, C = a.chunk;
   const int NC = (a.T + C - 1) / C;
-  const size_t smem = sizeof(float) * (2 * D * D + 2 * 128 * D + 2 * 128 + D);
+  const size_t smem = sizeof(float) * (2 * D * (D + 4) + 2 * C * D + 2 * C + D);
   auto kfn = mesa_cg_rows_kernel<D, TIO>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return -1;

@@ -103,11 +103,26 @@ __global__ void __launch_bounds__(256) mesa_scan_kernel(const float *__restrict_
   float *S = (isG ? ws.SG : ws.SH) + (size_t)u * NC * D * D + e;
   const float *S0 = isG ? G0 : H0;
   float s = S0 ? S0[(size_t)u * D * D + e] : 0.0f;
-  for (int c = 0; c < NC; c++) {
-    const int last = min(T, (c + 1) * C) - 1;
-    const float a = expf(ell[(size_t)u * T + last]);
-    s = fmaf(a, s, S[(size_t)c * D * D]);
-    S[(size_t)c * D * D] = s;
+  // groups of 8 chunks: the loads of a group are issued before its dependent updates
+  constexpr int G = 8;
+  for (int c0 = 0; c0 < NC; c0 += G) {
+    float dl[G], av[G];
+#pragma unroll
+    for (int g = 0; g < G; g++) {
+      const int c = c0 + g;
+      if (c < NC) {
+        dl[g] = S[(size_t)c * D * D];
+        av[g] = ell[(size_t)u * T + min(T, (c + 1) * C) - 1];
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; g++) {
+      const int c = c0 + g;
+      if (c < NC) {
+        s = fmaf(expf(av[g]), s, dl[g]);
+        S[(size_t)c * D * D] = s;
+      }
+    }
   }
   float *F = isG ? Gf : Hf;
   if (F) F[(size_t)u * D * D + e] = s;

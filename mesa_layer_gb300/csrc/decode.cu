@@ -336,7 +336,10 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
 
 // (Measured alternatives, 256 x 16 decode workload: H in shared memory with three units per
 // SM, 0.287 ms per step; a persistent kernel that streams the next unit's H and G in while
-// one unit per SM runs its CG, 0.328 ms; this kernel, two units per SM, 0.256 ms.)
+// one unit per SM runs its CG, 0.328 ms; this kernel, two units per SM, 0.256 ms.  A
+// persistent kernel with two CTAs per SM, the next unit's H streamed into shared memory and
+// G fetched into L2 during the CG: 0.269 against 0.264 ms in an interleaved comparison; its
+// phase clocks show the CG chain, ~1.5k cycles per iteration, taking 62 % of a unit's time.)
 constexpr int kDecode128Smem = (128 * 128 + 4 * 128 + 2 * 8) * sizeof(float);
 
 template <int D, typename TIO>

@@ -5,7 +5,7 @@
 // inside a framework that only passes it input and output buffers, or code that records
 // work into a CUDA graph, where cudaMalloc is not allowed while the stream is captured.
 // This entry point needs nothing from them beyond inputs and outputs: its scratch memory is
-// a fixed array in the library's device image (kNoAllocScratchBytes, 16 MiB), which every
+// a fixed array in the library's device image (kNoAllocScratchBytes, 32 MiB), which every
 // GPU that loads the library keeps until the process exits.
 //
 // The array's name in host code is only a host-side handle, not a device address, so the

@@ -51,9 +51,11 @@ def test_workspace_size(lib):
     assert ws(1, 1, 256, 17, 17, 64) == 0     # unsupported d
     assert ws(1, 1, 256, 64, 32, 64) == 0     # dk != dv
     assert ws(1, 1, 256, 64, 64, 48) == 0     # unsupported chunk
-    # state sections scale with the number of chunks (ceil(T / chunk))
-    a, b = ws(2, 4, 2048, 64, 64, 64), ws(2, 4, 2048, 64, 64, 128)
-    assert a > b
+    # state sections scale with the number of working chunks: ceil(T / chunk) for d = 128,
+    # ceil(T / min(chunk, 32)) for d <= 64 (the fp32 CUDA-core path's chunk cap)
+    assert ws(2, 4, 2048, 128, 128, 64) > ws(2, 4, 2048, 128, 128, 128)
+    assert ws(2, 4, 2048, 64, 64, 16) > ws(2, 4, 2048, 64, 64, 32)
+    assert ws(2, 4, 2048, 64, 64, 32) == ws(2, 4, 2048, 64, 64, 64) == ws(2, 4, 2048, 64, 64, 128)
 
 
 def _fwd(lib, **kw):

@@ -3,7 +3,7 @@ one, through the C ABI.
 
 It serves callers that cannot allocate device memory where they run the layer (a host that
 owns all GPU memory, a plugin that only gets its input and output buffers, code recorded
-into a CUDA graph); its scratch is a fixed 16 MiB array inside the library.  This file is
+into a CUDA graph); its scratch is a fixed 32 MiB array inside the library.  This file is
 collected last so that a run stopping at the first failure has run every other test first;
 it passes alone in a fresh process too.
 """
