@@ -44,8 +44,10 @@ struct Misc {
   float e2c[TILE];   // 2^{-l2_j} (used when the chunk's decays fit fp32 as factors)
   float lam[DH];     // Lambda diagonal of this head
   float red[48];
-  uint64_t mbar;    // barrier A: W = P K^T, then Y = Z K
-  uint64_t mbar_u;  // barrier U: U = P S
+  uint64_t mbar_w1;  // W = P K^T, keys 0..63
+  uint64_t mbar_w2;  // W = P K^T, keys 64..127 (and, issued before it, keys 0..63)
+  uint64_t mbar_y;   // Y = Z K
+  uint64_t mbar_u;   // U = P S
   uint32_t tmem_base;
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc block too large");
@@ -115,7 +117,8 @@ __global__ void __launch_bounds__(512, 1)
   uint8_t *Shi = sm + OFF_SHI, *Slo = sm + OFF_SLO, *Ks = sm + OFF_K;
   uint8_t *Phi = sm + OFF_PHI, *Plo = sm + OFF_PLO, *Zhi = sm + OFF_ZHI, *Zlo = sm + OFF_ZLO;
   Misc *m = reinterpret_cast<Misc *>(sm + OFF_MISC);
-  const uint32_t aBarA = tc::smem_u32(&m->mbar), aBarU = tc::smem_u32(&m->mbar_u);
+  const uint32_t aBarW1 = tc::smem_u32(&m->mbar_w1), aBarW2 = tc::smem_u32(&m->mbar_w2);
+  const uint32_t aBarY = tc::smem_u32(&m->mbar_y), aBarU = tc::smem_u32(&m->mbar_u);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, grp = warp >> 2;  // lane quadrant, column group
@@ -170,7 +173,9 @@ __global__ void __launch_bounds__(512, 1)
   // ---- set-up: tensor memory, barriers, per-chunk constants --------------------------
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 512);
   if (tid == 0) {
-    tc::mbar_init(aBarA, 1);
+    tc::mbar_init(aBarW1, 1);
+    tc::mbar_init(aBarW2, 1);
+    tc::mbar_init(aBarY, 1);
     tc::mbar_init(aBarU, 1);
   }
   bool small = true;  // |l2| <= 100: D_ij = 2^{l2_i} 2^{-l2_j} without overflow
@@ -288,18 +293,26 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t id_kk = tc::idesc_f16(TILE, DH, false, false);  // A, B K-major
   const uint32_t id_kmn = tc::idesc_f16(TILE, DH, false, true);  // B MN-major
 
-  // W (cols 128..255) = P K^T, committed to barrier A (thread 0).
+  // W (cols 128..255) = P K^T in two halves of 64 keys (N = 64), committed to barriers W1
+  // and W2 (thread 0): the warps whose 32 Z columns are keys 0..63 start on the first half
+  // while the tensor pipe computes the second.  Keys 64..127 are rows 64.. of the K tile,
+  // 8 KB further into each 64-column block.
+  const uint32_t id_kk64 = tc::idesc_f16(TILE, 64, false, false);
   auto issue_W = [&]() {
 #pragma unroll
-    for (int s = 0; s < 8; s++) {
-      tc::mma_f16(tbase + COL_W, kdesc(OFF_PHI, s), kdesc(OFF_K, s), id_kk, s > 0);
-      if (NTERMS == 2) tc::mma_f16(tbase + COL_W, kdesc(OFF_PLO, s), kdesc(OFF_K, s), id_kk, true);
+    for (int half = 0; half < 2; half++) {
+#pragma unroll
+      for (int s = 0; s < 8; s++) {
+        const uint64_t kb = kdesc(OFF_K, s) + (uint64_t)(half * (64 * 128 / 16));
+        tc::mma_f16(tbase + COL_W + 64 * half, kdesc(OFF_PHI, s), kb, id_kk64, s > 0);
+        if (NTERMS == 2) tc::mma_f16(tbase + COL_W + 64 * half, kdesc(OFF_PLO, s), kb, id_kk64, true);
+      }
+      tc::mma_commit(half ? aBarW2 : aBarW1);
     }
-    tc::mma_commit(aBarA);
   };
-  // U (cols 0..127) = P S, committed to barrier U.  Issued by lane 0 of warp 4, which lies
-  // above the diagonal and has no Z to build: it may stall while the tensor pipe's queue is
-  // full without holding up the warps that build Z.
+  // U (cols 0..127) = P S, committed to barrier U.  Issued by lane 0 of warp 4 once W is
+  // complete: warp 4 lies above the diagonal and has no Z to build, so it may stall while
+  // the tensor pipe's queue is full without holding up the warps that build Z.
   auto issue_U = [&]() {
 #pragma unroll
     for (int s = 0; s < 8; s++) {
@@ -311,25 +324,46 @@ __global__ void __launch_bounds__(512, 1)
     }
     tc::mma_commit(aBarU);
   };
-  // Y (cols 128..255) = Z K, K read as an MN-major operand; barrier A (thread 0).
+  // Y (cols 128..255) = Z K, K read as an MN-major operand; barrier Y (thread 0).
   auto issue_Y = [&]() {
 #pragma unroll
     for (int s = 0; s < 8; s++) {
       tc::mma_f16(tbase + COL_W, kdesc(OFF_ZHI, s), kmn_desc(s), id_kmn, s > 0);
       if (NTERMS == 2) tc::mma_f16(tbase + COL_W, kdesc(OFF_ZLO, s), kmn_desc(s), id_kmn, true);
     }
-    tc::mma_commit(aBarA);
+    tc::mma_commit(aBarY);
   };
-  uint32_t phA = 0, phU = 0;
-  // Bounded wait for barrier A (and U); all threads agree on the outcome.
-  auto wait_mma = [&](bool with_u) -> bool {
-    bool ok = tc::mbar_wait(aBarA, phA);
-    phA ^= 1;
-    if (with_u) {
-      ok = tc::mbar_wait(aBarU, phU) && ok;
-      phU ^= 1;
+  // Which half of W this warp waits for: the half holding its Z columns; warp 4 (which
+  // issues U) the second, which completes after the first; warps above the diagonal none.
+  const int w_half = (warp == 4) ? 2 : (z_upper ? 0 : (grp <= 1 ? 1 : 2));
+  uint32_t phW = 0, phY = 0, phU = 0;
+  // Bounded wait for this warp's half of W; no block-wide step (the outcome is agreed on at
+  // the barrier before Y is issued).
+  auto wait_W = [&]() -> bool {
+    bool ok = true;
+    if (w_half) {
+      ok = tc::mbar_wait(w_half == 1 ? aBarW1 : aBarW2, phW);
+      phW ^= 1;
     }
     tc::fence_after_sync();
+    return ok;
+  };
+  // Bounded waits for Y and U; all threads agree on the outcome.
+  auto wait_YU = [&]() -> bool {
+    bool ok = tc::mbar_wait(aBarY, phY);
+    phY ^= 1;
+    ok = tc::mbar_wait(aBarU, phU) && ok;
+    phU ^= 1;
+    tc::fence_after_sync();
+    const int bad = __syncthreads_or(!ok);
+    tc::fence_after_sync();
+    if (bad && tid == 0) atomicOr(status, tc::kErrMmaTimeout);
+    return !bad;
+  };
+  // The barrier before Y = Z K is issued, also agreeing on the outcome of the W waits.
+  auto sync_Z = [&](bool ok) -> bool {
+    tc::fence_smem_to_async();
+    tc::fence_before_sync();
     const int bad = __syncthreads_or(!ok);
     tc::fence_after_sync();
     if (bad && tid == 0) atomicOr(status, tc::kErrMmaTimeout);
@@ -423,16 +457,13 @@ __global__ void __launch_bounds__(512, 1)
     __syncwarp();
     // the previous iteration's x += alpha p runs while W = P K^T is on the tensor pipe
     if (it > 0) x_update(alpha_prev);
-    if (!wait_mma(false)) {
+    const bool okW = wait_W();
+    if (tid == 128 && okW) issue_U();
+    const float zs = build_z(mP);
+    if (!sync_Z(okW)) {
       failed = true;
       break;
     }
-    if (tid == 128) issue_U();
-    const float zs = build_z(mP);
-    tc::fence_smem_to_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
     if (tid == 0) issue_Y();
     // p back from its operand copy while Y = Z K and U = P S run
 #pragma unroll
@@ -442,7 +473,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) p[8 * g + kk] = p8[kk];
     }
-    if (!wait_mma(true)) {
+    if (!wait_YU()) {
       failed = true;
       break;
     }
@@ -562,17 +593,21 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) issue_W();
-    failed = !wait_mma(false);
+    __syncwarp();
+    const bool okW = wait_W();
+    if (tid == 128 && okW) issue_U();
+    const float zs = build_z(mX);
+    // X K^T is complete once every warp that waits on its halves has passed the barrier
+    // below, so V may only replace K after it
+    failed = !sync_Z(okW);
     if (!failed) {
-      if (tid == 128) issue_U();
-      const float zs = build_z(mX);
-      tc::store_rows(vr, nullptr, sV, Ks, nullptr);  // X K^T is complete: K's slot is free
+      tc::store_rows(vr, nullptr, sV, Ks, nullptr);
       tc::fence_smem_to_async();
       tc::fence_before_sync();
       __syncthreads();
       tc::fence_after_sync();
       if (tid == 0) issue_Y();
-      failed = !wait_mma(true);
+      failed = !wait_YU();
       if (!failed) {
         const float fu = e2r_i * mX / sG, fy = zs / sV;
         float uu[CW], yy[CW];
