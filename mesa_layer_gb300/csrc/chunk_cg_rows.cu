@@ -317,12 +317,14 @@ __global__ void __launch_bounds__(128, 4) mesa_cg_rows64_kernel(FwdArgs a, FwdWo
 #pragma unroll
     for (int r = 0; r < 2; r++) {
       float *zr = zw + (2 * g + r) * D;
-      *reinterpret_cast<float4 *>(zr + 4 * o) = make_float4(z[r][0], z[r][1], z[r][2], z[r][3]);
-      *reinterpret_cast<float4 *>(zr + 32 + 4 * o) = make_float4(z[r][4], z[r][5], z[r][6], z[r][7]);
+      const float f = el[r];  // the state term takes e^{l_i} z
+      *reinterpret_cast<float4 *>(zr + 4 * o) = make_float4(f * z[r][0], f * z[r][1], f * z[r][2], f * z[r][3]);
+      *reinterpret_cast<float4 *>(zr + 32 + 4 * o) =
+          make_float4(f * z[r][4], f * z[r][5], f * z[r][6], f * z[r][7]);
     }
     __syncwarp();
     const float *z0 = zw + (2 * g) * D, *z1 = z0 + D;
-#pragma unroll 4
+#pragma unroll 8
     for (int e4 = 0; e4 < D / 4; e4++) {
       const float4 za = reinterpret_cast<const float4 *>(z0)[e4];
       const float4 zc = reinterpret_cast<const float4 *>(z1)[e4];
@@ -331,7 +333,7 @@ __global__ void __launch_bounds__(128, 4) mesa_cg_rows64_kernel(FwdArgs a, FwdWo
       for (int ee = 0; ee < 4; ee++) {
         float s8[8];
         ld_row(Sm + (4 * e4 + ee) * SP, s8);
-        const float ze0 = el[0] * a4[ee], ze1 = el[1] * b4[ee];
+        const float ze0 = a4[ee], ze1 = b4[ee];
 #pragma unroll
         for (int n = 0; n < 8; n++) {
           y[0][n] = fmaf(ze0, s8[n], y[0][n]);
