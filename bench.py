@@ -55,33 +55,33 @@ def parse_args():
     return p.parse_args()
 
 
-def source_digest() -> str:
-    """sha256 over the library's sources (kernels, headers): DRAM traffic figures recorded
-    in profiles/traffic.json hold only for the sources they were measured on."""
-    import glob
+def source_digest(files) -> str:
+    """sha256 over the named library source files (paths relative to the repository)."""
     import hashlib
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "mesa_layer_gb300", "csrc", "*")) +
-                   glob.glob(os.path.join(ROOT, "include", "*.h")))
     for f in files:
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+        h.update(f.encode())
+        with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
 
 
 def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu record, or None
-    when there is none or the sources changed since it was taken."""
+    when there is none or the kernel's sources changed since it was taken (each entry names
+    the files its kernel is built from and their sha256)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
-    if rec.get("source_sha256") != source_digest():
-        return None
     entry = rec.get("workloads", {}).get(workload)
     if not entry or entry.get("kernel") != kernel:
+        return None
+    try:
+        if source_digest(entry["sources"]) != entry.get("sources_sha256"):
+            return None
+    except (KeyError, OSError):
         return None
     return entry.get("dram_bytes_per_launch")
 
