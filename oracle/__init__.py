@@ -62,6 +62,10 @@ def _bind(lib):
     lib.oracle_state_trace.argtypes = [ctypes.c_int] * 3 + [_D] * 5
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
+    lib.oracle_qk_preprocess.restype = None
+    lib.oracle_qk_preprocess.argtypes = [ctypes.c_int] * 5 + [_D] * 3
+    lib.oracle_qk_preprocess_step.restype = None
+    lib.oracle_qk_preprocess_step.argtypes = [ctypes.c_int] * 4 + [_D] * 4
     return lib
 
 
@@ -159,3 +163,31 @@ def state_trace(k, v, gamma, lib=None):
     Ga = np.zeros((T, dv, dk))
     lib.oracle_state_trace(T, dk, dv, _ptr(k), _ptr(v), _ptr(gamma), _ptr(Ha), _ptr(Ga))
     return Ha, Ga
+
+
+def qk_preprocess(x, w, lib=None):
+    """Query/key preprocessing ("Arquitetura (MesaNet)", "Pre-processamento"): causal
+    depthwise convolution over time with W taps per (head, channel), then each token divided
+    by its Euclidean norm.  x: [B, heads, T, d]; w: [heads, d, W] (tap s multiplies the input
+    s tokens back).  Returns [B, heads, T, d] fp64."""
+    lib = lib or load()
+    x, w = _f64(x), _f64(w)
+    B, heads, T, d = x.shape
+    W = w.shape[-1]
+    out = np.zeros_like(x)
+    lib.oracle_qk_preprocess(B * heads, heads, T, d, W, _ptr(x), _ptr(w), _ptr(out))
+    return out
+
+
+def qk_preprocess_step(x, w, hist, lib=None):
+    """One decode step of qk_preprocess.  x: [N, heads, d]; w: [heads, d, W]; hist:
+    [N, heads, W-1, d] float64 C-contiguous, the previous raw inputs (hist[..., s, :] is the
+    input s+1 tokens back), updated in place.  Returns [N, heads, d] fp64."""
+    lib = lib or load()
+    assert hist.dtype == np.float64 and hist.flags.c_contiguous
+    x, w = _f64(x), _f64(w)
+    N, heads, d = x.shape
+    W = w.shape[-1]
+    out = np.zeros_like(x)
+    lib.oracle_qk_preprocess_step(N * heads, heads, d, W, _ptr(x), _ptr(w), _ptr(hist), _ptr(out))
+    return out

@@ -220,6 +220,67 @@ void oracle_state_trace(int T, int dk, int dv, const double *k, const double *v,
   free(G);
 }
 
+/*
+ * Query/key preprocessing before the layer: section "Arquitetura (MesaNet)", the
+ * "Pre-processamento" bullet (keys and queries are normalised and convolved with a small
+ * window before the Mesa layer).  Readings taken where the page is silent:
+ *   - the convolution is causal and depthwise over time: W taps per (head, channel),
+ *     y_t[c] = sum_{s=0..W-1} w[c][s] x_{t-s}[c], with x_{t'} = 0 before the first token;
+ *   - the normalisation is the Euclidean one over the d channels of a token and comes
+ *     last (the layer's inputs are L2-normalised): out_t = y_t / ||y_t||_2; a zero y_t
+ *     stays zero.
+ *   x [U, T, d], w [heads, d, W], out [U, T, d]; unit u uses head u % heads.
+ */
+static void normalise(int d, const double *y, double *out) {
+  double s = 0.0;
+  for (int c = 0; c < d; c++) s += y[c] * y[c];
+  const double n = sqrt(s);
+  for (int c = 0; c < d; c++) out[c] = n > 0.0 ? y[c] / n : 0.0;
+}
+
+void oracle_qk_preprocess(int U, int heads, int T, int d, int W, const double *x,
+                          const double *w, double *out) {
+  double *y = (double *)malloc(sizeof(double) * (d > 0 ? d : 1));
+  for (int u = 0; u < U; u++) {
+    const double *wu = w + (size_t)(u % heads) * d * W;
+    for (int t = 0; t < T; t++) {
+      for (int c = 0; c < d; c++) {
+        double acc = 0.0;
+        for (int s = 0; s < W && s <= t; s++)
+          acc += wu[(size_t)c * W + s] * x[((size_t)u * T + (t - s)) * d + c];
+        y[c] = acc;
+      }
+      normalise(d, y, out + ((size_t)u * T + t) * d);
+    }
+  }
+  free(y);
+}
+
+/*
+ * One decode step of the same preprocessing.  hist [U, W-1, d] holds the unit's previous
+ * raw inputs, hist[u][s] = x_{t-1-s} (zeros before the first token); on return it holds
+ * the window moved on by the current input x [U, d].  out [U, d].
+ */
+void oracle_qk_preprocess_step(int U, int heads, int d, int W, const double *x,
+                               const double *w, double *hist, double *out) {
+  double *y = (double *)malloc(sizeof(double) * (d > 0 ? d : 1));
+  for (int u = 0; u < U; u++) {
+    const double *wu = w + (size_t)(u % heads) * d * W;
+    double *hu = hist + (size_t)u * (W - 1) * d;
+    const double *xu = x + (size_t)u * d;
+    for (int c = 0; c < d; c++) {
+      double acc = wu[(size_t)c * W] * xu[c];
+      for (int s = 1; s < W; s++) acc += wu[(size_t)c * W + s] * hu[(size_t)(s - 1) * d + c];
+      y[c] = acc;
+    }
+    normalise(d, y, out + (size_t)u * d);
+    for (int s = W - 2; s >= 1; s--)
+      memcpy(hu + (size_t)s * d, hu + (size_t)(s - 1) * d, sizeof(double) * d);
+    if (W > 1) memcpy(hu, xu, sizeof(double) * d);
+  }
+  free(y);
+}
+
 /* Exposed so callers can record how many host threads the oracle may use. */
 int oracle_max_threads(void) {
 #ifdef _OPENMP
