@@ -128,6 +128,12 @@ def state_flops(w) -> float:
     return float(w.B * w.H * w.T) * 4.0 * w.dk * w.dk
 
 
+def preprocess_bytes(w) -> float:
+    """Raw q and k read once, preprocessed q and k written once, plus the taps."""
+    esz = 2 if w.dtype == "bf16" else 4
+    return float(w.B * w.H * w.T * w.dk) * esz * 2 * 2 + 2.0 * w.H * w.dk * w.conv_taps * 4
+
+
 def decode_bytes(w) -> float:
     """Per unit and step: H and G read and written in fp32, plus q, k, v, gamma, out, iters."""
     esz = 2 if w.dtype == "bf16" else 4
@@ -206,6 +212,18 @@ def oracle_sample(w, budget_s: float = 20.0):
     import oracle
 
     threads = oracle.max_threads()
+    if w.conv_taps:
+        units = min(w.B * w.H, 8)
+        inp = synth.preprocess_inputs(synth.workload(w.name, B=1, H=units))
+        total, dt, passes = 0, 0.0, 0
+        while dt < budget_s / 4 or passes == 0:
+            t0 = time.perf_counter()
+            oracle.qk_preprocess(inp["q_raw"], inp["wq"])
+            oracle.qk_preprocess(inp["k_raw"], inp["wk"])
+            dt += time.perf_counter() - t0
+            total += units * w.T
+            passes += 1
+        return total / dt / w.H, 1, f"{passes} pass(es) over {units} (batch, head) units x {w.T} tokens, q and k", dt
     if w.decode_steps:
         units = min(w.B * w.H, 64 * max(1, threads))
         steps = 8
@@ -283,6 +301,10 @@ def workload_config(w, extra=None):
     if w.decode_steps:
         cfg.update({"sequences": w.B, "decode_steps": w.decode_steps, "prefix": w.prefix})
         cfg.pop("T")
+    if w.conv_taps:
+        cfg = {"workload": w.name, "B": w.B, "heads": w.H, "T": w.T, "d": w.dk, "qk_dtype": w.dtype,
+               "conv_taps": w.conv_taps, "step": "q/k preprocessing: causal depthwise conv + L2 norm",
+               "parallelism": "replicas"}
     cfg.update(extra or {})
     return cfg
 
@@ -332,7 +354,9 @@ def main():
     names = kind_names(lib)
     dev = torch.device("cuda", local)
     peaks = measured_peaks()
-    if w.decode_steps:
+    if w.conv_taps:
+        res = bench_preprocess(args, w, rank, world, dev, lib, torch, binding)
+    elif w.decode_steps:
         res = bench_decode(args, w, rank, world, dev, lib, torch, binding)
     else:
         res = bench_forward(args, w, rank, world, dev, lib, torch, binding)
@@ -498,6 +522,50 @@ def bench_decode(args, w, rank, world, dev, lib, torch, binding):
     return res
 
 
+def bench_preprocess(args, w, rank, world, dev, lib, torch, binding):
+    import torch.distributed as dist
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    inp = synth.preprocess_inputs(w, seed=rank)
+    d_in = {k: torch.from_numpy(v).to(dev).to(td if k.endswith("_raw") else torch.float32).contiguous()
+            for k, v in inp.items()}
+    qo, ko = torch.empty_like(d_in["q_raw"]), torch.empty_like(d_in["k_raw"])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    in_bytes = sum(d_in[k].numel() * d_in[k].element_size() for k in ("q_raw", "k_raw"))
+    needs_flush = in_bytes < 2 * (129 << 20)
+
+    def step(i):
+        binding.mesa_qk_preprocess(d_in["q_raw"], d_in["k_raw"], d_in["wq"], d_in["wk"], q_out=qo, k_out=ko)
+
+    res = timed_loop(args, torch, lib, step, (lambda: flush.random_(0, 255)) if needs_flush else None,
+                     world, dist, dev)
+    res.update({"iters": np.zeros(1, dtype=np.int32), "tokens_per_step": w.B * w.T, "flush": needs_flush})
+    if not args.no_e2e:
+        h = {k: torch.from_numpy(inp[k]).to(td).pin_memory() for k in ("q_raw", "k_raw")}
+        d = {k: torch.empty_like(h[k], device=dev) for k in h}
+        hq, hk = torch.empty_like(h["q_raw"]).pin_memory(), torch.empty_like(h["k_raw"]).pin_memory()
+
+        def estep():
+            for k in h:
+                d[k].copy_(h[k], non_blocking=True)
+            binding.mesa_qk_preprocess(d["q_raw"], d["k_raw"], d_in["wq"], d_in["wk"], q_out=qo, k_out=ko)
+            hq.copy_(qo, non_blocking=True)
+            hk.copy_(ko, non_blocking=True)
+
+        for _ in range(3):
+            estep()
+        torch.cuda.synchronize()
+        n = max(3, min(args.steps, 50))
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record()
+        for _ in range(n):
+            estep()
+        e_.record()
+        torch.cuda.synchronize()
+        nb = sum(t.numel() * t.element_size() for t in h.values())
+        res["e2e"] = {"ms_per_step": s_.elapsed_time(e_) / n, "h2d": nb, "d2h": nb}
+    return res
+
+
 def aggregate(step_ms: float, tokens_per_rank: int, world: int, torch, dist, device="cuda"):
     """Whole-job figures of a replicated run: the slowest rank's time per step and the
     tokens of all ranks.  Each rank runs its own replica (independent sequences), so the
@@ -524,7 +592,13 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
     launches_per_step = sum(kind_n) / args.steps
     it = res["iters"]
     traffic = recorded_traffic(w.name, top_name)
-    if w.decode_steps:
+    if w.conv_taps:
+        bytes_ = preprocess_bytes(w)
+        achieved = bytes_ / (avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": top_name,
+                "peak_source": peaks["source"], "algorithmic_bytes": bytes_}
+    elif w.decode_steps:
         bytes_ = decode_bytes(w)
         achieved = bytes_ / (avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -548,10 +622,11 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
     kernels = {names[i] if i < len(names) else f"kind{i}": {"ms_per_step": kind_ms[i] / args.steps,
                                                              "launches": kind_n[i]}
                for i in range(len(kind_ms)) if kind_n[i] > 0}
-    extra = {"mean_iters": float(it.mean()), "max_iters": int(it.max()),
+    extra = {} if w.conv_taps else {"mean_iters": float(it.mean()), "max_iters": int(it.max())}
+    extra.update({
              "l2": ("flushed between timed steps (256 MiB device write)" if res["flush"]
                     else "working set larger than L2, not flushed"),
-             "kernels": kernels, "wall_s_timed_loop": res["wall_s"]}
+             "kernels": kernels, "wall_s_timed_loop": res["wall_s"]})
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, see mesa_layer_gb300/synth.py)",

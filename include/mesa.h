@@ -68,8 +68,10 @@ const char *mesa_status_string(int status);
 /*
  * Bytes of device workspace mesa_forward_chunked needs for these sizes (256-byte
  * aligned start required).  It holds a status word, the per-token log-decays [B, H, T] and the
- * chunk-boundary states S^H_c [B, H, ceil(T/chunk), dk, dk] and
- * S^G_c [B, H, ceil(T/chunk), dv, dk] in fp32.  Returns 0 for unsupported sizes.
+ * chunk-boundary states S^H_c [B, H, NC, dk, dk] and S^G_c [B, H, NC, dv, dk] in fp32, where
+ * NC = ceil(T / C) and C = chunk (C = min(chunk, 32) when dk <= 64: that path works on chunks
+ * of at most 32 tokens), plus, for dk = 128, segment carries of the tensor-core path.
+ * Returns 0 for unsupported sizes.
  */
 size_t mesa_forward_workspace_size(int B, int H, int T, int dk, int dv, int chunk);
 
@@ -91,6 +93,7 @@ size_t mesa_forward_workspace_size(int B, int H, int T, int dk, int dv, int chun
  *   H_final, G_final  NULL or [B, H, dk, dk] / [B, H, dv, dk] fp32: states after token T-1
  *             (both or neither)
  *   workspace device scratch of at least mesa_forward_workspace_size() bytes
+ * B * H <= 65535 (MESA_ERR_UNSUPPORTED otherwise).
  */
 int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const void *q,
                          const void *k, const void *v, const float *gamma,
@@ -112,6 +115,35 @@ int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state,
                      float *G_state, const void *q, const void *k, const void *v,
                      const float *gamma, const float *lambda_diag, int cg_iters,
                      float cg_tol, void *out, int32_t *iters_used, cudaStream_t stream);
+
+/*
+ * Query/key preprocessing in front of the layer ("Arquitetura (MesaNet)",
+ * "Pre-processamento": keys and queries are normalised and convolved with a small window
+ * before the Mesa layer).  For each (batch, head) unit, channel c and token t, for q and k:
+ *   y_t[c] = sum_{s=0..W-1} w[h][c][s] x_{t-s}[c]   (x before the first token is 0)
+ *   out_t  = y_t / ||y_t||_2                         (a zero y_t gives 0)
+ * -- a causal depthwise convolution, then the Euclidean normalisation of each token.
+ *   q_raw, k_raw [B, H, T, d] dtype; wq, wk [H, d, W] fp32 (unit b*H + h uses head h);
+ *   q_out, k_out [B, H, T, d] dtype, not aliasing the inputs.
+ *   d in {16, 32, 64, 128}; 1 <= W <= 8; B * H <= 65535; activations 16-byte aligned.
+ * Device pointers; nothing is allocated; asynchronous on `stream`.  Errors: INVALID_ARG for
+ * bad sizes, pointers or aliasing, UNSUPPORTED for d or B * H, CUDA for a failed launch.
+ */
+int mesa_qk_preprocess(int B, int H, int T, int d, int W, int dtype, const void *q_raw,
+                       const void *k_raw, const float *wq, const float *wk, void *q_out,
+                       void *k_out, cudaStream_t stream);
+
+/*
+ * One decode step of mesa_qk_preprocess for N sequences x H heads.
+ *   q_raw, k_raw, q_out, k_out [N, H, d] dtype (16-byte aligned)
+ *   conv_state [N, H, 2, W-1, d] fp32 (in/out; [.., 0, ..] for q, [.., 1, ..] for k): the
+ *   previous raw inputs, [.., s, :] being the one s+1 tokens back (zeros at the start of a
+ *   sequence, or the last W-1 raw inputs of its prefill); on return it has moved on by this
+ *   step's inputs.  May be NULL when W = 1.
+ */
+int mesa_qk_preprocess_step(int N, int H, int d, int W, int dtype, const void *q_raw,
+                            const void *k_raw, const float *wq, const float *wk,
+                            float *conv_state, void *q_out, void *k_out, cudaStream_t stream);
 
 /*
  * mesa_forward_chunked without a caller-provided workspace (no counterpart on the MesaNet

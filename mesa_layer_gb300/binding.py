@@ -58,6 +58,10 @@ def load(build_if_missing: bool = True):
     lib.mesa_tc_selftest.argtypes = [_vp] * 6 + [_vp]
     lib.mesa_decode_step.restype = _i
     lib.mesa_decode_step.argtypes = [_i] * 5 + [_fp, _fp, _vp, _vp, _vp, _fp, _fp, _i, _f, _vp, _ip, _vp]
+    lib.mesa_qk_preprocess.restype = _i
+    lib.mesa_qk_preprocess.argtypes = [_i] * 6 + [_vp, _vp, _fp, _fp, _vp, _vp, _vp]
+    lib.mesa_qk_preprocess_step.restype = _i
+    lib.mesa_qk_preprocess_step.argtypes = [_i] * 5 + [_vp, _vp, _fp, _fp, _fp, _vp, _vp, _vp]
     _lib = lib
     return lib
 
@@ -155,6 +159,50 @@ def mesa_decode_step(H_state, G_state, q, k, v, gamma, lambda_diag, cg_iters, cg
                               _ptr(out), _ptr(iters_used), _stream(stream))
     _check(st, "mesa_decode_step")
     return out, iters_used
+
+
+def mesa_qk_preprocess(q_raw, k_raw, wq, wk, q_out=None, k_out=None, stream=None):
+    """Query/key preprocessing: causal depthwise convolution with W taps per (head, channel),
+    then each token divided by its Euclidean norm.  q_raw, k_raw [B, H, T, d] (fp32 or bf16),
+    wq, wk [H, d, W] fp32.  Returns (q_out, k_out) of the input dtype."""
+    lib = load()
+    B, H, T, d = q_raw.shape
+    W = wq.shape[-1]
+    code = _dtype_code(q_raw)
+    _require(q_raw, "q_raw")
+    _require(k_raw, "k_raw", q_raw.dtype)
+    _require(wq, "wq", torch.float32)
+    _require(wk, "wk", torch.float32)
+    if q_out is None:
+        q_out = torch.empty_like(q_raw)
+    if k_out is None:
+        k_out = torch.empty_like(k_raw)
+    st = lib.mesa_qk_preprocess(B, H, T, d, W, code, _ptr(q_raw), _ptr(k_raw), _ptr(wq), _ptr(wk),
+                                _ptr(q_out), _ptr(k_out), _stream(stream))
+    _check(st, "mesa_qk_preprocess")
+    return q_out, k_out
+
+
+def mesa_qk_preprocess_step(q_raw, k_raw, wq, wk, conv_state, q_out=None, k_out=None, stream=None):
+    """One decode step of the preprocessing.  q_raw, k_raw [N, H, d]; conv_state
+    [N, H, 2, W-1, d] fp32, updated in place (None when W = 1).  Returns (q_out, k_out)."""
+    lib = load()
+    N, H, d = q_raw.shape
+    W = wq.shape[-1]
+    code = _dtype_code(q_raw)
+    _require(q_raw, "q_raw")
+    _require(k_raw, "k_raw", q_raw.dtype)
+    _require(wq, "wq", torch.float32)
+    _require(wk, "wk", torch.float32)
+    _require(conv_state, "conv_state", torch.float32)
+    if q_out is None:
+        q_out = torch.empty_like(q_raw)
+    if k_out is None:
+        k_out = torch.empty_like(k_raw)
+    st = lib.mesa_qk_preprocess_step(N, H, d, W, code, _ptr(q_raw), _ptr(k_raw), _ptr(wq), _ptr(wk),
+                                     _ptr(conv_state), _ptr(q_out), _ptr(k_out), _stream(stream))
+    _check(st, "mesa_qk_preprocess_step")
+    return q_out, k_out
 
 
 def mesa_forward_status(workspace, stream=None) -> int:

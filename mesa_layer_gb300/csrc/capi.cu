@@ -9,6 +9,7 @@
 namespace {
 
 constexpr int kMaxIters = 4096;
+constexpr size_t kMaxUnits = 65535;  // (batch, head) units index a grid dimension
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -145,6 +146,7 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_CG_TC: return "mesa_cg_tc_kernel";
     case mesa::K_DELTA_TC: return "mesa_states_tc_kernel";
     case mesa::K_CG_ROWS: return "mesa_cg_rows_kernel";
+    case mesa::K_PREPROC: return "mesa_qk_preprocess_kernel";
   }
   return nullptr;
 }
@@ -195,6 +197,7 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
   if ((H0 == nullptr) != (G0 == nullptr) || (H_final == nullptr) != (G_final == nullptr))
     return MESA_ERR_INVALID_ARG;
   if (!dim_ok(dk) || dv != dk || !chunk_ok(chunk)) return MESA_ERR_UNSUPPORTED;
+  if ((size_t)B * H > kMaxUnits) return MESA_ERR_UNSUPPORTED;
   const size_t U = (size_t)B * H;
   if (U == 0) return MESA_OK;
   if (!lambda_diag) return MESA_ERR_INVALID_ARG;
@@ -245,6 +248,38 @@ int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state, fl
   mesa::DecArgs a{N, H, dk, dv, dtype, H_state, G_state, q, k, v, gamma, lambda_diag,
                   cg_iters, cg_tol, out, iters_used};
   return mesa::launch_decode(a, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
+}
+
+int mesa_qk_preprocess(int B, int H, int T, int d, int W, int dtype, const void *q_raw,
+                       const void *k_raw, const float *wq, const float *wk, void *q_out,
+                       void *k_out, cudaStream_t stream) {
+  if (B < 0 || H < 0 || T < 0 || W < 1 || W > 8) return MESA_ERR_INVALID_ARG;
+  if (dtype != MESA_F32 && dtype != MESA_BF16) return MESA_ERR_INVALID_ARG;
+  if (!dim_ok(d)) return MESA_ERR_UNSUPPORTED;
+  if ((size_t)B * H > kMaxUnits) return MESA_ERR_UNSUPPORTED;
+  if ((size_t)B * H * T == 0) return MESA_OK;
+  if (!q_raw || !k_raw || !wq || !wk || !q_out || !k_out) return MESA_ERR_INVALID_ARG;
+  if (!aligned(q_raw, 16) || !aligned(k_raw, 16) || !aligned(q_out, 16) || !aligned(k_out, 16))
+    return MESA_ERR_INVALID_ARG;
+  if (q_raw == q_out || k_raw == k_out) return MESA_ERR_INVALID_ARG;
+  mesa::PreArgs a{B * H, H, T, d, W, dtype, q_raw, k_raw, wq, wk, nullptr, q_out, k_out};
+  return mesa::launch_qk_preprocess(a, false, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
+}
+
+int mesa_qk_preprocess_step(int N, int H, int d, int W, int dtype, const void *q_raw,
+                            const void *k_raw, const float *wq, const float *wk,
+                            float *conv_state, void *q_out, void *k_out, cudaStream_t stream) {
+  if (N < 0 || H < 0 || W < 1 || W > 8) return MESA_ERR_INVALID_ARG;
+  if (dtype != MESA_F32 && dtype != MESA_BF16) return MESA_ERR_INVALID_ARG;
+  if (!dim_ok(d)) return MESA_ERR_UNSUPPORTED;
+  if ((size_t)N * H == 0) return MESA_OK;
+  if (!q_raw || !k_raw || !wq || !wk || !q_out || !k_out || (W > 1 && !conv_state))
+    return MESA_ERR_INVALID_ARG;
+  if (!aligned(q_raw, 16) || !aligned(k_raw, 16) || !aligned(q_out, 16) || !aligned(k_out, 16) ||
+      (W > 1 && !aligned(conv_state, 16)))
+    return MESA_ERR_INVALID_ARG;
+  mesa::PreArgs a{N * H, H, 0, d, W, dtype, q_raw, k_raw, wq, wk, conv_state, q_out, k_out};
+  return mesa::launch_qk_preprocess(a, true, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -33,9 +33,19 @@ struct DecArgs {
   int32_t *iters;
 };
 
+// Query/key preprocessing (causal depthwise convolution + L2 normalisation).
+struct PreArgs {
+  int U, H, T, d, W, dtype;  // U = B * H units (sequence form) or N * H (step form)
+  const void *q_raw, *k_raw;
+  const float *wq, *wk;       // [H, d, W]
+  float *conv_state;          // step form: [U, 2, W-1, d]
+  void *q_out, *k_out;
+};
+
 // Kernel kinds, for the optional per-kernel timing of benchmarks (mesa_timing_*).
 enum KernelKind {
-  K_ELL = 0, K_DELTA = 1, K_SCAN = 2, K_CG_SIMT = 3, K_DECODE = 4, K_CG_TC = 5, K_DELTA_TC = 6, K_CG_ROWS = 7, K_NUM_KINDS = 8
+  K_ELL = 0, K_DELTA = 1, K_SCAN = 2, K_CG_SIMT = 3, K_DECODE = 4, K_CG_TC = 5, K_DELTA_TC = 6, K_CG_ROWS = 7,
+  K_PREPROC = 8, K_NUM_KINDS = 9
 };
 
 // Record a timing event before / after a launch of `kind` on `st` (no-op unless enabled).
@@ -58,5 +68,7 @@ int launch_tc_selftest(const float *A, const float *B, float *C1, float *C2, flo
 // segment-local states, segment carries and the final state (see FwdWorkspace).
 int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st);
 int launch_decode(const DecArgs &a, cudaStream_t st);
+// step == false: whole sequences [U, T, d]; step == true: one decode step [U, d].
+int launch_qk_preprocess(const PreArgs &a, bool step, cudaStream_t st);
 
 }  // namespace mesa

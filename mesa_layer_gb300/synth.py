@@ -21,7 +21,7 @@ from dataclasses import dataclass, replace
 
 import numpy as np
 
-_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "gamma": 4, "lam": 5}
+_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "gamma": 4, "lam": 5, "q_raw": 6, "k_raw": 7, "wq": 8, "wk": 9}
 
 
 @dataclass(frozen=True)
@@ -44,6 +44,7 @@ class Workload:
     lam_hi: float
     decode_steps: int = 0      # > 0: recurrent decode workload (B = sequences)
     prefix: int = 0            # decode: tokens folded into the state before the steps
+    conv_taps: int = 0         # > 0: query/key preprocessing workload with this window
 
     @property
     def tokens(self) -> int:
@@ -67,6 +68,9 @@ WORKLOADS = {
                  "sigmoid", 5.0, 1.5, 0.05, 0.5),
         Workload("decode_bf16_d128", 5, "bf16", 256, 16, 1, 128, 128, 64, 30, 1e-3,
                  "sigmoid", 4.0, 1.0, 0.05, 0.5, decode_steps=512, prefix=1024),
+        # query/key preprocessing in front of the layer, on the shape of fwd_bf16_d128
+        Workload("qkpre_bf16_d128", 6, "bf16", 8, 16, 4096, 128, 128, 64, 0, 0.0,
+                 "sigmoid", 4.0, 1.0, 0.05, 0.5, conv_taps=4),
     ]
 }
 WORKLOAD_ORDER = [w.name for w in sorted(WORKLOADS.values(), key=lambda w: w.wid)]
@@ -142,4 +146,18 @@ def decode_inputs(w: Workload, step: int, seed: int = 0) -> dict:
         "k": _cast(w, _unit_rows(_rng(seed, w.wid, "k", s), (N, H, w.dk))),
         "v": _cast(w, _rng(seed, w.wid, "v", s).standard_normal(size=(N, H, w.dv), dtype=np.float32)),
         "gamma": _gamma(w, _rng(seed, w.wid, "gamma", s), (N, H)),
+    }
+
+
+def preprocess_inputs(w: Workload, taps: int | None = None, seed: int = 0) -> dict:
+    """Raw queries and keys of the preprocessing workloads: q_raw, k_raw [B, H, T, dk]
+    ~ N(0, 1) rounded to the workload dtype; convolution taps wq, wk [H, dk, taps]
+    ~ N(0, 1 / taps) in fp32 (tap s multiplies the input s tokens back)."""
+    W = taps or w.conv_taps or 4
+    shape = (w.B, w.H, w.T, w.dk)
+    return {
+        "q_raw": _cast(w, _rng(seed, w.wid, "q_raw").standard_normal(size=shape, dtype=np.float32)),
+        "k_raw": _cast(w, _rng(seed, w.wid, "k_raw").standard_normal(size=shape, dtype=np.float32)),
+        "wq": (_rng(seed, w.wid, "wq").standard_normal(size=(w.H, w.dk, W)) / np.sqrt(W)).astype(np.float32),
+        "wk": (_rng(seed, w.wid, "wk").standard_normal(size=(w.H, w.dk, W)) / np.sqrt(W)).astype(np.float32),
     }

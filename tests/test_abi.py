@@ -109,3 +109,30 @@ def test_binding_raises_without_gpu_or_library():
     q = torch.zeros(1, 1, 4, 16)
     with pytest.raises(Exception):
         binding.mesa_forward_chunked(q, q, q, torch.ones(1, 1, 4), torch.ones(1, 16), 2, 0.0, 16)
+
+
+def test_qk_preprocess_validation(lib):
+    f = lib.mesa_qk_preprocess
+    p = ctypes.c_void_p(256)
+    args = lambda **kw: [kw.get(k, v) for k, v in dict(B=1, H=2, T=8, d=64, W=4, dtype=0, q=p, k=p, wq=p, wk=p,
+                                                     qo=ctypes.c_void_p(512), ko=ctypes.c_void_p(768), st=None).items()]
+    assert f(*args(W=0)) == 1 and f(*args(W=9)) == 1          # window out of range
+    assert f(*args(dtype=5)) == 1
+    assert f(*args(d=48)) == 2                                  # unsupported channel count
+    assert f(*args(B=70000)) == 2                               # B * H over the grid limit
+    assert f(*args(q=None)) == 1 and f(*args(wk=None)) == 1
+    assert f(*args(qo=p)) == 1                                  # output aliases the input
+    assert f(*args(q=ctypes.c_void_p(264))) == 1                # misaligned activation
+    assert f(*args(T=0)) == 0                                   # nothing to do, nothing enqueued
+
+
+def test_qk_preprocess_step_validation(lib):
+    f = lib.mesa_qk_preprocess_step
+    p = ctypes.c_void_p(256)
+    args = lambda **kw: [kw.get(k, v) for k, v in dict(N=2, H=2, d=32, W=3, dtype=1, q=p, k=p, wq=p, wk=p,
+                                                     cs=p, qo=p, ko=p, st=None).items()]
+    assert f(*args(W=0)) == 1 and f(*args(W=9)) == 1
+    assert f(*args(d=24)) == 2
+    assert f(*args(cs=None)) == 1                               # a window needs its state
+    assert f(*args(cs=ctypes.c_void_p(264))) == 1               # misaligned state
+    assert f(*args(N=0)) == 0
