@@ -62,6 +62,11 @@ def _bind(lib):
     lib.oracle_state_trace.argtypes = [ctypes.c_int] * 3 + [_D] * 5
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
+    lib.oracle_cg_from.restype = ctypes.c_int
+    lib.oracle_cg_from.argtypes = [ctypes.c_int, _D, _D, _D, _D, ctypes.c_int, ctypes.c_double, _D, _D]
+    lib.oracle_decode_step_from.restype = ctypes.c_int
+    lib.oracle_decode_step_from.argtypes = [ctypes.c_int] * 4 + [_D] * 7 + [
+        ctypes.c_int, ctypes.c_double, _D, _D, _I, ctypes.c_int]
     lib.oracle_qk_preprocess.restype = None
     lib.oracle_qk_preprocess.argtypes = [ctypes.c_int] * 5 + [_D] * 3
     lib.oracle_qk_preprocess_step.restype = None
@@ -95,14 +100,20 @@ def max_threads(lib=None) -> int:
     return (lib or load()).oracle_max_threads()
 
 
-def cg(Hm, lam, q, maxit, tol=0.0, lib=None):
-    """Textbook CG on (Hm + diag(lam)) x = q from x0 = 0.  Returns (x, iterations)."""
+def cg(Hm, lam, q, maxit, tol=0.0, x0=None, lib=None):
+    """Textbook CG on (Hm + diag(lam)) x = q from x0 (None: 0; the stopping rule stays
+    relative to ||q||).  Returns (x, iterations)."""
     lib = lib or load()
     Hm, lam, q = _f64(Hm), _f64(lam), _f64(q)
     n = q.shape[0]
     x = np.zeros(n)
     work = np.zeros(3 * n)
-    it = lib.oracle_cg(n, _ptr(Hm), _ptr(lam), _ptr(q), int(maxit), float(tol), _ptr(x), _ptr(work))
+    if x0 is None:
+        it = lib.oracle_cg(n, _ptr(Hm), _ptr(lam), _ptr(q), int(maxit), float(tol), _ptr(x), _ptr(work))
+    else:
+        x0 = _f64(x0)
+        it = lib.oracle_cg_from(n, _ptr(Hm), _ptr(lam), _ptr(q), _ptr(x0), int(maxit), float(tol), _ptr(x),
+                                _ptr(work))
     return x, it
 
 
@@ -133,10 +144,12 @@ def forward(q, k, v, gamma, lam, cg_iters, cg_tol=0.0, replay=None, H0=None, G0=
     return out, iters
 
 
-def decode_step(Hs, Gs, q, k, v, gamma, lam, cg_iters, cg_tol=0.0, nthreads=None, lib=None):
+def decode_step(Hs, Gs, q, k, v, gamma, lam, cg_iters, cg_tol=0.0, nthreads=None, X=None, lib=None):
     """One decode step, in place on the fp64 states Hs [N, heads, dk, dk] and
     Gs [N, heads, dv, dk] (must be float64 C-contiguous).  q, k: [N, heads, dk];
-    v: [N, heads, dv]; gamma: [N, heads].  Returns (out [N, heads, dv], iters [N, heads])."""
+    v: [N, heads, dv]; gamma: [N, heads].  X: None, or [N, heads, dk] float64 C-contiguous,
+    the start of each unit's CG (warm start), replaced in place by this step's solution.
+    Returns (out [N, heads, dv], iters [N, heads])."""
     lib = lib or load()
     assert Hs.dtype == np.float64 and Hs.flags.c_contiguous
     assert Gs.dtype == np.float64 and Gs.flags.c_contiguous
@@ -146,9 +159,15 @@ def decode_step(Hs, Gs, q, k, v, gamma, lam, cg_iters, cg_tol=0.0, nthreads=None
     out = np.zeros((N, heads, dv))
     iters = np.zeros((N, heads), dtype=np.int32)
     nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
-    lib.oracle_decode_step(N * heads, heads, dk, dv, _ptr(Hs), _ptr(Gs), _ptr(q), _ptr(k), _ptr(v),
-                           _ptr(gamma), _ptr(lam), int(cg_iters), float(cg_tol), _ptr(out),
-                           _ptr(iters, _I), int(nt))
+    if X is None:
+        lib.oracle_decode_step(N * heads, heads, dk, dv, _ptr(Hs), _ptr(Gs), _ptr(q), _ptr(k), _ptr(v),
+                               _ptr(gamma), _ptr(lam), int(cg_iters), float(cg_tol), _ptr(out),
+                               _ptr(iters, _I), int(nt))
+    else:
+        assert X.dtype == np.float64 and X.flags.c_contiguous
+        lib.oracle_decode_step_from(N * heads, heads, dk, dv, _ptr(Hs), _ptr(Gs), _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(gamma), _ptr(lam), int(cg_iters), float(cg_tol), _ptr(X), _ptr(out),
+                                    _ptr(iters, _I), int(nt))
     return out, iters
 
 

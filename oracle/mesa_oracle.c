@@ -65,22 +65,35 @@ static double dot(int n, const double *a, const double *b) {
 }
 
 /*
- * Textbook conjugate gradient on (H + diag(lam)) x = q, started from x = 0.
+ * Textbook conjugate gradient on (H + diag(lam)) x = q, started from x0 (x0 == NULL: from
+ * x = 0, then r0 = q).  From a given x0 the first residual is r0 = q - (H + diag(lam)) x0;
+ * the dynamic stopping rule stays relative to ||q|| (the same accuracy target as from 0).
  *   maxit: iteration cap (fixed mode: exact count)
  *   tol  : > 0 selects the dynamic stopping rule ||r|| <= tol ||q||, else fixed
  *   work : 3n doubles of scratch
  * Returns the number of iterations executed.
+ * Warm start is the reading of the pages' remark ("Significancia") that warm-start
+ * strategies could lower the CG cost: the previous decode step's solution as x0.
  */
-int oracle_cg(int n, const double *H, const double *lam, const double *q,
-              int maxit, double tol, double *x, double *work) {
+int oracle_cg_from(int n, const double *H, const double *lam, const double *q,
+                   const double *x0, int maxit, double tol, double *x, double *work) {
   double *r = work, *p = work + n, *w = work + 2 * n;
-  for (int i = 0; i < n; i++) {
-    x[i] = 0.0;
-    r[i] = q[i];
-    p[i] = q[i];
+  if (x0) {
+    spd_apply(n, H, lam, x0, w);
+    for (int i = 0; i < n; i++) {
+      x[i] = x0[i];
+      r[i] = q[i] - w[i];
+      p[i] = r[i];
+    }
+  } else {
+    for (int i = 0; i < n; i++) {
+      x[i] = 0.0;
+      r[i] = q[i];
+      p[i] = q[i];
+    }
   }
   double rho = dot(n, r, r);
-  const double qnorm = sqrt(rho);
+  const double qnorm = x0 ? sqrt(dot(n, q, q)) : sqrt(rho);
   int it = 0;
   for (; it < maxit; it++) {
     if (tol > 0.0 && sqrt(rho) <= tol * qnorm) break;
@@ -99,19 +112,24 @@ int oracle_cg(int n, const double *H, const double *lam, const double *q,
   return it;
 }
 
+int oracle_cg(int n, const double *H, const double *lam, const double *q,
+              int maxit, double tol, double *x, double *work) {
+  return oracle_cg_from(n, H, lam, q, NULL, maxit, tol, x, work);
+}
+
 /* One token of the recurrence on one unit: decay and rank-1 update of H and G,
  * the CG solve, and the readout o = G x.  H is dk x dk, G is dv x dk. */
 static int mesa_token(int dk, int dv, double *H, double *G, const double *q,
                       const double *k, const double *v, double gamma,
                       const double *lam, int maxit, double tol, double *o,
-                      double *x, double *work) {
+                      double *x, double *work, const double *x0) {
   for (int a = 0; a < dk; a++)
     for (int b = 0; b < dk; b++)
       H[(size_t)a * dk + b] = gamma * H[(size_t)a * dk + b] + k[a] * k[b];
   for (int a = 0; a < dv; a++)
     for (int b = 0; b < dk; b++)
       G[(size_t)a * dk + b] = gamma * G[(size_t)a * dk + b] + v[a] * k[b];
-  const int it = oracle_cg(dk, H, lam, q, maxit, tol, x, work);
+  const int it = oracle_cg_from(dk, H, lam, q, x0, maxit, tol, x, work);
   for (int a = 0; a < dv; a++) o[a] = dot(dk, G + (size_t)a * dk, x);
   return it;
 }
@@ -159,7 +177,7 @@ int oracle_forward(int U, int heads, int T, int dk, int dv, const double *q,
       }
       iters[tok] = mesa_token(dk, dv, H, G, q + tok * dk, k + tok * dk,
                               v + tok * dv, gamma[tok], lam_u, maxit, tol,
-                              out + tok * dv, x, work);
+                              out + tok * dv, x, work, NULL);
     }
     if (H_final) memcpy(H_final + (size_t)u * dk * dk, H, sizeof(double) * dk * dk);
     if (G_final) memcpy(G_final + (size_t)u * dv * dk, G, sizeof(double) * dv * dk);
@@ -175,25 +193,38 @@ int oracle_forward(int U, int heads, int T, int dk, int dv, const double *q,
  * One recurrent decode step for N sequences x heads units, in place:
  *   H [U, dk, dk], G [U, dv, dk] (in/out), q, k [U, dk], v [U, dv], gamma [U],
  *   lam [heads, dk], out [U, dv], iters [U]; U = N * heads.
+ *   X: NULL (CG from 0) or [U, dk] in/out: the start of each unit's CG (warm start, e.g. the
+ *   previous step's solution), replaced by this step's solution.
  * Returns the number of threads used.
  */
-int oracle_decode_step(int U, int heads, int dk, int dv, double *H, double *G,
-                       const double *q, const double *k, const double *v,
-                       const double *gamma, const double *lam, int cg_iters,
-                       double cg_tol, double *out, int32_t *iters, int nthreads) {
+int oracle_decode_step_from(int U, int heads, int dk, int dv, double *H, double *G,
+                            const double *q, const double *k, const double *v,
+                            const double *gamma, const double *lam, int cg_iters,
+                            double cg_tol, double *X, double *out, int32_t *iters,
+                            int nthreads) {
   const int nt = pick_threads(nthreads, U);
 #pragma omp parallel for schedule(dynamic, 4) num_threads(nt)
   for (int u = 0; u < U; u++) {
     double *x = (double *)malloc(sizeof(double) * dk);
     double *work = (double *)malloc(sizeof(double) * 3 * dk);
+    double *xu = X ? X + (size_t)u * dk : NULL;
     iters[u] = mesa_token(dk, dv, H + (size_t)u * dk * dk, G + (size_t)u * dv * dk,
                           q + (size_t)u * dk, k + (size_t)u * dk, v + (size_t)u * dv,
                           gamma[u], lam + (size_t)(u % heads) * dk, cg_iters,
-                          cg_tol, out + (size_t)u * dv, x, work);
+                          cg_tol, out + (size_t)u * dv, x, work, xu);
+    if (xu) memcpy(xu, x, sizeof(double) * dk);
     free(x);
     free(work);
   }
   return nt;
+}
+
+int oracle_decode_step(int U, int heads, int dk, int dv, double *H, double *G,
+                       const double *q, const double *k, const double *v,
+                       const double *gamma, const double *lam, int cg_iters,
+                       double cg_tol, double *out, int32_t *iters, int nthreads) {
+  return oracle_decode_step_from(U, heads, dk, dv, H, G, q, k, v, gamma, lam, cg_iters,
+                                 cg_tol, NULL, out, iters, nthreads);
 }
 
 /*
