@@ -138,7 +138,8 @@ def decode_bytes(w) -> float:
     """Per unit and step: H and G read and written in fp32, plus q, k, v, gamma, out, iters."""
     esz = 2 if w.dtype == "bf16" else 4
     U = w.B * w.H
-    return float(U) * (2 * 4 * (w.dk * w.dk + w.dv * w.dk) + esz * (2 * w.dk + 2 * w.dv) + 4 + 4)
+    warm = 2 * 4 * w.dk if w.warm else 0  # the start vector read and written
+    return float(U) * (2 * 4 * (w.dk * w.dk + w.dv * w.dk) + esz * (2 * w.dk + 2 * w.dv) + 4 + 4 + warm)
 
 
 # ------------------------------------------------------------------------------------------
@@ -235,9 +236,10 @@ def oracle_sample(w, budget_s: float = 20.0):
         lam = synth.lambdas(w)[np.arange(units) % w.H]  # unit i keeps its head's lambda
         Hs = np.zeros((1, units, w.dk, w.dk))
         Gs = np.zeros((1, units, w.dv, w.dk))
+        X = np.zeros((1, units, w.dk)) if w.warm else None
         t0 = time.perf_counter()
         for _ in range(steps):
-            oracle.decode_step(Hs, Gs, q, k, v, g, lam, w.cg_iters, w.cg_tol, nthreads=threads)
+            oracle.decode_step(Hs, Gs, q, k, v, g, lam, w.cg_iters, w.cg_tol, nthreads=threads, X=X)
         dt = time.perf_counter() - t0
         return units * steps / dt / w.H, min(threads, units), f"{units} (sequence, head) units x {steps} steps", dt
     # forward: whole units (sequences are sequential in t); the unit count grows until one
@@ -301,6 +303,8 @@ def workload_config(w, extra=None):
     if w.decode_steps:
         cfg.update({"sequences": w.B, "decode_steps": w.decode_steps, "prefix": w.prefix})
         cfg.pop("T")
+        if w.warm:
+            cfg["cg"] += ", warm start from the previous step's solution"
     if w.conv_taps:
         cfg = {"workload": w.name, "B": w.B, "heads": w.H, "T": w.T, "d": w.dk, "qk_dtype": w.dtype,
                "conv_taps": w.conv_taps, "step": "q/k preprocessing: causal depthwise conv + L2 norm",
@@ -470,7 +474,14 @@ def bench_decode(args, w, rank, world, dev, lib, torch, binding):
     lam = torch.from_numpy(synth.lambdas(w)).to(dev)
     Hs = torch.zeros(N, H, d, d, device=dev)
     Gs = torch.zeros(N, H, w.dv, d, device=dev)
+    Xs = torch.zeros(N, H, d, device=dev) if w.warm else None
     out = torch.empty(N, H, w.dv, dtype=td, device=dev)
+
+    def decode(q, k, v, g):
+        if Xs is not None:
+            binding.mesa_decode_step_warm(Hs, Gs, Xs, q, k, v, g, lam, w.cg_iters, w.cg_tol, out=out, iters_used=iters)
+        else:
+            binding.mesa_decode_step(Hs, Gs, q, k, v, g, lam, w.cg_iters, w.cg_tol, out=out, iters_used=iters)
     iters = torch.empty(N, H, dtype=torch.int32, device=dev)
 
     def dev_inputs(s):
@@ -487,8 +498,7 @@ def bench_decode(args, w, rank, world, dev, lib, torch, binding):
 
     def step(i):
         x = steps[i % n_steps]
-        binding.mesa_decode_step(Hs, Gs, x["q"], x["k"], x["v"], x["gamma"], lam, w.cg_iters, w.cg_tol,
-                                 out=out, iters_used=iters)
+        decode(x["q"], x["k"], x["v"], x["gamma"])
 
     res = timed_loop(args, torch, lib, step, None, world, dist, dev)
     res.update({"iters": iters.cpu().numpy(), "tokens_per_step": N, "flush": False})
@@ -501,8 +511,7 @@ def bench_decode(args, w, rank, world, dev, lib, torch, binding):
         def estep():
             for k in h:
                 dd[k].copy_(h[k], non_blocking=True)
-            binding.mesa_decode_step(Hs, Gs, dd["q"], dd["k"], dd["v"], dd["gamma"], lam, w.cg_iters, w.cg_tol,
-                                     out=out, iters_used=iters)
+            decode(dd["q"], dd["k"], dd["v"], dd["gamma"])
             h_out.copy_(out, non_blocking=True)
             h_it.copy_(iters, non_blocking=True)
 

@@ -117,6 +117,21 @@ int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state,
                      float cg_tol, void *out, int32_t *iters_used, cudaStream_t stream);
 
 /*
+ * mesa_decode_step with a warm-started CG (no counterpart in the pages beyond their remark,
+ * "Significancia", that warm-start strategies could lower the CG cost): each unit's CG starts
+ * from X_state instead of 0, with r0 = q - (H_state + Lambda) X_state, and the stopping rule
+ * stays relative to ||q|| (the same accuracy target); on return X_state holds this step's
+ * solution, the start of the next step.
+ *   X_state [N, H, dk] fp32 (in/out, 16-byte aligned); zeros give exactly mesa_decode_step.
+ * Other arguments, layouts and errors as mesa_decode_step.
+ */
+int mesa_decode_step_warm(int N, int H, int dk, int dv, int dtype, float *H_state,
+                          float *G_state, float *X_state, const void *q, const void *k,
+                          const void *v, const float *gamma, const float *lambda_diag,
+                          int cg_iters, float cg_tol, void *out, int32_t *iters_used,
+                          cudaStream_t stream);
+
+/*
  * Query/key preprocessing in front of the layer ("Arquitetura (MesaNet)",
  * "Pre-processamento": keys and queries are normalised and convolved with a small window
  * before the Mesa layer).  For each (batch, head) unit, channel c and token t, for q and k:

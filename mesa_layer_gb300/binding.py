@@ -58,6 +58,8 @@ def load(build_if_missing: bool = True):
     lib.mesa_tc_selftest.argtypes = [_vp] * 6 + [_vp]
     lib.mesa_decode_step.restype = _i
     lib.mesa_decode_step.argtypes = [_i] * 5 + [_fp, _fp, _vp, _vp, _vp, _fp, _fp, _i, _f, _vp, _ip, _vp]
+    lib.mesa_decode_step_warm.restype = _i
+    lib.mesa_decode_step_warm.argtypes = [_i] * 5 + [_fp, _fp, _fp, _vp, _vp, _vp, _fp, _fp, _i, _f, _vp, _ip, _vp]
     lib.mesa_qk_preprocess.restype = _i
     lib.mesa_qk_preprocess.argtypes = [_i] * 6 + [_vp, _vp, _fp, _fp, _vp, _vp, _vp]
     lib.mesa_qk_preprocess_step.restype = _i
@@ -203,6 +205,30 @@ def mesa_qk_preprocess_step(q_raw, k_raw, wq, wk, conv_state, q_out=None, k_out=
                                      _ptr(conv_state), _ptr(q_out), _ptr(k_out), _stream(stream))
     _check(st, "mesa_qk_preprocess_step")
     return q_out, k_out
+
+
+def mesa_decode_step_warm(H_state, G_state, X_state, q, k, v, gamma, lambda_diag, cg_iters, cg_tol,
+                          out=None, iters_used=None, stream=None):
+    """mesa_decode_step whose CG starts from X_state [N, H, dk] (fp32, in/out: replaced by this
+    step's solution).  Returns (out, iters_used)."""
+    lib = load()
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, q.dtype)
+    for name, t in (("H_state", H_state), ("G_state", G_state), ("X_state", X_state), ("gamma", gamma),
+                    ("lambda_diag", lambda_diag)):
+        _require(t, name, torch.float32)
+    if out is None:
+        out = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    if iters_used is None:
+        iters_used = torch.empty((N, H), dtype=torch.int32, device=q.device)
+    st = lib.mesa_decode_step_warm(N, H, dk, dv, code, _ptr(H_state), _ptr(G_state), _ptr(X_state), _ptr(q),
+                                   _ptr(k), _ptr(v), _ptr(gamma), _ptr(lambda_diag), int(cg_iters), float(cg_tol),
+                                   _ptr(out), _ptr(iters_used), _stream(stream))
+    _check(st, "mesa_decode_step_warm")
+    return out, iters_used
 
 
 def mesa_forward_status(workspace, stream=None) -> int:

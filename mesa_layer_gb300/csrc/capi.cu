@@ -245,7 +245,26 @@ int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state, fl
   if (!H_state || !G_state || !q || !k || !v || !gamma || !lambda_diag || !out)
     return MESA_ERR_INVALID_ARG;
   if (!aligned(H_state, 16) || !aligned(G_state, 16)) return MESA_ERR_INVALID_ARG;
-  mesa::DecArgs a{N, H, dk, dv, dtype, H_state, G_state, q, k, v, gamma, lambda_diag,
+  mesa::DecArgs a{N, H, dk, dv, dtype, H_state, G_state, nullptr, q, k, v, gamma, lambda_diag,
+                  cg_iters, cg_tol, out, iters_used};
+  return mesa::launch_decode(a, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
+}
+
+int mesa_decode_step_warm(int N, int H, int dk, int dv, int dtype, float *H_state,
+                          float *G_state, float *X_state, const void *q, const void *k,
+                          const void *v, const float *gamma, const float *lambda_diag,
+                          int cg_iters, float cg_tol, void *out, int32_t *iters_used,
+                          cudaStream_t stream) {
+  if (N < 0 || H < 0 || cg_iters < 0 || cg_iters > kMaxIters || isnan(cg_tol))
+    return MESA_ERR_INVALID_ARG;
+  if (dtype != MESA_F32 && dtype != MESA_BF16) return MESA_ERR_INVALID_ARG;
+  if (!dim_ok(dk) || dv != dk) return MESA_ERR_UNSUPPORTED;
+  if ((size_t)N * H == 0) return MESA_OK;
+  if (!H_state || !G_state || !X_state || !q || !k || !v || !gamma || !lambda_diag || !out)
+    return MESA_ERR_INVALID_ARG;
+  if (!aligned(H_state, 16) || !aligned(G_state, 16) || !aligned(X_state, 16))
+    return MESA_ERR_INVALID_ARG;
+  mesa::DecArgs a{N, H, dk, dv, dtype, H_state, G_state, X_state, q, k, v, gamma, lambda_diag,
                   cg_iters, cg_tol, out, iters_used};
   return mesa::launch_decode(a, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
 }

@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(4 * D) mesa_decode_kernel(DecArgs a) {
   __shared__ __align__(16) float kvec[D];
   __shared__ __align__(16) float vvec[D];
   __shared__ __align__(16) float pvec[D];
+  __shared__ __align__(16) float xvec[D];
   __shared__ float lamv[D];
   __shared__ float red[2][NW];
 
@@ -50,6 +51,7 @@ __global__ void __launch_bounds__(4 * D) mesa_decode_kernel(DecArgs a) {
     vvec[i] = ld(v, (size_t)u * D + i);
     pvec[i] = ld(q, (size_t)u * D + i);
     lamv[i] = a.lambda[(size_t)(u % a.H) * D + i];
+    if (a.Xs) xvec[i] = a.Xs[(size_t)u * D + i];
   }
   const float g = a.gamma[u];
   float4 *Hp = reinterpret_cast<float4 *>(a.Hs + (size_t)u * D * D);
@@ -88,7 +90,30 @@ __global__ void __launch_bounds__(4 * D) mesa_decode_kernel(DecArgs a) {
     if (owner) s += qv * qv;
   }
   float rho = block_sum<NW>(s, red, 0, warp, lane);
-  const float nq = sqrtf(rho);
+  const float nq = sqrtf(rho);  // the stopping rule is relative to ||q||
+  if (a.Xs) {  // warm start: x = x0, r = p = q - (H + Lambda) x0
+    const float4 xc0 = *reinterpret_cast<const float4 *>(&xvec[4 * cgp]);
+    s = 0.0f;
+#pragma unroll
+    for (int p = 0; p < NP; p++) {
+      float t = h[p].x * xc0.x;
+      t = fmaf(h[p].y, xc0.y, t);
+      t = fmaf(h[p].z, xc0.z, t);
+      t = fmaf(h[p].w, xc0.w, t);
+#pragma unroll
+      for (int o = LPR / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      xr[p] = xvec[row[p]];
+      rr[p] = rr[p] - fmaf(lr[p], xr[p], t);
+      pr[p] = rr[p];
+      if (owner) s += rr[p] * rr[p];
+    }
+    __syncthreads();  // every thread has read q from pvec
+#pragma unroll
+    for (int p = 0; p < NP; p++)
+      if (owner) pvec[row[p]] = pr[p];
+    rho = block_sum<NW>(s, red, 1, warp, lane);  // its barrier also publishes p
+    __syncthreads();  // red[1] is read before the first CG step writes it again
+  }
   const bool dynamic = a.cg_tol > 0.0f;
   int it = 0;
   for (; it < a.cg_iters; it++) {
@@ -152,6 +177,7 @@ __global__ void __launch_bounds__(4 * D) mesa_decode_kernel(DecArgs a) {
 #pragma unroll
     for (int o = LPR / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
     if (owner) st(out, (size_t)u * D + row[p], t);
+    if (owner && a.Xs) a.Xs[(size_t)u * D + row[p]] = xr[p];
   }
   if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
 }
@@ -269,12 +295,28 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
   // second reduction of a step every thread updates its own copy of p from the new
   // residual (rvec) without a further barrier.
   float xr = 0.0f, rr = pvec[row], pr = rr;
-  float4 pc[4];
+  float rho = block_rows_sum(rr * rr, 0);
+  const float nq = sqrtf(rho);  // the stopping rule is relative to ||q||
   const float4 *p4 = reinterpret_cast<const float4 *>(pvec);
+  if (a.Xs) {  // warm start: x = x0, r = p = q - (H + Lambda) x0, p's columns via rvec
+    const float4 *x4 = reinterpret_cast<const float4 *>(a.Xs + (size_t)u * D);
+    float4 xc0[4];
+#pragma unroll
+    for (int j = 0; j < 4; j++) xc0[j] = x4[cb + 8 * j];
+    float s0[4];
+    matvec_rows(xc0, s0);
+    xr = a.Xs[(size_t)u * D + row];
+    rr = rr - fmaf(lam_r, xr, rowsum(s0));
+    pr = rr;
+    if ((lane & 1) == 0) rvec[row] = rr;
+    rho = block_rows_sum(rr * rr, 1);  // its barrier also publishes rvec
+    __syncthreads();                   // red[1] is read before the first CG step writes it
+    p4 = reinterpret_cast<const float4 *>(rvec);
+  }
+  float4 pc[4];
 #pragma unroll
   for (int j = 0; j < 4; j++) pc[j] = p4[cb + 8 * j];
-  float rho = block_rows_sum(rr * rr, 0);
-  const float nq = sqrtf(rho);
+  p4 = reinterpret_cast<const float4 *>(pvec);
   const bool dynamic = a.cg_tol > 0.0f;
   const float4 *r4 = reinterpret_cast<const float4 *>(rvec);
   int it = 0;
@@ -331,6 +373,7 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
   }
   const float o = rowsum(s);
   if ((lane & 1) == 0) st((TIO *)a.out, (size_t)u * D + row, o);
+  if ((lane & 1) == 0 && a.Xs) a.Xs[(size_t)u * D + row] = xr;
   if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
 }
 

@@ -25,6 +25,7 @@ struct FwdArgs {
 struct DecArgs {
   int N, H, dk, dv, dtype;
   float *Hs, *Gs;
+  float *Xs;  // nullptr: CG from 0; else [N*H, dk] start vectors, replaced by the solutions
   const void *q, *k, *v;
   const float *gamma, *lambda;
   int cg_iters;

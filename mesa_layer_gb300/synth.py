@@ -45,6 +45,7 @@ class Workload:
     decode_steps: int = 0      # > 0: recurrent decode workload (B = sequences)
     prefix: int = 0            # decode: tokens folded into the state before the steps
     conv_taps: int = 0         # > 0: query/key preprocessing workload with this window
+    warm: bool = False         # decode: each step's CG starts from the previous solution
 
     @property
     def tokens(self) -> int:
@@ -71,6 +72,9 @@ WORKLOADS = {
         # query/key preprocessing in front of the layer, on the shape of fwd_bf16_d128
         Workload("qkpre_bf16_d128", 6, "bf16", 8, 16, 4096, 128, 128, 64, 0, 0.0,
                  "sigmoid", 4.0, 1.0, 0.05, 0.5, conv_taps=4),
+        # the decode workload with warm-started CG (inputs drawn as for decode_bf16_d128)
+        Workload("decode_warm_bf16_d128", 5, "bf16", 256, 16, 1, 128, 128, 64, 30, 1e-3,
+                 "sigmoid", 4.0, 1.0, 0.05, 0.5, decode_steps=512, prefix=1024, warm=True),
     ]
 }
 WORKLOAD_ORDER = [w.name for w in sorted(WORKLOADS.values(), key=lambda w: w.wid)]

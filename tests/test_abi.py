@@ -136,3 +136,19 @@ def test_qk_preprocess_step_validation(lib):
     assert f(*args(cs=None)) == 1                               # a window needs its state
     assert f(*args(cs=ctypes.c_void_p(264))) == 1               # misaligned state
     assert f(*args(N=0)) == 0
+
+
+def test_decode_step_warm_validation(lib):
+    f = lib.mesa_decode_step_warm  # argument types set by the binding
+    p = ctypes.c_void_p(256)
+    def call(**kw):
+        a = dict(N=2, H=2, dk=64, dv=64, dt=1, Hs=p, Gs=p, Xs=p, q=p, k=p, v=p, g=p, lam=p, it=5, tol=0.0,
+                 out=p, its=None, st=None)
+        a.update(kw)
+        return f(a["N"], a["H"], a["dk"], a["dv"], a["dt"], a["Hs"], a["Gs"], a["Xs"], a["q"], a["k"], a["v"],
+                 a["g"], a["lam"], a["it"], a["tol"], a["out"], a["its"], a["st"])
+    assert call(Xs=None) == 1                        # the start vectors are required
+    assert call(Xs=ctypes.c_void_p(264)) == 1        # misaligned start vectors
+    assert call(dk=48, dv=48) == 2
+    assert call(it=-1) == 1
+    assert call(N=0) == 0
