@@ -108,7 +108,7 @@ __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, con
 
 template <int NTERMS>
 __global__ void __launch_bounds__(512, 1)
-    mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, unsigned *status) {
+    mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, int lookahead, unsigned *status) {
   constexpr int NG = 4;           // column groups (threads per token row)
   constexpr int CW = DH / NG;     // columns per thread
   constexpr int NV = CW / 8;      // 8-column vectors per thread
@@ -232,6 +232,24 @@ __global__ void __launch_bounds__(512, 1)
       const uint32_t off = tc::sw128_offset(i, c0 + 8 * g, TILE);
       *reinterpret_cast<uint4 *>(Zhi + off) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4 *>(Zlo + off) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  {  // CTAs start in block order as SMs free up (one per SM), so the chunk `lookahead`
+     // blocks on runs about one wave later: its inputs go into L2 now
+    const long long wn = (long long)blockIdx.x + (long long)NC * blockIdx.y + lookahead;
+    if (lookahead > 0 && wn < (long long)NC * gridDim.y) {
+      const int cn = (int)(wn % NC), un = (int)(wn / NC);
+      const int Tn = min(TILE, T - cn * TILE);
+      const size_t tbn = (size_t)un * T + (size_t)cn * TILE;
+      if (cn > 0) {
+        tc::prefetch_l2(ws.SH + ((size_t)un * NC + (cn - 1)) * DH * DH, sizeof(float) * DH * DH);
+        const int segn = (cn - 1) / ((NC + ws.nseg - 1) / ws.nseg);
+        if (segn > 0)
+          tc::prefetch_l2(ws.carry + ((size_t)un * ws.nseg + segn) * 2 * DH * DH, sizeof(float) * DH * DH);
+      }
+      tc::prefetch_l2(k + tbn * DH, sizeof(__nv_bfloat16) * DH * Tn);
+      tc::prefetch_l2(q + tbn * DH, sizeof(__nv_bfloat16) * DH * Tn);
+      tc::prefetch_l2(ws.ell + tbn, sizeof(float) * Tn);
     }
   }
   tc::fence_before_sync();
@@ -654,7 +672,7 @@ int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *statu
       cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_TC, st);
-  kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(a, ws, NC, status);
+  kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(a, ws, NC, sm_count(), status);
   timing_mark_end(K_CG_TC, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

@@ -64,4 +64,14 @@ inline int tc_segments(int U, int NC) {
   return s < 1 ? 1 : s;
 }
 
+// Multiprocessors of the current device (0 if it cannot be read): the size of the
+// persistent grids.
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 0;
+  return n;
+}
+
 }  // namespace mesa
