@@ -11,14 +11,16 @@
 // power-of-two scale per row (P, X, Z) or per matrix (S, K, V) and split into two fp16
 // terms (hi + lo, ~22 significant bits); products take hi*hi + hi*lo + lo*hi (the state)
 // or hi*K + lo*K (K and V are bf16 inputs, exact in fp16 after scaling).  Accumulation is
-// fp32.  The CG scalars and the x, r vectors stay fp32 (x, r in tensor memory).
+// fp32.  The CG scalars and the x, r vectors stay fp32 (r in tensor memory, x in shared
+// memory); the P operand of the two products that read it lives in tensor memory.
 //
 // One CTA of 512 threads per chunk.  Warp w reads tensor-memory lane quadrant q = w % 4
 // (token rows 32q .. 32q+31, one row per lane) and column group g = w / 4 (32 of the 128
 // columns), so each token row is handled by 4 threads in 4 warps; their per-row partial
 // sums and maxima meet in shared memory behind a 128-thread named barrier per quadrant.
 // Tensor memory (512 columns): [0,128) U = P S, [128,256) W = P K^T then Y = Z K,
-// [256,384) x, [384,512) r.
+// [256,320) and [320,384) the P operand (hi, lo: fp16 pairs, the MMAs' A operand),
+// [384,512) r.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -33,11 +35,61 @@ using tc::TILE;
 constexpr uint32_t MAT_BYTES = TILE * DH * 2;  // one fp16 128x128 operand (32 KB)
 // shared-memory map (offsets from a 1024-aligned base)
 constexpr uint32_t OFF_SHI = 0, OFF_SLO = MAT_BYTES, OFF_K = 2 * MAT_BYTES,
-                   OFF_PHI = 3 * MAT_BYTES, OFF_PLO = 4 * MAT_BYTES, OFF_ZHI = 5 * MAT_BYTES,
-                   OFF_ZLO = 6 * MAT_BYTES, OFF_MISC = 7 * MAT_BYTES;
+                   OFF_X = 3 * MAT_BYTES,  // x, fp32 128 x 128 (two operand slots)
+                   OFF_ZHI = 5 * MAT_BYTES, OFF_ZLO = 6 * MAT_BYTES, OFF_MISC = 7 * MAT_BYTES;
 constexpr uint32_t MISC_BYTES = 2048;
 constexpr uint32_t SMEM_TC = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
-constexpr uint32_t COL_U = 0, COL_W = 128, COL_X = 256, COL_R = 384;
+constexpr uint32_t COL_U = 0, COL_W = 128, COL_PH = 256, COL_PL = 320, COL_R = 384;
+
+// Byte offset of x[i][c .. c+3] (c a multiple of 4): row i is 512 bytes, its 16-byte chunks
+// permuted by chunk ^ (i % 8), so that a warp reading the same columns of 32 rows is spread
+// over all banks.
+__device__ __forceinline__ uint32_t x_offset(int i, int c) {
+  return (uint32_t)(i * 512 + (((c >> 2) ^ (i & 7)) << 4));
+}
+
+// 16 values v of a row, times inv, as fp16 hi (+ lo) pairs into the P operand: 8 columns
+// at tph (hi) and tpl (lo).
+template <int NTERMS>
+__device__ __forceinline__ void stage16_p(uint32_t tph, uint32_t tpl, const float *v, float inv) {
+  float hi[8], lo[8];
+#pragma unroll
+  for (int k = 0; k < 8; k++) {
+    const float a = v[2 * k] * inv, b = v[2 * k + 1] * inv;
+    __half2 h = __floats2half2_rn(a, b);
+    hi[k] = __uint_as_float(*reinterpret_cast<uint32_t *>(&h));
+    if constexpr (NTERMS == 2) {
+      const float2 back = __half22float2(h);
+      __half2 l = __floats2half2_rn(a - back.x, b - back.y);
+      lo[k] = __uint_as_float(*reinterpret_cast<uint32_t *>(&l));
+    }
+  }
+  tc::tmem_st8(tph, hi);
+  if constexpr (NTERMS == 2) tc::tmem_st8(tpl, lo);
+}
+
+// 16 values of a row back from the P operand (8 columns at tph, tpl), times mul.
+template <int NTERMS>
+__device__ __forceinline__ void load16_p(uint32_t tph, uint32_t tpl, float mul, float *v) {
+  float hi[8], lo[8];
+  tc::tmem_ld8(tph, hi);
+  if constexpr (NTERMS == 2) tc::tmem_ld8(tpl, lo);
+  tc::tmem_ld_wait();
+#pragma unroll
+  for (int k = 0; k < 8; k++) {
+    uint32_t hb = __float_as_uint(hi[k]);
+    const float2 a = __half22float2(*reinterpret_cast<__half2 *>(&hb));
+    if constexpr (NTERMS == 2) {
+      uint32_t lb = __float_as_uint(lo[k]);
+      const float2 b = __half22float2(*reinterpret_cast<__half2 *>(&lb));
+      v[2 * k] = mul * (a.x + b.x);
+      v[2 * k + 1] = mul * (a.y + b.y);
+    } else {
+      v[2 * k] = mul * a.x;
+      v[2 * k + 1] = mul * a.y;
+    }
+  }
+}
 
 struct Misc {
   float ell2[TILE];  // log2-decays l_i * log2(e)
@@ -115,7 +167,7 @@ __global__ void __launch_bounds__(512, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t *Shi = sm + OFF_SHI, *Slo = sm + OFF_SLO, *Ks = sm + OFF_K;
-  uint8_t *Phi = sm + OFF_PHI, *Plo = sm + OFF_PLO, *Zhi = sm + OFF_ZHI, *Zlo = sm + OFF_ZLO;
+  uint8_t *Xs = sm + OFF_X, *Zhi = sm + OFF_ZHI, *Zlo = sm + OFF_ZLO;
   Misc *m = reinterpret_cast<Misc *>(sm + OFF_MISC);
   const uint32_t aBarW1 = tc::smem_u32(&m->mbar_w1), aBarW2 = tc::smem_u32(&m->mbar_w2);
   const uint32_t aBarY = tc::smem_u32(&m->mbar_y), aBarU = tc::smem_u32(&m->mbar_u);
@@ -257,10 +309,13 @@ __global__ void __launch_bounds__(512, 1)
   tc::fence_after_sync();
   const uint32_t tbase = m->tmem_base;
   const uint32_t tl = tbase + ((uint32_t)(32 * qd) << 16) + c0;  // lane quadrant, column group
+  // this thread's 16 columns of the P operand (32 fp16 values of its row), hi and lo
+  const uint32_t tph = tbase + ((uint32_t)(32 * qd) << 16) + COL_PH + CW / 2 * grp;
+  const uint32_t tpl = tph + (COL_PL - COL_PH);
   const float ell2_i = m->ell2[i];
   const float e2r_i = valid ? exp2f(ell2_i) : 0.0f;  // 2^{l2_i} = e^{l_i}; invalid rows: D = 0
 
-  // CG start: x = 0, r = p = q_i (this thread's CW columns).  p lives in shared memory as
+  // CG start: x = 0, r = p = q_i (this thread's CW columns).  p lives in tensor memory as
   // the scaled hi + lo MMA operand; each iteration reads it back once into registers.
   float rho, nq, mP;
   {
@@ -281,19 +336,13 @@ __global__ void __launch_bounds__(512, 1)
     rho = s;
     nq = sqrtf(rho);
     mP = tc::pow2_ceil(mx);
-    float z[CW];
 #pragma unroll
-    for (int kk = 0; kk < CW; kk++) z[kk] = 0.0f;
-    tc::tmem_st<CW>(tl + COL_X, z);
+    for (int g4 = 0; g4 < CW / 4; g4++)
+      *reinterpret_cast<float4 *>(Xs + x_offset(i, c0 + 4 * g4)) = make_float4(0, 0, 0, 0);
     tc::tmem_st<CW>(tl + COL_R, p);
     const float inv = 1.0f / mP;
-#pragma unroll
-    for (int g = 0; g < NV; g++) {
-      float x8[8];
-#pragma unroll
-      for (int kk = 0; kk < 8; kk++) x8[kk] = p[g * 8 + kk];
-      st8<NTERMS>(Phi, Plo, i, c0 + 8 * g, x8, inv);
-    }
+    stage16_p<NTERMS>(tph, tpl, p, inv);
+    stage16_p<NTERMS>(tph + 8, tpl + 8, p + 16, inv);
     tc::tmem_st_wait();
   }
 
@@ -322,8 +371,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
       for (int s = 0; s < 8; s++) {
         const uint64_t kb = kdesc(OFF_K, s) + (uint64_t)(half * (64 * 128 / 16));
-        tc::mma_f16(tbase + COL_W + 64 * half, kdesc(OFF_PHI, s), kb, id_kk64, s > 0);
-        if (NTERMS == 2) tc::mma_f16(tbase + COL_W + 64 * half, kdesc(OFF_PLO, s), kb, id_kk64, true);
+        tc::mma_f16_ts(tbase + COL_W + 64 * half, tbase + COL_PH + 8 * s, kb, id_kk64, s > 0);
+        if (NTERMS == 2) tc::mma_f16_ts(tbase + COL_W + 64 * half, tbase + COL_PL + 8 * s, kb, id_kk64, true);
       }
       tc::mma_commit(half ? aBarW2 : aBarW1);
     }
@@ -334,10 +383,10 @@ __global__ void __launch_bounds__(512, 1)
   auto issue_U = [&]() {
 #pragma unroll
     for (int s = 0; s < 8; s++) {
-      tc::mma_f16(tbase + COL_U, kdesc(OFF_PHI, s), kdesc(OFF_SHI, s), id_kk, s > 0);
+      tc::mma_f16_ts(tbase + COL_U, tbase + COL_PH + 8 * s, kdesc(OFF_SHI, s), id_kk, s > 0);
       if (NTERMS == 2) {
-        tc::mma_f16(tbase + COL_U, kdesc(OFF_PHI, s), kdesc(OFF_SLO, s), id_kk, true);
-        tc::mma_f16(tbase + COL_U, kdesc(OFF_PLO, s), kdesc(OFF_SHI, s), id_kk, true);
+        tc::mma_f16_ts(tbase + COL_U, tbase + COL_PH + 8 * s, kdesc(OFF_SLO, s), id_kk, true);
+        tc::mma_f16_ts(tbase + COL_U, tbase + COL_PL + 8 * s, kdesc(OFF_SHI, s), id_kk, true);
       }
     }
     tc::mma_commit(aBarU);
@@ -453,13 +502,14 @@ __global__ void __launch_bounds__(512, 1)
   int iters_run = 0;  // completed iterations (the same in every thread)
   auto x_update = [&](float al) {
 #pragma unroll
-    for (int h = 0; h < CW / 16; h++) {
-      float xx[16];
-      tc::tmem_ld16(tl + COL_X + 16 * h, xx);
-      tc::tmem_ld_wait();
-#pragma unroll
-      for (int kk = 0; kk < 16; kk++) xx[kk] = fmaf(al, p[16 * h + kk], xx[kk]);
-      tc::tmem_st16(tl + COL_X + 16 * h, xx);
+    for (int g4 = 0; g4 < CW / 4; g4++) {
+      float4 *xp = reinterpret_cast<float4 *>(Xs + x_offset(i, c0 + 4 * g4));
+      float4 xx = *xp;
+      xx.x = fmaf(al, p[4 * g4], xx.x);
+      xx.y = fmaf(al, p[4 * g4 + 1], xx.y);
+      xx.z = fmaf(al, p[4 * g4 + 2], xx.z);
+      xx.w = fmaf(al, p[4 * g4 + 3], xx.w);
+      *xp = xx;
     }
   };
 
@@ -484,13 +534,8 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (tid == 0) issue_Y();
     // p back from its operand copy while Y = Z K and U = P S run
-#pragma unroll
-    for (int g = 0; g < NV; g++) {
-      float p8[8];
-      ld8<NTERMS>(Phi, Plo, i, c0 + 8 * g, mP, p8);
-#pragma unroll
-      for (int kk = 0; kk < 8; kk++) p[8 * g + kk] = p8[kk];
-    }
+    load16_p<NTERMS>(tph, tpl, mP, p);
+    load16_p<NTERMS>(tph + 8, tpl + 8, mP, p + 16);
     if (!wait_YU()) {
       failed = true;
       break;
@@ -545,25 +590,22 @@ __global__ void __launch_bounds__(512, 1)
     const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
     // for an active row p = r + beta p, staged with the scale
     // mNew >= max|r| + beta max|p| >= max|p_new|; the old p stays in registers for the
-    // deferred x += alpha p (a finished row keeps its p and has alpha = 0; the
-    // tensor-memory loads stay unconditional: they are warp-collective)
-    const float mNew = tc::pow2_ceil(rmax + beta * mP);
+    // deferred x += alpha p.  A finished row keeps its p (alpha = 0): it is staged again
+    // with its old scale, which gives back the same hi and lo (p was read from them, and
+    // hi + lo and the power-of-two scales are exact in fp32).  The tensor-memory accesses
+    // stay unconditional: they are warp-collective.
+    const float mNew = act ? tc::pow2_ceil(rmax + beta * mP) : mP;
     const float inv = 1.0f / mNew;
 #pragma unroll
     for (int h = 0; h < CW / 16; h++) {
-      float rr[16];
+      float rr[16], pv[16];
       tc::tmem_ld16(tl + COL_R + 16 * h, rr);
       tc::tmem_ld_wait();
-      if (act) {
 #pragma unroll
-        for (int g = 0; g < 2; g++) {
-          float p8[8];
-#pragma unroll
-          for (int kk = 0; kk < 8; kk++) p8[kk] = fmaf(beta, p[16 * h + 8 * g + kk], rr[8 * g + kk]);
-          st8<NTERMS>(Phi, Plo, i, c0 + 16 * h + 8 * g, p8, inv);
-        }
-      }
+      for (int kk = 0; kk < 16; kk++) pv[kk] = act ? fmaf(beta, p[16 * h + kk], rr[kk]) : p[16 * h + kk];
+      stage16_p<NTERMS>(tph + 8 * h, tpl + 8 * h, pv, inv);
     }
+    tc::tmem_st_wait();
     if (act) {
       mP = mNew;
       rho = rn;
@@ -580,20 +622,23 @@ __global__ void __launch_bounds__(512, 1)
   if (!failed) {
     tc::prefetch_l2(v + tokbase * DH, sizeof(__nv_bfloat16) * DH * Tv);  // the value tile
     float xx[CW];
-    tc::tmem_ld<CW>(tl + COL_X, xx);
-    tc::tmem_ld_wait();
+#pragma unroll
+    for (int g4 = 0; g4 < CW / 4; g4++) {
+      const float4 x4 = *reinterpret_cast<const float4 *>(Xs + x_offset(i, c0 + 4 * g4));
+      xx[4 * g4] = x4.x;
+      xx[4 * g4 + 1] = x4.y;
+      xx[4 * g4 + 2] = x4.z;
+      xx[4 * g4 + 3] = x4.w;
+    }
     float mx = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < CW; kk++) mx = fmaxf(mx, fabsf(xx[kk]));
     const float mX = tc::pow2_ceil(rowred(mx, true));
     const float inv = 1.0f / mX;
-#pragma unroll
-    for (int g = 0; g < NV; g++) {
-      float x8[8];
-#pragma unroll
-      for (int kk = 0; kk < 8; kk++) x8[kk] = xx[g * 8 + kk];
-      st8<NTERMS>(Phi, Plo, i, c0 + 8 * g, x8, inv);
-    }
+    // X replaces P as the A operand of W and U
+    stage16_p<NTERMS>(tph, tpl, xx, inv);
+    stage16_p<NTERMS>(tph + 8, tpl + 8, xx + 16, inv);
+    tc::tmem_st_wait();
     float sG, sV;
     tc::Rows8 vr;
     {
