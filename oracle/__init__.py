@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the Mesa layer forward pass (ctypes wrapper over mesa_oracle.c).
+"""fp64 CPU oracle for the Mesa layer forward and backward passes (ctypes wrapper over mesa_oracle.c).
 
 TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference leg of ``bench.py``.  The product path (``mesa_layer_gb300``)
@@ -71,6 +71,9 @@ def _bind(lib):
     lib.oracle_qk_preprocess.argtypes = [ctypes.c_int] * 5 + [_D] * 3
     lib.oracle_qk_preprocess_step.restype = None
     lib.oracle_qk_preprocess_step.argtypes = [ctypes.c_int] * 4 + [_D] * 4
+    lib.oracle_backward.restype = ctypes.c_int
+    lib.oracle_backward.argtypes = [ctypes.c_int] * 5 + [_D] * 6 + [ctypes.c_int, ctypes.c_double] + [_D] * 5 + [
+        _I, _I, ctypes.c_int]
     return lib
 
 
@@ -142,6 +145,27 @@ def forward(q, k, v, gamma, lam, cg_iters, cg_tol=0.0, replay=None, H0=None, G0=
     if want_final:
         return out, iters, Hf, Gf
     return out, iters
+
+
+def backward(q, k, v, gamma, lam, dout, cg_iters, cg_tol=0.0, nthreads=None, lib=None):
+    """Gradients of a loss through the Mesa layer forward, given dout = dL/do
+    [B, heads, T, dv]: implicit differentiation through each token's solve (one more CG per
+    token, on (H_t + Lambda) y = G_t^T g_t, with the forward's CG rule), then the state
+    recurrence differentiated backwards in time.  Zero initial states.  Returns a dict with
+    dq, dk [B, heads, T, dk], dv [B, heads, T, dv], dgamma [B, heads, T], dlam [heads, dk]
+    (summed over the batch), iters_fwd and iters_bwd [B, heads, T] int32."""
+    lib = lib or load()
+    q, k, v, gamma, lam, dout = _f64(q), _f64(k), _f64(v), _f64(gamma), _f64(lam), _f64(dout)
+    B, heads, T, dk = q.shape
+    dv = v.shape[-1]
+    r = {"dq": np.zeros((B, heads, T, dk)), "dk": np.zeros((B, heads, T, dk)), "dv": np.zeros((B, heads, T, dv)),
+         "dgamma": np.zeros((B, heads, T)), "dlam": np.zeros((heads, dk)),
+         "iters_fwd": np.zeros((B, heads, T), dtype=np.int32), "iters_bwd": np.zeros((B, heads, T), dtype=np.int32)}
+    nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
+    lib.oracle_backward(B * heads, heads, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(lam), _ptr(dout),
+                        int(cg_iters), float(cg_tol), _ptr(r["dq"]), _ptr(r["dk"]), _ptr(r["dv"]), _ptr(r["dgamma"]),
+                        _ptr(r["dlam"]), _ptr(r["iters_fwd"], _I), _ptr(r["iters_bwd"], _I), int(nt))
+    return r
 
 
 def decode_step(Hs, Gs, q, k, v, gamma, lam, cg_iters, cg_tol=0.0, nthreads=None, X=None, lib=None):

@@ -1,5 +1,5 @@
 /*
- * mesa_oracle.c -- plain fp64 CPU oracle for the Mesa layer forward pass.
+ * mesa_oracle.c -- plain fp64 CPU oracle for the Mesa layer forward and backward passes.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library and
  * its Python binding) may include, link or call this file.  It exists so that
@@ -310,6 +310,128 @@ void oracle_qk_preprocess_step(int U, int heads, int d, int W, const double *x,
     if (W > 1) memcpy(hu, xu, sizeof(double) * d);
   }
   free(y);
+}
+
+/*
+ * Backward pass: the gradients of a loss L through the forward above, given dL/do_t.
+ *
+ * The pages claim training ("Paralelizacao" bullet: O(T) training; "Contribuicoes", item 1:
+ * efficient training with the chunkwise CG solver) but give no gradient.  Reading taken:
+ * implicit differentiation through the solve.  Each CG iterate x_t stands for
+ * (H_t + Lambda)^{-1} q_t, so with g_t = dL/do_t and o_t = G_t x_t:
+ *     b_t = G_t^T g_t,   y_t = CG(H_t + Lambda, b_t)   (the same CG rule, count and tolerance)
+ *     dL/dq_t = y_t,     dL/dLambda = -sum_t diag(y_t x_t^T)
+ *     direct state gradients  dH_t^dir = -y_t x_t^T,   dG_t^dir = g_t x_t^T
+ * and the recurrence H_t = gamma_t H_{t-1} + k_t k_t^T (same for G) is differentiated
+ * backwards in time with the total adjoints dH_t = dH_t^dir + gamma_{t+1} dH_{t+1}:
+ *     dL/dk_t = (dH_t + dH_t^T) k_t + dG_t^T v_t,   dL/dv_t = dG_t k_t,
+ *     dL/dgamma_t = <dH_t, H_{t-1}> + <dG_t, G_{t-1}>   (Frobenius products).
+ * With exact solves these are the exact gradients of o_t = G_t (H_t + Lambda)^{-1} q_t.
+ *
+ * Two sweeps per unit.  Forward in t: the states, x_t, b_t and y_t; the states before every
+ * 64th token are kept.  Backward in t: the adjoints; the states H_{t-1}, G_{t-1} of each
+ * 64-token stretch are rebuilt from its kept state by the same recurrence (so they are
+ * bit-identical to the forward sweep's).
+ *   dout [U, T, dv]; dq, dk [U, T, dk]; dv [U, T, dv]; dgamma [U, T];
+ *   dlam [heads, dk] (summed over the units of each head); iters_fwd, iters_bwd [U, T]
+ *   (iterations of the x and y solves).  Zero initial states.
+ * Returns the number of threads used.
+ */
+#define ORACLE_BWD_KEEP 64
+
+static void state_step(int dk, int dv, double *H, double *G, const double *k, const double *v,
+                       double gamma) {
+  for (int a = 0; a < dk; a++)
+    for (int b = 0; b < dk; b++)
+      H[(size_t)a * dk + b] = gamma * H[(size_t)a * dk + b] + k[a] * k[b];
+  for (int a = 0; a < dv; a++)
+    for (int b = 0; b < dk; b++)
+      G[(size_t)a * dk + b] = gamma * G[(size_t)a * dk + b] + v[a] * k[b];
+}
+
+int oracle_backward(int U, int heads, int T, int dk, int dv, const double *q, const double *k,
+                    const double *v, const double *gamma, const double *lam, const double *dout,
+                    int cg_iters, double cg_tol, double *dq, double *dkk, double *dvv,
+                    double *dgamma, double *dlam, int32_t *iters_fwd, int32_t *iters_bwd,
+                    int nthreads) {
+  const int nt = pick_threads(nthreads, U);
+  const size_t hh = (size_t)dk * dk, gg = (size_t)dv * dk;
+  const int nkeep = (T + ORACLE_BWD_KEEP - 1) / ORACLE_BWD_KEEP;
+  double *dlam_u = (double *)calloc((size_t)(U > 0 ? U : 1) * dk, sizeof(double));
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+  for (int u = 0; u < U; u++) {
+    double *H = (double *)calloc(hh, sizeof(double));
+    double *G = (double *)calloc(gg, sizeof(double));
+    double *keepH = (double *)malloc(sizeof(double) * hh * (nkeep > 0 ? nkeep : 1));
+    double *keepG = (double *)malloc(sizeof(double) * gg * (nkeep > 0 ? nkeep : 1));
+    double *prevH = (double *)malloc(sizeof(double) * hh * ORACLE_BWD_KEEP);
+    double *prevG = (double *)malloc(sizeof(double) * gg * ORACLE_BWD_KEEP);
+    double *X = (double *)malloc(sizeof(double) * ((size_t)T * dk + 1));
+    double *b = (double *)malloc(sizeof(double) * dk);
+    double *work = (double *)malloc(sizeof(double) * 3 * dk);
+    double *dH = (double *)calloc(hh, sizeof(double));
+    double *dG = (double *)calloc(gg, sizeof(double));
+    const double *lam_u = lam + (size_t)(u % heads) * dk;
+    /* forward sweep */
+    for (int t = 0; t < T; t++) {
+      const size_t tok = (size_t)u * T + t;
+      if (t % ORACLE_BWD_KEEP == 0) {
+        memcpy(keepH + (size_t)(t / ORACLE_BWD_KEEP) * hh, H, sizeof(double) * hh);
+        memcpy(keepG + (size_t)(t / ORACLE_BWD_KEEP) * gg, G, sizeof(double) * gg);
+      }
+      state_step(dk, dv, H, G, k + tok * dk, v + tok * dv, gamma[tok]);
+      iters_fwd[tok] = oracle_cg(dk, H, lam_u, q + tok * dk, cg_iters, cg_tol,
+                                 X + (size_t)t * dk, work);
+      const double *g = dout + tok * dv;
+      for (int c = 0; c < dk; c++) {
+        double s = 0.0;
+        for (int a = 0; a < dv; a++) s += G[(size_t)a * dk + c] * g[a];
+        b[c] = s;
+      }
+      iters_bwd[tok] = oracle_cg(dk, H, lam_u, b, cg_iters, cg_tol, dq + tok * dk, work);
+    }
+    /* backward sweep, one kept stretch at a time */
+    for (int s0 = (nkeep - 1) * ORACLE_BWD_KEEP; s0 >= 0; s0 -= ORACLE_BWD_KEEP) {
+      const int s1 = (s0 + ORACLE_BWD_KEEP < T) ? s0 + ORACLE_BWD_KEEP : T;
+      memcpy(H, keepH + (size_t)(s0 / ORACLE_BWD_KEEP) * hh, sizeof(double) * hh);
+      memcpy(G, keepG + (size_t)(s0 / ORACLE_BWD_KEEP) * gg, sizeof(double) * gg);
+      for (int t = s0; t < s1; t++) {  /* prevH[t - s0] = H_{t-1} */
+        const size_t tok = (size_t)u * T + t;
+        memcpy(prevH + (size_t)(t - s0) * hh, H, sizeof(double) * hh);
+        memcpy(prevG + (size_t)(t - s0) * gg, G, sizeof(double) * gg);
+        state_step(dk, dv, H, G, k + tok * dk, v + tok * dv, gamma[tok]);
+      }
+      for (int t = s1 - 1; t >= s0; t--) {
+        const size_t tok = (size_t)u * T + t;
+        const double *x = X + (size_t)t * dk, *y = dq + tok * dk, *g = dout + tok * dv;
+        const double *kt = k + tok * dk, *vt = v + tok * dv;
+        for (int a = 0; a < dk; a++)
+          for (int c = 0; c < dk; c++) dH[(size_t)a * dk + c] -= y[a] * x[c];
+        for (int a = 0; a < dv; a++)
+          for (int c = 0; c < dk; c++) dG[(size_t)a * dk + c] += g[a] * x[c];
+        for (int a = 0; a < dk; a++) {
+          double s = 0.0;
+          for (int c = 0; c < dk; c++) s += (dH[(size_t)a * dk + c] + dH[(size_t)c * dk + a]) * kt[c];
+          for (int c = 0; c < dv; c++) s += dG[(size_t)c * dk + a] * vt[c];
+          dkk[tok * dk + a] = s;
+        }
+        for (int a = 0; a < dv; a++) dvv[tok * dv + a] = dot(dk, dG + (size_t)a * dk, kt);
+        const double *Hp = prevH + (size_t)(t - s0) * hh, *Gp = prevG + (size_t)(t - s0) * gg;
+        dgamma[tok] = dot((int)hh, dH, Hp) + dot((int)gg, dG, Gp);
+        for (size_t e = 0; e < hh; e++) dH[e] *= gamma[tok];
+        for (size_t e = 0; e < gg; e++) dG[e] *= gamma[tok];
+        for (int c = 0; c < dk; c++) dlam_u[(size_t)u * dk + c] -= y[c] * x[c];
+      }
+    }
+    free(H); free(G); free(keepH); free(keepG); free(prevH); free(prevG);
+    free(X); free(b); free(work); free(dH); free(dG);
+  }
+  for (int h = 0; h < heads; h++)
+    for (int c = 0; c < dk; c++) dlam[(size_t)h * dk + c] = 0.0;
+  for (int u = 0; u < U; u++)
+    for (int c = 0; c < dk; c++) dlam[(size_t)(u % heads) * dk + c] += dlam_u[(size_t)u * dk + c];
+  free(dlam_u);
+  return nt;
 }
 
 /* Exposed so callers can record how many host threads the oracle may use. */
