@@ -117,18 +117,24 @@ int oracle_cg(int n, const double *H, const double *lam, const double *q,
   return oracle_cg_from(n, H, lam, q, NULL, maxit, tol, x, work);
 }
 
-/* One token of the recurrence on one unit: decay and rank-1 update of H and G,
- * the CG solve, and the readout o = G x.  H is dk x dk, G is dv x dk. */
-static int mesa_token(int dk, int dv, double *H, double *G, const double *q,
-                      const double *k, const double *v, double gamma,
-                      const double *lam, int maxit, double tol, double *o,
-                      double *x, double *work, const double *x0) {
+/* The state recurrence for one token: H = gamma H + k k^T, G = gamma G + v k^T. */
+static void state_step(int dk, int dv, double *H, double *G, const double *k, const double *v,
+                       double gamma) {
   for (int a = 0; a < dk; a++)
     for (int b = 0; b < dk; b++)
       H[(size_t)a * dk + b] = gamma * H[(size_t)a * dk + b] + k[a] * k[b];
   for (int a = 0; a < dv; a++)
     for (int b = 0; b < dk; b++)
       G[(size_t)a * dk + b] = gamma * G[(size_t)a * dk + b] + v[a] * k[b];
+}
+
+/* One token of the recurrence on one unit: decay and rank-1 update of H and G,
+ * the CG solve, and the readout o = G x.  H is dk x dk, G is dv x dk. */
+static int mesa_token(int dk, int dv, double *H, double *G, const double *q,
+                      const double *k, const double *v, double gamma,
+                      const double *lam, int maxit, double tol, double *o,
+                      double *x, double *work, const double *x0) {
+  state_step(dk, dv, H, G, k, v, gamma);
   const int it = oracle_cg_from(dk, H, lam, q, x0, maxit, tol, x, work);
   for (int a = 0; a < dv; a++) o[a] = dot(dk, G + (size_t)a * dk, x);
   return it;
@@ -338,16 +344,6 @@ void oracle_qk_preprocess_step(int U, int heads, int d, int W, const double *x,
  * Returns the number of threads used.
  */
 #define ORACLE_BWD_KEEP 64
-
-static void state_step(int dk, int dv, double *H, double *G, const double *k, const double *v,
-                       double gamma) {
-  for (int a = 0; a < dk; a++)
-    for (int b = 0; b < dk; b++)
-      H[(size_t)a * dk + b] = gamma * H[(size_t)a * dk + b] + k[a] * k[b];
-  for (int a = 0; a < dv; a++)
-    for (int b = 0; b < dk; b++)
-      G[(size_t)a * dk + b] = gamma * G[(size_t)a * dk + b] + v[a] * k[b];
-}
 
 int oracle_backward(int U, int heads, int T, int dk, int dv, const double *q, const double *k,
                     const double *v, const double *gamma, const double *lam, const double *dout,
