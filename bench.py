@@ -6,7 +6,8 @@
 A step is one pass of the hot path over one batch of seeded synthetic input: for the forward
 workloads one mesa_forward_chunked call (log-decays, chunk states, chunk-level scan, batched
 per-token CG with the fused readout); for the decode workload one mesa_decode_step over all
-sequences and heads.  Inputs are resident in HBM before the timed region; the L2 (129 MB) is
+sequences and heads; for the backward workload one mesa_backward_chunked call (the forward's
+solves recomputed, the second solve per token, the state adjoints and every gradient).  Inputs are resident in HBM before the timed region; the L2 (129 MB) is
 flushed by a 256 MiB device write between timed steps unless the step's working set is
 larger than L2.  Kernel times come from CUDA events on the launching stream; `e2e` repeats
 the measurement through the same C-ABI call with pinned host buffers, copies included.
@@ -35,6 +36,7 @@ sys.path.insert(0, ROOT)
 from mesa_layer_gb300 import synth  # noqa: E402
 
 METRIC = "Mesa-layer fwd tokens/s on 1 GB300 (per CG iters) + % tensor/HBM roofline"
+METRIC_BWD = "Mesa-layer bwd (all gradients) tokens/s on 1 GB300 (per CG iters) + % roofline of the top kernel"
 DEFAULT_WORKLOAD = "fwd_fp32_d64"
 SM_COUNT = 152
 FP32_LANES_PER_SM = 128
@@ -111,7 +113,7 @@ def cg_flops(w, iters: np.ndarray) -> float:
     return float((iters.astype(np.float64) + 1.0).sum() * per)
 
 
-def tc_executed_flops(w, iters: np.ndarray) -> float:
+def tc_executed_flops(w, iters: np.ndarray, readout: bool = True) -> float:
     """MMA flops the tensor-core CG kernel issues: per 128-token chunk and iteration 7
     products of 128x128x128 (3 for the split state product, 2 + 2 for the key products);
     iterations run until the slowest token of the chunk stops, plus the readout."""
@@ -119,13 +121,28 @@ def tc_executed_flops(w, iters: np.ndarray) -> float:
     nc = (T + 127) // 128
     pad = np.zeros((B, H, nc * 128), dtype=np.int64)
     pad[:, :, :T] = iters
-    per_chunk = pad.reshape(B, H, nc, 128).max(axis=-1) + 1
+    per_chunk = pad.reshape(B, H, nc, 128).max(axis=-1) + (1 if readout else 0)
     return float(per_chunk.sum()) * 7 * 2.0 * 128 ** 3
 
 
 def state_flops(w) -> float:
     """Chunk-local state sums: 2 d^2 multiply-adds per token for H and for G."""
     return float(w.B * w.H * w.T) * 4.0 * w.dk * w.dk
+
+
+def bwd_grad_flops(w) -> float:
+    """The gradient kernel per token-head (32-token chunks, causal halves): the three C x C
+    dot-product blocks G V^T, X K^T, Y K^T (3 d (C + 1)), the four intra-chunk products with
+    them (4 d (C + 1)) and six d x d products with the chunk states and state adjoints
+    (12 d^2)."""
+    d, C = w.dk, 32
+    return float(w.B * w.H * w.T) * (12.0 * d * d + 7.0 * d * (C + 1))
+
+
+def bwd_rhs_flops(w) -> float:
+    """b = G_t^T g_t in chunk form: 2 d^2 + 2 d (C + 1) per token-head."""
+    d, C = w.dk, 32
+    return float(w.B * w.H * w.T) * (2.0 * d * d + 2.0 * d * (C + 1))
 
 
 def preprocess_bytes(w) -> float:
@@ -225,6 +242,19 @@ def oracle_sample(w, budget_s: float = 20.0):
             total += units * w.T
             passes += 1
         return total / dt / w.H, 1, f"{passes} pass(es) over {units} (batch, head) units x {w.T} tokens, q and k", dt
+    if w.backward:
+        # whole units: the fp64 backward per unit (two solves per token and the adjoint sweep)
+        n_units = min(w.B * w.H, max(1, threads))
+        sub = synth.backward_inputs(synth.workload(w.name, B=1, H=n_units))
+        total, dt, passes = 0, 0.0, 0
+        while dt < budget_s / 2 or passes == 0:
+            t0 = time.perf_counter()
+            oracle.backward(sub["q"], sub["k"], sub["v"], sub["gamma"], sub["lam"], sub["dout"], w.cg_iters,
+                            w.cg_tol, nthreads=threads)
+            dt += time.perf_counter() - t0
+            total += n_units * w.T
+            passes += 1
+        return total / dt / w.H, min(threads, n_units), f"{passes} pass(es) over {n_units} (batch, head) units x {w.T} tokens", dt
     if w.decode_steps:
         units = min(w.B * w.H, 64 * max(1, threads))
         steps = 8
@@ -305,6 +335,10 @@ def workload_config(w, extra=None):
         cfg.pop("T")
         if w.warm:
             cfg["cg"] += ", warm start from the previous step's solution"
+    if w.backward:
+        cfg["step"] = ("backward: forward solves recomputed, second CG per token on G_t^T dout_t, "
+                       "state adjoints, dq/dk/dv/dgamma/dlambda")
+        cfg["chunk"] = "32 (gradient kernels), 128 (tensor-core solves)"
     if w.conv_taps:
         cfg = {"workload": w.name, "B": w.B, "heads": w.H, "T": w.T, "d": w.dk, "qk_dtype": w.dtype,
                "conv_taps": w.conv_taps, "step": "q/k preprocessing: causal depthwise conv + L2 norm",
@@ -360,6 +394,8 @@ def main():
     peaks = measured_peaks()
     if w.conv_taps:
         res = bench_preprocess(args, w, rank, world, dev, lib, torch, binding)
+    elif w.backward:
+        res = bench_backward(args, w, rank, world, dev, lib, torch, binding)
     elif w.decode_steps:
         res = bench_decode(args, w, rank, world, dev, lib, torch, binding)
     else:
@@ -575,6 +611,61 @@ def bench_preprocess(args, w, rank, world, dev, lib, torch, binding):
     return res
 
 
+def bench_backward(args, w, rank, world, dev, lib, torch, binding):
+    import torch.distributed as dist
+    inp = synth.backward_inputs(w, seed=rank)
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    keys = ("q", "k", "v", "gamma", "dout")
+    d_in = {k: torch.from_numpy(inp[k]).to(dev).to(td if k in ("q", "k", "v", "dout") else torch.float32).contiguous()
+            for k in keys + ("lam",)}
+    B, H, T, dk, dv = w.B, w.H, w.T, w.dk, w.dv
+    outs = {"dq": torch.empty((B, H, T, dk), dtype=td, device=dev), "dk": torch.empty((B, H, T, dk), dtype=td, device=dev),
+            "dv": torch.empty((B, H, T, dv), dtype=td, device=dev),
+            "dgamma": torch.empty((B, H, T), dtype=torch.float32, device=dev),
+            "dlambda": torch.empty((H, dk), dtype=torch.float32, device=dev),
+            "iters_fwd": torch.empty((B, H, T), dtype=torch.int32, device=dev),
+            "iters_bwd": torch.empty((B, H, T), dtype=torch.int32, device=dev)}
+    ws = torch.empty(binding.mesa_backward_workspace_size(B, H, T, dk, dv), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    in_bytes = sum(d_in[k].numel() * d_in[k].element_size() for k in keys)
+    needs_flush = in_bytes < 2 * (129 << 20)
+
+    def call(d):
+        binding.mesa_backward_chunked(d["q"], d["k"], d["v"], d["gamma"], d_in["lam"], d["dout"], w.cg_iters, w.cg_tol,
+                                      workspace=ws, **outs)
+
+    res = timed_loop(args, torch, lib, lambda i: call(d_in), (lambda: flush.random_(0, 255)) if needs_flush else None,
+                     world, dist, dev)
+    res.update({"iters": outs["iters_bwd"].cpu().numpy(), "tokens_per_step": B * T, "flush": needs_flush})
+    if not args.no_e2e:
+        h = {k: torch.from_numpy(inp[k]).to(td if k in ("q", "k", "v", "dout") else torch.float32).pin_memory()
+             for k in keys}
+        d = {k: torch.empty_like(h[k], device=dev) for k in h}
+        back = {k: torch.empty(outs[k].shape, dtype=outs[k].dtype).pin_memory() for k in ("dq", "dk", "dv", "dgamma", "dlambda")}
+
+        def estep():
+            for k in h:
+                d[k].copy_(h[k], non_blocking=True)
+            call(d)
+            for k in back:
+                back[k].copy_(outs[k], non_blocking=True)
+
+        for _ in range(3):
+            estep()
+        torch.cuda.synchronize()
+        n = max(3, min(args.steps, 20))
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record()
+        for _ in range(n):
+            estep()
+        e_.record()
+        torch.cuda.synchronize()
+        res["e2e"] = {"ms_per_step": s_.elapsed_time(e_) / n,
+                      "h2d": sum(t.numel() * t.element_size() for t in h.values()),
+                      "d2h": sum(t.numel() * t.element_size() for t in back.values())}
+    return res
+
+
 def aggregate(step_ms: float, tokens_per_rank: int, world: int, torch, dist, device="cuda"):
     """Whole-job figures of a replicated run: the slowest rank's time per step and the
     tokens of all ranks.  Each rank runs its own replica (independent sequences), so the
@@ -614,7 +705,16 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
                 "frac": achieved / peaks["hbm_gbs"], "traffic": traffic, "kernel": top_name,
                 "peak_source": peaks["source"], "algorithmic_bytes": bytes_}
     else:
-        flops = cg_flops(w, it) if "cg" in top_name else state_flops(w)
+        if "cg" in top_name:
+            # a backward solve has no readout: iterations only
+            flops = cg_flops(w, it) - (0.0 if not w.backward else
+                                       float(it.size) * (2.0 * w.dk * w.dk + 2.0 * w.dk * (w.chunk + 1)))
+        elif "bwd_grad" in top_name:
+            flops = bwd_grad_flops(w)
+        elif "bwd_rhs" in top_name:
+            flops = bwd_rhs_flops(w)
+        else:
+            flops = state_flops(w)
         achieved = flops / (avg_ms / 1e3) / 1e12
         if "_tc_" in top_name:
             # fp16 tcgen05 MMAs run at the bf16 dense rate; the measured cuBLAS bf16 peak
@@ -622,7 +722,7 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": traffic, "kernel": top_name,
                     "peak_source": f"{peaks['source']} bf16 dense (fp16 kind, same rate)",
-                    "executed_tensor_tflops": tc_executed_flops(w, it) / (avg_ms / 1e3) / 1e12}
+                    "executed_tensor_tflops": tc_executed_flops(w, it, not w.backward) / (avg_ms / 1e3) / 1e12}
         else:
             peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
             roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -636,7 +736,7 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
              "l2": ("flushed between timed steps (256 MiB device write)" if res["flush"]
                     else "working set larger than L2, not flushed"),
              "kernels": kernels, "wall_s_timed_loop": res["wall_s"]})
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+    line = {"metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, see mesa_layer_gb300/synth.py)",
             "config": workload_config(w, extra), "roofline": roof, "cpu_baseline": cpu,

@@ -103,6 +103,39 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
                          size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Backward pass of mesa_forward_chunked (zero initial states): the gradients of a loss L
+ * given dout = dL/dout.  The pages claim training ("Paralelizacao" bullet: O(T) training;
+ * "Contribuicoes", item 1) but give no gradient; this is implicit differentiation through
+ * each token's solve, taking the CG iterate x_t as (H_t + Lambda)^-1 q_t.  With g_t = dout_t:
+ *     b_t = G_t^T g_t,   y_t = CG(H_t + Lambda, b_t)     (the forward's CG rule and cg_iters,
+ *                                                          cg_tol; from 0)
+ *     dq_t = y_t,        dlambda = -sum over batch and time of y_t o x_t
+ * and the state gradients -y_t x_t^T (of H_t) and g_t x_t^T (of G_t) carried back through
+ * H_t = gamma_t H_{t-1} + k_t k_t^T, G_t = gamma_t G_{t-1} + v_t k_t^T:
+ *     dk_t = (dH_t + dH_t^T) k_t + dG_t^T v_t,  dv_t = dG_t k_t,
+ *     dgamma_t = <dH_t, H_{t-1}> + <dG_t, G_{t-1}>,
+ * dH_t, dG_t the total adjoints of the states after token t.  With exact solves these are
+ * the exact gradients of o_t = G_t (H_t + Lambda)^-1 q_t (not those of k unrolled CG steps).
+ * The forward's solves x_t are recomputed (nothing is kept from the forward call).
+ *   q, k, dq, dk_out  [B, H, T, dk]  dtype;   v, dout, dv_out  [B, H, T, dv]  dtype
+ *   gamma, dgamma [B, H, T] fp32 (a gate below e^-80, where the forward clamps the log-gate,
+ *                 gets dgamma = 0);  lambda_diag, dlambda [H, dk] fp32 (dlambda is summed
+ *                 over the batch and overwritten)
+ *   iters_fwd, iters_bwd  [B, H, T] int32 or NULL: iterations of the x and y solves
+ *   workspace  device scratch of at least mesa_backward_workspace_size() bytes, 256-byte
+ *              aligned; its first word is the status word read by mesa_forward_status.
+ * Sizes, errors and stream semantics as mesa_forward_chunked; the work is chunked in
+ * 32-token chunks (128 for the tensor-core solves: bf16, d = 128, 16-byte aligned).
+ */
+size_t mesa_backward_workspace_size(int B, int H, int T, int dk, int dv);
+int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const void *q,
+                          const void *k, const void *v, const float *gamma,
+                          const float *lambda_diag, const void *dout, int cg_iters, float cg_tol,
+                          void *dq, void *dk_out, void *dv_out, float *dgamma, float *dlambda,
+                          int32_t *iters_fwd, int32_t *iters_bwd, void *workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * One recurrent decode step for N sequences x H heads ("Paralelizacao" bullet: O(1)
  * inference), in place on the caller's fp32 states:
  *   H_state [N, H, dk, dk] (symmetric; 16-byte aligned)  <- gamma H_state + k k^T

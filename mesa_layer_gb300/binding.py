@@ -64,6 +64,11 @@ def load(build_if_missing: bool = True):
     lib.mesa_qk_preprocess.argtypes = [_i] * 6 + [_vp, _vp, _fp, _fp, _vp, _vp, _vp]
     lib.mesa_qk_preprocess_step.restype = _i
     lib.mesa_qk_preprocess_step.argtypes = [_i] * 5 + [_vp, _vp, _fp, _fp, _fp, _vp, _vp, _vp]
+    lib.mesa_backward_workspace_size.restype = _sz
+    lib.mesa_backward_workspace_size.argtypes = [_i] * 5
+    lib.mesa_backward_chunked.restype = _i
+    lib.mesa_backward_chunked.argtypes = [_i] * 6 + [_vp] * 3 + [_fp, _fp, _vp, _i, _f] + [_vp] * 3 + [
+        _fp, _fp, _ip, _ip, _vp, _sz, _vp]
     _lib = lib
     return lib
 
@@ -136,6 +141,50 @@ def mesa_forward_chunked(q, k, v, gamma, lambda_diag, cg_iters, cg_tol, chunk, o
                                   _ptr(G_final), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "mesa_forward_chunked")
     return out, iters_used
+
+
+def mesa_backward_workspace_size(B, H, T, dk, dv) -> int:
+    return int(load().mesa_backward_workspace_size(B, H, T, dk, dv))
+
+
+def mesa_backward_chunked(q, k, v, gamma, lambda_diag, dout, cg_iters, cg_tol, dq=None, dk=None, dv=None,
+                          dgamma=None, dlambda=None, iters_fwd=None, iters_bwd=None, workspace=None,
+                          stream=None):
+    """Backward pass of mesa_forward_chunked (zero initial states): gradients of a loss given
+    dout = dL/dout [B, H, T, dv] (dtype of q).  Returns (dq, dk, dv, dgamma, dlambda,
+    iters_fwd, iters_bwd); dlambda [H, dk] is summed over the batch."""
+    lib = load()
+    B, H, T, dkk = q.shape
+    dvv = v.shape[-1]
+    code = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        _require(t, name, q.dtype)
+    _require(gamma, "gamma", torch.float32)
+    _require(lambda_diag, "lambda_diag", torch.float32)
+    dev = q.device
+    dq = torch.empty((B, H, T, dkk), dtype=q.dtype, device=dev) if dq is None else dq
+    dk = torch.empty((B, H, T, dkk), dtype=q.dtype, device=dev) if dk is None else dk
+    dv = torch.empty((B, H, T, dvv), dtype=q.dtype, device=dev) if dv is None else dv
+    dgamma = torch.empty((B, H, T), dtype=torch.float32, device=dev) if dgamma is None else dgamma
+    dlambda = torch.empty((H, dkk), dtype=torch.float32, device=dev) if dlambda is None else dlambda
+    iters_fwd = torch.empty((B, H, T), dtype=torch.int32, device=dev) if iters_fwd is None else iters_fwd
+    iters_bwd = torch.empty((B, H, T), dtype=torch.int32, device=dev) if iters_bwd is None else iters_bwd
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _require(t, name, q.dtype)
+    for name, t in (("dgamma", dgamma), ("dlambda", dlambda)):
+        _require(t, name, torch.float32)
+    _require(iters_fwd, "iters_fwd", torch.int32)
+    _require(iters_bwd, "iters_bwd", torch.int32)
+    need = mesa_backward_workspace_size(B, H, T, dkk, dvv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _require(workspace, "workspace")
+    st = lib.mesa_backward_chunked(B, H, T, dkk, dvv, code, _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
+                                   _ptr(lambda_diag), _ptr(dout), int(cg_iters), float(cg_tol), _ptr(dq),
+                                   _ptr(dk), _ptr(dv), _ptr(dgamma), _ptr(dlambda), _ptr(iters_fwd),
+                                   _ptr(iters_bwd), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "mesa_backward_chunked")
+    return dq, dk, dv, dgamma, dlambda, iters_fwd, iters_bwd
 
 
 def mesa_decode_step(H_state, G_state, q, k, v, gamma, lambda_diag, cg_iters, cg_tol, out=None,

@@ -1,0 +1,481 @@
+// backward.cu -- the backward pass of the Mesa layer (gradients of a loss through the layer).
+//
+// MesaNet technical summary (gist.science/pt/paper/2506.05233): the layer is trained
+// ("Paralelizacao" bullet: O(T) training; "Contribuicoes", item 1: efficient training with the
+// chunkwise CG solver); the pages give no gradient.  Implicit differentiation through each
+// token's solve: the CG iterate x_t stands for (H_t + Lambda)^{-1} q_t, so with g_t = dL/do_t
+//     b_t = G_t^T g_t,  y_t = CG(H_t + Lambda, b_t),  dq_t = y_t,  dlambda = -sum_t y_t o x_t,
+// the direct state gradients are -y_t x_t^T (H_t) and g_t x_t^T (G_t), and the recurrence
+// H_t = gamma_t H_{t-1} + k_t k_t^T (same for G) carries them back in time.
+//
+// Chunked form (chunks of BC tokens, l_i = sum of log gates inside the chunk, D_ij =
+// e^{l_i - l_j} for j <= i, w_j = e^{l_last - l_j}, a_c = e^{l_last}).  Per chunk, rows =
+// tokens, with X, Y, G (the incoming gradients), K, V the chunk's tiles:
+//   b      = diag(e^l) G S^G_{c-1} + ((G V^T) o D) K                       (mesa_bwd_rhs_kernel)
+//   dG^c   = sum over later tokens t of zeta(t, end of c) g_t x_t^T, dH^c likewise with
+//            -y_t x_t^T: the adjoints of the states after chunk c, from the chunk sums
+//            Delta_c = G^T diag(e^l) X (and -Y^T diag(e^l) X) by the reverse scan
+//            dG^{c-1} = a_c dG^c + Delta_c                 (mesa_bwd_delta/scan_kernel)
+//   dV     = M2^T G + diag(w) K dG^c^T
+//   dK     = (M1 - M3)^T X - M2^T Y + diag(w) (V dG^c + K dH^c + K dH^c^T)
+//            with M1 = (G V^T) o D, M2 = (X K^T) o D, M3 = (Y K^T) o D   (mesa_bwd_grad_kernel)
+// Gate gradient.  With c_ts = zeta_ts (x_t . k_s) [(g_t . v_s) - (y_t . k_s)] the gradient of
+// log gamma_u is the sum of c_ts over the pairs t >= u > s.  Per chunk it splits into the
+// pairs inside the chunk (a rectangle of the C x C matrix M2 o (G V^T - Y K^T)), the pairs
+// whose later token is in the chunk and earlier one before it (sum over t >= u of
+// e^{l_t} [g_t . S^G x_t - y_t . S^H x_t]), the pairs whose earlier token is in the chunk
+// and later one after it (sum over s < u of w_s [v_s . dG^c k_s + k_s . dH^c k_s]) and the
+// pairs across the whole chunk (a_c [<dG^c, S^G_{c-1}> + <dH^c, S^H_{c-1}>]).  Each part is
+// a sum of like terms, with no sequence-long cumulative sum of differences;
+// dL/dgamma_u = (that sum) / gamma_u (0 for gates below the log-gate floor, where the
+// forward is flat).
+//
+// CUDA-core fp32 kernels.  A CTA of 2D threads works on one chunk (BC = 32 tokens); thread
+// (rg, c4) holds 4 rows (rg + 8m) x 4 columns (4 c4 .. 4 c4 + 3) of every C x D result.
+#include "common.cuh"
+#include "launch.h"
+
+namespace mesa {
+
+namespace {
+constexpr int BC = kBwdChunk;
+
+// [BC][D + 4] fp32 tile of chunk rows from global memory (rows >= Cv are zero).
+template <int D, typename T>
+__device__ __forceinline__ void load_tile(float *dst, const T *src, int Cv) {
+  for (int e = threadIdx.x; e < BC * D; e += blockDim.x) {
+    const int r = e / D, c = e % D;
+    dst[r * (D + 4) + c] = r < Cv ? ld(src, (size_t)e) : 0.0f;
+  }
+}
+
+// [D][D + 4] copy of a D x D fp32 matrix (transposed: dst[b][a] = S[a][b]); S == nullptr: 0.
+template <int D>
+__device__ __forceinline__ void load_state(float *dst, const float *S, bool transpose) {
+  for (int e4 = threadIdx.x; e4 < D * D / 4; e4 += blockDim.x) {
+    const int r = (4 * e4) / D, c = (4 * e4) % D;
+    const float4 v = S ? reinterpret_cast<const float4 *>(S)[e4] : make_float4(0, 0, 0, 0);
+    if (transpose) {
+      dst[(c + 0) * (D + 4) + r] = v.x;
+      dst[(c + 1) * (D + 4) + r] = v.y;
+      dst[(c + 2) * (D + 4) + r] = v.z;
+      dst[(c + 3) * (D + 4) + r] = v.w;
+    } else {
+      *reinterpret_cast<float4 *>(dst + r * (D + 4) + c) = v;
+    }
+  }
+}
+
+// acc[m][n] += sum_{a < K} A(rg + 8m, a) * B[a][4 c4 + n]; A(r, a) = A[r * ars + a * acs].
+__device__ __forceinline__ void mm_acc(float (&acc)[4][4], const float *A, int ars, int acs, int rg,
+                                       const float *B, int ldb, int c4, int K) {
+#pragma unroll 4
+  for (int a = 0; a < K; a++) {
+    const float4 b = *reinterpret_cast<const float4 *>(B + a * ldb + 4 * c4);
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+      const float av = A[(rg + 8 * m) * ars + a * acs];
+      acc[m][0] = fmaf(av, b.x, acc[m][0]);
+      acc[m][1] = fmaf(av, b.y, acc[m][1]);
+      acc[m][2] = fmaf(av, b.z, acc[m][2]);
+      acc[m][3] = fmaf(av, b.w, acc[m][3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void zero4x4(float (&acc)[4][4]) {
+#pragma unroll
+  for (int m = 0; m < 4; m++)
+#pragma unroll
+    for (int n = 0; n < 4; n++) acc[m][n] = 0.0f;
+}
+
+// Row-dot of two [BC][D + 4] tiles: sum_a A[i][a] B[j][a].
+template <int D>
+__device__ __forceinline__ float row_dot(const float *A, int i, const float *B, int j) {
+  const float4 *a = reinterpret_cast<const float4 *>(A + i * (D + 4));
+  const float4 *b = reinterpret_cast<const float4 *>(B + j * (D + 4));
+  float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll 4
+  for (int e = 0; e < D / 4; e += 2) {
+    const float4 x = a[e], y = b[e];
+    s0 = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, s0))));
+    if (e + 1 < D / 4) {
+      const float4 x1 = a[e + 1], y1 = b[e + 1];
+      s1 = fmaf(x1.x, y1.x, fmaf(x1.y, y1.y, fmaf(x1.z, y1.z, fmaf(x1.w, y1.w, s1))));
+    }
+  }
+  return s0 + s1;
+}
+}  // namespace
+
+// b = diag(e^l) G S^G_{c-1} + ((G V^T) o D) K.  grid (NC, U), block 2D.
+template <int D, typename TIO>
+__global__ void __launch_bounds__(256) mesa_bwd_rhs_kernel(BwdArgs a, FwdWorkspace ws, int NC) {
+  constexpr int SPD = D + 4, SPC = BC + 1;
+  const int c = blockIdx.x, u = blockIdx.y, T = a.T;
+  const int t0 = c * BC, Cv = min(BC, T - t0);
+  const size_t tokbase = (size_t)u * T + t0;
+  extern __shared__ __align__(16) float smem[];
+  float *Gs = smem, *Vs = Gs + BC * SPD, *Ks = Vs + BC * SPD, *Sg = Ks + BC * SPD;
+  float *M = Sg + D * SPD, *el = M + BC * SPC;
+  load_tile<D>(Gs, (const TIO *)a.dout + tokbase * D, Cv);
+  load_tile<D>(Vs, (const TIO *)a.v + tokbase * D, Cv);
+  load_tile<D>(Ks, (const TIO *)a.k + tokbase * D, Cv);
+  load_state<D>(Sg, c > 0 ? ws.SG + ((size_t)u * NC + c - 1) * D * D : nullptr, false);
+  for (int j = threadIdx.x; j < BC; j += blockDim.x) el[j] = j < Cv ? ws.ell[tokbase + j] : 0.0f;
+  __syncthreads();
+  for (int e = threadIdx.x; e < BC * BC; e += blockDim.x) {
+    const int i = e / BC, j = e % BC;
+    M[i * SPC + j] = (j <= i && i < Cv) ? expf(el[i] - el[j]) * row_dot<D>(Gs, i, Vs, j) : 0.0f;
+  }
+  __syncthreads();
+  const int rg = threadIdx.x / (D / 4), c4 = threadIdx.x % (D / 4);
+  float acc[4][4], acc2[4][4];
+  zero4x4(acc);
+  zero4x4(acc2);
+  mm_acc(acc, Gs, SPD, 1, rg, Sg, SPD, c4, D);
+  mm_acc(acc2, M, SPC, 1, rg, Ks, SPD, c4, BC);
+#pragma unroll
+  for (int m = 0; m < 4; m++) {
+    const int i = rg + 8 * m;
+    if (i >= Cv) continue;
+    const float e = expf(el[i]);
+    float4 o;
+    o.x = fmaf(e, acc[m][0], acc2[m][0]);
+    o.y = fmaf(e, acc[m][1], acc2[m][1]);
+    o.z = fmaf(e, acc[m][2], acc2[m][2]);
+    o.w = fmaf(e, acc[m][3], acc2[m][3]);
+    *reinterpret_cast<float4 *>(a.rhs + (tokbase + i) * D + 4 * c4) = o;
+  }
+}
+
+// Chunk sums of the state adjoints: Delta^G_c = sum_i e^{l_i} g_i x_i^T (z = 0, into dGs)
+// and Delta^H_c = -sum_i e^{l_i} y_i x_i^T (z = 1, into dHs).  grid (NC, U, 2), block 256;
+// each thread owns a (D/16) x (D/16) register tile.
+template <int D, typename TIO>
+__global__ void __launch_bounds__(256) mesa_bwd_delta_kernel(BwdArgs a, FwdWorkspace ws, int NC) {
+  constexpr int TM = D / 16;
+  const int c = blockIdx.x, u = blockIdx.y, isH = blockIdx.z, T = a.T;
+  const int t0 = c * BC, Cv = min(BC, T - t0);
+  const size_t tokbase = (size_t)u * T + t0;
+  __shared__ __align__(16) float Ls[BC * D], Xs[BC * D], wv[BC];
+  for (int e = threadIdx.x; e < Cv * D; e += blockDim.x) {
+    Ls[e] = isH ? -a.Y[tokbase * D + e] : ld((const TIO *)a.dout, tokbase * D + e);
+    Xs[e] = a.X[tokbase * D + e];
+  }
+  for (int j = threadIdx.x; j < Cv; j += blockDim.x) wv[j] = expf(ws.ell[tokbase + j]);
+  __syncthreads();
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[TM][TM];
+#pragma unroll
+  for (int m = 0; m < TM; m++)
+#pragma unroll
+    for (int n = 0; n < TM; n++) acc[m][n] = 0.0f;
+  for (int j = 0; j < Cv; j++) {
+    const float wj = wv[j];
+    float la[TM], xb[TM];
+#pragma unroll
+    for (int m = 0; m < TM; m++) la[m] = Ls[j * D + ty + 16 * m] * wj;
+#pragma unroll
+    for (int n = 0; n < TM; n++) xb[n] = Xs[j * D + tx + 16 * n];
+#pragma unroll
+    for (int m = 0; m < TM; m++)
+#pragma unroll
+      for (int n = 0; n < TM; n++) acc[m][n] = fmaf(la[m], xb[n], acc[m][n]);
+  }
+  float *S = (isH ? a.dHs : a.dGs) + ((size_t)u * NC + c) * D * D;
+#pragma unroll
+  for (int m = 0; m < TM; m++)
+#pragma unroll
+    for (int n = 0; n < TM; n++) S[(ty + 16 * m) * D + tx + 16 * n] = acc[m][n];
+}
+
+// Reverse scan in place: entry c becomes the adjoint after chunk c (zero for the last chunk),
+// dS^{c-1} = a_c dS^c + Delta_c.  grid (ceil(2 D^2 / 256), U), block 256.
+template <int D>
+__global__ void __launch_bounds__(256) mesa_bwd_scan_kernel(BwdArgs a, FwdWorkspace ws, int NC) {
+  const int u = blockIdx.y, T = a.T;
+  int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= 2 * D * D) return;
+  const bool isH = e >= D * D;
+  if (isH) e -= D * D;
+  float *S = (isH ? a.dHs : a.dGs) + (size_t)u * NC * D * D + e;
+  float s = 0.0f;
+  constexpr int G = 8;  // the loads of a group of chunks go out before its dependent updates
+  for (int c0 = NC - 1; c0 >= 0; c0 -= G) {
+    float dl[G], av[G];
+#pragma unroll
+    for (int g = 0; g < G; g++) {
+      const int c = c0 - g;
+      if (c >= 0) {
+        dl[g] = S[(size_t)c * D * D];
+        av[g] = ws.ell[(size_t)u * T + min(T, (c + 1) * BC) - 1];
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; g++) {
+      const int c = c0 - g;
+      if (c >= 0) {
+        S[(size_t)c * D * D] = s;
+        s = fmaf(expf(av[g]), s, dl[g]);
+      }
+    }
+  }
+}
+
+// dq, dk, dv, dgamma and the per-chunk dlambda partials.  grid (NC, U), block 2D.
+template <int D, typename TIO>
+__global__ void __launch_bounds__(256) mesa_bwd_grad_kernel(BwdArgs a, FwdWorkspace ws, int NC) {
+  constexpr int SPD = D + 4, SPC = BC + 1, NQ = D / 4;
+  const int c = blockIdx.x, u = blockIdx.y, T = a.T;
+  const int t0 = c * BC, Cv = min(BC, T - t0);
+  const size_t tokbase = (size_t)u * T + t0;
+  extern __shared__ __align__(16) float smem[];
+  float *Ks = smem, *Vs = Ks + BC * SPD, *Gs = Vs + BC * SPD, *Xs = Gs + BC * SPD;
+  float *Ys = Xs + BC * SPD, *St = Ys + BC * SPD;
+  float *M1 = St + D * SPD, *M2 = M1 + BC * SPC, *M3 = M2 + BC * SPC, *Cm = M3 + BC * SPC;
+  float *part = Cm + BC * SPC;         // [BC][NQ + 1] per-thread partial row sums
+  float *el = part + BC * (NQ + 1);    // [BC] l_i
+  float *wv = el + BC;                 // [BC] w_j
+  float *rowi = wv + BC;               // [BC] e^{l_t} (g_t . S^G x_t - y_t . S^H x_t)
+  float *coli = rowi + BC;             // [BC] w_s (v_s . dG k_s + k_s . dH k_s)
+  float *red = coli + BC;              // [2D] block-reduction scratch
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int rg = tid / NQ, c4 = tid % NQ;
+  const bool last = c == NC - 1, first = c == 0;
+
+  load_tile<D>(Ks, (const TIO *)a.k + tokbase * D, Cv);
+  load_tile<D>(Vs, (const TIO *)a.v + tokbase * D, Cv);
+  load_tile<D>(Gs, (const TIO *)a.dout + tokbase * D, Cv);
+  load_tile<D>(Xs, a.X + tokbase * D, Cv);
+  load_tile<D>(Ys, a.Y + tokbase * D, Cv);
+  for (int j = tid; j < BC; j += nt) el[j] = j < Cv ? ws.ell[tokbase + j] : 0.0f;
+  __syncthreads();
+  const float lend = el[Cv - 1];
+  for (int j = tid; j < BC; j += nt) wv[j] = j < Cv ? expf(lend - el[j]) : 0.0f;
+  for (int e = tid; e < BC * BC; e += nt) {
+    const int i = e / BC, j = e % BC;
+    float m1 = 0.0f, m2 = 0.0f, m3 = 0.0f, cm = 0.0f;
+    if (j <= i && i < Cv) {
+      const float dd = expf(el[i] - el[j]);
+      const float p1 = row_dot<D>(Gs, i, Vs, j), p2 = row_dot<D>(Xs, i, Ks, j),
+                  p3 = row_dot<D>(Ys, i, Ks, j);
+      m1 = dd * p1;
+      m2 = dd * p2;
+      m3 = dd * p3;
+      cm = m2 * (p1 - p3);
+    }
+    M1[i * SPC + j] = m1;
+    M2[i * SPC + j] = m2;
+    M3[i * SPC + j] = m3;
+    Cm[i * SPC + j] = cm;
+  }
+  __syncthreads();
+
+  // intra-chunk parts: dV = M2^T G, dK = (M1 - M3)^T X - M2^T Y
+  float accV[4][4], accK[4][4], t[4][4];
+  zero4x4(accV);
+  zero4x4(accK);
+  mm_acc(accV, M2, 1, SPC, rg, Gs, SPD, c4, BC);
+  mm_acc(accK, M1, 1, SPC, rg, Xs, SPD, c4, BC);
+  zero4x4(t);
+  mm_acc(t, M3, 1, SPC, rg, Xs, SPD, c4, BC);
+  mm_acc(t, M2, 1, SPC, rg, Ys, SPD, c4, BC);
+#pragma unroll
+  for (int m = 0; m < 4; m++)
+#pragma unroll
+    for (int n = 0; n < 4; n++) accK[m][n] -= t[m][n];
+
+  // per-row sums of this thread's 4 columns of t . Z (Z a tile), finished over the row
+  auto row_partial = [&](const float *Z) {
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+      const int r = rg + 8 * m;
+      const float4 z = *reinterpret_cast<const float4 *>(Z + r * SPD + 4 * c4);
+      part[r * (NQ + 1) + c4] = t[m][0] * z.x + t[m][1] * z.y + t[m][2] * z.z + t[m][3] * z.w;
+    }
+  };
+  auto row_finish = [&](float *dst, bool add) {  // dst[r] (+)= sum of the row's partials
+    for (int r = tid; r < BC; r += nt) {
+      float s = 0.0f;
+      for (int q = 0; q < NQ; q++) s += part[r * (NQ + 1) + q];
+      dst[r] = add ? dst[r] + s : s;
+    }
+  };
+  auto stage = [&](const float *S, bool transpose) {
+    __syncthreads();  // every thread is done with the previous contents of St and part
+    load_state<D>(St, S, transpose);
+    __syncthreads();
+  };
+  for (int r = tid; r < BC; r += nt) rowi[r] = coli[r] = 0.0f;
+
+  // later chunks: dG^c, dH^c (zero after the last chunk)
+  if (!last) {
+    const float *dG = a.dGs + ((size_t)u * NC + c) * D * D;
+    const float *dH = a.dHs + ((size_t)u * NC + c) * D * D;
+    stage(dG, true);  // St = dG^T: t = K dG^T, rows (dG k_s)^T
+    zero4x4(t);
+    mm_acc(t, Ks, SPD, 1, rg, St, SPD, c4, D);
+    row_partial(Vs);
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+#pragma unroll
+      for (int n = 0; n < 4; n++) accV[m][n] = fmaf(wv[rg + 8 * m], t[m][n], accV[m][n]);
+    __syncthreads();
+    row_finish(coli, false);
+    stage(dG, false);  // St = dG: t = V dG, rows (dG^T v_s)^T
+    zero4x4(t);
+    mm_acc(t, Vs, SPD, 1, rg, St, SPD, c4, D);
+    stage(dH, false);  // St = dH: t += K dH, rows (dH^T k_s)^T
+    mm_acc(t, Ks, SPD, 1, rg, St, SPD, c4, D);
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+#pragma unroll
+      for (int n = 0; n < 4; n++) accK[m][n] = fmaf(wv[rg + 8 * m], t[m][n], accK[m][n]);
+    stage(dH, true);  // St = dH^T: t = K dH^T, rows (dH k_s)^T
+    zero4x4(t);
+    mm_acc(t, Ks, SPD, 1, rg, St, SPD, c4, D);
+    row_partial(Ks);
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+#pragma unroll
+      for (int n = 0; n < 4; n++) accK[m][n] = fmaf(wv[rg + 8 * m], t[m][n], accK[m][n]);
+    __syncthreads();
+    row_finish(coli, true);
+  }
+  // earlier chunks: S^G_{c-1}, S^H_{c-1} (zero before the first chunk)
+  float through = 0.0f;
+  if (!first) {
+    const float *SG = ws.SG + ((size_t)u * NC + c - 1) * D * D;
+    const float *SH = ws.SH + ((size_t)u * NC + c - 1) * D * D;
+    stage(SG, true);  // St = S^G^T: t = X S^G^T, rows (S^G x_t)^T
+    zero4x4(t);
+    mm_acc(t, Xs, SPD, 1, rg, St, SPD, c4, D);
+    row_partial(Gs);
+    __syncthreads();
+    row_finish(rowi, false);
+    stage(SH, false);  // S^H symmetric: t = X S^H, rows (S^H x_t)^T
+    zero4x4(t);
+    mm_acc(t, Xs, SPD, 1, rg, St, SPD, c4, D);
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+#pragma unroll
+      for (int n = 0; n < 4; n++) t[m][n] = -t[m][n];
+    row_partial(Ys);
+    __syncthreads();
+    row_finish(rowi, true);
+    // pairs across the whole chunk: a_c (<dG^c, S^G_{c-1}> + <dH^c, S^H_{c-1}>)
+    if (!last) {
+      const float4 *dG4 = reinterpret_cast<const float4 *>(a.dGs + ((size_t)u * NC + c) * D * D);
+      const float4 *dH4 = reinterpret_cast<const float4 *>(a.dHs + ((size_t)u * NC + c) * D * D);
+      const float4 *SG4 = reinterpret_cast<const float4 *>(SG), *SH4 = reinterpret_cast<const float4 *>(SH);
+      float s = 0.0f;
+      for (int e = tid; e < D * D / 4; e += nt) {
+        const float4 x = dG4[e], y = SG4[e], z = dH4[e], w = SH4[e];
+        s += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w + z.x * w.x + z.y * w.y + z.z * w.z + z.w * w.w;
+      }
+      red[tid] = s;
+      __syncthreads();
+      float tot = 0.0f;
+      for (int q = 0; q < nt; q++) tot += red[q];  // the same order in every thread
+      through = expf(lend) * tot;
+    }
+  }
+  __syncthreads();
+
+  // outputs
+#pragma unroll
+  for (int m = 0; m < 4; m++) {
+    const int i = rg + 8 * m;
+    if (i >= Cv) continue;
+    const size_t o = (tokbase + i) * D + 4 * c4;
+    const float4 y = *reinterpret_cast<const float4 *>(Ys + i * SPD + 4 * c4);
+    st((TIO *)a.dq_out, o + 0, y.x);
+    st((TIO *)a.dq_out, o + 1, y.y);
+    st((TIO *)a.dq_out, o + 2, y.z);
+    st((TIO *)a.dq_out, o + 3, y.w);
+#pragma unroll
+    for (int n = 0; n < 4; n++) {
+      st((TIO *)a.dk_out, o + n, accK[m][n]);
+      st((TIO *)a.dv_out, o + n, accV[m][n]);
+    }
+  }
+  for (int col = tid; col < D; col += nt) {  // -sum_t y_t o x_t over the chunk
+    float s = 0.0f;
+    for (int i = 0; i < Cv; i++) s = fmaf(Ys[i * SPD + col], Xs[i * SPD + col], s);
+    a.dlam_part[((size_t)u * NC + c) * D + col] = -s;
+  }
+  for (int uu = tid; uu < Cv; uu += nt) {
+    float s = through;
+    for (int tt = uu; tt < Cv; tt++) {  // later token in the chunk
+      s += rowi[tt] * expf(el[tt]);
+      for (int ss = 0; ss < uu; ss++) s += Cm[tt * SPC + ss];
+    }
+    for (int ss = 0; ss < uu; ss++) s += coli[ss] * wv[ss];  // later token after the chunk
+    const float g = a.gamma[tokbase + uu];
+    a.dgamma[tokbase + uu] = (logf(g) >= kLogGateFloor) ? s / g : 0.0f;
+  }
+}
+
+// dlambda[h] = sum over the batch and the chunks of the partials.  grid H, block D.
+__global__ void mesa_bwd_lambda_kernel(BwdArgs a, int NC) {
+  const int h = blockIdx.x, col = threadIdx.x, D = a.dk;
+  float s = 0.0f;
+  for (int b = 0; b < a.B; b++)
+    for (int c = 0; c < NC; c++) s += a.dlam_part[(((size_t)b * a.H + h) * NC + c) * D + col];
+  a.dlambda[(size_t)h * D + col] = s;
+}
+
+namespace {
+template <int D, typename TIO>
+int launch_bwd_t(const BwdArgs &a, const FwdWorkspace &ws, int phase, cudaStream_t st) {
+  const int U = a.B * a.H, NC = (a.T + BC - 1) / BC;
+  constexpr int SPD = D + 4, SPC = BC + 1;
+  if (phase == 0) {
+    const size_t smem = sizeof(float) * (3 * BC * SPD + D * SPD + BC * SPC + BC);
+    auto k = mesa_bwd_rhs_kernel<D, TIO>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return -1;
+    timing_mark_begin(K_BWD_RHS, st);
+    k<<<dim3(NC, U), 2 * D, smem, st>>>(a, ws, NC);
+    timing_mark_end(K_BWD_RHS, st);
+  } else {
+    timing_mark_begin(K_BWD_STATES, st);
+    mesa_bwd_delta_kernel<D, TIO><<<dim3(NC, U, 2), 256, 0, st>>>(a, ws, NC);
+    mesa_bwd_scan_kernel<D><<<dim3((2 * D * D + 255) / 256, U), 256, 0, st>>>(a, ws, NC);
+    timing_mark_end(K_BWD_STATES, st);
+    const size_t smem = sizeof(float) * (5 * BC * SPD + D * SPD + 4 * BC * SPC + BC * (D / 4 + 1) +
+                                         4 * BC + 2 * D);
+    auto k = mesa_bwd_grad_kernel<D, TIO>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return -1;
+    timing_mark_begin(K_BWD_GRAD, st);
+    k<<<dim3(NC, U), 2 * D, smem, st>>>(a, ws, NC);
+    mesa_bwd_lambda_kernel<<<a.H, D, 0, st>>>(a, NC);
+    timing_mark_end(K_BWD_GRAD, st);
+  }
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+template <typename TIO>
+int launch_bwd_d(const BwdArgs &a, const FwdWorkspace &ws, int phase, cudaStream_t st) {
+  switch (a.dk) {
+    case 16: return launch_bwd_t<16, TIO>(a, ws, phase, st);
+    case 32: return launch_bwd_t<32, TIO>(a, ws, phase, st);
+    case 64: return launch_bwd_t<64, TIO>(a, ws, phase, st);
+    case 128: return launch_bwd_t<128, TIO>(a, ws, phase, st);
+  }
+  return -1;
+}
+}  // namespace
+
+int launch_bwd_rhs(const BwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+  return a.dtype == 1 ? launch_bwd_d<__nv_bfloat16>(a, ws, 0, st) : launch_bwd_d<float>(a, ws, 0, st);
+}
+
+int launch_bwd_grads(const BwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+  return a.dtype == 1 ? launch_bwd_d<__nv_bfloat16>(a, ws, 1, st) : launch_bwd_d<float>(a, ws, 1, st);
+}
+
+}  // namespace mesa

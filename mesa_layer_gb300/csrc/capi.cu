@@ -52,6 +52,31 @@ size_t workspace_parts(int B, int H, int T, int dk, int dv, int chunk, size_t *o
   return end;
 }
 
+// Backward workspace: [status | chunk-32 log-decays | S^H | S^G (chunk 32) | 128-token
+// log-decays | S^H (128) | X | Y | b | S^G (128) | segment log-decays Lc | segment carries |
+// dG adjoints | dH adjoints | dlambda partials].  The 128-token parts serve the tensor-core
+// solves (d = 128) and are empty otherwise.
+constexpr int kBwdParts = 15;
+size_t backward_parts(int B, int H, int T, int dk, size_t *off) {
+  const size_t U = (size_t)B * H, C = mesa::kBwdChunk;
+  const size_t NC = (T + C - 1) / C, NC128 = (T + 127) / 128;
+  const bool big = dk == 128;
+  const size_t st = U * NC * dk * dk * sizeof(float), tok = U * T * sizeof(float);
+  const size_t vec = U * T * dk * sizeof(float);
+  const size_t st128 = big ? U * NC128 * dk * dk * sizeof(float) : 0;
+  const size_t nseg = big ? (size_t)mesa::tc_segments((int)U, (int)NC128) : 0;
+  const size_t sizes[kBwdParts - 1] = {
+      tok, st, st,                                       // ell, SH, SG (chunk 32)
+      big ? tok : 0, st128,                              // ell, SH (128)
+      vec, vec, vec,                                     // X, Y, b
+      st128, big ? U * NC128 * sizeof(float) : 0,        // SG (128), Lc
+      U * nseg * 2 * dk * dk * sizeof(float),            // carries
+      st, st, U * NC * dk * sizeof(float)};              // dG, dH, dlambda partials
+  off[0] = kStatusBytes;
+  for (int i = 0; i < kBwdParts - 1; i++) off[i + 1] = off[i] + align256(sizes[i]);
+  return off[kBwdParts - 1];
+}
+
 // The tensor-core path covers bf16 inputs with dk = dv = 128 (16-byte aligned operands).
 bool use_tc(int dtype, int dk, int dv, const void *q, const void *k, const void *v, const void *out,
             const float *H0, const float *G0) {
@@ -147,6 +172,9 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_DELTA_TC: return "mesa_states_tc_kernel";
     case mesa::K_CG_ROWS: return "mesa_cg_rows_kernel";
     case mesa::K_PREPROC: return "mesa_qk_preprocess_kernel";
+    case mesa::K_BWD_RHS: return "mesa_bwd_rhs_kernel";
+    case mesa::K_BWD_STATES: return "mesa_bwd_delta_kernel+mesa_bwd_scan_kernel";
+    case mesa::K_BWD_GRAD: return "mesa_bwd_grad_kernel+mesa_bwd_lambda_kernel";
   }
   return nullptr;
 }
@@ -231,6 +259,80 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
                  : (dk <= 64 ? mesa::launch_chunk_cg_rows(a, ws, stream)
                              : mesa::launch_chunk_cg_simt(a, ws, stream));
   return rc == 0 ? MESA_OK : MESA_ERR_CUDA;
+}
+
+size_t mesa_backward_workspace_size(int B, int H, int T, int dk, int dv) {
+  if (B < 0 || H < 0 || T < 0 || !dim_ok(dk) || dv != dk) return 0;
+  size_t off[kBwdParts];
+  return backward_parts(B, H, T, dk, off);
+}
+
+int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const void *q,
+                          const void *k, const void *v, const float *gamma,
+                          const float *lambda_diag, const void *dout, int cg_iters, float cg_tol,
+                          void *dq, void *dk_out, void *dv_out, float *dgamma, float *dlambda,
+                          int32_t *iters_fwd, int32_t *iters_bwd, void *workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  if (B < 0 || H < 0 || T < 0 || cg_iters < 0 || cg_iters > kMaxIters || isnan(cg_tol))
+    return MESA_ERR_INVALID_ARG;
+  if (dtype != MESA_F32 && dtype != MESA_BF16) return MESA_ERR_INVALID_ARG;
+  if (!dim_ok(dk) || dv != dk) return MESA_ERR_UNSUPPORTED;
+  if ((size_t)B * H > kMaxUnits) return MESA_ERR_UNSUPPORTED;
+  if (H > 0 && !dlambda) return MESA_ERR_INVALID_ARG;
+  const size_t U = (size_t)B * H;
+  if (U == 0 || T == 0) {  // no token: every gradient is zero (dlambda is the only output)
+    if (H > 0 && cudaMemsetAsync(dlambda, 0, sizeof(float) * H * dk, stream) != cudaSuccess)
+      return MESA_ERR_CUDA;
+    return MESA_OK;
+  }
+  if (!q || !k || !v || !gamma || !lambda_diag || !dout || !dq || !dk_out || !dv_out || !dgamma)
+    return MESA_ERR_INVALID_ARG;
+  size_t off[kBwdParts];
+  const size_t need = backward_parts(B, H, T, dk, off);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return MESA_ERR_WORKSPACE;
+  char *w = (char *)workspace;
+  unsigned *status = (unsigned *)w;
+  float *X = (float *)(w + off[5]), *Y = (float *)(w + off[6]), *Bv = (float *)(w + off[7]);
+  // the solves on the tensor cores need 16-byte aligned bf16 operands and d = 128
+  const bool tc = use_tc(dtype, dk, dv, q, k, v, dout, nullptr, nullptr);
+  const int C = mesa::kBwdChunk;
+  // chunk-C states and log-decays: read by the backward kernels, and by the CUDA-core solves
+  mesa::FwdArgs a{B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol, C,
+                  nullptr, iters_fwd, nullptr, nullptr, nullptr, nullptr};
+  mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2]),
+                        nullptr, nullptr, 1};
+  if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
+  if (mesa::launch_chunk_states(a, ws, nullptr, stream) != 0) return MESA_ERR_CUDA;
+  // the tensor-core solves work on 128-token chunks with their own states
+  mesa::FwdArgs a128 = a;
+  a128.chunk = 128;
+  mesa::FwdWorkspace ws128{(float *)(w + off[3]), (float *)(w + off[4]), (float *)(w + off[8]),
+                           (float *)(w + off[9]), (float *)(w + off[10]),
+                           tc ? mesa::tc_segments((int)U, (T + 127) / 128) : 1};
+  if (tc && mesa::launch_chunk_states(a128, ws128, status, stream) != 0) return MESA_ERR_CUDA;
+  auto solve = [&](const float *rhs, float *x_out, int32_t *iters) -> int {
+    mesa::SolveArgs sv;
+    sv.rhs = rhs;
+    sv.x_out = x_out;
+    if (tc) {
+      mesa::FwdArgs b = a128;
+      b.iters = iters;
+      return mesa::launch_chunk_cg_tc(b, ws128, status, stream, sv);
+    }
+    mesa::FwdArgs b = a;
+    b.iters = iters;
+    return dk <= 64 ? mesa::launch_chunk_cg_rows(b, ws, stream, sv)
+                    : mesa::launch_chunk_cg_simt(b, ws, stream, sv);
+  };
+  // x_t (the forward's solves, recomputed), b_t = G_t^T g_t, y_t, then the gradients
+  mesa::BwdArgs ba{B, H, T, dk, dv, dtype, k, v, dout, gamma, X, Y, Bv,
+                   (float *)(w + off[11]), (float *)(w + off[12]), (float *)(w + off[13]),
+                   dq, dk_out, dv_out, dgamma, dlambda};
+  if (solve(nullptr, X, iters_fwd) != 0) return MESA_ERR_CUDA;
+  if (mesa::launch_bwd_rhs(ba, ws, stream) != 0) return MESA_ERR_CUDA;
+  if (solve(Bv, Y, iters_bwd) != 0) return MESA_ERR_CUDA;
+  if (mesa::launch_bwd_grads(ba, ws, stream) != 0) return MESA_ERR_CUDA;
+  return MESA_OK;
 }
 
 int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state, float *G_state,

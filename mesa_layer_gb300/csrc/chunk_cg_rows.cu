@@ -16,8 +16,11 @@
 
 namespace mesa {
 
-template <int D, typename TIO>
-__global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspace ws, int NC) {
+// SOLVE = true: a solve of the backward pass (right-hand sides sv.rhs or q, the iterate to
+// sv.x_out, no readout); false: the forward.
+template <int D, typename TIO, bool SOLVE>
+__global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspace ws, int NC,
+                                                           SolveArgs sv) {
   constexpr int DC = D / 4;  // columns per lane
   const int C = a.chunk, T = a.T;
   const int c = blockIdx.x, u = blockIdx.y;
@@ -101,7 +104,8 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
   float s0 = 0.0f;
 #pragma unroll
   for (int n = 0; n < DC; n++) {
-    const float qv = valid ? ld(q, (tokbase + i) * D + col(n)) : 0.0f;
+    const size_t qi = (tokbase + i) * D + col(n);
+    const float qv = valid ? ((SOLVE && sv.rhs) ? sv.rhs[qi] : ld(q, qi)) : 0.0f;
     p[n] = qv;
     r[n] = qv;
     x[n] = 0.0f;
@@ -209,6 +213,14 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
     }
   }
 
+  if constexpr (SOLVE) {  // the iterate itself, no readout
+    if (valid) {
+#pragma unroll
+      for (int n = 0; n < DC; n++) sv.x_out[(tokbase + i) * D + col(n)] = x[n];
+      if (part == 0 && a.iters) a.iters[tokbase + i] = cnt;
+    }
+    return;
+  }
   // readout o = e^{l_i} S^G x + sum_j D_ij (x . k_j) v_j  (S^G stored transposed)
   float o[DC];
 #pragma unroll
@@ -230,8 +242,9 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
 // the four-lanes-per-row mapping gets; p reaches the lanes through a per-warp buffer in
 // shared memory instead of one shuffle per column.  The state S^H and, after the CG, S^G
 // (transposed) share one padded buffer.
-template <typename TIO>
-__global__ void __launch_bounds__(128, 4) mesa_cg_rows64_kernel(FwdArgs a, FwdWorkspace ws, int NC) {
+template <typename TIO, bool SOLVE>
+__global__ void __launch_bounds__(128, 4) mesa_cg_rows64_kernel(FwdArgs a, FwdWorkspace ws, int NC,
+                                                                SolveArgs sv) {
   constexpr int D = 64, SP = D + 4;
   const int C = a.chunk, T = a.T;
   const int c = blockIdx.x, u = blockIdx.y;
@@ -410,7 +423,7 @@ __global__ void __launch_bounds__(128, 4) mesa_cg_rows64_kernel(FwdArgs a, FwdWo
 #pragma unroll
     for (int n = 0; n < 8; n++) {
       const int cidx = n < 4 ? 4 * o + n : 32 + 4 * o + (n - 4);
-      const float qv = valid[r] ? ld(q, base + cidx) : 0.0f;
+      const float qv = valid[r] ? ((SOLVE && sv.rhs) ? sv.rhs[base + cidx] : ld(q, base + cidx)) : 0.0f;
       p[r][n] = qv;
       rr[r][n] = qv;
       x[r][n] = 0.0f;
@@ -480,6 +493,17 @@ __global__ void __launch_bounds__(128, 4) mesa_cg_rows64_kernel(FwdArgs a, FwdWo
     }
   }
 
+  if constexpr (SOLVE) {  // the iterate itself, no readout
+#pragma unroll
+    for (int r = 0; r < 2; r++) {
+      if (!valid[r]) continue;
+      const size_t base = (tokbase + i0 + r) * D;
+#pragma unroll
+      for (int n = 0; n < 8; n++) sv.x_out[base + (n < 4 ? 4 * o + n : 32 + 4 * o + (n - 4))] = x[r][n];
+      if (o == 0 && a.iters) a.iters[tokbase + i0 + r] = cnt[r];
+    }
+    return;
+  }
   // readout o = e^{l_i} S^G x + sum_j D_ij (x . k_j) v_j, with (S^G)^T in the state buffer
   __syncthreads();  // every warp is done with S^H
   for (int e4 = threadIdx.x; e4 < D * D / 4; e4 += blockDim.x) {
@@ -509,41 +533,46 @@ __global__ void __launch_bounds__(128, 4) mesa_cg_rows64_kernel(FwdArgs a, FwdWo
 }
 
 template <typename TIO>
-static int launch_rows64_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+static int launch_rows64_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st,
+                           const SolveArgs &sv) {
   constexpr int D = 64;
   const int U = a.B * a.H, C = a.chunk;
   const int NC = (a.T + C - 1) / C;
   const int nwarp = (C + 7) / 8;
   const size_t smem = sizeof(float) * (D * (D + 4) + 2 * C * D + nwarp * 8 * D + 2 * C + D);
-  auto kfn = mesa_cg_rows64_kernel<TIO>;
+  if (!a.out && !sv.x_out) return -1;
+  auto kfn = a.out ? mesa_cg_rows64_kernel<TIO, false> : mesa_cg_rows64_kernel<TIO, true>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_ROWS, st);
-  kfn<<<dim3(NC, U), 32 * nwarp, smem, st>>>(a, ws, NC);
+  kfn<<<dim3(NC, U), 32 * nwarp, smem, st>>>(a, ws, NC, sv);
   timing_mark_end(K_CG_ROWS, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 template <int D, typename TIO>
-static int launch_rows_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+static int launch_rows_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st,
+                         const SolveArgs &sv) {
   const int U = a.B * a.H, C = a.chunk;
   const int NC = (a.T + C - 1) / C;
   const size_t smem = sizeof(float) * (2 * D * (D + 4) + 2 * C * D + 2 * C + D);
-  auto kfn = mesa_cg_rows_kernel<D, TIO>;
+  if (!a.out && !sv.x_out) return -1;
+  auto kfn = a.out ? mesa_cg_rows_kernel<D, TIO, false> : mesa_cg_rows_kernel<D, TIO, true>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_ROWS, st);
-  kfn<<<dim3(NC, U), 4 * ((C + 7) / 8) * 8, smem, st>>>(a, ws, NC);
+  kfn<<<dim3(NC, U), 4 * ((C + 7) / 8) * 8, smem, st>>>(a, ws, NC, sv);
   timing_mark_end(K_CG_ROWS, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
-int launch_chunk_cg_rows(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+int launch_chunk_cg_rows(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st,
+                         const SolveArgs &sv) {
   const bool bf = a.dtype == 1;
   switch (a.dk) {
-    case 16: return bf ? launch_rows_t<16, __nv_bfloat16>(a, ws, st) : launch_rows_t<16, float>(a, ws, st);
-    case 32: return bf ? launch_rows_t<32, __nv_bfloat16>(a, ws, st) : launch_rows_t<32, float>(a, ws, st);
-    case 64: return bf ? launch_rows64_t<__nv_bfloat16>(a, ws, st) : launch_rows64_t<float>(a, ws, st);
+    case 16: return bf ? launch_rows_t<16, __nv_bfloat16>(a, ws, st, sv) : launch_rows_t<16, float>(a, ws, st, sv);
+    case 32: return bf ? launch_rows_t<32, __nv_bfloat16>(a, ws, st, sv) : launch_rows_t<32, float>(a, ws, st, sv);
+    case 64: return bf ? launch_rows64_t<__nv_bfloat16>(a, ws, st, sv) : launch_rows64_t<float>(a, ws, st, sv);
   }
   return -1;
 }

@@ -18,9 +18,11 @@
 
 namespace mesa {
 
-template <int D, int R, typename TIO>
+// SOLVE = true: a solve of the backward pass (right-hand sides sv.rhs or q, the iterate to
+// sv.x_out, no readout); false: the forward.
+template <int D, int R, typename TIO, bool SOLVE>
 __global__ void __launch_bounds__(256) mesa_cg_simt_kernel(FwdArgs a, FwdWorkspace ws, int NC,
-                                                           int RB) {
+                                                           int RB, SolveArgs sv) {
   constexpr int RPW = R / 8;                 // rows per warp
   constexpr int DN = D >= 32 ? D / 32 : 1;   // columns per lane (d = lane + 32 n)
   constexpr int SP = D + 1;                  // padded row stride of S and K in smem
@@ -80,7 +82,8 @@ __global__ void __launch_bounds__(256) mesa_cg_simt_kernel(FwdArgs a, FwdWorkspa
 #pragma unroll
     for (int n = 0; n < DN; n++) {
       const int d = lane + 32 * n;
-      const float qv = (valid && d < D) ? ld(q, (tokbase + gi) * D + d) : 0.0f;
+      const size_t qi = (tokbase + gi) * D + d;
+      const float qv = (valid && d < D) ? ((SOLVE && sv.rhs) ? sv.rhs[qi] : ld(q, qi)) : 0.0f;
       X[m][n] = 0.0f;
       Rr[m][n] = qv;
       if (d < D) Ps[i * D + d] = qv;
@@ -218,7 +221,13 @@ __global__ void __launch_bounds__(256) mesa_cg_simt_kernel(FwdArgs a, FwdWorkspa
     for (int n = 0; n < DN; n++)
       if (lane + 32 * n < D) Ps[i * D + lane + 32 * n] = X[m][n];
     if (lane == 0 && r0 + i < Cv && a.iters) a.iters[tokbase + r0 + i] = cnt[m];
+    if (SOLVE && r0 + i < Cv) {
+#pragma unroll
+      for (int n = 0; n < DN; n++)
+        if (lane + 32 * n < D) sv.x_out[(tokbase + r0 + i) * D + lane + 32 * n] = X[m][n];
+    }
   }
+  if constexpr (SOLVE) return;  // no readout
   __syncwarp();
   {
     constexpr int JM = 4;
@@ -303,29 +312,32 @@ __global__ void __launch_bounds__(256) mesa_cg_simt_kernel(FwdArgs a, FwdWorkspa
 }
 
 template <int D, typename TIO>
-static int launch_cg_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+static int launch_cg_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st,
+                       const SolveArgs &sv) {
   constexpr int R = 32;
   const int U = a.B * a.H, C = a.chunk;
   const int NC = (a.T + C - 1) / C;
   const int RB = (C + R - 1) / R;
   const size_t smem = sizeof(float) * ((size_t)D * (D + 1) + (size_t)C * (D + 1) + R * D +
                                        2 * (size_t)R * C + C + R);
-  auto kfn = mesa_cg_simt_kernel<D, R, TIO>;
+  if (!a.out && !sv.x_out) return -1;
+  auto kfn = a.out ? mesa_cg_simt_kernel<D, R, TIO, false> : mesa_cg_simt_kernel<D, R, TIO, true>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_SIMT, st);
-  kfn<<<dim3(NC * RB, U), 256, smem, st>>>(a, ws, NC, RB);
+  kfn<<<dim3(NC * RB, U), 256, smem, st>>>(a, ws, NC, RB, sv);
   timing_mark_end(K_CG_SIMT, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
-int launch_chunk_cg_simt(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+int launch_chunk_cg_simt(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st,
+                         const SolveArgs &sv) {
   const bool bf = a.dtype == 1;
   switch (a.dk) {
-    case 16: return bf ? launch_cg_t<16, __nv_bfloat16>(a, ws, st) : launch_cg_t<16, float>(a, ws, st);
-    case 32: return bf ? launch_cg_t<32, __nv_bfloat16>(a, ws, st) : launch_cg_t<32, float>(a, ws, st);
-    case 64: return bf ? launch_cg_t<64, __nv_bfloat16>(a, ws, st) : launch_cg_t<64, float>(a, ws, st);
-    case 128: return bf ? launch_cg_t<128, __nv_bfloat16>(a, ws, st) : launch_cg_t<128, float>(a, ws, st);
+    case 16: return bf ? launch_cg_t<16, __nv_bfloat16>(a, ws, st, sv) : launch_cg_t<16, float>(a, ws, st, sv);
+    case 32: return bf ? launch_cg_t<32, __nv_bfloat16>(a, ws, st, sv) : launch_cg_t<32, float>(a, ws, st, sv);
+    case 64: return bf ? launch_cg_t<64, __nv_bfloat16>(a, ws, st, sv) : launch_cg_t<64, float>(a, ws, st, sv);
+    case 128: return bf ? launch_cg_t<128, __nv_bfloat16>(a, ws, st, sv) : launch_cg_t<128, float>(a, ws, st, sv);
   }
   return -1;
 }

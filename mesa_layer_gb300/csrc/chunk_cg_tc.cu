@@ -158,9 +158,13 @@ __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, con
 
 }  // namespace
 
-template <int NTERMS>
+// SOLVE = false: the forward (queries q, readout o = G x).  SOLVE = true: a solve of the
+// backward pass: right-hand sides sv.rhs (fp32) or q, the iterate written to sv.x_out, no
+// readout.
+template <int NTERMS, bool SOLVE>
 __global__ void __launch_bounds__(512, 1)
-    mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, int lookahead, unsigned *status) {
+    mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, int lookahead, unsigned *status,
+                      SolveArgs sv) {
   constexpr int NG = 4;           // column groups (threads per token row)
   constexpr int CW = DH / NG;     // columns per thread
   constexpr int NV = CW / 8;      // 8-column vectors per thread
@@ -261,7 +265,7 @@ __global__ void __launch_bounds__(512, 1)
   {
     const uint4 *src = reinterpret_cast<const uint4 *>(q + (tokbase + i) * DH + c0);
 #pragma unroll
-    for (int g = 0; g < NV; g++) qraw[g] = valid ? src[g] : make_uint4(0, 0, 0, 0);
+    for (int g = 0; g < NV; g++) qraw[g] = (valid && !(SOLVE && sv.rhs)) ? src[g] : make_uint4(0, 0, 0, 0);
   }
   tc::Rows8 kr;
   tc::load_rows(k + tokbase * DH, Tv, kr);
@@ -320,11 +324,23 @@ __global__ void __launch_bounds__(512, 1)
   float rho, nq, mP;
   {
     float p[CW];
+    if (SOLVE && sv.rhs) {  // fp32 right-hand sides
+      const float4 *src = reinterpret_cast<const float4 *>(sv.rhs + (tokbase + i) * DH + c0);
 #pragma unroll
-    for (int g = 0; g < NV; g++) {
-      const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&qraw[g]);
+      for (int g4 = 0; g4 < CW / 4; g4++) {
+        const float4 f = valid ? src[g4] : make_float4(0, 0, 0, 0);
+        p[4 * g4] = f.x;
+        p[4 * g4 + 1] = f.y;
+        p[4 * g4 + 2] = f.z;
+        p[4 * g4 + 3] = f.w;
+      }
+    } else {
 #pragma unroll
-      for (int kk = 0; kk < 8; kk++) p[g * 8 + kk] = __bfloat162float(b[kk]);
+      for (int g = 0; g < NV; g++) {
+        const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&qraw[g]);
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) p[g * 8 + kk] = __bfloat162float(b[kk]);
+      }
     }
     float s = 0.0f, mx = 0.0f;
 #pragma unroll
@@ -618,8 +634,18 @@ __global__ void __launch_bounds__(512, 1)
   if (!failed && iters_run > 0) x_update(alpha_prev);
   tc::tmem_st_wait();
 
+  if constexpr (SOLVE) {  // the iterate itself, no readout
+    if (!failed && valid) {
+      float4 *dst = reinterpret_cast<float4 *>(sv.x_out + (tokbase + i) * DH + c0);
+#pragma unroll
+      for (int g4 = 0; g4 < CW / 4; g4++)
+        dst[g4] = *reinterpret_cast<const float4 *>(Xs + x_offset(i, c0 + 4 * g4));
+      if (grp == 0 && a.iters) a.iters[tokbase + i] = cnt;
+    }
+  }
+
   // ---- readout O = e^l X S^G^T + ((X K^T) o D) V ------------------------------------------
-  if (!failed) {
+  if (!SOLVE && !failed) {
     tc::prefetch_l2(v + tokbase * DH, sizeof(__nv_bfloat16) * DH * Tv);  // the value tile
     float xx[CW];
 #pragma unroll
@@ -709,15 +735,17 @@ __global__ void __launch_bounds__(512, 1)
 static_assert(MESA_TC_TERMS == 1 || MESA_TC_TERMS == 2, "1 or 2 fp16 terms");
 
 int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status,
-                       cudaStream_t st) {
+                       cudaStream_t st, const SolveArgs &sv) {
   const int U = a.B * a.H;
   const int NC = (a.T + TILE - 1) / TILE;
-  auto kfn = mesa_cg_tc_kernel<MESA_TC_TERMS>;
+  // a backward-pass solve: no output, the iterate goes to sv.x_out
+  if (!a.out && !sv.x_out) return -1;
+  auto kfn = a.out ? mesa_cg_tc_kernel<MESA_TC_TERMS, false> : mesa_cg_tc_kernel<MESA_TC_TERMS, true>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC) !=
       cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_TC, st);
-  kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(a, ws, NC, sm_count(), status);
+  kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(a, ws, NC, sm_count(), status, sv);
   timing_mark_end(K_CG_TC, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

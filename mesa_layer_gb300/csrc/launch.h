@@ -22,6 +22,15 @@ struct FwdArgs {
   float *H_final, *G_final;
 };
 
+// Solves of the backward pass (a separate kernel argument, so that the forward's argument
+// block is unchanged): rhs != nullptr replaces q by fp32 right-hand sides [U, T, dk];
+// x_out != nullptr receives the fp32 CG iterate [U, T, dk].  With FwdArgs::out == nullptr
+// the CG kernels skip the readout (iters is still written).
+struct SolveArgs {
+  const float *rhs = nullptr;
+  float *x_out = nullptr;
+};
+
 struct DecArgs {
   int N, H, dk, dv, dtype;
   float *Hs, *Gs;
@@ -32,6 +41,21 @@ struct DecArgs {
   float cg_tol;
   void *out;
   int32_t *iters;
+};
+
+// Backward pass (chunks of kBwdChunk tokens; the states, log-decays and solves come from the
+// forward pipeline run at that chunk length).
+constexpr int kBwdChunk = 32;
+struct BwdArgs {
+  int B, H, T, dk, dv, dtype;
+  const void *k, *v, *dout;          // dout = dL/do [U, T, dv]
+  const float *gamma;
+  const float *X, *Y;                // the two solves [U, T, dk] (x_t and y_t)
+  float *rhs;                        // [U, T, dk] right-hand sides b_t = G_t^T g_t (written)
+  float *dGs, *dHs;                  // [U, NC, dv|dk, dk] state adjoints after each chunk
+  float *dlam_part;                  // [U, NC, dk]
+  void *dq_out, *dk_out, *dv_out;    // dtype
+  float *dgamma, *dlambda;           // [U, T], [H, dk]
 };
 
 // Query/key preprocessing (causal depthwise convolution + L2 normalisation).
@@ -46,7 +70,7 @@ struct PreArgs {
 // Kernel kinds, for the optional per-kernel timing of benchmarks (mesa_timing_*).
 enum KernelKind {
   K_ELL = 0, K_DELTA = 1, K_SCAN = 2, K_CG_SIMT = 3, K_DECODE = 4, K_CG_TC = 5, K_DELTA_TC = 6, K_CG_ROWS = 7,
-  K_PREPROC = 8, K_NUM_KINDS = 9
+  K_PREPROC = 8, K_BWD_RHS = 9, K_BWD_STATES = 10, K_BWD_GRAD = 11, K_NUM_KINDS = 12
 };
 
 // Record a timing event before / after a launch of `kind` on `st` (no-op unless enabled).
@@ -57,18 +81,25 @@ void timing_mark_end(int kind, cudaStream_t st);
 // tc_status != nullptr selects the tensor-core chunk sums (bf16, d = 128, chunk = 128).
 int launch_chunk_states(const FwdArgs &a, const FwdWorkspace &ws, unsigned *tc_status,
                         cudaStream_t st);
-int launch_chunk_cg_simt(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
+int launch_chunk_cg_simt(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st,
+                         const SolveArgs &sv = SolveArgs());
 // fp32 path for dk = dv <= 64: four lanes per token row, no barrier in the CG loop.
-int launch_chunk_cg_rows(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
+int launch_chunk_cg_rows(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st,
+                         const SolveArgs &sv = SolveArgs());
 // Tensor-core path: bf16 q/k/v, dk = dv = 128, 128-token chunks (states and log-decays
 // must have been built with chunk = 128).  Bounded-wait failures set bits in *status.
-int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st);
+int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st,
+                       const SolveArgs &sv = SolveArgs());
 int launch_tc_selftest(const float *A, const float *B, float *C1, float *C2, float *C3,
                        unsigned *status, cudaStream_t st);
 // Chunk-boundary states on the tensor cores (bf16 inputs, d = 128, 128-token chunks):
 // segment-local states, segment carries and the final state (see FwdWorkspace).
 int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st);
 int launch_decode(const DecArgs &a, cudaStream_t st);
+// Backward pass: the right-hand sides of the second solve (needs ws's chunk-kBwdChunk states
+// and log-decays), then the state adjoints and every gradient.
+int launch_bwd_rhs(const BwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
+int launch_bwd_grads(const BwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
 // step == false: whole sequences [U, T, d]; step == true: one decode step [U, d].
 int launch_qk_preprocess(const PreArgs &a, bool step, cudaStream_t st);
 

@@ -1,7 +1,7 @@
 """Seeded synthetic inputs for the Mesa layer workloads.
 
 This module only draws random numbers and shapes them into the input distributions of the
-five workloads; it holds none of the layer's arithmetic.  Both the CUDA path's tests and
+workloads; it holds none of the layer's arithmetic.  Both the CUDA path's tests and
 benchmark and the CPU oracle take their inputs from here.
 
 Recipe (every workload, seed 0 unless stated):
@@ -21,7 +21,8 @@ from dataclasses import dataclass, replace
 
 import numpy as np
 
-_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "gamma": 4, "lam": 5, "q_raw": 6, "k_raw": 7, "wq": 8, "wk": 9}
+_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "gamma": 4, "lam": 5, "q_raw": 6, "k_raw": 7, "wq": 8, "wk": 9,
+               "dout": 10}
 
 
 @dataclass(frozen=True)
@@ -46,6 +47,7 @@ class Workload:
     prefix: int = 0            # decode: tokens folded into the state before the steps
     conv_taps: int = 0         # > 0: query/key preprocessing workload with this window
     warm: bool = False         # decode: each step's CG starts from the previous solution
+    backward: bool = False     # the backward pass (gradients given dL/dout)
 
     @property
     def tokens(self) -> int:
@@ -75,6 +77,9 @@ WORKLOADS = {
         # the decode workload with warm-started CG (inputs drawn as for decode_bf16_d128)
         Workload("decode_warm_bf16_d128", 5, "bf16", 256, 16, 1, 128, 128, 64, 30, 1e-3,
                  "sigmoid", 4.0, 1.0, 0.05, 0.5, decode_steps=512, prefix=1024, warm=True),
+        # the backward pass on the shape and distributions of fwd_bf16_d128
+        Workload("bwd_bf16_d128", 7, "bf16", 8, 16, 4096, 128, 128, 64, 15, 0.0,
+                 "sigmoid", 4.0, 1.0, 0.05, 0.5, backward=True),
     ]
 }
 WORKLOAD_ORDER = [w.name for w in sorted(WORKLOADS.values(), key=lambda w: w.wid)]
@@ -138,6 +143,15 @@ def forward_inputs(w: Workload, seed: int = 0) -> dict:
         "gamma": _gamma(w, _rng(seed, w.wid, "gamma"), (B, H, T)),
         "lam": lambdas(w, seed),
     }
+
+
+def backward_inputs(w: Workload, seed: int = 0) -> dict:
+    """forward_inputs plus dout [B, H, T, dv] ~ N(0, 1) (the incoming gradient dL/dout),
+    rounded to the workload dtype."""
+    inp = forward_inputs(w, seed)
+    shape = (w.B, w.H, w.T, w.dv)
+    inp["dout"] = _cast(w, _rng(seed, w.wid, "dout").standard_normal(size=shape, dtype=np.float32))
+    return inp
 
 
 def decode_inputs(w: Workload, step: int, seed: int = 0) -> dict:

@@ -152,3 +152,33 @@ def test_decode_step_warm_validation(lib):
     assert call(dk=48, dv=48) == 2
     assert call(it=-1) == 1
     assert call(N=0) == 0
+
+
+def test_backward_workspace_and_validation(lib):
+    ws = lib.mesa_backward_workspace_size
+    assert ws(2, 3, 100, 48, 48) == 0          # unsupported d
+    assert ws(2, 3, 100, 64, 32) == 0          # dk != dv
+    small, big = ws(2, 3, 100, 64, 64), ws(2, 3, 1000, 64, 64)
+    assert 0 < small < big
+    # d = 128 also holds the 128-token states of the tensor-core solves
+    assert ws(1, 1, 256, 128, 128) > 2 * ws(1, 1, 256, 64, 64)
+    f = lib.mesa_backward_chunked  # argument types set by the binding
+    p = ctypes.c_void_p(256)
+
+    def call(**kw):
+        a = dict(B=2, H=2, T=64, dk=64, dv=64, dt=1, q=p, k=p, v=p, g=p, lam=p, do=p, it=5, tol=0.0, dq=p,
+                 dk_=p, dv_=p, dg=p, dl=p, itf=None, itb=None, ws=p, wsz=1 << 40, st=None)
+        a.update(kw)
+        return f(a["B"], a["H"], a["T"], a["dk"], a["dv"], a["dt"], a["q"], a["k"], a["v"], a["g"], a["lam"],
+                 a["do"], a["it"], a["tol"], a["dq"], a["dk_"], a["dv_"], a["dg"], a["dl"], a["itf"], a["itb"],
+                 a["ws"], a["wsz"], a["st"])
+    assert call(dk=48, dv=48) == 2
+    assert call(dv=32) == 2
+    assert call(it=-1) == 1
+    assert call(dt=7) == 1
+    assert call(do=None) == 1
+    assert call(dl=None) == 1
+    assert call(dg=None) == 1
+    assert call(wsz=1000) == 3                 # workspace too small
+    assert call(ws=ctypes.c_void_p(264)) == 3  # workspace not 256-byte aligned
+    assert call(B=0, H=0) == 0                 # nothing to do, nothing launched

@@ -1,0 +1,165 @@
+"""GPU parity of the backward pass (mesa_backward_chunked through the C ABI) against the fp64
+oracle's backward: every d, both dtypes, ragged chunks, sequences spanning several chunks of
+both chunk lengths (32 for the CUDA-core kernels, 128 for the tensor-core solves), a zero
+incoming gradient, closed gates, dynamic mode, and the benchmark's workload at full size on
+sampled (batch, head) units.
+
+Metric: per (batch, head) unit, max |grad_gpu - grad_ref| / max |grad_ref| for dq, dk, dv and
+dgamma; per head for dlambda (summed over the batch).  Tolerances as the forward's: 1e-4 for
+fp32 inputs, 2e-2 for bf16 inputs (whose gradients are rounded to bf16 on output)."""
+import numpy as np
+import pytest
+
+import oracle
+from mesa_layer_gb300 import synth
+from helpers import TOL, unit_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from mesa_layer_gb300 import binding, build
+    build.build()
+    binding.load()
+
+
+def _wl(dtype, **kw):
+    """Small cases: fp32 inputs take the fp32 workload's distributions (its Lambda range; the
+    bf16 workload's smaller Lambda makes 15 un-converged fp32 CG steps conditioning-limited
+    above 1e-4, on the CPU in plain fp32 as on the GPU), bf16 inputs the backward workload's."""
+    if dtype == "f32":
+        return synth.workload("fwd_fp32_d64", cg_tol=0.0, **kw)
+    return synth.workload("bwd_bf16_d128", **kw)
+
+
+def _gpu(inp, dtype, iters, tol):
+    import torch
+
+    from mesa_layer_gb300 import binding
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    t = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).cuda().to(td if k in ("q", "k", "v", "dout")
+                                                                     else torch.float32).contiguous()
+         for k in ("q", "k", "v", "gamma", "lam", "dout")}
+    B, H, T, dk = t["q"].shape
+    ws = torch.empty(max(256, binding.mesa_backward_workspace_size(B, H, T, dk, dk)), dtype=torch.uint8,
+                     device="cuda")
+    dq, dk_, dv, dg, dl, itf, itb = binding.mesa_backward_chunked(t["q"], t["k"], t["v"], t["gamma"], t["lam"],
+                                                                 t["dout"], iters, tol, workspace=ws)
+    torch.cuda.synchronize()
+    assert binding.mesa_forward_status(ws) == 0, "a kernel reported a bounded-wait timeout"
+    f = lambda x: x.float().cpu().numpy().astype(np.float64)
+    return {"dq": f(dq), "dk": f(dk_), "dv": f(dv), "dgamma": f(dg), "dlam": f(dl),
+            "iters_fwd": itf.cpu().numpy(), "iters_bwd": itb.cpu().numpy()}
+
+
+def _errs(g, r, mask=None):
+    """Per-quantity max over units of the unit metric (dgamma as a one-feature sequence)."""
+    e = {k: float(unit_err(g[k], r[k], mask).max()) for k in ("dq", "dk", "dv")}
+    e["dgamma"] = float(unit_err(g["dgamma"][..., None], r["dgamma"][..., None], mask).max())
+    e["dlam"] = float((np.abs(g["dlam"] - r["dlam"]).max(axis=-1) / np.abs(r["dlam"]).max(axis=-1)).max())
+    return e
+
+
+def _check(g, r, dtype, label, mask=None, counts=True):
+    e = _errs(g, r, mask)
+    print(f"{label}: " + ", ".join(f"{k} {v:.2e}" for k, v in e.items()))
+    if counts:
+        assert np.array_equal(g["iters_fwd"], r["iters_fwd"]) and np.array_equal(g["iters_bwd"], r["iters_bwd"])
+    for k, v in e.items():
+        assert v <= TOL[dtype], f"{label}: {k} {v:.3e}"
+    return e
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+def test_against_oracle_fixed(dtype, d):
+    """75 tokens: two full 32-token chunks and a ragged one (one ragged 128-token chunk)."""
+    w = _wl(dtype, B=2, H=2, T=75, dk=d, dv=d)
+    inp = synth.backward_inputs(w, seed=d)
+    g = _gpu(inp, dtype, 6, 0.0)
+    r = oracle.backward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], inp["dout"], 6)
+    _check(g, r, dtype, f"bwd d={d} {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_several_chunks_d128(dtype):
+    """300 tokens at d = 128: three 128-token chunks (tensor-core solves for bf16) and ten
+    32-token chunks, the workload's 15 iterations."""
+    w = _wl(dtype, B=1, H=3, T=300, dk=128, dv=128)
+    inp = synth.backward_inputs(w, seed=5)
+    g = _gpu(inp, dtype, 15, 0.0)
+    r = oracle.backward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], inp["dout"], 15)
+    _check(g, r, dtype, f"bwd T=300 {dtype}")
+
+
+def test_single_token_and_zero_gradient():
+    w = _wl("f32", B=2, H=2, T=1, dk=32, dv=32)
+    inp = synth.backward_inputs(w, seed=1)
+    g = _gpu(inp, "f32", 8, 0.0)
+    r = oracle.backward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], inp["dout"], 8)
+    _check(g, r, "f32", "bwd T=1")
+    assert np.all(g["dgamma"] == 0.0)  # no earlier state
+    w = _wl("f32", B=1, H=2, T=40, dk=64, dv=64)
+    inp = synth.backward_inputs(w, seed=2)
+    inp["dout"][:] = 0.0
+    g = _gpu(inp, "f32", 8, 1e-4)
+    for k in ("dq", "dk", "dv", "dgamma", "dlam"):
+        assert np.all(g[k] == 0.0), k
+    assert np.all(g["iters_bwd"] == 0)
+
+
+def test_closed_gates():
+    """Gates of exactly 0 cut the sequence: the GPU gives them a zero gate gradient (the
+    forward clamps the log-gate there); every other gradient matches the oracle."""
+    w = _wl("f32", B=1, H=2, T=70, dk=32, dv=32)
+    inp = synth.backward_inputs(w, seed=3)
+    inp["gamma"][:, :, [5, 33, 64]] = 0.0
+    g = _gpu(inp, "f32", 8, 0.0)
+    r = oracle.backward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], inp["dout"], 8)
+    open_gate = inp["gamma"] > 0
+    _check(g, r, "f32", "bwd closed gates", mask=open_gate)
+    assert np.all(g["dgamma"][~open_gate] == 0.0)
+
+
+def test_dynamic_mode():
+    """Dynamic stopping (tol 1e-3, cap 30): counts may differ at the threshold; the units whose
+    counts all agree must meet the tolerance, and at least 95 % of the counts agree."""
+    w = _wl("f32", B=2, H=2, T=96, dk=64, dv=64)
+    inp = synth.backward_inputs(w, seed=4)
+    g = _gpu(inp, "f32", 30, 1e-3)
+    r = oracle.backward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], inp["dout"], 30, 1e-3)
+    agree = (g["iters_fwd"] == r["iters_fwd"]) & (g["iters_bwd"] == r["iters_bwd"])
+    print(f"bwd dynamic: counts agree {agree.mean():.4f}, mean iters fwd {g['iters_fwd'].mean():.2f} "
+          f"bwd {g['iters_bwd'].mean():.2f}")
+    assert agree.mean() >= 0.95
+    units = agree.all(axis=-1)
+    for b, h in zip(*np.nonzero(units)):
+        e = {k: float(unit_err(g[k][b, h], r[k][b, h])) for k in ("dq", "dk", "dv")}
+        e["dgamma"] = float(unit_err(g["dgamma"][b, h][:, None], r["dgamma"][b, h][:, None]))
+        for k, v in e.items():
+            assert v <= TOL["f32"], f"unit ({b}, {h}) {k} {v:.3e}"
+
+
+def test_full_workload_sampled_units():
+    """The benchmark's backward workload (B=8 H=16 T=4096 d=128 bf16, 15 iterations), all
+    units on the GPU; the oracle follows three (batch, head) units (dlambda, a sum over the
+    batch, is covered by the small cases)."""
+    w = synth.workload("bwd_bf16_d128")
+    inp = synth.backward_inputs(w)
+    g = _gpu(inp, w.dtype, w.cg_iters, w.cg_tol)
+    assert np.all(g["iters_fwd"] == w.cg_iters) and np.all(g["iters_bwd"] == w.cg_iters)
+    units = ((0, 0), (3, 7), (7, 15))
+    bs, hs = [u[0] for u in units], [u[1] for u in units]
+    # the sampled units side by side as three heads of one sequence batch (each its own lambda)
+    sub = {k: inp[k][bs, hs][None] for k in ("q", "k", "v", "gamma", "dout")}
+    r = oracle.backward(sub["q"], sub["k"], sub["v"], sub["gamma"], inp["lam"][hs], sub["dout"],
+                        w.cg_iters, w.cg_tol)
+    for n, (b, h) in enumerate(units):
+        e = {k: float(unit_err(g[k][b, h], r[k][0, n])) for k in ("dq", "dk", "dv")}
+        e["dgamma"] = float(unit_err(g["dgamma"][b, h][:, None], r["dgamma"][0, n][:, None]))
+        print(f"bwd full b={b} h={h}: " + ", ".join(f"{k} {v:.2e}" for k, v in e.items()))
+        for k, v in e.items():
+            assert v <= TOL[w.dtype], f"({b}, {h}) {k} {v:.3e}"
