@@ -124,6 +124,7 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
  *   iters_fwd, iters_bwd  [B, H, T] int32 or NULL: iterations of the x and y solves
  *   workspace  device scratch of at least mesa_backward_workspace_size() bytes, 256-byte
  *              aligned; its first word is the status word read by mesa_forward_status.
+ * q, k, v, dout, dq, dk_out and dv_out must be 16-byte aligned (MESA_ERR_INVALID_ARG).
  * Sizes, errors and stream semantics as mesa_forward_chunked; the work is chunked in
  * 32-token chunks (128 for the tensor-core solves: bf16, d = 128, 16-byte aligned).
  */

@@ -287,6 +287,9 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
   }
   if (!q || !k || !v || !gamma || !lambda_diag || !dout || !dq || !dk_out || !dv_out || !dgamma)
     return MESA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
+      !aligned(dk_out, 16) || !aligned(dv_out, 16))
+    return MESA_ERR_INVALID_ARG;
   size_t off[kBwdParts];
   const size_t need = backward_parts(B, H, T, dk, off);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return MESA_ERR_WORKSPACE;

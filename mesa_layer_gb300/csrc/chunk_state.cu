@@ -45,16 +45,17 @@ __global__ void __launch_bounds__(256) mesa_delta_kernel(const TIO *__restrict__
                                                          const float *__restrict__ ell,
                                                          FwdWorkspace ws, int T, int C) {
   constexpr int TM = D / 16;
-  extern __shared__ float smem[];
+  extern __shared__ __align__(16) float smem[];
   float *Xs = smem;              // [C, D] rows x_j (k or v)
-  float *Ks = smem + 128 * D;    // [C, D] rows k_j
-  float *wv = smem + 256 * D;    // [C]
+  float *Ks = smem + C * D;      // [C, D] rows k_j
+  float *wv = smem + 2 * C * D;  // [C]
   const int c = blockIdx.x, u = blockIdx.y, isG = blockIdx.z;
   const int NC = gridDim.x;
   const int t0 = c * C;
   const int Cv = min(C, T - t0);
   const size_t base = ((size_t)u * T + t0) * D;
   const TIO *X = isG ? v : k;
+#pragma unroll 4
   for (int e = threadIdx.x; e < Cv * D; e += blockDim.x) {
     Ks[e] = ld(k, base + e);
     Xs[e] = ld(X, base + e);
@@ -64,28 +65,8 @@ __global__ void __launch_bounds__(256) mesa_delta_kernel(const TIO *__restrict__
     wv[j] = expf(lend - ell[(size_t)u * T + t0 + j]);
   __syncthreads();
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[TM][TM];
-#pragma unroll
-  for (int m = 0; m < TM; m++)
-#pragma unroll
-    for (int n = 0; n < TM; n++) acc[m][n] = 0.0f;
-  for (int j = 0; j < Cv; j++) {
-    const float wj = wv[j];
-    float xa[TM], kb[TM];
-#pragma unroll
-    for (int m = 0; m < TM; m++) xa[m] = Xs[j * D + ty + 16 * m] * wj;
-#pragma unroll
-    for (int n = 0; n < TM; n++) kb[n] = Ks[j * D + tx + 16 * n];
-#pragma unroll
-    for (int m = 0; m < TM; m++)
-#pragma unroll
-      for (int n = 0; n < TM; n++) acc[m][n] = fmaf(xa[m], kb[n], acc[m][n]);
-  }
   float *S = (isG ? ws.SG : ws.SH) + ((size_t)u * NC + c) * D * D;
-#pragma unroll
-  for (int m = 0; m < TM; m++)
-#pragma unroll
-    for (int n = 0; n < TM; n++) S[(ty + 16 * m) * D + tx + 16 * n] = acc[m][n];
+  outer_sum<D>(Xs, Ks, wv, Cv, tx, ty, S);
 }
 
 // grid (ceil(2 D^2 / 256), U), block 256.  Entry e < D^2 belongs to S^H, else to S^G.
@@ -139,7 +120,7 @@ static int launch_states_t(const FwdArgs &a, const FwdWorkspace &ws, unsigned *t
   if (tc_status) {  // chunk sums and the chunk-level scan on the tensor cores
     return launch_states_tc(a, ws, tc_status, st);
   } else {
-    const size_t smem = (size_t)(256 * D + 128) * sizeof(float);
+    const size_t smem = (size_t)(2 * a.chunk * D + a.chunk) * sizeof(float);
     auto kd = mesa_delta_kernel<D, TIO>;
     if (cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)

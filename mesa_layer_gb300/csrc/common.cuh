@@ -32,10 +32,90 @@ __device__ __forceinline__ void st<__nv_bfloat16>(__nv_bfloat16 *p, size_t i, fl
   p[i] = __float2bfloat16_rn(x);
 }
 
+// Four consecutive elements as fp32 (p + i 16-byte aligned for float, 8-byte for bf16).
+template <typename T>
+__device__ __forceinline__ float4 load4(const T *p, size_t i);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float *p, size_t i) {
+  return *reinterpret_cast<const float4 *>(p + i);
+}
+template <>
+__device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p, size_t i) {
+  const uint2 raw = *reinterpret_cast<const uint2 *>(p + i);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
+}
+
+// S[a][b] = sum_{j < n} w_j L[j][a] R[j][b] for D x D, L and R [n][D] in shared memory; 256
+// threads (tx, ty) of 16 x 16, each a (D/16) x (D/16) register tile.  For D >= 64 the tile
+// is made of 4 x 4 blocks (rows 64 g + 4 ty + r, columns 64 h + 4 tx + s) read and written
+// as float4; below, rows ty + 16 m and columns tx + 16 n.  Every entry is the same FMA chain
+// over j in both layouts.
+template <int D>
+__device__ __forceinline__ void outer_sum(const float *L, const float *R, const float *w, int n,
+                                          int tx, int ty, float *S) {
+  constexpr int TM = D / 16;
+  float acc[TM][TM];
+#pragma unroll
+  for (int m = 0; m < TM; m++)
+#pragma unroll
+    for (int q = 0; q < TM; q++) acc[m][q] = 0.0f;
+  if constexpr (D >= 64) {
+    constexpr int G = TM / 4;
+    for (int j = 0; j < n; j++) {
+      const float wj = w[j];
+      float la[TM], rb[TM];
+#pragma unroll
+      for (int g = 0; g < G; g++) {
+        const float4 l4 = *reinterpret_cast<const float4 *>(L + j * D + 64 * g + 4 * ty);
+        const float4 r4 = *reinterpret_cast<const float4 *>(R + j * D + 64 * g + 4 * tx);
+        la[4 * g] = l4.x * wj;
+        la[4 * g + 1] = l4.y * wj;
+        la[4 * g + 2] = l4.z * wj;
+        la[4 * g + 3] = l4.w * wj;
+        rb[4 * g] = r4.x;
+        rb[4 * g + 1] = r4.y;
+        rb[4 * g + 2] = r4.z;
+        rb[4 * g + 3] = r4.w;
+      }
+#pragma unroll
+      for (int m = 0; m < TM; m++)
+#pragma unroll
+        for (int q = 0; q < TM; q++) acc[m][q] = fmaf(la[m], rb[q], acc[m][q]);
+    }
+#pragma unroll
+    for (int m = 0; m < TM; m++) {
+      const int row = 64 * (m / 4) + 4 * ty + (m % 4);
+#pragma unroll
+      for (int h = 0; h < G; h++)
+        *reinterpret_cast<float4 *>(S + row * D + 64 * h + 4 * tx) =
+            make_float4(acc[m][4 * h], acc[m][4 * h + 1], acc[m][4 * h + 2], acc[m][4 * h + 3]);
+    }
+  } else {
+    for (int j = 0; j < n; j++) {
+      const float wj = w[j];
+      float la[TM], rb[TM];
+#pragma unroll
+      for (int m = 0; m < TM; m++) la[m] = L[j * D + ty + 16 * m] * wj;
+#pragma unroll
+      for (int q = 0; q < TM; q++) rb[q] = R[j * D + tx + 16 * q];
+#pragma unroll
+      for (int m = 0; m < TM; m++)
+#pragma unroll
+        for (int q = 0; q < TM; q++) acc[m][q] = fmaf(la[m], rb[q], acc[m][q]);
+    }
+#pragma unroll
+    for (int m = 0; m < TM; m++)
+#pragma unroll
+      for (int q = 0; q < TM; q++) S[(ty + 16 * m) * D + tx + 16 * q] = acc[m][q];
+  }
 }
 
 // Workspace carve-up of the chunked forward (all fp32, each section 256-byte aligned).

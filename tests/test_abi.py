@@ -182,3 +182,5 @@ def test_backward_workspace_and_validation(lib):
     assert call(wsz=1000) == 3                 # workspace too small
     assert call(ws=ctypes.c_void_p(264)) == 3  # workspace not 256-byte aligned
     assert call(B=0, H=0) == 0                 # nothing to do, nothing launched
+    assert call(q=ctypes.c_void_p(264)) == 1   # operands must be 16-byte aligned
+    assert call(dv_=ctypes.c_void_p(264)) == 1
