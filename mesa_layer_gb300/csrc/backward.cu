@@ -257,6 +257,51 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
   const int rg = tid / NQ, c4 = tid % NQ;
   const bool last = c == NC - 1, first = c == 0;
 
+  constexpr int NR = D / 8;  // float4 of a D x D state per thread (2D threads)
+  const float *dGp = a.dGs + ((size_t)u * NC + c) * D * D, *dHp = a.dHs + ((size_t)u * NC + c) * D * D;
+  const float *SGp = first ? nullptr : ws.SG + ((size_t)u * NC + c - 1) * D * D;
+  const float *SHp = first ? nullptr : ws.SH + ((size_t)u * NC + c - 1) * D * D;
+  int kinds[6], ns = 0;
+  if (!last) { kinds[ns++] = 1; kinds[ns++] = 2; }
+  if (!first) kinds[ns++] = 3;
+  if (!last) kinds[ns++] = 4;
+  if (!first) kinds[ns++] = 5;
+  if (!last) kinds[ns++] = 6;
+  auto src = [&](int kind) { return kind <= 2 ? dGp : kind == 3 ? SGp : kind == 5 ? SHp : dHp; };
+  auto transposed = [](int kind) { return kind == 1 || kind == 6; };
+  float4 R[NR];
+  auto pos = [&](int q, bool tr, int &r, int &cc) {
+    const int e4 = tid + q * nt;
+    r = tr ? e4 % D : (4 * e4) / D;
+    cc = tr ? 4 * (e4 / D) : (4 * e4) % D;
+  };
+  auto fetch = [&](int kind) {
+    const float *S = src(kind);
+    const bool tr = transposed(kind);
+#pragma unroll
+    for (int q = 0; q < NR; q++) {
+      int r, cc;
+      pos(q, tr, r, cc);
+      R[q] = *reinterpret_cast<const float4 *>(S + r * D + cc);
+    }
+  };
+  auto commit = [&](int kind) {
+    const bool tr = transposed(kind);
+#pragma unroll
+    for (int q = 0; q < NR; q++) {
+      int r, cc;
+      pos(q, tr, r, cc);
+      if (tr) {
+        St[(cc + 0) * SPD + r] = R[q].x;
+        St[(cc + 1) * SPD + r] = R[q].y;
+        St[(cc + 2) * SPD + r] = R[q].z;
+        St[(cc + 3) * SPD + r] = R[q].w;
+      } else {
+        *reinterpret_cast<float4 *>(St + r * SPD + cc) = R[q];
+      }
+    }
+  };
+  if (ns > 0) fetch(kinds[0]);  // in flight while the tiles load and the intra-chunk parts run
   load_tile<D>(Ks, (const TIO *)a.k + tokbase * D, Cv);
   load_tile<D>(Vs, (const TIO *)a.v + tokbase * D, Cv);
   load_tile<D>(Gs, (const TIO *)a.dout + tokbase * D, Cv);
@@ -266,22 +311,48 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
   __syncthreads();
   const float lend = el[Cv - 1];
   for (int j = tid; j < BC; j += nt) wv[j] = j < Cv ? expf(lend - el[j]) : 0.0f;
-  for (int e = tid; e < BC * BC; e += nt) {
-    const int i = e / BC, j = e % BC;
-    float m1 = 0.0f, m2 = 0.0f, m3 = 0.0f, cm = 0.0f;
-    if (j <= i && i < Cv) {
-      const float dd = expf(el[i] - el[j]);
-      const float p1 = row_dot<D>(Gs, i, Vs, j), p2 = row_dot<D>(Xs, i, Ks, j),
-                  p3 = row_dot<D>(Ys, i, Ks, j);
-      m1 = dd * p1;
-      m2 = dd * p2;
-      m3 = dd * p3;
-      cm = m2 * (p1 - p3);
+  // the C x C blocks G V^T, X K^T, Y K^T in 2 x 2 register tiles (rows ti, ti + 16, columns
+  // tj, tj + 16): 10 float4 shared-memory loads per 48 FMAs
+  constexpr int HB = BC / 2;
+  for (int tile = tid; tile < HB * HB; tile += nt) {
+    const int ti = tile / HB, tj = tile % HB;
+    float p1[2][2] = {{0, 0}, {0, 0}}, p2[2][2] = {{0, 0}, {0, 0}}, p3[2][2] = {{0, 0}, {0, 0}};
+    auto dot4 = [](float4 x, float4 y, float acc) {
+      return fmaf(x.w, y.w, fmaf(x.z, y.z, fmaf(x.y, y.y, fmaf(x.x, y.x, acc))));
+    };
+#pragma unroll 2
+    for (int e = 0; e < D; e += 4) {
+      float4 g[2], x[2], y[2], vv[2], kk[2];
+#pragma unroll
+      for (int r = 0; r < 2; r++) {
+        const int i = ti + HB * r, j = tj + HB * r;
+        g[r] = *reinterpret_cast<const float4 *>(Gs + i * SPD + e);
+        x[r] = *reinterpret_cast<const float4 *>(Xs + i * SPD + e);
+        y[r] = *reinterpret_cast<const float4 *>(Ys + i * SPD + e);
+        vv[r] = *reinterpret_cast<const float4 *>(Vs + j * SPD + e);
+        kk[r] = *reinterpret_cast<const float4 *>(Ks + j * SPD + e);
+      }
+#pragma unroll
+      for (int r = 0; r < 2; r++)
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+          p1[r][q] = dot4(g[r], vv[q], p1[r][q]);
+          p2[r][q] = dot4(x[r], kk[q], p2[r][q]);
+          p3[r][q] = dot4(y[r], kk[q], p3[r][q]);
+        }
     }
-    M1[i * SPC + j] = m1;
-    M2[i * SPC + j] = m2;
-    M3[i * SPC + j] = m3;
-    Cm[i * SPC + j] = cm;
+#pragma unroll
+    for (int r = 0; r < 2; r++)
+#pragma unroll
+      for (int q = 0; q < 2; q++) {
+        const int i = ti + HB * r, j = tj + HB * q;
+        const bool in = j <= i && i < Cv;
+        const float dd = in ? expf(el[i] - el[j]) : 0.0f;
+        M1[i * SPC + j] = dd * p1[r][q];
+        M2[i * SPC + j] = dd * p2[r][q];
+        M3[i * SPC + j] = dd * p3[r][q];
+        Cm[i * SPC + j] = dd * p2[r][q] * (p1[r][q] - p3[r][q]);
+      }
   }
   __syncthreads();
 
@@ -299,100 +370,79 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
 #pragma unroll
     for (int n = 0; n < 4; n++) accK[m][n] -= t[m][n];
 
-  // per-row sums of this thread's 4 columns of t . Z (Z a tile), finished over the row
-  auto row_partial = [&](const float *Z) {
+  // The chunk states pass through St one at a time; the next one is loaded into registers
+  // while the product with the current one runs (one CTA per SM: nothing else hides the
+  // latency).  Kinds, with t the C x D product and rows s (or t) of the chunk:
+  //   1 dG^T: t = K dG^T, rows (dG k_s)^T      dv += w t,  col += t . v_s
+  //   2 dG  : t = V dG,   rows (dG^T v_s)^T    dk += w t
+  //   3 S^G : t = G S^G,  rows (S^G^T g_t)^T   row += t . x_t
+  //   4 dH  : t = K dH,   rows (dH^T k_s)^T    dk += w t
+  //   5 S^H : t = X S^H,  rows (S^H x_t)^T     row -= t . y_t      (S^H symmetric)
+  //   6 dH^T: t = K dH^T, rows (dH k_s)^T      dk += w t,  col += t . k_s
+  // The adjoints dG^c, dH^c are zero after the last chunk and the states S_{c-1} before the
+  // first: those kinds are skipped.  While St holds dG (dH) and the registers S^G (S^H),
+  // their Frobenius product, the pairs across the whole chunk, is taken on the way.
+  float colp[4] = {0, 0, 0, 0}, rowp[4] = {0, 0, 0, 0}, thr = 0.0f;
+  auto dot_rows = [&](float (&acc)[4], const float *Z, float sign) {
 #pragma unroll
     for (int m = 0; m < 4; m++) {
-      const int r = rg + 8 * m;
-      const float4 z = *reinterpret_cast<const float4 *>(Z + r * SPD + 4 * c4);
-      part[r * (NQ + 1) + c4] = t[m][0] * z.x + t[m][1] * z.y + t[m][2] * z.z + t[m][3] * z.w;
+      const float4 z = *reinterpret_cast<const float4 *>(Z + (rg + 8 * m) * SPD + 4 * c4);
+      acc[m] += sign * (t[m][0] * z.x + t[m][1] * z.y + t[m][2] * z.z + t[m][3] * z.w);
     }
   };
-  auto row_finish = [&](float *dst, bool add) {  // dst[r] (+)= sum of the row's partials
-    for (int r = tid; r < BC; r += nt) {
-      float s = 0.0f;
-      for (int q = 0; q < NQ; q++) s += part[r * (NQ + 1) + q];
-      dst[r] = add ? dst[r] + s : s;
-    }
+  auto add_w = [&](float (&acc)[4][4]) {
+#pragma unroll
+    for (int m = 0; m < 4; m++)
+#pragma unroll
+      for (int n = 0; n < 4; n++) acc[m][n] = fmaf(wv[rg + 8 * m], t[m][n], acc[m][n]);
   };
-  auto stage = [&](const float *S, bool transpose) {
-    __syncthreads();  // every thread is done with the previous contents of St and part
-    load_state<D>(St, S, transpose);
+  for (int i = 0; i < ns; i++) {
+    const int kind = kinds[i];
+    __syncthreads();  // every thread is done with the previous contents of St
+    commit(kind);
     __syncthreads();
-  };
-  for (int r = tid; r < BC; r += nt) rowi[r] = coli[r] = 0.0f;
-
-  // later chunks: dG^c, dH^c (zero after the last chunk)
-  if (!last) {
-    const float *dG = a.dGs + ((size_t)u * NC + c) * D * D;
-    const float *dH = a.dHs + ((size_t)u * NC + c) * D * D;
-    stage(dG, true);  // St = dG^T: t = K dG^T, rows (dG k_s)^T
+    const int next = i + 1 < ns ? kinds[i + 1] : 0;
+    if (next) fetch(next);
     zero4x4(t);
-    mm_acc_rows(t, Ks, SPD, rg, St, SPD, c4, D);
-    row_partial(Vs);
+    const float *A = (kind == 2) ? Vs : (kind == 3) ? Gs : (kind == 5) ? Xs : Ks;
+    mm_acc_rows(t, A, SPD, rg, St, SPD, c4, D);
+    if (kind == 1) { add_w(accV); dot_rows(colp, Vs, 1.0f); }
+    if (kind == 2 || kind == 4 || kind == 6) add_w(accK);
+    if (kind == 3) dot_rows(rowp, Xs, 1.0f);
+    if (kind == 5) dot_rows(rowp, Ys, -1.0f);
+    if (kind == 6) dot_rows(colp, Ks, 1.0f);
+    if ((kind == 2 && next == 3) || (kind == 4 && next == 5)) {  // <dG, S^G> or <dH, S^H>
 #pragma unroll
-    for (int m = 0; m < 4; m++)
-#pragma unroll
-      for (int n = 0; n < 4; n++) accV[m][n] = fmaf(wv[rg + 8 * m], t[m][n], accV[m][n]);
-    __syncthreads();
-    row_finish(coli, false);
-    stage(dG, false);  // St = dG: t = V dG, rows (dG^T v_s)^T
-    zero4x4(t);
-    mm_acc_rows(t, Vs, SPD, rg, St, SPD, c4, D);
-    stage(dH, false);  // St = dH: t += K dH, rows (dH^T k_s)^T
-    mm_acc_rows(t, Ks, SPD, rg, St, SPD, c4, D);
-#pragma unroll
-    for (int m = 0; m < 4; m++)
-#pragma unroll
-      for (int n = 0; n < 4; n++) accK[m][n] = fmaf(wv[rg + 8 * m], t[m][n], accK[m][n]);
-    stage(dH, true);  // St = dH^T: t = K dH^T, rows (dH k_s)^T
-    zero4x4(t);
-    mm_acc_rows(t, Ks, SPD, rg, St, SPD, c4, D);
-    row_partial(Ks);
-#pragma unroll
-    for (int m = 0; m < 4; m++)
-#pragma unroll
-      for (int n = 0; n < 4; n++) accK[m][n] = fmaf(wv[rg + 8 * m], t[m][n], accK[m][n]);
-    __syncthreads();
-    row_finish(coli, true);
-  }
-  // earlier chunks: S^G_{c-1}, S^H_{c-1} (zero before the first chunk)
-  float through = 0.0f;
-  if (!first) {
-    const float *SG = ws.SG + ((size_t)u * NC + c - 1) * D * D;
-    const float *SH = ws.SH + ((size_t)u * NC + c - 1) * D * D;
-    stage(SG, true);  // St = S^G^T: t = X S^G^T, rows (S^G x_t)^T
-    zero4x4(t);
-    mm_acc_rows(t, Xs, SPD, rg, St, SPD, c4, D);
-    row_partial(Gs);
-    __syncthreads();
-    row_finish(rowi, false);
-    stage(SH, false);  // S^H symmetric: t = X S^H, rows (S^H x_t)^T
-    zero4x4(t);
-    mm_acc_rows(t, Xs, SPD, rg, St, SPD, c4, D);
-#pragma unroll
-    for (int m = 0; m < 4; m++)
-#pragma unroll
-      for (int n = 0; n < 4; n++) t[m][n] = -t[m][n];
-    row_partial(Ys);
-    __syncthreads();
-    row_finish(rowi, true);
-    // pairs across the whole chunk: a_c (<dG^c, S^G_{c-1}> + <dH^c, S^H_{c-1}>)
-    if (!last) {
-      const float4 *dG4 = reinterpret_cast<const float4 *>(a.dGs + ((size_t)u * NC + c) * D * D);
-      const float4 *dH4 = reinterpret_cast<const float4 *>(a.dHs + ((size_t)u * NC + c) * D * D);
-      const float4 *SG4 = reinterpret_cast<const float4 *>(SG), *SH4 = reinterpret_cast<const float4 *>(SH);
-      float s = 0.0f;
-      for (int e = tid; e < D * D / 4; e += nt) {
-        const float4 x = dG4[e], y = SG4[e], z = dH4[e], w = SH4[e];
-        s += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w + z.x * w.x + z.y * w.y + z.z * w.z + z.w * w.w;
+      for (int q = 0; q < NR; q++) {
+        int r, cc;
+        pos(q, false, r, cc);
+        const float4 z = *reinterpret_cast<const float4 *>(St + r * SPD + cc);
+        thr += z.x * R[q].x + z.y * R[q].y + z.z * R[q].z + z.w * R[q].w;
       }
-      red[tid] = s;
-      __syncthreads();
-      float tot = 0.0f;
-      for (int q = 0; q < nt; q++) tot += red[q];  // the same order in every thread
-      through = expf(lend) * tot;
     }
+  }
+  // finish the per-row sums over the threads of a row, and the pair sum over the block
+  __syncthreads();
+#pragma unroll
+  for (int m = 0; m < 4; m++) part[(rg + 8 * m) * (NQ + 1) + c4] = colp[m];
+  red[tid] = thr;
+  __syncthreads();
+  for (int r = tid; r < BC; r += nt) {
+    float sc = 0.0f;
+    for (int q = 0; q < NQ; q++) sc += part[r * (NQ + 1) + q];
+    coli[r] = sc;
+  }
+  float through = 0.0f;
+  for (int q = 0; q < nt; q++) through += red[q];  // the same order in every thread
+  through *= expf(lend);
+  __syncthreads();
+#pragma unroll
+  for (int m = 0; m < 4; m++) part[(rg + 8 * m) * (NQ + 1) + c4] = rowp[m];
+  __syncthreads();
+  for (int r = tid; r < BC; r += nt) {
+    float sc = 0.0f;
+    for (int q = 0; q < NQ; q++) sc += part[r * (NQ + 1) + q];
+    rowi[r] = sc;
   }
   __syncthreads();
 
@@ -418,15 +468,26 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
     for (int i = 0; i < Cv; i++) s = fmaf(Ys[i * SPD + col], Xs[i * SPD + col], s);
     a.dlam_part[((size_t)u * NC + c) * D + col] = -s;
   }
-  for (int uu = tid; uu < Cv; uu += nt) {
-    float s = through;
-    for (int tt = uu; tt < Cv; tt++) {  // later token in the chunk
-      s += rowi[tt] * expf(el[tt]);
+  // gate gradients: token uu of the chunk takes the pairs t >= uu > s; eight lanes per
+  // token split the later tokens t (t = uu + p, uu + p + 8, ...) and meet by shuffles
+  for (int idx = tid; idx < BC * 8; idx += nt) {  // the same trip count in every thread
+    const int uu = idx / 8, p = idx % 8;
+    float s = 0.0f;
+    for (int tt = uu + p; tt < Cv; tt += 8) {  // later token in the chunk
+      s += rowi[tt] * expf(el[tt]);            // ... and earlier token before it
       for (int ss = 0; ss < uu; ss++) s += Cm[tt * SPC + ss];
     }
-    for (int ss = 0; ss < uu; ss++) s += coli[ss] * wv[ss];  // later token after the chunk
-    const float g = a.gamma[tokbase + uu];
-    a.dgamma[tokbase + uu] = (logf(g) >= kLogGateFloor) ? s / g : 0.0f;
+    if (p == 0 && uu < Cv) {
+      s += through;                                            // pairs across the chunk
+      for (int ss = 0; ss < uu; ss++) s += coli[ss] * wv[ss];  // later token after it
+    }
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    if (p == 0 && uu < Cv) {
+      const float g = a.gamma[tokbase + uu];
+      a.dgamma[tokbase + uu] = (logf(g) >= kLogGateFloor) ? s / g : 0.0f;
+    }
   }
 }
 
