@@ -180,59 +180,79 @@ __global__ void __launch_bounds__(256) mesa_bwd_rhs_kernel(BwdArgs a, FwdWorkspa
   }
 }
 
-// Chunk sums of the state adjoints: Delta^G_c = sum_i e^{l_i} g_i x_i^T (z = 0, into dGs)
-// and Delta^H_c = -sum_i e^{l_i} y_i x_i^T (z = 1, into dHs).  grid (NC, U, 2), block 256;
-// each thread owns a (D/16) x (D/16) register tile.
-template <int D, typename TIO>
-__global__ void __launch_bounds__(256) mesa_bwd_delta_kernel(BwdArgs a, FwdWorkspace ws, int NC) {
-  const int c = blockIdx.x, u = blockIdx.y, isH = blockIdx.z, T = a.T;
-  const int t0 = c * BC, Cv = min(BC, T - t0);
-  const size_t tokbase = (size_t)u * T + t0;
-  __shared__ __align__(16) float Ls[BC * D], Xs[BC * D], wv[BC];
-#pragma unroll 4
-  for (int e4 = threadIdx.x; e4 < Cv * D / 4; e4 += blockDim.x) {
-    const size_t e = tokbase * D + 4 * e4;
-    float4 l = isH ? load4(a.Y, e) : load4((const TIO *)a.dout, e);
-    if (isH) l = make_float4(-l.x, -l.y, -l.z, -l.w);
-    reinterpret_cast<float4 *>(Ls)[e4] = l;
-    reinterpret_cast<float4 *>(Xs)[e4] = load4(a.X, e);
-  }
-  for (int j = threadIdx.x; j < Cv; j += blockDim.x) wv[j] = expf(ws.ell[tokbase + j]);
-  __syncthreads();
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  outer_sum<D>(Ls, Xs, wv, Cv, tx, ty, (isH ? a.dHs : a.dGs) + ((size_t)u * NC + c) * D * D);
-}
-
-// Reverse scan in place: entry c becomes the adjoint after chunk c (zero for the last chunk),
-// dS^{c-1} = a_c dS^c + Delta_c.  grid (ceil(2 D^2 / 256), U), block 256.
-template <int D>
-__global__ void __launch_bounds__(256) mesa_bwd_scan_kernel(BwdArgs a, FwdWorkspace ws, int NC) {
-  const int u = blockIdx.y, T = a.T;
-  int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= 2 * D * D) return;
-  const bool isH = e >= D * D;
-  if (isH) e -= D * D;
-  float *S = (isH ? a.dHs : a.dGs) + (size_t)u * NC * D * D + e;
-  float s = 0.0f;
-  constexpr int G = 8;  // the loads of a group of chunks go out before its dependent updates
-  for (int c0 = NC - 1; c0 >= 0; c0 -= G) {
-    float dl[G], av[G];
+// The chunk states of one unit in one sweep over its chunks (grid (2, U), z picks the state),
+// each chunk's sum built on the fly from its token rows and added to the running state held
+// in registers, which is written once per chunk; the next chunk's rows are loaded into
+// registers while the current chunk's FMAs run.
+//   BWD = false, the forward states S_c after chunk c (ascending), zero initial state:
+//     z = 0: S^H, L = k, R = k;  z = 1: S^G, L = v, R = k;  S_c = a_c S_{c-1} + sum_j w_j L_j R_j^T
+//   BWD = true, the state adjoints dS^c after chunk c (descending, zero after the last chunk):
+//     z = 0: dG, L = dout, R = x;  z = 1: dH, L = -y, R = x;
+//     dS^{c-1} = a_c dS^c + sum_j e^{l_j} L_j R_j^T
+template <int D, typename TIO, bool BWD>
+__global__ void __launch_bounds__(256, 2) mesa_state_sweep_kernel(BwdArgs a, FwdWorkspace ws, int NC) {
+  constexpr int TM = D / 16, NV = BC * D / 4, NP = (NV + 255) / 256;
+  const int z = blockIdx.x, u = blockIdx.y, T = a.T, tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  __shared__ __align__(16) float Ls[BC * D], Rs[BC * D], wv[BC];
+  float acc[TM][TM];
 #pragma unroll
-    for (int g = 0; g < G; g++) {
-      const int c = c0 - g;
-      if (c >= 0) {
-        dl[g] = S[(size_t)c * D * D];
-        av[g] = ws.ell[(size_t)u * T + min(T, (c + 1) * BC) - 1];
+  for (int m = 0; m < TM; m++)
+#pragma unroll
+    for (int q = 0; q < TM; q++) acc[m][q] = 0.0f;
+  float4 pl[NP], pr[NP];
+  auto fetch = [&](int c) {
+    const int t0 = c * BC, Cv = min(BC, T - t0);
+    const size_t base = ((size_t)u * T + t0) * D;
+#pragma unroll
+    for (int q = 0; q < NP; q++) {
+      const int e4 = tid + 256 * q;
+      if (e4 < Cv * D / 4) {
+        const size_t e = base + 4 * (size_t)e4;
+        if constexpr (BWD) {
+          if (z) {
+            const float4 y = load4(a.Y, e);
+            pl[q] = make_float4(-y.x, -y.y, -y.z, -y.w);
+          } else {
+            pl[q] = load4((const TIO *)a.dout, e);
+          }
+          pr[q] = load4(a.X, e);
+        } else {
+          pl[q] = load4(z ? (const TIO *)a.v : (const TIO *)a.k, e);
+          pr[q] = load4((const TIO *)a.k, e);
+        }
+      } else {
+        pl[q] = pr[q] = make_float4(0, 0, 0, 0);
       }
     }
+  };
+  int c = BWD ? NC - 1 : 0;
+  fetch(c);
+  for (int it = 0; it < NC; it++, c += BWD ? -1 : 1) {
+    const int t0 = c * BC, Cv = min(BC, T - t0);
+    const float *ell = ws.ell + (size_t)u * T + t0;
+    __syncthreads();  // every thread is done with the previous chunk's rows
 #pragma unroll
-    for (int g = 0; g < G; g++) {
-      const int c = c0 - g;
-      if (c >= 0) {
-        S[(size_t)c * D * D] = s;
-        s = fmaf(expf(av[g]), s, dl[g]);
+    for (int q = 0; q < NP; q++) {
+      const int e4 = tid + 256 * q;
+      if (e4 < NV) {
+        reinterpret_cast<float4 *>(Ls)[e4] = pl[q];
+        reinterpret_cast<float4 *>(Rs)[e4] = pr[q];
       }
     }
+    const float lend = ell[Cv - 1];
+    if (tid < Cv) wv[tid] = expf(BWD ? ell[tid] : lend - ell[tid]);
+    __syncthreads();
+    if (it + 1 < NC) fetch(c + (BWD ? -1 : 1));
+    float *S = (BWD ? (z ? a.dHs : a.dGs) : (z ? ws.SG : ws.SH)) + ((size_t)u * NC + c) * D * D;
+    if (BWD) tile_store<D>(acc, S, tx, ty);
+    const float ac = expf(lend);
+#pragma unroll
+    for (int m = 0; m < TM; m++)
+#pragma unroll
+      for (int q = 0; q < TM; q++) acc[m][q] *= ac;
+    outer_acc<D>(Ls, Rs, wv, Cv, tx, ty, acc);
+    if (!BWD) tile_store<D>(acc, S, tx, ty);
   }
 }
 
@@ -505,7 +525,11 @@ template <int D, typename TIO>
 int launch_bwd_t(const BwdArgs &a, const FwdWorkspace &ws, int phase, cudaStream_t st) {
   const int U = a.B * a.H, NC = (a.T + BC - 1) / BC;
   constexpr int SPD = D + 4, SPC = BC + 1;
-  if (phase == 0) {
+  if (phase == 2) {  // the forward's chunk states (ws.ell must hold the log-decays)
+    timing_mark_begin(K_BWD_FSTATES, st);
+    mesa_state_sweep_kernel<D, TIO, false><<<dim3(2, U), 256, 0, st>>>(a, ws, NC);
+    timing_mark_end(K_BWD_FSTATES, st);
+  } else if (phase == 0) {
     const size_t smem = sizeof(float) * (3 * BC * SPD + D * SPD + BC * SPC + BC);
     auto k = mesa_bwd_rhs_kernel<D, TIO>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
@@ -515,8 +539,7 @@ int launch_bwd_t(const BwdArgs &a, const FwdWorkspace &ws, int phase, cudaStream
     timing_mark_end(K_BWD_RHS, st);
   } else {
     timing_mark_begin(K_BWD_STATES, st);
-    mesa_bwd_delta_kernel<D, TIO><<<dim3(NC, U, 2), 256, 0, st>>>(a, ws, NC);
-    mesa_bwd_scan_kernel<D><<<dim3((2 * D * D + 255) / 256, U), 256, 0, st>>>(a, ws, NC);
+    mesa_state_sweep_kernel<D, TIO, true><<<dim3(2, U), 256, 0, st>>>(a, ws, NC);
     timing_mark_end(K_BWD_STATES, st);
     const size_t smem = sizeof(float) * (5 * BC * SPD + D * SPD + 4 * BC * SPC + BC * (D / 4 + 1) +
                                          4 * BC + 2 * D);
@@ -549,6 +572,10 @@ int launch_bwd_rhs(const BwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
 
 int launch_bwd_grads(const BwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
   return a.dtype == 1 ? launch_bwd_d<__nv_bfloat16>(a, ws, 1, st) : launch_bwd_d<float>(a, ws, 1, st);
+}
+
+int launch_bwd_states(const BwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+  return a.dtype == 1 ? launch_bwd_d<__nv_bfloat16>(a, ws, 2, st) : launch_bwd_d<float>(a, ws, 2, st);
 }
 
 }  // namespace mesa

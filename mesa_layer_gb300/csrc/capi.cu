@@ -173,7 +173,8 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_CG_ROWS: return "mesa_cg_rows_kernel";
     case mesa::K_PREPROC: return "mesa_qk_preprocess_kernel";
     case mesa::K_BWD_RHS: return "mesa_bwd_rhs_kernel";
-    case mesa::K_BWD_STATES: return "mesa_bwd_delta_kernel+mesa_bwd_scan_kernel";
+    case mesa::K_BWD_STATES: return "mesa_state_sweep_kernel<adjoints>";
+    case mesa::K_BWD_FSTATES: return "mesa_state_sweep_kernel<states>";
     case mesa::K_BWD_GRAD: return "mesa_bwd_grad_kernel+mesa_bwd_lambda_kernel";
   }
   return nullptr;
@@ -304,8 +305,12 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
                   nullptr, iters_fwd, nullptr, nullptr, nullptr, nullptr};
   mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2]),
                         nullptr, nullptr, 1};
+  mesa::BwdArgs ba{B, H, T, dk, dv, dtype, k, v, dout, gamma, X, Y, Bv,
+                   (float *)(w + off[11]), (float *)(w + off[12]), (float *)(w + off[13]),
+                   dq, dk_out, dv_out, dgamma, dlambda};
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
-  if (mesa::launch_chunk_states(a, ws, nullptr, stream) != 0) return MESA_ERR_CUDA;
+  if (mesa::launch_ell(a, ws, stream) != 0 || mesa::launch_bwd_states(ba, ws, stream) != 0)
+    return MESA_ERR_CUDA;
   // the tensor-core solves work on 128-token chunks with their own states
   mesa::FwdArgs a128 = a;
   a128.chunk = 128;
@@ -328,9 +333,6 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
                     : mesa::launch_chunk_cg_simt(b, ws, stream, sv);
   };
   // x_t (the forward's solves, recomputed), b_t = G_t^T g_t, y_t, then the gradients
-  mesa::BwdArgs ba{B, H, T, dk, dv, dtype, k, v, dout, gamma, X, Y, Bv,
-                   (float *)(w + off[11]), (float *)(w + off[12]), (float *)(w + off[13]),
-                   dq, dk_out, dv_out, dgamma, dlambda};
   if (solve(nullptr, X, iters_fwd) != 0) return MESA_ERR_CUDA;
   if (mesa::launch_bwd_rhs(ba, ws, stream) != 0) return MESA_ERR_CUDA;
   if (solve(Bv, Y, iters_bwd) != 0) return MESA_ERR_CUDA;

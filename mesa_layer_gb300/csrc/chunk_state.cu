@@ -109,6 +109,14 @@ __global__ void __launch_bounds__(256) mesa_scan_kernel(const float *__restrict_
   if (F) F[(size_t)u * D * D + e] = s;
 }
 
+int launch_ell(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st) {
+  const int NC = (a.T + a.chunk - 1) / a.chunk;
+  timing_mark_begin(K_ELL, st);
+  mesa_ell_kernel<<<dim3(NC, a.B * a.H), 128, 0, st>>>(a.gamma, ws.ell, a.T, a.chunk);
+  timing_mark_end(K_ELL, st);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
 template <int D, typename TIO>
 static int launch_states_t(const FwdArgs &a, const FwdWorkspace &ws, unsigned *tc_status,
                            cudaStream_t st) {

@@ -53,27 +53,21 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// S[a][b] = sum_{j < n} w_j L[j][a] R[j][b] for D x D, L and R [n][D] in shared memory; 256
-// threads (tx, ty) of 16 x 16, each a (D/16) x (D/16) register tile.  For D >= 64 the tile
-// is made of 4 x 4 blocks (rows 64 g + 4 ty + r, columns 64 h + 4 tx + s) read and written
-// as float4; below, rows ty + 16 m and columns tx + 16 n.  Every entry is the same FMA chain
-// over j in both layouts.
+// Outer-product sums over token rows: acc[a][b] += sum_{j < n} w_j L[j][a] R[j][b] for a
+// D x D matrix, L and R [n][D] in shared memory, 256 threads (tx, ty) of 16 x 16 holding a
+// (D/16) x (D/16) register tile.  For D >= 64 the tile is made of 4 x 4 blocks (rows
+// 64 g + 4 ty + r, columns 64 h + 4 tx + s), read and written as float4; below, rows
+// ty + 16 m and columns tx + 16 n.  Every entry is one FMA chain over j in both layouts.
 template <int D>
-__device__ __forceinline__ void outer_sum(const float *L, const float *R, const float *w, int n,
-                                          int tx, int ty, float *S) {
+__device__ __forceinline__ void outer_acc(const float *L, const float *R, const float *w, int n,
+                                          int tx, int ty, float (&acc)[D / 16][D / 16]) {
   constexpr int TM = D / 16;
-  float acc[TM][TM];
+  for (int j = 0; j < n; j++) {
+    const float wj = w[j];
+    float la[TM], rb[TM];
+    if constexpr (D >= 64) {
 #pragma unroll
-  for (int m = 0; m < TM; m++)
-#pragma unroll
-    for (int q = 0; q < TM; q++) acc[m][q] = 0.0f;
-  if constexpr (D >= 64) {
-    constexpr int G = TM / 4;
-    for (int j = 0; j < n; j++) {
-      const float wj = w[j];
-      float la[TM], rb[TM];
-#pragma unroll
-      for (int g = 0; g < G; g++) {
+      for (int g = 0; g < TM / 4; g++) {
         const float4 l4 = *reinterpret_cast<const float4 *>(L + j * D + 64 * g + 4 * ty);
         const float4 r4 = *reinterpret_cast<const float4 *>(R + j * D + 64 * g + 4 * tx);
         la[4 * g] = l4.x * wj;
@@ -85,37 +79,52 @@ __device__ __forceinline__ void outer_sum(const float *L, const float *R, const 
         rb[4 * g + 2] = r4.z;
         rb[4 * g + 3] = r4.w;
       }
-#pragma unroll
-      for (int m = 0; m < TM; m++)
-#pragma unroll
-        for (int q = 0; q < TM; q++) acc[m][q] = fmaf(la[m], rb[q], acc[m][q]);
-    }
-#pragma unroll
-    for (int m = 0; m < TM; m++) {
-      const int row = 64 * (m / 4) + 4 * ty + (m % 4);
-#pragma unroll
-      for (int h = 0; h < G; h++)
-        *reinterpret_cast<float4 *>(S + row * D + 64 * h + 4 * tx) =
-            make_float4(acc[m][4 * h], acc[m][4 * h + 1], acc[m][4 * h + 2], acc[m][4 * h + 3]);
-    }
-  } else {
-    for (int j = 0; j < n; j++) {
-      const float wj = w[j];
-      float la[TM], rb[TM];
+    } else {
 #pragma unroll
       for (int m = 0; m < TM; m++) la[m] = L[j * D + ty + 16 * m] * wj;
 #pragma unroll
       for (int q = 0; q < TM; q++) rb[q] = R[j * D + tx + 16 * q];
-#pragma unroll
-      for (int m = 0; m < TM; m++)
-#pragma unroll
-        for (int q = 0; q < TM; q++) acc[m][q] = fmaf(la[m], rb[q], acc[m][q]);
     }
+#pragma unroll
+    for (int m = 0; m < TM; m++)
+#pragma unroll
+      for (int q = 0; q < TM; q++) acc[m][q] = fmaf(la[m], rb[q], acc[m][q]);
+  }
+}
+
+// Writes the register tile of outer_acc to the D x D row-major matrix S.
+template <int D>
+__device__ __forceinline__ void tile_store(const float (&acc)[D / 16][D / 16], float *S, int tx,
+                                           int ty) {
+  constexpr int TM = D / 16;
+  if constexpr (D >= 64) {
+#pragma unroll
+    for (int m = 0; m < TM; m++) {
+      const int row = 64 * (m / 4) + 4 * ty + (m % 4);
+#pragma unroll
+      for (int h = 0; h < TM / 4; h++)
+        *reinterpret_cast<float4 *>(S + row * D + 64 * h + 4 * tx) =
+            make_float4(acc[m][4 * h], acc[m][4 * h + 1], acc[m][4 * h + 2], acc[m][4 * h + 3]);
+    }
+  } else {
 #pragma unroll
     for (int m = 0; m < TM; m++)
 #pragma unroll
       for (int q = 0; q < TM; q++) S[(ty + 16 * m) * D + tx + 16 * q] = acc[m][q];
   }
+}
+
+// S = sum_{j < n} w_j L[j] R[j]^T (outer_acc from zero, then tile_store).
+template <int D>
+__device__ __forceinline__ void outer_sum(const float *L, const float *R, const float *w, int n,
+                                          int tx, int ty, float *S) {
+  float acc[D / 16][D / 16];
+#pragma unroll
+  for (int m = 0; m < D / 16; m++)
+#pragma unroll
+    for (int q = 0; q < D / 16; q++) acc[m][q] = 0.0f;
+  outer_acc<D>(L, R, w, n, tx, ty, acc);
+  tile_store<D>(acc, S, tx, ty);
 }
 
 // Workspace carve-up of the chunked forward (all fp32, each section 256-byte aligned).

@@ -70,7 +70,8 @@ struct PreArgs {
 // Kernel kinds, for the optional per-kernel timing of benchmarks (mesa_timing_*).
 enum KernelKind {
   K_ELL = 0, K_DELTA = 1, K_SCAN = 2, K_CG_SIMT = 3, K_DECODE = 4, K_CG_TC = 5, K_DELTA_TC = 6, K_CG_ROWS = 7,
-  K_PREPROC = 8, K_BWD_RHS = 9, K_BWD_STATES = 10, K_BWD_GRAD = 11, K_NUM_KINDS = 12
+  K_PREPROC = 8, K_BWD_RHS = 9, K_BWD_STATES = 10, K_BWD_GRAD = 11, K_BWD_FSTATES = 12,
+  K_NUM_KINDS = 13
 };
 
 // Record a timing event before / after a launch of `kind` on `st` (no-op unless enabled).
@@ -100,6 +101,11 @@ int launch_decode(const DecArgs &a, cudaStream_t st);
 // and log-decays), then the state adjoints and every gradient.
 int launch_bwd_rhs(const BwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
 int launch_bwd_grads(const BwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
+// The forward's chunk-kBwdChunk states S^H, S^G (zero initial state) for the backward, in one
+// sweep per unit; ws.ell must already hold the chunk log-decays (launch_ell).
+int launch_bwd_states(const BwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
+// The per-token log-decays l_i of chunks of a.chunk tokens into ws.ell.
+int launch_ell(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st);
 // step == false: whole sequences [U, T, d]; step == true: one decode step [U, d].
 int launch_qk_preprocess(const PreArgs &a, bool step, cudaStream_t st);
 
