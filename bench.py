@@ -539,12 +539,17 @@ def bench_decode(args, w, rank, world, dev, lib, torch, binding):
     res = timed_loop(args, torch, lib, step, None, world, dist, dev)
     res.update({"iters": iters.cpu().numpy(), "tokens_per_step": N, "flush": False})
     if not args.no_e2e:
-        h = {k: steps[0][k].cpu().pin_memory() for k in steps[0]}
+        # each step's own inputs from pinned host memory, in the same order as the device loop
+        # (repeating one step's inputs would hand the warm start its own solution)
+        hs = [{k: st_[k].cpu().pin_memory() for k in st_} for st_ in steps]
         dd = {k: torch.empty_like(steps[0][k]) for k in steps[0]}
         h_out = torch.empty(out.shape, dtype=td).pin_memory()
         h_it = torch.empty(iters.shape, dtype=torch.int32).pin_memory()
+        ecount = [0]
 
         def estep():
+            h = hs[ecount[0] % n_steps]
+            ecount[0] += 1
             for k in h:
                 dd[k].copy_(h[k], non_blocking=True)
             decode(dd["q"], dd["k"], dd["v"], dd["gamma"])
@@ -562,7 +567,7 @@ def bench_decode(args, w, rank, world, dev, lib, torch, binding):
         e.record()
         torch.cuda.synchronize()
         res["e2e"] = {"ms_per_step": s.elapsed_time(e) / n,
-                      "h2d": sum(t.numel() * t.element_size() for t in h.values()),
+                      "h2d": sum(t.numel() * t.element_size() for t in hs[0].values()),
                       "d2h": h_out.numel() * h_out.element_size() + h_it.numel() * 4}
     return res
 
