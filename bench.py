@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--impl", default="mesa", choices=["mesa", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--batch", type=int, default=None,
+                   help="override the workload's batch B (small cases for profiler captures; not a bench line)")
     p.add_argument("--decode-prefix", type=int, default=None,
                    help="decode workload: state-only prefix steps (default: the workload's)")
     return p.parse_args()
@@ -369,7 +371,7 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
-    w = synth.workload(args.workload)
+    w = synth.workload(args.workload, **({"B": args.batch} if args.batch else {}))
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, desc, _ = oracle_sample(w, budget_s=10.0)
