@@ -338,8 +338,8 @@ def workload_config(w, extra=None):
         if w.warm:
             cfg["cg"] += ", warm start from the previous step's solution"
     if w.backward:
-        cfg["step"] = ("backward: forward solves recomputed, second CG per token on G_t^T dout_t, "
-                       "state adjoints, dq/dk/dv/dgamma/dlambda")
+        cfg["step"] = ("backward given the forward's kept iterates: second CG per token on G_t^T dout_t, "
+                       "chunk states and state adjoints, dq/dk/dv/dgamma/dlambda")
         cfg["chunk"] = "32 (gradient kernels), 128 (tensor-core solves)"
     if w.conv_taps:
         cfg = {"workload": w.name, "B": w.B, "heads": w.H, "T": w.T, "d": w.dk, "qk_dtype": w.dtype,
@@ -619,6 +619,9 @@ def bench_preprocess(args, w, rank, world, dev, lib, torch, binding):
 
 
 def bench_backward(args, w, rank, world, dev, lib, torch, binding):
+    """One step = one mesa_backward_chunked call given the forward's kept iterates (as in
+    training: mesa_forward_chunked_save runs once, untimed, before the loop); the call that
+    recomputes the forward's solves itself is timed as well and reported in config."""
     import torch.distributed as dist
     inp = synth.backward_inputs(w, seed=rank)
     td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -633,27 +636,44 @@ def bench_backward(args, w, rank, world, dev, lib, torch, binding):
             "iters_fwd": torch.empty((B, H, T), dtype=torch.int32, device=dev),
             "iters_bwd": torch.empty((B, H, T), dtype=torch.int32, device=dev)}
     ws = torch.empty(binding.mesa_backward_workspace_size(B, H, T, dk, dv), dtype=torch.uint8, device=dev)
+    _, _, xs = binding.mesa_forward_chunked_save(d_in["q"], d_in["k"], d_in["v"], d_in["gamma"], d_in["lam"],
+                                                 w.cg_iters, w.cg_tol, w.chunk)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     in_bytes = sum(d_in[k].numel() * d_in[k].element_size() for k in keys)
     needs_flush = in_bytes < 2 * (129 << 20)
 
-    def call(d):
+    def call(d, x_saved):
         binding.mesa_backward_chunked(d["q"], d["k"], d["v"], d["gamma"], d_in["lam"], d["dout"], w.cg_iters, w.cg_tol,
-                                      workspace=ws, **outs)
+                                      workspace=ws, x_saved=x_saved, **outs)
 
-    res = timed_loop(args, torch, lib, lambda i: call(d_in), (lambda: flush.random_(0, 255)) if needs_flush else None,
-                     world, dist, dev)
+    fl = (lambda: flush.random_(0, 255)) if needs_flush else None
+    res = timed_loop(args, torch, lib, lambda i: call(d_in, xs), fl, world, dist, dev)
     res.update({"iters": outs["iters_bwd"].cpu().numpy(), "tokens_per_step": B * T, "flush": needs_flush})
+    # the self-contained call (the forward's solves recomputed inside), a few steps
+    rec = []
+    for r in range(max(3, min(args.steps, 10)) + 1):
+        if fl:
+            fl()
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record()
+        call(d_in, None)
+        e_.record()
+        torch.cuda.synchronize()
+        if r:
+            rec.append(s_.elapsed_time(e_))
+    res["extra"] = {"x_saved": "from mesa_forward_chunked_save (untimed, before the loop)",
+                    "ms_per_step_recomputing_the_forward_solves": float(np.median(rec))}
     if not args.no_e2e:
         h = {k: torch.from_numpy(inp[k]).to(td if k in ("q", "k", "v", "dout") else torch.float32).pin_memory()
              for k in keys}
+        h["x_saved"] = xs.cpu().pin_memory()
         d = {k: torch.empty_like(h[k], device=dev) for k in h}
         back = {k: torch.empty(outs[k].shape, dtype=outs[k].dtype).pin_memory() for k in ("dq", "dk", "dv", "dgamma", "dlambda")}
 
         def estep():
             for k in h:
                 d[k].copy_(h[k], non_blocking=True)
-            call(d)
+            call(d, d["x_saved"])
             for k in back:
                 back[k].copy_(outs[k], non_blocking=True)
 
@@ -739,6 +759,7 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
                                                              "launches": kind_n[i]}
                for i in range(len(kind_ms)) if kind_n[i] > 0}
     extra = {} if w.conv_taps else {"mean_iters": float(it.mean()), "max_iters": int(it.max())}
+    extra.update(res.get("extra", {}))
     extra.update({
              "l2": ("flushed between timed steps (256 MiB device write)" if res["flush"]
                     else "working set larger than L2, not flushed"),

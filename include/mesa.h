@@ -116,7 +116,9 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
  *     dgamma_t = <dH_t, H_{t-1}> + <dG_t, G_{t-1}>,
  * dH_t, dG_t the total adjoints of the states after token t.  With exact solves these are
  * the exact gradients of o_t = G_t (H_t + Lambda)^-1 q_t (not those of k unrolled CG steps).
- * The forward's solves x_t are recomputed (nothing is kept from the forward call).
+ * x_saved: NULL, or the forward's iterates [B, H, T, dk] fp32 as written by
+ * mesa_forward_chunked_save (16-byte aligned); NULL recomputes them (the same kernels as the
+ * forward; iters_fwd then receives their counts, and is not written when x_saved is given).
  *   q, k, dq, dk_out  [B, H, T, dk]  dtype;   v, dout, dv_out  [B, H, T, dv]  dtype
  *   gamma, dgamma [B, H, T] fp32 (a gate below e^-80, where the forward clamps the log-gate,
  *                 gets dgamma = 0);  lambda_diag, dlambda [H, dk] fp32 (dlambda is summed
@@ -131,10 +133,23 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
 size_t mesa_backward_workspace_size(int B, int H, int T, int dk, int dv);
 int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const void *q,
                           const void *k, const void *v, const float *gamma,
-                          const float *lambda_diag, const void *dout, int cg_iters, float cg_tol,
-                          void *dq, void *dk_out, void *dv_out, float *dgamma, float *dlambda,
-                          int32_t *iters_fwd, int32_t *iters_bwd, void *workspace,
-                          size_t workspace_bytes, cudaStream_t stream);
+                          const float *lambda_diag, const void *dout, const float *x_saved,
+                          int cg_iters, float cg_tol, void *dq, void *dk_out, void *dv_out,
+                          float *dgamma, float *dlambda, int32_t *iters_fwd, int32_t *iters_bwd,
+                          void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * mesa_forward_chunked (zero initial state, no final state) that also keeps its CG iterates
+ * for the backward pass: x_saved [B, H, T, dk] fp32 (written, 16-byte aligned) receives x_t,
+ * the iterate the readout o_t = G_t x_t used.  Passed to mesa_backward_chunked as x_saved,
+ * it replaces the recomputation of the forward's solves there.  Other arguments, layouts and
+ * errors as mesa_forward_chunked; x_saved NULL (with B H T > 0) is MESA_ERR_INVALID_ARG.
+ */
+int mesa_forward_chunked_save(int B, int H, int T, int dk, int dv, int dtype, const void *q,
+                              const void *k, const void *v, const float *gamma,
+                              const float *lambda_diag, int cg_iters, float cg_tol, int chunk,
+                              void *out, int32_t *iters_used, float *x_saved, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * One recurrent decode step for N sequences x H heads ("Paralelizacao" bullet: O(1)

@@ -67,8 +67,10 @@ def load(build_if_missing: bool = True):
     lib.mesa_backward_workspace_size.restype = _sz
     lib.mesa_backward_workspace_size.argtypes = [_i] * 5
     lib.mesa_backward_chunked.restype = _i
-    lib.mesa_backward_chunked.argtypes = [_i] * 6 + [_vp] * 3 + [_fp, _fp, _vp, _i, _f] + [_vp] * 3 + [
+    lib.mesa_backward_chunked.argtypes = [_i] * 6 + [_vp] * 3 + [_fp, _fp, _vp, _fp, _i, _f] + [_vp] * 3 + [
         _fp, _fp, _ip, _ip, _vp, _sz, _vp]
+    lib.mesa_forward_chunked_save.restype = _i
+    lib.mesa_forward_chunked_save.argtypes = [_i] * 6 + [_vp] * 5 + [_i, _f, _i, _vp, _ip, _fp, _vp, _sz, _vp]
     _lib = lib
     return lib
 
@@ -147,12 +149,44 @@ def mesa_backward_workspace_size(B, H, T, dk, dv) -> int:
     return int(load().mesa_backward_workspace_size(B, H, T, dk, dv))
 
 
+def mesa_forward_chunked_save(q, k, v, gamma, lambda_diag, cg_iters, cg_tol, chunk, out=None,
+                              iters_used=None, x_saved=None, workspace=None, stream=None):
+    """mesa_forward_chunked (zero initial state) that also returns its CG iterates x_saved
+    [B, H, T, dk] fp32 for mesa_backward_chunked.  Returns (out, iters_used, x_saved)."""
+    lib = load()
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    code = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, name, q.dtype)
+    _require(gamma, "gamma", torch.float32)
+    _require(lambda_diag, "lambda_diag", torch.float32)
+    out = torch.empty((B, H, T, dv), dtype=q.dtype, device=q.device) if out is None else out
+    iters_used = torch.empty((B, H, T), dtype=torch.int32, device=q.device) if iters_used is None else iters_used
+    x_saved = torch.empty((B, H, T, dk), dtype=torch.float32, device=q.device) if x_saved is None else x_saved
+    _require(out, "out", q.dtype)
+    _require(iters_used, "iters_used", torch.int32)
+    _require(x_saved, "x_saved", torch.float32)
+    need = mesa_forward_workspace_size(B, H, T, dk, dv, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _require(workspace, "workspace")
+    st = lib.mesa_forward_chunked_save(B, H, T, dk, dv, code, _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
+                                       _ptr(lambda_diag), int(cg_iters), float(cg_tol), int(chunk), _ptr(out),
+                                       _ptr(iters_used), _ptr(x_saved), _ptr(workspace), workspace.numel(),
+                                       _stream(stream))
+    _check(st, "mesa_forward_chunked_save")
+    return out, iters_used, x_saved
+
+
 def mesa_backward_chunked(q, k, v, gamma, lambda_diag, dout, cg_iters, cg_tol, dq=None, dk=None, dv=None,
                           dgamma=None, dlambda=None, iters_fwd=None, iters_bwd=None, workspace=None,
-                          stream=None):
+                          stream=None, x_saved=None):
     """Backward pass of mesa_forward_chunked (zero initial states): gradients of a loss given
-    dout = dL/dout [B, H, T, dv] (dtype of q).  Returns (dq, dk, dv, dgamma, dlambda,
-    iters_fwd, iters_bwd); dlambda [H, dk] is summed over the batch."""
+    dout = dL/dout [B, H, T, dv] (dtype of q).  x_saved: None (the forward's solves are
+    recomputed) or the iterates from mesa_forward_chunked_save.  Returns (dq, dk, dv, dgamma,
+    dlambda, iters_fwd, iters_bwd); dlambda [H, dk] is summed over the batch; iters_fwd is
+    left unwritten when x_saved is given."""
     lib = load()
     B, H, T, dkk = q.shape
     dvv = v.shape[-1]
@@ -175,12 +209,13 @@ def mesa_backward_chunked(q, k, v, gamma, lambda_diag, dout, cg_iters, cg_tol, d
         _require(t, name, torch.float32)
     _require(iters_fwd, "iters_fwd", torch.int32)
     _require(iters_bwd, "iters_bwd", torch.int32)
+    _require(x_saved, "x_saved", torch.float32)
     need = mesa_backward_workspace_size(B, H, T, dkk, dvv)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     _require(workspace, "workspace")
     st = lib.mesa_backward_chunked(B, H, T, dkk, dvv, code, _ptr(q), _ptr(k), _ptr(v), _ptr(gamma),
-                                   _ptr(lambda_diag), _ptr(dout), int(cg_iters), float(cg_tol), _ptr(dq),
+                                   _ptr(lambda_diag), _ptr(dout), _ptr(x_saved), int(cg_iters), float(cg_tol), _ptr(dq),
                                    _ptr(dk), _ptr(dv), _ptr(dgamma), _ptr(dlambda), _ptr(iters_fwd),
                                    _ptr(iters_bwd), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "mesa_backward_chunked")

@@ -214,12 +214,15 @@ size_t mesa_forward_workspace_size(int B, int H, int T, int dk, int dv, int chun
   return workspace_parts(B, H, T, dk, dv, chunk, off);
 }
 
-int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const void *q,
-                         const void *k, const void *v, const float *gamma,
-                         const float *lambda_diag, int cg_iters, float cg_tol, int chunk,
-                         void *out, int32_t *iters_used, const float *H0, const float *G0,
-                         float *H_final, float *G_final, void *workspace,
-                         size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+// The chunked forward; x_saved != nullptr also writes the CG iterates [B, H, T, dk] fp32.
+int forward_impl(int B, int H, int T, int dk, int dv, int dtype, const void *q, const void *k,
+                 const void *v, const float *gamma, const float *lambda_diag, int cg_iters,
+                 float cg_tol, int chunk, void *out, int32_t *iters_used, const float *H0,
+                 const float *G0, float *H_final, float *G_final, float *x_saved, void *workspace,
+                 size_t workspace_bytes, cudaStream_t stream) {
   if (B < 0 || H < 0 || T < 0 || cg_iters < 0 || cg_iters > kMaxIters || isnan(cg_tol))
     return MESA_ERR_INVALID_ARG;
   if (dtype != MESA_F32 && dtype != MESA_BF16) return MESA_ERR_INVALID_ARG;
@@ -256,10 +259,37 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
                         tc ? mesa::tc_segments((int)U, (T + 127) / 128) : 1};
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
   if (mesa::launch_chunk_states(a, ws, tc ? status : nullptr, stream) != 0) return MESA_ERR_CUDA;
-  const int rc = tc ? mesa::launch_chunk_cg_tc(a, ws, status, stream)
-                 : (dk <= 64 ? mesa::launch_chunk_cg_rows(a, ws, stream)
-                             : mesa::launch_chunk_cg_simt(a, ws, stream));
+  mesa::SolveArgs sv;
+  sv.x_out = x_saved;
+  const int rc = tc ? mesa::launch_chunk_cg_tc(a, ws, status, stream, sv)
+                 : (dk <= 64 ? mesa::launch_chunk_cg_rows(a, ws, stream, sv)
+                             : mesa::launch_chunk_cg_simt(a, ws, stream, sv));
   return rc == 0 ? MESA_OK : MESA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const void *q,
+                         const void *k, const void *v, const float *gamma,
+                         const float *lambda_diag, int cg_iters, float cg_tol, int chunk,
+                         void *out, int32_t *iters_used, const float *H0, const float *G0,
+                         float *H_final, float *G_final, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+  return forward_impl(B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol, chunk,
+                      out, iters_used, H0, G0, H_final, G_final, nullptr, workspace,
+                      workspace_bytes, stream);
+}
+
+int mesa_forward_chunked_save(int B, int H, int T, int dk, int dv, int dtype, const void *q,
+                              const void *k, const void *v, const float *gamma,
+                              const float *lambda_diag, int cg_iters, float cg_tol, int chunk,
+                              void *out, int32_t *iters_used, float *x_saved, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  if ((size_t)B * H * T > 0 && (!x_saved || !aligned(x_saved, 16))) return MESA_ERR_INVALID_ARG;
+  return forward_impl(B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol, chunk,
+                      out, iters_used, nullptr, nullptr, nullptr, nullptr, x_saved, workspace,
+                      workspace_bytes, stream);
 }
 
 size_t mesa_backward_workspace_size(int B, int H, int T, int dk, int dv) {
@@ -270,10 +300,10 @@ size_t mesa_backward_workspace_size(int B, int H, int T, int dk, int dv) {
 
 int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const void *q,
                           const void *k, const void *v, const float *gamma,
-                          const float *lambda_diag, const void *dout, int cg_iters, float cg_tol,
-                          void *dq, void *dk_out, void *dv_out, float *dgamma, float *dlambda,
-                          int32_t *iters_fwd, int32_t *iters_bwd, void *workspace,
-                          size_t workspace_bytes, cudaStream_t stream) {
+                          const float *lambda_diag, const void *dout, const float *x_saved,
+                          int cg_iters, float cg_tol, void *dq, void *dk_out, void *dv_out,
+                          float *dgamma, float *dlambda, int32_t *iters_fwd, int32_t *iters_bwd,
+                          void *workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (B < 0 || H < 0 || T < 0 || cg_iters < 0 || cg_iters > kMaxIters || isnan(cg_tol))
     return MESA_ERR_INVALID_ARG;
   if (dtype != MESA_F32 && dtype != MESA_BF16) return MESA_ERR_INVALID_ARG;
@@ -289,14 +319,15 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
   if (!q || !k || !v || !gamma || !lambda_diag || !dout || !dq || !dk_out || !dv_out || !dgamma)
     return MESA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
-      !aligned(dk_out, 16) || !aligned(dv_out, 16))
+      !aligned(dk_out, 16) || !aligned(dv_out, 16) || (x_saved && !aligned(x_saved, 16)))
     return MESA_ERR_INVALID_ARG;
   size_t off[kBwdParts];
   const size_t need = backward_parts(B, H, T, dk, off);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return MESA_ERR_WORKSPACE;
   char *w = (char *)workspace;
   unsigned *status = (unsigned *)w;
-  float *X = (float *)(w + off[5]), *Y = (float *)(w + off[6]), *Bv = (float *)(w + off[7]);
+  float *Xw = (float *)(w + off[5]), *Y = (float *)(w + off[6]), *Bv = (float *)(w + off[7]);
+  const float *X = x_saved ? x_saved : Xw;  // the forward's iterates, kept or recomputed
   // the solves on the tensor cores need 16-byte aligned bf16 operands and d = 128
   const bool tc = use_tc(dtype, dk, dv, q, k, v, dout, nullptr, nullptr);
   const int C = mesa::kBwdChunk;
@@ -332,8 +363,8 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
     return dk <= 64 ? mesa::launch_chunk_cg_rows(b, ws, stream, sv)
                     : mesa::launch_chunk_cg_simt(b, ws, stream, sv);
   };
-  // x_t (the forward's solves, recomputed), b_t = G_t^T g_t, y_t, then the gradients
-  if (solve(nullptr, X, iters_fwd) != 0) return MESA_ERR_CUDA;
+  // x_t (the forward's solves, unless kept), b_t = G_t^T g_t, y_t, then the gradients
+  if (!x_saved && solve(nullptr, Xw, iters_fwd) != 0) return MESA_ERR_CUDA;
   if (mesa::launch_bwd_rhs(ba, ws, stream) != 0) return MESA_ERR_CUDA;
   if (solve(Bv, Y, iters_bwd) != 0) return MESA_ERR_CUDA;
   if (mesa::launch_bwd_grads(ba, ws, stream) != 0) return MESA_ERR_CUDA;

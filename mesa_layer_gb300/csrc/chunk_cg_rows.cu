@@ -17,8 +17,8 @@
 namespace mesa {
 
 // SOLVE = true: a solve of the backward pass (right-hand sides sv.rhs or q, the iterate to
-// sv.x_out, no readout); false: the forward.
-template <int D, typename TIO, bool SOLVE>
+// sv.x_out, no readout); false: the forward, with SAVE the iterate also written to sv.x_out.
+template <int D, typename TIO, bool SOLVE, bool SAVE>
 __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspace ws, int NC,
                                                            SolveArgs sv) {
   constexpr int DC = D / 4;  // columns per lane
@@ -213,13 +213,13 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
     }
   }
 
-  if constexpr (SOLVE) {  // the iterate itself, no readout
+  if constexpr (SOLVE || SAVE) {  // the iterate itself
     if (valid) {
 #pragma unroll
       for (int n = 0; n < DC; n++) sv.x_out[(tokbase + i) * D + col(n)] = x[n];
-      if (part == 0 && a.iters) a.iters[tokbase + i] = cnt;
+      if (SOLVE && part == 0 && a.iters) a.iters[tokbase + i] = cnt;
     }
-    return;
+    if (SOLVE) return;  // no readout
   }
   // readout o = e^{l_i} S^G x + sum_j D_ij (x . k_j) v_j  (S^G stored transposed)
   float o[DC];
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
 // the four-lanes-per-row mapping gets; p reaches the lanes through a per-warp buffer in
 // shared memory instead of one shuffle per column.  The state S^H and, after the CG, S^G
 // (transposed) share one padded buffer.
-template <typename TIO, bool SOLVE>
+template <typename TIO, bool SOLVE, bool SAVE>
 __global__ void __launch_bounds__(128, 4) mesa_cg_rows64_kernel(FwdArgs a, FwdWorkspace ws, int NC,
                                                                 SolveArgs sv) {
   constexpr int D = 64, SP = D + 4;
@@ -493,16 +493,16 @@ __global__ void __launch_bounds__(128, 4) mesa_cg_rows64_kernel(FwdArgs a, FwdWo
     }
   }
 
-  if constexpr (SOLVE) {  // the iterate itself, no readout
+  if constexpr (SOLVE || SAVE) {  // the iterate itself
 #pragma unroll
     for (int r = 0; r < 2; r++) {
       if (!valid[r]) continue;
       const size_t base = (tokbase + i0 + r) * D;
 #pragma unroll
       for (int n = 0; n < 8; n++) sv.x_out[base + (n < 4 ? 4 * o + n : 32 + 4 * o + (n - 4))] = x[r][n];
-      if (o == 0 && a.iters) a.iters[tokbase + i0 + r] = cnt[r];
+      if (SOLVE && o == 0 && a.iters) a.iters[tokbase + i0 + r] = cnt[r];
     }
-    return;
+    if (SOLVE) return;  // no readout (the same for the whole block)
   }
   // readout o = e^{l_i} S^G x + sum_j D_ij (x . k_j) v_j, with (S^G)^T in the state buffer
   __syncthreads();  // every warp is done with S^H
@@ -541,7 +541,9 @@ static int launch_rows64_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_
   const int nwarp = (C + 7) / 8;
   const size_t smem = sizeof(float) * (D * (D + 4) + 2 * C * D + nwarp * 8 * D + 2 * C + D);
   if (!a.out && !sv.x_out) return -1;
-  auto kfn = a.out ? mesa_cg_rows64_kernel<TIO, false> : mesa_cg_rows64_kernel<TIO, true>;
+  auto kfn = !a.out    ? mesa_cg_rows64_kernel<TIO, true, false>
+             : sv.x_out ? mesa_cg_rows64_kernel<TIO, false, true>
+                        : mesa_cg_rows64_kernel<TIO, false, false>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_ROWS, st);
@@ -557,7 +559,9 @@ static int launch_rows_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t 
   const int NC = (a.T + C - 1) / C;
   const size_t smem = sizeof(float) * (2 * D * (D + 4) + 2 * C * D + 2 * C + D);
   if (!a.out && !sv.x_out) return -1;
-  auto kfn = a.out ? mesa_cg_rows_kernel<D, TIO, false> : mesa_cg_rows_kernel<D, TIO, true>;
+  auto kfn = !a.out    ? mesa_cg_rows_kernel<D, TIO, true, false>
+             : sv.x_out ? mesa_cg_rows_kernel<D, TIO, false, true>
+                        : mesa_cg_rows_kernel<D, TIO, false, false>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_ROWS, st);

@@ -19,8 +19,8 @@
 namespace mesa {
 
 // SOLVE = true: a solve of the backward pass (right-hand sides sv.rhs or q, the iterate to
-// sv.x_out, no readout); false: the forward.
-template <int D, int R, typename TIO, bool SOLVE>
+// sv.x_out, no readout); false: the forward, with SAVE the iterate also written to sv.x_out.
+template <int D, int R, typename TIO, bool SOLVE, bool SAVE>
 __global__ void __launch_bounds__(256) mesa_cg_simt_kernel(FwdArgs a, FwdWorkspace ws, int NC,
                                                            int RB, SolveArgs sv) {
   constexpr int RPW = R / 8;                 // rows per warp
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(256) mesa_cg_simt_kernel(FwdArgs a, FwdWorkspa
     for (int n = 0; n < DN; n++)
       if (lane + 32 * n < D) Ps[i * D + lane + 32 * n] = X[m][n];
     if (lane == 0 && r0 + i < Cv && a.iters) a.iters[tokbase + r0 + i] = cnt[m];
-    if (SOLVE && r0 + i < Cv) {
+    if ((SOLVE || SAVE) && r0 + i < Cv) {
 #pragma unroll
       for (int n = 0; n < DN; n++)
         if (lane + 32 * n < D) sv.x_out[(tokbase + r0 + i) * D + lane + 32 * n] = X[m][n];
@@ -321,7 +321,9 @@ static int launch_cg_t(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t st
   const size_t smem = sizeof(float) * ((size_t)D * (D + 1) + (size_t)C * (D + 1) + R * D +
                                        2 * (size_t)R * C + C + R);
   if (!a.out && !sv.x_out) return -1;
-  auto kfn = a.out ? mesa_cg_simt_kernel<D, R, TIO, false> : mesa_cg_simt_kernel<D, R, TIO, true>;
+  auto kfn = !a.out    ? mesa_cg_simt_kernel<D, R, TIO, true, false>
+             : sv.x_out ? mesa_cg_simt_kernel<D, R, TIO, false, true>
+                        : mesa_cg_simt_kernel<D, R, TIO, false, false>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_SIMT, st);

@@ -158,10 +158,10 @@ __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, con
 
 }  // namespace
 
-// SOLVE = false: the forward (queries q, readout o = G x).  SOLVE = true: a solve of the
-// backward pass: right-hand sides sv.rhs (fp32) or q, the iterate written to sv.x_out, no
-// readout.
-template <int NTERMS, bool SOLVE>
+// SOLVE = false: the forward (queries q, readout o = G x), with SAVE the iterate also
+// written to sv.x_out (kept for the backward pass).  SOLVE = true: a solve of the backward
+// pass: right-hand sides sv.rhs (fp32) or q, the iterate written to sv.x_out, no readout.
+template <int NTERMS, bool SOLVE, bool SAVE>
 __global__ void __launch_bounds__(512, 1)
     mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, int lookahead, unsigned *status,
                       SolveArgs sv) {
@@ -656,6 +656,14 @@ __global__ void __launch_bounds__(512, 1)
       xx[4 * g4 + 2] = x4.z;
       xx[4 * g4 + 3] = x4.w;
     }
+    if constexpr (SAVE) {
+      if (valid) {
+        float4 *dst = reinterpret_cast<float4 *>(sv.x_out + (tokbase + i) * DH + c0);
+#pragma unroll
+        for (int g4 = 0; g4 < CW / 4; g4++)
+          dst[g4] = make_float4(xx[4 * g4], xx[4 * g4 + 1], xx[4 * g4 + 2], xx[4 * g4 + 3]);
+      }
+    }
     float mx = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < CW; kk++) mx = fmaxf(mx, fabsf(xx[kk]));
@@ -740,7 +748,9 @@ int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *statu
   const int NC = (a.T + TILE - 1) / TILE;
   // a backward-pass solve: no output, the iterate goes to sv.x_out
   if (!a.out && !sv.x_out) return -1;
-  auto kfn = a.out ? mesa_cg_tc_kernel<MESA_TC_TERMS, false> : mesa_cg_tc_kernel<MESA_TC_TERMS, true>;
+  auto kfn = !a.out    ? mesa_cg_tc_kernel<MESA_TC_TERMS, true, false>
+             : sv.x_out ? mesa_cg_tc_kernel<MESA_TC_TERMS, false, true>
+                        : mesa_cg_tc_kernel<MESA_TC_TERMS, false, false>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC) !=
       cudaSuccess)
     return -1;

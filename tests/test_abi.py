@@ -166,12 +166,12 @@ def test_backward_workspace_and_validation(lib):
     p = ctypes.c_void_p(256)
 
     def call(**kw):
-        a = dict(B=2, H=2, T=64, dk=64, dv=64, dt=1, q=p, k=p, v=p, g=p, lam=p, do=p, it=5, tol=0.0, dq=p,
-                 dk_=p, dv_=p, dg=p, dl=p, itf=None, itb=None, ws=p, wsz=1 << 40, st=None)
+        a = dict(B=2, H=2, T=64, dk=64, dv=64, dt=1, q=p, k=p, v=p, g=p, lam=p, do=p, xs=None, it=5, tol=0.0,
+                 dq=p, dk_=p, dv_=p, dg=p, dl=p, itf=None, itb=None, ws=p, wsz=1 << 40, st=None)
         a.update(kw)
         return f(a["B"], a["H"], a["T"], a["dk"], a["dv"], a["dt"], a["q"], a["k"], a["v"], a["g"], a["lam"],
-                 a["do"], a["it"], a["tol"], a["dq"], a["dk_"], a["dv_"], a["dg"], a["dl"], a["itf"], a["itb"],
-                 a["ws"], a["wsz"], a["st"])
+                 a["do"], a["xs"], a["it"], a["tol"], a["dq"], a["dk_"], a["dv_"], a["dg"], a["dl"], a["itf"],
+                 a["itb"], a["ws"], a["wsz"], a["st"])
     assert call(dk=48, dv=48) == 2
     assert call(dv=32) == 2
     assert call(it=-1) == 1
@@ -184,3 +184,6 @@ def test_backward_workspace_and_validation(lib):
     assert call(B=0, H=0) == 0                 # nothing to do, nothing launched
     assert call(q=ctypes.c_void_p(264)) == 1   # operands must be 16-byte aligned
     assert call(dv_=ctypes.c_void_p(264)) == 1
+    assert call(xs=ctypes.c_void_p(264)) == 1   # saved iterates must be 16-byte aligned
+    fs = lib.mesa_forward_chunked_save          # the saved iterates are required
+    assert fs(1, 1, 64, 64, 64, 0, p, p, p, p, p, 4, 0.0, 64, p, None, None, p, 1 << 40, None) == 1

@@ -35,19 +35,26 @@ def _wl(dtype, **kw):
     return synth.workload("bwd_bf16_d128", **kw)
 
 
-def _gpu(inp, dtype, iters, tol):
+def _dev(inp, dtype):
+    import torch
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    return {k: torch.from_numpy(np.ascontiguousarray(inp[k])).cuda().to(td if k in ("q", "k", "v", "dout")
+                                                                        else torch.float32).contiguous()
+            for k in ("q", "k", "v", "gamma", "lam", "dout")}
+
+
+def _gpu(inp, dtype, iters, tol, x_saved=None):
     import torch
 
     from mesa_layer_gb300 import binding
-    td = torch.bfloat16 if dtype == "bf16" else torch.float32
-    t = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).cuda().to(td if k in ("q", "k", "v", "dout")
-                                                                     else torch.float32).contiguous()
-         for k in ("q", "k", "v", "gamma", "lam", "dout")}
+    t = _dev(inp, dtype)
     B, H, T, dk = t["q"].shape
     ws = torch.empty(max(256, binding.mesa_backward_workspace_size(B, H, T, dk, dk)), dtype=torch.uint8,
                      device="cuda")
+    itf = torch.full((B, H, T), -1, dtype=torch.int32, device="cuda")
     dq, dk_, dv, dg, dl, itf, itb = binding.mesa_backward_chunked(t["q"], t["k"], t["v"], t["gamma"], t["lam"],
-                                                                 t["dout"], iters, tol, workspace=ws)
+                                                                 t["dout"], iters, tol, workspace=ws,
+                                                                 iters_fwd=itf, x_saved=x_saved)
     torch.cuda.synchronize()
     assert binding.mesa_forward_status(ws) == 0, "a kernel reported a bounded-wait timeout"
     f = lambda x: x.float().cpu().numpy().astype(np.float64)
@@ -163,3 +170,29 @@ def test_full_workload_sampled_units():
         print(f"bwd full b={b} h={h}: " + ", ".join(f"{k} {v:.2e}" for k, v in e.items()))
         for k, v in e.items():
             assert v <= TOL[w.dtype], f"({b}, {h}) {k} {v:.3e}"
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 128), ("f32", 64), ("bf16", 32)])
+def test_saved_iterates(dtype, d):
+    """mesa_forward_chunked_save gives the forward's outputs bit for bit plus its iterates;
+    the backward from them matches the oracle (and, on the tensor-core path, where the
+    recomputation runs the same kernel on the same chunks, the recomputing backward bit for
+    bit); iters_fwd is then left alone."""
+    import torch
+
+    from mesa_layer_gb300 import binding
+    w = _wl(dtype, B=2, H=2, T=150, dk=d, dv=d)
+    inp = synth.backward_inputs(w, seed=9)
+    t = _dev(inp, dtype)
+    o0, i0 = binding.mesa_forward_chunked(t["q"], t["k"], t["v"], t["gamma"], t["lam"], 10, 0.0, w.chunk)
+    o1, i1, xs = binding.mesa_forward_chunked_save(t["q"], t["k"], t["v"], t["gamma"], t["lam"], 10, 0.0, w.chunk)
+    assert torch.equal(o0, o1) and torch.equal(i0, i1)
+    g1 = _gpu(inp, dtype, 10, 0.0, x_saved=xs)
+    assert np.all(g1["iters_fwd"] == -1)
+    r = oracle.backward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], inp["dout"], 10)
+    g1["iters_fwd"] = r["iters_fwd"]
+    _check(g1, r, dtype, f"bwd saved iterates d={d} {dtype}")
+    if dtype == "bf16" and d == 128:
+        g0 = _gpu(inp, dtype, 10, 0.0)
+        for k in ("dq", "dk", "dv", "dgamma", "dlam"):
+            assert np.array_equal(g0[k], g1[k]), k
