@@ -120,23 +120,6 @@ __device__ __forceinline__ void zero4x4(float (&acc)[4][4]) {
     for (int n = 0; n < 4; n++) acc[m][n] = 0.0f;
 }
 
-// Row-dot of two [BC][D + 4] tiles: sum_a A[i][a] B[j][a].
-template <int D>
-__device__ __forceinline__ float row_dot(const float *A, int i, const float *B, int j) {
-  const float4 *a = reinterpret_cast<const float4 *>(A + i * (D + 4));
-  const float4 *b = reinterpret_cast<const float4 *>(B + j * (D + 4));
-  float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll 4
-  for (int e = 0; e < D / 4; e += 2) {
-    const float4 x = a[e], y = b[e];
-    s0 = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, s0))));
-    if (e + 1 < D / 4) {
-      const float4 x1 = a[e + 1], y1 = b[e + 1];
-      s1 = fmaf(x1.x, y1.x, fmaf(x1.y, y1.y, fmaf(x1.z, y1.z, fmaf(x1.w, y1.w, s1))));
-    }
-  }
-  return s0 + s1;
-}
 }  // namespace
 
 // b = diag(e^l) G S^G_{c-1} + ((G V^T) o D) K.  grid (NC, U), block 2D.
@@ -149,15 +132,49 @@ __global__ void __launch_bounds__(256) mesa_bwd_rhs_kernel(BwdArgs a, FwdWorkspa
   extern __shared__ __align__(16) float smem[];
   float *Gs = smem, *Vs = Gs + BC * SPD, *Ks = Vs + BC * SPD, *Sg = Ks + BC * SPD;
   float *M = Sg + D * SPD, *el = M + BC * SPC;
+  // S^G_{c-1} into registers first: its loads run while the tiles load and M is formed
+  constexpr int NR = D / 8;  // float4 of a D x D state per thread (2D threads)
+  const float *SGp = c > 0 ? ws.SG + ((size_t)u * NC + c - 1) * D * D : nullptr;
+  float4 R[NR];
+#pragma unroll
+  for (int q = 0; q < NR; q++)
+    R[q] = SGp ? reinterpret_cast<const float4 *>(SGp)[threadIdx.x + q * blockDim.x] : make_float4(0, 0, 0, 0);
   load_tile<D>(Gs, (const TIO *)a.dout + tokbase * D, Cv);
   load_tile<D>(Vs, (const TIO *)a.v + tokbase * D, Cv);
   load_tile<D>(Ks, (const TIO *)a.k + tokbase * D, Cv);
-  load_state<D>(Sg, c > 0 ? ws.SG + ((size_t)u * NC + c - 1) * D * D : nullptr, false);
   for (int j = threadIdx.x; j < BC; j += blockDim.x) el[j] = j < Cv ? ws.ell[tokbase + j] : 0.0f;
   __syncthreads();
-  for (int e = threadIdx.x; e < BC * BC; e += blockDim.x) {
-    const int i = e / BC, j = e % BC;
-    M[i * SPC + j] = (j <= i && i < Cv) ? expf(el[i] - el[j]) * row_dot<D>(Gs, i, Vs, j) : 0.0f;
+  // M = (G V^T) o D in 2 x 2 register tiles (rows ti, ti + 16, columns tj, tj + 16)
+  constexpr int HB = BC / 2;
+  for (int tile = threadIdx.x; tile < HB * HB; tile += blockDim.x) {
+    const int ti = tile / HB, tj = tile % HB;
+    float p[2][2] = {{0, 0}, {0, 0}};
+#pragma unroll 2
+    for (int e = 0; e < D; e += 4) {
+      float4 g[2], vv[2];
+#pragma unroll
+      for (int r = 0; r < 2; r++) {
+        g[r] = *reinterpret_cast<const float4 *>(Gs + (ti + HB * r) * SPD + e);
+        vv[r] = *reinterpret_cast<const float4 *>(Vs + (tj + HB * r) * SPD + e);
+      }
+#pragma unroll
+      for (int r = 0; r < 2; r++)
+#pragma unroll
+        for (int q = 0; q < 2; q++)
+          p[r][q] = fmaf(g[r].w, vv[q].w, fmaf(g[r].z, vv[q].z, fmaf(g[r].y, vv[q].y, fmaf(g[r].x, vv[q].x, p[r][q]))));
+    }
+#pragma unroll
+    for (int r = 0; r < 2; r++)
+#pragma unroll
+      for (int q = 0; q < 2; q++) {
+        const int i = ti + HB * r, j = tj + HB * q;
+        M[i * SPC + j] = (j <= i && i < Cv) ? expf(el[i] - el[j]) * p[r][q] : 0.0f;
+      }
+  }
+#pragma unroll
+  for (int q = 0; q < NR; q++) {
+    const int e4 = threadIdx.x + q * blockDim.x;
+    *reinterpret_cast<float4 *>(Sg + ((4 * e4) / D) * SPD + (4 * e4) % D) = R[q];
   }
   __syncthreads();
   const int rg = threadIdx.x / (D / 4), c4 = threadIdx.x % (D / 4);

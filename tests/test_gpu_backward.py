@@ -103,10 +103,14 @@ def test_several_chunks_d128(dtype):
 
 
 def test_single_token_and_zero_gradient():
+    # one token: H + Lambda is Lambda plus one rank-1 term, d distinct eigenvalues, so CG is
+    # run to convergence (d steps); an unconverged fixed-count fp32 iterate of such a spread
+    # spectrum is an ill-conditioned function of rounding (a reordered dot product moved it
+    # from 6e-5 to 1.9e-4 of the unit's scale at 8 steps)
     w = _wl("f32", B=2, H=2, T=1, dk=32, dv=32)
     inp = synth.backward_inputs(w, seed=1)
-    g = _gpu(inp, "f32", 8, 0.0)
-    r = oracle.backward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], inp["dout"], 8)
+    g = _gpu(inp, "f32", 32, 0.0)
+    r = oracle.backward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], inp["dout"], 32)
     _check(g, r, "f32", "bwd T=1")
     assert np.all(g["dgamma"] == 0.0)  # no earlier state
     w = _wl("f32", B=1, H=2, T=40, dk=64, dv=64)
