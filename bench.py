@@ -10,7 +10,9 @@ sequences and heads; for the backward workload one mesa_backward_chunked call (t
 solves recomputed, the second solve per token, the state adjoints and every gradient).  Inputs are resident in HBM before the timed region; the L2 (129 MB) is
 flushed by a 256 MiB device write between timed steps unless the step's working set is
 larger than L2.  Kernel times come from CUDA events on the launching stream; `e2e` repeats
-the measurement through the same C-ABI call with pinned host buffers, copies included.
+the measurement through the same C-ABI call with pinned host buffers, every step's host-to-
+device upload of its inputs and download of its results inside the timed region (uploads
+double-buffered on a second stream, so that step i+1's upload overlaps step i's compute).
 Under torchrun every rank runs its own replica (independent sequences, no collective) and
 `value` is the aggregate over ranks with the max-over-ranks time.
 
@@ -469,39 +471,63 @@ def bench_forward(args, w, rank, world, dev, lib, torch, binding):
     return res
 
 
+def pipelined_e2e(torch, dev, host_in: dict, run, host_out: dict, steps: int, warmup: int = 3):
+    """Time `steps` end-to-end steps: each copies its inputs from pinned host memory to the
+    device, runs the call, and copies its results back to pinned host memory.  Inputs are
+    double-buffered on the device and uploaded on a second stream, so that step i+1's upload
+    overlaps step i's compute and download (as a caller streaming batches would run it).
+    `run(d_in, stream)` launches the call on `stream` and returns the device results, matched
+    by name to `host_out`.  Returns ms per step (first upload issued to last download done)."""
+    s_copy, s_comp = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    bufs = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
+    for e in free:
+        e.record(s_comp)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    n_all = warmup + steps
+    for i in range(n_all):
+        b = i % 2
+        if i == warmup:
+            torch.cuda.synchronize()
+            start.record(s_copy)
+        with torch.cuda.stream(s_copy):
+            s_copy.wait_event(free[b])  # the compute that read this buffer is done
+            for k, v in host_in.items():
+                bufs[b][k].copy_(v, non_blocking=True)
+            ready[b].record(s_copy)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ready[b])
+            out = run(bufs[b], s_comp)
+            for k, v in host_out.items():
+                v.copy_(out[k], non_blocking=True)
+            free[b].record(s_comp)
+    end.record(s_comp)
+    s_comp.wait_stream(s_copy)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
 def e2e_forward(args, w, dev, torch, binding, inp, td, ws):
     """Same call through the C ABI with pinned host buffers: H2D of q, k, v, gamma and D2H of
-    out and iters_used inside the timed region of every step."""
+    out and iters_used inside the timed region of every step (uploads double-buffered)."""
     h = {k: torch.from_numpy(inp[k]).to(td if k in ("q", "k", "v") else torch.float32).pin_memory()
          for k in ("q", "k", "v", "gamma")}
     lam = torch.from_numpy(inp["lam"]).to(dev)
-    d = {k: torch.empty_like(h[k], device=dev) for k in h}
     out = torch.empty((w.B, w.H, w.T, w.dv), dtype=td, device=dev)
     iters = torch.empty((w.B, w.H, w.T), dtype=torch.int32, device=dev)
-    h_out = torch.empty(out.shape, dtype=td).pin_memory()
-    h_it = torch.empty(iters.shape, dtype=torch.int32).pin_memory()
+    h_out = {"out": torch.empty(out.shape, dtype=td).pin_memory(),
+             "iters": torch.empty(iters.shape, dtype=torch.int32).pin_memory()}
     h2d = sum(t.numel() * t.element_size() for t in h.values())
-    d2h = h_out.numel() * h_out.element_size() + h_it.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
-    def step():
-        for k in h:
-            d[k].copy_(h[k], non_blocking=True)
+    def run(d, stream):
         binding.mesa_forward_chunked(d["q"], d["k"], d["v"], d["gamma"], lam, w.cg_iters, w.cg_tol, w.chunk,
-                                     out=out, iters_used=iters, workspace=ws)
-        h_out.copy_(out, non_blocking=True)
-        h_it.copy_(iters, non_blocking=True)
+                                     out=out, iters_used=iters, workspace=ws, stream=stream)
+        return {"out": out, "iters": iters}
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    n = max(3, min(args.steps, 50))
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(n):
-        step()
-    e.record()
-    torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / n
+    ms = pipelined_e2e(torch, dev, h, run, h_out, max(3, min(args.steps, 50)), max(3, args.warmup))
     return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h}
 
 
@@ -593,28 +619,16 @@ def bench_preprocess(args, w, rank, world, dev, lib, torch, binding):
     res.update({"iters": np.zeros(1, dtype=np.int32), "tokens_per_step": w.B * w.T, "flush": needs_flush})
     if not args.no_e2e:
         h = {k: torch.from_numpy(inp[k]).to(td).pin_memory() for k in ("q_raw", "k_raw")}
-        d = {k: torch.empty_like(h[k], device=dev) for k in h}
-        hq, hk = torch.empty_like(h["q_raw"]).pin_memory(), torch.empty_like(h["k_raw"]).pin_memory()
+        back = {"q": torch.empty_like(h["q_raw"]).pin_memory(), "k": torch.empty_like(h["k_raw"]).pin_memory()}
 
-        def estep():
-            for k in h:
-                d[k].copy_(h[k], non_blocking=True)
-            binding.mesa_qk_preprocess(d["q_raw"], d["k_raw"], d_in["wq"], d_in["wk"], q_out=qo, k_out=ko)
-            hq.copy_(qo, non_blocking=True)
-            hk.copy_(ko, non_blocking=True)
+        def run(d, stream):
+            binding.mesa_qk_preprocess(d["q_raw"], d["k_raw"], d_in["wq"], d_in["wk"], q_out=qo, k_out=ko,
+                                       stream=stream)
+            return {"q": qo, "k": ko}
 
-        for _ in range(3):
-            estep()
-        torch.cuda.synchronize()
-        n = max(3, min(args.steps, 50))
-        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s_.record()
-        for _ in range(n):
-            estep()
-        e_.record()
-        torch.cuda.synchronize()
+        ms = pipelined_e2e(torch, dev, h, run, back, max(3, min(args.steps, 50)))
         nb = sum(t.numel() * t.element_size() for t in h.values())
-        res["e2e"] = {"ms_per_step": s_.elapsed_time(e_) / n, "h2d": nb, "d2h": nb}
+        res["e2e"] = {"ms_per_step": ms, "h2d": nb, "d2h": nb}
     return res
 
 
@@ -667,28 +681,15 @@ def bench_backward(args, w, rank, world, dev, lib, torch, binding):
         h = {k: torch.from_numpy(inp[k]).to(td if k in ("q", "k", "v", "dout") else torch.float32).pin_memory()
              for k in keys}
         h["x_saved"] = xs.cpu().pin_memory()
-        d = {k: torch.empty_like(h[k], device=dev) for k in h}
         back = {k: torch.empty(outs[k].shape, dtype=outs[k].dtype).pin_memory() for k in ("dq", "dk", "dv", "dgamma", "dlambda")}
 
-        def estep():
-            for k in h:
-                d[k].copy_(h[k], non_blocking=True)
-            call(d, d["x_saved"])
-            for k in back:
-                back[k].copy_(outs[k], non_blocking=True)
+        def run(d, stream):
+            binding.mesa_backward_chunked(d["q"], d["k"], d["v"], d["gamma"], d_in["lam"], d["dout"], w.cg_iters,
+                                          w.cg_tol, workspace=ws, x_saved=d["x_saved"], stream=stream, **outs)
+            return outs
 
-        for _ in range(3):
-            estep()
-        torch.cuda.synchronize()
-        n = max(3, min(args.steps, 20))
-        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s_.record()
-        for _ in range(n):
-            estep()
-        e_.record()
-        torch.cuda.synchronize()
-        res["e2e"] = {"ms_per_step": s_.elapsed_time(e_) / n,
-                      "h2d": sum(t.numel() * t.element_size() for t in h.values()),
+        ms = pipelined_e2e(torch, dev, h, run, back, max(3, min(args.steps, 20)))
+        res["e2e"] = {"ms_per_step": ms, "h2d": sum(t.numel() * t.element_size() for t in h.values()),
                       "d2h": sum(t.numel() * t.element_size() for t in back.values())}
     return res
 
