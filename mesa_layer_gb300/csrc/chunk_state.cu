@@ -6,7 +6,8 @@
 // the state after the chunk is
 //     S_c = e^{l_{C-1}} S_{c-1} + sum_j e^{l_{C-1} - l_j} x_j k_j^T       (x = k for H, v for G)
 // (unrolling H_t = gamma_t H_{t-1} + k_t k_t^T over the chunk).  Three kernels:
-//   mesa_ell_kernel    l_i per token (block scan of log gates inside each chunk);
+//   mesa_ell_kernel    l_i per token (block scan of log gates inside each chunk; on the fp32
+//                      path mesa_delta_kernel computes them itself and writes them out);
 //   mesa_delta_kernel  the chunk-local sums  sum_j w_j x_j k_j^T  for every chunk, in parallel;
 //   mesa_scan_kernel   the chunk-level prefix scan S_c = a_c S_{c-1} + Delta_c, in place,
 //                      parallel over state entries, sequential over chunks.
@@ -15,54 +16,77 @@
 
 namespace mesa {
 
+// l_i of token i of chunk c (threads 0..127 of the block, chunk <= 128): an inclusive scan
+// of the log gates, by warps and then across the four warps.  Every thread of the block must
+// call it (it holds a barrier); threads >= 128 get 0.  wsum: 4 floats of shared memory.
+__device__ __forceinline__ float chunk_log_decay(const float *__restrict__ gamma, int T, int C,
+                                                 int c, int u, float *wsum, bool &valid) {
+  const int i = threadIdx.x, t = c * C + i;
+  valid = (i < C) && (i < 128) && (t < T);
+  float v = valid ? log_gate(gamma[(size_t)u * T + t]) : 0.0f;
+  const int lane = i & 31, warp = i >> 5;
+  if (i < 128) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float n = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += n;
+    }
+    if (lane == 31) wsum[warp] = v;
+  }
+  __syncthreads();
+  if (i < 128)
+    for (int w = 0; w < warp; w++) v += wsum[w];
+  return v;
+}
+
 // grid (NC, U), block 128 (>= chunk).  ell[u, t] for every token of chunk c.
 __global__ void __launch_bounds__(128) mesa_ell_kernel(const float *__restrict__ gamma,
                                                        float *__restrict__ ell, int T, int C) {
-  const int c = blockIdx.x, u = blockIdx.y, i = threadIdx.x;
-  const int t = c * C + i;
-  const bool valid = (i < C) && (t < T);
-  float v = valid ? log_gate(gamma[(size_t)u * T + t]) : 0.0f;
-  // inclusive scan over the block
-  const int lane = i & 31, warp = i >> 5;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
   __shared__ float wsum[4];
-  if (lane == 31) wsum[warp] = v;
-  __syncthreads();
-  for (int w = 0; w < warp; w++) v += wsum[w];
-  if (valid) ell[(size_t)u * T + t] = v;
+  bool valid;
+  const float v = chunk_log_decay(gamma, T, C, blockIdx.x, blockIdx.y, wsum, valid);
+  if (valid) ell[(size_t)blockIdx.y * T + blockIdx.x * C + threadIdx.x] = v;
 }
 
 // grid (NC, U, 2): z = 0 builds Delta^H = sum_j w_j k_j k_j^T, z = 1 builds
 // Delta^G = sum_j w_j v_j k_j^T, w_j = e^{l_last - l_j}.  Block 256; each thread owns a
 // (D/16) x (D/16) register tile of the D x D result.
+// The chunk's log-decays are computed here as well (chunk_log_decay, the same arithmetic as
+// mesa_ell_kernel) and written to ws.ell by the z = 0 blocks: the later kernels read them
+// there.
 template <int D, typename TIO>
 __global__ void __launch_bounds__(256) mesa_delta_kernel(const TIO *__restrict__ k,
                                                          const TIO *__restrict__ v,
-                                                         const float *__restrict__ ell,
+                                                         const float *__restrict__ gamma,
                                                          FwdWorkspace ws, int T, int C) {
-  constexpr int TM = D / 16;
   extern __shared__ __align__(16) float smem[];
   float *Xs = smem;              // [C, D] rows x_j (k or v)
   float *Ks = smem + C * D;      // [C, D] rows k_j
   float *wv = smem + 2 * C * D;  // [C]
+  float *ls = wv + C;            // [C]  l_j
+  __shared__ float wsum[4];
   const int c = blockIdx.x, u = blockIdx.y, isG = blockIdx.z;
   const int NC = gridDim.x;
   const int t0 = c * C;
   const int Cv = min(C, T - t0);
   const size_t base = ((size_t)u * T + t0) * D;
   const TIO *X = isG ? v : k;
+  {
+    bool valid;
+    const float l = chunk_log_decay(gamma, T, C, c, u, wsum, valid);
+    if (valid) {
+      ls[threadIdx.x] = l;
+      if (!isG) ws.ell[(size_t)u * T + t0 + threadIdx.x] = l;
+    }
+  }
 #pragma unroll 4
   for (int e = threadIdx.x; e < Cv * D; e += blockDim.x) {
     Ks[e] = ld(k, base + e);
     Xs[e] = ld(X, base + e);
   }
-  const float lend = ell[(size_t)u * T + t0 + Cv - 1];
-  for (int j = threadIdx.x; j < Cv; j += blockDim.x)
-    wv[j] = expf(lend - ell[(size_t)u * T + t0 + j]);
+  __syncthreads();
+  const float lend = ls[Cv - 1];
+  for (int j = threadIdx.x; j < Cv; j += blockDim.x) wv[j] = expf(lend - ls[j]);
   __syncthreads();
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   float *S = (isG ? ws.SG : ws.SH) + ((size_t)u * NC + c) * D * D;
@@ -122,19 +146,19 @@ static int launch_states_t(const FwdArgs &a, const FwdWorkspace &ws, unsigned *t
                            cudaStream_t st) {
   const int U = a.B * a.H;
   const int NC = (a.T + a.chunk - 1) / a.chunk;
-  timing_mark_begin(K_ELL, st);
-  mesa_ell_kernel<<<dim3(NC, U), 128, 0, st>>>(a.gamma, ws.ell, a.T, a.chunk);
-  timing_mark_end(K_ELL, st);
   if (tc_status) {  // chunk sums and the chunk-level scan on the tensor cores
+    timing_mark_begin(K_ELL, st);
+    mesa_ell_kernel<<<dim3(NC, U), 128, 0, st>>>(a.gamma, ws.ell, a.T, a.chunk);
+    timing_mark_end(K_ELL, st);
     return launch_states_tc(a, ws, tc_status, st);
-  } else {
-    const size_t smem = (size_t)(2 * a.chunk * D + a.chunk) * sizeof(float);
+  } else {  // the log-decays are computed by the chunk-sum kernel
+    const size_t smem = (size_t)(2 * a.chunk * D + 2 * a.chunk) * sizeof(float);
     auto kd = mesa_delta_kernel<D, TIO>;
     if (cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return -1;
     timing_mark_begin(K_DELTA, st);
-    kd<<<dim3(NC, U, 2), 256, smem, st>>>((const TIO *)a.k, (const TIO *)a.v, ws.ell, ws, a.T,
+    kd<<<dim3(NC, U, 2), 256, smem, st>>>((const TIO *)a.k, (const TIO *)a.v, a.gamma, ws, a.T,
                                           a.chunk);
     timing_mark_end(K_DELTA, st);
   }
