@@ -53,8 +53,8 @@ __global__ void __launch_bounds__(128) mesa_ell_kernel(const float *__restrict__
 // (D/16) x (D/16) register tile of the D x D result.
 // The chunk's log-decays are computed here as well (chunk_log_decay, the same arithmetic as
 // mesa_ell_kernel) and written to ws.ell by the z = 0 blocks: the later kernels read them
-// there.
-template <int D, typename TIO>
+// there.  VEC: k and v are 16-byte aligned, rows are loaded four elements at a time.
+template <int D, typename TIO, bool VEC>
 __global__ void __launch_bounds__(256) mesa_delta_kernel(const TIO *__restrict__ k,
                                                          const TIO *__restrict__ v,
                                                          const float *__restrict__ gamma,
@@ -79,10 +79,18 @@ __global__ void __launch_bounds__(256) mesa_delta_kernel(const TIO *__restrict__
       if (!isG) ws.ell[(size_t)u * T + t0 + threadIdx.x] = l;
     }
   }
+  if constexpr (VEC) {
 #pragma unroll 4
-  for (int e = threadIdx.x; e < Cv * D; e += blockDim.x) {
-    Ks[e] = ld(k, base + e);
-    Xs[e] = ld(X, base + e);
+    for (int e4 = threadIdx.x; e4 < Cv * D / 4; e4 += blockDim.x) {
+      reinterpret_cast<float4 *>(Ks)[e4] = load4(k, base + 4 * (size_t)e4);
+      reinterpret_cast<float4 *>(Xs)[e4] = load4(X, base + 4 * (size_t)e4);
+    }
+  } else {
+#pragma unroll 4
+    for (int e = threadIdx.x; e < Cv * D; e += blockDim.x) {
+      Ks[e] = ld(k, base + e);
+      Xs[e] = ld(X, base + e);
+    }
   }
   __syncthreads();
   const float lend = ls[Cv - 1];
@@ -153,7 +161,8 @@ static int launch_states_t(const FwdArgs &a, const FwdWorkspace &ws, unsigned *t
     return launch_states_tc(a, ws, tc_status, st);
   } else {  // the log-decays are computed by the chunk-sum kernel
     const size_t smem = (size_t)(2 * a.chunk * D + 2 * a.chunk) * sizeof(float);
-    auto kd = mesa_delta_kernel<D, TIO>;
+    const bool vec = ((uintptr_t)a.k % 16 == 0) && ((uintptr_t)a.v % 16 == 0);
+    auto kd = vec ? mesa_delta_kernel<D, TIO, true> : mesa_delta_kernel<D, TIO, false>;
     if (cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
       return -1;

@@ -179,3 +179,42 @@ def test_initial_and_final_states():
     o1, _ = gpu_forward(first, w.dtype, w.cg_iters, 0.0, 32, H_final=H1, G_final=G1)
     o2, _ = gpu_forward(second, w.dtype, w.cg_iters, 0.0, 64, H0=H1, G0=G1)
     assert unit_err(np.concatenate([o1, o2], axis=2), ro).max() <= TOL["f32"]
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("f32", 16), ("bf16", 128)])
+def test_unaligned_inputs(dtype, d):
+    """q, k, v starting 4 (fp32) or 2 (bf16) bytes past a 16-byte boundary: the fp32 path
+    takes its element-wise loads (bit for bit the aligned result), and bf16 d = 128 leaves
+    the tensor-core path for the CUDA-core one (checked against the oracle)."""
+    import torch
+
+    from mesa_layer_gb300 import binding
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    w = synth.workload("fwd_fp32_d64" if dtype == "f32" else "fwd_bf16_d128", B=1, H=2, T=100, dk=d, dv=d,
+                       cg_tol=0.0, cg_iters=8)
+    inp = synth.forward_inputs(w, seed=3)
+
+    def shifted(x):
+        flat = torch.from_numpy(np.ascontiguousarray(x)).to(td).reshape(-1)
+        buf = torch.empty(flat.numel() + 1, dtype=td, device="cuda")
+        view = buf[1:].view(x.shape)
+        view.copy_(flat.view(x.shape))
+        assert view.data_ptr() % 16 != 0
+        return view
+
+    al = {k: torch.from_numpy(inp[k]).cuda().to(td).contiguous() for k in ("q", "k", "v")}
+    un = {k: shifted(inp[k]) for k in ("q", "k", "v")}
+    g = torch.from_numpy(inp["gamma"]).cuda()
+    lam = torch.from_numpy(inp["lam"]).cuda()
+    o_al, i_al = binding.mesa_forward_chunked(al["q"], al["k"], al["v"], g, lam, 8, 0.0, w.chunk)
+    out_un = torch.empty((1, 2, 100, d), dtype=td, device="cuda")
+    o_un, i_un = binding.mesa_forward_chunked(un["q"], un["k"], un["v"], g, lam, 8, 0.0, w.chunk, out=out_un)
+    torch.cuda.synchronize()
+    assert torch.equal(i_al, i_un)
+    if dtype == "f32":
+        assert torch.equal(o_al, o_un)
+    else:
+        ro, rit = oracle.forward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], 8)
+        assert np.array_equal(i_un.cpu().numpy(), rit)
+        err = unit_err(o_un.float().cpu().numpy(), ro).max()
+        assert err <= TOL["bf16"], err
