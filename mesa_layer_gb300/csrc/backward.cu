@@ -287,8 +287,8 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
   float *part = Cm + BC * SPC;         // [BC][NQ + 1] per-thread partial row sums
   float *el = part + BC * (NQ + 1);    // [BC] l_i
   float *wv = el + BC;                 // [BC] w_j
-  float *rowi = wv + BC;               // [BC] e^{l_t} (g_t . S^G x_t - y_t . S^H x_t)
-  float *coli = rowi + BC;             // [BC] w_s (v_s . dG k_s + k_s . dH k_s)
+  float *rowi = wv + BC;               // [BC] g_t . S^G x_t - y_t . S^H x_t (times e^{l_t} where used)
+  float *coli = rowi + BC;             // [BC] v_s . dG k_s + k_s . dH k_s (times w_s where used)
   float *red = coli + BC;              // [2D] block-reduction scratch
   const int tid = threadIdx.x, nt = blockDim.x;
   const int rg = tid / NQ, c4 = tid % NQ;
