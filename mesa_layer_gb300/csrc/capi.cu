@@ -365,7 +365,8 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
   };
   // x_t (the forward's solves, unless kept), b_t = G_t^T g_t, y_t, then the gradients
   if (!x_saved && solve(nullptr, Xw, iters_fwd) != 0) return MESA_ERR_CUDA;
-  if (mesa::launch_bwd_rhs(ba, ws, stream) != 0) return MESA_ERR_CUDA;
+  if ((tc ? mesa::launch_rhs_tc(a128, ws128, status, stream, dout, Bv) : mesa::launch_bwd_rhs(ba, ws, stream)) != 0)
+    return MESA_ERR_CUDA;
   if (solve(Bv, Y, iters_bwd) != 0) return MESA_ERR_CUDA;
   if (mesa::launch_bwd_grads(ba, ws, stream) != 0) return MESA_ERR_CUDA;
   return MESA_OK;

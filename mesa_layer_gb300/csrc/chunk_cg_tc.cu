@@ -161,7 +161,12 @@ __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, con
 // SOLVE = false: the forward (queries q, readout o = G x), with SAVE the iterate also
 // written to sv.x_out (kept for the backward pass).  SOLVE = true: a solve of the backward
 // pass: right-hand sides sv.rhs (fp32) or q, the iterate written to sv.x_out, no readout.
-template <int NTERMS, bool SOLVE, bool SAVE>
+// RHS = true (with cg_iters = 0): the readout alone, of the right-hand sides of the backward
+// pass's second solve, b_t = G_t^T g_t = e^{l_t} S^G^T g_t + sum_{j<=t} D_tj (g_t . v_j) k_j:
+// the readout's rows are g (a.q = dout), its keys v (a.k = v), its values k (a.v = k), and
+// its state product g S^G reads the staged S^G as an MN-major operand (the transpose of the
+// forward's x S^G^T); b is written in fp32 to sv.x_out.
+template <int NTERMS, bool SOLVE, bool SAVE, bool RHS>
 __global__ void __launch_bounds__(512, 1)
     mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, int lookahead, unsigned *status,
                       SolveArgs sv) {
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(512, 1)
   float sS, sK;
   {
     tc::Mat32 S;
-    tc::load_mat(SH, CH, cf, S);
+    tc::load_mat(RHS ? nullptr : SH, RHS ? nullptr : CH, cf, S);  // (RHS: no CG, no S^H)
     float mS = tc::mat_absmax(S), mK = tc::rows_absmax(kr, nullptr), unused = 0.0f;
     tc::block_max3(mS, mK, unused, m->red);
     sS = 1.0f / tc::pow2_ceil(mS);
@@ -396,13 +401,19 @@ __global__ void __launch_bounds__(512, 1)
   // U (cols 0..127) = P S, committed to barrier U.  Issued by lane 0 of warp 4 once W is
   // complete: warp 4 lies above the diagonal and has no Z to build, so it may stall while
   // the tensor pipe's queue is full without holding up the warps that build Z.
+  // (RHS: the state read MN-major, k-step s = rows 16 s .. 16 s + 15 of the staged tile)
+  auto sdesc = [&](uint32_t off, int s) -> uint64_t {
+    if constexpr (RHS) return tc::mnmajor_desc(sbase + off, TILE, 0) + (uint64_t)(s * (2048 / 16));
+    else return kdesc(off, s);
+  };
+  const uint32_t id_s = RHS ? tc::idesc_f16(TILE, DH, false, true) : id_kk;
   auto issue_U = [&]() {
 #pragma unroll
     for (int s = 0; s < 8; s++) {
-      tc::mma_f16_ts(tbase + COL_U, tbase + COL_PH + 8 * s, kdesc(OFF_SHI, s), id_kk, s > 0);
+      tc::mma_f16_ts(tbase + COL_U, tbase + COL_PH + 8 * s, sdesc(OFF_SHI, s), id_s, s > 0);
       if (NTERMS == 2) {
-        tc::mma_f16_ts(tbase + COL_U, tbase + COL_PH + 8 * s, kdesc(OFF_SLO, s), id_kk, true);
-        tc::mma_f16_ts(tbase + COL_U, tbase + COL_PL + 8 * s, kdesc(OFF_SHI, s), id_kk, true);
+        tc::mma_f16_ts(tbase + COL_U, tbase + COL_PH + 8 * s, sdesc(OFF_SLO, s), id_s, true);
+        tc::mma_f16_ts(tbase + COL_U, tbase + COL_PL + 8 * s, sdesc(OFF_SHI, s), id_s, true);
       }
     }
     tc::mma_commit(aBarU);
@@ -648,13 +659,24 @@ __global__ void __launch_bounds__(512, 1)
   if (!SOLVE && !failed) {
     tc::prefetch_l2(v + tokbase * DH, sizeof(__nv_bfloat16) * DH * Tv);  // the value tile
     float xx[CW];
+    if constexpr (RHS) {  // the rows g_t of the incoming gradient (bf16, a.q)
+      const uint4 *src = reinterpret_cast<const uint4 *>(q + (tokbase + i) * DH + c0);
 #pragma unroll
-    for (int g4 = 0; g4 < CW / 4; g4++) {
-      const float4 x4 = *reinterpret_cast<const float4 *>(Xs + x_offset(i, c0 + 4 * g4));
-      xx[4 * g4] = x4.x;
-      xx[4 * g4 + 1] = x4.y;
-      xx[4 * g4 + 2] = x4.z;
-      xx[4 * g4 + 3] = x4.w;
+      for (int g = 0; g < NV; g++) {
+        const uint4 raw = valid ? src[g] : make_uint4(0, 0, 0, 0);
+        const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&raw);
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) xx[g * 8 + kk] = __bfloat162float(b[kk]);
+      }
+    } else {
+#pragma unroll
+      for (int g4 = 0; g4 < CW / 4; g4++) {
+        const float4 x4 = *reinterpret_cast<const float4 *>(Xs + x_offset(i, c0 + 4 * g4));
+        xx[4 * g4] = x4.x;
+        xx[4 * g4 + 1] = x4.y;
+        xx[4 * g4 + 2] = x4.z;
+        xx[4 * g4 + 3] = x4.w;
+      }
     }
     if constexpr (SAVE) {
       if (valid) {
@@ -711,7 +733,14 @@ __global__ void __launch_bounds__(512, 1)
         tc::tmem_ld<CW>(tl + COL_U, uu);
         tc::tmem_ld<CW>(tl + COL_W, yy);
         tc::tmem_ld_wait();
-        if (valid) {
+        if (valid && RHS) {  // b in fp32
+          float4 *outf = reinterpret_cast<float4 *>(sv.x_out + (tokbase + i) * DH + c0);
+#pragma unroll
+          for (int g4 = 0; g4 < CW / 4; g4++)
+            outf[g4] = make_float4(fmaf(fu, uu[4 * g4], fy * yy[4 * g4]), fmaf(fu, uu[4 * g4 + 1], fy * yy[4 * g4 + 1]),
+                                   fmaf(fu, uu[4 * g4 + 2], fy * yy[4 * g4 + 2]),
+                                   fmaf(fu, uu[4 * g4 + 3], fy * yy[4 * g4 + 3]));
+        } else if (valid) {
           __nv_bfloat16 *out = (__nv_bfloat16 *)a.out + (tokbase + i) * DH + c0;
 #pragma unroll
           for (int g = 0; g < NV; g++) {
@@ -748,15 +777,38 @@ int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *statu
   const int NC = (a.T + TILE - 1) / TILE;
   // a backward-pass solve: no output, the iterate goes to sv.x_out
   if (!a.out && !sv.x_out) return -1;
-  auto kfn = !a.out    ? mesa_cg_tc_kernel<MESA_TC_TERMS, true, false>
-             : sv.x_out ? mesa_cg_tc_kernel<MESA_TC_TERMS, false, true>
-                        : mesa_cg_tc_kernel<MESA_TC_TERMS, false, false>;
+  auto kfn = !a.out    ? mesa_cg_tc_kernel<MESA_TC_TERMS, true, false, false>
+             : sv.x_out ? mesa_cg_tc_kernel<MESA_TC_TERMS, false, true, false>
+                        : mesa_cg_tc_kernel<MESA_TC_TERMS, false, false, false>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC) !=
       cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_TC, st);
   kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(a, ws, NC, sm_count(), status, sv);
   timing_mark_end(K_CG_TC, st);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_rhs_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st,
+                  const void *dout, float *b) {
+  const int U = a.B * a.H;
+  const int NC = (a.T + TILE - 1) / TILE;
+  FwdArgs r = a;  // the readout's rows, keys and values: dout, v, k
+  r.q = dout;
+  r.k = a.v;
+  r.v = a.k;
+  r.cg_iters = 0;
+  r.iters = nullptr;
+  r.out = b;
+  SolveArgs sv;
+  sv.x_out = b;
+  auto kfn = mesa_cg_tc_kernel<MESA_TC_TERMS, false, false, true>;
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC) !=
+      cudaSuccess)
+    return -1;
+  timing_mark_begin(K_BWD_RHS, st);
+  kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(r, ws, NC, sm_count(), status, sv);
+  timing_mark_end(K_BWD_RHS, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 

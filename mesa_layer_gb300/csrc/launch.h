@@ -91,6 +91,10 @@ int launch_chunk_cg_rows(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t 
 // must have been built with chunk = 128).  Bounded-wait failures set bits in *status.
 int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st,
                        const SolveArgs &sv = SolveArgs());
+// The right-hand sides b_t = G_t^T dout_t of the backward pass's second solve on the tensor
+// cores (bf16, d = 128, the 128-token states of ws), written to b [U, T, dk] fp32.
+int launch_rhs_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st,
+                  const void *dout, float *b);
 int launch_tc_selftest(const float *A, const float *B, float *C1, float *C2, float *C3,
                        unsigned *status, cudaStream_t st);
 // Chunk-boundary states on the tensor cores (bf16 inputs, d = 128, 128-token chunks):
