@@ -282,12 +282,12 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
   const size_t tokbase = (size_t)u * T + t0;
   extern __shared__ __align__(16) float smem[];
   float *Ks = smem, *Vs = Ks + BC * SPD, *Gs = Vs + BC * SPD, *Xs = Gs + BC * SPD;
-  float *Ys = Xs + BC * SPD, *St = Ys + BC * SPD;
+  float *Ys = Xs + BC * SPD, *Bs = Ys + BC * SPD, *St = Bs + BC * SPD;  // Bs: b_t rows
   float *M1 = St + D * SPD, *M2 = M1 + BC * SPC, *M3 = M2 + BC * SPC, *Cm = M3 + BC * SPC;
   float *part = Cm + BC * SPC;         // [BC][NQ + 1] per-thread partial row sums
   float *el = part + BC * (NQ + 1);    // [BC] l_i
   float *wv = el + BC;                 // [BC] w_j
-  float *rowi = wv + BC;               // [BC] g_t . S^G x_t - y_t . S^H x_t (times e^{l_t} where used)
+  float *rowi = wv + BC;               // [BC] e^{l_t} (g_t . S^G x_t - y_t . S^H x_t)
   float *coli = rowi + BC;             // [BC] v_s . dG k_s + k_s . dH k_s (times w_s where used)
   float *red = coli + BC;              // [2D] block-reduction scratch
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
     cc = tr ? 4 * (e4 / D) : (4 * e4) % D;
   };
   auto fetch = [&](int kind) {
+    if (kind == 3 && last) return;  // S^G is needed only next to dG (the pair sum)
     const float *S = src(kind);
     const bool tr = transposed(kind);
 #pragma unroll
@@ -344,6 +345,7 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
   load_tile<D>(Gs, (const TIO *)a.dout + tokbase * D, Cv);
   load_tile<D>(Xs, a.X + tokbase * D, Cv);
   load_tile<D>(Ys, a.Y + tokbase * D, Cv);
+  if (!first) load_tile<D>(Bs, a.rhs + tokbase * D, Cv);
   for (int j = tid; j < BC; j += nt) el[j] = j < Cv ? ws.ell[tokbase + j] : 0.0f;
   __syncthreads();
   const float lend = el[Cv - 1];
@@ -412,14 +414,16 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
   // latency).  Kinds, with t the C x D product and rows s (or t) of the chunk:
   //   1 dG^T: t = K dG^T, rows (dG k_s)^T      dv += w t,  col += t . v_s
   //   2 dG  : t = V dG,   rows (dG^T v_s)^T    dk += w t
-  //   3 S^G : t = G S^G,  rows (S^G^T g_t)^T   row += t . x_t
+  //   3 S^G : no product: e^{l_t} S^G^T g_t is the inter-chunk part of the right-hand side
+  //           b_t = G_t^T g_t of the second solve, so row += x_t . (b_t - (M1 K)_t) with the
+  //           intra-chunk part M1 K (C x C x D); S^G itself is read only for <dG, S^G>
   //   4 dH  : t = K dH,   rows (dH^T k_s)^T    dk += w t
   //   5 S^H : t = X S^H,  rows (S^H x_t)^T     row -= t . y_t      (S^H symmetric)
   //   6 dH^T: t = K dH^T, rows (dH k_s)^T      dk += w t,  col += t . k_s
   // The adjoints dG^c, dH^c are zero after the last chunk and the states S_{c-1} before the
   // first: those kinds are skipped.  While St holds dG (dH) and the registers S^G (S^H),
   // their Frobenius product, the pairs across the whole chunk, is taken on the way.
-  float colp[4] = {0, 0, 0, 0}, rowp[4] = {0, 0, 0, 0}, thr = 0.0f;
+  float colp[4] = {0, 0, 0, 0}, rowp[4] = {0, 0, 0, 0}, rowq[4] = {0, 0, 0, 0}, thr = 0.0f;
   auto dot_rows = [&](float (&acc)[4], const float *Z, float sign) {
 #pragma unroll
     for (int m = 0; m < 4; m++) {
@@ -436,16 +440,27 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
   for (int i = 0; i < ns; i++) {
     const int kind = kinds[i];
     __syncthreads();  // every thread is done with the previous contents of St
-    commit(kind);
+    if (kind != 3) commit(kind);
     __syncthreads();
     const int next = i + 1 < ns ? kinds[i + 1] : 0;
     if (next) fetch(next);
     zero4x4(t);
-    const float *A = (kind == 2) ? Vs : (kind == 3) ? Gs : (kind == 5) ? Xs : Ks;
-    mm_acc_rows(t, A, SPD, rg, St, SPD, c4, D);
+    if (kind == 3) {  // t = M1 K, then row += x_t . (b_t - t_t)
+      mm_acc(t, M1, SPC, 1, rg, Ks, SPD, c4, BC);
+#pragma unroll
+      for (int m = 0; m < 4; m++) {
+        const int r = rg + 8 * m;
+        const float4 x = *reinterpret_cast<const float4 *>(Xs + r * SPD + 4 * c4);
+        const float4 b = *reinterpret_cast<const float4 *>(Bs + r * SPD + 4 * c4);
+        rowq[m] += x.x * (b.x - t[m][0]) + x.y * (b.y - t[m][1]) + x.z * (b.z - t[m][2]) +
+                   x.w * (b.w - t[m][3]);
+      }
+    } else {
+      const float *A = (kind == 2) ? Vs : (kind == 5) ? Xs : Ks;
+      mm_acc_rows(t, A, SPD, rg, St, SPD, c4, D);
+    }
     if (kind == 1) { add_w(accV); dot_rows(colp, Vs, 1.0f); }
     if (kind == 2 || kind == 4 || kind == 6) add_w(accK);
-    if (kind == 3) dot_rows(rowp, Xs, 1.0f);
     if (kind == 5) dot_rows(rowp, Ys, -1.0f);
     if (kind == 6) dot_rows(colp, Ks, 1.0f);
     if ((kind == 2 && next == 3) || (kind == 4 && next == 5)) {  // <dG, S^G> or <dH, S^H>
@@ -474,7 +489,10 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
   through *= expf(lend);
   __syncthreads();
 #pragma unroll
-  for (int m = 0; m < 4; m++) part[(rg + 8 * m) * (NQ + 1) + c4] = rowp[m];
+  for (int m = 0; m < 4; m++) {
+    const int r = rg + 8 * m;
+    part[r * (NQ + 1) + c4] = fmaf(expf(el[r]), rowp[m], rowq[m]);
+  }
   __syncthreads();
   for (int r = tid; r < BC; r += nt) {
     float sc = 0.0f;
@@ -511,7 +529,7 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
     const int uu = idx / 8, p = idx % 8;
     float s = 0.0f;
     for (int tt = uu + p; tt < Cv; tt += 8) {  // later token in the chunk
-      s += rowi[tt] * expf(el[tt]);            // ... and earlier token before it
+      s += rowi[tt];                           // ... and earlier token before it
       for (int ss = 0; ss < uu; ss++) s += Cm[tt * SPC + ss];
     }
     if (p == 0 && uu < Cv) {
@@ -558,7 +576,7 @@ int launch_bwd_t(const BwdArgs &a, const FwdWorkspace &ws, int phase, cudaStream
     timing_mark_begin(K_BWD_STATES, st);
     mesa_state_sweep_kernel<D, TIO, true><<<dim3(2, U), 256, 0, st>>>(a, ws, NC);
     timing_mark_end(K_BWD_STATES, st);
-    const size_t smem = sizeof(float) * (5 * BC * SPD + D * SPD + 4 * BC * SPC + BC * (D / 4 + 1) +
+    const size_t smem = sizeof(float) * (6 * BC * SPD + D * SPD + 4 * BC * SPC + BC * (D / 4 + 1) +
                                          4 * BC + 2 * D);
     auto k = mesa_bwd_grad_kernel<D, TIO>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
