@@ -60,7 +60,7 @@ def _fd_elements(lib, case, iters, h=1e-6):
 
 
 def _battery(lib) -> list:
-    """Names of the backward pins that fail for this build of the oracle."""
+    """Names of the backward pins that fail for this compiled copy of the oracle."""
     failed = []
     rng = np.random.default_rng(21)
     # (1) per-element central differences; CG with d iterations is the exact solve

@@ -39,7 +39,7 @@ def _explicit(k, v, gamma, t):
 
 
 def _battery(lib) -> list:
-    """Returns the names of the pins that fail for this build of the oracle."""
+    """Returns the names of the pins that fail for this compiled copy of the oracle."""
     failed = []
     f1 = lambda q, k, v, g, lam, n, tol=0.0: [x[0, 0] for x in oracle.forward(
         q[None, None], k[None, None], v[None, None], g[None, None], lam[None], n, tol, lib=lib)]

@@ -32,7 +32,7 @@ def _np_reference(x, w):
 
 
 def _battery(lib) -> list:
-    """Names of the preprocessing pins that fail for this build of the oracle."""
+    """Names of the preprocessing pins that fail for this compiled copy of the oracle."""
     failed = []
     rng = np.random.default_rng(3)
     B, H, T, d, W = 2, 3, 11, 5, 4
