@@ -45,3 +45,17 @@ def test_decode_inputs_per_step_streams():
     assert s0["q"].shape == (4, 2, 128) and s0["gamma"].shape == (4, 2)
     assert not np.array_equal(s0["k"], s1["k"]) and not np.array_equal(s0["k"], p["k"])
     assert np.array_equal(synth.decode_inputs(w, 1)["v"], s1["v"])
+
+
+def test_backward_inputs_add_an_independent_gradient_stream():
+    w = synth.workload("bwd_bf16_d128", B=1, H=2, T=96)
+    a = synth.backward_inputs(w, seed=0)
+    f = synth.forward_inputs(w, seed=0)
+    for key in ("q", "k", "v", "gamma", "lam"):
+        assert np.array_equal(a[key], f[key])          # the forward's inputs, unchanged
+    assert a["dout"].shape == (1, 2, 96, 128) and a["dout"].dtype == np.float32
+    assert np.all(a["dout"].view(np.uint32) & 0xFFFF == 0)   # bf16 values
+    assert np.array_equal(synth.backward_inputs(w, seed=0)["dout"], a["dout"])
+    assert not np.array_equal(synth.backward_inputs(w, seed=1)["dout"], a["dout"])
+    assert not np.allclose(a["dout"], a["v"])          # its own stream, not v's
+    assert abs(float(a["dout"].std()) - 1.0) < 0.05
