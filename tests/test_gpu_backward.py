@@ -200,3 +200,22 @@ def test_saved_iterates(dtype, d):
         g0 = _gpu(inp, dtype, 10, 0.0)
         for k in ("dq", "dk", "dv", "dgamma", "dlam"):
             assert np.array_equal(g0[k], g1[k]), k
+
+
+def test_dynamic_mode_tensor_cores():
+    """Dynamic stopping on the tensor-core path (bf16, d = 128, tol 1e-3, cap 30, the long
+    workload's rule): both solves stop per token; at least 95 % of the counts agree with the
+    oracle's and the units whose counts all agree meet the bf16 tolerance."""
+    w = synth.workload("bwd_bf16_d128", B=2, H=2, T=256, cg_iters=30, cg_tol=1e-3)
+    inp = synth.backward_inputs(w, seed=6)
+    g = _gpu(inp, "bf16", 30, 1e-3)
+    r = oracle.backward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], inp["dout"], 30, 1e-3)
+    agree = (g["iters_fwd"] == r["iters_fwd"]) & (g["iters_bwd"] == r["iters_bwd"])
+    print(f"bwd dynamic tc: counts agree {agree.mean():.4f}, mean iters fwd {g['iters_fwd'].mean():.2f} "
+          f"bwd {g['iters_bwd'].mean():.2f}")
+    assert agree.mean() >= 0.95
+    for b, h in zip(*np.nonzero(agree.all(axis=-1))):
+        e = {k: float(unit_err(g[k][b, h], r[k][b, h])) for k in ("dq", "dk", "dv")}
+        e["dgamma"] = float(unit_err(g["dgamma"][b, h][:, None], r["dgamma"][b, h][:, None]))
+        for k, v in e.items():
+            assert v <= TOL["bf16"], f"unit ({b}, {h}) {k} {v:.3e}"
