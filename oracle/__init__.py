@@ -54,10 +54,10 @@ def _bind(lib):
     lib.oracle_cg.argtypes = [ctypes.c_int, _D, _D, _D, ctypes.c_int, ctypes.c_double, _D, _D]
     lib.oracle_forward.restype = ctypes.c_int
     lib.oracle_forward.argtypes = [ctypes.c_int] * 5 + [_D] * 5 + [
-        ctypes.c_int, ctypes.c_double, _I, _D, _D, _D, _I, _D, _D, ctypes.c_int]
+        ctypes.c_int, ctypes.c_double, _I, _D, _D, _D, _I, _D, _D, _D, ctypes.c_int]
     lib.oracle_decode_step.restype = ctypes.c_int
     lib.oracle_decode_step.argtypes = [ctypes.c_int] * 4 + [_D] * 7 + [
-        ctypes.c_int, ctypes.c_double, _D, _I, ctypes.c_int]
+        ctypes.c_int, ctypes.c_double, _D, _I, _D, ctypes.c_int]
     lib.oracle_state_trace.restype = None
     lib.oracle_state_trace.argtypes = [ctypes.c_int] * 3 + [_D] * 5
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -66,7 +66,7 @@ def _bind(lib):
     lib.oracle_cg_from.argtypes = [ctypes.c_int, _D, _D, _D, _D, ctypes.c_int, ctypes.c_double, _D, _D]
     lib.oracle_decode_step_from.restype = ctypes.c_int
     lib.oracle_decode_step_from.argtypes = [ctypes.c_int] * 4 + [_D] * 7 + [
-        ctypes.c_int, ctypes.c_double, _D, _D, _I, ctypes.c_int]
+        ctypes.c_int, ctypes.c_double, _D, _D, _I, _D, ctypes.c_int]
     lib.oracle_qk_preprocess.restype = None
     lib.oracle_qk_preprocess.argtypes = [ctypes.c_int] * 5 + [_D] * 3
     lib.oracle_qk_preprocess_step.restype = None
@@ -99,6 +99,15 @@ def _ptr(a, t=_D):
     return None if a is None else a.ctypes.data_as(t)
 
 
+def _scale_buf(a, shape):
+    """The caller's readout-magnitude array, checked (None stays None)."""
+    if a is None:
+        return None
+    assert a.dtype == np.float64 and a.flags.c_contiguous and a.shape == tuple(shape), \
+        f"scale_out must be float64 C-contiguous {tuple(shape)}"
+    return a
+
+
 def max_threads(lib=None) -> int:
     return (lib or load()).oracle_max_threads()
 
@@ -121,11 +130,13 @@ def cg(Hm, lam, q, maxit, tol=0.0, x0=None, lib=None):
 
 
 def forward(q, k, v, gamma, lam, cg_iters, cg_tol=0.0, replay=None, H0=None, G0=None,
-            want_final=False, nthreads=None, lib=None):
+            want_final=False, nthreads=None, lib=None, scale_out=None):
     """Mesa layer forward.  q, k: [B, heads, T, dk]; v: [B, heads, T, dv];
     gamma: [B, heads, T]; lam: [heads, dk].  Returns (out [B, heads, T, dv] fp64,
     iters [B, heads, T] int32[, H_final [B, heads, dk, dk], G_final [B, heads, dv, dk]]).
-    ``replay`` (int32 [B, heads, T]) runs each token for exactly that many iterations."""
+    ``replay`` (int32 [B, heads, T]) runs each token for exactly that many iterations.
+    ``scale_out``: None, or a float64 C-contiguous [B, heads, T] array that receives each
+    token's readout magnitude || |G_t| |x_t| ||_2 (>= ||out_t||)."""
     lib = lib or load()
     q, k, v, gamma, lam = _f64(q), _f64(k), _f64(v), _f64(gamma), _f64(lam)
     B, heads, T, dk = q.shape
@@ -141,7 +152,8 @@ def forward(q, k, v, gamma, lam, cg_iters, cg_tol=0.0, replay=None, H0=None, G0=
     nt = nthreads if nthreads is not None else (os.cpu_count() or 1)
     lib.oracle_forward(U, heads, T, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(gamma), _ptr(lam),
                        int(cg_iters), float(cg_tol), _ptr(rep, _I), _ptr(H0), _ptr(G0),
-                       _ptr(out), _ptr(iters, _I), _ptr(Hf), _ptr(Gf), int(nt))
+                       _ptr(out), _ptr(iters, _I), _ptr(Hf), _ptr(Gf), _ptr(_scale_buf(scale_out, (B, heads, T))),
+                       int(nt))
     if want_final:
         return out, iters, Hf, Gf
     return out, iters
@@ -168,11 +180,13 @@ def backward(q, k, v, gamma, lam, dout, cg_iters, cg_tol=0.0, nthreads=None, lib
     return r
 
 
-def decode_step(Hs, Gs, q, k, v, gamma, lam, cg_iters, cg_tol=0.0, nthreads=None, X=None, lib=None):
+def decode_step(Hs, Gs, q, k, v, gamma, lam, cg_iters, cg_tol=0.0, nthreads=None, X=None, lib=None,
+                scale_out=None):
     """One decode step, in place on the fp64 states Hs [N, heads, dk, dk] and
     Gs [N, heads, dv, dk] (must be float64 C-contiguous).  q, k: [N, heads, dk];
     v: [N, heads, dv]; gamma: [N, heads].  X: None, or [N, heads, dk] float64 C-contiguous,
     the start of each unit's CG (warm start), replaced in place by this step's solution.
+    scale_out: None, or float64 C-contiguous [N, heads], each unit's || |G| |x| ||_2.
     Returns (out [N, heads, dv], iters [N, heads])."""
     lib = lib or load()
     assert Hs.dtype == np.float64 and Hs.flags.c_contiguous
@@ -186,12 +200,12 @@ def decode_step(Hs, Gs, q, k, v, gamma, lam, cg_iters, cg_tol=0.0, nthreads=None
     if X is None:
         lib.oracle_decode_step(N * heads, heads, dk, dv, _ptr(Hs), _ptr(Gs), _ptr(q), _ptr(k), _ptr(v),
                                _ptr(gamma), _ptr(lam), int(cg_iters), float(cg_tol), _ptr(out),
-                               _ptr(iters, _I), int(nt))
+                               _ptr(iters, _I), _ptr(_scale_buf(scale_out, (N, heads))), int(nt))
     else:
         assert X.dtype == np.float64 and X.flags.c_contiguous
         lib.oracle_decode_step_from(N * heads, heads, dk, dv, _ptr(Hs), _ptr(Gs), _ptr(q), _ptr(k), _ptr(v),
                                     _ptr(gamma), _ptr(lam), int(cg_iters), float(cg_tol), _ptr(X), _ptr(out),
-                                    _ptr(iters, _I), int(nt))
+                                    _ptr(iters, _I), _ptr(_scale_buf(scale_out, (N, heads))), int(nt))
     return out, iters
 
 

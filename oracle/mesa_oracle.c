@@ -129,14 +129,27 @@ static void state_step(int dk, int dv, double *H, double *G, const double *k, co
 }
 
 /* One token of the recurrence on one unit: decay and rank-1 update of H and G,
- * the CG solve, and the readout o = G x.  H is dk x dk, G is dv x dk. */
+ * the CG solve, and the readout o = G x.  H is dk x dk, G is dv x dk.
+ * scale: NULL, or one double that receives || |G| |x| ||_2, the Euclidean norm of the
+ * readout taken with absolute values (sum_b |G_ab| |x_b| per output row a).  It is the
+ * magnitude on which the rounding of o = G x is measured: ||o|| <= scale, with equality
+ * when no term of a row cancels another. */
 static int mesa_token(int dk, int dv, double *H, double *G, const double *q,
                       const double *k, const double *v, double gamma,
                       const double *lam, int maxit, double tol, double *o,
-                      double *x, double *work, const double *x0) {
+                      double *x, double *work, const double *x0, double *scale) {
   state_step(dk, dv, H, G, k, v, gamma);
   const int it = oracle_cg_from(dk, H, lam, q, x0, maxit, tol, x, work);
   for (int a = 0; a < dv; a++) o[a] = dot(dk, G + (size_t)a * dk, x);
+  if (scale) {
+    double s2 = 0.0;
+    for (int a = 0; a < dv; a++) {
+      double m = 0.0;
+      for (int b = 0; b < dk; b++) m += fabs(G[(size_t)a * dk + b]) * fabs(x[b]);
+      s2 += m * m;
+    }
+    *scale = sqrt(s2);
+  }
   return it;
 }
 
@@ -155,6 +168,7 @@ static int pick_threads(int nthreads, int units) {
  *   runs exactly replay[u, t] iterations (fixed mode) and tol is ignored.
  *   H0/G0: NULL (zero initial state) or [U, dk, dk] / [U, dv, dk] initial states.
  *   H_final/G_final: NULL, or [U, dk, dk] / [U, dv, dk] states after token T-1.
+ *   scale: NULL, or [U, T]: each token's readout magnitude || |G_t| |x_t| ||_2.
  * Returns the number of threads used.
  */
 int oracle_forward(int U, int heads, int T, int dk, int dv, const double *q,
@@ -162,7 +176,7 @@ int oracle_forward(int U, int heads, int T, int dk, int dv, const double *q,
                    const double *lam, int cg_iters, double cg_tol,
                    const int32_t *replay, const double *H0, const double *G0,
                    double *out, int32_t *iters, double *H_final, double *G_final,
-                   int nthreads) {
+                   double *scale, int nthreads) {
   const int nt = pick_threads(nthreads, U);
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
   for (int u = 0; u < U; u++) {
@@ -183,7 +197,7 @@ int oracle_forward(int U, int heads, int T, int dk, int dv, const double *q,
       }
       iters[tok] = mesa_token(dk, dv, H, G, q + tok * dk, k + tok * dk,
                               v + tok * dv, gamma[tok], lam_u, maxit, tol,
-                              out + tok * dv, x, work, NULL);
+                              out + tok * dv, x, work, NULL, scale ? scale + tok : NULL);
     }
     if (H_final) memcpy(H_final + (size_t)u * dk * dk, H, sizeof(double) * dk * dk);
     if (G_final) memcpy(G_final + (size_t)u * dv * dk, G, sizeof(double) * dv * dk);
@@ -201,13 +215,14 @@ int oracle_forward(int U, int heads, int T, int dk, int dv, const double *q,
  *   lam [heads, dk], out [U, dv], iters [U]; U = N * heads.
  *   X: NULL (CG from 0) or [U, dk] in/out: the start of each unit's CG (warm start, e.g. the
  *   previous step's solution), replaced by this step's solution.
+ *   scale: NULL, or [U]: each unit's readout magnitude || |G| |x| ||_2.
  * Returns the number of threads used.
  */
 int oracle_decode_step_from(int U, int heads, int dk, int dv, double *H, double *G,
                             const double *q, const double *k, const double *v,
                             const double *gamma, const double *lam, int cg_iters,
                             double cg_tol, double *X, double *out, int32_t *iters,
-                            int nthreads) {
+                            double *scale, int nthreads) {
   const int nt = pick_threads(nthreads, U);
 #pragma omp parallel for schedule(dynamic, 4) num_threads(nt)
   for (int u = 0; u < U; u++) {
@@ -217,7 +232,7 @@ int oracle_decode_step_from(int U, int heads, int dk, int dv, double *H, double 
     iters[u] = mesa_token(dk, dv, H + (size_t)u * dk * dk, G + (size_t)u * dv * dk,
                           q + (size_t)u * dk, k + (size_t)u * dk, v + (size_t)u * dv,
                           gamma[u], lam + (size_t)(u % heads) * dk, cg_iters,
-                          cg_tol, out + (size_t)u * dv, x, work, xu);
+                          cg_tol, out + (size_t)u * dv, x, work, xu, scale ? scale + u : NULL);
     if (xu) memcpy(xu, x, sizeof(double) * dk);
     free(x);
     free(work);
@@ -228,9 +243,10 @@ int oracle_decode_step_from(int U, int heads, int dk, int dv, double *H, double 
 int oracle_decode_step(int U, int heads, int dk, int dv, double *H, double *G,
                        const double *q, const double *k, const double *v,
                        const double *gamma, const double *lam, int cg_iters,
-                       double cg_tol, double *out, int32_t *iters, int nthreads) {
+                       double cg_tol, double *out, int32_t *iters, double *scale,
+                       int nthreads) {
   return oracle_decode_step_from(U, heads, dk, dv, H, G, q, k, v, gamma, lam, cg_iters,
-                                 cg_tol, NULL, out, iters, nthreads);
+                                 cg_tol, NULL, out, iters, scale, nthreads);
 }
 
 /*

@@ -321,3 +321,46 @@ def test_heads_use_their_own_lambda_and_units_are_independent():
         for h in range(heads):
             o1, _ = _fwd1(q[b, h], k[b, h], v[b, h], gamma[b, h], lam[h], dk)
             np.testing.assert_array_equal(out[b, h], o1)
+
+
+def test_readout_magnitude_one_token_closed_form():
+    """The readout magnitude s_t = || |G_t| |x_t| || the oracle reports next to o_t, pinned
+    on one token after one CG step: H = k k^T, G = v k^T and x_1 = c q with
+    c = q.q / q.(H + Lambda) q > 0, so |G| |x| = |v| (|k| . |x|) and s = ||v|| c sum_b |k_b q_b|."""
+    rng = np.random.default_rng(31)
+    dk, dv = 5, 3
+    q, k, v = rng.standard_normal(dk), rng.standard_normal(dk), rng.standard_normal(dv)
+    lam = rng.uniform(0.3, 1.0, dk)
+    c = (q @ q) / (q @ (np.outer(k, k) @ q + lam * q))
+    a = lambda x: np.asarray(x, dtype=np.float64)[None, None, None]
+    s = np.zeros((1, 1, 1))
+    o, _ = oracle.forward(a(q), a(k), a(v), a([0.7]).reshape(1, 1, 1), lam[None], 1, scale_out=s)
+    np.testing.assert_allclose(o[0, 0, 0], v * c * (k @ q), rtol=1e-12)
+    np.testing.assert_allclose(s[0, 0, 0], np.linalg.norm(v) * c * np.abs(k * q).sum(), rtol=1e-12)
+
+
+def test_readout_magnitude_properties():
+    """s_t >= ||o_t|| on every token (equality in one dimension); flipping the values' sign
+    flips o and keeps s; scaling the values scales both; the decode step reports the same
+    magnitudes as the forward."""
+    rng = np.random.default_rng(32)
+    T, dk, dv = 40, 6, 4
+    q, k, v, gamma, lam = _rand_case(rng, T, dk, dv)
+    a = lambda x: x[None, None]
+    s = np.zeros((1, 1, T))
+    o, _ = oracle.forward(a(q), a(k), a(v), a(gamma), lam[None], 3, scale_out=s)
+    n = np.linalg.norm(o[0, 0], axis=-1)
+    assert np.all(s[0, 0] >= n * (1 - 1e-12)) and np.any(s[0, 0] > n * 1.01)
+    s2 = np.zeros((1, 1, T))
+    o2, _ = oracle.forward(a(q), a(k), a(-2.0 * v), a(gamma), lam[None], 3, scale_out=s2)
+    np.testing.assert_allclose(o2, -2.0 * o, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(s2, 2.0 * s, rtol=1e-12)
+    s1 = np.zeros((1, 1, T))
+    o1, _ = oracle.forward(a(q[:, :1]), a(k[:, :1]), a(v[:, :1]), a(gamma), lam[None, :1], 2, scale_out=s1)
+    np.testing.assert_allclose(s1[0, 0], np.abs(o1[0, 0, :, 0]), rtol=1e-12)
+    Hs, Gs = np.zeros((1, 1, dk, dk)), np.zeros((1, 1, dv, dk))
+    for t in range(T):
+        sd = np.zeros((1, 1))
+        oracle.decode_step(Hs, Gs, q[t][None, None], k[t][None, None], v[t][None, None], gamma[t].reshape(1, 1),
+                           lam[None], 3, scale_out=sd)
+        assert sd[0, 0] == s[0, 0, t]
