@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 from mesa_layer_gb300 import synth
-from helpers import TOL, check_against_oracle, unit_err
+from helpers import TOL, check_against_oracle, oracle_decode_units, unit_err
 
 pytestmark = pytest.mark.gpu
 
@@ -48,38 +48,29 @@ def _run(w, steps, prefix, units=None, iters=None, tol=None):
     Ho, Go = np.zeros((U, 1, d, d)), np.zeros((U, 1, d, d))
     Xo = np.zeros((U, 1, d))
     lam_u = lam[hidx]
-    og_all, ro_all, ig_all, rit_all = [], [], [], []
+    acc = {k: [] for k in ("og", "ig", "ro", "rit", "rr", "rs")}
     xerr = 0.0
     for s in range(-prefix, steps):
         inp = synth.decode_inputs(w, s)
         dev = _dev(inp, td)
-        sub = lambda x: x[nidx, hidx][:, None]
         if s < 0:  # state-only prefix (no CG; the start vectors stay zero)
             binding.mesa_decode_step(Hs, Gs, dev["q"], dev["k"], dev["v"], dev["gamma"], lam_t, 0, tol)
-            for i in range(U):
-                oracle.decode_step(Ho[i:i + 1], Go[i:i + 1], sub(inp["q"])[i:i + 1], sub(inp["k"])[i:i + 1],
-                                   sub(inp["v"])[i:i + 1], sub(inp["gamma"])[i:i + 1], lam_u[i][None], 0, tol)
+            oracle_decode_units(Ho, Go, inp, nidx, hidx, lam_u, 0, tol)
             continue
         o, it = binding.mesa_decode_step_warm(Hs, Gs, Xs, dev["q"], dev["k"], dev["v"], dev["gamma"], lam_t, iters, tol)
-        ro = np.zeros((U, 1, d))
-        rit = np.zeros((U, 1), dtype=np.int32)
-        for i in range(U):
-            xi = np.ascontiguousarray(Xo[i:i + 1])
-            ro[i], rit[i] = oracle.decode_step(Ho[i:i + 1], Go[i:i + 1], sub(inp["q"])[i:i + 1], sub(inp["k"])[i:i + 1],
-                                               sub(inp["v"])[i:i + 1], sub(inp["gamma"])[i:i + 1], lam_u[i][None],
-                                               iters, tol, X=xi)
-            Xo[i] = xi[0]
         torch.cuda.synchronize()
-        og_all.append(o.float().cpu().numpy()[nidx, hidx])
-        ig_all.append(it.cpu().numpy()[nidx, hidx])
-        ro_all.append(ro[:, 0])
-        rit_all.append(rit[:, 0])
+        ig = it.cpu().numpy()[nidx, hidx]
+        # the oracle's start vectors follow the GPU's counts (replayed where they differ)
+        ro, rit, rr, rs = oracle_decode_units(Ho, Go, inp, nidx, hidx, lam_u, iters, tol, gpu_counts=ig, Xo=Xo)
+        for k, v in (("og", o.float().cpu().numpy()[nidx, hidx]), ("ig", ig), ("ro", ro), ("rit", rit),
+                     ("rr", rr), ("rs", rs)):
+            acc[k].append(v)
         xg = Xs.cpu().numpy()[nidx, hidx]
         xerr = max(xerr, float(unit_err(xg[:, None], Xo[:, 0][:, None]).max()))
-    og, ro = np.stack(og_all, axis=1), np.stack(ro_all, axis=1)
-    ig, rit = np.stack(ig_all, axis=1), np.stack(rit_all, axis=1)
-    err, _ = check_against_oracle(og, ig, ro, rit, w.dtype, tol, "decode warm")
-    return err, xerr, ig, rit
+    a = {k: np.stack(v, axis=1) for k, v in acc.items()}
+    r = check_against_oracle(a["og"], a["ig"], a["ro"], a["rit"], a["rs"], w.dtype, tol, "decode warm",
+                             replay=lambda counts: (a["rr"], a["rs"]))
+    return r, xerr, a["ig"], a["rit"]
 
 
 def test_zero_start_is_the_cold_step():
@@ -109,8 +100,8 @@ def test_zero_start_is_the_cold_step():
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_warm_fixed_iterations(d, dtype):
     w = synth.workload("decode_bf16_d128", B=3, H=2, dk=d, dv=d, dtype=dtype, prefix=8)
-    err, xerr, ig, rit = _run(w, steps=16, prefix=8, iters=6, tol=0.0)
-    print(f"decode warm d={d} {dtype}: max rel err {err:.3e}, start vectors {xerr:.3e}")
+    r, xerr, ig, rit = _run(w, steps=16, prefix=8, iters=6, tol=0.0)
+    print(f"decode warm d={d} {dtype}: {r}, start vectors {xerr:.3e}")
     assert np.array_equal(ig, rit)
     assert xerr <= TOL[dtype]
 
@@ -120,9 +111,9 @@ def test_warm_dynamic_full_size_sampled_units():
     64-step prefix, 24 warm steps, four units followed by the oracle."""
     w = synth.workload("decode_bf16_d128")
     units = [(0, 0), (17, 5), (128, 9), (255, 15)]
-    err, xerr, ig, rit = _run(w, steps=24, prefix=64, units=units)
+    r, xerr, ig, rit = _run(w, steps=24, prefix=64, units=units)
     agree = (ig == rit).mean()
     # (the start vectors are reported only: after a token whose count differs by one the two
     # sides carry starts that differ by up to the stopping tolerance's reach)
-    print(f"decode warm full: max rel err {err:.3e}, start vectors {xerr:.3e}, counts agree {agree:.4f}, "
+    print(f"decode warm full: {r}, start vectors {xerr:.3e}, counts agree {agree:.4f}, "
           f"mean iters {ig.mean():.2f} (oracle {rit.mean():.2f})")

@@ -5,7 +5,7 @@ import pytest
 
 import oracle
 from mesa_layer_gb300 import synth
-from helpers import TOL, check_against_oracle, gpu_forward, unit_err
+from helpers import forward_check, gpu_forward
 
 pytestmark = pytest.mark.gpu
 
@@ -19,55 +19,51 @@ def _lib():
     binding.load()
 
 
-def _oracle(inp, w, **kw):
-    return oracle.forward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], w.cg_iters, w.cg_tol, **kw)
-
-
 def test_tiny_fp32_d16_full():
+    """The tiny fp32 workload (d = 16, 16 iterations: CG has converged), strict per-token."""
     w = synth.workload("tiny_fp32_d16")
     inp = synth.forward_inputs(w)
     o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
-    ro, rit = _oracle(inp, w)
-    err, tok = check_against_oracle(o, it, ro, rit, w.dtype, w.cg_tol, "tiny")
+    r = forward_check(inp, o, it, w.dtype, w.cg_iters, w.cg_tol, "tiny", metric="strict")
     assert (it == 16).all()
-    print(f"tiny: max rel err {err:.3e}, per-token max {tok.max():.3e}")
+    print(f"tiny: {r}")
 
 
 def test_fp32_d64_dynamic_full():
+    """The dynamic fp32 workload at full size: every token against the oracle replaying the
+    GPU's own counts, on the readout's magnitude (strict per-token reported)."""
     w = synth.workload("fwd_fp32_d64")
     inp = synth.forward_inputs(w)
     o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
-    ro, rit = _oracle(inp, w)
-    err, tok = check_against_oracle(o, it, ro, rit, w.dtype, w.cg_tol, "fp32_d64")
-    print(f"fp32_d64: max rel err {err:.3e}, per-token median {np.median(tok):.2e}, counts agree "
-          f"{np.mean(it == rit):.4f}, mean iters {it.mean():.2f}")
+    r = forward_check(inp, o, it, w.dtype, w.cg_iters, w.cg_tol, "fp32_d64")
+    print(f"fp32_d64: {r}, mean iters {it.mean():.2f}")
 
 
-def _sample_units(w, inp, units):
-    """Inputs of a subset of (batch, head) units, keeping each unit's own lambda row."""
-    sub = {}
-    for key in ("q", "k", "v", "gamma"):
-        sub[key] = np.stack([inp[key][b, h] for b, h in units])[None]
-    sub["lam_rows"] = np.stack([inp["lam"][h] for _, h in units])
-    return sub
+def _unit_inputs(inp, b, h, t0=0, t1=None):
+    """One (batch, head) unit over tokens [t0, t1) as a 1 x 1 batch, with its lambda row."""
+    sl = {k: inp[k][b, h][None, None, t0:t1] for k in ("q", "k", "v", "gamma")}
+    sl["lam"] = inp["lam"][h][None]
+    return sl
 
 
-def _oracle_units(w, inp, units, t0=0, t1=None):
+def _check_units(w, inp, o, it, units, t0=0, t1=None, label=""):
     """Oracle on selected units over tokens [t0, t1); the state at t0 comes from the
     oracle's own state-only pass (cg_iters = 0) over tokens [0, t0)."""
-    outs, its = [], []
+    import oracle
+    results = []
     for b, h in units:
-        sl = lambda x, a, z: x[b, h][None, None, a:z]
-        lam = inp["lam"][h][None]
-        H0 = G0 = None
+        kw = {}
         if t0 > 0:
-            _, _, H0, G0 = oracle.forward(sl(inp["q"], 0, t0), sl(inp["k"], 0, t0), sl(inp["v"], 0, t0),
-                                          inp["gamma"][b, h][None, None, :t0], lam, 0, 0.0, want_final=True)
-        o, it = oracle.forward(sl(inp["q"], t0, t1), sl(inp["k"], t0, t1), sl(inp["v"], t0, t1),
-                               inp["gamma"][b, h][None, None, t0:t1], lam, w.cg_iters, w.cg_tol, H0=H0, G0=G0)
-        outs.append(o[0, 0])
-        its.append(it[0, 0])
-    return np.stack(outs), np.stack(its)
+            pre = _unit_inputs(inp, b, h, 0, t0)
+            _, _, H0, G0 = oracle.forward(pre["q"], pre["k"], pre["v"], pre["gamma"], pre["lam"], 0, 0.0,
+                                          want_final=True)
+            kw = {"H0": H0, "G0": G0}
+        sub = _unit_inputs(inp, b, h, t0, t1)
+        og = o[b, h, t0:t1][None, None]
+        ig = it[b, h, t0:t1][None, None]
+        results.append(forward_check(sub, og, ig, w.dtype, w.cg_iters, w.cg_tol, f"{label}({b},{h})[{t0}:{t1}]",
+                                     **kw))
+    return results
 
 
 def test_bf16_d128_full_size_sampled_units():
@@ -75,12 +71,8 @@ def test_bf16_d128_full_size_sampled_units():
     inp = synth.forward_inputs(w)
     o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
     assert (it == w.cg_iters).all()
-    units = [(0, 0), (3, 7), (7, 15)]
-    ro, rit = _oracle_units(w, inp, units)
-    og = np.stack([o[b, h] for b, h in units])
-    ig = np.stack([it[b, h] for b, h in units])
-    err, tok = check_against_oracle(og, ig, ro, rit, w.dtype, w.cg_tol, "bf16_d128")
-    print(f"bf16_d128: max rel err {err:.3e}, per-token max {tok.max():.2e} median {np.median(tok):.2e}")
+    for r in _check_units(w, inp, o, it, [(0, 0), (3, 7), (7, 15)], label="bf16_d128"):
+        print(f"bf16_d128: {r}")
 
 
 def test_long_bf16_full_size_sampled_windows():
@@ -89,11 +81,8 @@ def test_long_bf16_full_size_sampled_windows():
     o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
     assert it.min() >= 0 and it.max() <= w.cg_iters
     for (b, h), (t0, t1) in [((0, 0), (0, 2048)), ((0, 11), (w.T - 2048, w.T))]:
-        ro, rit = _oracle_units(w, inp, [(b, h)], t0, t1)
-        err, tok = check_against_oracle(o[b, h, t0:t1], it[b, h, t0:t1], ro[0], rit[0], w.dtype, w.cg_tol,
-                                        f"long[{h}, {t0}:{t1}]")
-        print(f"long head {h} tokens {t0}:{t1}: max rel err {err:.3e}, "
-              f"counts agree {np.mean(it[b, h, t0:t1] == rit[0]):.4f}")
+        r, = _check_units(w, inp, o, it, [(b, h)], t0, t1, label="long")
+        print(f"long head {h} tokens {t0}:{t1}: {r}")
 
 
 EDGE = [
@@ -115,17 +104,16 @@ def test_edge_shapes(case):
                        cg_iters=iters, cg_tol=tol)
     inp = synth.forward_inputs(w, seed=5)
     o, it = gpu_forward(inp, dtype, iters, tol, chunk)
-    ro, rit = _oracle(inp, w)
-    check_against_oracle(o, it, ro, rit, dtype, tol, str(case))
+    r = forward_check(inp, o, it, dtype, iters, tol, str(case))
+    print(f"{case}: {r}")
     if iters == 0:
         assert np.all(o == 0)
 
 
 @pytest.mark.parametrize("regime", ["gamma_near_zero", "gamma_one", "lambda_large", "zero_queries"])
 def test_edge_values(regime):
-    # enough iterations to converge: these regimes check decay and masking, not how an
-    # unconverged CG iterate amplifies rounding
-    w = synth.workload("fwd_fp32_d64", B=1, H=2, T=192, dk=32, dv=32, chunk=64, cg_iters=48, cg_tol=0.0)
+    """Edge regimes at 12 iterations (d = 32: CG has not converged), every token."""
+    w = synth.workload("fwd_fp32_d64", B=1, H=2, T=192, dk=32, dv=32, chunk=64, cg_iters=12, cg_tol=0.0)
     inp = synth.forward_inputs(w, seed=9)
     if regime == "gamma_near_zero":
         inp["gamma"][:] = np.float32(1e-3)
@@ -138,36 +126,37 @@ def test_edge_values(regime):
     else:
         inp["q"][0, 1, ::3] = 0.0
     o, it = gpu_forward(inp, w.dtype, w.cg_iters, w.cg_tol, w.chunk)
-    ro, rit = _oracle(inp, w)
-    check_against_oracle(o, it, ro, rit, w.dtype, 0.0, regime)
+    r = forward_check(inp, o, it, w.dtype, w.cg_iters, 0.0, regime)
+    print(f"{regime}: {r}")
     if regime == "zero_queries":
         assert np.all(o[0, 1, ::3] == 0)
         # dynamic mode stops zero queries before the first iteration
         o2, it2 = gpu_forward(inp, w.dtype, 48, 1e-3, w.chunk)
         assert np.all(it2[0, 1, ::3] == 0) and np.all(o2[0, 1, ::3] == 0)
+        forward_check(inp, o2, it2, w.dtype, 48, 1e-3, "zero_queries dynamic")
 
 
 def test_chunk_size_invariance():
-    w = synth.workload("fwd_fp32_d64", B=1, H=2, T=256, dk=32, dv=32, cg_iters=40, cg_tol=0.0)
+    """d = 64, 16 iterations (not converged): every chunk length against the oracle, per token."""
+    w = synth.workload("fwd_fp32_d64", B=1, H=2, T=256, dk=64, dv=64, cg_iters=16, cg_tol=0.0)
     inp = synth.forward_inputs(w, seed=3)
-    ro, _ = _oracle(inp, w)
-    outs = [gpu_forward(inp, w.dtype, w.cg_iters, 0.0, c)[0] for c in (16, 32, 64, 128)]
-    for o in outs:
-        assert unit_err(o, ro).max() <= TOL["f32"]
-        assert unit_err(o, outs[0]).max() <= TOL["f32"]
+    for c in (16, 32, 64, 128):
+        o, it = gpu_forward(inp, w.dtype, w.cg_iters, 0.0, c)
+        r = forward_check(inp, o, it, w.dtype, w.cg_iters, 0.0, f"chunk {c}")
+        print(f"chunk {c}: {r}")
 
 
 def test_initial_and_final_states():
+    import oracle
     import torch
 
     w = synth.workload("fwd_fp32_d64", B=2, H=2, T=160, cg_iters=10, cg_tol=0.0)
     inp = synth.forward_inputs(w, seed=4)
-    ro, rit, Hf, Gf = _oracle(inp, w, want_final=True)
+    _, _, Hf, Gf = oracle.forward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], 0, 0.0, want_final=True)
     B, H, d = w.B, w.H, w.dk
-    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
     Hg, Gg = torch.empty(B, H, d, d, device="cuda"), torch.empty(B, H, d, d, device="cuda")
     o, it = gpu_forward(inp, w.dtype, w.cg_iters, 0.0, 64, H_final=Hg, G_final=Gg)
-    check_against_oracle(o, it, ro, rit, w.dtype, 0.0, "full")
+    forward_check(inp, o, it, w.dtype, w.cg_iters, 0.0, "full")
     for a, b in ((Hg, Hf), (Gg, Gf)):
         a = a.cpu().numpy().astype(np.float64)
         assert np.abs(a - b).max() <= 1e-5 * np.abs(b).max()
@@ -178,7 +167,7 @@ def test_initial_and_final_states():
     H1, G1 = torch.empty_like(Hg), torch.empty_like(Gg)
     o1, _ = gpu_forward(first, w.dtype, w.cg_iters, 0.0, 32, H_final=H1, G_final=G1)
     o2, _ = gpu_forward(second, w.dtype, w.cg_iters, 0.0, 64, H0=H1, G0=G1)
-    assert unit_err(np.concatenate([o1, o2], axis=2), ro).max() <= TOL["f32"]
+    forward_check(inp, np.concatenate([o1, o2], axis=2), it, w.dtype, w.cg_iters, 0.0, "split")
 
 
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("f32", 16), ("bf16", 128)])
@@ -214,7 +203,4 @@ def test_unaligned_inputs(dtype, d):
     if dtype == "f32":
         assert torch.equal(o_al, o_un)
     else:
-        ro, rit = oracle.forward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], 8)
-        assert np.array_equal(i_un.cpu().numpy(), rit)
-        err = unit_err(o_un.float().cpu().numpy(), ro).max()
-        assert err <= TOL["bf16"], err
+        forward_check(inp, o_un.float().cpu().numpy(), i_un.cpu().numpy(), "bf16", 8, 0.0, "unaligned")

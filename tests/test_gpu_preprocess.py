@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 from mesa_layer_gb300 import synth
-from helpers import TOL, unit_err
+from helpers import TOL, token_err
 
 pytestmark = pytest.mark.gpu
 
@@ -33,8 +33,9 @@ def _dev(inp, dtype):
 
 
 def _check(o_gpu, o_ref, dtype, label):
-    err = unit_err(o_gpu.reshape(-1, *o_gpu.shape[-2:]), o_ref.reshape(-1, *o_ref.shape[-2:])).max()
-    print(f"{label}: max rel err {err:.3e}")
+    """Strict per-token error (each output token is a unit vector or zero)."""
+    err = token_err(o_gpu.reshape(-1, *o_gpu.shape[-2:]), o_ref.reshape(-1, *o_ref.shape[-2:])).max()
+    print(f"{label}: strict per-token max {err:.3e}")
     assert err <= TOL[dtype], f"{label}: {err:.3e}"
     return err
 
