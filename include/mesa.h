@@ -54,7 +54,9 @@ enum mesa_status {
   MESA_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad alignment       */
   MESA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. dk not in set)    */
   MESA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required        */
-  MESA_ERR_CUDA = 4          /* a kernel launch failed                            */
+  MESA_ERR_CUDA = 4,         /* a kernel launch failed                            */
+  MESA_ERR_TIMEOUT = 5,      /* (status queries) a bounded device wait gave up    */
+  MESA_ERR_NONFINITE = 6     /* (status queries) a kernel wrote a non-finite value */
 };
 
 enum mesa_dtype { MESA_F32 = 0, MESA_BF16 = 1 };
@@ -236,13 +238,43 @@ int mesa_forward_chunked_noalloc(int B, int H, int T, int dk, int dv, int dtype,
                                  void *out, int32_t *iters_used, cudaStream_t stream);
 
 /*
- * Device status word of the last mesa_forward_chunked call that used `workspace`:
- * synchronises `stream`, then copies the word to *flags (host).  0 means no kernel gave up;
- * bit 0 set means a tensor-core kernel's bounded wait for its matrix multiplies expired and
- * the affected chunks' outputs were not written.  The word is cleared at the start of every
- * forward call.
+ * Device status word of the last mesa_forward_chunked (or _save, or mesa_backward_chunked)
+ * call that used `workspace`: copies the word to *flags (host) on `stream` and synchronises
+ * it.  Bits: 0 (1) a tensor-core kernel's bounded wait for its matrix multiplies gave up --
+ * the kernel then waits for the multiplies still in flight, releases its tensor memory and
+ * returns, and the affected chunks' outputs are not written; 1 (2) a non-finite output was
+ * written (a NaN or infinity in q, k, v or gamma, or an overflow); 2 (4) the wait for the
+ * in-flight multiplies after a give-up expired too.  The word is cleared at the start of
+ * every call that uses the workspace.  Returns MESA_ERR_TIMEOUT if bit 0 or 2 is set, else
+ * MESA_ERR_NONFINITE if bit 1 is set, else MESA_OK (MESA_ERR_INVALID_ARG / MESA_ERR_CUDA
+ * when the word could not be read).
+ *
+ * Non-finite inputs: the call still ends (in dynamic mode a token whose residual is NaN runs
+ * to cg_iters).  A NaN or infinity in q_t affects o_t alone.  One in k_t, v_t or gamma_t of
+ * a unit leaves that unit's tokens before the 128-token block holding t, and every other
+ * unit, unchanged; later outputs of the unit are unspecified (non-finite in general).
  */
 int mesa_forward_status(const void *workspace, cudaStream_t stream, unsigned *flags);
+
+/*
+ * Device status word of the decode steps (mesa_decode_step, mesa_decode_step_warm) on the
+ * current device -- one word per device, shared by every decode call on it: copies it to
+ * *flags (host), clears it, both on `stream`, and synchronises `stream`.  Bit 1 (2): a decode
+ * step wrote a non-finite output since the last query.  Returns MESA_ERR_NONFINITE if it is
+ * set, else MESA_OK (MESA_ERR_INVALID_ARG / MESA_ERR_CUDA when the word could not be read).
+ * A non-finite q, k, v or gamma affects only its own (sequence, head) unit.
+ */
+int mesa_decode_status(cudaStream_t stream, unsigned *flags);
+
+/*
+ * Test hook (no counterpart on the MesaNet pages): the number of polls after which the
+ * tensor-core kernels' waits for their matrix multiplies give up, for the launches that
+ * follow in this process; polls < 0 restores the default (2^22), 0 gives up at the first
+ * wait.  A give-up is reported through mesa_forward_status (MESA_ERR_TIMEOUT) and leaves the
+ * device usable: the kernel waits, with the default limit, for its multiplies in flight,
+ * then returns.  Process-wide, not thread-safe; MESA_ERR_INVALID_ARG above 2^32 - 1.
+ */
+int mesa_debug_set_wait_limit(long long polls);
 
 /*
  * Diagnostic of the tensor-core building blocks (no counterpart on the MesaNet pages):

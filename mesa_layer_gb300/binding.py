@@ -15,8 +15,10 @@ import torch
 from . import build as _build
 
 MESA_F32, MESA_BF16 = 0, 1
+MESA_OK, MESA_ERR_TIMEOUT, MESA_ERR_NONFINITE = 0, 5, 6
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported size or option",
-           3: "workspace missing or too small", 4: "CUDA launch failed"}
+           3: "workspace missing or too small", 4: "CUDA launch failed",
+           5: "a bounded device wait gave up", 6: "a kernel wrote a non-finite value"}
 
 _lib = None
 _vp, _fp, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
@@ -54,6 +56,10 @@ def load(build_if_missing: bool = True):
     lib.mesa_forward_chunked_noalloc.argtypes = [_i] * 6 + [_vp] * 5 + [_i, _f, _i, _vp, _ip, _vp]
     lib.mesa_forward_status.restype = _i
     lib.mesa_forward_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.mesa_decode_status.restype = _i
+    lib.mesa_decode_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint)]
+    lib.mesa_debug_set_wait_limit.restype = _i
+    lib.mesa_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
     lib.mesa_tc_selftest.restype = _i
     lib.mesa_tc_selftest.argtypes = [_vp] * 6 + [_vp]
     lib.mesa_decode_step.restype = _i
@@ -317,11 +323,36 @@ def mesa_decode_step_warm(H_state, G_state, X_state, q, k, v, gamma, lambda_diag
 
 def mesa_forward_status(workspace, stream=None) -> int:
     """Synchronise the stream and return the device status word of the last forward call
-    that used ``workspace`` (0: every kernel completed)."""
+    that used ``workspace`` (0: every kernel completed with finite outputs; bit 0: a bounded
+    wait gave up; bit 1: a non-finite output; bit 2: the drain after a give-up expired)."""
+    return mesa_forward_status_code(workspace, stream)[1]
+
+
+def mesa_forward_status_code(workspace, stream=None):
+    """(status code, flags) of mesa_forward_status: MESA_OK, MESA_ERR_TIMEOUT or
+    MESA_ERR_NONFINITE, and the raw word."""
     lib = load()
     flags = ctypes.c_uint(0)
-    _check(lib.mesa_forward_status(_ptr(workspace), _stream(stream), ctypes.byref(flags)), "mesa_forward_status")
-    return int(flags.value)
+    rc = lib.mesa_forward_status(_ptr(workspace), _stream(stream), ctypes.byref(flags))
+    if rc not in (MESA_OK, MESA_ERR_TIMEOUT, MESA_ERR_NONFINITE):
+        _check(rc, "mesa_forward_status")
+    return int(rc), int(flags.value)
+
+
+def mesa_decode_status(stream=None):
+    """(status code, flags) of the decode steps on the current device since the last query
+    (the word is cleared): MESA_OK or MESA_ERR_NONFINITE (bit 1 of flags)."""
+    lib = load()
+    flags = ctypes.c_uint(0)
+    rc = lib.mesa_decode_status(_stream(stream), ctypes.byref(flags))
+    if rc not in (MESA_OK, MESA_ERR_NONFINITE):
+        _check(rc, "mesa_decode_status")
+    return int(rc), int(flags.value)
+
+
+def mesa_debug_set_wait_limit(polls: int):
+    """Test hook: polls after which the tensor-core kernels' waits give up (< 0: default)."""
+    _check(load().mesa_debug_set_wait_limit(int(polls)), "mesa_debug_set_wait_limit")
 
 
 def mesa_tc_selftest(A, B, stream=None):

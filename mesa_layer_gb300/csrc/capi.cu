@@ -5,6 +5,7 @@
 
 #include "../../include/mesa.h"
 #include "launch.h"
+#include "tc_common.cuh"
 
 namespace {
 
@@ -32,8 +33,9 @@ int work_chunk(int dk, int chunk) {
 
 // Workspace: [status word | log-decays | S^H states | S^G states | (d = 128) segment
 // log-decays Lc | segment carries].  Sized for the working chunk (<= 128), so it also covers
-// the tensor-core path's 128-token chunks.
-size_t workspace_parts(int B, int H, int T, int dk, int dv, int chunk, size_t *off) {
+// the tensor-core path's 128-token chunks.  nseg: segments per unit of the tensor-core
+// state build (< 0: mesa::tc_segments for the current device).
+size_t workspace_parts(int B, int H, int T, int dk, int dv, int chunk, size_t *off, int nseg_in = -1) {
   const size_t U = (size_t)B * H;
   chunk = work_chunk(dk, chunk);
   const size_t NC = (size_t)(T + chunk - 1) / chunk;
@@ -45,7 +47,7 @@ size_t workspace_parts(int B, int H, int T, int dk, int dv, int chunk, size_t *o
   off[4] = end;
   if (dk == 128 && dv == 128) {
     const int NC128 = (T + 127) / 128;
-    const size_t nseg = (size_t)mesa::tc_segments((int)U, NC128);
+    const size_t nseg = nseg_in > 0 ? (size_t)nseg_in : (size_t)mesa::tc_segments((int)U, NC128);
     off[4] = off[3] + align256(U * NC128 * sizeof(float));
     end = off[4] + align256(U * nseg * 2 * dk * dk * sizeof(float));
   }
@@ -57,14 +59,14 @@ size_t workspace_parts(int B, int H, int T, int dk, int dv, int chunk, size_t *o
 // dG adjoints | dH adjoints | dlambda partials].  The 128-token parts serve the tensor-core
 // solves (d = 128) and are empty otherwise.
 constexpr int kBwdParts = 15;
-size_t backward_parts(int B, int H, int T, int dk, size_t *off) {
+size_t backward_parts(int B, int H, int T, int dk, size_t *off, int nseg_in = -1) {
   const size_t U = (size_t)B * H, C = mesa::kBwdChunk;
   const size_t NC = (T + C - 1) / C, NC128 = (T + 127) / 128;
   const bool big = dk == 128;
   const size_t st = U * NC * dk * dk * sizeof(float), tok = U * T * sizeof(float);
   const size_t vec = U * T * dk * sizeof(float);
   const size_t st128 = big ? U * NC128 * dk * dk * sizeof(float) : 0;
-  const size_t nseg = big ? (size_t)mesa::tc_segments((int)U, (int)NC128) : 0;
+  const size_t nseg = !big ? 0 : nseg_in > 0 ? (size_t)nseg_in : (size_t)mesa::tc_segments((int)U, (int)NC128);
   const size_t sizes[kBwdParts - 1] = {
       tok, st, st,                                       // ell, SH, SG (chunk 32)
       big ? tok : 0, st128,                              // ell, SH (128)
@@ -96,9 +98,23 @@ struct TimingState {
 };
 TimingState g_timing;
 
+// Polls of the tensor-core kernels' bounded waits (mesa_debug_set_wait_limit); negative: the
+// default.
+long long g_wait_limit = -1;
+
+// The device status word's bits as a status code (a timeout first: it means outputs are
+// missing, not only non-finite).
+int status_from_flags(unsigned f) {
+  if (f & (mesa::tc::kErrMmaTimeout | mesa::tc::kErrDrainTimeout)) return MESA_ERR_TIMEOUT;
+  if (f & mesa::tc::kErrNonFinite) return MESA_ERR_NONFINITE;
+  return MESA_OK;
+}
+
 }  // namespace
 
 namespace mesa {
+
+unsigned wait_limit() { return g_wait_limit < 0 ? tc::kWaitLimit : (unsigned)g_wait_limit; }
 
 void timing_mark_begin(int kind, cudaStream_t st) {
   TimingState &t = g_timing;
@@ -188,6 +204,18 @@ int mesa_forward_status(const void *workspace, cudaStream_t stream, unsigned *fl
           cudaSuccess ||
       cudaStreamSynchronize(stream) != cudaSuccess)
     return MESA_ERR_CUDA;
+  return status_from_flags(*flags);
+}
+
+int mesa_decode_status(cudaStream_t stream, unsigned *flags) {
+  if (!flags) return MESA_ERR_INVALID_ARG;
+  if (mesa::decode_status(stream, flags) != 0) return MESA_ERR_CUDA;
+  return status_from_flags(*flags);
+}
+
+int mesa_debug_set_wait_limit(long long polls) {
+  if (polls > (long long)0xFFFFFFFFu) return MESA_ERR_INVALID_ARG;
+  g_wait_limit = polls < 0 ? -1 : polls;
   return MESA_OK;
 }
 
@@ -204,6 +232,8 @@ const char *mesa_status_string(int s) {
     case MESA_ERR_UNSUPPORTED: return "unsupported size or option";
     case MESA_ERR_WORKSPACE: return "workspace missing or too small";
     case MESA_ERR_CUDA: return "CUDA launch failed";
+    case MESA_ERR_TIMEOUT: return "a bounded wait on the device gave up (outputs not written)";
+    case MESA_ERR_NONFINITE: return "a kernel wrote a non-finite output";
   }
   return "unknown status";
 }
@@ -245,18 +275,22 @@ int forward_impl(int B, int H, int T, int dk, int dv, int dtype, const void *q, 
     return MESA_OK;
   }
   if (!q || !k || !v || !gamma || !out) return MESA_ERR_INVALID_ARG;
+  const bool tc = use_tc(dtype, dk, dv, q, k, v, out, H0, G0);
+  // segments of the tensor-core state build: the current device's choice, or fewer when the
+  // workspace was sized on a device with fewer SMs (the carries are its last part)
+  int nseg = tc ? mesa::tc_segments((int)U, (T + 127) / 128) : 1;
   size_t off[5];
-  const size_t need = workspace_parts(B, H, T, dk, dv, chunk, off);
+  size_t need = workspace_parts(B, H, T, dk, dv, chunk, off, nseg);
+  while (tc && nseg > 1 && workspace_bytes < need) need = workspace_parts(B, H, T, dk, dv, chunk, off, --nseg);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return MESA_ERR_WORKSPACE;
 
-  const bool tc = use_tc(dtype, dk, dv, q, k, v, out, H0, G0);
-  mesa::FwdArgs a{B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol,
-                  tc ? 128 : work_chunk(dk, chunk), out, iters_used, H0, G0, H_final, G_final};
   char *w = (char *)workspace;
   unsigned *status = (unsigned *)w;
+  mesa::FwdArgs a{B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol,
+                  tc ? 128 : work_chunk(dk, chunk), out, iters_used, H0, G0, H_final, G_final,
+                  status, mesa::wait_limit()};
   mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2]),
-                        (float *)(w + off[3]), (float *)(w + off[4]),
-                        tc ? mesa::tc_segments((int)U, (T + 127) / 128) : 1};
+                        (float *)(w + off[3]), (float *)(w + off[4]), nseg};
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
   if (mesa::launch_chunk_states(a, ws, tc ? status : nullptr, stream) != 0) return MESA_ERR_CUDA;
   mesa::SolveArgs sv;
@@ -321,8 +355,12 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
       !aligned(dk_out, 16) || !aligned(dv_out, 16) || (x_saved && !aligned(x_saved, 16)))
     return MESA_ERR_INVALID_ARG;
+  // segments of the tensor-core state build: the current device's choice, or fewer when the
+  // workspace was sized on a device with fewer SMs
+  int nseg = dk == 128 ? mesa::tc_segments((int)U, (T + 127) / 128) : 1;
   size_t off[kBwdParts];
-  const size_t need = backward_parts(B, H, T, dk, off);
+  size_t need = backward_parts(B, H, T, dk, off, nseg);
+  while (nseg > 1 && workspace_bytes < need) need = backward_parts(B, H, T, dk, off, --nseg);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return MESA_ERR_WORKSPACE;
   char *w = (char *)workspace;
   unsigned *status = (unsigned *)w;
@@ -333,7 +371,7 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
   const int C = mesa::kBwdChunk;
   // chunk-C states and log-decays: read by the backward kernels, and by the CUDA-core solves
   mesa::FwdArgs a{B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol, C,
-                  nullptr, iters_fwd, nullptr, nullptr, nullptr, nullptr};
+                  nullptr, iters_fwd, nullptr, nullptr, nullptr, nullptr, status, mesa::wait_limit()};
   mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2]),
                         nullptr, nullptr, 1};
   mesa::BwdArgs ba{B, H, T, dk, dv, dtype, k, v, dout, gamma, X, Y, Bv,
@@ -346,8 +384,7 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
   mesa::FwdArgs a128 = a;
   a128.chunk = 128;
   mesa::FwdWorkspace ws128{(float *)(w + off[3]), (float *)(w + off[4]), (float *)(w + off[8]),
-                           (float *)(w + off[9]), (float *)(w + off[10]),
-                           tc ? mesa::tc_segments((int)U, (T + 127) / 128) : 1};
+                           (float *)(w + off[9]), (float *)(w + off[10]), tc ? nseg : 1};
   if (tc && mesa::launch_chunk_states(a128, ws128, status, stream) != 0) return MESA_ERR_CUDA;
   auto solve = [&](const float *rhs, float *x_out, int32_t *iters) -> int {
     mesa::SolveArgs sv;

@@ -228,8 +228,13 @@ __global__ void __launch_bounds__(512) mesa_cg_rows_kernel(FwdArgs a, FwdWorkspa
   apply(x, o, SGt, Ks, Vs);
   if (valid) {
     TIO *out = (TIO *)a.out;
+    bool fin = true;
 #pragma unroll
-    for (int n = 0; n < DC; n++) st(out, (tokbase + i) * D + col(n), o[n]);
+    for (int n = 0; n < DC; n++) {
+      st(out, (tokbase + i) * D + col(n), o[n]);
+      fin = fin && isfinite(o[n]);
+    }
+    if (!fin && a.status) atomicOr(a.status, tc_err_nonfinite());
     if (part == 0 && a.iters) a.iters[tokbase + i] = cnt;
   }
 }
@@ -527,7 +532,13 @@ __global__ void __launch_bounds__(128, 4) mesa_cg_rows64_kernel(FwdArgs a, FwdWo
     if (!valid[r]) continue;
     const size_t base = (tokbase + i0 + r) * D;
 #pragma unroll
-    for (int n = 0; n < 8; n++) st(out, base + (n < 4 ? 4 * o + n : 32 + 4 * o + (n - 4)), ov[r][n]);
+    bool fin = true;
+#pragma unroll
+    for (int n = 0; n < 8; n++) {
+      st(out, base + (n < 4 ? 4 * o + n : 32 + 4 * o + (n - 4)), ov[r][n]);
+      fin = fin && isfinite(ov[r][n]);
+    }
+    if (!fin && a.status) atomicOr(a.status, tc_err_nonfinite());
     if (o == 0 && a.iters) a.iters[tokbase + i0 + r] = cnt[r];
   }
 }

@@ -302,11 +302,17 @@ __global__ void __launch_bounds__(256) mesa_cg_simt_kernel(FwdArgs a, FwdWorkspa
     for (int m = 0; m < RPW; m++) {
       const int i = warp + 8 * m, gi = r0 + i;
       if (gi >= Cv) continue;
+      bool fin = true;
 #pragma unroll
       for (int n = 0; n < DN; n++) {
         const int d = lane + 32 * n;
-        if (d < D) st(out, (tokbase + gi) * D + d, fmaf(sc[i], a1[m][n], a2[m][n]));
+        if (d < D) {
+          const float o = fmaf(sc[i], a1[m][n], a2[m][n]);
+          st(out, (tokbase + gi) * D + d, o);
+          fin = fin && isfinite(o);
+        }
       }
+      if (!fin && a.status) atomicOr(a.status, tc_err_nonfinite());
     }
   }
 }

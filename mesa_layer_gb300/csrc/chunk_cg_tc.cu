@@ -28,6 +28,8 @@
 
 namespace mesa {
 
+static_assert(tc::kErrNonFinite == tc_err_nonfinite(), "one status bit for non-finite outputs");
+
 namespace {
 
 using tc::DH;
@@ -100,6 +102,7 @@ struct Misc {
   uint64_t mbar_w2;  // W = P K^T, keys 64..127 (and, issued before it, keys 0..63)
   uint64_t mbar_y;   // Y = Z K
   uint64_t mbar_u;   // U = P S
+  uint64_t mbar_drain;  // after a give-up: completion of every multiply issued (2 issuers)
   uint32_t tmem_base;
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc block too large");
@@ -180,6 +183,8 @@ __global__ void __launch_bounds__(512, 1)
   Misc *m = reinterpret_cast<Misc *>(sm + OFF_MISC);
   const uint32_t aBarW1 = tc::smem_u32(&m->mbar_w1), aBarW2 = tc::smem_u32(&m->mbar_w2);
   const uint32_t aBarY = tc::smem_u32(&m->mbar_y), aBarU = tc::smem_u32(&m->mbar_u);
+  const uint32_t aBarDrain = tc::smem_u32(&m->mbar_drain);
+  const unsigned wlim = a.wait_limit;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, grp = warp >> 2;  // lane quadrant, column group
@@ -238,6 +243,7 @@ __global__ void __launch_bounds__(512, 1)
     tc::mbar_init(aBarW2, 1);
     tc::mbar_init(aBarY, 1);
     tc::mbar_init(aBarU, 1);
+    tc::mbar_init(aBarDrain, 2);  // threads 0 (W, Y) and 128 (U) issue the multiplies
   }
   bool small = true;  // |l2| <= 100: D_ij = 2^{l2_i} 2^{-l2_j} without overflow
   if (tid < TILE) {
@@ -436,7 +442,7 @@ __global__ void __launch_bounds__(512, 1)
   auto wait_W = [&]() -> bool {
     bool ok = true;
     if (w_half) {
-      ok = tc::mbar_wait(w_half == 1 ? aBarW1 : aBarW2, phW);
+      ok = tc::mbar_wait(w_half == 1 ? aBarW1 : aBarW2, phW, wlim);
       phW ^= 1;
     }
     tc::fence_after_sync();
@@ -444,9 +450,9 @@ __global__ void __launch_bounds__(512, 1)
   };
   // Bounded waits for Y and U; all threads agree on the outcome.
   auto wait_YU = [&]() -> bool {
-    bool ok = tc::mbar_wait(aBarY, phY);
+    bool ok = tc::mbar_wait(aBarY, phY, wlim);
     phY ^= 1;
-    ok = tc::mbar_wait(aBarU, phU) && ok;
+    ok = tc::mbar_wait(aBarU, phU, wlim) && ok;
     phU ^= 1;
     tc::fence_after_sync();
     const int bad = __syncthreads_or(!ok);
@@ -465,13 +471,17 @@ __global__ void __launch_bounds__(512, 1)
   };
   // Z = (W mrow / sK) o D into the Z operand (warps above the diagonal keep their zeros);
   // returns the row scale.  The column factor 2^{-l2_j} multiplies W here, the row factor
-  // goes into the scale.
-  auto build_z = [&](float mrow) -> float {
+  // goes into the scale.  okW false (this warp's wait for W gave up): W is not read (the
+  // multiply may still be writing it) and the row reductions still run, so that the
+  // quadrant's barriers are met; the block then gives up at the next barrier.
+  auto build_z = [&](float mrow, bool okW) -> float {
     const float f = mrow / sK;
     const float rowf = factored ? f * e2r_i : f;
     float w[CW];
+#pragma unroll
+    for (int kk = 0; kk < CW; kk++) w[kk] = 0.0f;
     float zmax = 0.0f;
-    if (!z_upper) {
+    if (!z_upper && okW) {
       if (factored) {
         const bool diag = grp == qd;  // the only block that straddles the diagonal
 #pragma unroll
@@ -505,7 +515,7 @@ __global__ void __launch_bounds__(512, 1)
       }
     }
     const float zs = tc::pow2_ceil(rowred(zmax * rowf, true));
-    if (!z_upper) {
+    if (!z_upper && okW) {
       const float inv = rowf / zs;
 #pragma unroll
       for (int g = 0; g < NV; g++) {
@@ -554,7 +564,7 @@ __global__ void __launch_bounds__(512, 1)
     if (it > 0) x_update(alpha_prev);
     const bool okW = wait_W();
     if (tid == 128 && okW) issue_U();
-    const float zs = build_z(mP);
+    const float zs = build_z(mP, okW);
     if (!sync_Z(okW)) {
       failed = true;
       break;
@@ -715,7 +725,7 @@ __global__ void __launch_bounds__(512, 1)
     __syncwarp();
     const bool okW = wait_W();
     if (tid == 128 && okW) issue_U();
-    const float zs = build_z(mX);
+    const float zs = build_z(mX, okW);
     // X K^T is complete once every warp that waits on its halves has passed the barrier
     // below, so V may only replace K after it
     failed = !sync_Z(okW);
@@ -742,20 +752,28 @@ __global__ void __launch_bounds__(512, 1)
                                    fmaf(fu, uu[4 * g4 + 3], fy * yy[4 * g4 + 3]));
         } else if (valid) {
           __nv_bfloat16 *out = (__nv_bfloat16 *)a.out + (tokbase + i) * DH + c0;
+          bool fin = true;
 #pragma unroll
           for (int g = 0; g < NV; g++) {
             __align__(16) __nv_bfloat16 o8[8];
 #pragma unroll
-            for (int kk = 0; kk < 8; kk++)
-              o8[kk] = __float2bfloat16_rn(fmaf(fu, uu[g * 8 + kk], fy * yy[g * 8 + kk]));
+            for (int kk = 0; kk < 8; kk++) {
+              const float o = fmaf(fu, uu[g * 8 + kk], fy * yy[g * 8 + kk]);
+              fin = fin && isfinite(o);
+              o8[kk] = __float2bfloat16_rn(o);
+            }
             *reinterpret_cast<uint4 *>(out + 8 * g) = *reinterpret_cast<uint4 *>(o8);
           }
+          if (!fin) atomicOr(status, tc::kErrNonFinite);
           if (grp == 0 && a.iters) a.iters[tokbase + i] = cnt;
         }
       }
     }
   }
 
+  // a wait gave up (the same outcome in every thread): let every multiply still in flight
+  // finish before the tensor memory is released
+  if (failed) tc::drain_mmas(aBarDrain, tid == 0 || tid == 128, status);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_free(tbase, 512);

@@ -14,6 +14,9 @@ constexpr float kLogGateFloor = -80.0f;
 
 __device__ __forceinline__ float log_gate(float g) { return fmaxf(logf(g), kLogGateFloor); }
 
+// Device status-word bit for a non-finite output (the same value as tc::kErrNonFinite).
+__host__ __device__ constexpr unsigned tc_err_nonfinite() { return 2u; }
+
 template <typename T>
 __device__ __forceinline__ float ld(const T *p, size_t i);
 template <>
@@ -143,16 +146,6 @@ struct FwdWorkspace {
   int nseg;
 };
 
-// Segments per unit for the tensor-core state build (one CTA per SM each): enough CTAs to
-// fill the 152 SMs once when there are few (batch, head) units, one segment when there are
-// many.
-inline int tc_segments(int U, int NC) {
-  int s = U > 0 ? 148 / U : 1;
-  if (s > 16) s = 16;
-  if (s > NC) s = NC;
-  return s < 1 ? 1 : s;
-}
-
 // Multiprocessors of the current device (0 if it cannot be read): the size of the
 // persistent grids.
 inline int sm_count() {
@@ -161,6 +154,19 @@ inline int sm_count() {
       cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
     return 0;
   return n;
+}
+
+// Segments per unit for the tensor-core state build (one CTA per SM each): enough CTAs to
+// fill the current device's SMs about once when there are few (batch, head) units, one
+// segment when there are many; at most 16.  Without a readable device (a size query on a
+// host with no GPU) the count of a GB300, 152, stands in.
+inline int tc_segments(int U, int NC) {
+  int sms = sm_count();
+  if (sms <= 0) sms = 152;
+  int s = U > 0 ? sms / U : 1;
+  if (s > 16) s = 16;
+  if (s > NC) s = NC;
+  return s < 1 ? 1 : s;
 }
 
 }  // namespace mesa

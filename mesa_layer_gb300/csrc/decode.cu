@@ -14,6 +14,13 @@
 #include "launch.h"
 
 namespace mesa {
+// Status word of the decode kernels on this device (each device that loads the library has
+// its own copy): bit tc_err_nonfinite() when a decode step wrote a non-finite output.  Read
+// and cleared by decode_status (mesa_decode_status).
+__device__ unsigned g_decode_status = 0;
+}  // namespace mesa
+
+namespace mesa {
 
 template <int NW>
 __device__ __forceinline__ float block_sum(float v, float (*red)[NW], int buf, int warp,
@@ -178,6 +185,7 @@ __global__ void __launch_bounds__(4 * D) mesa_decode_kernel(DecArgs a) {
     for (int o = LPR / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
     if (owner) st(out, (size_t)u * D + row[p], t);
     if (owner && a.Xs) a.Xs[(size_t)u * D + row[p]] = xr[p];
+    if (owner && !isfinite(t)) atomicOr(&g_decode_status, tc_err_nonfinite());
   }
   if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
 }
@@ -374,6 +382,7 @@ __global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
   const float o = rowsum(s);
   if ((lane & 1) == 0) st((TIO *)a.out, (size_t)u * D + row, o);
   if ((lane & 1) == 0 && a.Xs) a.Xs[(size_t)u * D + row] = xr;
+  if ((lane & 1) == 0 && !isfinite(o)) atomicOr(&g_decode_status, tc_err_nonfinite());
   if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
 }
 
@@ -404,6 +413,17 @@ static int launch_dec_t(const DecArgs &a, cudaStream_t st) {
   }
   timing_mark_end(K_DECODE, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int decode_status(cudaStream_t st, unsigned *flags) {
+  static const unsigned zero = 0;
+  if (cudaMemcpyFromSymbolAsync(flags, g_decode_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaMemcpyToSymbolAsync(g_decode_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return -1;
+  return 0;
 }
 
 int launch_decode(const DecArgs &a, cudaStream_t st) {

@@ -26,6 +26,7 @@ struct StateMisc {
   float w[128];
   float red[48];
   uint64_t mbar;
+  uint64_t mbar_drain;  // after a give-up: completion of every multiply issued (thread 0)
   uint32_t tmem_base;
 };
 }  // namespace
@@ -50,7 +51,10 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
   const int row = 32 * (warp & 3) + lane, cg = warp >> 2;
 
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 256);
-  if (tid == 0) tc::mbar_init(aBar, 1);
+  if (tid == 0) {
+    tc::mbar_init(aBar, 1);
+    tc::mbar_init(tc::smem_u32(&m->mbar_drain), 1);
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -71,7 +75,7 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     tc::mma_commit(aBar);
   };
   auto wait = [&]() -> bool {
-    const bool done = tc::mbar_wait(aBar, phase);
+    const bool done = tc::mbar_wait(aBar, phase, a.wait_limit);
     phase ^= 1;
     tc::fence_after_sync();
     const int bad = __syncthreads_or(!done);
@@ -171,6 +175,9 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     }
     if (tid == 0) ws.Lc[(size_t)u * NC + c] = Lsum;
   }
+  // a wait gave up (the same outcome in every thread): let the multiplies still in flight
+  // finish before the tensor memory is released
+  if (!ok) tc::drain_mmas(tc::smem_u32(&m->mbar_drain), tid == 0, status);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_free(tbase, 256);

@@ -20,7 +20,13 @@ struct FwdArgs {
   int32_t *iters;
   const float *H0, *G0;
   float *H_final, *G_final;
+  unsigned *status = nullptr;  // device status word (error bits of tc_common.cuh) or nullptr
+  unsigned wait_limit = 0;     // polls of a bounded mbarrier wait (tensor-core kernels)
 };
+
+// Polls of the tensor-core kernels' bounded waits for the next launches: the default, or the
+// value set through mesa_debug_set_wait_limit (a test hook).
+unsigned wait_limit();
 
 // Solves of the backward pass (a separate kernel argument, so that the forward's argument
 // block is unchanged): rhs != nullptr replaces q by fp32 right-hand sides [U, T, dk];
@@ -42,6 +48,11 @@ struct DecArgs {
   void *out;
   int32_t *iters;
 };
+
+// The decode kernels' device status word (one per device, shared by every decode call on
+// it): `flags` receives it and it is cleared, both ordered on `st`, which is then
+// synchronised.  Returns 0, or -1 when a copy failed.
+int decode_status(cudaStream_t st, unsigned *flags);
 
 // Backward pass (chunks of kBwdChunk tokens; the states, log-decays and solves come from the
 // forward pipeline run at that chunk length).

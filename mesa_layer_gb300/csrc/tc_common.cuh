@@ -10,9 +10,14 @@
 namespace mesa {
 namespace tc {
 
-// Error bits written to the device status word when a bounded wait gives up.
+// Error bits of the device status word: a bounded wait for matrix multiplies gave up; a
+// kernel wrote a non-finite output; the wait that drains in-flight multiplies after a
+// give-up expired as well (the tensor pipe did not answer).
 constexpr unsigned kErrMmaTimeout = 1u;
-// Polls of an mbarrier before giving up (each poll may itself suspend for a while).
+constexpr unsigned kErrNonFinite = 2u;
+constexpr unsigned kErrDrainTimeout = 4u;
+// Polls of an mbarrier before giving up (each poll may itself suspend for a while); the
+// launchers pass it unless a caller set another limit (mesa_debug_set_wait_limit).
 constexpr unsigned kWaitLimit = 1u << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -207,9 +212,11 @@ __device__ __forceinline__ void mbar_init(uint32_t mbar_saddr, uint32_t count) {
   asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 }
 
-// Wait until the phase with parity `parity` completes; false if the poll limit is hit.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar_saddr, uint32_t parity) {
-  for (unsigned i = 0; i < kWaitLimit; i++) {
+// Wait until the phase with parity `parity` completes; false after `limit` unsuccessful
+// polls (limit 0: give up at once, without polling).
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar_saddr, uint32_t parity,
+                                          unsigned limit = kWaitLimit) {
+  for (unsigned i = 0; i < limit; i++) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -220,6 +227,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar_saddr, uint32_t parity) 
     if (done) return true;
   }
   return false;
+}
+
+// After a bounded wait gave up, no matrix multiply of the CTA may still be in flight when its
+// tensor memory is released.  Every thread that issued multiplies (issuer == true) commits the
+// completion of all of them to `drain_bar` (initialised with the number of issuing threads);
+// then every thread of the block waits for that phase with the default limit.  Returns false
+// (and sets kErrDrainTimeout) if even that wait expires.  Block-wide: all threads call it.
+__device__ __forceinline__ bool drain_mmas(uint32_t drain_bar, bool issuer, unsigned *status) {
+  if (issuer) mma_commit(drain_bar);
+  const bool done = mbar_wait(drain_bar, 0, kWaitLimit);
+  fence_after_sync();
+  const int bad = __syncthreads_or(!done);
+  if (bad && threadIdx.x == 0) atomicOr(status, kErrDrainTimeout);
+  return !bad;
 }
 
 // ---- fp16 splitting -------------------------------------------------------------------

@@ -18,6 +18,7 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t *As = sm, *Bs = sm + 32768;
   uint64_t *mbar = reinterpret_cast<uint64_t *>(sm + 65536);
   uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + 65544);
+  uint64_t *drain = reinterpret_cast<uint64_t *>(sm + 65552);
   const int tid = threadIdx.x, warp = tid >> 5;
   for (int e = tid; e < 128 * 128; e += blockDim.x) {
     const int r = e >> 7, c = e & 127;
@@ -25,7 +26,10 @@ __global__ void __launch_bounds__(128, 1)
     *reinterpret_cast<__half *>(Bs + tc::sw128_offset(r, c, 128)) = __float2half_rn(B[e]);
   }
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(tslot), 512);
-  if (tid == 0) tc::mbar_init(tc::smem_u32(mbar), 1);
+  if (tid == 0) {
+    tc::mbar_init(tc::smem_u32(mbar), 1);
+    tc::mbar_init(tc::smem_u32(drain), 1);
+  }
   tc::fence_smem_to_async();
   tc::fence_before_sync();
   __syncthreads();
@@ -44,16 +48,21 @@ __global__ void __launch_bounds__(128, 1)
       tc::mma_f16(tbase + 256, tc::mnmajor_desc(aA, 128, s), tc::mnmajor_desc(aB, 128, s), id3, s > 0);
     tc::mma_commit(tc::smem_u32(mbar));
   }
-  const bool ok = tc::mbar_wait(tc::smem_u32(mbar), 0);
+  const bool ok = !__syncthreads_or(!tc::mbar_wait(tc::smem_u32(mbar), 0));
   tc::fence_after_sync();
-  if (!ok) atomicOr(status, tc::kErrMmaTimeout);
+  if (!ok) {  // give up: wait for the multiplies in flight, write zeros
+    if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
+    tc::drain_mmas(tc::smem_u32(drain), tid == 0, status);
+  }
   const uint32_t tl = tbase + ((uint32_t)(32 * warp) << 16);
   for (int half = 0; half < 3; half++) {
     float *C = half == 0 ? C1 : (half == 1 ? C2 : C3);
     for (int cc = 0; cc < 4; cc++) {
-      float v[32];
-      tc::tmem_ld32(tl + half * 128 + cc * 32, v);
-      tc::tmem_ld_wait();
+      float v[32] = {};
+      if (ok) {
+        tc::tmem_ld32(tl + half * 128 + cc * 32, v);
+        tc::tmem_ld_wait();
+      }
       for (int k = 0; k < 32; k++) C[tid * 128 + cc * 32 + k] = ok ? v[k] : 0.0f;
     }
   }

@@ -42,6 +42,17 @@ def test_version_and_status_strings(lib):
     assert lib.mesa_version() >= 100
     assert lib.mesa_status_string(0) == b"ok"
     assert lib.mesa_status_string(3).startswith(b"workspace")
+    assert b"wait" in lib.mesa_status_string(5) and b"non-finite" in lib.mesa_status_string(6)
+
+
+def test_status_queries_and_wait_limit_hook_validate_on_the_host(lib):
+    """The status queries reject a null flags pointer before touching a stream, and the
+    wait-limit hook only records a host-side number (range-checked)."""
+    assert lib.mesa_decode_status(None, None) == 1
+    assert lib.mesa_forward_status(None, None, None) == 1
+    assert lib.mesa_debug_set_wait_limit(1 << 33) == 1
+    assert lib.mesa_debug_set_wait_limit(0) == 0
+    assert lib.mesa_debug_set_wait_limit(-1) == 0
 
 
 def test_workspace_size(lib):
