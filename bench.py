@@ -39,9 +39,10 @@ from mesa_layer_gb300 import synth  # noqa: E402
 
 METRIC = "Mesa-layer fwd tokens/s on 1 GB300 (per CG iters) + % tensor/HBM roofline"
 METRIC_BWD = "Mesa-layer bwd (all gradients) tokens/s on 1 GB300 (per CG iters) + % roofline of the top kernel"
-DEFAULT_WORKLOAD = "fwd_fp32_d64"
-SM_COUNT = 152
+# the largest configuration that fits one GPU: B=1, 16 heads, T=65536, d=128, bf16, dynamic CG
+DEFAULT_WORKLOAD = "long_bf16_d128"
 FP32_LANES_PER_SM = 128
+ORACLE_MAX_T = 8192  # the CPU oracle's timed sample takes at most this many tokens per unit
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -278,10 +279,12 @@ def oracle_sample(w, budget_s: float = 20.0):
         return units * steps / dt / w.H, min(threads, units), f"{units} (sequence, head) units x {steps} steps", dt
     # forward: whole units (sequences are sequential in t); the unit count grows until one
     # pass takes a good part of the budget, then passes repeat until the budget is used
-    full = synth.forward_inputs(w) if w.B * w.H * w.T <= (1 << 22) else None
+    # a long sequence is sampled as its first ORACLE_MAX_T tokens (the oracle's cost per
+    # token does not depend on the position)
+    T = min(w.T, ORACLE_MAX_T)
+    full = synth.forward_inputs(w) if w.B * w.H * w.T <= (1 << 22) and T == w.T else None
     U = w.B * w.H
     n_units = min(U, max(1, threads))
-    T = w.T
     total_th, total_t, passes = 0, 0.0, 0
     while True:
         if full is not None:
@@ -301,7 +304,8 @@ def oracle_sample(w, budget_s: float = 20.0):
         passes += 1
         if total_t >= budget_s or dt > budget_s / 2:
             break
-    desc = f"{passes} pass(es) over {n_units} (batch, head) units x {T} tokens"
+    desc = f"{passes} pass(es) over {n_units} (batch, head) units x {T} tokens" + (
+        f" (the first {T} of each unit's {w.T})" if T < w.T else "")
     # tokens/s of the workload = token-heads/s divided by the heads per token
     return total_th / total_t / w.H, min(threads, n_units), desc, total_t
 
@@ -327,6 +331,18 @@ def run_reference(args, rank, world):
             "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def arithmetic(w) -> str:
+    """What the timed path computes in, for the line's config."""
+    if w.conv_taps:
+        return f"{w.dtype} in and out, fp32 convolution and norm"
+    if w.decode_steps:
+        return f"{w.dtype} q/k/v, fp32 states and CG (CUDA cores)"
+    if w.dtype == "bf16" and w.dk == 128:
+        return ("bf16 inputs; tensor-core products of fp16 hi+lo split operands with fp32 "
+                "accumulation; fp32 CG vectors and scalars")
+    return f"{w.dtype} inputs, fp32 CUDA-core arithmetic"
 
 
 def workload_config(w, extra=None):
@@ -396,6 +412,7 @@ def main():
     names = kind_names(lib)
     dev = torch.device("cuda", local)
     peaks = measured_peaks()
+    peaks["sm_count"] = torch.cuda.get_device_properties(dev).multi_processor_count
     if w.conv_taps:
         res = bench_preprocess(args, w, rank, world, dev, lib, torch, binding)
     elif w.backward:
@@ -752,14 +769,17 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
                     "peak_source": f"{peaks['source']} bf16 dense (fp16 kind, same rate)",
                     "executed_tensor_tflops": tc_executed_flops(w, it, not w.backward) / (avg_ms / 1e3) / 1e12}
         else:
-            peak = SM_COUNT * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+            sms = peaks["sm_count"]
+            peak = sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
             roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": traffic, "kernel": top_name,
-                    "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flop x max SM clock"}
+                    "peak_source": f"fp32 FMA: {sms} SMs (device) x 128 lanes x 2 flop x max SM clock"}
     kernels = {names[i] if i < len(names) else f"kind{i}": {"ms_per_step": kind_ms[i] / args.steps,
                                                              "launches": kind_n[i]}
                for i in range(len(kind_ms)) if kind_n[i] > 0}
     extra = {} if w.conv_taps else {"mean_iters": float(it.mean()), "max_iters": int(it.max())}
+    extra["sm_count"] = peaks["sm_count"]
+    extra["arithmetic"] = arithmetic(w)
     extra.update(res.get("extra", {}))
     extra.update({
              "l2": ("flushed between timed steps (256 MiB device write)" if res["flush"]
@@ -767,7 +787,7 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
              "kernels": kernels, "wall_s_timed_loop": res["wall_s"]})
     line = {"metric": METRIC_BWD if w.backward else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, see mesa_layer_gb300/synth.py)",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded, see mesa_layer_gb300/synth.py)",
             "config": workload_config(w, extra), "roofline": roof, "cpu_baseline": cpu,
             "gpu_launches": int(sum(kind_n)), "launches_per_step": launches_per_step,
             "clocks": res["clocks"]}
