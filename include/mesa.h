@@ -250,9 +250,11 @@ int mesa_forward_chunked_noalloc(int B, int H, int T, int dk, int dv, int dtype,
  * when the word could not be read).
  *
  * Non-finite inputs: the call still ends (in dynamic mode a token whose residual is NaN runs
- * to cg_iters).  A NaN or infinity in q_t affects o_t alone.  One in k_t, v_t or gamma_t of
- * a unit leaves that unit's tokens before the 128-token block holding t, and every other
- * unit, unchanged; later outputs of the unit are unspecified (non-finite in general).
+ * to cg_iters).  A NaN or infinity in q_t affects o_t alone (non-finite in general; zero when
+ * an infinite query meets the dynamic stopping rule at once, inf <= tol * inf).  One in k_t,
+ * v_t or gamma_t (a NaN gate stays NaN) leaves that unit's tokens before the 128-token block
+ * holding t, and every other unit, unchanged; later outputs of the unit are unspecified
+ * (non-finite in general).
  */
 int mesa_forward_status(const void *workspace, cudaStream_t stream, unsigned *flags);
 

@@ -12,7 +12,10 @@ namespace mesa {
 // log-decays keep differences l_i - l_j free of inf - inf.
 constexpr float kLogGateFloor = -80.0f;
 
-__device__ __forceinline__ float log_gate(float g) { return fmaxf(logf(g), kLogGateFloor); }
+// A NaN gate stays NaN (fmaxf alone would turn it into the floor, i.e. a closed gate).
+__device__ __forceinline__ float log_gate(float g) {
+  return isnan(g) ? g : fmaxf(logf(g), kLogGateFloor);
+}
 
 // Device status-word bit for a non-finite output (the same value as tc::kErrNonFinite).
 __host__ __device__ constexpr unsigned tc_err_nonfinite() { return 2u; }
