@@ -270,11 +270,12 @@ int mesa_decode_status(cudaStream_t stream, unsigned *flags);
 
 /*
  * Test hook (no counterpart on the MesaNet pages): the number of polls after which the
- * tensor-core kernels' waits for their matrix multiplies give up, for the launches that
- * follow in this process; polls < 0 restores the default (2^22), 0 gives up at the first
- * wait.  A give-up is reported through mesa_forward_status (MESA_ERR_TIMEOUT) and leaves the
- * device usable: the kernel waits, with the default limit, for its multiplies in flight,
- * then returns.  Process-wide, not thread-safe; MESA_ERR_INVALID_ARG above 2^32 - 1.
+ * tensor-core kernels' waits for their matrix multiplies and bulk copies give up, for the
+ * launches that follow in this process; polls < 0 restores the default (2^22), 0 gives up
+ * at the first wait.  A give-up is reported through mesa_forward_status (MESA_ERR_TIMEOUT)
+ * and leaves the device usable: the kernel waits, with the default limit, for its multiplies
+ * and copies in flight, then returns.  Process-wide, not thread-safe; MESA_ERR_INVALID_ARG
+ * above 2^32 - 1.
  */
 int mesa_debug_set_wait_limit(long long polls);
 

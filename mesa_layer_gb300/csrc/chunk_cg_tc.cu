@@ -14,6 +14,11 @@
 // fp32.  The CG scalars and the x, r vectors stay fp32 (r in tensor memory, x in shared
 // memory); the P operand of the two products that read it lives in tensor memory.
 //
+// Operand tiles arrive by bulk copies (the tensor memory accelerator, untiled form): the
+// chunk's key and query rows and the state S^H_{c-1} (with its segment carry) are copied raw
+// into shared-memory regions that the CG uses only later (the x, Z and S regions) and staged
+// from there as MMA operands; S^G_{c-1} for the readout likewise, once x is in registers.
+//
 // One CTA of 512 threads per chunk.  Warp w reads tensor-memory lane quadrant q = w % 4
 // (token rows 32q .. 32q+31, one row per lane) and column group g = w / 4 (32 of the 128
 // columns), so each token row is handled by 4 threads in 4 warps; their per-row partial
@@ -103,6 +108,7 @@ struct Misc {
   uint64_t mbar_y;   // Y = Z K
   uint64_t mbar_u;   // U = P S
   uint64_t mbar_drain;  // after a give-up: completion of every multiply issued (2 issuers)
+  uint64_t mbar_ld;     // bulk copies of the chunk's operands (phase 0) and of S^G (phase 1)
   uint32_t tmem_base;
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc block too large");
@@ -183,7 +189,8 @@ __global__ void __launch_bounds__(512, 1)
   Misc *m = reinterpret_cast<Misc *>(sm + OFF_MISC);
   const uint32_t aBarW1 = tc::smem_u32(&m->mbar_w1), aBarW2 = tc::smem_u32(&m->mbar_w2);
   const uint32_t aBarY = tc::smem_u32(&m->mbar_y), aBarU = tc::smem_u32(&m->mbar_u);
-  const uint32_t aBarDrain = tc::smem_u32(&m->mbar_drain);
+  const uint32_t aBarDrain = tc::smem_u32(&m->mbar_drain), aBarLd = tc::smem_u32(&m->mbar_ld);
+  const uint32_t sbase = tc::smem_u32(sm);
   const unsigned wlim = a.wait_limit;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -238,22 +245,6 @@ __global__ void __launch_bounds__(512, 1)
 
   // ---- set-up: tensor memory, barriers, per-chunk constants --------------------------
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 512);
-  if (tid == 0) {
-    tc::mbar_init(aBarW1, 1);
-    tc::mbar_init(aBarW2, 1);
-    tc::mbar_init(aBarY, 1);
-    tc::mbar_init(aBarU, 1);
-    tc::mbar_init(aBarDrain, 2);  // threads 0 (W, Y) and 128 (U) issue the multiplies
-  }
-  bool small = true;  // |l2| <= 100: D_ij = 2^{l2_i} 2^{-l2_j} without overflow
-  if (tid < TILE) {
-    const float l2 = (tid < Tv ? ws.ell[tokbase + tid] : 0.0f) * kLog2e;
-    m->ell2[tid] = l2;
-    m->e2c[tid] = tid < Tv ? exp2f(-l2) : 0.0f;
-    small = fabsf(l2) <= 100.0f;
-  }
-  if (tid >= 256 && tid < 256 + DH) m->lam[tid - 256] = a.lambda[(size_t)(u % a.H) * DH + tid - 256];
-
   // S_{c-1}: the segment-local state plus exp(Lc) times the carry into its segment
   const float *SH = nullptr, *SG = nullptr, *CH = nullptr, *CG = nullptr;
   float cf = 0.0f;
@@ -270,37 +261,38 @@ __global__ void __launch_bounds__(512, 1)
     SH = a.H0 + (size_t)u * DH * DH;
     SG = a.G0 + (size_t)u * DH * DH;
   }
-  // loads in flight together: this thread's query columns, the key tile, the state; the
-  // readout's state is only needed after the CG and is fetched into L2 meanwhile
-  uint4 qraw[NV];
-  {
-    const uint4 *src = reinterpret_cast<const uint4 *>(q + (tokbase + i) * DH + c0);
-#pragma unroll
-    for (int g = 0; g < NV; g++) qraw[g] = (valid && !(SOLVE && sv.rhs)) ? src[g] : make_uint4(0, 0, 0, 0);
+  const float *SHu = RHS ? nullptr : SH, *CHu = RHS ? nullptr : CH;  // (RHS: no CG, no S^H)
+  const bool load_q = !(SOLVE && sv.rhs);
+  constexpr uint32_t MAT32 = sizeof(float) * DH * DH;  // one fp32 state (64 KB)
+  const uint32_t rows_bytes = (uint32_t)Tv * DH * 2;     // Tv bf16 rows
+  if (tid == 0) {
+    tc::mbar_init(aBarW1, 1);
+    tc::mbar_init(aBarW2, 1);
+    tc::mbar_init(aBarY, 1);
+    tc::mbar_init(aBarU, 1);
+    tc::mbar_init(aBarDrain, 2);  // threads 0 (W, Y) and 128 (U) issue the multiplies
+    tc::mbar_init(aBarLd, 1);
+    // this chunk's operands by bulk copies, raw: the keys and the queries (bf16 rows) into
+    // the x region, S^H_{c-1} into the Z region, its segment carry into the S region (all
+    // three regions are written only after these are read)
+    tc::fence_smem_to_async();
+    tc::mbar_arrive_expect_tx(aBarLd, rows_bytes * (load_q ? 2 : 1) + (SHu ? MAT32 : 0) + (CHu ? MAT32 : 0));
+    tc::bulk_g2s(sbase + OFF_X, k + tokbase * DH, rows_bytes, aBarLd);
+    if (load_q) tc::bulk_g2s(sbase + OFF_X + MAT_BYTES, q + tokbase * DH, rows_bytes, aBarLd);
+    if (SHu) tc::bulk_g2s(sbase + OFF_ZHI, SHu, MAT32, aBarLd);
+    if (CHu) tc::bulk_g2s(sbase + OFF_SHI, CHu, MAT32, aBarLd);
   }
-  tc::Rows8 kr;
-  tc::load_rows(k + tokbase * DH, Tv, kr);
+  bool small = true;  // |l2| <= 100: D_ij = 2^{l2_i} 2^{-l2_j} without overflow
+  if (tid < TILE) {
+    const float l2 = (tid < Tv ? ws.ell[tokbase + tid] : 0.0f) * kLog2e;
+    m->ell2[tid] = l2;
+    m->e2c[tid] = tid < Tv ? exp2f(-l2) : 0.0f;
+    small = fabsf(l2) <= 100.0f;
+  }
+  if (tid >= 256 && tid < 256 + DH) m->lam[tid - 256] = a.lambda[(size_t)(u % a.H) * DH + tid - 256];
+  // the readout's state is only needed after the CG and is fetched into L2 meanwhile
   tc::prefetch_l2(SG, sizeof(float) * DH * DH);
   tc::prefetch_l2(CG, sizeof(float) * DH * DH);
-  float sS, sK;
-  {
-    tc::Mat32 S;
-    tc::load_mat(RHS ? nullptr : SH, RHS ? nullptr : CH, cf, S);  // (RHS: no CG, no S^H)
-    float mS = tc::mat_absmax(S), mK = tc::rows_absmax(kr, nullptr), unused = 0.0f;
-    tc::block_max3(mS, mK, unused, m->red);
-    sS = 1.0f / tc::pow2_ceil(mS);
-    sK = 1.0f / tc::pow2_ceil(mK);
-    tc::store_mat(S, sS, Shi, NTERMS == 2 ? Slo : nullptr);
-    tc::store_rows(kr, nullptr, sK, Ks, nullptr);
-  }
-  if (z_upper) {
-#pragma unroll
-    for (int g = 0; g < NV; g++) {
-      const uint32_t off = tc::sw128_offset(i, c0 + 8 * g, TILE);
-      *reinterpret_cast<uint4 *>(Zhi + off) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4 *>(Zlo + off) = make_uint4(0, 0, 0, 0);
-    }
-  }
   {  // CTAs start in block order as SMs free up (one per SM), so the chunk `lookahead`
      // blocks on runs about one wave later: its inputs go into L2 now
     const long long wn = (long long)blockIdx.x + (long long)NC * blockIdx.y + lookahead;
@@ -317,6 +309,46 @@ __global__ void __launch_bounds__(512, 1)
       tc::prefetch_l2(k + tbn * DH, sizeof(__nv_bfloat16) * DH * Tn);
       tc::prefetch_l2(q + tbn * DH, sizeof(__nv_bfloat16) * DH * Tn);
       tc::prefetch_l2(ws.ell + tbn, sizeof(float) * Tn);
+    }
+  }
+  __syncthreads();  // barrier initialisations (and the per-chunk constants) visible
+  // Bounded wait for the copies; on a give-up the block waits (default limit) until they have
+  // landed, so that nothing writes this CTA's shared memory after it ends, and skips the chunk.
+  bool failed = false;
+  if (__syncthreads_or(!tc::mbar_wait(aBarLd, 0, wlim))) {
+    failed = true;
+    if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
+    if (__syncthreads_or(!tc::mbar_wait(aBarLd, 0, tc::kWaitLimit)) && tid == 0)
+      atomicOr(status, tc::kErrDrainTimeout);
+  }
+  uint32_t phLd = 1;
+  // this thread's query columns, the key tile and the state, from the staged copies
+  uint4 qraw[NV];
+  {
+    const uint8_t *qrow = sm + OFF_X + MAT_BYTES + (size_t)i * DH * 2 + c0 * 2;
+#pragma unroll
+    for (int g = 0; g < NV; g++)
+      qraw[g] = (valid && load_q) ? *reinterpret_cast<const uint4 *>(qrow + 16 * g) : make_uint4(0, 0, 0, 0);
+  }
+  tc::Rows8 kr;
+  tc::load_rows_smem(sm + OFF_X, Tv, kr);
+  float sS, sK;
+  {
+    tc::Mat32 S;
+    tc::load_mat_smem(SHu ? sm + OFF_ZHI : nullptr, CHu ? sm + OFF_SHI : nullptr, cf, S);
+    float mS = tc::mat_absmax(S), mK = tc::rows_absmax(kr, nullptr), unused = 0.0f;
+    tc::block_max3(mS, mK, unused, m->red);  // (its barrier: every staged copy has been read)
+    sS = 1.0f / tc::pow2_ceil(mS);
+    sK = 1.0f / tc::pow2_ceil(mK);
+    tc::store_mat(S, sS, Shi, NTERMS == 2 ? Slo : nullptr);
+    tc::store_rows(kr, nullptr, sK, Ks, nullptr);
+  }
+  if (z_upper) {
+#pragma unroll
+    for (int g = 0; g < NV; g++) {
+      const uint32_t off = tc::sw128_offset(i, c0 + 8 * g, TILE);
+      *reinterpret_cast<uint4 *>(Zhi + off) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4 *>(Zlo + off) = make_uint4(0, 0, 0, 0);
     }
   }
   tc::fence_before_sync();
@@ -377,7 +409,6 @@ __global__ void __launch_bounds__(512, 1)
   // (in the descriptor's 16-byte units): a tile's offset, and for k-step s (K-major)
   // (s / 4) 64-column blocks of 16 KB + (s % 4) 32 B, or (MN-major) 16 rows of 128 B.
   // Built by the issuing thread only, so that no register holds them across the loop.
-  const uint32_t sbase = tc::smem_u32(sm);
   auto kdesc = [&](uint32_t off, int s) -> uint64_t {
     return tc::kmajor_desc(sbase, TILE, 0) + (uint64_t)((off >> 4) + (s >> 2) * (TILE * 128 / 16) + (s & 3) * 2);
   };
@@ -531,7 +562,6 @@ __global__ void __launch_bounds__(512, 1)
   bool act = valid;
   int cnt = 0;
   const bool dynamic = a.cg_tol > 0.0f;
-  bool failed = false;
   // x += alpha p of an iteration is applied at the start of the next (its tensor-memory
   // traffic then overlaps the next W = P K^T) or after the last one
   float p[CW];
@@ -551,7 +581,7 @@ __global__ void __launch_bounds__(512, 1)
   };
 
   // ---- CG iterations ---------------------------------------------------------------------
-  for (int it = 0; it < a.cg_iters; it++) {
+  for (int it = 0; it < a.cg_iters && !failed; it++) {
     if (dynamic && act && sqrtf(rho) <= a.cg_tol * nq) act = false;
     tc::fence_smem_to_async();
     tc::fence_before_sync();
@@ -688,6 +718,16 @@ __global__ void __launch_bounds__(512, 1)
         xx[4 * g4 + 3] = x4.w;
       }
     }
+    // The x region is free once every thread holds its x, the S region once the last state
+    // product is done: S^G_{c-1} and its segment carry come in there by bulk copies.
+    const uint32_t gbytes = (SG ? MAT32 : 0) + (CG ? MAT32 : 0);
+    tc::fence_smem_to_async();
+    __syncthreads();
+    if (tid == 0 && gbytes) {
+      tc::mbar_arrive_expect_tx(aBarLd, gbytes);
+      if (SG) tc::bulk_g2s(sbase + OFF_X, SG, MAT32, aBarLd);
+      if (CG) tc::bulk_g2s(sbase + OFF_SHI, CG, MAT32, aBarLd);
+    }
     if constexpr (SAVE) {
       if (valid) {
         float4 *dst = reinterpret_cast<float4 *>(sv.x_out + (tokbase + i) * DH + c0);
@@ -707,12 +747,20 @@ __global__ void __launch_bounds__(512, 1)
     tc::tmem_st_wait();
     float sG, sV;
     tc::Rows8 vr;
+    tc::load_rows(v + tokbase * DH, Tv, vr);
+    if (gbytes && __syncthreads_or(!tc::mbar_wait(aBarLd, phLd, wlim))) {
+      // give up on the readout, once the copies have landed (default limit)
+      failed = true;
+      if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
+      if (__syncthreads_or(!tc::mbar_wait(aBarLd, phLd, tc::kWaitLimit)) && tid == 0)
+        atomicOr(status, tc::kErrDrainTimeout);
+    }
+    phLd ^= 1;
     {
       tc::Mat32 G;
-      tc::load_mat(SG, CG, cf, G);
-      tc::load_rows(v + tokbase * DH, Tv, vr);
+      tc::load_mat_smem(SG ? sm + OFF_X : nullptr, CG ? sm + OFF_SHI : nullptr, cf, G);
       float mG = tc::mat_absmax(G), mV = tc::rows_absmax(vr, nullptr), unused = 0.0f;
-      tc::block_max3(mG, mV, unused, m->red);
+      tc::block_max3(mG, mV, unused, m->red);  // (its barrier: the staged copies have been read)
       sG = 1.0f / tc::pow2_ceil(mG);
       sV = 1.0f / tc::pow2_ceil(mV);
       tc::store_mat(G, sG, Shi, NTERMS == 2 ? Slo : nullptr);
@@ -721,9 +769,9 @@ __global__ void __launch_bounds__(512, 1)
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (tid == 0) issue_W();
+    if (tid == 0 && !failed) issue_W();
     __syncwarp();
-    const bool okW = wait_W();
+    const bool okW = !failed && wait_W();
     if (tid == 128 && okW) issue_U();
     const float zs = build_z(mX, okW);
     // X K^T is complete once every warp that waits on its halves has passed the barrier

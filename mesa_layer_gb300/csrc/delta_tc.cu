@@ -9,6 +9,8 @@
 // by the change of operand scale), adds the chunk's sums with two 128x128x128 MMAs each
 // (A = (w x)^T read MN-major from the token-major tile, x = k or v, split hi + lo fp16;
 // B = K read MN-major, fp16, exact after a power-of-two scale), and writes the state.
+// The raw key and value rows of the next chunk arrive by bulk copies (tensor memory
+// accelerator) into staging buffers while the current chunk's MMAs and write-out run.
 // Segment 0 starts from the initial state, later segments from zero; mesa_carry_tc_kernel then
 // chains the segments (carry[s] = global state before segment s) and writes the final state,
 // and the CG kernel adds exp(Lc) carry when it loads a state.
@@ -21,12 +23,15 @@ namespace mesa {
 
 namespace {
 constexpr uint32_t DT_MAT = 128 * 128 * 2;
-constexpr uint32_t DT_SMEM = 3 * DT_MAT + 1024 + 1024;
+// K operand | A hi | A lo | misc (1 KB) | raw key rows | raw value rows, + alignment slack
+constexpr uint32_t DT_STAGE = 3 * DT_MAT + 1024;
+constexpr uint32_t DT_SMEM = DT_STAGE + 2 * DT_MAT + 1024;
 struct StateMisc {
   float w[128];
   float red[48];
   uint64_t mbar;
   uint64_t mbar_drain;  // after a give-up: completion of every multiply issued (thread 0)
+  uint64_t mbar_ld;     // bulk copies of a chunk's raw key and value rows
   uint32_t tmem_base;
 };
 }  // namespace
@@ -39,6 +44,9 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t *Ks = sm, *Ahi = sm + DT_MAT, *Alo = sm + 2 * DT_MAT;
   StateMisc *m = reinterpret_cast<StateMisc *>(sm + 3 * DT_MAT);
+  static_assert(sizeof(StateMisc) <= 1024, "misc block too large");
+  const uint8_t *Kraw = sm + DT_STAGE, *Vraw = sm + DT_STAGE + DT_MAT;
+  const uint32_t aKraw = tc::smem_u32(Kraw), aVraw = tc::smem_u32(Vraw), aLd = tc::smem_u32(&m->mbar_ld);
   const uint32_t aK = tc::smem_u32(Ks), aAhi = tc::smem_u32(Ahi), aAlo = tc::smem_u32(Alo);
   const uint32_t aBar = tc::smem_u32(&m->mbar);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -51,10 +59,22 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
   const int row = 32 * (warp & 3) + lane, cg = warp >> 2;
 
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 256);
+  // raw key and value rows of chunk c into the staging buffers by bulk copies (thread 0)
+  auto fetch = [&](int c) {
+    const size_t tb = (size_t)u * T + (size_t)c * TILE;
+    const uint32_t bytes = (uint32_t)min(TILE, T - c * TILE) * DH * 2;
+    tc::mbar_arrive_expect_tx(aLd, 2 * bytes);
+    tc::bulk_g2s(aKraw, (const __nv_bfloat16 *)a.k + tb * DH, bytes, aLd);
+    tc::bulk_g2s(aVraw, (const __nv_bfloat16 *)a.v + tb * DH, bytes, aLd);
+  };
   if (tid == 0) {
     tc::mbar_init(aBar, 1);
     tc::mbar_init(tc::smem_u32(&m->mbar_drain), 1);
+    tc::mbar_init(aLd, 1);
+    fetch(c_begin);
   }
+  uint32_t phLd = 0;
+  bool pending = true;  // a fetch is in flight
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -107,25 +127,37 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     tc::tmem_st_wait();
   };
 
-  // keys and values of the next chunk are loaded into registers while the current chunk's
-  // MMAs run
+  // the keys and values of the next chunk come in by bulk copies while the current chunk's
+  // MMAs and write-out run
   tc::Rows8 kr, vr;
-  {
-    const size_t tb = (size_t)u * T + (size_t)c_begin * TILE;
-    const int Tv = min(TILE, T - c_begin * TILE);
-    tc::load_rows((const __nv_bfloat16 *)a.k + tb * DH, Tv, kr);
-    tc::load_rows((const __nv_bfloat16 *)a.v + tb * DH, Tv, vr);
-  }
   for (int c = c_begin; c < c_end && ok; c++) {
     const bool first = c == c_begin;
     const float *H0 = (seg == 0) ? a.H0 : nullptr;
     const float *G0 = (seg == 0) ? a.G0 : nullptr;
     const int t0 = c * TILE, Tv = min(TILE, T - t0);
     const size_t tokbase = (size_t)u * T + t0;
+    // this chunk's rows (bounded wait; on a give-up the copies are waited for with the default
+    // limit before the block stops)
+    const bool got = tc::mbar_wait(aLd, phLd, a.wait_limit);
+    if (__syncthreads_or(!got)) {
+      if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
+      if (__syncthreads_or(!tc::mbar_wait(aLd, phLd, tc::kWaitLimit)) && tid == 0)
+        atomicOr(status, tc::kErrDrainTimeout);
+      pending = false;
+      ok = false;
+      break;
+    }
+    phLd ^= 1;
+    pending = false;
+    tc::load_rows_smem(Kraw, Tv, kr);
+    tc::load_rows_smem(Vraw, Tv, vr);
     const float lend = ws.ell[tokbase + Tv - 1];
     const float ac = expf(lend);
     if (tid < TILE) m->w[tid] = tid < Tv ? expf(lend - ws.ell[tokbase + tid]) : 0.0f;
-    __syncthreads();
+    tc::fence_smem_to_async();
+    __syncthreads();  // (also: every thread holds its rows, the staging buffers are free)
+    if (tid == 0 && c + 1 < c_end) fetch(c + 1);
+    pending = c + 1 < c_end;
     float mk = tc::rows_absmax(kr, nullptr), mak = tc::rows_absmax(kr, m->w),
           mav = tc::rows_absmax(vr, m->w);
     tc::block_max3(mk, mak, mav, m->red);
@@ -149,12 +181,6 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) issue(128, !first || G0 != nullptr);
-    if (c + 1 < c_end) {  // next chunk's rows, in flight during the MMAs and the write-out
-      const size_t tb = tokbase + TILE;
-      const int Tn = min(TILE, T - t0 - TILE);
-      tc::load_rows((const __nv_bfloat16 *)a.k + tb * DH, Tn, kr);
-      tc::load_rows((const __nv_bfloat16 *)a.v + tb * DH, Tn, vr);
-    }
     ok = wait();
     if (!ok) break;
     sigH = nsigH;
@@ -175,9 +201,13 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     }
     if (tid == 0) ws.Lc[(size_t)u * NC + c] = Lsum;
   }
-  // a wait gave up (the same outcome in every thread): let the multiplies still in flight
-  // finish before the tensor memory is released
-  if (!ok) tc::drain_mmas(tc::smem_u32(&m->mbar_drain), tid == 0, status);
+  // a wait gave up (the same outcome in every thread): let the multiplies and the copy still
+  // in flight finish before the tensor memory and the shared memory are released
+  if (!ok) {
+    tc::drain_mmas(tc::smem_u32(&m->mbar_drain), tid == 0, status);
+    if (pending && __syncthreads_or(!tc::mbar_wait(aLd, phLd, tc::kWaitLimit)) && tid == 0)
+      atomicOr(status, tc::kErrDrainTimeout);
+  }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_free(tbase, 256);

@@ -229,6 +229,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar_saddr, uint32_t parity,
   return false;
 }
 
+// ---- bulk copies (TMA, untiled) ------------------------------------------------------------
+// Arrive on the mbarrier (count 1) and add `bytes` to the transaction count its current phase
+// waits for; the phase completes when the arrivals and the bytes are both in.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar_saddr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar_saddr), "r"(bytes)
+               : "memory");
+}
+
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) from global memory into
+// this CTA's shared memory by the tensor memory accelerator; completion is signalled to the
+// mbarrier as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst_saddr, const void *src, uint32_t bytes,
+                                         uint32_t mbar_saddr) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          dst_saddr),
+      "l"(src), "r"(bytes), "r"(mbar_saddr)
+      : "memory");
+}
+
 // After a bounded wait gave up, no matrix multiply of the CTA may still be in flight when its
 // tensor memory is released.  Every thread that issued multiplies (issuer == true) commits the
 // completion of all of them to `drain_bar` (initialised with the number of issuing threads);

@@ -170,6 +170,16 @@ __device__ __forceinline__ void load_rows(const __nv_bfloat16 *src, int Tv, Rows
   }
 }
 
+// The same from a bf16 tile staged row-major in shared memory (rows >= Tv read as zero).
+__device__ __forceinline__ void load_rows_smem(const uint8_t *stage, int Tv, Rows8 &x) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int n = 0; n < 4; n++) {
+    const int e = 8 * t + 4096 * n;
+    x.v[n] = (e / DH < Tv) ? *reinterpret_cast<const uint4 *>(stage + 2 * e) : make_uint4(0, 0, 0, 0);
+  }
+}
+
 // max over this thread's values of |w_row * x|  (w == nullptr: |x|)
 __device__ __forceinline__ float rows_absmax(const Rows8 &x, const float *w) {
   const int t = threadIdx.x;
@@ -232,6 +242,25 @@ __device__ __forceinline__ void load_mat(const float *src, const float *add, flo
       x.v[n].z = fmaf(f, y.z, x.v[n].z);
       x.v[n].w = fmaf(f, y.w, x.v[n].w);
     }
+  }
+}
+
+// The same from fp32 matrices staged row-major in shared memory (src == nullptr: zero,
+// add == nullptr: nothing added).
+__device__ __forceinline__ void load_mat_smem(const uint8_t *src, const uint8_t *add, float f, Mat32 &x) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int n = 0; n < 8; n++) {
+    const int e = 8 * t + 4096 * (n >> 1) + 4 * (n & 1);
+    float4 v = src ? *reinterpret_cast<const float4 *>(src + 4 * e) : make_float4(0, 0, 0, 0);
+    if (add) {
+      const float4 y = *reinterpret_cast<const float4 *>(add + 4 * e);
+      v.x = fmaf(f, y.x, v.x);
+      v.y = fmaf(f, y.y, v.y);
+      v.z = fmaf(f, y.z, v.z);
+      v.w = fmaf(f, y.w, v.w);
+    }
+    x.v[n] = v;
   }
 }
 
