@@ -235,7 +235,7 @@ def oracle_sample(w, budget_s: float = 20.0):
     import oracle
 
     threads = oracle.max_threads()
-    if w.conv_taps:
+    if w.conv_taps and not w.fused:
         units = min(w.B * w.H, 8)
         inp = synth.preprocess_inputs(synth.workload(w.name, B=1, H=units))
         total, dt, passes = 0, 0.0, 0
@@ -293,7 +293,11 @@ def oracle_sample(w, budget_s: float = 20.0):
         else:
             sub = synth.forward_inputs(synth.workload(w.name, B=1, H=n_units, T=T))
             lam = sub["lam"]
+        pre = synth.preprocess_inputs(synth.workload(w.name, B=1, H=n_units, T=T)) if w.fused else None
         t0 = time.perf_counter()
+        if pre is not None:  # the preprocessing, then the layer (rounded to the dtype between)
+            sub["q"] = synth.round_bf16(oracle.qk_preprocess(pre["q_raw"], pre["wq"]).astype(np.float32))
+            sub["k"] = synth.round_bf16(oracle.qk_preprocess(pre["k_raw"], pre["wk"]).astype(np.float32))
         oracle.forward(sub["q"], sub["k"], sub["v"], sub["gamma"], lam, w.cg_iters, w.cg_tol, nthreads=threads)
         dt = time.perf_counter() - t0
         if n_units < U and dt < 0.25 * budget_s:
@@ -335,12 +339,13 @@ def run_reference(args, rank, world):
 
 def arithmetic(w) -> str:
     """What the timed path computes in, for the line's config."""
-    if w.conv_taps:
+    if w.conv_taps and not w.fused:
         return f"{w.dtype} in and out, fp32 convolution and norm"
     if w.decode_steps:
         return f"{w.dtype} q/k/v, fp32 states and CG (CUDA cores)"
     if w.dtype == "bf16" and w.dk == 128:
-        return ("bf16 inputs; tensor-core products of fp16 hi+lo split operands with fp32 "
+        return (("raw q, k preprocessed in fp32 and rounded to bf16 in the prologues; " if w.fused else "") +
+                "bf16 inputs; tensor-core products of fp16 hi+lo split operands with fp32 "
                 "accumulation; fp32 CG vectors and scalars")
     return f"{w.dtype} inputs, fp32 CUDA-core arithmetic"
 
@@ -359,7 +364,11 @@ def workload_config(w, extra=None):
         cfg["step"] = ("backward given the forward's kept iterates: second CG per token on G_t^T dout_t, "
                        "chunk states and state adjoints, dq/dk/dv/dgamma/dlambda")
         cfg["chunk"] = "32 (gradient kernels), 128 (tensor-core solves)"
-    if w.conv_taps:
+    if w.fused:
+        cfg["conv_taps"] = w.conv_taps
+        cfg["step"] = (f"query/key preprocessing (causal depthwise conv, {w.conv_taps} taps, + L2 norm) fused "
+                       "into the forward's prologues, then the layer")
+    elif w.conv_taps:
         cfg = {"workload": w.name, "B": w.B, "heads": w.H, "T": w.T, "d": w.dk, "qk_dtype": w.dtype,
                "conv_taps": w.conv_taps, "step": "q/k preprocessing: causal depthwise conv + L2 norm",
                "parallelism": "replicas"}
@@ -413,7 +422,7 @@ def main():
     dev = torch.device("cuda", local)
     peaks = measured_peaks()
     peaks["sm_count"] = torch.cuda.get_device_properties(dev).multi_processor_count
-    if w.conv_taps:
+    if w.conv_taps and not w.fused:
         res = bench_preprocess(args, w, rank, world, dev, lib, torch, binding)
     elif w.backward:
         res = bench_backward(args, w, rank, world, dev, lib, torch, binding)
@@ -465,19 +474,29 @@ def bench_forward(args, w, rank, world, dev, lib, torch, binding):
     import torch.distributed as dist
     inp = synth.forward_inputs(w, seed=rank)
     td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    if w.fused:  # raw queries and keys with their taps in place of q and k
+        pre = synth.preprocess_inputs(w, seed=rank)
+        inp["q"], inp["k"] = pre["q_raw"], pre["k_raw"]
+        inp["wq"], inp["wk"] = pre["wq"], pre["wk"]
     d_in = {k: torch.from_numpy(inp[k]).to(dev).to(td if k in ("q", "k", "v") else torch.float32).contiguous()
-            for k in ("q", "k", "v", "gamma", "lam")}
+            for k in ("q", "k", "v", "gamma", "lam") + (("wq", "wk") if w.fused else ())}
     out = torch.empty((w.B, w.H, w.T, w.dv), dtype=td, device=dev)
     iters = torch.empty((w.B, w.H, w.T), dtype=torch.int32, device=dev)
-    ws = torch.empty(binding.mesa_forward_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.chunk),
+    ws = torch.empty(binding.mesa_forward_pre_workspace_size(w.B, w.H, w.T, w.dk, w.dv, w.chunk,
+                                                             1 if w.dtype == "bf16" else 0),
                      dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     in_bytes = sum(d_in[k].numel() * d_in[k].element_size() for k in ("q", "k", "v", "gamma"))
     needs_flush = in_bytes < 2 * (129 << 20)
 
     def step(i):
-        binding.mesa_forward_chunked(d_in["q"], d_in["k"], d_in["v"], d_in["gamma"], d_in["lam"],
-                                     w.cg_iters, w.cg_tol, w.chunk, out=out, iters_used=iters, workspace=ws)
+        if w.fused:
+            binding.mesa_forward_chunked_pre(d_in["q"], d_in["k"], d_in["wq"], d_in["wk"], d_in["v"], d_in["gamma"],
+                                             d_in["lam"], w.cg_iters, w.cg_tol, w.chunk, out=out, iters_used=iters,
+                                             workspace=ws)
+        else:
+            binding.mesa_forward_chunked(d_in["q"], d_in["k"], d_in["v"], d_in["gamma"], d_in["lam"],
+                                         w.cg_iters, w.cg_tol, w.chunk, out=out, iters_used=iters, workspace=ws)
 
     res = timed_loop(args, torch, lib, step, (lambda: flush.random_(0, 255)) if needs_flush else None,
                      world, dist, dev)
@@ -539,9 +558,16 @@ def e2e_forward(args, w, dev, torch, binding, inp, td, ws):
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
+    taps = {k: torch.from_numpy(inp[k]).to(dev) for k in ("wq", "wk")} if w.fused else None
+
     def run(d, stream):
-        binding.mesa_forward_chunked(d["q"], d["k"], d["v"], d["gamma"], lam, w.cg_iters, w.cg_tol, w.chunk,
-                                     out=out, iters_used=iters, workspace=ws, stream=stream)
+        if taps is not None:
+            binding.mesa_forward_chunked_pre(d["q"], d["k"], taps["wq"], taps["wk"], d["v"], d["gamma"], lam,
+                                             w.cg_iters, w.cg_tol, w.chunk, out=out, iters_used=iters, workspace=ws,
+                                             stream=stream)
+        else:
+            binding.mesa_forward_chunked(d["q"], d["k"], d["v"], d["gamma"], lam, w.cg_iters, w.cg_tol, w.chunk,
+                                         out=out, iters_used=iters, workspace=ws, stream=stream)
         return {"out": out, "iters": iters}
 
     ms = pipelined_e2e(torch, dev, h, run, h_out, max(3, min(args.steps, 50)), max(3, args.warmup))
@@ -737,7 +763,7 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
     launches_per_step = sum(kind_n) / args.steps
     it = res["iters"]
     traffic = recorded_traffic(w.name, top_name)
-    if w.conv_taps:
+    if w.conv_taps and not w.fused:
         bytes_ = preprocess_bytes(w)
         achieved = bytes_ / (avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -777,7 +803,7 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
     kernels = {names[i] if i < len(names) else f"kind{i}": {"ms_per_step": kind_ms[i] / args.steps,
                                                              "launches": kind_n[i]}
                for i in range(len(kind_ms)) if kind_n[i] > 0}
-    extra = {} if w.conv_taps else {"mean_iters": float(it.mean()), "max_iters": int(it.max())}
+    extra = {} if (w.conv_taps and not w.fused) else {"mean_iters": float(it.mean()), "max_iters": int(it.max())}
     extra["sm_count"] = peaks["sm_count"]
     extra["arithmetic"] = arithmetic(w)
     extra.update(res.get("extra", {}))

@@ -213,6 +213,30 @@ int mesa_qk_preprocess_step(int N, int H, int d, int W, int dtype, const void *q
                             float *conv_state, void *q_out, void *k_out, cudaStream_t stream);
 
 /*
+ * The query/key preprocessing (mesa_qk_preprocess: "Arquitetura (MesaNet)",
+ * "Pre-processamento") followed by the chunked forward, in one call: out and iters_used are
+ * those of mesa_forward_chunked on q = qk_preprocess(q_raw, wq), k = qk_preprocess(k_raw, wk)
+ * (each token's preprocessed q and k rounded to dtype, as the preprocessing pass writes
+ * them), with zero initial state.  For bf16 with dk = dv = 128 the preprocessing runs inside
+ * the tensor-core kernels' prologues (each chunk's raw rows, plus the W-1 rows before it, are
+ * preprocessed where they are staged), so preprocessed q and k never go to memory; results are
+ * bit-identical to the two calls.  Other sizes and types run the preprocessing pass into the
+ * workspace, then the layer.
+ *   q_raw, k_raw [B, H, T, dk] dtype; wq, wk [H, dk, W] fp32, 1 <= W <= 8; v, gamma,
+ *   lambda_diag, cg_iters, cg_tol, chunk, out, iters_used as mesa_forward_chunked.
+ *   q_raw, k_raw, v and out 16-byte aligned (MESA_ERR_INVALID_ARG otherwise).
+ *   workspace: at least mesa_forward_pre_workspace_size() bytes (256-byte aligned), whose
+ *   first word is the status word read by mesa_forward_status.
+ */
+size_t mesa_forward_pre_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype);
+int mesa_forward_chunked_pre(int B, int H, int T, int dk, int dv, int dtype, const void *q_raw,
+                             const void *k_raw, const float *wq, const float *wk, int W,
+                             const void *v, const float *gamma, const float *lambda_diag,
+                             int cg_iters, float cg_tol, int chunk, void *out,
+                             int32_t *iters_used, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream);
+
+/*
  * mesa_forward_chunked without a caller-provided workspace (no counterpart on the MesaNet
  * pages).  For callers that cannot allocate device memory where they run the layer: a host
  * that forbids cudaMalloc and owns every byte of device memory, a plugin that only receives

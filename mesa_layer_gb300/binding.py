@@ -54,6 +54,11 @@ def load(build_if_missing: bool = True):
         [_fp] * 4 + [_vp, _sz, _vp]
     lib.mesa_forward_chunked_noalloc.restype = _i
     lib.mesa_forward_chunked_noalloc.argtypes = [_i] * 6 + [_vp] * 5 + [_i, _f, _i, _vp, _ip, _vp]
+    lib.mesa_forward_pre_workspace_size.restype = _sz
+    lib.mesa_forward_pre_workspace_size.argtypes = [_i] * 7
+    lib.mesa_forward_chunked_pre.restype = _i
+    lib.mesa_forward_chunked_pre.argtypes = [_i] * 6 + [_vp, _vp, _fp, _fp, _i, _vp, _fp, _fp, _i, _f, _i, _vp, _ip,
+                                                        _vp, _sz, _vp]
     lib.mesa_forward_status.restype = _i
     lib.mesa_forward_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint)]
     lib.mesa_decode_status.restype = _i
@@ -148,6 +153,44 @@ def mesa_forward_chunked(q, k, v, gamma, lambda_diag, cg_iters, cg_tol, chunk, o
                                   _ptr(out), _ptr(iters_used), _ptr(H0), _ptr(G0), _ptr(H_final),
                                   _ptr(G_final), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "mesa_forward_chunked")
+    return out, iters_used
+
+
+def mesa_forward_pre_workspace_size(B, H, T, dk, dv, chunk, dtype_code) -> int:
+    return int(load().mesa_forward_pre_workspace_size(B, H, T, dk, dv, chunk, dtype_code))
+
+
+def mesa_forward_chunked_pre(q_raw, k_raw, wq, wk, v, gamma, lambda_diag, cg_iters, cg_tol, chunk, out=None,
+                             iters_used=None, workspace=None, stream=None):
+    """The query/key preprocessing (taps wq, wk [H, dk, W] fp32) and the chunked forward in one
+    call (zero initial state).  q_raw, k_raw [B, H, T, dk], v [B, H, T, dv] (fp32 or bf16).
+    Returns (out, iters_used)."""
+    lib = load()
+    B, H, T, dk = q_raw.shape
+    dv = v.shape[-1]
+    W = wq.shape[-1]
+    code = _dtype_code(q_raw)
+    for name, t in (("q_raw", q_raw), ("k_raw", k_raw), ("v", v)):
+        _require(t, name, q_raw.dtype)
+    for name, t in (("wq", wq), ("wk", wk), ("gamma", gamma), ("lambda_diag", lambda_diag)):
+        _require(t, name, torch.float32)
+    if tuple(wk.shape) != tuple(wq.shape):
+        raise MesaError("wq and wk must have the same shape [H, dk, W]")
+    if out is None:
+        out = torch.empty((B, H, T, dv), dtype=q_raw.dtype, device=q_raw.device)
+    if iters_used is None:
+        iters_used = torch.empty((B, H, T), dtype=torch.int32, device=q_raw.device)
+    _require(out, "out", q_raw.dtype)
+    _require(iters_used, "iters_used", torch.int32)
+    need = mesa_forward_pre_workspace_size(B, H, T, dk, dv, chunk, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q_raw.device)
+    _require(workspace, "workspace")
+    st = lib.mesa_forward_chunked_pre(B, H, T, dk, dv, code, _ptr(q_raw), _ptr(k_raw), _ptr(wq), _ptr(wk), int(W),
+                                      _ptr(v), _ptr(gamma), _ptr(lambda_diag), int(cg_iters), float(cg_tol),
+                                      int(chunk), _ptr(out), _ptr(iters_used), _ptr(workspace), workspace.numel(),
+                                      _stream(stream))
+    _check(st, "mesa_forward_chunked_pre")
     return out, iters_used
 
 

@@ -252,7 +252,8 @@ int forward_impl(int B, int H, int T, int dk, int dv, int dtype, const void *q, 
                  const void *v, const float *gamma, const float *lambda_diag, int cg_iters,
                  float cg_tol, int chunk, void *out, int32_t *iters_used, const float *H0,
                  const float *G0, float *H_final, float *G_final, float *x_saved, void *workspace,
-                 size_t workspace_bytes, cudaStream_t stream) {
+                 size_t workspace_bytes, cudaStream_t stream, const float *pre_wq = nullptr,
+                 const float *pre_wk = nullptr, int pre_W = 0) {
   if (B < 0 || H < 0 || T < 0 || cg_iters < 0 || cg_iters > kMaxIters || isnan(cg_tol))
     return MESA_ERR_INVALID_ARG;
   if (dtype != MESA_F32 && dtype != MESA_BF16) return MESA_ERR_INVALID_ARG;
@@ -288,7 +289,8 @@ int forward_impl(int B, int H, int T, int dk, int dv, int dtype, const void *q, 
   unsigned *status = (unsigned *)w;
   mesa::FwdArgs a{B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol,
                   tc ? 128 : work_chunk(dk, chunk), out, iters_used, H0, G0, H_final, G_final,
-                  status, mesa::wait_limit()};
+                  status, mesa::wait_limit(), pre_wq, pre_wk, pre_W};
+  if (pre_W > 0 && !tc) return MESA_ERR_UNSUPPORTED;  // (the fused prologues are tensor-core only)
   mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2]),
                         (float *)(w + off[3]), (float *)(w + off[4]), nseg};
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
@@ -407,6 +409,48 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
   if (solve(Bv, Y, iters_bwd) != 0) return MESA_ERR_CUDA;
   if (mesa::launch_bwd_grads(ba, ws, stream) != 0) return MESA_ERR_CUDA;
   return MESA_OK;
+}
+
+size_t mesa_forward_pre_workspace_size(int B, int H, int T, int dk, int dv, int chunk, int dtype) {
+  const size_t fw = mesa_forward_workspace_size(B, H, T, dk, dv, chunk);
+  if (fw == 0 || (dtype != MESA_F32 && dtype != MESA_BF16)) return 0;
+  if (dtype == MESA_BF16 && dk == 128) return fw;  // fused: nothing more
+  const size_t esz = dtype == MESA_BF16 ? 2 : 4;
+  return fw + 2 * align256((size_t)B * H * T * dk * esz);
+}
+
+int mesa_forward_chunked_pre(int B, int H, int T, int dk, int dv, int dtype, const void *q_raw,
+                             const void *k_raw, const float *wq, const float *wk, int W,
+                             const void *v, const float *gamma, const float *lambda_diag,
+                             int cg_iters, float cg_tol, int chunk, void *out,
+                             int32_t *iters_used, void *workspace, size_t workspace_bytes,
+                             cudaStream_t stream) {
+  if (B < 0 || H < 0 || T < 0 || W < 1 || W > 8) return MESA_ERR_INVALID_ARG;
+  if (dtype != MESA_F32 && dtype != MESA_BF16) return MESA_ERR_INVALID_ARG;
+  if (!dim_ok(dk) || dv != dk || !chunk_ok(chunk)) return MESA_ERR_UNSUPPORTED;
+  if ((size_t)B * H > kMaxUnits) return MESA_ERR_UNSUPPORTED;
+  if ((size_t)B * H * T == 0)
+    return forward_impl(B, H, T, dk, dv, dtype, q_raw, k_raw, v, gamma, lambda_diag, cg_iters, cg_tol,
+                        chunk, out, iters_used, nullptr, nullptr, nullptr, nullptr, nullptr, workspace,
+                        workspace_bytes, stream);
+  if (!q_raw || !k_raw || !wq || !wk || !v || !gamma || !lambda_diag || !out) return MESA_ERR_INVALID_ARG;
+  if (!aligned(q_raw, 16) || !aligned(k_raw, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return MESA_ERR_INVALID_ARG;
+  if (workspace_bytes < mesa_forward_pre_workspace_size(B, H, T, dk, dv, chunk, dtype) || !workspace ||
+      !aligned(workspace, 256))
+    return MESA_ERR_WORKSPACE;
+  if (dtype == MESA_BF16 && dk == 128)  // fused into the tensor-core kernels' prologues
+    return forward_impl(B, H, T, dk, dv, dtype, q_raw, k_raw, v, gamma, lambda_diag, cg_iters, cg_tol,
+                        chunk, out, iters_used, nullptr, nullptr, nullptr, nullptr, nullptr, workspace,
+                        workspace_bytes, stream, wq, wk, W);
+  // other sizes and types: the preprocessing pass into the end of the workspace, then the layer
+  const size_t fw = mesa_forward_workspace_size(B, H, T, dk, dv, chunk);
+  const size_t esz = dtype == MESA_BF16 ? 2 : 4;
+  char *qp = (char *)workspace + fw, *kp = qp + align256((size_t)B * H * T * dk * esz);
+  mesa::PreArgs pa{B * H, H, T, dk, W, dtype, q_raw, k_raw, wq, wk, nullptr, qp, kp};
+  if (mesa::launch_qk_preprocess(pa, false, stream) != 0) return MESA_ERR_CUDA;
+  return forward_impl(B, H, T, dk, dv, dtype, qp, kp, v, gamma, lambda_diag, cg_iters, cg_tol, chunk,
+                      out, iters_used, nullptr, nullptr, nullptr, nullptr, nullptr, workspace, fw, stream);
 }
 
 int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state, float *G_state,

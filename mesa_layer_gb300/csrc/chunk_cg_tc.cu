@@ -108,7 +108,8 @@ struct Misc {
   uint64_t mbar_y;   // Y = Z K
   uint64_t mbar_u;   // U = P S
   uint64_t mbar_drain;  // after a give-up: completion of every multiply issued (2 issuers)
-  uint64_t mbar_ld;     // bulk copies of the chunk's operands (phase 0) and of S^G (phase 1)
+  uint64_t mbar_ld;     // bulk copies of the chunk's rows (phase 0) and of S^G (phase 1)
+  uint64_t mbar_ld2;    // bulk copies of the chunk's state S^H_{c-1} and its carry
   uint32_t tmem_base;
 };
 static_assert(sizeof(Misc) <= MISC_BYTES, "misc block too large");
@@ -175,7 +176,7 @@ __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, con
 // the readout's rows are g (a.q = dout), its keys v (a.k = v), its values k (a.v = k), and
 // its state product g S^G reads the staged S^G as an MN-major operand (the transpose of the
 // forward's x S^G^T); b is written in fp32 to sv.x_out.
-template <int NTERMS, bool SOLVE, bool SAVE, bool RHS>
+template <int NTERMS, bool SOLVE, bool SAVE, bool RHS, bool PRE = false>
 __global__ void __launch_bounds__(512, 1)
     mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, int lookahead, unsigned *status,
                       SolveArgs sv) {
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t aBarW1 = tc::smem_u32(&m->mbar_w1), aBarW2 = tc::smem_u32(&m->mbar_w2);
   const uint32_t aBarY = tc::smem_u32(&m->mbar_y), aBarU = tc::smem_u32(&m->mbar_u);
   const uint32_t aBarDrain = tc::smem_u32(&m->mbar_drain), aBarLd = tc::smem_u32(&m->mbar_ld);
+  const uint32_t aBarLd2 = tc::smem_u32(&m->mbar_ld2);
   const uint32_t sbase = tc::smem_u32(sm);
   const unsigned wlim = a.wait_limit;
 
@@ -265,6 +267,11 @@ __global__ void __launch_bounds__(512, 1)
   const bool load_q = !(SOLVE && sv.rhs);
   constexpr uint32_t MAT32 = sizeof(float) * DH * DH;  // one fp32 state (64 KB)
   const uint32_t rows_bytes = (uint32_t)Tv * DH * 2;     // Tv bf16 rows
+  // PRE: q and k are raw inputs of the query/key preprocessing, fused here: the h rows before
+  // the chunk (the convolution's window) come in too, into the K operand region, which is
+  // written only after the preprocessed rows have been read
+  const int pre_h = PRE ? min(a.pre_W - 1, t0) : 0;
+  constexpr uint32_t PRE_QHALO = 2048, PRE_KTAPS = 4096, PRE_QTAPS = 8192;  // offsets in the K region
   if (tid == 0) {
     tc::mbar_init(aBarW1, 1);
     tc::mbar_init(aBarW2, 1);
@@ -272,15 +279,24 @@ __global__ void __launch_bounds__(512, 1)
     tc::mbar_init(aBarU, 1);
     tc::mbar_init(aBarDrain, 2);  // threads 0 (W, Y) and 128 (U) issue the multiplies
     tc::mbar_init(aBarLd, 1);
+    tc::mbar_init(aBarLd2, 1);
     // this chunk's operands by bulk copies, raw: the keys and the queries (bf16 rows) into
     // the x region, S^H_{c-1} into the Z region, its segment carry into the S region (all
     // three regions are written only after these are read)
     tc::fence_smem_to_async();
-    tc::mbar_arrive_expect_tx(aBarLd, rows_bytes * (load_q ? 2 : 1) + (SHu ? MAT32 : 0) + (CHu ? MAT32 : 0));
+    const uint32_t halo_bytes = (uint32_t)pre_h * DH * 2;
+    // the rows (and halos) on one barrier, the state on another, so that the rows can be
+    // worked on while the state is still coming in
+    tc::mbar_arrive_expect_tx(aBarLd, (rows_bytes + halo_bytes) * (load_q ? 2 : 1));
+    tc::mbar_arrive_expect_tx(aBarLd2, (SHu ? MAT32 : 0) + (CHu ? MAT32 : 0));
     tc::bulk_g2s(sbase + OFF_X, k + tokbase * DH, rows_bytes, aBarLd);
     if (load_q) tc::bulk_g2s(sbase + OFF_X + MAT_BYTES, q + tokbase * DH, rows_bytes, aBarLd);
-    if (SHu) tc::bulk_g2s(sbase + OFF_ZHI, SHu, MAT32, aBarLd);
-    if (CHu) tc::bulk_g2s(sbase + OFF_SHI, CHu, MAT32, aBarLd);
+    if (PRE && pre_h > 0) {
+      tc::bulk_g2s(sbase + OFF_K, k + (tokbase - pre_h) * DH, halo_bytes, aBarLd);
+      tc::bulk_g2s(sbase + OFF_K + PRE_QHALO, q + (tokbase - pre_h) * DH, halo_bytes, aBarLd);
+    }
+    if (SHu) tc::bulk_g2s(sbase + OFF_ZHI, SHu, MAT32, aBarLd2);
+    if (CHu) tc::bulk_g2s(sbase + OFF_SHI, CHu, MAT32, aBarLd2);
   }
   bool small = true;  // |l2| <= 100: D_ij = 2^{l2_i} 2^{-l2_j} without overflow
   if (tid < TILE) {
@@ -290,6 +306,11 @@ __global__ void __launch_bounds__(512, 1)
     small = fabsf(l2) <= 100.0f;
   }
   if (tid >= 256 && tid < 256 + DH) m->lam[tid - 256] = a.lambda[(size_t)(u % a.H) * DH + tid - 256];
+  if constexpr (PRE) {  // the head's convolution taps, transposed
+    const size_t hw = (size_t)(u % a.H) * DH * a.pre_W;
+    tc::pre_taps(a.pre_wk + hw, a.pre_W, reinterpret_cast<float *>(sm + OFF_K + PRE_KTAPS));
+    tc::pre_taps(a.pre_wq + hw, a.pre_W, reinterpret_cast<float *>(sm + OFF_K + PRE_QTAPS));
+  }
   // the readout's state is only needed after the CG and is fetched into L2 meanwhile
   tc::prefetch_l2(SG, sizeof(float) * DH * DH);
   tc::prefetch_l2(CG, sizeof(float) * DH * DH);
@@ -312,16 +333,32 @@ __global__ void __launch_bounds__(512, 1)
     }
   }
   __syncthreads();  // barrier initialisations (and the per-chunk constants) visible
-  // Bounded wait for the copies; on a give-up the block waits (default limit) until they have
+  // Bounded waits for the copies; on a give-up the block waits (default limit) until they have
   // landed, so that nothing writes this CTA's shared memory after it ends, and skips the chunk.
   bool failed = false;
-  if (__syncthreads_or(!tc::mbar_wait(aBarLd, 0, wlim))) {
-    failed = true;
-    if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
-    if (__syncthreads_or(!tc::mbar_wait(aBarLd, 0, tc::kWaitLimit)) && tid == 0)
-      atomicOr(status, tc::kErrDrainTimeout);
-  }
+  auto wait_copies = [&](uint32_t bar, uint32_t phase) {
+    if (__syncthreads_or(!tc::mbar_wait(bar, phase, wlim))) {
+      failed = true;
+      if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
+      if (__syncthreads_or(!tc::mbar_wait(bar, phase, tc::kWaitLimit)) && tid == 0)
+        atomicOr(status, tc::kErrDrainTimeout);
+    }
+  };
+  wait_copies(aBarLd, 0);  // the rows
   uint32_t phLd = 1;
+  if constexpr (PRE) {  // the staged raw rows become the layer's k and q (bf16), in place
+    uint2 res[8];
+    tc::PreTile tk{sm + OFF_X, sm + OFF_K, pre_h, reinterpret_cast<const float *>(sm + OFF_K + PRE_KTAPS)};
+    tc::PreTile tq{sm + OFF_X + MAT_BYTES, sm + OFF_K + PRE_QHALO, pre_h,
+                   reinterpret_cast<const float *>(sm + OFF_K + PRE_QTAPS)};
+    tc::pre_compute<4>(tk, a.pre_W, Tv, res);
+    __syncthreads();
+    tc::pre_store(tk, Tv, res);
+    tc::pre_compute<4>(tq, a.pre_W, Tv, res);
+    __syncthreads();
+    tc::pre_store(tq, Tv, res);
+    __syncthreads();
+  }
   // this thread's query columns, the key tile and the state, from the staged copies
   uint4 qraw[NV];
   {
@@ -332,6 +369,7 @@ __global__ void __launch_bounds__(512, 1)
   }
   tc::Rows8 kr;
   tc::load_rows_smem(sm + OFF_X, Tv, kr);
+  wait_copies(aBarLd2, 0);  // the state
   float sS, sK;
   {
     tc::Mat32 S;
@@ -748,13 +786,7 @@ __global__ void __launch_bounds__(512, 1)
     float sG, sV;
     tc::Rows8 vr;
     tc::load_rows(v + tokbase * DH, Tv, vr);
-    if (gbytes && __syncthreads_or(!tc::mbar_wait(aBarLd, phLd, wlim))) {
-      // give up on the readout, once the copies have landed (default limit)
-      failed = true;
-      if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
-      if (__syncthreads_or(!tc::mbar_wait(aBarLd, phLd, tc::kWaitLimit)) && tid == 0)
-        atomicOr(status, tc::kErrDrainTimeout);
-    }
+    if (gbytes) wait_copies(aBarLd, phLd);  // (a give-up skips the readout)
     phLd ^= 1;
     {
       tc::Mat32 G;
@@ -843,9 +875,13 @@ int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *statu
   const int NC = (a.T + TILE - 1) / TILE;
   // a backward-pass solve: no output, the iterate goes to sv.x_out
   if (!a.out && !sv.x_out) return -1;
-  auto kfn = !a.out    ? mesa_cg_tc_kernel<MESA_TC_TERMS, true, false, false>
-             : sv.x_out ? mesa_cg_tc_kernel<MESA_TC_TERMS, false, true, false>
-                        : mesa_cg_tc_kernel<MESA_TC_TERMS, false, false, false>;
+  // (a.pre_W > 0: q and k are raw, the query/key preprocessing runs in the prologue; plain
+  // forward only)
+  if (a.pre_W > 0 && (!a.out || sv.x_out)) return -1;
+  auto kfn = !a.out       ? mesa_cg_tc_kernel<MESA_TC_TERMS, true, false, false>
+             : sv.x_out    ? mesa_cg_tc_kernel<MESA_TC_TERMS, false, true, false>
+             : a.pre_W > 0 ? mesa_cg_tc_kernel<MESA_TC_TERMS, false, false, false, true>
+                           : mesa_cg_tc_kernel<MESA_TC_TERMS, false, false, false>;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TC) !=
       cudaSuccess)
     return -1;

@@ -20,6 +20,50 @@ __device__ __forceinline__ float log_gate(float g) {
 // Device status-word bit for a non-finite output (the same value as tc::kErrNonFinite).
 __host__ __device__ constexpr unsigned tc_err_nonfinite() { return 2u; }
 
+// ---- query/key preprocessing of one token (shared by the preprocessing pass and the fused
+// forward, so that both round alike) ------------------------------------------------------
+// Sum over the TPT lanes of a group (TPT a power of two, groups aligned in the warp).
+template <int TPT>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = TPT / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// MesaNet technical summary, "Arquitetura (MesaNet)", "Pre-processamento": a causal
+// depthwise convolution over W taps, then the token's Euclidean normalisation.  This lane's
+// four channels: y = w[0] x[0] + sum_{s=1..W-1} w[s] x[s] (x[s] the input s tokens back,
+// w[s] the taps of these channels), then y / ||y|| with the norm summed over the TPT lanes
+// that hold the token (0 for y = 0).  In three steps, so that callers can interleave tokens:
+// qk_conv, qk_sumsq (this lane's part of ||y||^2; group_sum<TPT> completes it), qk_scale.
+// W <= WMAX taps (the arrays hold WMAX entries; those from W on are not read).
+template <int WMAX>
+__device__ __forceinline__ float4 qk_conv(const float4 (&w)[WMAX], const float4 (&x)[WMAX], int W) {
+  float4 y = make_float4(w[0].x * x[0].x, w[0].y * x[0].y, w[0].z * x[0].z, w[0].w * x[0].w);
+#pragma unroll
+  for (int s = 1; s < WMAX; s++) {
+    if (s < W) {
+      y.x = fmaf(w[s].x, x[s].x, y.x);
+      y.y = fmaf(w[s].y, x[s].y, y.y);
+      y.z = fmaf(w[s].z, x[s].z, y.z);
+      y.w = fmaf(w[s].w, x[s].w, y.w);
+    }
+  }
+  return y;
+}
+__device__ __forceinline__ float qk_sumsq(float4 y) {
+  return fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, y.w * y.w)));
+}
+__device__ __forceinline__ float4 qk_scale(float4 y, float ss) {
+  const float f = ss > 0.0f ? rsqrtf(ss) : 0.0f;
+  return make_float4(y.x * f, y.y * f, y.z * f, y.w * f);
+}
+template <int TPT, int WMAX>
+__device__ __forceinline__ float4 qk_conv_norm(const float4 (&w)[WMAX], const float4 (&x)[WMAX], int W) {
+  const float4 y = qk_conv(w, x, W);
+  return qk_scale(y, group_sum<TPT>(qk_sumsq(y)));
+}
+
 template <typename T>
 __device__ __forceinline__ float ld(const T *p, size_t i);
 template <>

@@ -23,9 +23,12 @@ namespace mesa {
 
 namespace {
 constexpr uint32_t DT_MAT = 128 * 128 * 2;
-// K operand | A hi | A lo | misc (1 KB) | raw key rows | raw value rows, + alignment slack
+// K operand | A hi | A lo | misc (1 KB) | raw key rows | raw value rows | (fused query/key
+// preprocessing) the raw key rows before the chunk (2 KB) and the head's taps (4 KB), +
+// alignment slack
 constexpr uint32_t DT_STAGE = 3 * DT_MAT + 1024;
-constexpr uint32_t DT_SMEM = DT_STAGE + 2 * DT_MAT + 1024;
+constexpr uint32_t DT_HALO = DT_STAGE + 2 * DT_MAT, DT_TAPS = DT_HALO + 2048;
+constexpr uint32_t DT_SMEM = DT_TAPS + 4096 + 1024;
 struct StateMisc {
   float w[128];
   float red[48];
@@ -36,6 +39,9 @@ struct StateMisc {
 };
 }  // namespace
 
+// PRE: k holds raw inputs of the query/key preprocessing, applied to each chunk's key rows
+// when they arrive (the pass's arithmetic, so the states equal those of preprocessed keys).
+template <bool PRE>
 __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC,
                                                              unsigned *status) {
   using tc::DH;
@@ -45,7 +51,8 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
   uint8_t *Ks = sm, *Ahi = sm + DT_MAT, *Alo = sm + 2 * DT_MAT;
   StateMisc *m = reinterpret_cast<StateMisc *>(sm + 3 * DT_MAT);
   static_assert(sizeof(StateMisc) <= 1024, "misc block too large");
-  const uint8_t *Kraw = sm + DT_STAGE, *Vraw = sm + DT_STAGE + DT_MAT;
+  uint8_t *Kraw = sm + DT_STAGE;
+  const uint8_t *Vraw = sm + DT_STAGE + DT_MAT;
   const uint32_t aKraw = tc::smem_u32(Kraw), aVraw = tc::smem_u32(Vraw), aLd = tc::smem_u32(&m->mbar_ld);
   const uint32_t aK = tc::smem_u32(Ks), aAhi = tc::smem_u32(Ahi), aAlo = tc::smem_u32(Alo);
   const uint32_t aBar = tc::smem_u32(&m->mbar);
@@ -63,10 +70,14 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
   auto fetch = [&](int c) {
     const size_t tb = (size_t)u * T + (size_t)c * TILE;
     const uint32_t bytes = (uint32_t)min(TILE, T - c * TILE) * DH * 2;
-    tc::mbar_arrive_expect_tx(aLd, 2 * bytes);
+    const int h = PRE ? min(a.pre_W - 1, c * TILE) : 0;  // the convolution's window
+    tc::mbar_arrive_expect_tx(aLd, 2 * bytes + (uint32_t)h * DH * 2);
     tc::bulk_g2s(aKraw, (const __nv_bfloat16 *)a.k + tb * DH, bytes, aLd);
     tc::bulk_g2s(aVraw, (const __nv_bfloat16 *)a.v + tb * DH, bytes, aLd);
+    if (h > 0) tc::bulk_g2s(tc::smem_u32(sm + DT_HALO), (const __nv_bfloat16 *)a.k + (tb - h) * DH, h * DH * 2, aLd);
   };
+  if constexpr (PRE) tc::pre_taps(a.pre_wk + (size_t)(u % a.H) * DH * a.pre_W, a.pre_W,
+                                  reinterpret_cast<float *>(sm + DT_TAPS));
   if (tid == 0) {
     tc::mbar_init(aBar, 1);
     tc::mbar_init(tc::smem_u32(&m->mbar_drain), 1);
@@ -149,6 +160,14 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     }
     phLd ^= 1;
     pending = false;
+    if constexpr (PRE) {  // the staged raw key rows become the layer's keys (bf16), in place
+      uint2 res[8];
+      tc::PreTile tk{Kraw, sm + DT_HALO, min(a.pre_W - 1, t0), reinterpret_cast<const float *>(sm + DT_TAPS)};
+      tc::pre_compute<4>(tk, a.pre_W, Tv, res);
+      __syncthreads();
+      tc::pre_store(tk, Tv, res);
+      __syncthreads();
+    }
     tc::load_rows_smem(Kraw, Tv, kr);
     tc::load_rows_smem(Vraw, Tv, vr);
     const float lend = ws.ell[tokbase + Tv - 1];
@@ -241,11 +260,11 @@ __global__ void __launch_bounds__(256) mesa_carry_tc_kernel(FwdWorkspace ws, int
 int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st) {
   const int U = a.B * a.H;
   const int NC = (a.T + 127) / 128;
-  if (cudaFuncSetAttribute(mesa_states_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)DT_SMEM) != cudaSuccess)
+  auto kfn = a.pre_W > 0 ? mesa_states_tc_kernel<true> : mesa_states_tc_kernel<false>;
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DT_SMEM) != cudaSuccess)
     return -1;
   timing_mark_begin(K_DELTA_TC, st);
-  mesa_states_tc_kernel<<<dim3(ws.nseg, U), 512, DT_SMEM, st>>>(a, ws, NC, status);
+  kfn<<<dim3(ws.nseg, U), 512, DT_SMEM, st>>>(a, ws, NC, status);
   timing_mark_end(K_DELTA_TC, st);
   if (ws.nseg > 1 || a.H_final) {
     timing_mark_begin(K_SCAN, st);

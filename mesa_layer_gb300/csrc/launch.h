@@ -22,6 +22,10 @@ struct FwdArgs {
   float *H_final, *G_final;
   unsigned *status = nullptr;  // device status word (error bits of tc_common.cuh) or nullptr
   unsigned wait_limit = 0;     // polls of a bounded mbarrier wait (tensor-core kernels)
+  // pre_W > 0 (tensor-core path only): q and k are raw inputs of the query/key preprocessing
+  // (pre_W taps [H, dk, pre_W] each), which the kernels apply in their prologues
+  const float *pre_wq = nullptr, *pre_wk = nullptr;
+  int pre_W = 0;
 };
 
 // Polls of the tensor-core kernels' bounded waits for the next launches: the default, or the

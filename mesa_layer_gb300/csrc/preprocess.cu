@@ -49,17 +49,6 @@ __device__ __forceinline__ void st4<__nv_bfloat16>(__nv_bfloat16 *p, size_t i, f
   *reinterpret_cast<uint2 *>(p + i) = raw;
 }
 
-// Sum over the TPT lanes of a group (TPT a power of two, groups aligned in the warp).
-template <int TPT>
-__device__ __forceinline__ float group_sum(float v) {
-#pragma unroll
-  for (int o = TPT / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-__device__ __forceinline__ float4 scale4(float4 v, float f) {
-  return make_float4(v.x * f, v.y * f, v.z * f, v.w * f);
-}
 }  // namespace
 
 // grid (ceil(T / tokens per CTA), U, 2 = q / k), block 256.
@@ -110,17 +99,12 @@ __global__ void __launch_bounds__(256) mesa_qk_preprocess_kernel(PreArgs a) {
     for (int j = 0; j < NB; j++) {
       const int t = t_begin + k0 + j;
       const float4 xt = xb[j];
-      float4 y = make_float4(wv[0].x * xt.x, wv[0].y * xt.y, wv[0].z * xt.z, wv[0].w * xt.w);
+      float4 xs[W];
+      xs[0] = xt;
 #pragma unroll
-      for (int s = 1; s < W; s++) {
-        y.x = fmaf(wv[s].x, win[s - 1].x, y.x);
-        y.y = fmaf(wv[s].y, win[s - 1].y, y.y);
-        y.z = fmaf(wv[s].z, win[s - 1].z, y.z);
-        y.w = fmaf(wv[s].w, win[s - 1].w, y.w);
-      }
-      const float ss = group_sum<TPT>(fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, y.w * y.w))));
-      const float f = ss > 0.0f ? rsqrtf(ss) : 0.0f;
-      if (t < T) st4(out, ubase + (size_t)t * D + c0, scale4(y, f));
+      for (int s = 1; s < W; s++) xs[s] = win[s - 1];
+      const float4 o = qk_conv_norm<TPT, W>(wv, xs, W);
+      if (t < T) st4(out, ubase + (size_t)t * D + c0, o);
 #pragma unroll
       for (int s = W - 2; s >= 1; s--) win[s] = win[s - 1];
       if (W > 1) win[0] = xt;
@@ -143,22 +127,22 @@ __global__ void __launch_bounds__(128) mesa_qk_preprocess_step_kernel(PreArgs a)
   const float *wh = wt + (size_t)(uu % a.H) * D * W;
   float *hist = a.conv_state + ((size_t)uu * 2 + which) * (W - 1) * D;  // [W-1][D]
   const float4 xt = valid ? ld4(x, (size_t)uu * D + c0) : make_float4(0, 0, 0, 0);
-  float4 y = make_float4(wh[(c0 + 0) * W] * xt.x, wh[(c0 + 1) * W] * xt.y, wh[(c0 + 2) * W] * xt.z,
-                         wh[(c0 + 3) * W] * xt.w);
+  float4 wv[W], xs[W];
   float4 win[W > 1 ? W - 1 : 1];
+  xs[0] = xt;
+#pragma unroll
+  for (int s = 0; s < W; s++)
+    wv[s] = make_float4(wh[(c0 + 0) * W + s], wh[(c0 + 1) * W + s], wh[(c0 + 2) * W + s],
+                        wh[(c0 + 3) * W + s]);
 #pragma unroll
   for (int s = 1; s < W; s++) {
     win[s - 1] = valid ? *reinterpret_cast<const float4 *>(hist + (size_t)(s - 1) * D + c0)
                        : make_float4(0, 0, 0, 0);
-    y.x = fmaf(wh[(c0 + 0) * W + s], win[s - 1].x, y.x);
-    y.y = fmaf(wh[(c0 + 1) * W + s], win[s - 1].y, y.y);
-    y.z = fmaf(wh[(c0 + 2) * W + s], win[s - 1].z, y.z);
-    y.w = fmaf(wh[(c0 + 3) * W + s], win[s - 1].w, y.w);
+    xs[s] = win[s - 1];
   }
-  const float ss = group_sum<TPT>(fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, y.w * y.w))));
-  const float f = ss > 0.0f ? rsqrtf(ss) : 0.0f;
+  const float4 o = qk_conv_norm<TPT, W>(wv, xs, W);
   if (!valid) return;
-  st4(out, (size_t)u * D + c0, scale4(y, f));
+  st4(out, (size_t)u * D + c0, o);
   // the window moves on by this step's input
 #pragma unroll
   for (int s = W - 2; s >= 1; s--) *reinterpret_cast<float4 *>(hist + (size_t)s * D + c0) = win[s - 1];

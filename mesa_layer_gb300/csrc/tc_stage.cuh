@@ -6,6 +6,7 @@
 
 #include <cuda_bf16.h>
 
+#include "common.cuh"
 #include "tc_common.cuh"
 
 namespace mesa {
@@ -178,6 +179,101 @@ __device__ __forceinline__ void load_rows_smem(const uint8_t *stage, int Tv, Row
     const int e = 8 * t + 4096 * n;
     x.v[n] = (e / DH < Tv) ? *reinterpret_cast<const uint4 *>(stage + 2 * e) : make_uint4(0, 0, 0, 0);
   }
+}
+
+// ---- query/key preprocessing of a staged tile (fused into the forward's prologues) --------
+// A 128-token tile staged raw (bf16, row-major, 256 bytes per row; rows [0, Tv) hold tokens
+// t0 .. t0+Tv-1), the h = min(W-1, t0) raw rows before it (halo row h-1 = token t0-1) and the
+// head's taps transposed to [W][128] fp32.  Row j becomes bf16(qk_conv_norm(...)) with lane l
+// owning channels 4l .. 4l+3 -- the preprocessing pass's layout for d = 128, so both round
+// alike.  Warp w takes rows 8w .. 8w+7 and slides the window over them in registers, as the
+// pass does (each raw row is read once, plus W-1 rows before the warp's first); pre_compute
+// keeps the results in registers, pre_store writes them back in place once every warp has
+// read the raw rows it needs (the caller puts a block barrier between the two).  16 warps.
+constexpr int kPreWMax = 8;
+struct PreTile {
+  uint8_t *rows;
+  const uint8_t *halo;
+  int h;
+  const float *taps;
+};
+
+__device__ __forceinline__ float4 bf16x4_at(const uint8_t *row, int lane) {
+  const uint2 raw = *reinterpret_cast<const uint2 *>(row + 8 * lane);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// W taps (compile time); NB rows are finished side by side (their norm reductions interleave).
+template <int NB, int W>
+__device__ __forceinline__ void pre_compute_w(const PreTile &pt, int Tv, uint2 (&res)[8]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j0 = 8 * warp;
+  float4 w[W], win[W];  // win[s]: the raw row s tokens back of the row being computed
+#pragma unroll
+  for (int s = 0; s < W; s++) w[s] = *reinterpret_cast<const float4 *>(pt.taps + s * DH + 4 * lane);
+  // before the first shift win[s] holds row j0-1-s: rows of the tile (another warp's, read
+  // raw), of the halo, or zeros before the sequence
+#pragma unroll
+  for (int s = 0; s + 1 < W; s++) {
+    const int r = j0 - 1 - s;
+    win[s] = r >= 0 ? bf16x4_at(pt.rows + r * DH * 2, lane)
+             : r >= -pt.h ? bf16x4_at(pt.halo + (pt.h + r) * DH * 2, lane)
+                          : make_float4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int n0 = 0; n0 < 8; n0 += NB) {
+    float4 y[NB];
+    float ss[NB];
+#pragma unroll
+    for (int b = 0; b < NB; b++) {
+      const int j = j0 + n0 + b;
+#pragma unroll
+      for (int s = W - 1; s > 0; s--) win[s] = win[s - 1];
+      win[0] = j < Tv ? bf16x4_at(pt.rows + j * DH * 2, lane) : make_float4(0, 0, 0, 0);
+      y[b] = qk_conv(w, win, W);
+      ss[b] = qk_sumsq(y[b]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int b = 0; b < NB; b++) ss[b] += __shfl_xor_sync(0xffffffffu, ss[b], o);
+#pragma unroll
+    for (int b = 0; b < NB; b++) {
+      const float4 v = qk_scale(y[b], ss[b]);
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      res[n0 + b] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+    }
+  }
+}
+
+template <int NB>
+__device__ __forceinline__ void pre_compute(const PreTile &pt, int W, int Tv, uint2 (&res)[8]) {
+  switch (W) {  // (uniform over the block)
+    case 1: pre_compute_w<NB, 1>(pt, Tv, res); break;
+    case 2: pre_compute_w<NB, 2>(pt, Tv, res); break;
+    case 3: pre_compute_w<NB, 3>(pt, Tv, res); break;
+    case 4: pre_compute_w<NB, 4>(pt, Tv, res); break;
+    case 5: pre_compute_w<NB, 5>(pt, Tv, res); break;
+    case 6: pre_compute_w<NB, 6>(pt, Tv, res); break;
+    case 7: pre_compute_w<NB, 7>(pt, Tv, res); break;
+    default: pre_compute_w<NB, 8>(pt, Tv, res); break;
+  }
+}
+
+__device__ __forceinline__ void pre_store(const PreTile &pt, int Tv, const uint2 (&res)[8]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int n = 0; n < 8; n++) {
+    const int j = 8 * warp + n;
+    if (j < Tv) *reinterpret_cast<uint2 *>(pt.rows + j * DH * 2 + 8 * lane) = res[n];
+  }
+}
+
+// The head's taps w [DH][W] (tap s of channel c at c W + s) transposed into dst [W][DH].
+__device__ __forceinline__ void pre_taps(const float *w, int W, float *dst) {
+  for (int e = threadIdx.x; e < DH * W; e += blockDim.x) dst[(e % W) * DH + e / W] = w[e];
 }
 
 // max over this thread's values of |w_row * x|  (w == nullptr: |x|)

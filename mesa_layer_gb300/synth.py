@@ -48,6 +48,7 @@ class Workload:
     conv_taps: int = 0         # > 0: query/key preprocessing workload with this window
     warm: bool = False         # decode: each step's CG starts from the previous solution
     backward: bool = False     # the backward pass (gradients given dL/dout)
+    fused: bool = False        # with conv_taps: the preprocessing fused into the forward
 
     @property
     def tokens(self) -> int:
@@ -80,6 +81,10 @@ WORKLOADS = {
         # the backward pass on the shape and distributions of fwd_bf16_d128
         Workload("bwd_bf16_d128", 7, "bf16", 8, 16, 4096, 128, 128, 64, 15, 0.0,
                  "sigmoid", 4.0, 1.0, 0.05, 0.5, backward=True),
+        # the forward of fwd_bf16_d128 on raw queries and keys, with the query/key
+        # preprocessing (window 4) fused into it
+        Workload("fwd_pre_bf16_d128", 8, "bf16", 8, 16, 4096, 128, 128, 64, 15, 0.0,
+                 "sigmoid", 4.0, 1.0, 0.05, 0.5, conv_taps=4, fused=True),
     ]
 }
 WORKLOAD_ORDER = [w.name for w in sorted(WORKLOADS.values(), key=lambda w: w.wid)]

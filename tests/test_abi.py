@@ -198,3 +198,26 @@ def test_backward_workspace_and_validation(lib):
     assert call(xs=ctypes.c_void_p(264)) == 1   # saved iterates must be 16-byte aligned
     fs = lib.mesa_forward_chunked_save          # the saved iterates are required
     assert fs(1, 1, 64, 64, 64, 0, p, p, p, p, p, 4, 0.0, 64, p, None, None, p, 1 << 40, None) == 1
+
+
+def test_fused_preprocessing_forward_validation(lib):
+    """mesa_forward_chunked_pre: workspace sizes (fused: the forward's; otherwise two more
+    activation buffers) and argument checks before anything is launched."""
+    fw = lib.mesa_forward_workspace_size(2, 4, 300, 128, 128, 64)
+    assert lib.mesa_forward_pre_workspace_size(2, 4, 300, 128, 128, 64, 1) == fw
+    fw64 = lib.mesa_forward_workspace_size(2, 4, 300, 64, 64, 64)
+    assert lib.mesa_forward_pre_workspace_size(2, 4, 300, 64, 64, 64, 0) >= fw64 + 2 * 2 * 4 * 300 * 64 * 4
+    assert lib.mesa_forward_pre_workspace_size(2, 4, 300, 64, 64, 64, 7) == 0
+    f = lib.mesa_forward_chunked_pre
+    f.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    f.argtypes = [ctypes.c_int] * 6 + [vp, vp, vp, vp, ctypes.c_int, vp, vp, vp, ctypes.c_int, ctypes.c_float,
+                                       ctypes.c_int, vp, vp, vp, ctypes.c_size_t, vp]
+    p = vp(4096)  # never dereferenced: every call below fails validation first
+    args = lambda W=4, dt=1, ws=p, nbytes=1 << 30, q=p: (1, 2, 300, 128, 128, dt, q, p, p, p, W, p, p, p, 8, 0.0,
+                                                         64, p, None, ws, nbytes, None)
+    assert f(*args(W=0)) == 1 and f(*args(W=9)) == 1
+    assert f(*args(dt=3)) == 1
+    assert f(*args(q=None)) == 1
+    assert f(*args(q=vp(4098))) == 1          # misaligned activations
+    assert f(*args(ws=None)) == 3 and f(*args(nbytes=16)) == 3
