@@ -186,12 +186,13 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     tc::store_rows(kr, m->w, sAH, Ahi, Alo);
     const float nsigH = sAH * sK, nsigG = sAG * sK;
     rescale(0, first ? ac * nsigH : ac * nsigH / sigH, first, H0);
-    rescale(128, first ? ac * nsigG : ac * nsigG / sigG, first, G0);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) issue(0, !first || H0 != nullptr);
+    // S^G's accumulator (columns the key sums do not touch) is rescaled while they run
+    rescale(128, first ? ac * nsigG : ac * nsigG / sigG, first, G0);
     ok = wait();
     if (!ok) break;
     tc::store_rows(vr, m->w, sAG, Ahi, Alo);
@@ -200,15 +201,9 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) issue(128, !first || G0 != nullptr);
-    ok = wait();
-    if (!ok) break;
-    sigH = nsigH;
-    sigG = nsigG;
-    Lsum += lend;
-    // segment-local state after chunk c
-#pragma unroll
-    for (int half = 0; half < 2; half++) {
-      const float f = 1.0f / (half ? sigG : sigH);
+    // segment-local state after chunk c (half 0: S^H, half 1: S^G), unscaled
+    auto write_state = [&](int half, float sig) {
+      const float f = 1.0f / sig;
       float *dst = (half ? ws.SG : ws.SH) + (((size_t)u * NC + c) * DH + row) * DH + 32 * cg;
       float x[32];
       tc::tmem_ld32(tl + half * 128, x);
@@ -217,7 +212,14 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
       for (int g = 0; g < 8; g++)
         reinterpret_cast<float4 *>(dst)[g] =
             make_float4(x[4 * g] * f, x[4 * g + 1] * f, x[4 * g + 2] * f, x[4 * g + 3] * f);
-    }
+    };
+    write_state(0, nsigH);  // S^H goes out while the tensor core adds the value sums into S^G
+    ok = wait();
+    if (!ok) break;
+    write_state(1, nsigG);
+    sigH = nsigH;
+    sigG = nsigG;
+    Lsum += lend;
     if (tid == 0) ws.Lc[(size_t)u * NC + c] = Lsum;
   }
   // a wait gave up (the same outcome in every thread): let the multiplies and the copy still
