@@ -218,8 +218,13 @@ __global__ void __launch_bounds__(512, 1)
   // which no warp above the diagonal owns, conflict-free across the lanes of a warp.  Only
   // the quadrant's own threads touch its rows, and never while Z is live.
   const uint32_t scr_row = (uint32_t)((i >> 3) * 1024 + (i & 7) * 128 + 4 * (lane >> 3));
-  auto scr = [&](int n, int g) -> float * {
-    return reinterpret_cast<float *>((n ? Zlo : Zhi) + scr_row + ((g ^ (i & 7)) << 4));
+  // Slot 1 (float (lane >> 3) ^ 2 of the same chunks) serves the CG step's two reductions
+  // after the Y product: Z is dead from then until the next step's Z build, and the step's
+  // first block barrier separates these reductions' reads from the next writes, so they keep
+  // one barrier each (the sum of sigma in slot 1, the residual's in slot 0).
+  auto scr = [&](int n, int g, int slot = 0) -> float * {
+    return reinterpret_cast<float *>((n ? Zlo : Zhi) + scr_row + ((g ^ (i & 7)) << 4)) + 2 * slot *
+           (((lane >> 3) & 2) ? -1 : 1);
   };
   auto rowred = [&](float val, bool mx) -> float {
     *scr(0, grp) = val;
@@ -243,6 +248,28 @@ __global__ void __launch_bounds__(512, 1)
     sum = s_;
     mx = m_;
     quad_bar<NG>(qd);
+  };
+  // the CG step's reductions after the Y product (one barrier each, see above)
+  auto step_sum = [&](float val) -> float {
+    *scr(0, grp, 1) = val;
+    quad_bar<NG>(qd);
+    float r = *scr(0, 0, 1);
+#pragma unroll
+    for (int g = 1; g < NG; g++) r += *scr(0, g, 1);
+    return r;
+  };
+  auto step_sum_max = [&](float &sum, float &mx) {
+    *scr(0, grp) = sum;
+    *scr(1, grp) = mx;
+    quad_bar<NG>(qd);
+    float s_ = *scr(0, 0), m_ = *scr(1, 0);
+#pragma unroll
+    for (int g = 1; g < NG; g++) {
+      s_ += *scr(0, g);
+      m_ = fmaxf(m_, *scr(1, g));
+    }
+    sum = s_;
+    mx = m_;
   };
 
   // ---- set-up: tensor memory, barriers, per-chunk constants --------------------------
@@ -671,7 +698,7 @@ __global__ void __launch_bounds__(512, 1)
       tc::tmem_st16(tl + COL_U + 16 * h, uu);
     }
     tc::tmem_st_wait();
-    const float sigma = rowred(sg, false);
+    const float sigma = step_sum(sg);
     const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
     // r -= alpha AP   (alpha = 0 leaves a finished row unchanged; the tensor-memory
     // accesses stay unconditional: they are warp-collective)
@@ -691,7 +718,7 @@ __global__ void __launch_bounds__(512, 1)
       tc::tmem_st16(tl + COL_R + 16 * h, rr);
     }
     tc::tmem_st_wait();
-    rowred2(rn, rmax);
+    step_sum_max(rn, rmax);
     const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
     // for an active row p = r + beta p, staged with the scale
     // mNew >= max|r| + beta max|p| >= max|p_new|; the old p stays in registers for the
