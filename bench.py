@@ -119,15 +119,20 @@ def cg_flops(w, iters: np.ndarray) -> float:
 
 
 def tc_executed_flops(w, iters: np.ndarray, readout: bool = True) -> float:
-    """MMA flops the tensor-core CG kernel issues: per 128-token chunk and iteration 7
-    products of 128x128x128 (3 for the split state product, 2 + 2 for the key products);
+    """MMA flops the tensor-core CG kernels issue per 128-token chunk and iteration: d = 128
+    (bf16 inputs) 7 products of 128x128x128 (3 for the split state product, 2 + 2 for the key
+    products); d = 64 (fp32 inputs, keys split too) 3 x (128x128x64 + 128x64x64 + 128x64x128);
     iterations run until the slowest token of the chunk stops, plus the readout."""
     B, H, T = iters.shape
     nc = (T + 127) // 128
     pad = np.zeros((B, H, nc * 128), dtype=np.int64)
     pad[:, :, :T] = iters
     per_chunk = pad.reshape(B, H, nc, 128).max(axis=-1) + (1 if readout else 0)
-    return float(per_chunk.sum()) * 7 * 2.0 * 128 ** 3
+    if w.dk == 64:
+        per = 3 * 2.0 * (128 * 128 * 64 + 128 * 64 * 64 + 128 * 64 * 128)
+    else:
+        per = 7 * 2.0 * 128 ** 3
+    return float(per_chunk.sum()) * per
 
 
 def state_flops(w) -> float:
@@ -347,6 +352,9 @@ def arithmetic(w) -> str:
         return (("raw q, k preprocessed in fp32 and rounded to bf16 in the prologues; " if w.fused else "") +
                 "bf16 inputs; tensor-core products of fp16 hi+lo split operands with fp32 "
                 "accumulation; fp32 CG vectors and scalars")
+    if w.dtype == "f32" and w.dk == 64:
+        return ("fp32 inputs; tensor-core products of fp16 hi+lo split operands (keys and values split "
+                "too) with fp32 accumulation; fp32 chunk states (CUDA cores), CG vectors and scalars")
     return f"{w.dtype} inputs, fp32 CUDA-core arithmetic"
 
 
@@ -787,7 +795,7 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
         else:
             flops = state_flops(w)
         achieved = flops / (avg_ms / 1e3) / 1e12
-        if "_tc_" in top_name:
+        if "_tc_" in top_name or "_tc64_" in top_name:
             # fp16 tcgen05 MMAs run at the bf16 dense rate; the measured cuBLAS bf16 peak
             peak = peaks["bf16_tflops"]
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -88,6 +88,16 @@ bool use_tc(int dtype, int dk, int dv, const void *q, const void *k, const void 
   return true;
 }
 
+// The fp32 tensor-core path covers fp32 inputs with dk = dv = 64 (16-byte aligned operands,
+// for the bulk copies).
+bool use_tc64(int dtype, int dk, int dv, const void *q, const void *k, const void *v, const void *out,
+              const float *H0, const float *G0) {
+  if (dtype != MESA_F32 || dk != 64 || dv != 64) return false;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return false;
+  if ((H0 && !aligned(H0, 16)) || (G0 && !aligned(G0, 16))) return false;
+  return true;
+}
+
 // ---- optional per-kernel timing (benchmarks only) --------------------------------------
 struct TimingState {
   bool on = false;
@@ -192,6 +202,7 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_BWD_STATES: return "mesa_state_sweep_kernel<adjoints>";
     case mesa::K_BWD_FSTATES: return "mesa_state_sweep_kernel<states>";
     case mesa::K_BWD_GRAD: return "mesa_bwd_grad_kernel+mesa_bwd_lambda_kernel";
+    case mesa::K_CG_TC64: return "mesa_cg_tc64_kernel";
   }
   return nullptr;
 }
@@ -277,6 +288,7 @@ int forward_impl(int B, int H, int T, int dk, int dv, int dtype, const void *q, 
   }
   if (!q || !k || !v || !gamma || !out) return MESA_ERR_INVALID_ARG;
   const bool tc = use_tc(dtype, dk, dv, q, k, v, out, H0, G0);
+  const bool tc64 = pre_W == 0 && use_tc64(dtype, dk, dv, q, k, v, out, H0, G0);
   // segments of the tensor-core state build: the current device's choice, or fewer when the
   // workspace was sized on a device with fewer SMs (the carries are its last part)
   int nseg = tc ? mesa::tc_segments((int)U, (T + 127) / 128) : 1;
@@ -288,7 +300,7 @@ int forward_impl(int B, int H, int T, int dk, int dv, int dtype, const void *q, 
   char *w = (char *)workspace;
   unsigned *status = (unsigned *)w;
   mesa::FwdArgs a{B, H, T, dk, dv, dtype, q, k, v, gamma, lambda_diag, cg_iters, cg_tol,
-                  tc ? 128 : work_chunk(dk, chunk), out, iters_used, H0, G0, H_final, G_final,
+                  (tc || tc64) ? 128 : work_chunk(dk, chunk), out, iters_used, H0, G0, H_final, G_final,
                   status, mesa::wait_limit(), pre_wq, pre_wk, pre_W};
   if (pre_W > 0 && !tc) return MESA_ERR_UNSUPPORTED;  // (the fused prologues are tensor-core only)
   mesa::FwdWorkspace ws{(float *)(w + off[0]), (float *)(w + off[1]), (float *)(w + off[2]),
@@ -297,7 +309,8 @@ int forward_impl(int B, int H, int T, int dk, int dv, int dtype, const void *q, 
   if (mesa::launch_chunk_states(a, ws, tc ? status : nullptr, stream) != 0) return MESA_ERR_CUDA;
   mesa::SolveArgs sv;
   sv.x_out = x_saved;
-  const int rc = tc ? mesa::launch_chunk_cg_tc(a, ws, status, stream, sv)
+  const int rc = tc     ? mesa::launch_chunk_cg_tc(a, ws, status, stream, sv)
+                 : tc64 ? mesa::launch_chunk_cg_tc64(a, ws, status, stream, sv)
                  : (dk <= 64 ? mesa::launch_chunk_cg_rows(a, ws, stream, sv)
                              : mesa::launch_chunk_cg_simt(a, ws, stream, sv));
   return rc == 0 ? MESA_OK : MESA_ERR_CUDA;

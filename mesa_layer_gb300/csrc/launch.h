@@ -86,7 +86,7 @@ struct PreArgs {
 enum KernelKind {
   K_ELL = 0, K_DELTA = 1, K_SCAN = 2, K_CG_SIMT = 3, K_DECODE = 4, K_CG_TC = 5, K_DELTA_TC = 6, K_CG_ROWS = 7,
   K_PREPROC = 8, K_BWD_RHS = 9, K_BWD_STATES = 10, K_BWD_GRAD = 11, K_BWD_FSTATES = 12,
-  K_NUM_KINDS = 13
+  K_CG_TC64 = 13, K_NUM_KINDS = 14
 };
 
 // Record a timing event before / after a launch of `kind` on `st` (no-op unless enabled).
@@ -106,6 +106,11 @@ int launch_chunk_cg_rows(const FwdArgs &a, const FwdWorkspace &ws, cudaStream_t 
 // must have been built with chunk = 128).  Bounded-wait failures set bits in *status.
 int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st,
                        const SolveArgs &sv = SolveArgs());
+// Tensor-core path for fp32 inputs with dk = dv = 64: 128-token chunks (the states and
+// log-decays of ws built by the CUDA-core state kernels with chunk = 128), split fp16 operands
+// for every product.  The forward only (sv.x_out: the iterates are kept as well).
+int launch_chunk_cg_tc64(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st,
+                         const SolveArgs &sv = SolveArgs());
 // The right-hand sides b_t = G_t^T dout_t of the backward pass's second solve on the tensor
 // cores (bf16, d = 128, the 128-token states of ws), written to b [U, T, dk] fp32.
 int launch_rhs_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st,

@@ -47,11 +47,15 @@ def _workspace(w):
     return torch.empty(n, dtype=torch.uint8, device="cuda")
 
 
-def test_wait_give_up_reports_timeout_and_the_next_call_is_clean():
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_wait_give_up_reports_timeout_and_the_next_call_is_clean(dtype, d):
     from mesa_layer_gb300 import binding
-    w = synth.workload("fwd_bf16_d128", B=1, H=2, T=300, cg_iters=12, cg_tol=0.0)
+    # (fp32: the fp32 workload's Lambda range; with the bf16 workload's, down to 0.05, a plain
+    # fp32 restatement of these 12 un-converged iterations already lands at 1.03e-4)
+    w = synth.workload("fwd_bf16_d128" if dtype == "bf16" else "fwd_fp32_d64", dtype=dtype, dk=d, dv=d, B=1, H=2,
+                       T=300, cg_iters=12, cg_tol=0.0)
     inp = synth.forward_inputs(w, seed=21)
-    t = torch_inputs(inp, "bf16")
+    t = torch_inputs(inp, dtype)
     ws = _workspace(w)
     binding.mesa_debug_set_wait_limit(0)
     try:
@@ -62,14 +66,15 @@ def test_wait_give_up_reports_timeout_and_the_next_call_is_clean():
     assert not flags & 4, "the drain of the in-flight multiplies expired"
     o, it, code, flags = _run(t, w.cg_iters, 0.0, w.chunk, ws)
     assert code == binding.MESA_OK and flags == 0
-    r = forward_check(inp, o, it, "bf16", w.cg_iters, 0.0, "after a give-up")
+    r = forward_check(inp, o, it, dtype, w.cg_iters, 0.0, "after a give-up")
     print(f"after a give-up: {r}")
 
 
 PATHS = {
     # name: (dtype, d, chunk)
     "tensor_core": ("bf16", 128, 64),
-    "rows_fp32_d64": ("f32", 64, 64),
+    "tensor_core_fp32_d64": ("f32", 64, 64),
+    "rows_fp32_d32": ("f32", 32, 64),
     "simt_fp32_d128": ("f32", 128, 64),
 }
 T_BAD = 150  # token with the planted value (inside the 128-token block [128, 256))
