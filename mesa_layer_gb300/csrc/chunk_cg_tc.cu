@@ -31,6 +31,15 @@
 #include "tc_common.cuh"
 #include "tc_stage.cuh"
 
+// fp16 terms of the A operand of the two key products of a CG step (W = P K^T, Y = Z K) when
+// the state product keeps two: 2 (default) or 1.  Measured: 1 term makes the forward 7 %
+// faster on the bf16 d = 128 workloads, but a CPU emulation of these numerics puts single
+// tokens of the fixed-count workload (15 un-converged iterations) at 1.8e-2 relative error
+// (9.7e-3 with 2 terms), too close to the 2e-2 bound.
+#ifndef MESA_TC_KTERMS
+#define MESA_TC_KTERMS 2
+#endif
+
 namespace mesa {
 
 static_assert(tc::kErrNonFinite == tc_err_nonfinite(), "one status bit for non-finite outputs");
@@ -183,6 +192,7 @@ __global__ void __launch_bounds__(512, 1)
   constexpr int NG = 4;           // column groups (threads per token row)
   constexpr int CW = DH / NG;     // columns per thread
   constexpr int NV = CW / 8;      // 8-column vectors per thread
+  constexpr int KT = NTERMS == 2 ? MESA_TC_KTERMS : 1;  // terms of the key products' A operand
   extern __shared__ uint8_t smem_raw[];
   uint8_t *sm = smem_raw + ((1024 - (tc::smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t *Shi = sm + OFF_SHI, *Slo = sm + OFF_SLO, *Ks = sm + OFF_K;
@@ -495,7 +505,7 @@ __global__ void __launch_bounds__(512, 1)
       for (int s = 0; s < 8; s++) {
         const uint64_t kb = kdesc(OFF_K, s) + (uint64_t)(half * (64 * 128 / 16));
         tc::mma_f16_ts(tbase + COL_W + 64 * half, tbase + COL_PH + 8 * s, kb, id_kk64, s > 0);
-        if (NTERMS == 2) tc::mma_f16_ts(tbase + COL_W + 64 * half, tbase + COL_PL + 8 * s, kb, id_kk64, true);
+        if (KT == 2) tc::mma_f16_ts(tbase + COL_W + 64 * half, tbase + COL_PL + 8 * s, kb, id_kk64, true);
       }
       tc::mma_commit(half ? aBarW2 : aBarW1);
     }
@@ -525,7 +535,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
     for (int s = 0; s < 8; s++) {
       tc::mma_f16(tbase + COL_W, kdesc(OFF_ZHI, s), kmn_desc(s), id_kmn, s > 0);
-      if (NTERMS == 2) tc::mma_f16(tbase + COL_W, kdesc(OFF_ZLO, s), kmn_desc(s), id_kmn, true);
+      if (KT == 2) tc::mma_f16(tbase + COL_W, kdesc(OFF_ZLO, s), kmn_desc(s), id_kmn, true);
     }
     tc::mma_commit(aBarY);
   };
@@ -618,7 +628,7 @@ __global__ void __launch_bounds__(512, 1)
         float x8[8];
 #pragma unroll
         for (int kk = 0; kk < 8; kk++) x8[kk] = w[g * 8 + kk];
-        st8<NTERMS>(Zhi, Zlo, i, c0 + 8 * g, x8, inv);
+        st8<KT>(Zhi, Zlo, i, c0 + 8 * g, x8, inv);
       }
     }
     return zs;

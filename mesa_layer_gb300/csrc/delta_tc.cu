@@ -10,10 +10,15 @@
 // (A = (w x)^T read MN-major from the token-major tile, x = k or v, split hi + lo fp16;
 // B = K read MN-major, fp16, exact after a power-of-two scale), and writes the state.
 // The raw key and value rows of the next chunk arrive by bulk copies (tensor memory
-// accelerator) into staging buffers while the current chunk's MMAs and write-out run.
+// accelerator) into staging buffers while the current chunk's MMAs and write-out run, and
+// the states leave the same way: each is moved from tensor memory into a 128-byte-swizzled
+// staging buffer and written by four tiled tensor stores (32 columns x 128 rows each), so
+// that the CTA goes on with the next chunk while HBM absorbs the 128 KB per chunk.
 // Segment 0 starts from the initial state, later segments from zero; mesa_carry_tc_kernel then
 // chains the segments (carry[s] = global state before segment s) and writes the final state,
 // and the CG kernel adds exp(Lc) carry when it loads a state.
+#include <cuda.h>  // CUtensorMap and its encoder's signature (the encoder is fetched at run time)
+
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -23,12 +28,17 @@ namespace mesa {
 
 namespace {
 constexpr uint32_t DT_MAT = 128 * 128 * 2;
-// K operand | A hi | A lo | misc (1 KB) | raw key rows | raw value rows | (fused query/key
-// preprocessing) the raw key rows before the chunk (2 KB) and the head's taps (4 KB), +
-// alignment slack
+// K operand | A hi | A lo | misc (1 KB) | raw key rows | raw value rows | then either the
+// state staging buffer (64 KB: four 16 KB slabs of 32 fp32 columns, 128-byte swizzled) or,
+// with the query/key preprocessing fused, the raw key rows before the chunk (2 KB) and the
+// head's taps (4 KB) (the states then go out by plain stores) | alignment slack
 constexpr uint32_t DT_STAGE = 3 * DT_MAT + 1024;
-constexpr uint32_t DT_HALO = DT_STAGE + 2 * DT_MAT, DT_TAPS = DT_HALO + 2048;
-constexpr uint32_t DT_SMEM = DT_TAPS + 4096 + 1024;
+constexpr uint32_t DT_OUT = DT_STAGE + 2 * DT_MAT, DT_SLAB = 128 * 32 * 4;
+constexpr uint32_t DT_HALO = DT_OUT, DT_TAPS = DT_HALO + 2048;
+constexpr uint32_t DT_SMEM = DT_OUT + 4 * DT_SLAB + 1024;
+constexpr uint32_t DT_SMEM_PRE = DT_TAPS + 4096 + 1024;
+static_assert(DT_OUT % 1024 == 0, "the swizzled staging buffer needs 1024-byte alignment");
+static_assert(DT_SMEM <= 232448 && DT_SMEM_PRE <= 232448, "shared memory per block");
 struct StateMisc {
   float w[128];
   float red[48];
@@ -41,9 +51,12 @@ struct StateMisc {
 
 // PRE: k holds raw inputs of the query/key preprocessing, applied to each chunk's key rows
 // when they arrive (the pass's arithmetic, so the states equal those of preprocessed keys).
+// mapH, mapG: tensor maps of ws.SH, ws.SG as [U NC 128 rows, 128 fp32 columns] with boxes of
+// 32 columns x 128 rows (128-byte swizzle); unused with PRE.
 template <bool PRE>
-__global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC,
-                                                             unsigned *status) {
+__global__ void __launch_bounds__(512, 1)
+    mesa_states_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, unsigned *status,
+                          const __grid_constant__ CUtensorMap mapH, const __grid_constant__ CUtensorMap mapG) {
   using tc::DH;
   using tc::TILE;
   extern __shared__ uint8_t smem_raw[];
@@ -141,12 +154,44 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
   // the keys and values of the next chunk come in by bulk copies while the current chunk's
   // MMAs and write-out run
   tc::Rows8 kr, vr;
+  // the log-decays a chunk needs (its last one; thread tid < 128: token tid's) are loaded one
+  // chunk ahead
+  float ell_end, ell_tid;
+  auto load_ell = [&](int c) {
+    const size_t tb = (size_t)u * T + (size_t)c * TILE;
+    const int tv = min(TILE, T - c * TILE);
+    ell_end = ws.ell[tb + tv - 1];
+    ell_tid = tid < tv ? ws.ell[tb + tid] : 0.0f;
+  };
+  load_ell(c_begin);
+  // state write-out (without PRE): tensor memory -> staging buffer -> four tensor stores.
+  // The staging buffer is reused once thread 0 has seen the previous stores read it
+  // (bulk_wait_read before the block barrier that precedes the next staging).
+  uint8_t *Out = sm + DT_OUT;
+  auto stage_state = [&](int half, float sig) {
+    const float f = 1.0f / sig;
+    float x[32];
+    tc::tmem_ld32(tl + half * 128, x);
+    tc::tmem_ld_wait();
+    uint8_t *dst = Out + cg * DT_SLAB + row * 128;
+#pragma unroll
+    for (int g = 0; g < 8; g++)
+      *reinterpret_cast<float4 *>(dst + ((g ^ (row & 7)) << 4)) =
+          make_float4(x[4 * g] * f, x[4 * g + 1] * f, x[4 * g + 2] * f, x[4 * g + 3] * f);
+    tc::fence_smem_to_async();
+  };
+  auto store_state = [&](int half, int c) {  // thread 0, after the barrier behind stage_state
+    const void *map = half ? (const void *)&mapG : (const void *)&mapH;
+    const int y = (u * NC + c) * TILE;
+#pragma unroll
+    for (int sl = 0; sl < 4; sl++) tc::tensor_s2g_2d(map, tc::smem_u32(Out + sl * DT_SLAB), 32 * sl, y);
+    tc::bulk_commit();
+  };
   for (int c = c_begin; c < c_end && ok; c++) {
     const bool first = c == c_begin;
     const float *H0 = (seg == 0) ? a.H0 : nullptr;
     const float *G0 = (seg == 0) ? a.G0 : nullptr;
     const int t0 = c * TILE, Tv = min(TILE, T - t0);
-    const size_t tokbase = (size_t)u * T + t0;
     // this chunk's rows (bounded wait; on a give-up the copies are waited for with the default
     // limit before the block stops)
     const bool got = tc::mbar_wait(aLd, phLd, a.wait_limit);
@@ -170,9 +215,10 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     }
     tc::load_rows_smem(Kraw, Tv, kr);
     tc::load_rows_smem(Vraw, Tv, vr);
-    const float lend = ws.ell[tokbase + Tv - 1];
+    const float lend = ell_end;
     const float ac = expf(lend);
-    if (tid < TILE) m->w[tid] = tid < Tv ? expf(lend - ws.ell[tokbase + tid]) : 0.0f;
+    if (tid < TILE) m->w[tid] = tid < Tv ? expf(lend - ell_tid) : 0.0f;
+    if (c + 1 < c_end) load_ell(c + 1);
     tc::fence_smem_to_async();
     __syncthreads();  // (also: every thread holds its rows, the staging buffers are free)
     if (tid == 0 && c + 1 < c_end) fetch(c + 1);
@@ -193,6 +239,7 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     if (tid == 0) issue(0, !first || H0 != nullptr);
     // S^G's accumulator (columns the key sums do not touch) is rescaled while they run
     rescale(128, first ? ac * nsigG : ac * nsigG / sigG, first, G0);
+    if (!PRE && tid == 0) tc::bulk_wait_read();  // the previous S^G has left the staging buffer
     ok = wait();
     if (!ok) break;
     tc::store_rows(vr, m->w, sAG, Ahi, Alo);
@@ -213,10 +260,26 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
         reinterpret_cast<float4 *>(dst)[g] =
             make_float4(x[4 * g] * f, x[4 * g + 1] * f, x[4 * g + 2] * f, x[4 * g + 3] * f);
     };
-    write_state(0, nsigH);  // S^H goes out while the tensor core adds the value sums into S^G
+    // S^H goes out while the tensor core adds the value sums into S^G
+    if constexpr (PRE) {
+      write_state(0, nsigH);
+    } else {
+      stage_state(0, nsigH);
+      __syncthreads();
+      if (tid == 0) {
+        store_state(0, c);
+        tc::bulk_wait_read();  // S^H has left the staging buffer before S^G comes in
+      }
+    }
     ok = wait();
     if (!ok) break;
-    write_state(1, nsigG);
+    if constexpr (PRE) {
+      write_state(1, nsigG);
+    } else {
+      stage_state(1, nsigG);
+      __syncthreads();
+      if (tid == 0) store_state(1, c);
+    }
     sigH = nsigH;
     sigG = nsigG;
     Lsum += lend;
@@ -229,6 +292,8 @@ __global__ void __launch_bounds__(512, 1) mesa_states_tc_kernel(FwdArgs a, FwdWo
     if (pending && __syncthreads_or(!tc::mbar_wait(aLd, phLd, tc::kWaitLimit)) && tid == 0)
       atomicOr(status, tc::kErrDrainTimeout);
   }
+  // the state stores still in flight complete before the block (and its shared memory) ends
+  if (!PRE && tid == 0) tc::bulk_wait_all();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_free(tbase, 256);
@@ -259,14 +324,49 @@ __global__ void __launch_bounds__(256) mesa_carry_tc_kernel(FwdWorkspace ws, int
   if (F) F[(size_t)u * D * D + e] = S[(size_t)(NC - 1) * D * D] + expf(ws.Lc[(size_t)u * NC + NC - 1]) * carry;
 }
 
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// The driver's tensor-map encoder (fetched once; nullptr if the driver does not provide it).
+EncodeTiledFn encode_tiled() {
+  static const EncodeTiledFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeTiledFn) nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+// [rows, 128] fp32 row-major at `base`, boxes of 32 columns x 128 rows, 128-byte swizzle.
+bool state_map(CUtensorMap *map, float *base, size_t rows) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {128 * sizeof(float)};
+  const cuuint32_t box[2] = {32, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st) {
   const int U = a.B * a.H;
   const int NC = (a.T + 127) / 128;
-  auto kfn = a.pre_W > 0 ? mesa_states_tc_kernel<true> : mesa_states_tc_kernel<false>;
-  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DT_SMEM) != cudaSuccess)
+  const bool pre = a.pre_W > 0;
+  auto kfn = pre ? mesa_states_tc_kernel<true> : mesa_states_tc_kernel<false>;
+  const uint32_t smem = pre ? DT_SMEM_PRE : DT_SMEM;
+  CUtensorMap mapH{}, mapG{};
+  if (!pre && (!state_map(&mapH, ws.SH, (size_t)U * NC * 128) || !state_map(&mapG, ws.SG, (size_t)U * NC * 128)))
+    return -1;
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return -1;
   timing_mark_begin(K_DELTA_TC, st);
-  kfn<<<dim3(ws.nseg, U), 512, DT_SMEM, st>>>(a, ws, NC, status);
+  kfn<<<dim3(ws.nseg, U), 512, smem, st>>>(a, ws, NC, status, mapH, mapG);
   timing_mark_end(K_DELTA_TC, st);
   if (ws.nseg > 1 || a.H_final) {
     timing_mark_begin(K_SCAN, st);

@@ -249,6 +249,25 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_saddr, const void *src, ui
       : "memory");
 }
 
+// ---- tensor stores (TMA, tiled) ---------------------------------------------------------
+// Store the box of the tensor map `map` (a kernel parameter declared __grid_constant__) whose
+// first element is at coordinates (x, y) from this CTA's shared memory at `src_saddr` (laid
+// out as the map's swizzle mode wants it) to global memory; tracked as a bulk group of the
+// issuing thread.  x times the element size must be a multiple of 16 bytes, and x, y >= 0.
+__device__ __forceinline__ void tensor_s2g_2d(const void *map, uint32_t src_saddr, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n" ::"l"(map),
+               "r"(src_saddr), "r"(x), "r"(y)
+               : "memory");
+}
+// Close the issuing thread's current bulk group.
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Wait until every bulk group of this thread has finished reading its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+// Wait until every bulk group of this thread has completed (its global writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 // After a bounded wait gave up, no matrix multiply of the CTA may still be in flight when its
 // tensor memory is released.  Every thread that issued multiplies (issuer == true) commits the
 // completion of all of them to `drain_bar` (initialised with the number of issuing threads);
