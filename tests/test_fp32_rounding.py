@@ -22,9 +22,11 @@ from helpers import oracle_forward, product_err, token_err
 from mesa_layer_gb300 import synth
 
 
-def restated_forward(inp, counts, dtype=np.float32):
+def restated_forward(inp, counts, dtype=np.float32, tol=0.0, counts_out=None):
     """o [B, H, T, dv] of the per-token recurrence and CG with every operation in `dtype`,
-    token t running exactly counts[b, h, t] iterations (the batch axis is vectorised)."""
+    token t running exactly counts[b, h, t] iterations (the batch axis is vectorised); with
+    tol > 0 each token also stops before an iteration once ||r|| <= tol ||q|| (the stopping
+    rule, evaluated in `dtype`), and counts_out [B, H, T] receives the iterations run."""
     q, k, v, g, lam = (inp[x] for x in ("q", "k", "v", "gamma", "lam"))
     B, H, T, d = q.shape
     dv = v.shape[-1]
@@ -43,9 +45,15 @@ def restated_forward(inp, counts, dtype=np.float32):
             r = q[:, h, t].astype(dtype)
             p = r.copy()
             rho = np.einsum("bi,bi->b", r, r)
+            nq = np.sqrt(rho)
             n = counts[:, h, t]
+            ran = np.zeros(B, dtype=np.int64)
             for it in range(int(n.max(initial=0))):
                 act = it < n
+                if tol > 0:
+                    act = act & ~(np.sqrt(rho) <= dtype(tol) * nq)
+                    n = np.where(act, n, np.minimum(n, it))
+                ran += act
                 w = np.einsum("bij,bj->bi", Hs, p) + L * p
                 sig = np.einsum("bi,bi->b", p, w)
                 ok = act & (sig > zero) & (rho > zero)
@@ -57,6 +65,8 @@ def restated_forward(inp, counts, dtype=np.float32):
                 p = np.where(act[:, None], r + be[:, None] * p, p)
                 rho = np.where(act, rn, rho)
             out[:, h, t] = np.einsum("bij,bj->bi", Gs, x)
+            if counts_out is not None:
+                counts_out[:, h, t] = ran
     return out
 
 
@@ -122,3 +132,40 @@ def test_fp32_chunk_invariance_case():
     print(f"fp32 restatement, d = 64 x 16 iterations: strict max {strict.max():.3e}, "
           f"product-scale max {prod.max():.3e}")
     assert prod.max() < 2.5e-5
+
+
+def _near_zero_gates_d128(tol):
+    """The tensor-core edge case of the GPU tests: bf16 inputs, d = 128, gates near zero."""
+    w = synth.workload("fwd_bf16_d128", B=1, H=2, T=400, cg_iters=12 if tol == 0.0 else 30, cg_tol=tol)
+    inp = synth.forward_inputs(w, seed=14)
+    inp["gamma"][:] = np.float32(1e-3)
+    inp["gamma"][0, 0, 170] = 0.0
+    return w, inp
+
+
+def test_fp32_near_zero_gates_d128_fixed():
+    """Gates near zero at d = 128 (bf16 inputs, 12 un-converged iterations): every state is
+    nearly the current token's rank-one term, the readout v_t (k_t . x) cancels in k_t . x, and
+    fp32 arithmetic misses even the bf16 bound 2e-2 per token while its error on the readout's
+    magnitude stays small.  The GPU test of this regime therefore asserts the latter."""
+    w, inp = _near_zero_gates_d128(0.0)
+    strict, prod = _errors(inp, w.cg_iters, 0.0)
+    print(f"fp32 restatement, d = 128 gates near zero: strict max {strict.max():.3e}, "
+          f"tokens over 2e-2 {int((strict > 2e-2).sum())} of {strict.size}, product-scale max {prod.max():.3e}")
+    assert strict.max() > 2e-2
+    assert prod.max() < 1e-3
+
+
+def test_fp32_near_zero_gates_d128_dynamic_counts():
+    """The same regime in dynamic mode (tol 1e-3): the fp32 restatement's own stopping
+    decisions agree with the fp64 oracle's on fewer than half of the tokens (24 %, at most two
+    iterations apart), so the GPU test of this regime checks every token against the oracle
+    replaying the GPU's counts and does not hold the agreement rate to the usual floor."""
+    w, inp = _near_zero_gates_d128(1e-3)
+    ro, rit, rs = oracle_forward(inp, w.cg_iters, w.cg_tol)
+    cnt = np.zeros_like(rit)
+    restated_forward(inp, np.full_like(rit, w.cg_iters), np.float32, tol=w.cg_tol, counts_out=cnt)
+    agree = float((cnt == rit).mean())
+    print(f"fp32 restatement, d = 128 gates near zero, dynamic: counts agree {agree:.4f}, "
+          f"max difference {int(np.abs(cnt - rit).max())}")
+    assert agree < 0.5 and np.abs(cnt - rit).max() <= 3
