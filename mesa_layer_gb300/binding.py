@@ -384,17 +384,19 @@ def mesa_forward_status_code(workspace, stream=None):
 
 def mesa_decode_status(stream=None):
     """(status code, flags) of the decode steps on the current device since the last query
-    (the word is cleared): MESA_OK or MESA_ERR_NONFINITE (bit 1 of flags)."""
+    (the word is cleared): MESA_OK, MESA_ERR_TIMEOUT (bits 0 / 2 of flags) or
+    MESA_ERR_NONFINITE (bit 1)."""
     lib = load()
     flags = ctypes.c_uint(0)
     rc = lib.mesa_decode_status(_stream(stream), ctypes.byref(flags))
-    if rc not in (MESA_OK, MESA_ERR_NONFINITE):
+    if rc not in (MESA_OK, MESA_ERR_TIMEOUT, MESA_ERR_NONFINITE):
         _check(rc, "mesa_decode_status")
     return int(rc), int(flags.value)
 
 
 def mesa_debug_set_wait_limit(polls: int):
-    """Test hook: polls after which the tensor-core kernels' waits give up (< 0: default)."""
+    """Test hook: polls after which the tensor-core kernels' (and the d = 128 decode step's)
+    bounded waits give up (< 0: default)."""
     _check(load().mesa_debug_set_wait_limit(int(polls)), "mesa_debug_set_wait_limit")
 
 

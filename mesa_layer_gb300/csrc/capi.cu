@@ -479,7 +479,7 @@ int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state, fl
     return MESA_ERR_INVALID_ARG;
   if (!aligned(H_state, 16) || !aligned(G_state, 16)) return MESA_ERR_INVALID_ARG;
   mesa::DecArgs a{N, H, dk, dv, dtype, H_state, G_state, nullptr, q, k, v, gamma, lambda_diag,
-                  cg_iters, cg_tol, out, iters_used};
+                  cg_iters, cg_tol, out, iters_used, mesa::wait_limit()};
   return mesa::launch_decode(a, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
 }
 
@@ -498,7 +498,7 @@ int mesa_decode_step_warm(int N, int H, int dk, int dv, int dtype, float *H_stat
   if (!aligned(H_state, 16) || !aligned(G_state, 16) || !aligned(X_state, 16))
     return MESA_ERR_INVALID_ARG;
   mesa::DecArgs a{N, H, dk, dv, dtype, H_state, G_state, X_state, q, k, v, gamma, lambda_diag,
-                  cg_iters, cg_tol, out, iters_used};
+                  cg_iters, cg_tol, out, iters_used, mesa::wait_limit()};
   return mesa::launch_decode(a, stream) == 0 ? MESA_OK : MESA_ERR_CUDA;
 }
 

@@ -12,6 +12,7 @@
 // products of each CG step are block reductions.
 #include "common.cuh"
 #include "launch.h"
+#include "tc_common.cuh"
 
 namespace mesa {
 // Status word of the decode kernels on this device (each device that loads the library has
@@ -192,223 +193,217 @@ __global__ void __launch_bounds__(4 * D) mesa_decode_kernel(DecArgs a) {
 
 
 // d = 128 specialisation.  Same update, CG rule and readout; differences:
-//  - 8 warps (256 threads); warp w owns rows 16w .. 16w+15.  Lane l = 8b + cb holds rows
-//    16w + 4b .. +3 and the float4 column groups cb, cb+8, cb+16, cb+24 of each (H in 64
-//    registers; the 8 lanes of a band read 128 contiguous bytes of a row), so a row sum is a
-//    16-term in-lane sum plus a 3-step reduce-scatter over the band's 8 lanes; after it,
-//    row 16w + 4b + ((l >> 1) & 3) is held, replicated, by lanes l and l^1, which also hold
-//    that row's x, r, p and lambda;
-//  - p's columns live in registers and its rows with their owners, so the second block
-//    reduction of a CG step also publishes the new residual and each thread updates its
-//    own copy of p: two barriers per step;
-//  - G is copied to shared memory with cp.async at the start (it is needed only for the
-//    readout), so its HBM read overlaps the CG;
-//  - two units per SM: one unit's HBM traffic overlaps the other's CG.
-template <typename TIO>
-__global__ void __launch_bounds__(256, 2) mesa_decode128_kernel(DecArgs a) {
-  constexpr int D = 128, NW = 8;
-  const int u = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int band = lane >> 3, cb = lane & 7;
-  const int row0 = 16 * warp + 4 * band;            // first of this lane's 4 rows
-  const int row = row0 + ((lane >> 1) & 3);         // the row this lane holds after the reduce
-  extern __shared__ __align__(16) float dsm[];
-  float *Gs = dsm;                                  // [128][128]
-  float *kvec = Gs + D * D, *vvec = kvec + D, *pvec = vvec + D, *rvec = pvec + D;
-  float *red = rvec + D;                            // [2][NW]
+//  - one thread per row of H (128 threads, three units per SM): the thread holds its row of
+//    the updated H in 128 registers, so a matrix-vector product is an in-thread dot product
+//    with the vector read from shared memory (the same address for every lane: a broadcast);
+//  - H comes in and goes out by tiled bulk copies (four boxes of 32 columns x 128 rows,
+//    128-byte swizzled in shared memory, so that each thread reads and writes its row without
+//    bank conflicts), G is fetched into L2 at the start and read row-coalesced by the readout;
+//  - CG keeps s = (H + Lambda) p by the recurrence s <- (H + Lambda) r + beta s, so the
+//    product is taken of r, which the second reduction of a step publishes anyway: two block
+//    barriers per step, one product, no further exchange.
+constexpr int kDec128Threads = 128;
+constexpr uint32_t kDecSlab = 128 * 32 * 4;  // one box: 32 fp32 columns x 128 rows
+constexpr uint32_t kDecOffK = 4 * kDecSlab, kDecOffV = kDecOffK + 512, kDecOffB0 = kDecOffV + 512,
+                   kDecOffB1 = kDecOffB0 + 512, kDecOffRed = kDecOffB1 + 512, kDecOffBar = kDecOffRed + 32;
+constexpr uint32_t kDecode128Smem = kDecOffBar + 16 + 1024;  // + alignment slack
 
-  const float4 *Hg = reinterpret_cast<const float4 *>(a.Hs + (size_t)u * D * D);
-  float4 *Hw = reinterpret_cast<float4 *>(a.Hs + (size_t)u * D * D);
-  float4 *Gw = reinterpret_cast<float4 *>(a.Gs + (size_t)u * D * D);
-  // G -> shared memory, asynchronously (16 x 16 bytes per thread)
-  {
-    const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(Gs);
-    const float4 *gsrc = reinterpret_cast<const float4 *>(a.Gs + (size_t)u * D * D);
+// Sums over the 32 lanes of 32 values per lane, scattered: lane l returns the sum of v[l].
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 #pragma unroll
-    for (int k = 0; k < 16; k++) {
-      const int e = threadIdx.x + 256 * k;  // float4 index
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sbase + 16 * e), "l"(gsrc + e)
-                   : "memory");
-    }
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
-  }
-  // h[i][j] = H[row0 + i][4 (cb + 8 j) .. +3]
-  float4 h[4][4];
+  for (int h = 16; h >= 1; h >>= 1) {
+    const bool up = lane & h;
 #pragma unroll
-  for (int i = 0; i < 4; i++)
-#pragma unroll
-    for (int j = 0; j < 4; j++) h[i][j] = Hg[(row0 + i) * 32 + cb + 8 * j];
-  const TIO *q = (const TIO *)a.q, *k = (const TIO *)a.k, *v = (const TIO *)a.v;
-  if (threadIdx.x < D) {
-    kvec[threadIdx.x] = ld(k, (size_t)u * D + threadIdx.x);
-    vvec[threadIdx.x] = ld(v, (size_t)u * D + threadIdx.x);
-    pvec[threadIdx.x] = ld(q, (size_t)u * D + threadIdx.x);
-  }
-  const float g = a.gamma[u];
-  const float lam_r = a.lambda[(size_t)(u % a.H) * D + row];
-  __syncthreads();
-
-  const float4 *k4 = reinterpret_cast<const float4 *>(kvec);
-  float4 kc[4];
-#pragma unroll
-  for (int j = 0; j < 4; j++) kc[j] = k4[cb + 8 * j];
-#pragma unroll
-  for (int i = 0; i < 4; i++) {
-    const float kr = kvec[row0 + i];
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-      h[i][j].x = fmaf(g, h[i][j].x, kr * kc[j].x);
-      h[i][j].y = fmaf(g, h[i][j].y, kr * kc[j].y);
-      h[i][j].z = fmaf(g, h[i][j].z, kr * kc[j].z);
-      h[i][j].w = fmaf(g, h[i][j].w, kr * kc[j].w);
-      Hw[(row0 + i) * 32 + cb + 8 * j] = h[i][j];
+    for (int t = 0; t < h; t++) {
+      const float send = up ? v[t] : v[t + h];
+      const float keep = up ? v[t + h] : v[t];
+      v[t] = keep + __shfl_xor_sync(0xffffffffu, send, h);
     }
   }
-
-  // reduce-scatter of s[0..3] (rows row0 .. row0+3) over the band's 8 lanes: the full sum
-  // of row row0 + ((lane >> 1) & 3)
-  auto rowsum = [&](float (&s)[4]) -> float {
-    const bool b2 = lane & 4, b1 = lane & 2;
-    float t2[2];
-#pragma unroll
-    for (int q2 = 0; q2 < 2; q2++)
-      t2[q2] = (b2 ? s[q2 + 2] : s[q2]) + __shfl_xor_sync(0xffffffffu, b2 ? s[q2] : s[q2 + 2], 4);
-    float t = (b1 ? t2[1] : t2[0]) + __shfl_xor_sync(0xffffffffu, b1 ? t2[0] : t2[1], 2);
-    return t + __shfl_xor_sync(0xffffffffu, t, 1);
-  };
-  // sum over the warp's 16 rows of a value replicated in each lane pair, then over warps
-  auto block_rows_sum = [&](float val, int buf) -> float {
-    val += __shfl_xor_sync(0xffffffffu, val, 2);
-    val += __shfl_xor_sync(0xffffffffu, val, 4);
-    val += __shfl_xor_sync(0xffffffffu, val, 8);
-    val += __shfl_xor_sync(0xffffffffu, val, 16);
-    if (lane == 0) red[buf * NW + warp] = val;
-    __syncthreads();
-    const float4 a0 = reinterpret_cast<const float4 *>(red + buf * NW)[0];
-    const float4 a1 = reinterpret_cast<const float4 *>(red + buf * NW)[1];
-    return ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
-  };
-  auto matvec_rows = [&](const float4 (&pc)[4], float (&s)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; i++) {  // four independent partial sums per row: short chains
-      float t[4];
-#pragma unroll
-      for (int j = 0; j < 4; j++)
-        t[j] = fmaf(h[i][j].w, pc[j].w, fmaf(h[i][j].z, pc[j].z, fmaf(h[i][j].y, pc[j].y, h[i][j].x * pc[j].x)));
-      s[i] = (t[0] + t[1]) + (t[2] + t[3]);
-    }
-  };
-
-  // p's columns live in registers (pc) and p's rows with their owners (pr); after the
-  // second reduction of a step every thread updates its own copy of p from the new
-  // residual (rvec) without a further barrier.
-  float xr = 0.0f, rr = pvec[row], pr = rr;
-  float rho = block_rows_sum(rr * rr, 0);
-  const float nq = sqrtf(rho);  // the stopping rule is relative to ||q||
-  const float4 *p4 = reinterpret_cast<const float4 *>(pvec);
-  if (a.Xs) {  // warm start: x = x0, r = p = q - (H + Lambda) x0, p's columns via rvec
-    const float4 *x4 = reinterpret_cast<const float4 *>(a.Xs + (size_t)u * D);
-    float4 xc0[4];
-#pragma unroll
-    for (int j = 0; j < 4; j++) xc0[j] = x4[cb + 8 * j];
-    float s0[4];
-    matvec_rows(xc0, s0);
-    xr = a.Xs[(size_t)u * D + row];
-    rr = rr - fmaf(lam_r, xr, rowsum(s0));
-    pr = rr;
-    if ((lane & 1) == 0) rvec[row] = rr;
-    rho = block_rows_sum(rr * rr, 1);  // its barrier also publishes rvec
-    __syncthreads();                   // red[1] is read before the first CG step writes it
-    p4 = reinterpret_cast<const float4 *>(rvec);
-  }
-  float4 pc[4];
-#pragma unroll
-  for (int j = 0; j < 4; j++) pc[j] = p4[cb + 8 * j];
-  p4 = reinterpret_cast<const float4 *>(pvec);
-  const bool dynamic = a.cg_tol > 0.0f;
-  const float4 *r4 = reinterpret_cast<const float4 *>(rvec);
-  int it = 0;
-  for (; it < a.cg_iters; it++) {
-    if (dynamic && sqrtf(rho) <= a.cg_tol * nq) break;
-    float s[4];
-    matvec_rows(pc, s);
-    const float w = fmaf(lam_r, pr, rowsum(s));
-    const float sigma = block_rows_sum(pr * w, 1);
-    const float alpha = (sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
-    xr = fmaf(alpha, pr, xr);
-    rr = fmaf(-alpha, w, rr);
-    if ((lane & 1) == 0) rvec[row] = rr;
-    const float rn = block_rows_sum(rr * rr, 0);  // its barrier also publishes rvec
-    const float beta = rho > 0.0f ? rn / rho : 0.0f;
-    pr = fmaf(beta, pr, rr);
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const float4 rc = r4[cb + 8 * j];
-      pc[j].x = fmaf(beta, pc[j].x, rc.x);
-      pc[j].y = fmaf(beta, pc[j].y, rc.y);
-      pc[j].z = fmaf(beta, pc[j].z, rc.z);
-      pc[j].w = fmaf(beta, pc[j].w, rc.w);
-    }
-    rho = rn;
-  }
-
-  // readout: G <- gamma G + v k^T (from the shared copy), o = G x
-  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-  __syncthreads();
-  if ((lane & 1) == 0) pvec[row] = xr;
-  __syncthreads();
-  float4 xc[4];
-#pragma unroll
-  for (int j = 0; j < 4; j++) xc[j] = p4[cb + 8 * j];
-  const float4 *G4 = reinterpret_cast<const float4 *>(Gs);
-  float s[4];
-#pragma unroll
-  for (int i = 0; i < 4; i++) {
-    const float vr = vvec[row0 + i];
-    float t = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const int e = (row0 + i) * 32 + cb + 8 * j;
-      float4 gg = G4[e];
-      gg.x = fmaf(g, gg.x, vr * kc[j].x);
-      gg.y = fmaf(g, gg.y, vr * kc[j].y);
-      gg.z = fmaf(g, gg.z, vr * kc[j].z);
-      gg.w = fmaf(g, gg.w, vr * kc[j].w);
-      Gw[e] = gg;
-      t = fmaf(gg.w, xc[j].w, fmaf(gg.z, xc[j].z, fmaf(gg.y, xc[j].y, fmaf(gg.x, xc[j].x, t))));
-    }
-    s[i] = t;
-  }
-  const float o = rowsum(s);
-  if ((lane & 1) == 0) st((TIO *)a.out, (size_t)u * D + row, o);
-  if ((lane & 1) == 0 && a.Xs) a.Xs[(size_t)u * D + row] = xr;
-  if ((lane & 1) == 0 && !isfinite(o)) atomicOr(&g_decode_status, tc_err_nonfinite());
-  if (threadIdx.x == 0 && a.iters) a.iters[u] = it;
+  return v[0];
 }
 
-// (Measured alternatives, 256 x 16 decode workload: H in shared memory with three units per
-// SM, 0.287 ms per step; a persistent kernel that streams the next unit's H and G in while
-// one unit per SM runs its CG, 0.328 ms; this kernel, two units per SM, 0.256 ms.  A
-// persistent kernel with two CTAs per SM, the next unit's H streamed into shared memory and
-// G fetched into L2 during the CG: 0.269 against 0.264 ms in an interleaved comparison; its
-// phase clocks show the CG chain, ~1.5k cycles per iteration, taking 62 % of a unit's time.
-// One barrier per CG step instead of two -- w published by rows, every lane updating its own
-// columns of r and p, p.w and |r|^2 as band reductions over columns: 0.303 against 0.264 ms.
-// Computing |r_new|^2 as rho - 2 alpha r.w + alpha^2 w.w would save the second reduction
-// too, but in an fp32 emulation its cancellation left the stopping decisions in agreement
-// with the fp64 oracle on only 76 % of units.)
-constexpr int kDecode128Smem = (128 * 128 + 4 * 128 + 2 * 8) * sizeof(float);
+template <typename TIO>
+__global__ void __launch_bounds__(kDec128Threads, 3)
+    mesa_decode128_kernel(DecArgs a, const __grid_constant__ CUtensorMap mapH) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t dec_raw[];
+  uint8_t *sm = dec_raw + ((1024 - (tc::smem_u32(dec_raw) & 1023)) & 1023);
+  float *kvec = reinterpret_cast<float *>(sm + kDecOffK), *vvec = reinterpret_cast<float *>(sm + kDecOffV);
+  float *b0 = reinterpret_cast<float *>(sm + kDecOffB0), *b1 = reinterpret_cast<float *>(sm + kDecOffB1);
+  float *red = reinterpret_cast<float *>(sm + kDecOffRed);  // [2][4]
+  const uint32_t bar = tc::smem_u32(sm + kDecOffBar);
+  const int u = blockIdx.x, i = threadIdx.x, warp = i >> 5, lane = i & 31;
+  const int y0 = u * D;  // this unit's first row in the [N H D, D] view of the states
+
+  if (i == 0) {  // H by four tiled bulk copies
+    tc::mbar_init(bar, 1);
+    tc::mbar_arrive_expect_tx(bar, 4 * kDecSlab);
+#pragma unroll
+    for (int b = 0; b < 4; b++) tc::tensor_g2s_2d(tc::smem_u32(sm + b * kDecSlab), &mapH, 32 * b, y0, bar);
+  }
+  {  // G into L2 meanwhile (the readout reads it)
+    const char *gp = reinterpret_cast<const char *>(a.Gs + (size_t)u * D * D);
+    for (int o = i * 128; o < D * D * 4; o += kDec128Threads * 128)
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(gp + o));
+  }
+  const TIO *q = (const TIO *)a.q, *k = (const TIO *)a.k, *v = (const TIO *)a.v;
+  kvec[i] = ld(k, (size_t)u * D + i);
+  vvec[i] = ld(v, (size_t)u * D + i);
+  const float qi = ld(q, (size_t)u * D + i);
+  const float g = a.gamma[u];
+  const float lam = a.lambda[(size_t)(u % a.H) * D + i];
+  const float x0 = a.Xs ? a.Xs[(size_t)u * D + i] : 0.0f;
+  __syncthreads();  // k, v and the barrier's initialisation visible
+  // H has landed (bounded wait; on a give-up the copies are waited for with the default limit
+  // and the unit is left as it was, reported in the status word)
+  if (__syncthreads_or(!tc::mbar_wait(bar, 0, a.wait_limit))) {
+    if (i == 0) atomicOr(&g_decode_status, tc::kErrMmaTimeout);
+    if (__syncthreads_or(!tc::mbar_wait(bar, 0, tc::kWaitLimit)) && i == 0)
+      atomicOr(&g_decode_status, tc::kErrDrainTimeout);
+    return;
+  }
+
+  // H <- gamma H + k k^T: row i, chunk c (4 columns) of box b at b*16K + 128 i + 16 (c ^ (i % 8))
+  float h[D];
+  const float ki = kvec[i];
+#pragma unroll
+  for (int b = 0; b < 4; b++) {
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+      float4 *hp = reinterpret_cast<float4 *>(sm + b * kDecSlab + i * 128 + ((c ^ (i & 7)) << 4));
+      float4 hv = *hp;
+      const float4 kc = reinterpret_cast<const float4 *>(kvec)[8 * b + c];
+      hv.x = fmaf(g, hv.x, ki * kc.x);
+      hv.y = fmaf(g, hv.y, ki * kc.y);
+      hv.z = fmaf(g, hv.z, ki * kc.z);
+      hv.w = fmaf(g, hv.w, ki * kc.w);
+      *hp = hv;
+      h[32 * b + 4 * c] = hv.x;
+      h[32 * b + 4 * c + 1] = hv.y;
+      h[32 * b + 4 * c + 2] = hv.z;
+      h[32 * b + 4 * c + 3] = hv.w;
+    }
+  }
+  tc::fence_smem_to_async();
+  __syncthreads();
+  if (i == 0) {  // the updated H goes out while the CG runs
+#pragma unroll
+    for (int b = 0; b < 4; b++) tc::tensor_s2g_2d(&mapH, tc::smem_u32(sm + b * kDecSlab), 32 * b, y0);
+    tc::bulk_commit();
+  }
+
+  auto block_sum = [&](float val, int slot) -> float {  // over the 128 threads
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) val += __shfl_xor_sync(0xffffffffu, val, o);
+    if (lane == 0) red[4 * slot + warp] = val;
+    __syncthreads();
+    const float4 r4 = reinterpret_cast<const float4 *>(red)[slot];
+    return (r4.x + r4.y) + (r4.z + r4.w);
+  };
+  auto matvec = [&](const float *vec) -> float {  // (H vec)_i, vec in shared memory
+    float acc[8];
+#pragma unroll
+    for (int t = 0; t < 8; t++) acc[t] = 0.0f;
+#pragma unroll
+    for (int c = 0; c < D / 4; c++) {
+      const float4 v4 = reinterpret_cast<const float4 *>(vec)[c];
+      const int t = 4 * (c & 1);
+      acc[t] = fmaf(h[4 * c], v4.x, acc[t]);
+      acc[t + 1] = fmaf(h[4 * c + 1], v4.y, acc[t + 1]);
+      acc[t + 2] = fmaf(h[4 * c + 2], v4.z, acc[t + 2]);
+      acc[t + 3] = fmaf(h[4 * c + 3], v4.w, acc[t + 3]);
+    }
+    return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+  };
+
+  // CG from x0 (0 unless warm): r = q - (H + Lambda) x0, p = r, s = (H + Lambda) p
+  const float nq = sqrtf(block_sum(qi * qi, 0));  // the stopping rule is relative to ||q||
+  float xr = x0, rr = qi;
+  if (a.Xs) {
+    b0[i] = x0;
+    __syncthreads();
+    rr = qi - fmaf(lam, x0, matvec(b0));
+  }
+  b1[i] = rr;
+  float rho = block_sum(rr * rr, 1);  // its barrier also publishes r
+  const bool dynamic = a.cg_tol > 0.0f;
+  float pr = rr, sr = 0.0f;
+  int it = 0;
+  if (a.cg_iters > 0 && !(dynamic && sqrtf(rho) <= a.cg_tol * nq)) sr = fmaf(lam, rr, matvec(b1));
+  for (; it < a.cg_iters; it++) {
+    if (dynamic && sqrtf(rho) <= a.cg_tol * nq) break;
+    const float sigma = block_sum(pr * sr, 0);
+    const float alpha = (sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
+    xr = fmaf(alpha, pr, xr);
+    rr = fmaf(-alpha, sr, rr);
+    b1[i] = rr;  // (every thread's product of the last r is done: it passed the barrier above)
+    const float rn = block_sum(rr * rr, 1);  // its barrier also publishes r
+    const float beta = rho > 0.0f ? rn / rho : 0.0f;
+    rho = rn;
+    pr = fmaf(beta, pr, rr);
+    // s = (H + Lambda) p = (H + Lambda) r + beta s, if another step follows
+    if (it + 1 < a.cg_iters && !(dynamic && sqrtf(rho) <= a.cg_tol * nq))
+      sr = fmaf(beta, sr, fmaf(lam, rr, matvec(b1)));
+  }
+
+  // readout: G <- gamma G + v k^T, o = G x; warp w takes rows 32w .. 32w+31 (lane l: their
+  // columns 4l .. 4l+3, 512 contiguous bytes per row)
+  b0[i] = xr;  // (b0 was last read before the first reduction of the CG)
+  __syncthreads();
+  const float4 kc = reinterpret_cast<const float4 *>(kvec)[lane];
+  const float4 xc = reinterpret_cast<const float4 *>(b0)[lane];
+  float4 *Gp = reinterpret_cast<float4 *>(a.Gs + (size_t)u * D * D);
+  float part[32];
+#pragma unroll
+  for (int half = 0; half < 2; half++) {
+    float4 gg[16];
+#pragma unroll
+    for (int r = 0; r < 16; r++) gg[r] = Gp[(32 * warp + 16 * half + r) * 32 + lane];
+#pragma unroll
+    for (int r = 0; r < 16; r++) {
+      const int row = 32 * warp + 16 * half + r;
+      const float vr = vvec[row];
+      gg[r].x = fmaf(g, gg[r].x, vr * kc.x);
+      gg[r].y = fmaf(g, gg[r].y, vr * kc.y);
+      gg[r].z = fmaf(g, gg[r].z, vr * kc.z);
+      gg[r].w = fmaf(g, gg[r].w, vr * kc.w);
+      Gp[row * 32 + lane] = gg[r];
+      part[16 * half + r] =
+          fmaf(gg[r].w, xc.w, fmaf(gg[r].z, xc.z, fmaf(gg[r].y, xc.y, gg[r].x * xc.x)));
+    }
+  }
+  const float o = reduce_scatter32(part, lane);  // row 32 warp + lane
+  st((TIO *)a.out, (size_t)u * D + 32 * warp + lane, o);
+  if (!isfinite(o)) atomicOr(&g_decode_status, tc_err_nonfinite());
+  if (a.Xs) a.Xs[(size_t)u * D + i] = xr;
+  if (i == 0 && a.iters) a.iters[u] = it;
+  if (i == 0) tc::bulk_wait_all();  // the H stores complete before the block ends
+}
+
+// (Measured alternatives, 256 x 16 decode workload: an earlier kernel with 256 threads per
+// unit -- four rows of H per thread, row sums as shuffles over 8-lane bands, two units per
+// SM, G copied to shared memory by cp.async -- 0.276 ms per step; in it, one barrier per CG
+// step (the Chronopoulos-Gear arrangement, r and s columns per lane) was 20 % slower and
+// prefetching the next wave's states into L2 7 % slower.  Before that: H in shared memory
+// with three units per SM, 0.287 ms; persistent kernels streaming the next unit's states,
+// 0.269-0.328 ms.  Computing |r_new|^2 as rho - 2 alpha r.w + alpha^2 w.w would save the
+// second reduction, but in an fp32 emulation its cancellation left the stopping decisions in
+// agreement with the fp64 oracle on only 76 % of units.)
 
 template <int D, typename TIO>
 static int launch_dec_t(const DecArgs &a, cudaStream_t st) {
-  timing_mark_begin(K_DECODE, st);
   if constexpr (D == 128) {
+    CUtensorMap mapH{};
+    if (!tmap_rows128_f32(&mapH, a.Hs, (size_t)a.N * a.H * 128)) return -1;
     auto kfn = mesa_decode128_kernel<TIO>;
-    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecode128Smem) !=
+    if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecode128Smem) !=
         cudaSuccess)
       return -1;
-    kfn<<<a.N * a.H, 256, kDecode128Smem, st>>>(a);
+    timing_mark_begin(K_DECODE, st);
+    kfn<<<a.N * a.H, kDec128Threads, kDecode128Smem, st>>>(a, mapH);
   } else {
+    timing_mark_begin(K_DECODE, st);
     mesa_decode_kernel<D, TIO><<<a.N * a.H, 4 * D, 0, st>>>(a);
   }
   timing_mark_end(K_DECODE, st);

@@ -17,8 +17,6 @@
 // Segment 0 starts from the initial state, later segments from zero; mesa_carry_tc_kernel then
 // chains the segments (carry[s] = global state before segment s) and writes the final state,
 // and the CG kernel adds exp(Lc) carry when it loads a state.
-#include <cuda.h>  // CUtensorMap and its encoder's signature (the encoder is fetched at run time)
-
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -340,8 +338,9 @@ EncodeTiledFn encode_tiled() {
   }();
   return fn;
 }
-// [rows, 128] fp32 row-major at `base`, boxes of 32 columns x 128 rows, 128-byte swizzle.
-bool state_map(CUtensorMap *map, float *base, size_t rows) {
+}  // namespace
+
+bool tmap_rows128_f32(CUtensorMap *map, float *base, size_t rows) {
   const EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
@@ -352,7 +351,6 @@ bool state_map(CUtensorMap *map, float *base, size_t rows) {
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-}  // namespace
 
 int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st) {
   const int U = a.B * a.H;
@@ -361,8 +359,8 @@ int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status,
   auto kfn = pre ? mesa_states_tc_kernel<true> : mesa_states_tc_kernel<false>;
   const uint32_t smem = pre ? DT_SMEM_PRE : DT_SMEM;
   CUtensorMap mapH{}, mapG{};
-  if (!pre && (!state_map(&mapH, ws.SH, (size_t)U * NC * 128) || !state_map(&mapG, ws.SG, (size_t)U * NC * 128)))
-    return -1;
+  const size_t rows = (size_t)U * NC * 128;
+  if (!pre && (!tmap_rows128_f32(&mapH, ws.SH, rows) || !tmap_rows128_f32(&mapG, ws.SG, rows))) return -1;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return -1;
   timing_mark_begin(K_DELTA_TC, st);

@@ -1,6 +1,7 @@
 // launch.h -- host-side argument bundles and kernel launchers (internal to the library).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the encoder itself is fetched from the driver at run time)
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -51,6 +52,7 @@ struct DecArgs {
   float cg_tol;
   void *out;
   int32_t *iters;
+  unsigned wait_limit = 0;  // polls of the bounded waits for bulk copies (d = 128 kernel)
 };
 
 // The decode kernels' device status word (one per device, shared by every decode call on
@@ -120,6 +122,10 @@ int launch_tc_selftest(const float *A, const float *B, float *C1, float *C2, flo
 // Chunk-boundary states on the tensor cores (bf16 inputs, d = 128, 128-token chunks):
 // segment-local states, segment carries and the final state (see FwdWorkspace).
 int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cudaStream_t st);
+// Tensor map of a [rows, 128] fp32 row-major array at `base` (16-byte aligned) with boxes of
+// 32 columns x 128 rows and the 128-byte swizzle; false if the driver offers no encoder or
+// it rejects the map.
+bool tmap_rows128_f32(CUtensorMap *map, float *base, size_t rows);
 int launch_decode(const DecArgs &a, cudaStream_t st);
 // Backward pass: the right-hand sides of the second solve (needs ws's chunk-kBwdChunk states
 // and log-decays), then the state adjoints and every gradient.

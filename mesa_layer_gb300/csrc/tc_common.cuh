@@ -249,7 +249,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_saddr, const void *src, ui
       : "memory");
 }
 
-// ---- tensor stores (TMA, tiled) ---------------------------------------------------------
+// ---- tensor loads and stores (TMA, tiled) -----------------------------------------------
+// Load the box of the tensor map `map` (a __grid_constant__ kernel parameter) whose first
+// element is at (x, y) into this CTA's shared memory at `dst_saddr` (1024-byte aligned for
+// the 128-byte swizzle), completing `bytes` transaction bytes on the mbarrier.  x times the
+// element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tensor_g2s_2d(uint32_t dst_saddr, const void *map, int x, int y,
+                                              uint32_t mbar_saddr) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          dst_saddr),
+      "l"(map), "r"(x), "r"(y), "r"(mbar_saddr)
+      : "memory");
+}
 // Store the box of the tensor map `map` (a kernel parameter declared __grid_constant__) whose
 // first element is at coordinates (x, y) from this CTA's shared memory at `src_saddr` (laid
 // out as the map's swizzle mode wants it) to global memory; tracked as a bulk group of the

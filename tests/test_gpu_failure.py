@@ -160,3 +160,40 @@ def test_nonfinite_decode_inputs(d, where):
         a, b = a.float().cpu().numpy(), b.float().cpu().numpy()
         assert np.array_equal(a[other], b[other])
     assert not np.isfinite(o2[1, 0].float().cpu().numpy()).all()
+
+
+def test_decode_wait_give_up_reports_timeout_and_leaves_the_state():
+    """d = 128 decode: its bounded wait for the bulk copy of H made to give up at once; the
+    step reports MESA_ERR_TIMEOUT through mesa_decode_status, leaves H and G as they were, and
+    the next step with the default limit is clean and equals a step from the same state."""
+    import torch
+
+    from mesa_layer_gb300 import binding
+    w = synth.workload("decode_bf16_d128", B=3, H=2)
+    lam = torch.from_numpy(synth.lambdas(w)).cuda()
+    H1 = torch.zeros(w.B, w.H, 128, 128, device="cuda")
+    G1 = torch.zeros_like(H1)
+
+    def dev(x):
+        return {k: torch.from_numpy(x[k]).cuda().to(torch.bfloat16 if k != "gamma" else torch.float32)
+                for k in ("q", "k", "v", "gamma")}
+
+    for s in range(-16, 0):
+        x = dev(synth.decode_inputs(w, s))
+        binding.mesa_decode_step(H1, G1, x["q"], x["k"], x["v"], x["gamma"], lam, 0, 0.0)
+    assert binding.mesa_decode_status()[0] == binding.MESA_OK
+    H0, G0 = H1.clone(), G1.clone()
+    x = dev(synth.decode_inputs(w, 0))
+    binding.mesa_debug_set_wait_limit(0)
+    try:
+        binding.mesa_decode_step(H1, G1, **x, lambda_diag=lam, cg_iters=w.cg_iters, cg_tol=w.cg_tol)
+    finally:
+        binding.mesa_debug_set_wait_limit(-1)
+    code, flags = binding.mesa_decode_status()
+    assert code == binding.MESA_ERR_TIMEOUT and flags & 1 and not flags & 4, (code, flags)
+    assert torch.equal(H1, H0) and torch.equal(G1, G0)
+    o1, i1 = binding.mesa_decode_step(H1, G1, **x, lambda_diag=lam, cg_iters=w.cg_iters, cg_tol=w.cg_tol)
+    assert binding.mesa_decode_status() == (binding.MESA_OK, 0)
+    H2, G2 = H0.clone(), G0.clone()
+    o2, i2 = binding.mesa_decode_step(H2, G2, **x, lambda_diag=lam, cg_iters=w.cg_iters, cg_tol=w.cg_tol)
+    assert torch.equal(o1, o2) and torch.equal(i1, i2) and torch.equal(H1, H2) and torch.equal(G1, G2)
