@@ -122,3 +122,4 @@ def test_full_workload_sampled_units():
             x = inp[raw][b:b + 1, h:h + 1]
             ref = oracle.qk_preprocess(x, inp[wt][h:h + 1])
             _check(o[b:b + 1, h:h + 1].float().cpu().numpy(), ref, w.dtype, f"pre full {name} b={b} h={h}")
+
