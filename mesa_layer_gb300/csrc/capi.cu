@@ -203,6 +203,7 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_BWD_FSTATES: return "mesa_state_sweep_kernel<states>";
     case mesa::K_BWD_GRAD: return "mesa_bwd_grad_kernel+mesa_bwd_lambda_kernel";
     case mesa::K_CG_TC64: return "mesa_cg_tc64_kernel";
+    case mesa::K_CARRY_TC: return "mesa_carry_tc_kernel";
   }
   return nullptr;
 }

@@ -367,10 +367,10 @@ int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status,
   kfn<<<dim3(ws.nseg, U), 512, smem, st>>>(a, ws, NC, status, mapH, mapG);
   timing_mark_end(K_DELTA_TC, st);
   if (ws.nseg > 1 || a.H_final) {
-    timing_mark_begin(K_SCAN, st);
+    timing_mark_begin(K_CARRY_TC, st);
     mesa_carry_tc_kernel<<<dim3((2 * 128 * 128 + 255) / 256, U), 256, 0, st>>>(ws, NC, a.H_final,
                                                                                 a.G_final);
-    timing_mark_end(K_SCAN, st);
+    timing_mark_end(K_CARRY_TC, st);
   }
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

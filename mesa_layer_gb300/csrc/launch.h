@@ -88,7 +88,7 @@ struct PreArgs {
 enum KernelKind {
   K_ELL = 0, K_DELTA = 1, K_SCAN = 2, K_CG_SIMT = 3, K_DECODE = 4, K_CG_TC = 5, K_DELTA_TC = 6, K_CG_ROWS = 7,
   K_PREPROC = 8, K_BWD_RHS = 9, K_BWD_STATES = 10, K_BWD_GRAD = 11, K_BWD_FSTATES = 12,
-  K_CG_TC64 = 13, K_NUM_KINDS = 14
+  K_CG_TC64 = 13, K_CARRY_TC = 14, K_NUM_KINDS = 15
 };
 
 // Record a timing event before / after a launch of `kind` on `st` (no-op unless enabled).
