@@ -515,40 +515,48 @@ def bench_forward(args, w, rank, world, dev, lib, torch, binding):
     return res
 
 
-def pipelined_e2e(torch, dev, host_in: dict, run, host_out: dict, steps: int, warmup: int = 3):
+def pipelined_e2e(torch, dev, host_in, run, host_out: dict, steps: int, warmup: int = 3):
     """Time `steps` end-to-end steps: each copies its inputs from pinned host memory to the
-    device, runs the call, and copies its results back to pinned host memory.  Inputs are
-    double-buffered on the device and uploaded on a second stream, so that step i+1's upload
-    overlaps step i's compute and download (as a caller streaming batches would run it).
-    `run(d_in, stream)` launches the call on `stream` and returns the device results, matched
-    by name to `host_out`.  Returns ms per step (first upload issued to last download done)."""
-    s_copy, s_comp = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    bufs = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
-    ready = [torch.cuda.Event() for _ in range(2)]
-    free = [torch.cuda.Event() for _ in range(2)]
-    for e in free:
+    device, runs the call, and copies its results back to pinned host memory.  Inputs and
+    results are double-buffered on the device, uploads and downloads run on streams of their
+    own, so that step i+1's upload and step i-1's download overlap step i's compute (as a
+    caller streaming batches would run it).  `host_in` is a dict of pinned tensors, or a list
+    of them used in turn.  `run(d_in, stream, slot)` launches the call on `stream` with its
+    results in device buffer set `slot` (0 or 1) and returns them, matched by name to
+    `host_out`.  Returns ms per step (first upload issued to last download done)."""
+    ins = host_in if isinstance(host_in, list) else [host_in]
+    s_up, s_comp, s_down = (torch.cuda.Stream(device=dev) for _ in range(3))
+    bufs = [{k: torch.empty_like(v, device=dev) for k, v in ins[0].items()} for _ in range(2)]
+    ev = lambda: [torch.cuda.Event() for _ in range(2)]
+    in_ready, in_free, out_ready, out_free = ev(), ev(), ev(), ev()
+    for e in in_free + out_free:
         e.record(s_comp)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    n_all = warmup + steps
-    for i in range(n_all):
+    for i in range(warmup + steps):
         b = i % 2
         if i == warmup:
             torch.cuda.synchronize()
-            start.record(s_copy)
-        with torch.cuda.stream(s_copy):
-            s_copy.wait_event(free[b])  # the compute that read this buffer is done
-            for k, v in host_in.items():
+            start.record(s_up)
+        with torch.cuda.stream(s_up):
+            s_up.wait_event(in_free[b])  # the compute that read this input buffer is done
+            for k, v in ins[i % len(ins)].items():
                 bufs[b][k].copy_(v, non_blocking=True)
-            ready[b].record(s_copy)
+            in_ready[b].record(s_up)
         with torch.cuda.stream(s_comp):
-            s_comp.wait_event(ready[b])
-            out = run(bufs[b], s_comp)
+            s_comp.wait_event(in_ready[b])
+            s_comp.wait_event(out_free[b])  # the download of this result buffer is done
+            out = run(bufs[b], s_comp, b)
+            in_free[b].record(s_comp)
+            out_ready[b].record(s_comp)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(out_ready[b])
             for k, v in host_out.items():
                 v.copy_(out[k], non_blocking=True)
-            free[b].record(s_comp)
-    end.record(s_comp)
-    s_comp.wait_stream(s_copy)
+            out_free[b].record(s_down)
+    s_down.wait_stream(s_up)
+    s_down.wait_stream(s_comp)
+    end.record(s_down)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / steps
 
@@ -559,24 +567,24 @@ def e2e_forward(args, w, dev, torch, binding, inp, td, ws):
     h = {k: torch.from_numpy(inp[k]).to(td if k in ("q", "k", "v") else torch.float32).pin_memory()
          for k in ("q", "k", "v", "gamma")}
     lam = torch.from_numpy(inp["lam"]).to(dev)
-    out = torch.empty((w.B, w.H, w.T, w.dv), dtype=td, device=dev)
-    iters = torch.empty((w.B, w.H, w.T), dtype=torch.int32, device=dev)
-    h_out = {"out": torch.empty(out.shape, dtype=td).pin_memory(),
-             "iters": torch.empty(iters.shape, dtype=torch.int32).pin_memory()}
+    outs = [{"out": torch.empty((w.B, w.H, w.T, w.dv), dtype=td, device=dev),
+             "iters": torch.empty((w.B, w.H, w.T), dtype=torch.int32, device=dev)} for _ in range(2)]
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs[0].items()}
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
 
     taps = {k: torch.from_numpy(inp[k]).to(dev) for k in ("wq", "wk")} if w.fused else None
 
-    def run(d, stream):
+    def run(d, stream, slot):
+        o = outs[slot]
         if taps is not None:
             binding.mesa_forward_chunked_pre(d["q"], d["k"], taps["wq"], taps["wk"], d["v"], d["gamma"], lam,
-                                             w.cg_iters, w.cg_tol, w.chunk, out=out, iters_used=iters, workspace=ws,
-                                             stream=stream)
+                                             w.cg_iters, w.cg_tol, w.chunk, out=o["out"], iters_used=o["iters"],
+                                             workspace=ws, stream=stream)
         else:
             binding.mesa_forward_chunked(d["q"], d["k"], d["v"], d["gamma"], lam, w.cg_iters, w.cg_tol, w.chunk,
-                                         out=out, iters_used=iters, workspace=ws, stream=stream)
-        return {"out": out, "iters": iters}
+                                         out=o["out"], iters_used=o["iters"], workspace=ws, stream=stream)
+        return o
 
     ms = pipelined_e2e(torch, dev, h, run, h_out, max(3, min(args.steps, 50)), max(3, args.warmup))
     return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h}
@@ -618,36 +626,25 @@ def bench_decode(args, w, rank, world, dev, lib, torch, binding):
     res = timed_loop(args, torch, lib, step, None, world, dist, dev)
     res.update({"iters": iters.cpu().numpy(), "tokens_per_step": N, "flush": False})
     if not args.no_e2e:
+        hs = [{k: st_[k].cpu().pin_memory() for k in st_} for st_ in steps]
+        douts = [{"out": torch.empty_like(out), "iters": torch.empty_like(iters)} for _ in range(2)]
+        h_back = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in douts[0].items()}
+
+        def run(d, stream, slot):
+            o = douts[slot]
+            if Xs is not None:
+                binding.mesa_decode_step_warm(Hs, Gs, Xs, d["q"], d["k"], d["v"], d["gamma"], lam, w.cg_iters,
+                                              w.cg_tol, out=o["out"], iters_used=o["iters"], stream=stream)
+            else:
+                binding.mesa_decode_step(Hs, Gs, d["q"], d["k"], d["v"], d["gamma"], lam, w.cg_iters, w.cg_tol,
+                                         out=o["out"], iters_used=o["iters"], stream=stream)
+            return o
+
         # each step's own inputs from pinned host memory, in the same order as the device loop
         # (repeating one step's inputs would hand the warm start its own solution)
-        hs = [{k: st_[k].cpu().pin_memory() for k in st_} for st_ in steps]
-        dd = {k: torch.empty_like(steps[0][k]) for k in steps[0]}
-        h_out = torch.empty(out.shape, dtype=td).pin_memory()
-        h_it = torch.empty(iters.shape, dtype=torch.int32).pin_memory()
-        ecount = [0]
-
-        def estep():
-            h = hs[ecount[0] % n_steps]
-            ecount[0] += 1
-            for k in h:
-                dd[k].copy_(h[k], non_blocking=True)
-            decode(dd["q"], dd["k"], dd["v"], dd["gamma"])
-            h_out.copy_(out, non_blocking=True)
-            h_it.copy_(iters, non_blocking=True)
-
-        for _ in range(3):
-            estep()
-        torch.cuda.synchronize()
-        n = max(3, min(args.steps, 50))
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record()
-        for _ in range(n):
-            estep()
-        e.record()
-        torch.cuda.synchronize()
-        res["e2e"] = {"ms_per_step": s.elapsed_time(e) / n,
-                      "h2d": sum(t.numel() * t.element_size() for t in hs[0].values()),
-                      "d2h": h_out.numel() * h_out.element_size() + h_it.numel() * 4}
+        ms = pipelined_e2e(torch, dev, hs, run, h_back, max(3, min(args.steps, 50)))
+        res["e2e"] = {"ms_per_step": ms, "h2d": sum(t.numel() * t.element_size() for t in hs[0].values()),
+                      "d2h": sum(t.numel() * t.element_size() for t in h_back.values())}
     return res
 
 
@@ -671,11 +668,13 @@ def bench_preprocess(args, w, rank, world, dev, lib, torch, binding):
     if not args.no_e2e:
         h = {k: torch.from_numpy(inp[k]).to(td).pin_memory() for k in ("q_raw", "k_raw")}
         back = {"q": torch.empty_like(h["q_raw"]).pin_memory(), "k": torch.empty_like(h["k_raw"]).pin_memory()}
+        pouts = [{"q": torch.empty_like(qo), "k": torch.empty_like(ko)} for _ in range(2)]
 
-        def run(d, stream):
-            binding.mesa_qk_preprocess(d["q_raw"], d["k_raw"], d_in["wq"], d_in["wk"], q_out=qo, k_out=ko,
+        def run(d, stream, slot):
+            o = pouts[slot]
+            binding.mesa_qk_preprocess(d["q_raw"], d["k_raw"], d_in["wq"], d_in["wk"], q_out=o["q"], k_out=o["k"],
                                        stream=stream)
-            return {"q": qo, "k": ko}
+            return o
 
         ms = pipelined_e2e(torch, dev, h, run, back, max(3, min(args.steps, 50)))
         nb = sum(t.numel() * t.element_size() for t in h.values())
@@ -734,10 +733,12 @@ def bench_backward(args, w, rank, world, dev, lib, torch, binding):
         h["x_saved"] = xs.cpu().pin_memory()
         back = {k: torch.empty(outs[k].shape, dtype=outs[k].dtype).pin_memory() for k in ("dq", "dk", "dv", "dgamma", "dlambda")}
 
-        def run(d, stream):
+        bouts = [outs, {k: torch.empty_like(v) for k, v in outs.items()}]
+
+        def run(d, stream, slot):
             binding.mesa_backward_chunked(d["q"], d["k"], d["v"], d["gamma"], d_in["lam"], d["dout"], w.cg_iters,
-                                          w.cg_tol, workspace=ws, x_saved=d["x_saved"], stream=stream, **outs)
-            return outs
+                                          w.cg_tol, workspace=ws, x_saved=d["x_saved"], stream=stream, **bouts[slot])
+            return bouts[slot]
 
         ms = pipelined_e2e(torch, dev, h, run, back, max(3, min(args.steps, 20)))
         res["e2e"] = {"ms_per_step": ms, "h2d": sum(t.numel() * t.element_size() for t in h.values()),
