@@ -1,7 +1,8 @@
 // tc_common.cuh -- sm_103a tensor-core building blocks in inline PTX: tcgen05.mma
 // (kind::f16, fp16 operands, fp32 accumulators in tensor memory), shared-memory matrix
 // descriptors for the 128-byte-swizzled canonical layouts, tensor-memory allocation and
-// loads/stores, and mbarrier completion with bounded waits.
+// loads/stores, mbarrier completion with bounded waits, and the tensor memory accelerator's
+// bulk copies (untiled loads; tiled loads and stores through tensor maps).
 #pragma once
 
 #include <cuda_fp16.h>
