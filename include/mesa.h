@@ -162,9 +162,11 @@ int mesa_forward_chunked_save(int B, int H, int T, int dk, int dv, int dtype, co
  * then CG on (H_state + Lambda) x = q and out = G_state x.
  *   q, k [N, H, dk], v [N, H, dv] dtype; gamma [N, H] fp32; lambda_diag [H, dk] fp32;
  *   out [N, H, dv] dtype; iters_used [N, H] int32 or NULL.
- * For dk = 128 the step reads and writes H_state by tiled bulk copies (MESA_ERR_CUDA if the
- * driver offers no tensor-map encoder); a bounded wait for that copy that gives up leaves the
- * unit's states, output and count untouched and is reported by mesa_decode_status.
+ * For dk = 128 the step reads and writes H_state and G_state by tiled bulk copies
+ * (MESA_ERR_CUDA if the driver offers no tensor-map encoder); a bounded wait for a copy that
+ * gives up is reported by mesa_decode_status and leaves that unit's output and count
+ * untouched, and its states as they were (for the copy of H) or with H updated and G not
+ * (for the copy of G).
  */
 int mesa_decode_step(int N, int H, int dk, int dv, int dtype, float *H_state,
                      float *G_state, const void *q, const void *k, const void *v,
@@ -289,8 +291,8 @@ int mesa_forward_status(const void *workspace, cudaStream_t stream, unsigned *fl
  * Device status word of the decode steps (mesa_decode_step, mesa_decode_step_warm) on the
  * current device -- one word per device, shared by every decode call on it: copies it to
  * *flags (host), clears it, both on `stream`, and synchronises `stream`.  Bit 0 (1): a
- * bounded wait for the bulk copy of a unit's H gave up (dk = 128; that unit was left as it
- * was); bit 2 (4): the wait for that copy to land expired too; bit 1 (2): a decode step wrote
+ * bounded wait for the bulk copy of a unit's H or G gave up (dk = 128; see mesa_decode_step);
+ * bit 2 (4): the wait for that copy to land expired too; bit 1 (2): a decode step wrote
  * a non-finite output since the last query.  Returns MESA_ERR_TIMEOUT if bit 0 or 2 is set,
  * else MESA_ERR_NONFINITE if bit 1 is set, else MESA_OK (MESA_ERR_INVALID_ARG / MESA_ERR_CUDA
  * when the word could not be read).  A non-finite q, k, v or gamma affects only its own

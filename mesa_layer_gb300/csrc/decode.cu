@@ -198,7 +198,9 @@ __global__ void __launch_bounds__(4 * D) mesa_decode_kernel(DecArgs a) {
 //    with the vector read from shared memory (the same address for every lane: a broadcast);
 //  - H comes in and goes out by tiled bulk copies (four boxes of 32 columns x 128 rows,
 //    128-byte swizzled in shared memory, so that each thread reads and writes its row without
-//    bank conflicts), G is fetched into L2 at the start and read row-coalesced by the readout;
+//    bank conflicts); G follows into the same staging buffer while the CG runs (once the H
+//    stores have read it), so the readout updates row i of G and takes o_i = G_i x in thread
+//    i, and G leaves by tiled bulk copies too;
 //  - CG keeps s = (H + Lambda) p by the recurrence s <- (H + Lambda) r + beta s, so the
 //    product is taken of r, which the second reduction of a step publishes anyway: two block
 //    barriers per step, one product, no further exchange.
@@ -208,24 +210,10 @@ constexpr uint32_t kDecOffK = 4 * kDecSlab, kDecOffV = kDecOffK + 512, kDecOffB0
                    kDecOffB1 = kDecOffB0 + 512, kDecOffRed = kDecOffB1 + 512, kDecOffBar = kDecOffRed + 32;
 constexpr uint32_t kDecode128Smem = kDecOffBar + 16 + 1024;  // + alignment slack
 
-// Sums over the 32 lanes of 32 values per lane, scattered: lane l returns the sum of v[l].
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int h = 16; h >= 1; h >>= 1) {
-    const bool up = lane & h;
-#pragma unroll
-    for (int t = 0; t < h; t++) {
-      const float send = up ? v[t] : v[t + h];
-      const float keep = up ? v[t + h] : v[t];
-      v[t] = keep + __shfl_xor_sync(0xffffffffu, send, h);
-    }
-  }
-  return v[0];
-}
-
 template <typename TIO>
 __global__ void __launch_bounds__(kDec128Threads, 3)
-    mesa_decode128_kernel(DecArgs a, const __grid_constant__ CUtensorMap mapH) {
+    mesa_decode128_kernel(DecArgs a, const __grid_constant__ CUtensorMap mapH,
+                          const __grid_constant__ CUtensorMap mapG) {
   constexpr int D = 128;
   extern __shared__ uint8_t dec_raw[];
   uint8_t *sm = dec_raw + ((1024 - (tc::smem_u32(dec_raw) & 1023)) & 1023);
@@ -241,11 +229,6 @@ __global__ void __launch_bounds__(kDec128Threads, 3)
     tc::mbar_arrive_expect_tx(bar, 4 * kDecSlab);
 #pragma unroll
     for (int b = 0; b < 4; b++) tc::tensor_g2s_2d(tc::smem_u32(sm + b * kDecSlab), &mapH, 32 * b, y0, bar);
-  }
-  {  // G into L2 meanwhile (the readout reads it)
-    const char *gp = reinterpret_cast<const char *>(a.Gs + (size_t)u * D * D);
-    for (int o = i * 128; o < D * D * 4; o += kDec128Threads * 128)
-      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(gp + o));
   }
   const TIO *q = (const TIO *)a.q, *k = (const TIO *)a.k, *v = (const TIO *)a.v;
   kvec[i] = ld(k, (size_t)u * D + i);
@@ -331,6 +314,12 @@ __global__ void __launch_bounds__(kDec128Threads, 3)
   float pr = rr, sr = 0.0f;
   int it = 0;
   if (a.cg_iters > 0 && !(dynamic && sqrtf(rho) <= a.cg_tol * nq)) sr = fmaf(lam, rr, matvec(b1));
+  if (i == 0) {  // G into the staging buffer once the H stores have read it, while the CG runs
+    tc::bulk_wait_read();
+    tc::mbar_arrive_expect_tx(bar, 4 * kDecSlab);
+#pragma unroll
+    for (int b = 0; b < 4; b++) tc::tensor_g2s_2d(tc::smem_u32(sm + b * kDecSlab), &mapG, 32 * b, y0, bar);
+  }
   for (; it < a.cg_iters; it++) {
     if (dynamic && sqrtf(rho) <= a.cg_tol * nq) break;
     const float sigma = block_sum(pr * sr, 0);
@@ -347,38 +336,48 @@ __global__ void __launch_bounds__(kDec128Threads, 3)
       sr = fmaf(beta, sr, fmaf(lam, rr, matvec(b1)));
   }
 
-  // readout: G <- gamma G + v k^T, o = G x; warp w takes rows 32w .. 32w+31 (lane l: their
-  // columns 4l .. 4l+3, 512 contiguous bytes per row)
+  // readout: G <- gamma G + v k^T, o = G x; thread i takes row i of G in the staging buffer
   b0[i] = xr;  // (b0 was last read before the first reduction of the CG)
-  __syncthreads();
-  const float4 kc = reinterpret_cast<const float4 *>(kvec)[lane];
-  const float4 xc = reinterpret_cast<const float4 *>(b0)[lane];
-  float4 *Gp = reinterpret_cast<float4 *>(a.Gs + (size_t)u * D * D);
-  float part[32];
-#pragma unroll
-  for (int half = 0; half < 2; half++) {
-    float4 gg[16];
-#pragma unroll
-    for (int r = 0; r < 16; r++) gg[r] = Gp[(32 * warp + 16 * half + r) * 32 + lane];
-#pragma unroll
-    for (int r = 0; r < 16; r++) {
-      const int row = 32 * warp + 16 * half + r;
-      const float vr = vvec[row];
-      gg[r].x = fmaf(g, gg[r].x, vr * kc.x);
-      gg[r].y = fmaf(g, gg[r].y, vr * kc.y);
-      gg[r].z = fmaf(g, gg[r].z, vr * kc.z);
-      gg[r].w = fmaf(g, gg[r].w, vr * kc.w);
-      Gp[row * 32 + lane] = gg[r];
-      part[16 * half + r] =
-          fmaf(gg[r].w, xc.w, fmaf(gg[r].z, xc.z, fmaf(gg[r].y, xc.y, gg[r].x * xc.x)));
-    }
+  if (__syncthreads_or(!tc::mbar_wait(bar, 1, a.wait_limit))) {  // (its barrier also publishes x)
+    if (i == 0) atomicOr(&g_decode_status, tc::kErrMmaTimeout);
+    if (__syncthreads_or(!tc::mbar_wait(bar, 1, tc::kWaitLimit)) && i == 0)
+      atomicOr(&g_decode_status, tc::kErrDrainTimeout);
+    if (i == 0) tc::bulk_wait_all();
+    return;
   }
-  const float o = reduce_scatter32(part, lane);  // row 32 warp + lane
-  st((TIO *)a.out, (size_t)u * D + 32 * warp + lane, o);
-  if (!isfinite(o)) atomicOr(&g_decode_status, tc_err_nonfinite());
+  {
+    const float vi = vvec[i];
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int b = 0; b < 4; b++) {
+#pragma unroll
+      for (int c = 0; c < 8; c++) {
+        float4 *gp = reinterpret_cast<float4 *>(sm + b * kDecSlab + i * 128 + ((c ^ (i & 7)) << 4));
+        float4 gv = *gp;
+        const float4 kc = reinterpret_cast<const float4 *>(kvec)[8 * b + c];
+        const float4 xc = reinterpret_cast<const float4 *>(b0)[8 * b + c];
+        gv.x = fmaf(g, gv.x, vi * kc.x);
+        gv.y = fmaf(g, gv.y, vi * kc.y);
+        gv.z = fmaf(g, gv.z, vi * kc.z);
+        gv.w = fmaf(g, gv.w, vi * kc.w);
+        *gp = gv;
+        acc[c & 3] = fmaf(gv.w, xc.w, fmaf(gv.z, xc.z, fmaf(gv.y, xc.y, fmaf(gv.x, xc.x, acc[c & 3]))));
+      }
+    }
+    const float o = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    tc::fence_smem_to_async();
+    __syncthreads();
+    if (i == 0) {  // the updated G goes out
+#pragma unroll
+      for (int b = 0; b < 4; b++) tc::tensor_s2g_2d(&mapG, tc::smem_u32(sm + b * kDecSlab), 32 * b, y0);
+      tc::bulk_commit();
+    }
+    st((TIO *)a.out, (size_t)u * D + i, o);
+    if (!isfinite(o)) atomicOr(&g_decode_status, tc_err_nonfinite());
+  }
   if (a.Xs) a.Xs[(size_t)u * D + i] = xr;
   if (i == 0 && a.iters) a.iters[u] = it;
-  if (i == 0) tc::bulk_wait_all();  // the H stores complete before the block ends
+  if (i == 0) tc::bulk_wait_all();  // the H and G stores complete before the block ends
 }
 
 // (Measured alternatives, 256 x 16 decode workload: an earlier kernel with 256 threads per
@@ -394,14 +393,16 @@ __global__ void __launch_bounds__(kDec128Threads, 3)
 template <int D, typename TIO>
 static int launch_dec_t(const DecArgs &a, cudaStream_t st) {
   if constexpr (D == 128) {
-    CUtensorMap mapH{};
-    if (!tmap_rows128_f32(&mapH, a.Hs, (size_t)a.N * a.H * 128)) return -1;
+    CUtensorMap mapH{}, mapG{};
+    if (!tmap_rows128_f32(&mapH, a.Hs, (size_t)a.N * a.H * 128) ||
+        !tmap_rows128_f32(&mapG, a.Gs, (size_t)a.N * a.H * 128))
+      return -1;
     auto kfn = mesa_decode128_kernel<TIO>;
     if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDecode128Smem) !=
         cudaSuccess)
       return -1;
     timing_mark_begin(K_DECODE, st);
-    kfn<<<a.N * a.H, kDec128Threads, kDecode128Smem, st>>>(a, mapH);
+    kfn<<<a.N * a.H, kDec128Threads, kDecode128Smem, st>>>(a, mapH, mapG);
   } else {
     timing_mark_begin(K_DECODE, st);
     mesa_decode_kernel<D, TIO><<<a.N * a.H, 4 * D, 0, st>>>(a);
