@@ -336,7 +336,8 @@ int mesa_tc_selftest(const float *A, const float *B, float *C1, float *C2, float
 int mesa_timing_begin(int max_launches);
 int mesa_timing_end(double *ms_per_kind, int *launches_per_kind, int nkinds);
 
-/* Name of a kernel kind used by the timing calls, or NULL past the last kind. */
+/* Name of a kernel kind used by the timing calls, or NULL past the last kind ("a|b": the
+ * kind is kernel a or kernel b, chosen by the head size). */
 const char *mesa_kernel_name(int kind);
 
 #ifdef __cplusplus

@@ -561,6 +561,7 @@ int launch_bwd_t(const BwdArgs &a, const FwdWorkspace &ws, int phase, cudaStream
   const int U = a.B * a.H, NC = (a.T + BC - 1) / BC;
   constexpr int SPD = D + 4, SPC = BC + 1;
   if (phase == 2) {  // the forward's chunk states (ws.ell must hold the log-decays)
+    if (D == 128) return launch_sweep_tc(a, ws, false, st);
     timing_mark_begin(K_BWD_FSTATES, st);
     mesa_state_sweep_kernel<D, TIO, false><<<dim3(2, U), 256, 0, st>>>(a, ws, NC);
     timing_mark_end(K_BWD_FSTATES, st);
@@ -573,9 +574,13 @@ int launch_bwd_t(const BwdArgs &a, const FwdWorkspace &ws, int phase, cudaStream
     k<<<dim3(NC, U), 2 * D, smem, st>>>(a, ws, NC);
     timing_mark_end(K_BWD_RHS, st);
   } else {
-    timing_mark_begin(K_BWD_STATES, st);
-    mesa_state_sweep_kernel<D, TIO, true><<<dim3(2, U), 256, 0, st>>>(a, ws, NC);
-    timing_mark_end(K_BWD_STATES, st);
+    if (D == 128) {
+      if (launch_sweep_tc(a, ws, true, st) != 0) return -1;
+    } else {
+      timing_mark_begin(K_BWD_STATES, st);
+      mesa_state_sweep_kernel<D, TIO, true><<<dim3(2, U), 256, 0, st>>>(a, ws, NC);
+      timing_mark_end(K_BWD_STATES, st);
+    }
     const size_t smem = sizeof(float) * (6 * BC * SPD + D * SPD + 4 * BC * SPC + BC * (D / 4 + 1) +
                                          4 * BC + 2 * D);
     auto k = mesa_bwd_grad_kernel<D, TIO>;

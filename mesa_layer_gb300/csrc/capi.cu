@@ -199,8 +199,8 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_CG_ROWS: return "mesa_cg_rows_kernel";
     case mesa::K_PREPROC: return "mesa_qk_preprocess_kernel";
     case mesa::K_BWD_RHS: return "mesa_bwd_rhs_kernel";
-    case mesa::K_BWD_STATES: return "mesa_state_sweep_kernel<adjoints>";
-    case mesa::K_BWD_FSTATES: return "mesa_state_sweep_kernel<states>";
+    case mesa::K_BWD_STATES: return "mesa_sweep_tc_kernel|mesa_state_sweep_kernel<adjoints>";
+    case mesa::K_BWD_FSTATES: return "mesa_sweep_tc_kernel|mesa_state_sweep_kernel<states>";
     case mesa::K_BWD_GRAD: return "mesa_bwd_grad_kernel+mesa_bwd_lambda_kernel";
     case mesa::K_CG_TC64: return "mesa_cg_tc64_kernel";
     case mesa::K_CARRY_TC: return "mesa_carry_tc_kernel";
@@ -392,7 +392,7 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
                         nullptr, nullptr, 1};
   mesa::BwdArgs ba{B, H, T, dk, dv, dtype, k, v, dout, gamma, X, Y, Bv,
                    (float *)(w + off[11]), (float *)(w + off[12]), (float *)(w + off[13]),
-                   dq, dk_out, dv_out, dgamma, dlambda};
+                   dq, dk_out, dv_out, dgamma, dlambda, status, mesa::wait_limit()};
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
   if (mesa::launch_ell(a, ws, stream) != 0 || mesa::launch_bwd_states(ba, ws, stream) != 0)
     return MESA_ERR_CUDA;

@@ -73,6 +73,8 @@ struct BwdArgs {
   float *dlam_part;                  // [U, NC, dk]
   void *dq_out, *dk_out, *dv_out;    // dtype
   float *dgamma, *dlambda;           // [U, T], [H, dk]
+  unsigned *status = nullptr;        // device status word (the tensor-core sweeps' bounded waits)
+  unsigned wait_limit = 0;           // polls of those waits
 };
 
 // Query/key preprocessing (causal depthwise convolution + L2 normalisation).
@@ -126,6 +128,9 @@ int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status,
 // 32 columns x 128 rows and the 128-byte swizzle; false if the driver offers no encoder or
 // it rejects the map.
 bool tmap_rows128_f32(CUtensorMap *map, float *base, size_t rows);
+// The backward pass's 32-token chunk states (bwd = false) or state adjoints (bwd = true) on
+// the tensor cores, d = 128 (sweep_tc.cu).
+int launch_sweep_tc(const BwdArgs &a, const FwdWorkspace &ws, bool bwd, cudaStream_t st);
 int launch_decode(const DecArgs &a, cudaStream_t st);
 // Backward pass: the right-hand sides of the second solve (needs ws's chunk-kBwdChunk states
 // and log-decays), then the state adjoints and every gradient.
