@@ -56,6 +56,14 @@ constexpr uint32_t OFF_SHI = 0, OFF_SLO = MAT_BYTES, OFF_K = 2 * MAT_BYTES,
 constexpr uint32_t MISC_BYTES = 2048;
 constexpr uint32_t SMEM_TC = OFF_MISC + MISC_BYTES + 1024;  // + alignment slack
 constexpr uint32_t COL_U = 0, COL_W = 128, COL_PH = 256, COL_PL = 320, COL_R = 384;
+// The A operand of the key and state products (p, at the readout x) is staged as
+// v * kPScale / m with m >= ||v||_2 a power of two, so its row has Euclidean norm at most
+// kPScale: every product with the key tile (entries at most 1 in magnitude, so rows of norm
+// at most sqrt(DH)) then stays below kPScale * sqrt(DH) = 2^12.5, eight times below the
+// largest finite fp16 value, and Z = W o D (D <= 1) can be staged without finding its row
+// maximum.  The factor keeps the largest entries of a row far above fp16's smallest normal
+// numbers, so that their lo terms keep their full 11 bits.
+constexpr float kPScale = 512.0f;
 
 // Byte offset of x[i][c .. c+3] (c a multiple of 4): row i is 512 bytes, its 16-byte chunks
 // permuted by chunk ^ (i % 8), so that a warp reading the same columns of 32 rows is spread
@@ -236,50 +244,23 @@ __global__ void __launch_bounds__(512, 1)
     return reinterpret_cast<float *>((n ? Zlo : Zhi) + scr_row + ((g ^ (i & 7)) << 4)) + 2 * slot *
            (((lane >> 3) & 2) ? -1 : 1);
   };
-  auto rowred = [&](float val, bool mx) -> float {
+  auto rowsum = [&](float val) -> float {
     *scr(0, grp) = val;
     quad_bar<NG>(qd);
     float r = *scr(0, 0);
 #pragma unroll
-    for (int g = 1; g < NG; g++) r = mx ? fmaxf(r, *scr(0, g)) : r + *scr(0, g);
+    for (int g = 1; g < NG; g++) r += *scr(0, g);
     quad_bar<NG>(qd);
     return r;
-  };
-  auto rowred2 = [&](float &sum, float &mx) {  // a sum and a max sharing the barriers
-    *scr(0, grp) = sum;
-    *scr(1, grp) = mx;
-    quad_bar<NG>(qd);
-    float s_ = *scr(0, 0), m_ = *scr(1, 0);
-#pragma unroll
-    for (int g = 1; g < NG; g++) {
-      s_ += *scr(0, g);
-      m_ = fmaxf(m_, *scr(1, g));
-    }
-    sum = s_;
-    mx = m_;
-    quad_bar<NG>(qd);
   };
   // the CG step's reductions after the Y product (one barrier each, see above)
-  auto step_sum = [&](float val) -> float {
-    *scr(0, grp, 1) = val;
+  auto step_sum = [&](float val, int slot) -> float {
+    *scr(0, grp, slot) = val;
     quad_bar<NG>(qd);
-    float r = *scr(0, 0, 1);
+    float r = *scr(0, 0, slot);
 #pragma unroll
-    for (int g = 1; g < NG; g++) r += *scr(0, g, 1);
+    for (int g = 1; g < NG; g++) r += *scr(0, g, slot);
     return r;
-  };
-  auto step_sum_max = [&](float &sum, float &mx) {
-    *scr(0, grp) = sum;
-    *scr(1, grp) = mx;
-    quad_bar<NG>(qd);
-    float s_ = *scr(0, 0), m_ = *scr(1, 0);
-#pragma unroll
-    for (int g = 1; g < NG; g++) {
-      s_ += *scr(0, g);
-      m_ = fmaxf(m_, *scr(1, g));
-    }
-    sum = s_;
-    mx = m_;
   };
 
   // ---- set-up: tensor memory, barriers, per-chunk constants --------------------------
@@ -439,7 +420,9 @@ __global__ void __launch_bounds__(512, 1)
 
   // CG start: x = 0, r = p = q_i (this thread's CW columns).  p lives in tensor memory as
   // the scaled hi + lo MMA operand; each iteration reads it back once into registers.
-  float rho, nq, mP;
+  // pn2: ||p||^2 by the recurrence ||p_new||^2 = ||r_new||^2 + beta^2 ||p||^2 (r_new is
+  // orthogonal to p), from which the power-of-two scale mP >= ||p|| of the staged p follows
+  float rho, nq, mP, pn2;
   {
     float p[CW];
     if (SOLVE && sv.rhs) {  // fp32 right-hand sides
@@ -460,21 +443,18 @@ __global__ void __launch_bounds__(512, 1)
         for (int kk = 0; kk < 8; kk++) p[g * 8 + kk] = __bfloat162float(b[kk]);
       }
     }
-    float s = 0.0f, mx = 0.0f;
+    float s = 0.0f;
 #pragma unroll
-    for (int d = 0; d < CW; d++) {
-      s = fmaf(p[d], p[d], s);
-      mx = fmaxf(mx, fabsf(p[d]));
-    }
-    rowred2(s, mx);
-    rho = s;
+    for (int d = 0; d < CW; d++) s = fmaf(p[d], p[d], s);
+    rho = rowsum(s);
     nq = sqrtf(rho);
-    mP = tc::pow2_ceil(mx);
+    pn2 = rho;
+    mP = tc::pow2_ceil(nq);
 #pragma unroll
     for (int g4 = 0; g4 < CW / 4; g4++)
       *reinterpret_cast<float4 *>(Xs + x_offset(i, c0 + 4 * g4)) = make_float4(0, 0, 0, 0);
     tc::tmem_st<CW>(tl + COL_R, p);
-    const float inv = 1.0f / mP;
+    const float inv = kPScale / mP;
     stage16_p<NTERMS>(tph, tpl, p, inv);
     stage16_p<NTERMS>(tph + 8, tpl + 8, p + 16, inv);
     tc::tmem_st_wait();
@@ -575,19 +555,14 @@ __global__ void __launch_bounds__(512, 1)
     if (bad && tid == 0) atomicOr(status, tc::kErrMmaTimeout);
     return !bad;
   };
-  // Z = (W mrow / sK) o D into the Z operand (warps above the diagonal keep their zeros);
-  // returns the row scale.  The column factor 2^{-l2_j} multiplies W here, the row factor
-  // goes into the scale.  okW false (this warp's wait for W gave up): W is not read (the
-  // multiply may still be writing it) and the row reductions still run, so that the
-  // quadrant's barriers are met; the block then gives up at the next barrier.
+  // Z = W o D into the Z operand (warps above the diagonal keep their zeros); returns the
+  // scale zs with (P K^T) o D = zs Z for the staged rows of scale mrow.  The column factor
+  // 2^{-l2_j} multiplies W first, the row factor 2^{l2_i} follows.  okW false (this warp's
+  // wait for W gave up): W is not read (the multiply may still be writing it); the block
+  // gives up at the next barrier.
   auto build_z = [&](float mrow, bool okW) -> float {
-    const float f = mrow / sK;
-    const float rowf = factored ? f * e2r_i : f;
-    float w[CW];
-#pragma unroll
-    for (int kk = 0; kk < CW; kk++) w[kk] = 0.0f;
-    float zmax = 0.0f;
     if (!z_upper && okW) {
+      float w[CW];
       if (factored) {
         const bool diag = grp == qd;  // the only block that straddles the diagonal
 #pragma unroll
@@ -604,7 +579,6 @@ __global__ void __launch_bounds__(512, 1)
               const int j = c0 + 16 * h + 4 * g + kk;
               const float z = wh[4 * g + kk] * e4[kk];
               w[16 * h + 4 * g + kk] = (!diag || j <= i) ? z : 0.0f;
-              zmax = fmaxf(zmax, fabsf(w[16 * h + 4 * g + kk]));
             }
           }
         }
@@ -614,15 +588,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int kk = 0; kk < CW; kk++) {
           const int j = c0 + kk;
-          const float dij = (valid && j <= i) ? exp2f(ell2_i - m->ell2[j]) : 0.0f;
-          w[kk] *= dij;
-          zmax = fmaxf(zmax, fabsf(w[kk]));
+          w[kk] *= (valid && j <= i) ? exp2f(ell2_i - m->ell2[j]) : 0.0f;
         }
       }
-    }
-    const float zs = tc::pow2_ceil(rowred(zmax * rowf, true));
-    if (!z_upper && okW) {
-      const float inv = rowf / zs;
+      const float inv = factored ? e2r_i : 1.0f;
 #pragma unroll
       for (int g = 0; g < NV; g++) {
         float x8[8];
@@ -631,7 +600,7 @@ __global__ void __launch_bounds__(512, 1)
         st8<KT>(Zhi, Zlo, i, c0 + 8 * g, x8, inv);
       }
     }
-    return zs;
+    return mrow / (kPScale * sK);
   };
 
   bool act = valid;
@@ -676,17 +645,17 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (tid == 0) issue_Y();
     // p back from its operand copy while Y = Z K and U = P S run
-    load16_p<NTERMS>(tph, tpl, mP, p);
-    load16_p<NTERMS>(tph + 8, tpl + 8, mP, p + 16);
+    load16_p<NTERMS>(tph, tpl, mP / kPScale, p);
+    load16_p<NTERMS>(tph + 8, tpl + 8, mP / kPScale, p + 16);
     if (!wait_YU()) {
       failed = true;
       break;
     }
 
-    // AP = e^l (mP/sS) U + (zs/sK) Y + lambda p, written over U (whose columns are free
+    // AP = e^l (mP/(kPScale sS)) U + (zs/sK) Y + lambda p, written over U (whose columns are free
     // until the next iteration's U = P S); sigma = p.AP.  The CG vectors move through
     // tensor memory 16 columns at a time so that only p is held in registers.
-    const float fu = e2r_i * mP / sS, fy = zs / sK;
+    const float fu = e2r_i * mP / (kPScale * sS), fy = zs / sK;
     float sg = 0.0f;
 #pragma unroll
     for (int h = 0; h < CW / 16; h++) {
@@ -708,11 +677,11 @@ __global__ void __launch_bounds__(512, 1)
       tc::tmem_st16(tl + COL_U + 16 * h, uu);
     }
     tc::tmem_st_wait();
-    const float sigma = step_sum(sg);
+    const float sigma = step_sum(sg, 1);
     const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
     // r -= alpha AP   (alpha = 0 leaves a finished row unchanged; the tensor-memory
     // accesses stay unconditional: they are warp-collective)
-    float rn = 0.0f, rmax = 0.0f;
+    float rn = 0.0f;
 #pragma unroll
     for (int h = 0; h < CW / 16; h++) {
       float rr[16], aa[16];
@@ -723,21 +692,20 @@ __global__ void __launch_bounds__(512, 1)
       for (int kk = 0; kk < 16; kk++) {
         rr[kk] = fmaf(-alpha, aa[kk], rr[kk]);
         rn = fmaf(rr[kk], rr[kk], rn);
-        rmax = fmaxf(rmax, fabsf(rr[kk]));
       }
       tc::tmem_st16(tl + COL_R + 16 * h, rr);
     }
     tc::tmem_st_wait();
-    step_sum_max(rn, rmax);
+    rn = step_sum(rn, 0);
     const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
-    // for an active row p = r + beta p, staged with the scale
-    // mNew >= max|r| + beta max|p| >= max|p_new|; the old p stays in registers for the
-    // deferred x += alpha p.  A finished row keeps its p (alpha = 0): it is staged again
-    // with its old scale, which gives back the same hi and lo (p was read from them, and
-    // hi + lo and the power-of-two scales are exact in fp32).  The tensor-memory accesses
-    // stay unconditional: they are warp-collective.
-    const float mNew = act ? tc::pow2_ceil(rmax + beta * mP) : mP;
-    const float inv = 1.0f / mNew;
+    // for an active row p = r + beta p, staged with the scale mNew > ||p_new||; the old p
+    // stays in registers for the deferred x += alpha p.  A finished row keeps its p
+    // (alpha = 0): it is staged again with its old scale, which gives back the same hi and
+    // lo (p was read from them, and hi + lo and the power-of-two scales are exact in fp32).
+    // The tensor-memory accesses stay unconditional: they are warp-collective.
+    const float pn2New = fmaf(beta * beta, pn2, rn);
+    const float mNew = act ? tc::pow2_ceil(sqrtf(pn2New)) : mP;
+    const float inv = kPScale / mNew;
 #pragma unroll
     for (int h = 0; h < CW / 16; h++) {
       float rr[16], pv[16];
@@ -750,6 +718,7 @@ __global__ void __launch_bounds__(512, 1)
     tc::tmem_st_wait();
     if (act) {
       mP = mNew;
+      pn2 = pn2New;
       rho = rn;
       cnt++;
     }
@@ -811,11 +780,11 @@ __global__ void __launch_bounds__(512, 1)
           dst[g4] = make_float4(xx[4 * g4], xx[4 * g4 + 1], xx[4 * g4 + 2], xx[4 * g4 + 3]);
       }
     }
-    float mx = 0.0f;
+    float xn = 0.0f;
 #pragma unroll
-    for (int kk = 0; kk < CW; kk++) mx = fmaxf(mx, fabsf(xx[kk]));
-    const float mX = tc::pow2_ceil(rowred(mx, true));
-    const float inv = 1.0f / mX;
+    for (int kk = 0; kk < CW; kk++) xn = fmaf(xx[kk], xx[kk], xn);
+    const float mX = tc::pow2_ceil(sqrtf(rowsum(xn)));
+    const float inv = kPScale / mX;
     // X replaces P as the A operand of W and U
     stage16_p<NTERMS>(tph, tpl, xx, inv);
     stage16_p<NTERMS>(tph + 8, tpl + 8, xx + 16, inv);
@@ -855,7 +824,7 @@ __global__ void __launch_bounds__(512, 1)
       if (tid == 0) issue_Y();
       failed = !wait_YU();
       if (!failed) {
-        const float fu = e2r_i * mX / sG, fy = zs / sV;
+        const float fu = e2r_i * mX / (kPScale * sG), fy = zs / sV;
         float uu[CW], yy[CW];
         tc::tmem_ld<CW>(tl + COL_U, uu);
         tc::tmem_ld<CW>(tl + COL_W, yy);
