@@ -63,7 +63,7 @@ constexpr uint32_t COL_U = 0, COL_W = 128, COL_PH = 256, COL_PL = 320, COL_R = 3
 // largest finite fp16 value, and Z = W o D (D <= 1) can be staged without finding its row
 // maximum.  The factor keeps the largest entries of a row far above fp16's smallest normal
 // numbers, so that their lo terms keep their full 11 bits.
-constexpr float kPScale = 512.0f;
+constexpr float kPScale = 512.0f, kPInv = 1.0f / 512.0f;
 
 // Byte offset of x[i][c .. c+3] (c a multiple of 4): row i is 512 bytes, its 16-byte chunks
 // permuted by chunk ^ (i % 8), so that a warp reading the same columns of 32 rows is spread
@@ -388,14 +388,16 @@ __global__ void __launch_bounds__(512, 1)
   tc::Rows8 kr;
   tc::load_rows_smem(sm + OFF_X, Tv, kr);
   wait_copies(aBarLd2, 0);  // the state
-  float sS, sK;
+  float sS, sK, pS, pK;  // the state's and the keys' scales s and their reciprocals p = 1/s
   {
     tc::Mat32 S;
     tc::load_mat_smem(SHu ? sm + OFF_ZHI : nullptr, CHu ? sm + OFF_SHI : nullptr, cf, S);
     float mS = tc::mat_absmax(S), mK = tc::rows_absmax(kr, nullptr), unused = 0.0f;
     tc::block_max3(mS, mK, unused, m->red);  // (its barrier: every staged copy has been read)
-    sS = 1.0f / tc::pow2_ceil(mS);
-    sK = 1.0f / tc::pow2_ceil(mK);
+    pS = tc::pow2_ceil(mS);
+    pK = tc::pow2_ceil(mK);
+    sS = 1.0f / pS;
+    sK = 1.0f / pK;
     tc::store_mat(S, sS, Shi, NTERMS == 2 ? Slo : nullptr);
     tc::store_rows(kr, nullptr, sK, Ks, nullptr);
   }
@@ -422,7 +424,7 @@ __global__ void __launch_bounds__(512, 1)
   // the scaled hi + lo MMA operand; each iteration reads it back once into registers.
   // pn2: ||p||^2 by the recurrence ||p_new||^2 = ||r_new||^2 + beta^2 ||p||^2 (r_new is
   // orthogonal to p), from which the power-of-two scale mP >= ||p|| of the staged p follows
-  float rho, nq, mP, pn2;
+  float rho, nq, mP, rP, pn2;  // (rP = 1 / mP)
   {
     float p[CW];
     if (SOLVE && sv.rhs) {  // fp32 right-hand sides
@@ -449,12 +451,12 @@ __global__ void __launch_bounds__(512, 1)
     rho = rowsum(s);
     nq = sqrtf(rho);
     pn2 = rho;
-    mP = tc::pow2_ceil(nq);
+    mP = tc::pow2_above_sqrt(rho, rP);
 #pragma unroll
     for (int g4 = 0; g4 < CW / 4; g4++)
       *reinterpret_cast<float4 *>(Xs + x_offset(i, c0 + 4 * g4)) = make_float4(0, 0, 0, 0);
     tc::tmem_st<CW>(tl + COL_R, p);
-    const float inv = kPScale / mP;
+    const float inv = kPScale * rP;
     stage16_p<NTERMS>(tph, tpl, p, inv);
     stage16_p<NTERMS>(tph + 8, tpl + 8, p + 16, inv);
     tc::tmem_st_wait();
@@ -600,7 +602,7 @@ __global__ void __launch_bounds__(512, 1)
         st8<KT>(Zhi, Zlo, i, c0 + 8 * g, x8, inv);
       }
     }
-    return mrow / (kPScale * sK);
+    return mrow * kPInv * pK;
   };
 
   bool act = valid;
@@ -645,17 +647,17 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (tid == 0) issue_Y();
     // p back from its operand copy while Y = Z K and U = P S run
-    load16_p<NTERMS>(tph, tpl, mP / kPScale, p);
-    load16_p<NTERMS>(tph + 8, tpl + 8, mP / kPScale, p + 16);
+    load16_p<NTERMS>(tph, tpl, mP * kPInv, p);
+    load16_p<NTERMS>(tph + 8, tpl + 8, mP * kPInv, p + 16);
     if (!wait_YU()) {
       failed = true;
       break;
     }
 
-    // AP = e^l (mP/(kPScale sS)) U + (zs/sK) Y + lambda p, written over U (whose columns are free
+    // AP = e^l (mP pS / kPScale) U + zs pK Y + lambda p, written over U (whose columns are free
     // until the next iteration's U = P S); sigma = p.AP.  The CG vectors move through
     // tensor memory 16 columns at a time so that only p is held in registers.
-    const float fu = e2r_i * mP / (kPScale * sS), fy = zs / sK;
+    const float fu = e2r_i * mP * kPInv * pS, fy = zs * pK;
     float sg = 0.0f;
 #pragma unroll
     for (int h = 0; h < CW / 16; h++) {
@@ -704,8 +706,11 @@ __global__ void __launch_bounds__(512, 1)
     // lo (p was read from them, and hi + lo and the power-of-two scales are exact in fp32).
     // The tensor-memory accesses stay unconditional: they are warp-collective.
     const float pn2New = fmaf(beta * beta, pn2, rn);
-    const float mNew = act ? tc::pow2_ceil(sqrtf(pn2New)) : mP;
-    const float inv = kPScale / mNew;
+    float rNew;
+    const float mNew0 = tc::pow2_above_sqrt(pn2New, rNew);
+    const float mNew = act ? mNew0 : mP;
+    rNew = act ? rNew : rP;
+    const float inv = kPScale * rNew;
 #pragma unroll
     for (int h = 0; h < CW / 16; h++) {
       float rr[16], pv[16];
@@ -718,6 +723,7 @@ __global__ void __launch_bounds__(512, 1)
     tc::tmem_st_wait();
     if (act) {
       mP = mNew;
+      rP = rNew;
       pn2 = pn2New;
       rho = rn;
       cnt++;
@@ -783,13 +789,14 @@ __global__ void __launch_bounds__(512, 1)
     float xn = 0.0f;
 #pragma unroll
     for (int kk = 0; kk < CW; kk++) xn = fmaf(xx[kk], xx[kk], xn);
-    const float mX = tc::pow2_ceil(sqrtf(rowsum(xn)));
-    const float inv = kPScale / mX;
+    float rX;
+    const float mX = tc::pow2_above_sqrt(rowsum(xn), rX);
+    const float inv = kPScale * rX;
     // X replaces P as the A operand of W and U
     stage16_p<NTERMS>(tph, tpl, xx, inv);
     stage16_p<NTERMS>(tph + 8, tpl + 8, xx + 16, inv);
     tc::tmem_st_wait();
-    float sG, sV;
+    float sG, pG, pV;
     tc::Rows8 vr;
     tc::load_rows(v + tokbase * DH, Tv, vr);
     if (gbytes) wait_copies(aBarLd, phLd);  // (a give-up skips the readout)
@@ -799,8 +806,9 @@ __global__ void __launch_bounds__(512, 1)
       tc::load_mat_smem(SG ? sm + OFF_X : nullptr, CG ? sm + OFF_SHI : nullptr, cf, G);
       float mG = tc::mat_absmax(G), mV = tc::rows_absmax(vr, nullptr), unused = 0.0f;
       tc::block_max3(mG, mV, unused, m->red);  // (its barrier: the staged copies have been read)
-      sG = 1.0f / tc::pow2_ceil(mG);
-      sV = 1.0f / tc::pow2_ceil(mV);
+      pG = tc::pow2_ceil(mG);
+      pV = tc::pow2_ceil(mV);
+      sG = 1.0f / pG;
       tc::store_mat(G, sG, Shi, NTERMS == 2 ? Slo : nullptr);
     }
     tc::fence_smem_to_async();
@@ -816,7 +824,7 @@ __global__ void __launch_bounds__(512, 1)
     // below, so V may only replace K after it
     failed = !sync_Z(okW);
     if (!failed) {
-      tc::store_rows(vr, nullptr, sV, Ks, nullptr);
+      tc::store_rows(vr, nullptr, 1.0f / pV, Ks, nullptr);
       tc::fence_smem_to_async();
       tc::fence_before_sync();
       __syncthreads();
@@ -824,7 +832,7 @@ __global__ void __launch_bounds__(512, 1)
       if (tid == 0) issue_Y();
       failed = !wait_YU();
       if (!failed) {
-        const float fu = e2r_i * mX / (kPScale * sG), fy = zs / sV;
+        const float fu = e2r_i * mX * kPInv * pG, fy = zs * pV;
         float uu[CW], yy[CW];
         tc::tmem_ld<CW>(tl + COL_U, uu);
         tc::tmem_ld<CW>(tl + COL_W, yy);

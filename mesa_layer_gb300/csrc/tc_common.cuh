@@ -309,6 +309,15 @@ __device__ __forceinline__ float pow2_ceil(float max_abs) {
   return ldexpf(1.0f, e);
 }
 
+// A power of two 2^k with sqrt(x) < 2^k <= 2 sqrt(x), and its reciprocal, from the exponent
+// bits of x alone (1 and 1 for x zero, subnormal, negative or not finite).
+__device__ __forceinline__ float pow2_above_sqrt(float x, float &rcp) {
+  const int e = (int)((__float_as_uint(x) >> 23) & 0xffu) - 127;  // x = 1.f * 2^e
+  const int k = (x > 0.0f && e > -127 && e < 128) ? (e + 2) >> 1 : 0;  // 4^k >= 2^(e+1) > x
+  rcp = __uint_as_float((uint32_t)(127 - k) << 23);
+  return __uint_as_float((uint32_t)(127 + k) << 23);
+}
+
 // x (already scaled into [-1, 1]) = hi + lo with fp16 hi and lo; |x - hi - lo| <= 2^-22 |x|
 // for |x| >= 2^-14 (the normal range of fp16), absolute error <= 2^-25 below.
 __device__ __forceinline__ void split_f16(float x, __half &hi, __half &lo) {
