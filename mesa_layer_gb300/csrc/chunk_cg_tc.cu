@@ -8,7 +8,8 @@
 //     (H + Lambda) P = diag(e^l) P S^H_{c-1} + ((P K^T) o D) K + P diag(lambda)
 //     O              = diag(e^l) X (S^G_{c-1})^T + ((X K^T) o D) V
 // Each product is a 128x128x128 MMA.  Operands are staged in shared memory as fp16 with a
-// power-of-two scale per row (P, X, Z) or per matrix (S, K, V) and split into two fp16
+// power-of-two scale per row (P and X from the row's Euclidean norm, Z from P's) or per
+// matrix (S, K, V) and split into two fp16
 // terms (hi + lo, ~22 significant bits); products take hi*hi + hi*lo + lo*hi (the state)
 // or hi*K + lo*K (K and V are bf16 inputs, exact in fp16 after scaling).  Accumulation is
 // fp32.  The CG scalars and the x, r vectors stay fp32 (r in tensor memory, x in shared

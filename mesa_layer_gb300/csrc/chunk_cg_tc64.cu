@@ -9,9 +9,9 @@
 //     O              = diag(e^l) X (S^G_{c-1})^T + ((X K^T) o D) V
 // The same algebra and step structure as the bf16 d = 128 kernel (chunk_cg_tc.cu), for fp32
 // inputs: every operand -- P, X, Z, the states and also the keys and values, which fp16 does
-// not hold exactly -- is staged as fp16 with a power-of-two scale per row (P, X, Z) or per
-// matrix (S, K, V) and split into hi + lo terms (~22 significant bits); each product takes
-// hi*hi + hi*lo + lo*hi, accumulated in fp32.  The chunk states come from the CUDA-core state
+// not hold exactly -- is staged as fp16 with a power-of-two scale per row (P and X from the
+// row's Euclidean norm, Z from P's) or per matrix (S, K, V) and split into hi + lo terms
+// (~22 significant bits); each product takes hi*hi + hi*lo + lo*hi, accumulated in fp32.  The chunk states come from the CUDA-core state
 // kernels at 128-token chunks (no segments).
 //
 // Operand tiles arrive by bulk copies (the tensor memory accelerator, untiled): the chunk's
@@ -48,6 +48,12 @@ constexpr uint32_t O_SHI = 0, O_SLO = S64_BYTES, O_KHI = 2 * S64_BYTES, O_KLO = 
 constexpr uint32_t MISC64_BYTES = 2048;
 constexpr uint32_t SMEM_TC64 = O_MISC + MISC64_BYTES + 1024;  // + alignment slack
 constexpr uint32_t C_U = 0, C_W = 64, C_PH = 192, C_PL = 224, C_R = 256, C_X = 320;
+// The A operand of the key and state products (p, at the readout x) is staged as
+// v * kPScale / m with m >= ||v||_2 a power of two: its rows have Euclidean norm at most
+// kPScale, every product with the keys (entries at most 1 in magnitude, rows of norm at most
+// sqrt(64)) stays below 8 kPScale = 2^12, eight times below the largest finite fp16 value,
+// and Z = W o D (D <= 1) is staged with that fixed scale, with no row maximum to find.
+constexpr float kPScale = 512.0f, kPInv = 1.0f / 512.0f;
 
 struct Misc64 {
   float ell2[T64];  // log2-decays l_i * log2(e)
@@ -186,50 +192,24 @@ __global__ void __launch_bounds__(512, 1)
     return reinterpret_cast<float *>((n ? Zlo : Zhi) + scr_row + ((g ^ (i & 7)) << 4)) + 2 * slot *
            (((lane >> 3) & 2) ? -1 : 1);
   };
-  auto rowred = [&](float val, bool mx) -> float {
+  auto rowsum = [&](float val) -> float {
     *scr(0, grp) = val;
     quad_bar64<NG>(qd);
     float r = *scr(0, 0);
 #pragma unroll
-    for (int g = 1; g < NG; g++) r = mx ? fmaxf(r, *scr(0, g)) : r + *scr(0, g);
+    for (int g = 1; g < NG; g++) r += *scr(0, g);
     quad_bar64<NG>(qd);
     return r;
   };
-  auto rowred2 = [&](float &sum, float &mx) {
-    *scr(0, grp) = sum;
-    *scr(1, grp) = mx;
+  // the CG step's reductions after the Y product: one barrier each, sigma in slot 1 and the
+  // residual in slot 0 (see the d = 128 kernel)
+  auto step_sum = [&](float val, int slot) -> float {
+    *scr(0, grp, slot) = val;
     quad_bar64<NG>(qd);
-    float s_ = *scr(0, 0), m_ = *scr(1, 0);
+    float r = *scr(0, 0, slot);
 #pragma unroll
-    for (int g = 1; g < NG; g++) {
-      s_ += *scr(0, g);
-      m_ = fmaxf(m_, *scr(1, g));
-    }
-    sum = s_;
-    mx = m_;
-    quad_bar64<NG>(qd);
-  };
-  // the CG step's reductions after the Y product: one barrier each (see the d = 128 kernel)
-  auto step_sum = [&](float val) -> float {
-    *scr(0, grp, 1) = val;
-    quad_bar64<NG>(qd);
-    float r = *scr(0, 0, 1);
-#pragma unroll
-    for (int g = 1; g < NG; g++) r += *scr(0, g, 1);
+    for (int g = 1; g < NG; g++) r += *scr(0, g, slot);
     return r;
-  };
-  auto step_sum_max = [&](float &sum, float &mx) {
-    *scr(0, grp) = sum;
-    *scr(1, grp) = mx;
-    quad_bar64<NG>(qd);
-    float s_ = *scr(0, 0), m_ = *scr(1, 0);
-#pragma unroll
-    for (int g = 1; g < NG; g++) {
-      s_ += *scr(0, g);
-      m_ = fmaxf(m_, *scr(1, g));
-    }
-    sum = s_;
-    mx = m_;
   };
 
   // ---- set-up --------------------------------------------------------------------------
@@ -296,9 +276,9 @@ __global__ void __launch_bounds__(512, 1)
   Raw8<1> sr;
   float mS = raw_load(SH ? sm + O_RAWS : nullptr, D64, sr), unused = 0.0f;
   tc::block_max3(mS, mK, unused, m->red);  // (its barrier: every staged copy has been read)
-  const float sS = 1.0f / tc::pow2_ceil(mS), sK = 1.0f / tc::pow2_ceil(mK);
-  raw_store(sr, sS, Shi, Slo, D64);
-  raw_store(kr, sK, Khi, Klo, T64);
+  const float pS = tc::pow2_ceil(mS), pK = tc::pow2_ceil(mK);  // (the scales are 1 / p)
+  raw_store(sr, 1.0f / pS, Shi, Slo, D64);
+  raw_store(kr, 1.0f / pK, Khi, Klo, T64);
   if (z_upper) {
 #pragma unroll
     for (int g = 0; g < KW / 8; g++) {
@@ -317,24 +297,23 @@ __global__ void __launch_bounds__(512, 1)
   const float e2r_i = valid ? exp2f(ell2_i) : 0.0f;  // 2^{l2_i} = e^{l_i}; invalid rows: D = 0
 
   // CG start: x = 0, r = p = q; p lives in tensor memory as the scaled hi + lo operand
-  float rho, nq, mP;
+  // pn2: ||p||^2 by the recurrence ||p_new||^2 = ||r_new||^2 + beta^2 ||p||^2; mP >= ||p||
+  // the staged p's power-of-two scale, rP = 1 / mP
+  float rho, nq, mP, rP, pn2;
   {
-    float s = 0.0f, mx = 0.0f;
+    float s = 0.0f;
 #pragma unroll
-    for (int d = 0; d < CW; d++) {
-      s = fmaf(qv[d], qv[d], s);
-      mx = fmaxf(mx, fabsf(qv[d]));
-    }
-    rowred2(s, mx);
-    rho = s;
+    for (int d = 0; d < CW; d++) s = fmaf(qv[d], qv[d], s);
+    rho = rowsum(s);
     nq = sqrtf(rho);
-    mP = tc::pow2_ceil(mx);
+    pn2 = rho;
+    mP = tc::pow2_above_sqrt(rho, rP);
     float zero[16];
 #pragma unroll
     for (int d = 0; d < 16; d++) zero[d] = 0.0f;
     tc::tmem_st16(tl + C_X + c0, zero);
     tc::tmem_st16(tl + C_R + c0, qv);
-    stage16(tph, tpl, qv, 1.0f / mP);
+    stage16(tph, tpl, qv, kPScale * rP);
     tc::tmem_st_wait();
   }
 
@@ -401,16 +380,12 @@ __global__ void __launch_bounds__(512, 1)
     if (bad && tid == 0) atomicOr(status, tc::kErrMmaTimeout);
     return !bad;
   };
-  // Z = (W mrow / sK) o D into the Z operand (warps above the diagonal keep their zeros);
-  // returns the row scale.  okW false: W is not read, the reductions still run.
+  // Z = W o D into the Z operand (warps above the diagonal keep their zeros); returns the
+  // scale zs with (P K^T) o D = zs Z for the staged rows of scale mrow.  okW false: W is
+  // not read (the block gives up at the next barrier).
   auto build_z = [&](float mrow, bool okW) -> float {
-    const float f = mrow / sK;
-    const float rowf = factored ? f * e2r_i : f;
-    float w[KW];
-#pragma unroll
-    for (int kk = 0; kk < KW; kk++) w[kk] = 0.0f;
-    float zmax = 0.0f;
     if (!z_upper && okW) {
+      float w[KW];
       const bool diag = grp == qd;
 #pragma unroll
       for (int h = 0; h < KW / 16; h++) {
@@ -423,15 +398,10 @@ __global__ void __launch_bounds__(512, 1)
           float z;
           if (factored) z = wh[kk] * m->e2c[j];
           else z = (valid && j <= i) ? wh[kk] * exp2f(ell2_i - m->ell2[j]) : 0.0f;
-          z = (!diag || j <= i) ? z : 0.0f;
-          w[16 * h + kk] = z;
-          zmax = fmaxf(zmax, fabsf(z));
+          w[16 * h + kk] = (!diag || j <= i) ? z : 0.0f;
         }
       }
-    }
-    const float zs = tc::pow2_ceil(rowred(zmax * rowf, true));
-    if (!z_upper && okW) {
-      const float inv = rowf / zs;
+      const float inv = factored ? e2r_i : 1.0f;
 #pragma unroll
       for (int g = 0; g < KW / 8; g++) {
         float x8[8];
@@ -440,7 +410,7 @@ __global__ void __launch_bounds__(512, 1)
         st8_split(Zhi, Zlo, i, k0 + 8 * g, T64, x8, inv);
       }
     }
-    return zs;
+    return mrow * kPInv * pK;
   };
 
   bool act = valid;
@@ -479,13 +449,13 @@ __global__ void __launch_bounds__(512, 1)
       break;
     }
     if (tid == 0) issue_Y();
-    load16(tph, tpl, mP, p);  // p back from its operand copy while Y and U run
+    load16(tph, tpl, mP * kPInv, p);  // p back from its operand copy while Y and U run
     if (!wait_YU()) {
       failed = true;
       break;
     }
-    // AP = e^l (mP/sS) U + (zs/sK) Y + lambda p (in registers); sigma = p.AP
-    const float fu = e2r_i * mP / sS, fy = zs / sK;
+    // AP = e^l (mP pS / kPScale) U + zs pK Y + lambda p (in registers); sigma = p.AP
+    const float fu = e2r_i * mP * kPInv * pS, fy = zs * pK;
     float ap[16];
     float sg = 0.0f;
     {
@@ -499,33 +469,38 @@ __global__ void __launch_bounds__(512, 1)
         sg = fmaf(p[d], ap[d], sg);
       }
     }
-    const float sigma = step_sum(sg);
+    const float sigma = step_sum(sg, 1);
     const float alpha = (act && sigma > 0.0f && rho > 0.0f) ? rho / sigma : 0.0f;
     // r -= alpha AP (alpha = 0 leaves a finished row unchanged)
-    float rr[16], rn = 0.0f, rmax = 0.0f;
+    float rr[16], rn = 0.0f;
     tc::tmem_ld16(tl + C_R + c0, rr);
     tc::tmem_ld_wait();
 #pragma unroll
     for (int d = 0; d < 16; d++) {
       rr[d] = fmaf(-alpha, ap[d], rr[d]);
       rn = fmaf(rr[d], rr[d], rn);
-      rmax = fmaxf(rmax, fabsf(rr[d]));
     }
     tc::tmem_st16(tl + C_R + c0, rr);
-    step_sum_max(rn, rmax);
+    rn = step_sum(rn, 0);
     const float beta = (act && rho > 0.0f) ? rn / rho : 0.0f;
-    // p = r + beta p for an active row, staged with mNew >= max|p_new|; a finished row
-    // stages its p again with its old scale (the same hi and lo bits)
-    const float mNew = act ? tc::pow2_ceil(rmax + beta * mP) : mP;
+    // p = r + beta p for an active row, staged with the scale mNew > ||p_new||; a finished
+    // row stages its p again with its old scale (the same hi and lo bits)
+    const float pn2New = fmaf(beta * beta, pn2, rn);
+    float rNew;
+    const float mNew0 = tc::pow2_above_sqrt(pn2New, rNew);
+    const float mNew = act ? mNew0 : mP;
+    rNew = act ? rNew : rP;
     {
       float pv[16];
 #pragma unroll
       for (int d = 0; d < 16; d++) pv[d] = act ? fmaf(beta, p[d], rr[d]) : p[d];
-      stage16(tph, tpl, pv, 1.0f / mNew);
+      stage16(tph, tpl, pv, kPScale * rNew);
     }
     tc::tmem_st_wait();
     if (act) {
       mP = mNew;
+      rP = rNew;
+      pn2 = pn2New;
       rho = rn;
       cnt++;
     }
@@ -556,11 +531,12 @@ __global__ void __launch_bounds__(512, 1)
         for (int g4 = 0; g4 < 4; g4++) dst[g4] = make_float4(xx[4 * g4], xx[4 * g4 + 1], xx[4 * g4 + 2], xx[4 * g4 + 3]);
       }
     }
-    float mx = 0.0f;
+    float xn = 0.0f;
 #pragma unroll
-    for (int d = 0; d < 16; d++) mx = fmaxf(mx, fabsf(xx[d]));
-    const float mX = tc::pow2_ceil(rowred(mx, true));
-    stage16(tph, tpl, xx, 1.0f / mX);  // X replaces P as the A operand of W and U
+    for (int d = 0; d < 16; d++) xn = fmaf(xx[d], xx[d], xn);
+    float rX;
+    const float mX = tc::pow2_above_sqrt(rowsum(xn), rX);
+    stage16(tph, tpl, xx, kPScale * rX);  // X replaces P as the A operand of W and U
     tc::tmem_st_wait();
     wait_copies(aBarLd, phLd);
     phLd ^= 1;
@@ -569,8 +545,8 @@ __global__ void __launch_bounds__(512, 1)
     float mG = raw_load(SG ? sm + O_RAWS : nullptr, D64, gr);
     float mV = raw_load(sm + O_RAW, Tv, vr), unused2 = 0.0f;
     tc::block_max3(mG, mV, unused2, m->red);
-    const float sG = 1.0f / tc::pow2_ceil(mG), sV = 1.0f / tc::pow2_ceil(mV);
-    raw_store(gr, sG, Shi, Slo, D64);
+    const float pG = tc::pow2_ceil(mG), pV = tc::pow2_ceil(mV);
+    raw_store(gr, 1.0f / pG, Shi, Slo, D64);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -583,7 +559,7 @@ __global__ void __launch_bounds__(512, 1)
     // X K^T is complete once every warp has passed this barrier, so V may replace K
     failed = !sync_Z(okW);
     if (!failed) {
-      raw_store(vr, sV, Khi, Klo, T64);
+      raw_store(vr, 1.0f / pV, Khi, Klo, T64);
       tc::fence_smem_to_async();
       tc::fence_before_sync();
       __syncthreads();
@@ -591,7 +567,7 @@ __global__ void __launch_bounds__(512, 1)
       if (tid == 0) issue_Y();
       failed = !wait_YU();
       if (!failed) {
-        const float fu = e2r_i * mX / sG, fy = zs / sV;
+        const float fu = e2r_i * mX * kPInv * pG, fy = zs * pV;
         float uu[16], yy[16];
         tc::tmem_ld16(tl + C_U + c0, uu);
         tc::tmem_ld16(tl + C_W + c0, yy);
