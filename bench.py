@@ -140,13 +140,26 @@ def state_flops(w) -> float:
     return float(w.B * w.H * w.T) * 4.0 * w.dk * w.dk
 
 
-def bwd_grad_flops(w) -> float:
+def bwd_grad_flops(w, states_apart: bool = False) -> float:
     """The gradient kernel per token-head (32-token chunks, causal halves): the three C x C
     dot-product blocks G V^T, X K^T, Y K^T (3 d (C + 1)), the four intra-chunk products with
     them (4 d (C + 1)) and six d x d products with the chunk states and state adjoints
-    (12 d^2)."""
+    (12 d^2) -- unless those products come from the tensor-core kernel (states_apart)."""
     d, C = w.dk, 32
-    return float(w.B * w.H * w.T) * (12.0 * d * d + 7.0 * d * (C + 1))
+    return float(w.B * w.H * w.T) * ((0.0 if states_apart else 12.0 * d * d) + 7.0 * d * (C + 1))
+
+
+def bwd_sprod_flops(w) -> float:
+    """The tensor-core products of the backward's rows with the chunk states, per token-head:
+    dG k, dG^T v, dH k, dH^T k, S^H x (2 d^2 each)."""
+    return float(w.B * w.H * w.T) * 10.0 * w.dk * w.dk
+
+
+def bwd_sprod_executed_flops(w) -> float:
+    """MMA flops that kernel issues per 32-token chunk: 88 products of 128 x 32 x 16 (the
+    states split hi + lo, x split as well: 16 + 16 + 32 + 24)."""
+    nc = w.B * w.H * ((w.T + 31) // 32)
+    return float(nc) * 88 * 2.0 * 128 * 32 * 16
 
 
 def bwd_rhs_flops(w) -> float:
@@ -790,7 +803,10 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
             flops = cg_flops(w, it) - (0.0 if not w.backward else
                                        float(it.size) * (2.0 * w.dk * w.dk + 2.0 * w.dk * (w.chunk + 1)))
         elif "bwd_grad" in top_name:
-            flops = bwd_grad_flops(w)
+            apart = any(n == "mesa_bwd_sprod_tc_kernel" and kind_n[i] > 0 for i, n in enumerate(names))
+            flops = bwd_grad_flops(w, apart)
+        elif "bwd_sprod" in top_name:
+            flops = bwd_sprod_flops(w)
         elif "bwd_rhs" in top_name:
             flops = bwd_rhs_flops(w)
         else:
@@ -802,7 +818,8 @@ def emit(args, w, res, peaks, cpu, rank, world, torch, dist):
             roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": traffic, "kernel": top_name,
                     "peak_source": f"{peaks['source']} bf16 dense (fp16 kind, same rate)",
-                    "executed_tensor_tflops": tc_executed_flops(w, it, not w.backward) / (avg_ms / 1e3) / 1e12}
+                    "executed_tensor_tflops": (bwd_sprod_executed_flops(w) if "bwd_sprod" in top_name else
+                                               tc_executed_flops(w, it, not w.backward)) / (avg_ms / 1e3) / 1e12}
         else:
             sms = peaks["sm_count"]
             peak = sms * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12

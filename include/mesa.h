@@ -130,8 +130,9 @@ int mesa_forward_chunked(int B, int H, int T, int dk, int dv, int dtype, const v
  *              aligned; its first word is the status word read by mesa_forward_status.
  * q, k, v, dout, dq, dk_out and dv_out must be 16-byte aligned (MESA_ERR_INVALID_ARG).
  * Sizes, errors and stream semantics as mesa_forward_chunked; the work is chunked in
- * 32-token chunks (128 for the tensor-core parts, the two solves and the right-hand sides of
- * the second: bf16, d = 128, 16-byte aligned).
+ * 32-token chunks (128 for the tensor-core solves and the right-hand sides of the second:
+ * bf16, d = 128, 16-byte aligned; there the products of each chunk's rows with its states
+ * also run on the tensor cores, into a part of the workspace sized for every d = 128 call).
  */
 size_t mesa_backward_workspace_size(int B, int H, int T, int dk, int dv);
 int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const void *q,

@@ -32,6 +32,8 @@
 //
 // CUDA-core fp32 kernels.  A CTA of 2D threads works on one chunk (BC = 32 tokens); thread
 // (rg, c4) holds 4 rows (rg + 8m) x 4 columns (4 c4 .. 4 c4 + 3) of every C x D result.
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -274,16 +276,19 @@ __global__ void __launch_bounds__(256, 2) mesa_state_sweep_kernel(BwdArgs a, Fwd
 }
 
 // dq, dk, dv, dgamma and the per-chunk dlambda partials.  grid (NC, U), block 2D.
-template <int D, typename TIO>
+// TCS: the products of the rows with the chunk states come precomputed (a.tprod, a.frob: the
+// tensor-core kernel of bwd_tc.cu) instead of being formed here through shared memory.
+template <int D, typename TIO, bool TCS>
 __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWorkspace ws, int NC) {
   constexpr int SPD = D + 4, SPC = BC + 1, NQ = D / 4;
+  constexpr int STN = TCS ? 0 : D * SPD;  // the state tile St (not needed with TCS)
   const int c = blockIdx.x, u = blockIdx.y, T = a.T;
   const int t0 = c * BC, Cv = min(BC, T - t0);
   const size_t tokbase = (size_t)u * T + t0;
   extern __shared__ __align__(16) float smem[];
   float *Ks = smem, *Vs = Ks + BC * SPD, *Gs = Vs + BC * SPD, *Xs = Gs + BC * SPD;
   float *Ys = Xs + BC * SPD, *Bs = Ys + BC * SPD, *St = Bs + BC * SPD;  // Bs: b_t rows
-  float *M1 = St + D * SPD, *M2 = M1 + BC * SPC, *M3 = M2 + BC * SPC, *Cm = M3 + BC * SPC;
+  float *M1 = St + STN, *M2 = M1 + BC * SPC, *M3 = M2 + BC * SPC, *Cm = M3 + BC * SPC;
   float *part = Cm + BC * SPC;         // [BC][NQ + 1] per-thread partial row sums
   float *el = part + BC * (NQ + 1);    // [BC] l_i
   float *wv = el + BC;                 // [BC] w_j
@@ -339,7 +344,7 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
       }
     }
   };
-  if (ns > 0) fetch(kinds[0]);  // in flight while the tiles load and the intra-chunk parts run
+  if (!TCS && ns > 0) fetch(kinds[0]);  // in flight while the tiles load and the intra-chunk parts run
   load_tile<D>(Ks, (const TIO *)a.k + tokbase * D, Cv);
   load_tile<D>(Vs, (const TIO *)a.v + tokbase * D, Cv);
   load_tile<D>(Gs, (const TIO *)a.dout + tokbase * D, Cv);
@@ -437,7 +442,45 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
 #pragma unroll
       for (int n = 0; n < 4; n++) acc[m][n] = fmaf(wv[rg + 8 * m], t[m][n], acc[m][n]);
   };
-  for (int i = 0; i < ns; i++) {
+  if constexpr (TCS) {
+    // the products from the tensor-core kernel: this thread's rows rg + 8m, columns 4 c4 ..
+    const size_t plane = (size_t)a.B * a.H * T * D;
+    auto load_t = [&](int g) {
+      const float *P = a.tprod + g * plane + tokbase * D + 4 * c4;
+#pragma unroll
+      for (int m = 0; m < 4; m++) {
+        const int r = rg + 8 * m;
+        const float4 v = r < Cv ? *reinterpret_cast<const float4 *>(P + (size_t)r * D) : make_float4(0, 0, 0, 0);
+        t[m][0] = v.x, t[m][1] = v.y, t[m][2] = v.z, t[m][3] = v.w;
+      }
+    };
+    if (!last) {
+      load_t(0);  // (dG k_s)^T
+      add_w(accV);
+      dot_rows(colp, Vs, 1.0f);
+      load_t(1);  // (dG^T v_s)^T
+      add_w(accK);
+      load_t(2);  // ((dH + dH^T) k_s)^T: k_s . dH k_s is half its dot with k_s
+      add_w(accK);
+      dot_rows(colp, Ks, 0.5f);
+    }
+    if (!first) {
+      load_t(3);  // (S^H^T x_t)^T
+      dot_rows(rowp, Ys, -1.0f);
+      zero4x4(t);  // t = M1 K, then row += x_t . (b_t - t_t)
+      mm_acc(t, M1, SPC, 1, rg, Ks, SPD, c4, BC);
+#pragma unroll
+      for (int m = 0; m < 4; m++) {
+        const int r = rg + 8 * m;
+        const float4 x = *reinterpret_cast<const float4 *>(Xs + r * SPD + 4 * c4);
+        const float4 b = *reinterpret_cast<const float4 *>(Bs + r * SPD + 4 * c4);
+        rowq[m] += x.x * (b.x - t[m][0]) + x.y * (b.y - t[m][1]) + x.z * (b.z - t[m][2]) +
+                   x.w * (b.w - t[m][3]);
+      }
+      if (!last && tid == 0) thr = a.frob[(size_t)u * NC + c];  // <dG, S^G> + <dH, S^H>
+    }
+  }
+  for (int i = 0; i < (TCS ? 0 : ns); i++) {
     const int kind = kinds[i];
     __syncthreads();  // every thread is done with the previous contents of St
     if (kind != 3) commit(kind);
@@ -589,9 +632,14 @@ int launch_bwd_t(const BwdArgs &a, const FwdWorkspace &ws, int phase, cudaStream
       mesa_state_sweep_kernel<D, TIO, true><<<dim3(2, U), 256, 0, st>>>(a, ws, NC);
       timing_mark_end(K_BWD_STATES, st);
     }
-    const size_t smem = sizeof(float) * (6 * BC * SPD + D * SPD + 4 * BC * SPC + BC * (D / 4 + 1) +
+    // bf16, d = 128, with room for them in the workspace: the products with the states on
+    // the tensor cores first
+    const bool tcs = D == 128 && std::is_same<TIO, __nv_bfloat16>::value && a.tprod && a.frob;
+    if (tcs && launch_bwd_sprod_tc(a, ws, a.tprod, a.frob, st) != 0)
+      return -1;
+    const size_t smem = sizeof(float) * (6 * BC * SPD + (tcs ? 0 : D * SPD) + 4 * BC * SPC + BC * (D / 4 + 1) +
                                          4 * BC + 2 * D);
-    auto k = mesa_bwd_grad_kernel<D, TIO>;
+    auto k = tcs ? mesa_bwd_grad_kernel<D, TIO, true> : mesa_bwd_grad_kernel<D, TIO, false>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return -1;
     timing_mark_begin(K_BWD_GRAD, st);

@@ -56,9 +56,10 @@ size_t workspace_parts(int B, int H, int T, int dk, int dv, int chunk, size_t *o
 
 // Backward workspace: [status | chunk-32 log-decays | S^H | S^G (chunk 32) | 128-token
 // log-decays | S^H (128) | X | Y | b | S^G (128) | segment log-decays Lc | segment carries |
-// dG adjoints | dH adjoints | dlambda partials].  The 128-token parts serve the tensor-core
-// solves (d = 128) and are empty otherwise.
-constexpr int kBwdParts = 15;
+// dG adjoints | dH adjoints | dlambda partials | products of the rows with the chunk states |
+// their Frobenius pairs].  The 128-token parts serve the tensor-core solves and the last two
+// the tensor-core products (d = 128); they are empty otherwise.
+constexpr int kBwdParts = 17;
 size_t backward_parts(int B, int H, int T, int dk, size_t *off, int nseg_in = -1) {
   const size_t U = (size_t)B * H, C = mesa::kBwdChunk;
   const size_t NC = (T + C - 1) / C, NC128 = (T + 127) / 128;
@@ -73,7 +74,8 @@ size_t backward_parts(int B, int H, int T, int dk, size_t *off, int nseg_in = -1
       vec, vec, vec,                                     // X, Y, b
       st128, big ? U * NC128 * sizeof(float) : 0,        // SG (128), Lc
       U * nseg * 2 * dk * dk * sizeof(float),            // carries
-      st, st, U * NC * dk * sizeof(float)};              // dG, dH, dlambda partials
+      st, st, U * NC * dk * sizeof(float),               // dG, dH, dlambda partials
+      big ? 4 * vec : 0, big ? U * NC * sizeof(float) : 0};  // products, Frobenius pairs
   off[0] = kStatusBytes;
   for (int i = 0; i < kBwdParts - 1; i++) off[i + 1] = off[i] + align256(sizes[i]);
   return off[kBwdParts - 1];
@@ -204,6 +206,7 @@ const char *mesa_kernel_name(int kind) {
     case mesa::K_BWD_GRAD: return "mesa_bwd_grad_kernel+mesa_bwd_lambda_kernel";
     case mesa::K_CG_TC64: return "mesa_cg_tc64_kernel";
     case mesa::K_CARRY_TC: return "mesa_carry_tc_kernel";
+    case mesa::K_BWD_SPROD: return "mesa_bwd_sprod_tc_kernel";
   }
   return nullptr;
 }
@@ -392,7 +395,8 @@ int mesa_backward_chunked(int B, int H, int T, int dk, int dv, int dtype, const 
                         nullptr, nullptr, 1};
   mesa::BwdArgs ba{B, H, T, dk, dv, dtype, k, v, dout, gamma, X, Y, Bv,
                    (float *)(w + off[11]), (float *)(w + off[12]), (float *)(w + off[13]),
-                   dq, dk_out, dv_out, dgamma, dlambda, status, mesa::wait_limit()};
+                   dq, dk_out, dv_out, dgamma, dlambda, status, mesa::wait_limit(),
+                   tc ? (float *)(w + off[14]) : nullptr, tc ? (float *)(w + off[15]) : nullptr};
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), stream) != cudaSuccess) return MESA_ERR_CUDA;
   if (mesa::launch_ell(a, ws, stream) != 0 || mesa::launch_bwd_states(ba, ws, stream) != 0)
     return MESA_ERR_CUDA;

@@ -75,6 +75,8 @@ struct BwdArgs {
   float *dgamma, *dlambda;           // [U, T], [H, dk]
   unsigned *status = nullptr;        // device status word (the tensor-core sweeps' bounded waits)
   unsigned wait_limit = 0;           // polls of those waits
+  float *tprod = nullptr;            // [4][U T][dk] products of the rows with the chunk states
+  float *frob = nullptr;             // [U NC] <dG^c, S^G_{c-1}> + <dH^c, S^H_{c-1}> (with tprod)
 };
 
 // Query/key preprocessing (causal depthwise convolution + L2 normalisation).
@@ -90,7 +92,7 @@ struct PreArgs {
 enum KernelKind {
   K_ELL = 0, K_DELTA = 1, K_SCAN = 2, K_CG_SIMT = 3, K_DECODE = 4, K_CG_TC = 5, K_DELTA_TC = 6, K_CG_ROWS = 7,
   K_PREPROC = 8, K_BWD_RHS = 9, K_BWD_STATES = 10, K_BWD_GRAD = 11, K_BWD_FSTATES = 12,
-  K_CG_TC64 = 13, K_CARRY_TC = 14, K_NUM_KINDS = 15
+  K_CG_TC64 = 13, K_CARRY_TC = 14, K_BWD_SPROD = 15, K_NUM_KINDS = 16
 };
 
 // Record a timing event before / after a launch of `kind` on `st` (no-op unless enabled).
@@ -131,6 +133,9 @@ bool tmap_rows128_f32(CUtensorMap *map, float *base, size_t rows);
 // The backward pass's 32-token chunk states (bwd = false) or state adjoints (bwd = true) on
 // the tensor cores, d = 128 (sweep_tc.cu).
 int launch_sweep_tc(const BwdArgs &a, const FwdWorkspace &ws, bool bwd, cudaStream_t st);
+// The backward's products of the 32-token chunks' rows with their states (bf16, d = 128):
+// tp [4][U T][128] (dG k, dG^T v, (dH + dH^T) k, S^H^T x per token), frob [U NC].
+int launch_bwd_sprod_tc(const BwdArgs &a, const FwdWorkspace &ws, float *tp, float *frob, cudaStream_t st);
 int launch_decode(const DecArgs &a, cudaStream_t st);
 // Backward pass: the right-hand sides of the second solve (needs ws's chunk-kBwdChunk states
 // and log-decays), then the state adjoints and every gradient.
