@@ -277,17 +277,20 @@ __global__ void __launch_bounds__(256, 2) mesa_state_sweep_kernel(BwdArgs a, Fwd
 
 // dq, dk, dv, dgamma and the per-chunk dlambda partials.  grid (NC, U), block 2D.
 // TCS: the products of the rows with the chunk states come precomputed (a.tprod, a.frob: the
-// tensor-core kernel of bwd_tc.cu) instead of being formed here through shared memory.
+// tensor-core kernel of bwd_tc.cu) instead of being formed here through shared memory; the
+// state tile and the b rows (read where used) then stay out of shared memory, and two CTAs
+// share an SM.
 template <int D, typename TIO, bool TCS>
-__global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWorkspace ws, int NC) {
+__global__ void __launch_bounds__(256, TCS ? 2 : 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWorkspace ws, int NC) {
   constexpr int SPD = D + 4, SPC = BC + 1, NQ = D / 4;
   constexpr int STN = TCS ? 0 : D * SPD;  // the state tile St (not needed with TCS)
+  constexpr int BSN = TCS ? 0 : BC * SPD;  // the b rows Bs (TCS: read from global memory)
   const int c = blockIdx.x, u = blockIdx.y, T = a.T;
   const int t0 = c * BC, Cv = min(BC, T - t0);
   const size_t tokbase = (size_t)u * T + t0;
   extern __shared__ __align__(16) float smem[];
   float *Ks = smem, *Vs = Ks + BC * SPD, *Gs = Vs + BC * SPD, *Xs = Gs + BC * SPD;
-  float *Ys = Xs + BC * SPD, *Bs = Ys + BC * SPD, *St = Bs + BC * SPD;  // Bs: b_t rows
+  float *Ys = Xs + BC * SPD, *Bs = Ys + BC * SPD, *St = Bs + BSN;  // Bs: b_t rows
   float *M1 = St + STN, *M2 = M1 + BC * SPC, *M3 = M2 + BC * SPC, *Cm = M3 + BC * SPC;
   float *part = Cm + BC * SPC;         // [BC][NQ + 1] per-thread partial row sums
   float *el = part + BC * (NQ + 1);    // [BC] l_i
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
   load_tile<D>(Gs, (const TIO *)a.dout + tokbase * D, Cv);
   load_tile<D>(Xs, a.X + tokbase * D, Cv);
   load_tile<D>(Ys, a.Y + tokbase * D, Cv);
-  if (!first) load_tile<D>(Bs, a.rhs + tokbase * D, Cv);
+  if (!TCS && !first) load_tile<D>(Bs, a.rhs + tokbase * D, Cv);
   for (int j = tid; j < BC; j += nt) el[j] = j < Cv ? ws.ell[tokbase + j] : 0.0f;
   __syncthreads();
   const float lend = el[Cv - 1];
@@ -473,7 +476,8 @@ __global__ void __launch_bounds__(256, 1) mesa_bwd_grad_kernel(BwdArgs a, FwdWor
       for (int m = 0; m < 4; m++) {
         const int r = rg + 8 * m;
         const float4 x = *reinterpret_cast<const float4 *>(Xs + r * SPD + 4 * c4);
-        const float4 b = *reinterpret_cast<const float4 *>(Bs + r * SPD + 4 * c4);
+        const float4 b = r < Cv ? *reinterpret_cast<const float4 *>(a.rhs + (tokbase + r) * D + 4 * c4)
+                                : make_float4(0, 0, 0, 0);
         rowq[m] += x.x * (b.x - t[m][0]) + x.y * (b.y - t[m][1]) + x.z * (b.z - t[m][2]) +
                    x.w * (b.w - t[m][3]);
       }
@@ -637,8 +641,8 @@ int launch_bwd_t(const BwdArgs &a, const FwdWorkspace &ws, int phase, cudaStream
     const bool tcs = D == 128 && std::is_same<TIO, __nv_bfloat16>::value && a.tprod && a.frob;
     if (tcs && launch_bwd_sprod_tc(a, ws, a.tprod, a.frob, st) != 0)
       return -1;
-    const size_t smem = sizeof(float) * (6 * BC * SPD + (tcs ? 0 : D * SPD) + 4 * BC * SPC + BC * (D / 4 + 1) +
-                                         4 * BC + 2 * D);
+    const size_t smem = sizeof(float) * ((tcs ? 5 : 6) * BC * SPD + (tcs ? 0 : D * SPD) + 4 * BC * SPC +
+                                         BC * (D / 4 + 1) + 4 * BC + 2 * D);
     auto k = tcs ? mesa_bwd_grad_kernel<D, TIO, true> : mesa_bwd_grad_kernel<D, TIO, false>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return -1;
