@@ -12,8 +12,10 @@
 // transposed reads) and the token rows as the B operand: states split into fp16 hi + lo with a
 // power-of-two scale per matrix, bf16 keys and values exact in fp16 after one, x split, fp32
 // accumulation in tensor memory (four 32-column accumulators).  dG and dH are staged into two
-// buffers so that dH's staging overlaps dG's products; S^H reuses dG's buffer.  The gradient
-// kernel reads the four products (fp32 [4][U T][d]) instead of forming them on CUDA cores.
+// buffers so that dH's staging overlaps dG's products; dH itself arrives by a bulk copy while
+// dG is loaded and staged, and S^H, read once for <dH, S^H>, stays in registers until dG's
+// products have freed its buffer.  The gradient kernel reads the four products (fp32
+// [4][U T][d]) instead of forming them on CUDA cores.
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -26,9 +28,10 @@ constexpr int SP_C = kBwdChunk;              // tokens per chunk (N of every pro
 constexpr int SP_D = 128;
 constexpr uint32_t SP_MAT = SP_D * SP_D * 2;  // one fp16 [128 x 128] operand (32 KB)
 constexpr uint32_t SP_ROW = SP_C * SP_D * 2;  // one fp16 [32 x 128] operand (8 KB)
-// A1 hi | A1 lo | A2 hi | A2 lo | K | V | X hi | X lo | misc
+// A1 hi | A1 lo | A2 hi | A2 lo | K | V | X hi | X lo | dH (fp32, by bulk copy) | misc
 constexpr uint32_t SP_A1 = 0, SP_A2 = 2 * SP_MAT, SP_K = 4 * SP_MAT, SP_V = SP_K + SP_ROW,
-                   SP_XHI = SP_V + SP_ROW, SP_XLO = SP_XHI + SP_ROW, SP_MISC = SP_XLO + SP_ROW;
+                   SP_XHI = SP_V + SP_ROW, SP_XLO = SP_XHI + SP_ROW, SP_LAND = SP_XLO + SP_ROW,
+                   SP_MISC = SP_LAND + 2 * SP_MAT;
 constexpr uint32_t SP_SMEM = SP_MISC + 1024 + 1024;  // + alignment slack
 static_assert(SP_C == 32, "N = 32 products");
 static_assert(SP_SMEM <= 232448, "shared memory per block");
@@ -38,6 +41,7 @@ struct SprodMisc {
   uint64_t mbar1;       // the products with A1 (dG, then S^H)
   uint64_t mbar2;       // the products with A2 (dH)
   uint64_t mbar_drain;  // after a give-up: completion of every product issued
+  uint64_t mbar_ld;     // the bulk copy of dH
   uint32_t tmem_base;
 };
 static_assert(sizeof(SprodMisc) <= 1024, "misc block too large");
@@ -116,10 +120,17 @@ __global__ void __launch_bounds__(512, 1)
   }
 
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 128);
+  const uint32_t aLd = tc::smem_u32(&m->mbar_ld);
   if (tid == 0) {
     tc::mbar_init(aBar1, 1);
     tc::mbar_init(aBar2, 1);
     tc::mbar_init(tc::smem_u32(&m->mbar_drain), 1);
+    tc::mbar_init(aLd, 1);
+    if (dHp) {  // dH comes in while dG is loaded and staged
+      tc::fence_smem_to_async();
+      tc::mbar_arrive_expect_tx(aLd, SP_D * SP_D * 4);
+      tc::bulk_g2s(tc::smem_u32(sm + SP_LAND), dHp, SP_D * SP_D * 4, aLd);
+    }
   }
   // the chunk's rows: keys, values (bf16, exact in fp16 after a power-of-two scale) and x
   float kx[8], vx[8], xx[8];
@@ -165,18 +176,39 @@ __global__ void __launch_bounds__(512, 1)
     }
     tc::mma_commit(aBar1);
   }
-  // dH (and <dH, S^H>) into A2 while those run; T46 (64..95) = (dH + dH^T) K^T
+  // bounded waits; all threads agree on the outcome
+  bool ok = true;
+  uint32_t ph1 = 0;
+  auto wait_bar = [&](uint32_t bar, uint32_t phase) {
+    const bool done = tc::mbar_wait(bar, phase, a.wait_limit);
+    tc::fence_after_sync();
+    if (__syncthreads_or(!done)) {
+      if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
+      ok = false;
+    }
+  };
+  // S^H (read once: <dH, S^H>, then staged from these registers) and dH from its bulk copy
+  tc::Mat32 Sh;
+  tc::load_mat(SHp, nullptr, 0.0f, Sh);
   float pH = 1.0f;
   if (dHp) {
-    tc::load_mat(dHp, nullptr, 0.0f, S);
-    if (SHp) {
-      tc::Mat32 H2;
-      tc::load_mat(SHp, nullptr, 0.0f, H2);
-      fr += dot_mat(S, H2);
+    if (__syncthreads_or(!tc::mbar_wait(aLd, 0, a.wait_limit))) {  // give up: the copy still lands before the block ends
+      if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
+      if (__syncthreads_or(!tc::mbar_wait(aLd, 0, tc::kWaitLimit)) && tid == 0)
+        atomicOr(status, tc::kErrDrainTimeout);
+      ok = false;
     }
-    float mH = tc::mat_absmax(S), z1 = 0.0f, z2 = 0.0f;
-    tc::block_max3(mH, z1, z2, m->red);
-    pH = tc::pow2_ceil(mH);
+  }
+  if (dHp && ok) {
+    tc::load_mat_smem(sm + SP_LAND, nullptr, 0.0f, S);
+    if (SHp) fr += dot_mat(S, Sh);
+  }
+  float mH = dHp && ok ? tc::mat_absmax(S) : 0.0f, mSH = tc::mat_absmax(Sh), z1 = 0.0f;
+  tc::block_max3(mH, mSH, z1, m->red);
+  pH = tc::pow2_ceil(mH);
+  const float pSH = tc::pow2_ceil(mSH);
+  // dH into A2 while dG's products run; T46 (64..95) = (dH + dH^T) K^T
+  if (dHp && ok) {
     tc::store_mat(S, 1.0f / pH, A2hi, A2lo);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
@@ -193,30 +225,14 @@ __global__ void __launch_bounds__(512, 1)
       tc::mma_commit(aBar2);
     }
   }
-  // bounded waits; all threads agree on the outcome
-  bool ok = true;
-  uint32_t ph1 = 0;
-  auto wait_bar = [&](uint32_t bar, uint32_t phase) {
-    const bool done = tc::mbar_wait(bar, phase, a.wait_limit);
-    tc::fence_after_sync();
-    if (__syncthreads_or(!done)) {
-      if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
-      ok = false;
-    }
-  };
   // S^H into A1 once dG's products have read it; T5 (96..127) = S^H^T X^T, both split
-  float pSH = 1.0f;
-  if (SHp) {
-    tc::load_mat(SHp, nullptr, 0.0f, S);
-    float mH = tc::mat_absmax(S), z1 = 0.0f, z2 = 0.0f;
-    tc::block_max3(mH, z1, z2, m->red);
-    pSH = tc::pow2_ceil(mH);
+  if (SHp && ok) {
     if (dGp) {
       wait_bar(aBar1, ph1);
       ph1 ^= 1;
     }
     if (ok) {
-      tc::store_mat(S, 1.0f / pSH, A1hi, A1lo);
+      tc::store_mat(Sh, 1.0f / pSH, A1hi, A1lo);
       tc::fence_smem_to_async();
       tc::fence_before_sync();
       __syncthreads();

@@ -197,3 +197,41 @@ def test_decode_wait_give_up_reports_timeout_and_leaves_the_state():
     H2, G2 = H0.clone(), G0.clone()
     o2, i2 = binding.mesa_decode_step(H2, G2, **x, lambda_diag=lam, cg_iters=w.cg_iters, cg_tol=w.cg_tol)
     assert torch.equal(o1, o2) and torch.equal(i1, i2) and torch.equal(H1, H2) and torch.equal(G1, G2)
+
+
+def test_backward_wait_give_up_reports_timeout_and_the_next_call_is_clean():
+    """The backward's tensor-core kernels (bf16, d = 128: the solves, the state sweeps and the
+    products of the rows with the chunk states) made to give up their waits at once: the
+    status word reports MESA_ERR_TIMEOUT with no expired drain, and the next call with the
+    default limit equals a call that never gave up, bit for bit."""
+    import torch
+
+    from mesa_layer_gb300 import binding
+    w = synth.workload("fwd_bf16_d128", B=1, H=2, T=300, cg_iters=10, cg_tol=0.0)
+    inp = synth.forward_inputs(w, seed=23)
+    t = torch_inputs(inp, "bf16")
+    g = torch.Generator().manual_seed(5)
+    dout = torch.randn(t["q"].shape, generator=g).to(torch.bfloat16).cuda()
+    ws = torch.empty(binding.mesa_backward_workspace_size(w.B, w.H, w.T, w.dk, w.dv), dtype=torch.uint8,
+                     device="cuda")
+
+    def call():
+        r = binding.mesa_backward_chunked(t["q"], t["k"], t["v"], t["gamma"], t["lam"], dout, w.cg_iters, 0.0,
+                                          workspace=ws)
+        code, flags = binding.mesa_forward_status_code(ws)
+        torch.cuda.synchronize()
+        return [x.float().cpu() for x in r[:5]], code, flags
+
+    clean, code, flags = call()
+    assert code == binding.MESA_OK and flags == 0
+    binding.mesa_debug_set_wait_limit(0)
+    try:
+        _, code, flags = call()
+    finally:
+        binding.mesa_debug_set_wait_limit(-1)
+    assert code == binding.MESA_ERR_TIMEOUT and flags & 1, (code, flags)
+    assert not flags & 4, "the drain of the in-flight multiplies expired"
+    again, code, flags = call()
+    assert code == binding.MESA_OK and flags == 0
+    for a, b in zip(again, clean):
+        assert torch.equal(a, b)
