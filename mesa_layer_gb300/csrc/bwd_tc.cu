@@ -83,6 +83,32 @@ __device__ __forceinline__ void store_row8(const float (&x)[8], float s, uint8_t
   *reinterpret_cast<uint4 *>(hi + off) = *reinterpret_cast<uint4 *>(h);
   if (lo) *reinterpret_cast<uint4 *>(lo + off) = *reinterpret_cast<uint4 *>(l);
 }
+// Block-wide maxima of four values (red: 4 floats per warp, 16 warps).
+__device__ __forceinline__ void block_max4(float &a, float &b, float &c, float &d, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+    c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
+    d = fmaxf(d, __shfl_xor_sync(0xffffffffu, d, o));
+  }
+  __syncthreads();
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    red[4 * w] = a;
+    red[4 * w + 1] = b;
+    red[4 * w + 2] = c;
+    red[4 * w + 3] = d;
+  }
+  __syncthreads();
+  a = red[0], b = red[1], c = red[2], d = red[3];
+  for (int k = 1; k < (int)(blockDim.x >> 5); k++) {
+    a = fmaxf(a, red[4 * k]);
+    b = fmaxf(b, red[4 * k + 1]);
+    c = fmaxf(c, red[4 * k + 2]);
+    d = fmaxf(d, red[4 * k + 3]);
+  }
+}
 __device__ __forceinline__ float dot_mat(const tc::Mat32 &x, const tc::Mat32 &y) {
   float s = 0.0f;
 #pragma unroll
@@ -119,6 +145,15 @@ __global__ void __launch_bounds__(512, 1)
     return;
   }
 
+  // the chunk's rows (keys, values: bf16, exact in fp16 after a power-of-two scale; x), dG
+  // and S^G: their loads are issued before the set-up below, which they then overlap
+  float kx[8], vx[8], xx[8];
+  load_row8_bf16((const __nv_bfloat16 *)a.k + tokbase * D, Cv, kx);
+  load_row8_bf16((const __nv_bfloat16 *)a.v + tokbase * D, Cv, vx);
+  load_row8_f32(a.X + tokbase * D, Cv, xx);
+  tc::Mat32 S, G2;
+  tc::load_mat(dGp, nullptr, 0.0f, S);
+  tc::load_mat(dGp ? SGp : nullptr, nullptr, 0.0f, G2);
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&m->tmem_base), 128);
   const uint32_t aLd = tc::smem_u32(&m->mbar_ld);
   if (tid == 0) {
@@ -132,24 +167,10 @@ __global__ void __launch_bounds__(512, 1)
       tc::bulk_g2s(tc::smem_u32(sm + SP_LAND), dHp, SP_D * SP_D * 4, aLd);
     }
   }
-  // the chunk's rows: keys, values (bf16, exact in fp16 after a power-of-two scale) and x
-  float kx[8], vx[8], xx[8];
-  load_row8_bf16((const __nv_bfloat16 *)a.k + tokbase * D, Cv, kx);
-  load_row8_bf16((const __nv_bfloat16 *)a.v + tokbase * D, Cv, vx);
-  load_row8_f32(a.X + tokbase * D, Cv, xx);
-  // dG and, where the chunk has both, <dG, S^G>
-  float fr = 0.0f;
-  tc::Mat32 S;
-  tc::load_mat(dGp, nullptr, 0.0f, S);
-  if (dGp && SGp) {
-    tc::Mat32 G2;
-    tc::load_mat(SGp, nullptr, 0.0f, G2);
-    fr = dot_mat(S, G2);
-  }
-  float mS = tc::mat_absmax(S), mK = absmax8(kx), mV = absmax8(vx);
-  tc::block_max3(mS, mK, mV, m->red);
-  float mX = absmax8(xx), u1 = 0.0f, u2 = 0.0f;
-  tc::block_max3(mX, u1, u2, m->red);  // (its first barrier orders the reuse of red)
+  // <dG, S^G> where the chunk has both
+  float fr = (dGp && SGp) ? dot_mat(S, G2) : 0.0f;
+  float mS = tc::mat_absmax(S), mK = absmax8(kx), mV = absmax8(vx), mX = absmax8(xx);
+  block_max4(mS, mK, mV, mX, m->red);
   const float pG = tc::pow2_ceil(mS), pK = tc::pow2_ceil(mK), pV = tc::pow2_ceil(mV), pX = tc::pow2_ceil(mX);
   if (dGp) tc::store_mat(S, 1.0f / pG, A1hi, A1lo);
   store_row8(kx, 1.0f / pK, Kh, nullptr);
