@@ -12,8 +12,9 @@
 // The raw key and value rows of the next chunk arrive by bulk copies (tensor memory
 // accelerator) into staging buffers while the current chunk's MMAs and write-out run, and
 // the states leave the same way: each is moved from tensor memory into a 128-byte-swizzled
-// staging buffer and written by four tiled tensor stores (32 columns x 128 rows each), so
-// that the CTA goes on with the next chunk while HBM absorbs the 128 KB per chunk.
+// staging buffer (S^H a buffer of its own, S^G the A operand region, free once the value sums
+// are done) and written by four tiled tensor stores (32 columns x 128 rows each), so that the
+// CTA goes on with the next chunk while HBM absorbs the 128 KB per chunk.
 // Segment 0 starts from the initial state, later segments from zero; mesa_carry_tc_kernel then
 // chains the segments (carry[s] = global state before segment s) and writes the final state,
 // and the CG kernel adds exp(Lc) carry when it loads a state.
@@ -163,15 +164,18 @@ __global__ void __launch_bounds__(512, 1)
   };
   load_ell(c_begin);
   // state write-out (without PRE): tensor memory -> staging buffer -> four tensor stores.
-  // The staging buffer is reused once thread 0 has seen the previous stores read it
-  // (bulk_wait_read before the block barrier that precedes the next staging).
+  // S^H goes through the staging buffer, S^G through the A operand region (free once the
+  // value sums are done, until the next chunk's key operand is staged there), so that
+  // neither waits for the other's stores; a buffer is reused once thread 0 has seen the
+  // stores from it read it (bulk_wait_read before the block barrier that precedes the reuse).
   uint8_t *Out = sm + DT_OUT;
+  auto out_buf = [&](int half) { return half ? Ahi : Out; };
   auto stage_state = [&](int half, float sig) {
     const float f = 1.0f / sig;
     float x[32];
     tc::tmem_ld32(tl + half * 128, x);
     tc::tmem_ld_wait();
-    uint8_t *dst = Out + cg * DT_SLAB + row * 128;
+    uint8_t *dst = out_buf(half) + cg * DT_SLAB + row * 128;
 #pragma unroll
     for (int g = 0; g < 8; g++)
       *reinterpret_cast<float4 *>(dst + ((g ^ (row & 7)) << 4)) =
@@ -182,7 +186,7 @@ __global__ void __launch_bounds__(512, 1)
     const void *map = half ? (const void *)&mapG : (const void *)&mapH;
     const int y = (u * NC + c) * TILE;
 #pragma unroll
-    for (int sl = 0; sl < 4; sl++) tc::tensor_s2g_2d(map, tc::smem_u32(Out + sl * DT_SLAB), 32 * sl, y);
+    for (int sl = 0; sl < 4; sl++) tc::tensor_s2g_2d(map, tc::smem_u32(out_buf(half) + sl * DT_SLAB), 32 * sl, y);
     tc::bulk_commit();
   };
   for (int c = c_begin; c < c_end && ok; c++) {
@@ -218,6 +222,9 @@ __global__ void __launch_bounds__(512, 1)
     if (tid < TILE) m->w[tid] = tid < Tv ? expf(lend - ell_tid) : 0.0f;
     if (c + 1 < c_end) load_ell(c + 1);
     tc::fence_smem_to_async();
+    // the previous chunk's states have left their buffers (S^G: the A operand region, about
+    // to take this chunk's weighted keys)
+    if (!PRE && tid == 0) tc::bulk_wait_read();
     __syncthreads();  // (also: every thread holds its rows, the staging buffers are free)
     if (tid == 0 && c + 1 < c_end) fetch(c + 1);
     pending = c + 1 < c_end;
@@ -237,7 +244,6 @@ __global__ void __launch_bounds__(512, 1)
     if (tid == 0) issue(0, !first || H0 != nullptr);
     // S^G's accumulator (columns the key sums do not touch) is rescaled while they run
     rescale(128, first ? ac * nsigG : ac * nsigG / sigG, first, G0);
-    if (!PRE && tid == 0) tc::bulk_wait_read();  // the previous S^G has left the staging buffer
     ok = wait();
     if (!ok) break;
     tc::store_rows(vr, m->w, sAG, Ahi, Alo);
@@ -264,12 +270,9 @@ __global__ void __launch_bounds__(512, 1)
     } else {
       stage_state(0, nsigH);
       __syncthreads();
-      if (tid == 0) {
-        store_state(0, c);
-        tc::bulk_wait_read();  // S^H has left the staging buffer before S^G comes in
-      }
+      if (tid == 0) store_state(0, c);
     }
-    ok = wait();
+    ok = wait();  // (the value sums are done: the A operand region is free for S^G)
     if (!ok) break;
     if constexpr (PRE) {
       write_state(1, nsigG);
