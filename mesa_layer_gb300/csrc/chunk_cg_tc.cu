@@ -196,7 +196,7 @@ __device__ __forceinline__ void st8(uint8_t *hi, uint8_t *lo, int i, int c0, con
 // forward's x S^G^T); b is written in fp32 to sv.x_out.
 template <int NTERMS, bool SOLVE, bool SAVE, bool RHS, bool PRE = false>
 __global__ void __launch_bounds__(512, 1)
-    mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, int lookahead, unsigned *status,
+    mesa_cg_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, unsigned *status,
                       SolveArgs sv) {
   constexpr int NG = 4;           // column groups (threads per token row)
   constexpr int CW = DH / NG;     // columns per thread
@@ -333,24 +333,6 @@ __global__ void __launch_bounds__(512, 1)
   // the readout's state is only needed after the CG and is fetched into L2 meanwhile
   tc::prefetch_l2(SG, sizeof(float) * DH * DH);
   tc::prefetch_l2(CG, sizeof(float) * DH * DH);
-  {  // CTAs start in block order as SMs free up (one per SM), so the chunk `lookahead`
-     // blocks on runs about one wave later: its inputs go into L2 now
-    const long long wn = (long long)blockIdx.x + (long long)NC * blockIdx.y + lookahead;
-    if (lookahead > 0 && wn < (long long)NC * gridDim.y) {
-      const int cn = (int)(wn % NC), un = (int)(wn / NC);
-      const int Tn = min(TILE, T - cn * TILE);
-      const size_t tbn = (size_t)un * T + (size_t)cn * TILE;
-      if (cn > 0) {
-        tc::prefetch_l2(ws.SH + ((size_t)un * NC + (cn - 1)) * DH * DH, sizeof(float) * DH * DH);
-        const int segn = (cn - 1) / ((NC + ws.nseg - 1) / ws.nseg);
-        if (segn > 0)
-          tc::prefetch_l2(ws.carry + ((size_t)un * ws.nseg + segn) * 2 * DH * DH, sizeof(float) * DH * DH);
-      }
-      tc::prefetch_l2(k + tbn * DH, sizeof(__nv_bfloat16) * DH * Tn);
-      tc::prefetch_l2(q + tbn * DH, sizeof(__nv_bfloat16) * DH * Tn);
-      tc::prefetch_l2(ws.ell + tbn, sizeof(float) * Tn);
-    }
-  }
   __syncthreads();  // barrier initialisations (and the per-chunk constants) visible
   // Bounded waits for the copies; on a give-up the block waits (default limit) until they have
   // landed, so that nothing writes this CTA's shared memory after it ends, and skips the chunk.
@@ -901,7 +883,7 @@ int launch_chunk_cg_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *statu
       cudaSuccess)
     return -1;
   timing_mark_begin(K_CG_TC, st);
-  kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(a, ws, NC, sm_count(), status, sv);
+  kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(a, ws, NC, status, sv);
   timing_mark_end(K_CG_TC, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
@@ -924,7 +906,7 @@ int launch_rhs_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status, cu
       cudaSuccess)
     return -1;
   timing_mark_begin(K_BWD_RHS, st);
-  kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(r, ws, NC, sm_count(), status, sv);
+  kfn<<<dim3(NC, U), 512, SMEM_TC, st>>>(r, ws, NC, status, sv);
   timing_mark_end(K_BWD_RHS, st);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
