@@ -155,3 +155,26 @@ def test_tc_dynamic_initial_state():
                         G0=torch.from_numpy(G0).cuda())
     r = forward_check(inp, o, it, "bf16", w.cg_iters, w.cg_tol, "dynamic from a state", H0=H0, G0=G0)
     print(f"tc dynamic from a state: {r}")
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+@pytest.mark.parametrize("tol", [0.0, 1e-3], ids=["fixed", "dynamic"])
+def test_tc_query_scale_is_exact(dtype, d, tol):
+    """The CG iterate is homogeneous in q, and the tensor-core kernels take every operand scale
+    from exponent bits: q times 2^k (k = -40, 40) gives exactly 2^k times the outputs, bit for
+    bit, with the same iteration counts (the stopping rule compares norms that scale alike),
+    and the scaled call still matches the oracle -- on the readout's magnitude: at 12
+    un-converged iterations one token of this case has a cancelling readout (strict 2.2e-2,
+    as in the unscaled call, whose outputs are the same bits up to the power of two)."""
+    w = synth.workload("fwd_bf16_d128" if dtype == "bf16" else "fwd_fp32_d64", dtype=dtype, dk=d, dv=d, B=1, H=2,
+                       T=300, cg_iters=12 if tol == 0.0 else 30, cg_tol=tol)
+    inp = synth.forward_inputs(w, seed=17)
+    o, it = gpu_forward(inp, dtype, w.cg_iters, tol, 64)
+    for k in (-40, 40):
+        sc = dict(inp)
+        sc["q"] = (inp["q"] * np.float32(2.0 ** k)).astype(np.float32)
+        o2, it2 = gpu_forward(sc, dtype, w.cg_iters, tol, 64)
+        assert np.array_equal(it2, it), k
+        assert np.array_equal(o2, (o * np.float32(2.0 ** k)).astype(np.float32)), k
+    r = forward_check(sc, o2, it2, dtype, w.cg_iters, tol, f"q x 2^{k}", metric="product")
+    print(f"q x 2^{k}: {r}")
