@@ -232,35 +232,33 @@ __global__ void __launch_bounds__(512, 1)
   // row i of the quadrant): their block of Z is zero for every p, written once below.
   const bool z_upper = grp > qd;
 
-  // Row-reduction scratch: value n of column group g for row 32 qd + l sits in float l / 8
-  // of the 16-byte chunk g of that row of Z (hi for n = 0, lo for n = 1): columns 0..31,
-  // which no warp above the diagonal owns, conflict-free across the lanes of a warp.  Only
-  // the quadrant's own threads touch its rows, and never while Z is live.
+  // Row-reduction scratch: the value of column group g for row 32 qd + l sits in float l / 8
+  // of the 16-byte chunk g of that row of Z hi: columns 0..31, conflict-free across the lanes
+  // of a warp.  Only the quadrant's own threads touch its rows, and never while Z is live.
   const uint32_t scr_row = (uint32_t)((i >> 3) * 1024 + (i & 7) * 128 + 4 * (lane >> 3));
   // Slot 1 (float (lane >> 3) ^ 2 of the same chunks) serves the CG step's two reductions
   // after the Y product: Z is dead from then until the next step's Z build, and the step's
   // first block barrier separates these reductions' reads from the next writes, so they keep
   // one barrier each (the sum of sigma in slot 1, the residual's in slot 0).
-  auto scr = [&](int n, int g, int slot = 0) -> float * {
-    return reinterpret_cast<float *>((n ? Zlo : Zhi) + scr_row + ((g ^ (i & 7)) << 4)) + 2 * slot *
-           (((lane >> 3) & 2) ? -1 : 1);
+  auto scr = [&](int g, int slot = 0) -> float * {
+    return reinterpret_cast<float *>(Zhi + scr_row + ((g ^ (i & 7)) << 4)) + 2 * slot * (((lane >> 3) & 2) ? -1 : 1);
   };
   auto rowsum = [&](float val) -> float {
-    *scr(0, grp) = val;
+    *scr(grp) = val;
     quad_bar<NG>(qd);
-    float r = *scr(0, 0);
+    float r = *scr(0);
 #pragma unroll
-    for (int g = 1; g < NG; g++) r += *scr(0, g);
+    for (int g = 1; g < NG; g++) r += *scr(g);
     quad_bar<NG>(qd);
     return r;
   };
   // the CG step's reductions after the Y product (one barrier each, see above)
   auto step_sum = [&](float val, int slot) -> float {
-    *scr(0, grp, slot) = val;
+    *scr(grp, slot) = val;
     quad_bar<NG>(qd);
-    float r = *scr(0, 0, slot);
+    float r = *scr(0, slot);
 #pragma unroll
-    for (int g = 1; g < NG; g++) r += *scr(0, g, slot);
+    for (int g = 1; g < NG; g++) r += *scr(g, slot);
     return r;
   };
 

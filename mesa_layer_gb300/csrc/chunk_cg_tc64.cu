@@ -188,27 +188,26 @@ __global__ void __launch_bounds__(512, 1)
   // Row-reduction scratch in the Z operand's rows (columns 0..31, never above the diagonal),
   // used only while Z is dead: as in the d = 128 kernel.
   const uint32_t scr_row = (uint32_t)((i >> 3) * 1024 + (i & 7) * 128 + 4 * (lane >> 3));
-  auto scr = [&](int n, int g, int slot = 0) -> float * {
-    return reinterpret_cast<float *>((n ? Zlo : Zhi) + scr_row + ((g ^ (i & 7)) << 4)) + 2 * slot *
-           (((lane >> 3) & 2) ? -1 : 1);
+  auto scr = [&](int g, int slot = 0) -> float * {
+    return reinterpret_cast<float *>(Zhi + scr_row + ((g ^ (i & 7)) << 4)) + 2 * slot * (((lane >> 3) & 2) ? -1 : 1);
   };
   auto rowsum = [&](float val) -> float {
-    *scr(0, grp) = val;
+    *scr(grp) = val;
     quad_bar64<NG>(qd);
-    float r = *scr(0, 0);
+    float r = *scr(0);
 #pragma unroll
-    for (int g = 1; g < NG; g++) r += *scr(0, g);
+    for (int g = 1; g < NG; g++) r += *scr(g);
     quad_bar64<NG>(qd);
     return r;
   };
   // the CG step's reductions after the Y product: one barrier each, sigma in slot 1 and the
   // residual in slot 0 (see the d = 128 kernel)
   auto step_sum = [&](float val, int slot) -> float {
-    *scr(0, grp, slot) = val;
+    *scr(grp, slot) = val;
     quad_bar64<NG>(qd);
-    float r = *scr(0, 0, slot);
+    float r = *scr(0, slot);
 #pragma unroll
-    for (int g = 1; g < NG; g++) r += *scr(0, g, slot);
+    for (int g = 1; g < NG; g++) r += *scr(g, slot);
     return r;
   };
 
