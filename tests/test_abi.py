@@ -171,8 +171,11 @@ def test_backward_workspace_and_validation(lib):
     assert ws(2, 3, 100, 64, 32) == 0          # dk != dv
     small, big = ws(2, 3, 100, 64, 64), ws(2, 3, 1000, 64, 64)
     assert 0 < small < big
-    # d = 128 also holds the 128-token states of the tensor-core solves
+    # d = 128 also holds the 128-token states of the tensor-core solves, and the four fp32
+    # products of each token's row with the chunk states (4 T d floats per unit) with one
+    # Frobenius pair per 32-token chunk
     assert ws(1, 1, 256, 128, 128) > 2 * ws(1, 1, 256, 64, 64)
+    assert ws(1, 1, 256, 128, 128) >= 4 * 4 * 256 * 128 + 4 * (256 // 32) + 2 * 4 * (256 // 32) * 128 * 128
     f = lib.mesa_backward_chunked  # argument types set by the binding
     p = ctypes.c_void_p(256)
 

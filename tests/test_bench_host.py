@@ -57,6 +57,17 @@ def test_backward_flop_models():
     assert bench.bwd_rhs_flops(w) == 64 * (2 * d * d + 2 * d * 33)
 
 
+def test_backward_split_flop_models():
+    # with the row x state products on the tensor cores the gradient kernel keeps only the
+    # intra-chunk work (7 d (C + 1) per token-head, C = 32); the products kernel counts five
+    # d x d products (10 d^2) and issues 88 MMAs of 128 x 32 x 16 per 32-token chunk
+    w = synth.workload("bwd_bf16_d128", B=1, H=1, T=64)
+    assert bench.bwd_grad_flops(w, True) == 64 * 7 * 128 * 33
+    assert bench.bwd_grad_flops(w) == 64 * (12 * 128 * 128 + 7 * 128 * 33)
+    assert bench.bwd_sprod_flops(w) == 64 * 10 * 128 * 128
+    assert bench.bwd_sprod_executed_flops(w) == 2 * 88 * 2 * 128 * 32 * 16
+
+
 def test_preprocess_bytes():
     w = synth.workload("qkpre_bf16_d128", B=1, H=2, T=10)
     # q and k read and written in bf16, plus both tap arrays in fp32
