@@ -135,6 +135,20 @@ def test_closed_gates():
     assert np.all(g["dgamma"][~open_gate] == 0.0)
 
 
+def test_closed_gates_tensor_cores():
+    """The same at bf16, d = 128 (the tensor-core solves, state sweeps and row x state
+    products), over several 32- and 128-token chunks with a closed gate inside and at the
+    first token of a 32-token chunk."""
+    w = _wl("bf16", B=1, H=2, T=200, dk=128, dv=128)
+    inp = synth.backward_inputs(w, seed=4)
+    inp["gamma"][:, :, [7, 64, 150]] = 0.0
+    g = _gpu(inp, "bf16", 10, 0.0)
+    r = oracle.backward(inp["q"], inp["k"], inp["v"], inp["gamma"], inp["lam"], inp["dout"], 10)
+    open_gate = inp["gamma"] > 0
+    _check(g, r, "bf16", "bwd closed gates, tensor cores", mask=open_gate)
+    assert np.all(g["dgamma"][~open_gate] == 0.0)
+
+
 def test_dynamic_mode():
     """Dynamic stopping (tol 1e-3, cap 30): counts may differ at the threshold; the units whose
     counts all agree must meet the tolerance, and at least 95 % of the counts agree."""
