@@ -348,6 +348,15 @@ __global__ void __launch_bounds__(256, TCS ? 2 : 1) mesa_bwd_grad_kernel(BwdArgs
     }
   };
   if (!TCS && ns > 0) fetch(kinds[0]);  // in flight while the tiles load and the intra-chunk parts run
+  if constexpr (TCS) {  // the product rows and b (read after the intra-chunk parts) into L2 now
+    const size_t plane = (size_t)a.B * a.H * T * D, bytes = (size_t)Cv * D * sizeof(float);
+    for (size_t o = (size_t)tid * 128; o < bytes; o += (size_t)nt * 128) {
+#pragma unroll
+      for (int g = 0; g < 4; g++)
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"((const char *)(a.tprod + g * plane + tokbase * D) + o));
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"((const char *)(a.rhs + tokbase * D) + o));
+    }
+  }
   load_tile<D>(Ks, (const TIO *)a.k + tokbase * D, Cv);
   load_tile<D>(Vs, (const TIO *)a.v + tokbase * D, Cv);
   load_tile<D>(Gs, (const TIO *)a.dout + tokbase * D, Cv);
