@@ -30,7 +30,7 @@ constexpr uint32_t DT_MAT = 128 * 128 * 2;
 // K operand | A hi | A lo | misc (1 KB) | raw key rows | raw value rows | then either the
 // state staging buffer (64 KB: four 16 KB slabs of 32 fp32 columns, 128-byte swizzled) or,
 // with the query/key preprocessing fused, the raw key rows before the chunk (2 KB) and the
-// head's taps (4 KB) (the states then go out by plain stores) | alignment slack
+// head's taps (4 KB) (both states then go out through the A operand region) | alignment slack
 constexpr uint32_t DT_STAGE = 3 * DT_MAT + 1024;
 constexpr uint32_t DT_OUT = DT_STAGE + 2 * DT_MAT, DT_SLAB = 128 * 32 * 4;
 constexpr uint32_t DT_HALO = DT_OUT, DT_TAPS = DT_HALO + 2048;
@@ -51,7 +51,7 @@ struct StateMisc {
 // PRE: k holds raw inputs of the query/key preprocessing, applied to each chunk's key rows
 // when they arrive (the pass's arithmetic, so the states equal those of preprocessed keys).
 // mapH, mapG: tensor maps of ws.SH, ws.SG as [U NC 128 rows, 128 fp32 columns] with boxes of
-// 32 columns x 128 rows (128-byte swizzle); unused with PRE.
+// 32 columns x 128 rows (128-byte swizzle).
 template <bool PRE>
 __global__ void __launch_bounds__(512, 1)
     mesa_states_tc_kernel(FwdArgs a, FwdWorkspace ws, int NC, unsigned *status,
@@ -163,13 +163,14 @@ __global__ void __launch_bounds__(512, 1)
     ell_tid = tid < tv ? ws.ell[tb + tid] : 0.0f;
   };
   load_ell(c_begin);
-  // state write-out (without PRE): tensor memory -> staging buffer -> four tensor stores.
+  // state write-out: tensor memory -> staging buffer -> four tensor stores.
   // S^H goes through the staging buffer, S^G through the A operand region (free once the
   // value sums are done, until the next chunk's key operand is staged there), so that
-  // neither waits for the other's stores; a buffer is reused once thread 0 has seen the
-  // stores from it read it (bulk_wait_read before the block barrier that precedes the reuse).
+  // neither waits for the other's stores (PRE: both through the A operand region, one after
+  // the other); a buffer is reused once thread 0 has seen the stores from it read it
+  // (bulk_wait_read before the block barrier that precedes the reuse).
   uint8_t *Out = sm + DT_OUT;
-  auto out_buf = [&](int half) { return half ? Ahi : Out; };
+  auto out_buf = [&](int half) { return (PRE || half) ? Ahi : Out; };
   auto stage_state = [&](int half, float sig) {
     const float f = 1.0f / sig;
     float x[32];
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(512, 1)
     tc::fence_smem_to_async();
     // the previous chunk's states have left their buffers (S^G: the A operand region, about
     // to take this chunk's weighted keys)
-    if (!PRE && tid == 0) tc::bulk_wait_read();
+    if (tid == 0) tc::bulk_wait_read();
     __syncthreads();  // (also: every thread holds its rows, the staging buffers are free)
     if (tid == 0 && c + 1 < c_end) fetch(c + 1);
     pending = c + 1 < c_end;
@@ -252,22 +253,10 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) issue(128, !first || G0 != nullptr);
-    // segment-local state after chunk c (half 0: S^H, half 1: S^G), unscaled
-    auto write_state = [&](int half, float sig) {
-      const float f = 1.0f / sig;
-      float *dst = (half ? ws.SG : ws.SH) + (((size_t)u * NC + c) * DH + row) * DH + 32 * cg;
-      float x[32];
-      tc::tmem_ld32(tl + half * 128, x);
-      tc::tmem_ld_wait();
-#pragma unroll
-      for (int g = 0; g < 8; g++)
-        reinterpret_cast<float4 *>(dst)[g] =
-            make_float4(x[4 * g] * f, x[4 * g + 1] * f, x[4 * g + 2] * f, x[4 * g + 3] * f);
-    };
-    // S^H goes out while the tensor core adds the value sums into S^G
-    if constexpr (PRE) {
-      write_state(0, nsigH);
-    } else {
+    // S^H goes out while the tensor core adds the value sums into S^G (with the fused
+    // preprocessing, whose window rows and taps take the staging buffer's place, both states
+    // leave one after the other through the A operand region once the value sums are done)
+    if constexpr (!PRE) {
       stage_state(0, nsigH);
       __syncthreads();
       if (tid == 0) store_state(0, c);
@@ -275,12 +264,17 @@ __global__ void __launch_bounds__(512, 1)
     ok = wait();  // (the value sums are done: the A operand region is free for S^G)
     if (!ok) break;
     if constexpr (PRE) {
-      write_state(1, nsigG);
-    } else {
-      stage_state(1, nsigG);
+      stage_state(0, nsigH);
       __syncthreads();
-      if (tid == 0) store_state(1, c);
+      if (tid == 0) {
+        store_state(0, c);
+        tc::bulk_wait_read();  // S^H has left the A region before S^G comes in
+      }
+      __syncthreads();
     }
+    stage_state(1, nsigG);
+    __syncthreads();
+    if (tid == 0) store_state(1, c);
     sigH = nsigH;
     sigG = nsigG;
     Lsum += lend;
@@ -294,7 +288,7 @@ __global__ void __launch_bounds__(512, 1)
       atomicOr(status, tc::kErrDrainTimeout);
   }
   // the state stores still in flight complete before the block (and its shared memory) ends
-  if (!PRE && tid == 0) tc::bulk_wait_all();
+  if (tid == 0) tc::bulk_wait_all();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_free(tbase, 256);
@@ -363,7 +357,7 @@ int launch_states_tc(const FwdArgs &a, const FwdWorkspace &ws, unsigned *status,
   const uint32_t smem = pre ? DT_SMEM_PRE : DT_SMEM;
   CUtensorMap mapH{}, mapG{};
   const size_t rows = (size_t)U * NC * 128;
-  if (!pre && (!tmap_rows128_f32(&mapH, ws.SH, rows) || !tmap_rows128_f32(&mapG, ws.SG, rows))) return -1;
+  if (!tmap_rows128_f32(&mapH, ws.SH, rows) || !tmap_rows128_f32(&mapG, ws.SG, rows)) return -1;
   if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return -1;
   timing_mark_begin(K_DELTA_TC, st);
