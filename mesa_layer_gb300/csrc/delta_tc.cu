@@ -223,10 +223,7 @@ __global__ void __launch_bounds__(512, 1)
     if (tid < TILE) m->w[tid] = tid < Tv ? expf(lend - ell_tid) : 0.0f;
     if (c + 1 < c_end) load_ell(c + 1);
     tc::fence_smem_to_async();
-    // the previous chunk's states have left their buffers (S^G: the A operand region, about
-    // to take this chunk's weighted keys)
-    if (tid == 0) tc::bulk_wait_read();
-    __syncthreads();  // (also: every thread holds its rows, the staging buffers are free)
+    __syncthreads();  // every thread holds its rows: the staging buffers are free
     if (tid == 0 && c + 1 < c_end) fetch(c + 1);
     pending = c + 1 < c_end;
     float mk = tc::rows_absmax(kr, nullptr), mak = tc::rows_absmax(kr, m->w),
@@ -235,6 +232,11 @@ __global__ void __launch_bounds__(512, 1)
     const float sK = 1.0f / tc::pow2_ceil(mk), sAH = 1.0f / tc::pow2_ceil(mak),
                 sAG = 1.0f / tc::pow2_ceil(mav);
     tc::store_rows(kr, nullptr, sK, Ks, nullptr);
+    // the previous chunk's states have left their staging buffers (S^G: the A operand region,
+    // about to take this chunk's weighted keys); waited for only here, so that the stores
+    // drain while the rows are loaded and their scales found
+    if (tid == 0) tc::bulk_wait_read();
+    __syncthreads();
     tc::store_rows(kr, m->w, sAH, Ahi, Alo);
     const float nsigH = sAH * sK, nsigG = sAG * sK;
     rescale(0, first ? ac * nsigH : ac * nsigH / sigH, first, H0);
