@@ -172,10 +172,10 @@ __global__ void __launch_bounds__(512, 1)
   float mS = tc::mat_absmax(S), mK = absmax8(kx), mV = absmax8(vx), mX = absmax8(xx);
   block_max4(mS, mK, mV, mX, m->red);
   const float pG = tc::pow2_ceil(mS), pK = tc::pow2_ceil(mK), pV = tc::pow2_ceil(mV), pX = tc::pow2_ceil(mX);
-  if (dGp) tc::store_mat(S, 1.0f / pG, A1hi, A1lo);
-  store_row8(kx, 1.0f / pK, Kh, nullptr);
-  store_row8(vx, 1.0f / pV, Vh, nullptr);
-  store_row8(xx, 1.0f / pX, Xhi, Xlo);
+  if (dGp) tc::store_mat(S, tc::rcp_pow2_ceil(mS), A1hi, A1lo);
+  store_row8(kx, tc::rcp_pow2_ceil(mK), Kh, nullptr);
+  store_row8(vx, tc::rcp_pow2_ceil(mV), Vh, nullptr);
+  store_row8(xx, tc::rcp_pow2_ceil(mX), Xhi, Xlo);
   tc::fence_smem_to_async();
   tc::fence_before_sync();
   __syncthreads();
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(512, 1)
   const float pSH = tc::pow2_ceil(mSH);
   // dH into A2 while dG's products run; T46 (64..95) = (dH + dH^T) K^T
   if (dHp && ok) {
-    tc::store_mat(S, 1.0f / pH, A2hi, A2lo);
+    tc::store_mat(S, tc::rcp_pow2_ceil(mH), A2hi, A2lo);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(512, 1)
       ph1 ^= 1;
     }
     if (ok) {
-      tc::store_mat(Sh, 1.0f / pSH, A1hi, A1lo);
+      tc::store_mat(Sh, tc::rcp_pow2_ceil(mSH), A1hi, A1lo);
       tc::fence_smem_to_async();
       tc::fence_before_sync();
       __syncthreads();

@@ -377,8 +377,8 @@ __global__ void __launch_bounds__(512, 1)
     tc::block_max3(mS, mK, unused, m->red);  // (its barrier: every staged copy has been read)
     pS = tc::pow2_ceil(mS);
     pK = tc::pow2_ceil(mK);
-    sS = 1.0f / pS;
-    sK = 1.0f / pK;
+    sS = tc::rcp_pow2_ceil(mS);
+    sK = tc::rcp_pow2_ceil(mK);
     tc::store_mat(S, sS, Shi, NTERMS == 2 ? Slo : nullptr);
     tc::store_rows(kr, nullptr, sK, Ks, nullptr);
   }
@@ -789,7 +789,7 @@ __global__ void __launch_bounds__(512, 1)
       tc::block_max3(mG, mV, unused, m->red);  // (its barrier: the staged copies have been read)
       pG = tc::pow2_ceil(mG);
       pV = tc::pow2_ceil(mV);
-      sG = 1.0f / pG;
+      sG = tc::rcp_pow2_ceil(mG);
       tc::store_mat(G, sG, Shi, NTERMS == 2 ? Slo : nullptr);
     }
     tc::fence_smem_to_async();

@@ -276,8 +276,8 @@ __global__ void __launch_bounds__(512, 1)
   float mS = raw_load(SH ? sm + O_RAWS : nullptr, D64, sr), unused = 0.0f;
   tc::block_max3(mS, mK, unused, m->red);  // (its barrier: every staged copy has been read)
   const float pS = tc::pow2_ceil(mS), pK = tc::pow2_ceil(mK);  // (the scales are 1 / p)
-  raw_store(sr, 1.0f / pS, Shi, Slo, D64);
-  raw_store(kr, 1.0f / pK, Khi, Klo, T64);
+  raw_store(sr, tc::rcp_pow2_ceil(mS), Shi, Slo, D64);
+  raw_store(kr, tc::rcp_pow2_ceil(mK), Khi, Klo, T64);
   if (z_upper) {
 #pragma unroll
     for (int g = 0; g < KW / 8; g++) {
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(512, 1)
     float mV = raw_load(sm + O_RAW, Tv, vr), unused2 = 0.0f;
     tc::block_max3(mG, mV, unused2, m->red);
     const float pG = tc::pow2_ceil(mG), pV = tc::pow2_ceil(mV);
-    raw_store(gr, 1.0f / pG, Shi, Slo, D64);
+    raw_store(gr, tc::rcp_pow2_ceil(mG), Shi, Slo, D64);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(512, 1)
     // X K^T is complete once every warp has passed this barrier, so V may replace K
     failed = !sync_Z(okW);
     if (!failed) {
-      raw_store(vr, 1.0f / pV, Khi, Klo, T64);
+      raw_store(vr, tc::rcp_pow2_ceil(mV), Khi, Klo, T64);
       tc::fence_smem_to_async();
       tc::fence_before_sync();
       __syncthreads();

@@ -46,6 +46,7 @@ struct StateMisc {
   uint64_t mbar_ld;     // bulk copies of a chunk's raw key and value rows
   uint32_t tmem_base;
 };
+
 }  // namespace
 
 // PRE: k holds raw inputs of the query/key preprocessing, applied to each chunk's key rows
@@ -229,8 +230,7 @@ __global__ void __launch_bounds__(512, 1)
     float mk = tc::rows_absmax(kr, nullptr), mak = tc::rows_absmax(kr, m->w),
           mav = tc::rows_absmax(vr, m->w);
     tc::block_max3(mk, mak, mav, m->red);
-    const float sK = 1.0f / tc::pow2_ceil(mk), sAH = 1.0f / tc::pow2_ceil(mak),
-                sAG = 1.0f / tc::pow2_ceil(mav);
+    const float sK = tc::rcp_pow2_ceil(mk), sAH = tc::rcp_pow2_ceil(mak), sAG = tc::rcp_pow2_ceil(mav);
     tc::store_rows(kr, nullptr, sK, Ks, nullptr);
     // the previous chunk's states have left their staging buffers (S^G: the A operand region,
     // about to take this chunk's weighted keys); waited for only here, so that the stores

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(256, 1)
     tc::block_max3(m0, m1, mb, m->red);  // (its barriers: every thread has read the raw tiles)
     pending = it + 1 < NC;
     if (tid == 0 && pending) fetch(c + stepc);
-    const float s0 = 1.0f / tc::pow2_ceil(m0), s1 = 1.0f / tc::pow2_ceil(m1), sb = 1.0f / tc::pow2_ceil(mb);
+    const float s0 = tc::rcp_pow2_ceil(m0), s1 = tc::rcp_pow2_ceil(m1), sb = tc::rcp_pow2_ceil(mb);
     const float nsig0 = s0 * sb, nsig1 = s1 * sb;
     const float ac = expf(lend);
     if constexpr (BWD) {  // dS^c goes out before chunk c adds to it

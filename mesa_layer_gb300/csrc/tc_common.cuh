@@ -302,11 +302,22 @@ __device__ __forceinline__ bool drain_mmas(uint32_t drain_bar, bool issuer, unsi
 
 // ---- fp16 splitting -------------------------------------------------------------------
 // Power-of-two scale 2^e with max_abs * 2^-e in (0.5, 1] (1 for max_abs == 0 or non-finite).
+// For a positive normal max_abs with biased exponent E this is 2^(E - 126), written from the
+// bits (E = 254 gives infinity, as ldexpf(1, 128) does); a subnormal takes frexpf / ldexpf.
 __device__ __forceinline__ float pow2_ceil(float max_abs) {
+  const uint32_t E = (__float_as_uint(max_abs) >> 23) & 0xffu;
+  if (max_abs > 0.0f && E >= 1u && E <= 254u) return __uint_as_float((E + 1u) << 23);
   if (!(max_abs > 0.0f) || !isfinite(max_abs)) return 1.0f;
   int e;
   frexpf(max_abs, &e);  // max_abs = m * 2^e, m in [0.5, 1)
   return ldexpf(1.0f, e);
+}
+// 1 / pow2_ceil(max_abs), bit for bit: 2^(126 - E), a normal number for 1 <= E <= 252; other
+// values divide.
+__device__ __forceinline__ float rcp_pow2_ceil(float max_abs) {
+  const uint32_t E = (__float_as_uint(max_abs) >> 23) & 0xffu;
+  if (max_abs > 0.0f && E >= 1u && E <= 252u) return __uint_as_float((253u - E) << 23);
+  return 1.0f / pow2_ceil(max_abs);
 }
 
 // A power of two 2^k with sqrt(x) < 2^k <= 2 sqrt(x), and its reciprocal, from the exponent

@@ -60,7 +60,7 @@ __device__ __forceinline__ float stage_state(const float *src, const float *add,
       mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
     }
   }
-  const float s = 1.0f / pow2_ceil(block_max(mx, red));
+  const float s = rcp_pow2_ceil(block_max(mx, red));
   for (int e = t * 4; e < TILE * DH; e += 4 * blockDim.x) {
     const float4 x = (src || add) ? value(e) : make_float4(0, 0, 0, 0);
     const int r = e / DH, c = e % DH;
@@ -87,7 +87,7 @@ __device__ __forceinline__ float stage_rows(const __nv_bfloat16 *src, int Tv, ui
 #pragma unroll
     for (int k = 0; k < 8; k++) mx = fmaxf(mx, fabsf(__bfloat162float(b[k])));
   }
-  const float s = 1.0f / pow2_ceil(block_max(mx, red));
+  const float s = rcp_pow2_ceil(block_max(mx, red));
   for (int e = t * 8; e < TILE * DH; e += 8 * blockDim.x) {
     const int r = e / DH, c = e % DH;
     uint4 raw = make_uint4(0, 0, 0, 0);
@@ -137,7 +137,7 @@ __device__ __forceinline__ float stage_weighted_rows(const __nv_bfloat16 *src, c
 #pragma unroll
     for (int k = 0; k < 8; k++) mx = fmaxf(mx, fabsf(wj * __bfloat162float(b[k])));
   }
-  const float s = 1.0f / pow2_ceil(block_max(mx, red));
+  const float s = rcp_pow2_ceil(block_max(mx, red));
   for (int e = t * 8; e < TILE * DH; e += 8 * blockDim.x) {
     const int r = e / DH, c = e % DH;
     uint4 raw = make_uint4(0, 0, 0, 0);
