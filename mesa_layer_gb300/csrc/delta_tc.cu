@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(512, 1)
   uint8_t *Out = sm + DT_OUT;
   auto out_buf = [&](int half) { return (PRE || half) ? Ahi : Out; };
   auto stage_state = [&](int half, float sig) {
-    const float f = 1.0f / sig;
+    const float f = tc::div_pow2(1.0f, sig);
     float x[32];
     tc::tmem_ld32(tl + half * 128, x);
     tc::tmem_ld_wait();
@@ -239,14 +239,14 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc::store_rows(kr, m->w, sAH, Ahi, Alo);
     const float nsigH = sAH * sK, nsigG = sAG * sK;
-    rescale(0, first ? ac * nsigH : ac * nsigH / sigH, first, H0);
+    rescale(0, first ? ac * nsigH : tc::div_pow2(ac * nsigH, sigH), first, H0);
     tc::fence_smem_to_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     if (tid == 0) issue(0, !first || H0 != nullptr);
     // S^G's accumulator (columns the key sums do not touch) is rescaled while they run
-    rescale(128, first ? ac * nsigG : ac * nsigG / sigG, first, G0);
+    rescale(128, first ? ac * nsigG : tc::div_pow2(ac * nsigG, sigG), first, G0);
     ok = wait();
     if (!ok) break;
     tc::store_rows(vr, m->w, sAG, Ahi, Alo);

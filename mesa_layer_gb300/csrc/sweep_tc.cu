@@ -240,12 +240,12 @@ __global__ void __launch_bounds__(256, 1)
     const float nsig0 = s0 * sb, nsig1 = s1 * sb;
     const float ac = expf(lend);
     if constexpr (BWD) {  // dS^c goes out before chunk c adds to it
-      write_state(0, 1.0f / sig0, !have, c);
-      write_state(1, 1.0f / sig1, !have, c);
+      write_state(0, tc::div_pow2(1.0f, sig0), !have, c);
+      write_state(1, tc::div_pow2(1.0f, sig1), !have, c);
     }
     if (have) {
-      rescale(0, ac * nsig0 / sig0);
-      rescale(1, ac * nsig1 / sig1);
+      rescale(0, tc::div_pow2(ac * nsig0, sig0));
+      rescale(1, tc::div_pow2(ac * nsig1, sig1));
     }
     store16(A0hi, A0lo, r, c0, x0, s0);
     store16(A1hi, A1lo, r, c0, x1, s1);
@@ -282,8 +282,8 @@ __global__ void __launch_bounds__(256, 1)
     sig1 = nsig1;
     have = true;
     if constexpr (!BWD) {  // S_c goes out after chunk c added to it
-      write_state(0, 1.0f / sig0, false, c);
-      write_state(1, 1.0f / sig1, false, c);
+      write_state(0, tc::div_pow2(1.0f, sig0), false, c);
+      write_state(1, tc::div_pow2(1.0f, sig1), false, c);
     }
   }
   // a wait gave up (the same outcome in every thread): let the products and the copy still

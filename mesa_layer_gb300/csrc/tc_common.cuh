@@ -312,6 +312,14 @@ __device__ __forceinline__ float pow2_ceil(float max_abs) {
   frexpf(max_abs, &e);  // max_abs = m * 2^e, m in [0.5, 1)
   return ldexpf(1.0f, e);
 }
+// x / s, bit for bit, without a division where s is a power of two 2^k whose reciprocal is a
+// normal number (biased exponent of s in 1..253, mantissa bits zero): x * 2^-k is the same
+// exact value, rounded once.  Any other s divides.
+__device__ __forceinline__ float div_pow2(float x, float s) {
+  const uint32_t b = __float_as_uint(s), E = (b >> 23) & 0xffu;
+  if ((b & 0x807fffffu) == 0u && E >= 1u && E <= 253u) return x * __uint_as_float((254u - E) << 23);
+  return x / s;
+}
 // 1 / pow2_ceil(max_abs), bit for bit: 2^(126 - E), a normal number for 1 <= E <= 252; other
 // values divide.
 __device__ __forceinline__ float rcp_pow2_ceil(float max_abs) {
