@@ -198,10 +198,19 @@ __global__ void __launch_bounds__(256, 1)
   bool ok = true, pending = true;
   uint32_t phLd = 0, phMma = 0;
   const int r = tid >> 3, c0 = 16 * (tid & 7);  // this thread's share of a chunk's tiles
+  // the log-decays a chunk needs (its last one; thread tid < SW_C: token tid's), loaded one
+  // chunk ahead
+  float ell_end, ell_tid;
+  auto load_ell = [&](int c) {
+    const size_t tb = (size_t)u * T + (size_t)c * SW_C;
+    const int cv = min(SW_C, T - c * SW_C);
+    ell_end = ws.ell[tb + cv - 1];
+    ell_tid = tid < cv ? ws.ell[tb + tid] : 0.0f;
+  };
+  load_ell(first);
   for (int it = 0; it < NC && ok; it++) {
     const int c = first + stepc * it;
     const int t0 = c * SW_C, Cv = min(SW_C, T - t0);
-    const size_t tokbase = (size_t)u * T + t0;
     const bool got = tc::mbar_wait(aLd, phLd, a.wait_limit);
     if (__syncthreads_or(!got)) {
       if (tid == 0) atomicOr(status, tc::kErrMmaTimeout);
@@ -213,8 +222,9 @@ __global__ void __launch_bounds__(256, 1)
     }
     phLd ^= 1;
     pending = false;
-    const float lend = ws.ell[tokbase + Cv - 1];
-    if (tid < SW_C) m->w[tid] = tid < Cv ? expf(BWD ? ws.ell[tokbase + tid] : lend - ws.ell[tokbase + tid]) : 0.0f;
+    const float lend = ell_end;
+    if (tid < SW_C) m->w[tid] = tid < Cv ? expf(BWD ? ell_tid : lend - ell_tid) : 0.0f;
+    if (it + 1 < NC) load_ell(c + stepc);
     __syncthreads();
     float x0[16], x1[16], xr[16];
     const bool in = r < Cv;
