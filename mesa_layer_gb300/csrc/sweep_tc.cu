@@ -15,9 +15,9 @@
 // hi + lo with a power-of-two scale per matrix, three products hi*hi + hi*lo + lo*hi per
 // k-step of 16 tokens, fp32 accumulation.  The accumulators carry the operand scale of the
 // last update and are rescaled (a_c and the change of scale) before each one.  The next
-// chunk's raw rows arrive by bulk copies while a chunk is worked on; each state leaves through
-// a 128-byte-swizzled staging buffer of its own (so that its stores of one chunk overlap the
-// next) and four tiled tensor stores.
+// chunk's raw rows arrive by bulk copies while a chunk is worked on; both states of a chunk
+// are staged in one pass, each in a 128-byte-swizzled buffer of its own, and leave by four
+// tiled tensor stores each, which drain while the next chunk is worked on.
 #include <type_traits>
 
 #include "common.cuh"
@@ -151,34 +151,42 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tl = tbase + ((uint32_t)(32 * q) << 16) + 64 * h;
   const uint32_t id = tc::idesc_f16(128, D, true, true);
 
-  // state z (0 or 1) times f (zero: zeros) into the staging buffer, then out by tensor stores
-  // to chunk c's slot (block-wide)
-  auto write_state = [&](int z, float f, bool zero, int c) {
-    // state z's previous stores (two bulk groups ago) have read its staging buffer
-    if (tid == 0) tc::bulk_wait_read_but_one();
+  // both states, state z times f_z (zero: zeros), into their staging buffers, then out by
+  // tensor stores to chunk c's slots (block-wide, one bulk group per state)
+  auto write_states = [&](float f0, float f1, bool zero, int c) {
+    // the previous chunk's stores of both states have read their staging buffers
+    if (tid == 0) tc::bulk_wait_read();
     __syncthreads();
-    uint8_t *Oz = Out + z * 4 * SW_SLAB;
 #pragma unroll
-    for (int k = 0; k < 2; k++) {
-      float v[32];
-      if (!zero) {
-        tc::tmem_ld32(tl + 128 * z + 32 * k, v);
-        tc::tmem_ld_wait();
+    for (int z = 0; z < 2; z++) {
+      const float f = z ? f1 : f0;
+      uint8_t *Oz = Out + z * 4 * SW_SLAB;
+#pragma unroll
+      for (int k = 0; k < 2; k++) {
+        float v[32];
+        if (!zero) {
+          tc::tmem_ld32(tl + 128 * z + 32 * k, v);
+          tc::tmem_ld_wait();
+        }
+        uint8_t *dst = Oz + (2 * h + k) * SW_SLAB + row * 128;
+#pragma unroll
+        for (int g = 0; g < 8; g++)
+          *reinterpret_cast<float4 *>(dst + ((g ^ (row & 7)) << 4)) =
+              zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+                   : make_float4(v[4 * g] * f, v[4 * g + 1] * f, v[4 * g + 2] * f, v[4 * g + 3] * f);
       }
-      uint8_t *dst = Oz + (2 * h + k) * SW_SLAB + row * 128;
-#pragma unroll
-      for (int g = 0; g < 8; g++)
-        *reinterpret_cast<float4 *>(dst + ((g ^ (row & 7)) << 4)) =
-            zero ? make_float4(0.f, 0.f, 0.f, 0.f)
-                 : make_float4(v[4 * g] * f, v[4 * g + 1] * f, v[4 * g + 2] * f, v[4 * g + 3] * f);
     }
     tc::fence_smem_to_async();
     __syncthreads();
     if (tid == 0) {
-      const void *map = z ? (const void *)&map1 : (const void *)&map0;
 #pragma unroll
-      for (int s = 0; s < 4; s++) tc::tensor_s2g_2d(map, tc::smem_u32(Oz + s * SW_SLAB), 32 * s, (u * NC + c) * 128);
-      tc::bulk_commit();
+      for (int z = 0; z < 2; z++) {
+        const void *map = z ? (const void *)&map1 : (const void *)&map0;
+        uint8_t *Oz = Out + z * 4 * SW_SLAB;
+#pragma unroll
+        for (int s = 0; s < 4; s++) tc::tensor_s2g_2d(map, tc::smem_u32(Oz + s * SW_SLAB), 32 * s, (u * NC + c) * 128);
+        tc::bulk_commit();
+      }
     }
   };
   auto rescale = [&](int z, float f) {
@@ -250,8 +258,7 @@ __global__ void __launch_bounds__(256, 1)
     const float nsig0 = s0 * sb, nsig1 = s1 * sb;
     const float ac = expf(lend);
     if constexpr (BWD) {  // dS^c goes out before chunk c adds to it
-      write_state(0, tc::div_pow2(1.0f, sig0), !have, c);
-      write_state(1, tc::div_pow2(1.0f, sig1), !have, c);
+      write_states(tc::div_pow2(1.0f, sig0), tc::div_pow2(1.0f, sig1), !have, c);
     }
     if (have) {
       rescale(0, tc::div_pow2(ac * nsig0, sig0));
@@ -292,8 +299,7 @@ __global__ void __launch_bounds__(256, 1)
     sig1 = nsig1;
     have = true;
     if constexpr (!BWD) {  // S_c goes out after chunk c added to it
-      write_state(0, tc::div_pow2(1.0f, sig0), false, c);
-      write_state(1, tc::div_pow2(1.0f, sig1), false, c);
+      write_states(tc::div_pow2(1.0f, sig0), tc::div_pow2(1.0f, sig1), false, c);
     }
   }
   // a wait gave up (the same outcome in every thread): let the products and the copy still
