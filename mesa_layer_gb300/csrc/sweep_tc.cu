@@ -152,14 +152,16 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t id = tc::idesc_f16(128, D, true, true);
 
   // both states, state z times f_z (zero: zeros), into their staging buffers, then out by
-  // tensor stores to chunk c's slots (block-wide, one bulk group per state)
-  auto write_states = [&](float f0, float f1, bool zero, int c) {
+  // tensor stores to chunk c's slots (block-wide, one bulk group per state); with `resc`, the
+  // accumulators are multiplied by r_z in the same pass (the rescale before the next update)
+  auto write_states = [&](float f0, float f1, bool zero, int c, bool resc = false, float r0 = 1.0f,
+                          float r1 = 1.0f) {
     // the previous chunk's stores of both states have read their staging buffers
     if (tid == 0) tc::bulk_wait_read();
     __syncthreads();
 #pragma unroll
     for (int z = 0; z < 2; z++) {
-      const float f = z ? f1 : f0;
+      const float f = z ? f1 : f0, rz = z ? r1 : r0;
       uint8_t *Oz = Out + z * 4 * SW_SLAB;
 #pragma unroll
       for (int k = 0; k < 2; k++) {
@@ -174,6 +176,11 @@ __global__ void __launch_bounds__(256, 1)
           *reinterpret_cast<float4 *>(dst + ((g ^ (row & 7)) << 4)) =
               zero ? make_float4(0.f, 0.f, 0.f, 0.f)
                    : make_float4(v[4 * g] * f, v[4 * g + 1] * f, v[4 * g + 2] * f, v[4 * g + 3] * f);
+        if (resc && !zero) {
+#pragma unroll
+          for (int e = 0; e < 32; e++) v[e] *= rz;
+          tc::tmem_st32(tl + 128 * z + 32 * k, v);
+        }
       }
     }
     tc::fence_smem_to_async();
@@ -257,10 +264,10 @@ __global__ void __launch_bounds__(256, 1)
     const float s0 = tc::rcp_pow2_ceil(m0), s1 = tc::rcp_pow2_ceil(m1), sb = tc::rcp_pow2_ceil(mb);
     const float nsig0 = s0 * sb, nsig1 = s1 * sb;
     const float ac = expf(lend);
-    if constexpr (BWD) {  // dS^c goes out before chunk c adds to it
-      write_states(tc::div_pow2(1.0f, sig0), tc::div_pow2(1.0f, sig1), !have, c);
-    }
-    if (have) {
+    if constexpr (BWD) {  // dS^c goes out before chunk c adds to it (and is rescaled on the way)
+      write_states(tc::div_pow2(1.0f, sig0), tc::div_pow2(1.0f, sig1), !have, c, have,
+                   tc::div_pow2(ac * nsig0, sig0), tc::div_pow2(ac * nsig1, sig1));
+    } else if (have) {
       rescale(0, tc::div_pow2(ac * nsig0, sig0));
       rescale(1, tc::div_pow2(ac * nsig1, sig1));
     }
