@@ -281,7 +281,9 @@ __global__ void __launch_bounds__(512, 1)
     SG = a.G0 + (size_t)u * DH * DH;
   }
   const float *SHu = RHS ? nullptr : SH, *CHu = RHS ? nullptr : CH;  // (RHS: no CG, no S^H)
-  const bool load_q = !(SOLVE && sv.rhs);
+  // (fp32 right-hand sides, or the right-hand-side mode, which reads its rows g_t at the
+  // readout: no staged query rows)
+  const bool load_q = !(SOLVE && sv.rhs) && !RHS;
   constexpr uint32_t MAT32 = sizeof(float) * DH * DH;  // one fp32 state (64 KB)
   const uint32_t rows_bytes = (uint32_t)Tv * DH * 2;     // Tv bf16 rows
   // PRE: q and k are raw inputs of the query/key preprocessing, fused here: the h rows before
