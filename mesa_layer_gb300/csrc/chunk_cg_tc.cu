@@ -330,9 +330,11 @@ __global__ void __launch_bounds__(512, 1)
     tc::pre_taps(a.pre_wk + hw, a.pre_W, reinterpret_cast<float *>(sm + OFF_K + PRE_KTAPS));
     tc::pre_taps(a.pre_wq + hw, a.pre_W, reinterpret_cast<float *>(sm + OFF_K + PRE_QTAPS));
   }
-  // the readout's state is only needed after the CG and is fetched into L2 meanwhile
+  // the readout's state is only needed after the CG and is fetched into L2 meanwhile; fp32
+  // right-hand sides are read only once the state is staged
   tc::prefetch_l2(SG, sizeof(float) * DH * DH);
   tc::prefetch_l2(CG, sizeof(float) * DH * DH);
+  if (SOLVE && sv.rhs) tc::prefetch_l2(sv.rhs + tokbase * DH, sizeof(float) * DH * Tv);
   __syncthreads();  // barrier initialisations (and the per-chunk constants) visible
   // Bounded waits for the copies; on a give-up the block waits (default limit) until they have
   // landed, so that nothing writes this CTA's shared memory after it ends, and skips the chunk.

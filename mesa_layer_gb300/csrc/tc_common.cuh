@@ -278,11 +278,6 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
-// Wait until at most one bulk group of this thread (the most recent) is still reading its
-// shared-memory source.
-__device__ __forceinline__ void bulk_wait_read_but_one() {
-  asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory");
-}
 // Wait until every bulk group of this thread has completed (its global writes performed).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 
