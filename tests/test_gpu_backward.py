@@ -149,6 +149,23 @@ def test_closed_gates_tensor_cores():
     assert np.all(g["dgamma"][~open_gate] == 0.0)
 
 
+def test_gradient_scale_is_exact():
+    """Every gradient is linear in dL/dout, and the tensor-core path (bf16, d = 128: the
+    solves, the state sweeps, the row x state products) takes its operand scales from
+    exponent bits: dout times 2^k (k = -30, 30) gives exactly 2^k times every gradient, bit
+    for bit, with the same counts."""
+    w = _wl("bf16", B=1, H=2, T=200, dk=128, dv=128)
+    inp = synth.backward_inputs(w, seed=6)
+    g = _gpu(inp, "bf16", 10, 0.0)
+    for k in (-30, 30):
+        sc = dict(inp)
+        sc["dout"] = (inp["dout"] * 2.0 ** k).astype(inp["dout"].dtype)
+        g2 = _gpu(sc, "bf16", 10, 0.0)
+        assert np.array_equal(g2["iters_bwd"], g["iters_bwd"]), k
+        for name in ("dq", "dk", "dv", "dgamma", "dlam"):
+            assert np.array_equal(g2[name], g[name] * 2.0 ** k), (k, name)
+
+
 def test_dynamic_mode():
     """Dynamic stopping (tol 1e-3, cap 30): counts may differ at the threshold; the units whose
     counts all agree must meet the tolerance, and at least 95 % of the counts agree."""

@@ -159,6 +159,25 @@ def test_tc_dynamic_initial_state():
 
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
 @pytest.mark.parametrize("tol", [0.0, 1e-3], ids=["fixed", "dynamic"])
+def test_tc_value_scale_is_exact(dtype, d, tol):
+    """The readout is linear in v and the CG does not see v: v times 2^k (k = -40, 40) gives
+    exactly 2^k times the outputs with the same counts.  The value operands' scales come from
+    exponent bits, so the products see the same fp16 operands at every k: a check of those
+    scale paths over a wide range of exponents (the state build's and the readout's)."""
+    w = synth.workload("fwd_bf16_d128" if dtype == "bf16" else "fwd_fp32_d64", dtype=dtype, dk=d, dv=d, B=1, H=2,
+                       T=300, cg_iters=12 if tol == 0.0 else 30, cg_tol=tol)
+    inp = synth.forward_inputs(w, seed=19)
+    o, it = gpu_forward(inp, dtype, w.cg_iters, tol, 64)
+    for k in (-40, 40):
+        sc = dict(inp)
+        sc["v"] = (inp["v"] * np.float32(2.0 ** k)).astype(np.float32)
+        o2, it2 = gpu_forward(sc, dtype, w.cg_iters, tol, 64)
+        assert np.array_equal(it2, it), k
+        assert np.array_equal(o2, (o * np.float32(2.0 ** k)).astype(np.float32)), k
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+@pytest.mark.parametrize("tol", [0.0, 1e-3], ids=["fixed", "dynamic"])
 def test_tc_query_scale_is_exact(dtype, d, tol):
     """The CG iterate is homogeneous in q, and the tensor-core kernels take every operand scale
     from exponent bits: q times 2^k (k = -40, 40) gives exactly 2^k times the outputs, bit for
