@@ -78,6 +78,42 @@ def test_decode_small(d, dtype):
     print(f"decode d={d} {dtype}: {r}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_scale_is_exact(d):
+    """The step is homogeneous: q times 2^k scales x and o; v and G_state times 2^k scale o and
+    the new G_state; H_state is untouched by either.  In fp32 arithmetic with power-of-two
+    factors every result is exactly 2^k times the unscaled one (k = -40, 40), with the same
+    counts, in fixed and dynamic mode (the stopping rule compares norms that scale alike)."""
+    import torch
+
+    from mesa_layer_gb300 import binding
+    w = synth.workload("decode_bf16_d128", B=3, H=2, dk=d, dv=d, prefix=0)
+    N, H = w.B, w.H
+    lam_t = torch.from_numpy(synth.lambdas(w)).cuda()
+    rng = np.random.default_rng(21)
+    M = rng.standard_normal((N, H, d, d)).astype(np.float32) * 0.1
+    H0 = torch.from_numpy((M @ np.swapaxes(M, -1, -2)).astype(np.float32)).cuda()
+    G0 = torch.from_numpy((rng.standard_normal((N, H, d, d)) * 0.1).astype(np.float32)).cuda()
+    inp = synth.decode_inputs(w, 0)
+    dev = {k: torch.from_numpy(inp[k]).cuda().to(torch.bfloat16 if k != "gamma" else torch.float32)
+           for k in ("q", "k", "v", "gamma")}
+    for iters, tol in ((d // 2, 0.0), (30, 1e-3)):
+        Hb, Gb = H0.clone(), G0.clone()
+        o, it = binding.mesa_decode_step(Hb, Gb, dev["q"], dev["k"], dev["v"], dev["gamma"], lam_t, iters, tol)
+        for k in (-40, 40):
+            f = 2.0 ** k
+            Hq, Gq = H0.clone(), G0.clone()
+            oq, itq = binding.mesa_decode_step(Hq, Gq, dev["q"] * f, dev["k"], dev["v"], dev["gamma"], lam_t, iters, tol)
+            Hv, Gv = H0.clone(), (G0 * f).contiguous()
+            ov, itv = binding.mesa_decode_step(Hv, Gv, dev["q"], dev["k"], dev["v"] * f, dev["gamma"], lam_t, iters, tol)
+            torch.cuda.synchronize()
+            for o2, it2 in ((oq, itq), (ov, itv)):
+                assert torch.equal(it2, it), (iters, k)
+                assert torch.equal(o2.float(), o.float() * f), (iters, k)
+            assert torch.equal(Hq, Hb) and torch.equal(Gq, Gb) and torch.equal(Hv, Hb), (iters, k)
+            assert torch.equal(Gv, Gb * f), (iters, k)
+
+
 def test_decode_dynamic_with_prefix():
     # fp32 inputs and the 1e-4 tolerance of fp32 workloads: Lambda >= 0.5 keeps the systems
     # well enough conditioned for fp32 CG to track the fp64 iterates at that level
