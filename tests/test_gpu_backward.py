@@ -149,6 +149,23 @@ def test_closed_gates_tensor_cores():
     assert np.all(g["dgamma"][~open_gate] == 0.0)
 
 
+def test_units_are_independent_tensor_cores():
+    """New inputs for batch row 1 leave every gradient of batch row 0 unchanged, bit for bit
+    (bf16, d = 128: the tensor-core solves with segment carries, the sweeps, the products)."""
+    w = _wl("bf16", B=2, H=2, T=300, dk=128, dv=128)
+    a = synth.backward_inputs(w, seed=8)
+    b = synth.backward_inputs(w, seed=9)
+    g = _gpu(a, "bf16", 10, 0.0)
+    mixed = dict(a)
+    for key in ("q", "k", "v", "gamma", "dout"):
+        mixed[key] = a[key].copy()
+        mixed[key][1] = b[key][1]
+    g2 = _gpu(mixed, "bf16", 10, 0.0)
+    for name in ("dq", "dk", "dv", "dgamma"):
+        assert np.array_equal(g2[name][0], g[name][0]), name
+        assert not np.array_equal(g2[name][1], g[name][1]), name
+
+
 def test_gradient_scale_is_exact():
     """Every gradient is linear in dL/dout, and the tensor-core path (bf16, d = 128: the
     solves, the state sweeps, the row x state products) takes its operand scales from

@@ -158,6 +158,26 @@ def test_tc_dynamic_initial_state():
 
 
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_tc_units_are_independent(dtype, d):
+    """A unit's outputs do not depend on any other unit's inputs: with B*H = 4 units of eight
+    128-token chunks the state build runs one segment per chunk and the CG kernel adds the
+    segment carries, so a wrong unit, chunk or segment index anywhere would mix units.  New
+    inputs for batch row 1 leave batch row 0's outputs and counts unchanged, bit for bit."""
+    w = synth.workload("fwd_bf16_d128" if dtype == "bf16" else "fwd_fp32_d64", dtype=dtype, dk=d, dv=d, B=2, H=2,
+                       T=1000, cg_iters=30, cg_tol=1e-3)
+    a = synth.forward_inputs(w, seed=23)
+    b = synth.forward_inputs(w, seed=24)
+    o, it = gpu_forward(a, dtype, w.cg_iters, w.cg_tol, 64)
+    mixed = dict(a)
+    for key in ("q", "k", "v", "gamma"):
+        mixed[key] = a[key].copy()
+        mixed[key][1] = b[key][1]
+    o2, it2 = gpu_forward(mixed, dtype, w.cg_iters, w.cg_tol, 64)
+    assert np.array_equal(o2[0], o[0]) and np.array_equal(it2[0], it[0])
+    assert not np.array_equal(o2[1], o[1])
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
 @pytest.mark.parametrize("tol", [0.0, 1e-3], ids=["fixed", "dynamic"])
 def test_tc_value_scale_is_exact(dtype, d, tol):
     """The readout is linear in v and the CG does not see v: v times 2^k (k = -40, 40) gives
